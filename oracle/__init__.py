@@ -1,0 +1,165 @@
+"""ctypes loader for the CPU oracle (``oracle/oracle.cpp``).
+
+Test infrastructure only: the test suite, ``__graft_entry__.smoke()`` and the
+bench's CPU-baseline / reference leg use it. The CUDA library and its Python
+binding never import this package.
+
+All wrappers take CPU torch tensors (any strides whose innermost stride is 1)
+and work on their bytes, so the oracle sees exactly the bytes the GPU sees.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.cpp")
+_LIB = os.path.join(_HERE, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+F32, F16, BF16 = 0, 1, 2
+_FMT = {torch.float32: F32, torch.float16: F16, torch.bfloat16: BF16}
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.cpp into liboracle.so with g++ (plain C++17, -O2)."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        cmd = ["g++", "-std=c++17", "-O2", "-fno-fast-math", "-ffp-contract=off",
+               "-shared", "-fPIC", "-o", tmp, _SRC]
+        subprocess.run(cmd, check=True)
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded oracle library.
+
+    ``ORACLE_LIB_OVERRIDE`` (test-only) points at another build of oracle.cpp;
+    the mutation tests use it to load copies with planted mistakes.
+    """
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = os.environ.get("ORACLE_LIB_OVERRIDE")
+            if not path:
+                path = build()
+            L = ctypes.CDLL(path)
+            i64, i32, vp, dbl = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_double
+            L.orc_encode.argtypes = [dbl, i32]
+            L.orc_encode.restype = ctypes.c_uint32
+            L.orc_decode.argtypes = [ctypes.c_uint32, i32]
+            L.orc_decode.restype = dbl
+            L.orc_rmsnorm.argtypes = [vp, vp, vp, i64, i64, i64, i64, dbl, i32]
+            L.orc_rmsnorm.restype = i32
+            L.orc_add_rmsnorm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, dbl, i32]
+            L.orc_add_rmsnorm.restype = i32
+            L.orc_rope_kv_store.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32,
+                                            i64, i64, i64, i64, i64, i32, i32]
+            L.orc_rope_kv_store.restype = i64
+            L.orc_glu.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32]
+            L.orc_glu.restype = i32
+            _lib = L
+    return _lib
+
+
+def _cpu(t: torch.Tensor, name: str) -> torch.Tensor:
+    if t.device.type != "cpu":
+        raise ValueError(f"oracle: {name} must be a CPU tensor")
+    return t
+
+
+def _row_stride(t: torch.Tensor) -> int:
+    if t.dim() == 1:
+        return t.shape[0]
+    if t.stride(-1) != 1:
+        raise ValueError("oracle: innermost stride must be 1")
+    return t.stride(-2)
+
+
+def encode(v: float, fmt: int) -> int:
+    return int(lib().orc_encode(float(v), fmt))
+
+
+def decode(bits: int, fmt: int) -> float:
+    return float(lib().orc_decode(int(bits) & 0xFFFFFFFF, fmt))
+
+
+def rmsnorm(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor, eps: float) -> None:
+    """out <- rmsnorm(x) * w, all of one dtype; x and out are [rows, D] views."""
+    _cpu(x, "x"), _cpu(w, "w"), _cpu(out, "out")
+    rows, D = x.shape
+    rc = lib().orc_rmsnorm(x.data_ptr(), w.data_ptr(), out.data_ptr(), rows, D,
+                           _row_stride(x), _row_stride(out), float(eps), _FMT[x.dtype])
+    if rc != 0:
+        raise ValueError("oracle: bad rmsnorm arguments")
+
+
+def add_rmsnorm(x: torch.Tensor, res: torch.Tensor, w: torch.Tensor, out: torch.Tensor,
+                eps: float) -> None:
+    """x <- round(x + res) in place; out <- rmsnorm(x) * w."""
+    for t, n in ((x, "x"), (res, "res"), (w, "w"), (out, "out")):
+        _cpu(t, n)
+    rows, D = x.shape
+    rc = lib().orc_add_rmsnorm(x.data_ptr(), res.data_ptr(), w.data_ptr(), out.data_ptr(), rows, D,
+                               _row_stride(x), _row_stride(res), _row_stride(out), float(eps),
+                               _FMT[x.dtype])
+    if rc != 0:
+        raise ValueError("oracle: bad add_rmsnorm arguments")
+
+
+def _tok_stride(t: torch.Tensor) -> int:
+    # [T, H, D] with the head stride equal to D and unit innermost stride.
+    if t.stride(-1) != 1 or t.stride(-2) != t.shape[-1]:
+        raise ValueError("oracle: q/k/v must have contiguous heads within a token")
+    return t.stride(0)
+
+
+def rope_kv_store(q, k, v, cos, sin, pos, slot_mapping, kv_cache, max_pos: int | None = None) -> int:
+    """Rotate q in place, write rotated k and v into kv_cache through slot_mapping.
+
+    Returns the error count (bad positions plus out-of-range slots).
+    """
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (cos, "cos"), (sin, "sin"), (pos, "pos"),
+                 (slot_mapping, "slot_mapping"), (kv_cache, "kv_cache")):
+        _cpu(t, n)
+    assert cos.dtype == torch.float32 and sin.dtype == torch.float32
+    assert cos.is_contiguous() and sin.is_contiguous()
+    assert pos.dtype == torch.int64 and slot_mapping.dtype == torch.int64
+    assert kv_cache.is_contiguous()
+    T, n_head, hd = q.shape
+    n_kv = k.shape[1]
+    _, num_blocks, block_size, _, _ = kv_cache.shape
+    if max_pos is None:
+        max_pos = cos.shape[0]
+    n = lib().orc_rope_kv_store(q.data_ptr(), k.data_ptr(), v.data_ptr(), cos.data_ptr(),
+                                sin.data_ptr(), pos.data_ptr(), slot_mapping.data_ptr(),
+                                kv_cache.data_ptr(), T, n_head, n_kv, hd, _tok_stride(q),
+                                _tok_stride(k), _tok_stride(v), int(max_pos), num_blocks,
+                                block_size, _FMT[q.dtype])
+    if n < 0:
+        raise ValueError("oracle: bad rope_kv_store arguments or duplicate slots")
+    return int(n)
+
+
+def glu(gate_up: torch.Tensor, out: torch.Tensor, act: str = "silu") -> None:
+    """out[t, j] = act(gate_up[t, j]) * gate_up[t, I + j]; act in {'silu', 'relu'}."""
+    _cpu(gate_up, "gate_up"), _cpu(out, "out")
+    T, I = out.shape
+    rc = lib().orc_glu(gate_up.data_ptr(), out.data_ptr(), T, I, _row_stride(gate_up),
+                       _row_stride(out), {"silu": 0, "relu": 1}[act], _FMT[out.dtype])
+    if rc != 0:
+        raise ValueError("oracle: bad glu arguments")
+
+
+def swiglu(gate_up, out):
+    glu(gate_up, out, "silu")
+
+
+def reglu(gate_up, out):
+    glu(gate_up, out, "relu")

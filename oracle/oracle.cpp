@@ -1,0 +1,308 @@
+// Plain CPU oracle for the fused per-token decoder path (RMSNorm, residual-add +
+// RMSNorm, neox RoPE with paged KV-cache store, SwiGLU/ReGLU).
+//
+// TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check and the bench's
+// CPU-baseline leg load this file's library. The CUDA library never links,
+// includes or calls it, and it shares no source with the CUDA path.
+//
+// Every value is decoded to double, the operator's formula is applied in double
+// in the order the pages state it, and the result is rounded once to the
+// output format with round-to-nearest, ties-to-even. No blocking, no fusion,
+// no reordering beyond what the formula says.
+//
+// Sources ("pages"):
+//   [koas]  koas-w.github.io, "preformanceimprovement" (Qwen2.5-1.5B engine):
+//           section 1 (fused RoPE + paged KV store), section 2 (fused SwiGLU),
+//           section 3 (RMSNorm chain x.pow(2).mean(-1).add(eps).rsqrt().mul(x).mul(weight),
+//           fp32 compute, cast back on write), section 4 (fused add + norm, x updated
+//           in place, normed result returned).
+//   [lsln]  m.lsln.cn/news/61269, section 2.3 (RMSNorm in fp32, y.to(dtype) once;
+//           precomputed cos/sin caches).
+//   [mer]   mer.dev "AsyncT vllm ..." section 1.1 (KV cache layout
+//           [2, num_blocks, block_size, num_kv_heads, head_size]) and section 3.3
+//           (relu_and_mul for ReGLU).
+//   [csdn]  agent.csdn.net "使用Triton实现RMSNorm算子" (rsqrt(sum/D + eps) per row).
+//
+// Parity pins: every function here is pinned by the CPU tests (closed forms,
+// exhaustive format round trips, exact-rational brute force); none is "parity
+// unpinned". The one unpinned quantity is the drift accumulated over a
+// 28-layer chain, which the chain test reports rather than bounds.
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <set>
+
+namespace {
+
+// Element formats. The numbering mirrors the public enum by value only; the
+// two are declared separately on purpose.
+enum Fmt { F32 = 0, F16 = 1, BF16 = 2 };
+
+struct FormatSpec {
+    int p;     // significand bits, hidden bit included
+    int emin;  // exponent of the smallest normal
+    int emax;  // exponent of the largest finite
+};
+
+bool format_spec(int fmt, FormatSpec* s) {
+    switch (fmt) {
+        case F32:  *s = {24, -126, 127}; return true;
+        case F16:  *s = {11, -14, 15};   return true;
+        case BF16: *s = {8, -126, 127};  return true;
+        default:   return false;
+    }
+}
+
+// Round a double to the nearest value of a binary format with spec `s`,
+// ties to even, overflow to infinity (IEEE 754 roundTiesToEven).
+double round_to_format(double v, const FormatSpec& s) {
+    if (std::isnan(v) || std::isinf(v) || v == 0.0) return v;
+    double a = std::fabs(v);
+    int e2;
+    std::frexp(a, &e2);               // a = m * 2^e2 with m in [0.5, 1)
+    int lead = e2 - 1;                // exponent of a's leading bit
+    int q = (lead > s.emin ? lead : s.emin) - (s.p - 1);  // exponent of one ulp
+    double scaled = std::ldexp(a, -q);   // exact: a power-of-two rescale
+    double fl = std::floor(scaled);
+    double frac = scaled - fl;           // exact
+    if (frac > 0.5 || (frac == 0.5 && std::fmod(fl, 2.0) != 0.0)) fl += 1.0;
+    double r = std::ldexp(fl, q);
+    double maxfin = std::ldexp(std::ldexp(1.0, s.p) - 1.0, s.emax - (s.p - 1));
+    if (r > maxfin) r = INFINITY;
+    return std::copysign(r, v);
+}
+
+uint32_t encode_f16(double r) {
+    // r is already a representable half value (or inf / nan / zero).
+    uint32_t sign = std::signbit(r) ? 0x8000u : 0u;
+    if (std::isnan(r)) return 0x7E00u;
+    double a = std::fabs(r);
+    if (std::isinf(a)) return sign | 0x7C00u;
+    if (a == 0.0) return sign;
+    int e2;
+    std::frexp(a, &e2);
+    int lead = e2 - 1;
+    if (lead < -14) {  // subnormal: a = m * 2^-24 with integer m < 1024
+        uint32_t m = static_cast<uint32_t>(std::ldexp(a, 24));
+        return sign | m;
+    }
+    uint32_t exp_field = static_cast<uint32_t>(lead + 15);
+    uint32_t m = static_cast<uint32_t>(std::ldexp(a, 10 - lead)) - 1024u;
+    return sign | (exp_field << 10) | m;
+}
+
+double decode_f16(uint32_t b) {
+    double sign = (b & 0x8000u) ? -1.0 : 1.0;
+    uint32_t e = (b >> 10) & 0x1Fu;
+    uint32_t m = b & 0x3FFu;
+    if (e == 0x1Fu) return m ? NAN : sign * INFINITY;
+    if (e == 0) return sign * std::ldexp(static_cast<double>(m), -24);
+    return sign * std::ldexp(1024.0 + m, static_cast<int>(e) - 25);
+}
+
+uint32_t encode(double v, int fmt) {
+    FormatSpec s;
+    format_spec(fmt, &s);
+    if (std::isnan(v)) return fmt == F32 ? 0x7FC00000u : (fmt == BF16 ? 0x7FC0u : 0x7E00u);
+    double r = round_to_format(v, s);
+    if (fmt == F16) return encode_f16(r);
+    float f = static_cast<float>(r);  // exact: r is representable in binary32
+    uint32_t bits;
+    std::memcpy(&bits, &f, 4);
+    return fmt == F32 ? bits : (bits >> 16);
+}
+
+double decode(uint32_t bits, int fmt) {
+    if (fmt == F16) return decode_f16(bits & 0xFFFFu);
+    uint32_t b32 = fmt == F32 ? bits : ((bits & 0xFFFFu) << 16);
+    float f;
+    std::memcpy(&f, &b32, 4);
+    return static_cast<double>(f);
+}
+
+int elem_size(int fmt) { return fmt == F32 ? 4 : 2; }
+
+double load(const void* base, int64_t idx, int fmt) {
+    if (fmt == F32) {
+        uint32_t b;
+        std::memcpy(&b, static_cast<const char*>(base) + idx * 4, 4);
+        return decode(b, fmt);
+    }
+    uint16_t h;
+    std::memcpy(&h, static_cast<const char*>(base) + idx * 2, 2);
+    return decode(h, fmt);
+}
+
+void store(void* base, int64_t idx, double v, int fmt) {
+    uint32_t b = encode(v, fmt);
+    if (fmt == F32) {
+        std::memcpy(static_cast<char*>(base) + idx * 4, &b, 4);
+    } else {
+        uint16_t h = static_cast<uint16_t>(b);
+        std::memcpy(static_cast<char*>(base) + idx * 2, &h, 2);
+    }
+}
+
+// RMSNorm of one row already decoded to double ([koas] section 3; [lsln] 2.3;
+// [csdn]): mean of squares over D, eps inside the root, one rounding on write.
+void rmsnorm_row(const double* x, const void* w, void* out, int64_t out_off, int64_t D,
+                 double eps, int fmt) {
+    double sum_sq = 0.0;
+    for (int64_t j = 0; j < D; ++j) sum_sq += x[j] * x[j];
+    double mean_sq = sum_sq / static_cast<double>(D);
+    double inv_rms = 1.0 / std::sqrt(mean_sq + eps);
+    for (int64_t j = 0; j < D; ++j) {
+        double wj = load(w, j, fmt);
+        store(out, out_off + j, x[j] * inv_rms * wj, fmt);
+    }
+}
+
+}  // namespace
+
+extern "C" {
+
+int orc_version(void) { return 1; }
+
+// Round `v` to format `fmt` (0 = fp32, 1 = fp16, 2 = bf16), returning its bits.
+uint32_t orc_encode(double v, int fmt) { return encode(v, fmt); }
+
+// Value of the bit pattern `bits` in format `fmt`.
+double orc_decode(uint32_t bits, int fmt) { return decode(bits, fmt); }
+
+// out[r, :] = x[r, :] / sqrt(mean_j x[r, j]^2 + eps) * w[:]
+// x, out: rows x D, row strides in elements. Returns 0, or -1 on bad arguments.
+int orc_rmsnorm(const void* x, const void* w, void* out, int64_t rows, int64_t D,
+                int64_t x_row_stride, int64_t out_row_stride, double eps, int fmt) {
+    FormatSpec s;
+    if (!format_spec(fmt, &s) || rows < 0 || D <= 0) return -1;
+    double* row = new double[D];
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < D; ++j) row[j] = load(x, r * x_row_stride + j, fmt);
+        rmsnorm_row(row, w, out, r * out_row_stride, D, eps, fmt);
+    }
+    delete[] row;
+    return 0;
+}
+
+// Residual add then RMSNorm ([koas] section 4): x[r, :] <- round(x[r, :] + res[r, :])
+// in place; out[r, :] = rmsnorm(the rounded, stored x[r, :]).
+int orc_add_rmsnorm(void* x, const void* res, const void* w, void* out, int64_t rows,
+                    int64_t D, int64_t x_row_stride, int64_t res_row_stride,
+                    int64_t out_row_stride, double eps, int fmt) {
+    FormatSpec s;
+    if (!format_spec(fmt, &s) || rows < 0 || D <= 0) return -1;
+    double* row = new double[D];
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t j = 0; j < D; ++j) {
+            double sum = load(x, r * x_row_stride + j, fmt) + load(res, r * res_row_stride + j, fmt);
+            store(x, r * x_row_stride + j, sum, fmt);
+            row[j] = load(x, r * x_row_stride + j, fmt);  // the rounded value
+        }
+        rmsnorm_row(row, w, out, r * out_row_stride, D, eps, fmt);
+    }
+    delete[] row;
+    return 0;
+}
+
+// Neox half-rotation of every Q and K head at position pos[t], Q rotated in place,
+// K_rot and V written through slot_mapping into a paged cache ([koas] section 1;
+// cache layout [2, num_blocks, block_size, n_kv_head, head_dim] from [mer] 1.1).
+// With h = head_dim / 2, c = cos[p, i], s = sin[p, i] (tables [max_pos, h], fp32):
+//   y[i]     = x[i] * c - x[i + h] * s
+//   y[i + h] = x[i + h] * c + x[i] * s
+// Token t: a position outside [0, max_pos) counts one error and leaves q[t] and the
+// cache untouched; slot < 0 is a padding token (no cache write, no error); a slot
+// >= num_blocks * block_size counts one error and skips the cache write.
+// Returns the error count, or -1 on bad arguments or duplicate valid slots.
+int64_t orc_rope_kv_store(void* q, const void* k, const void* v, const float* cos_t,
+                          const float* sin_t, const int64_t* pos, const int64_t* slot_mapping,
+                          void* kv_cache, int64_t T, int n_head, int n_kv_head, int head_dim,
+                          int64_t q_tok_stride, int64_t k_tok_stride, int64_t v_tok_stride,
+                          int64_t max_pos, int64_t num_blocks, int block_size, int fmt) {
+    FormatSpec s;
+    if (!format_spec(fmt, &s) || T < 0 || n_head <= 0 || n_kv_head <= 0 || head_dim <= 0 ||
+        head_dim % 2 != 0 || n_head % n_kv_head != 0 || block_size <= 0 || num_blocks < 0)
+        return -1;
+    const int h = head_dim / 2;
+    const int64_t capacity = num_blocks * block_size;
+    std::set<int64_t> seen;
+    for (int64_t t = 0; t < T; ++t) {
+        int64_t sl = slot_mapping[t];
+        if (sl >= 0 && sl < capacity && pos[t] >= 0 && pos[t] < max_pos) {
+            if (!seen.insert(sl).second) return -1;
+        }
+    }
+    int64_t errors = 0;
+    double* xin = new double[head_dim];
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t p = pos[t];
+        const int64_t sl = slot_mapping[t];
+        const bool pos_ok = p >= 0 && p < max_pos;
+        const bool slot_in_range = sl < capacity;
+        if (!pos_ok) errors += 1;
+        if (sl >= 0 && !slot_in_range) errors += 1;
+        if (!pos_ok) continue;
+        const float* c_row = cos_t + p * h;
+        const float* s_row = sin_t + p * h;
+        // Q heads: rotate in place.
+        for (int hd = 0; hd < n_head; ++hd) {
+            const int64_t base = t * q_tok_stride + static_cast<int64_t>(hd) * head_dim;
+            for (int d = 0; d < head_dim; ++d) xin[d] = load(q, base + d, fmt);
+            for (int i = 0; i < h; ++i) {
+                const double c = c_row[i], sn = s_row[i];
+                store(q, base + i, xin[i] * c - xin[i + h] * sn, fmt);
+                store(q, base + i + h, xin[i + h] * c + xin[i] * sn, fmt);
+            }
+        }
+        if (sl < 0 || !slot_in_range) continue;
+        const int64_t blk = sl / block_size;
+        const int64_t off = sl % block_size;
+        for (int kvh = 0; kvh < n_kv_head; ++kvh) {
+            // cache[0 or 1, blk, off, kvh, :]
+            const int64_t k_dst = (((0 * num_blocks + blk) * block_size + off) * n_kv_head + kvh) *
+                                  static_cast<int64_t>(head_dim);
+            const int64_t v_dst = (((1 * num_blocks + blk) * block_size + off) * n_kv_head + kvh) *
+                                  static_cast<int64_t>(head_dim);
+            const int64_t k_src = t * k_tok_stride + static_cast<int64_t>(kvh) * head_dim;
+            const int64_t v_src = t * v_tok_stride + static_cast<int64_t>(kvh) * head_dim;
+            for (int d = 0; d < head_dim; ++d) xin[d] = load(k, k_src + d, fmt);
+            for (int i = 0; i < h; ++i) {
+                const double c = c_row[i], sn = s_row[i];
+                store(kv_cache, k_dst + i, xin[i] * c - xin[i + h] * sn, fmt);
+                store(kv_cache, k_dst + i + h, xin[i + h] * c + xin[i] * sn, fmt);
+            }
+            // V is stored unchanged: copy the element bits.
+            const int es = elem_size(fmt);
+            std::memcpy(static_cast<char*>(kv_cache) + v_dst * es,
+                        static_cast<const char*>(v) + v_src * es, static_cast<size_t>(head_dim) * es);
+        }
+    }
+    delete[] xin;
+    return errors;
+}
+
+// Gated linear unit over a fused gate_up tensor [T, 2I] (gate = columns [0, I),
+// up = columns [I, 2I)): out[t, j] = act(g) * u with act = silu (g / (1 + e^-g),
+// [koas] section 2) for act == 0 or relu (max(g, 0), [mer] section 3.3) for act == 1.
+int orc_glu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row_stride,
+            int64_t out_row_stride, int act, int fmt) {
+    FormatSpec s;
+    if (!format_spec(fmt, &s) || T < 0 || I <= 0 || (act != 0 && act != 1)) return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t j = 0; j < I; ++j) {
+            const double g = load(gate_up, t * in_row_stride + j, fmt);
+            const double u = load(gate_up, t * in_row_stride + I + j, fmt);
+            double a;
+            if (act == 0) {
+                a = g / (1.0 + std::exp(-g));
+            } else {
+                a = g > 0.0 ? g : 0.0;
+            }
+            store(out, t * out_row_stride + j, a * u, fmt);
+        }
+    }
+    return 0;
+}
+
+}  // extern "C"
