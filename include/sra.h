@@ -1,0 +1,218 @@
+/*
+ * sra.h — C ABI of the GB300 (sm_103a) per-token decoder-path library.
+ *
+ * Four bandwidth-bound operators of a transformer decoder layer, each a
+ * hand-written CUDA kernel chosen per shape:
+ *
+ *   sra_rmsnorm        row-wise RMSNorm, fp32 accumulation
+ *   sra_add_rmsnorm    residual add (in place) + RMSNorm
+ *   sra_rope_kv_store  neox RoPE of Q and K + paged KV-cache store through slot_mapping (GQA)
+ *   sra_glu            SwiGLU silu(gate) * up, or ReGLU relu(gate) * up, over a fused gate_up
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Pointers to tensors are DEVICE pointers (any memory the current device can
+ *    load from and store to). The caller owns every buffer; the library never
+ *    allocates, frees, zero-fills or keeps a pointer after the call returns.
+ *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
+ *    stream). Every call only enqueues work on that stream and returns at once;
+ *    results are visible after the stream is synchronised. The kernel runs on
+ *    the device that is current for the calling thread.
+ *  - Strides are in ELEMENTS, not bytes; the innermost (column) stride is 1.
+ *  - Any pointer alignment is accepted. 16-byte aligned rows and strides get the
+ *    128-bit vector kernels; other layouts get narrower accesses.
+ *  - Return value: SRA_OK (0) or a negative sra_status. Argument errors are
+ *    found on the host BEFORE anything is enqueued: on error nothing runs and
+ *    no output byte changes. SRA_ERR_LAUNCH reports a failed kernel launch
+ *    (cudaGetLastError after the launch). A zero-sized call (rows == 0 or
+ *    T == 0) validates its arguments, enqueues nothing and returns SRA_OK.
+ *  - No entry point waits on the device, traps or asserts on the device.
+ *  - Thread safety: calls may be made concurrently from several host threads.
+ *    sra_force_variant changes process-wide state and is meant for A/B
+ *    measurement only.
+ *
+ * Sources. The operators are those of these web pages (cited by title and section):
+ *  [koas] koas-w.github.io "preformanceimprovement": sec. 1 fused RoPE + paged KV
+ *         cache store; sec. 2 fused SwiGLU; sec. 3 Triton RMSNorm; sec. 4 fused add + norm.
+ *  [lsln] m.lsln.cn/news/61269 "21 个算子": sec. 2.3 RMSNorm and RoPE details.
+ *  [mer]  mer.dev "AsyncT vllm 适配加速笔记（一）": sec. 1.1 KV-cache layout;
+ *         sec. 3.3 kernel fusion (ReGLU as relu_and_mul; stride-aware kernels).
+ *  [csdn] agent.csdn.net "使用Triton实现RMSNorm算子": RMSNorm kernels and pitfalls.
+ */
+#ifndef SRA_H_
+#define SRA_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SRA_VERSION 1
+
+#if defined(__GNUC__)
+#define SRA_API __attribute__((visibility("default")))
+#else
+#define SRA_API
+#endif
+
+typedef enum sra_dtype {
+    SRA_F32 = 0,  /* IEEE binary32 */
+    SRA_F16 = 1,  /* IEEE binary16 */
+    SRA_BF16 = 2  /* bfloat16 */
+} sra_dtype_t;
+
+typedef enum sra_status {
+    SRA_OK = 0,
+    SRA_ERR_NULL = -1,     /* a required pointer is NULL */
+    SRA_ERR_SHAPE = -2,    /* a size is out of range (negative count, D <= 0, odd head_dim, ...) */
+    SRA_ERR_STRIDE = -3,   /* a row / token stride is smaller than the row it must hold */
+    SRA_ERR_DTYPE = -4,    /* dtype is not one of sra_dtype_t */
+    SRA_ERR_ALIAS = -5,    /* outputs overlap inputs in a way the operator forbids */
+    SRA_ERR_ARG = -6,      /* any other invalid argument (unknown activation, op name, ...) */
+    SRA_ERR_VARIANT = -7,  /* a forced kernel variant cannot handle this call */
+    SRA_ERR_LAUNCH = -8,   /* the CUDA launch failed (no device, bad context, ...) */
+    SRA_ERR_DEVICE = -9    /* the device could not be queried */
+} sra_status_t;
+
+typedef enum sra_act {
+    SRA_ACT_SILU = 0,  /* SwiGLU: silu(g) * u, silu(g) = g / (1 + e^-g)   [koas] sec. 2 */
+    SRA_ACT_RELU = 1   /* ReGLU:  max(g, 0) * u                            [mer] sec. 3.3 */
+} sra_act_t;
+
+/*
+ * sra_rmsnorm — [koas] sec. 3, [lsln] sec. 2.3, [csdn].
+ *
+ *   out[r, j] = x[r, j] * rsqrt( (1/D) * sum_k x[r, k]^2 + eps ) * w[j]
+ *
+ * x:    [rows, D] of dtype, row r at x + r * x_row_stride (x_row_stride >= D).
+ * w:    [D] of dtype, contiguous.
+ * out:  [rows, D] of dtype, row r at out + r * out_row_stride (>= D).
+ *       out may equal x exactly (in-place); any other overlap with x or w is
+ *       SRA_ERR_ALIAS.
+ * eps:  added to the mean of squares inside the root (eps >= 0).
+ * Arithmetic: inputs widened to fp32, fp32 sum of squares, one round-to-nearest-
+ * even to dtype on the store.
+ * Errors: NULL x/w/out (unless rows == 0) -> SRA_ERR_NULL; rows < 0 or D <= 0 ->
+ * SRA_ERR_SHAPE; stride < D -> SRA_ERR_STRIDE; eps < 0 or not finite -> SRA_ERR_ARG.
+ */
+SRA_API int sra_rmsnorm(const void* x, const void* w, void* out, int64_t rows, int64_t D,
+                int64_t x_row_stride, int64_t out_row_stride, float eps, int dtype,
+                void* stream);
+
+/*
+ * sra_add_rmsnorm — [koas] sec. 4 (x updated in place with the residual, the
+ * normalised result returned; read once, write twice).
+ *
+ *   x[r, j]   <- round_dtype( x[r, j] + res[r, j] )        (stored in place)
+ *   out[r, j]  = rmsnorm of the ROUNDED, stored x[r, :] as in sra_rmsnorm
+ *
+ * x:    [rows, D] in/out, row stride x_row_stride (>= D).
+ * res:  [rows, D] input, row stride res_row_stride (>= D). res may equal x exactly.
+ * w:    [D] contiguous.
+ * out:  [rows, D] output, row stride out_row_stride (>= D). out must not overlap
+ *       x, res or w (SRA_ERR_ALIAS).
+ * The stored sum is the correctly rounded x + res (fp32 add of two dtype values,
+ * then one RNE to dtype).
+ * Errors: as sra_rmsnorm, plus NULL res.
+ */
+SRA_API int sra_add_rmsnorm(void* x, const void* res, const void* w, void* out, int64_t rows, int64_t D,
+                    int64_t x_row_stride, int64_t res_row_stride, int64_t out_row_stride,
+                    float eps, int dtype, void* stream);
+
+/*
+ * sra_rope_kv_store — [koas] sec. 1 (RoPE fused with the paged KV-cache store,
+ * GQA through kv_head = head / (n_head / n_kv_head)); cache layout from [mer]
+ * sec. 1.1.
+ *
+ * For token t with p = pos[t], h = head_dim / 2, c = cos[p*h + i], s = sin[p*h + i]
+ * (neox half rotation, i < h):
+ *   y[i]     = x[i] * c - x[i + h] * s
+ *   y[i + h] = x[i + h] * c + x[i] * s
+ * - every Q head of token t is rotated IN PLACE in q;
+ * - every K head is rotated and written to kv_cache[0, b, o, kvh, :] and every
+ *   V head copied bit-for-bit to kv_cache[1, b, o, kvh, :], where
+ *   b = slot_mapping[t] / block_size and o = slot_mapping[t] % block_size.
+ * No other byte of the cache or of q changes; k and v are read-only.
+ *
+ * q:        [T, n_head, head_dim] of dtype; token t at q + t * q_tok_stride
+ *           (>= n_head * head_dim); heads contiguous within a token.
+ * k, v:     [T, n_kv_head, head_dim]; token strides k_tok_stride, v_tok_stride
+ *           (>= n_kv_head * head_dim). q, k and v may be views of one fused QKV
+ *           buffer; q must not overlap k or v.
+ * cos, sin: fp32 tables [max_pos, head_dim / 2], contiguous.
+ * pos, slot_mapping: int64 [T].
+ * kv_cache: [2, num_blocks, block_size, n_kv_head, head_dim] of dtype, contiguous.
+ * err_count: NULL, or a device int32 the kernel atomically increments by one for
+ *           every token whose position is outside [0, max_pos) and one more for
+ *           every token whose slot is >= num_blocks * block_size. The caller
+ *           zeroes it; the library only adds.
+ * Token rules: a position outside [0, max_pos) leaves q[t] unchanged and writes
+ * nothing to the cache; slot < 0 marks a padding token (Q still rotated, nothing
+ * written to the cache, not an error); a slot past the cache is skipped (and
+ * counted). Two tokens with the same valid slot race (undefined which wins).
+ * Errors (host): NULL pointers (err_count may be NULL) -> SRA_ERR_NULL;
+ * T < 0, n_head <= 0, n_kv_head <= 0, n_head % n_kv_head != 0, head_dim <= 0 or
+ * odd, block_size <= 0, num_blocks < 0, max_pos < 0 -> SRA_ERR_SHAPE;
+ * short strides -> SRA_ERR_STRIDE.
+ */
+SRA_API int sra_rope_kv_store(void* q, const void* k, const void* v, const float* cos, const float* sin,
+                      const int64_t* pos, const int64_t* slot_mapping, void* kv_cache, int64_t T,
+                      int n_head, int n_kv_head, int head_dim, int64_t q_tok_stride,
+                      int64_t k_tok_stride, int64_t v_tok_stride, int64_t max_pos,
+                      int64_t num_blocks, int block_size, int32_t* err_count, int dtype,
+                      void* stream);
+
+/*
+ * sra_glu — [koas] sec. 2 (SwiGLU: gate and up loaded together, activation and
+ * product in registers, one write), [mer] sec. 3.3 (ReGLU, relu_and_mul).
+ *
+ *   out[t, j] = act( gate_up[t, j] ) * gate_up[t, I + j],   0 <= j < I
+ *
+ * gate_up: [T, 2I] of dtype (gate = first I columns, up = last I), row stride
+ *          in_row_stride (>= 2I).
+ * out:     [T, I] of dtype, row stride out_row_stride (>= I); must not overlap gate_up.
+ * act:     SRA_ACT_SILU or SRA_ACT_RELU. fp32 arithmetic, one RNE on the store.
+ * Errors: NULL -> SRA_ERR_NULL; T < 0 or I <= 0 -> SRA_ERR_SHAPE; short strides
+ * -> SRA_ERR_STRIDE; unknown act -> SRA_ERR_ARG; overlap -> SRA_ERR_ALIAS.
+ */
+SRA_API int sra_glu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row_stride,
+            int64_t out_row_stride, int act, int dtype, void* stream);
+
+/* sra_swiglu — sra_glu with act = SRA_ACT_SILU (the spec call swiglu(gate_up, out, T, I)). */
+SRA_API int sra_swiglu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row_stride,
+               int64_t out_row_stride, int dtype, void* stream);
+
+/* Static text for a status code (never NULL). */
+SRA_API const char* sra_status_string(int status);
+
+/* SRA_VERSION of the loaded library. */
+SRA_API int sra_version(void);
+
+/*
+ * Kernel-variant control, for A/B measurement of the per-shape dispatch.
+ * op: "rmsnorm" (also used by add_rmsnorm), "rope_kv_store", "glu".
+ * variant: -1 = automatic per-shape choice (the default); otherwise an index
+ * < sra_variant_count(op). A forced variant that cannot serve a later call makes
+ * that call return SRA_ERR_VARIANT without enqueueing anything.
+ * Returns SRA_OK, or SRA_ERR_ARG for an unknown op or out-of-range variant.
+ */
+SRA_API int sra_force_variant(const char* op, int variant);
+SRA_API int sra_variant_count(const char* op);
+/* Name of a variant ("warp_rows", "cta_row", ...); NULL for bad arguments. */
+SRA_API const char* sra_variant_name(const char* op, int variant);
+/*
+ * The variant the automatic dispatch would pick for a call with these sizes and
+ * all pointers and strides 16-byte aligned, on a GPU with num_sms SMs
+ * (num_sms <= 0: query the current device). rmsnorm: a = rows, b = D;
+ * rope_kv_store: a = T, b = n_head, c = n_kv_head, d = head_dim; glu: a = T, b = I.
+ * Negative sra_status on bad arguments. Enqueues nothing.
+ */
+SRA_API int sra_pick_variant(const char* op, int64_t a, int64_t b, int64_t c, int64_t d, int dtype,
+                     int num_sms);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SRA_H_ */

@@ -1,0 +1,26 @@
+"""GB300-native fused per-token decoder path: RMSNorm, residual-add + RMSNorm,
+neox RoPE with paged KV-cache store, SwiGLU / ReGLU.
+
+Every operator runs in the hand-written sm_103a CUDA kernels of ``libsra.so``
+(C ABI in ``include/sra.h``). This module only marshals torch tensors into that
+ABI: pointers, sizes, strides, dtype code and the current CUDA stream. There is
+no CPU or PyTorch fallback: without the built library every call raises.
+"""
+from ._binding import (  # noqa: F401
+    SRAError,
+    add_rmsnorm,
+    force_variant,
+    glu,
+    lib,
+    pick_variant,
+    reglu,
+    rmsnorm,
+    rope_kv_store,
+    status_string,
+    swiglu,
+    variant_count,
+    variant_name,
+)
+
+__all__ = ["rmsnorm", "add_rmsnorm", "rope_kv_store", "swiglu", "reglu", "glu", "lib", "SRAError",
+           "force_variant", "variant_count", "variant_name", "pick_variant", "status_string"]

@@ -1,0 +1,262 @@
+"""ctypes binding of include/sra.h (argument marshalling only)."""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_PKG, "libsra.so")
+_lock = threading.Lock()
+_lib = None
+
+DTYPE_CODE = {torch.float32: 0, torch.float16: 1, torch.bfloat16: 2}
+ACT_CODE = {"silu": 0, "relu": 1}
+
+
+class SRAError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libsra.so. Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(_LIB_PATH):
+                raise RuntimeError(
+                    f"{_LIB_PATH} is missing: build it with `python -c \"import __graft_entry__ as g; "
+                    "g.build()\"` (needs nvcc). There is no fallback implementation.")
+            L = ctypes.CDLL(_LIB_PATH)
+            i64, i32, vp, f32 = ctypes.c_int64, ctypes.c_int, ctypes.c_void_p, ctypes.c_float
+            L.sra_rmsnorm.argtypes = [vp, vp, vp, i64, i64, i64, i64, f32, i32, vp]
+            L.sra_add_rmsnorm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, i32, vp]
+            L.sra_rope_kv_store.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i64,
+                                            i64, i64, i64, i32, vp, i32, vp]
+            L.sra_glu.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, vp]
+            L.sra_swiglu.argtypes = [vp, vp, i64, i64, i64, i64, i32, vp]
+            for fn in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_glu", "sra_swiglu"):
+                getattr(L, fn).restype = i32
+            L.sra_status_string.argtypes = [i32]
+            L.sra_status_string.restype = ctypes.c_char_p
+            L.sra_version.restype = i32
+            L.sra_force_variant.argtypes = [ctypes.c_char_p, i32]
+            L.sra_force_variant.restype = i32
+            L.sra_variant_count.argtypes = [ctypes.c_char_p]
+            L.sra_variant_count.restype = i32
+            L.sra_variant_name.argtypes = [ctypes.c_char_p, i32]
+            L.sra_variant_name.restype = ctypes.c_char_p
+            L.sra_pick_variant.argtypes = [ctypes.c_char_p, i64, i64, i64, i64, i32, i32]
+            L.sra_pick_variant.restype = i32
+            _lib = L
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().sra_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int) -> None:
+    if status != 0:
+        raise SRAError(fn, status)
+
+
+def force_variant(op: str, variant: int) -> None:
+    _check("sra_force_variant", lib().sra_force_variant(op.encode(), int(variant)))
+
+
+def variant_count(op: str) -> int:
+    return int(lib().sra_variant_count(op.encode()))
+
+
+def variant_name(op: str, variant: int) -> str | None:
+    r = lib().sra_variant_name(op.encode(), int(variant))
+    return r.decode() if r is not None else None
+
+
+def pick_variant(op: str, a: int, b: int, c: int = 0, d: int = 0, dtype=torch.bfloat16, num_sms: int = 0) -> int:
+    return int(lib().sra_pick_variant(op.encode(), a, b, c, d, DTYPE_CODE[dtype], num_sms))
+
+
+# --------------------------------------------------------------------- helpers
+def _cuda(t: torch.Tensor, name: str) -> None:
+    if not isinstance(t, torch.Tensor) or t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+
+
+def _dtype(t: torch.Tensor) -> int:
+    if t.dtype not in DTYPE_CODE:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    return DTYPE_CODE[t.dtype]
+
+
+def _as_rows(t: torch.Tensor, name: str) -> tuple[int, int, int]:
+    """(rows, width, row stride) of a [..., width] tensor whose rows share one stride."""
+    if t.dim() == 0:
+        raise ValueError(f"{name} must have at least one dimension")
+    if t.shape[-1] > 1 and t.stride(-1) != 1:
+        raise ValueError(f"{name}: innermost stride must be 1")
+    width = t.shape[-1]
+    if t.dim() == 1:
+        return 1, width, width
+    lead = t.shape[:-1]
+    rows = 1
+    for s in lead:
+        rows *= s
+    if rows <= 1:
+        return rows, width, max(width, t.stride(-2) if t.dim() >= 2 else width)
+    # leading dims must collapse to one uniform row stride
+    stride = t.stride(-2)
+    expect = stride
+    for i in range(t.dim() - 2, -1, -1):
+        if t.shape[i] != 1 and t.stride(i) != expect:
+            raise ValueError(f"{name}: leading dimensions do not collapse to one row stride")
+        expect *= t.shape[i]
+    return rows, width, stride
+
+
+def _stream(t: torch.Tensor, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(t.device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _same_device(*ts):
+    dev = ts[0].device
+    for t in ts:
+        if t is not None and t.device != dev:
+            raise ValueError("all tensors must be on the same CUDA device")
+
+
+# -------------------------------------------------------------------- operators
+def rmsnorm(x: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None, eps: float = 1e-6,
+            stream=None) -> torch.Tensor:
+    """out = x * rsqrt(mean(x^2, -1) + eps) * w (fp32 accumulation). out may be x."""
+    _cuda(x, "x"), _cuda(w, "w")
+    if out is None:
+        out = torch.empty_like(x)
+    _cuda(out, "out")
+    _same_device(x, w, out)
+    if w.dtype != x.dtype or out.dtype != x.dtype:
+        raise ValueError("x, w and out must share one dtype")
+    rows, D, xs = _as_rows(x, "x")
+    orows, oD, os_ = _as_rows(out, "out")
+    if (orows, oD) != (rows, D) or w.numel() != D or (D > 1 and not w.is_contiguous()):
+        raise ValueError("shape mismatch")
+    with torch.cuda.device(x.device):
+        st = lib().sra_rmsnorm(x.data_ptr(), w.data_ptr(), out.data_ptr(), rows, D, xs, os_, float(eps),
+                               _dtype(x), _stream(x, stream))
+    _check("sra_rmsnorm", st)
+    return out
+
+
+def add_rmsnorm(x: torch.Tensor, res: torch.Tensor, w: torch.Tensor, out: torch.Tensor | None = None,
+                eps: float = 1e-6, stream=None) -> torch.Tensor:
+    """x <- x + res (in place, rounded to x.dtype); returns out = rmsnorm(x) * w."""
+    for t, n in ((x, "x"), (res, "res"), (w, "w")):
+        _cuda(t, n)
+    if out is None:
+        out = torch.empty_like(x)
+    _cuda(out, "out")
+    _same_device(x, res, w, out)
+    if not (res.dtype == w.dtype == out.dtype == x.dtype):
+        raise ValueError("x, res, w and out must share one dtype")
+    rows, D, xs = _as_rows(x, "x")
+    rrows, rD, rs = _as_rows(res, "res")
+    orows, oD, os_ = _as_rows(out, "out")
+    if (rrows, rD) != (rows, D) or (orows, oD) != (rows, D) or w.numel() != D:
+        raise ValueError("shape mismatch")
+    with torch.cuda.device(x.device):
+        st = lib().sra_add_rmsnorm(x.data_ptr(), res.data_ptr(), w.data_ptr(), out.data_ptr(), rows, D, xs, rs,
+                                   os_, float(eps), _dtype(x), _stream(x, stream))
+    _check("sra_add_rmsnorm", st)
+    return out
+
+
+def _tok_stride(t: torch.Tensor, name: str) -> int:
+    if t.dim() != 3:
+        raise ValueError(f"{name} must be [T, heads, head_dim]")
+    if t.stride(-1) != 1 or (t.shape[1] > 1 and t.stride(1) != t.shape[2]):
+        raise ValueError(f"{name}: heads must be contiguous within a token")
+    return t.stride(0) if t.shape[0] > 1 else t.shape[1] * t.shape[2]
+
+
+def rope_kv_store(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor,
+                  pos: torch.Tensor, slot_mapping: torch.Tensor, kv_cache: torch.Tensor,
+                  err_count: torch.Tensor | None = None, max_pos: int | None = None, stream=None) -> None:
+    """Rotate q in place; write rotated k and v into kv_cache[0/1, slot // bs, slot % bs]."""
+    for t, n in ((q, "q"), (k, "k"), (v, "v"), (cos, "cos"), (sin, "sin"), (pos, "pos"),
+                 (slot_mapping, "slot_mapping"), (kv_cache, "kv_cache")):
+        _cuda(t, n)
+    _same_device(q, k, v, cos, sin, pos, slot_mapping, kv_cache, err_count)
+    if not (k.dtype == v.dtype == kv_cache.dtype == q.dtype):
+        raise ValueError("q, k, v and kv_cache must share one dtype")
+    if cos.dtype != torch.float32 or sin.dtype != torch.float32 or not cos.is_contiguous() \
+            or not sin.is_contiguous():
+        raise ValueError("cos and sin must be contiguous float32 [max_pos, head_dim // 2]")
+    if pos.dtype != torch.int64 or slot_mapping.dtype != torch.int64 or not pos.is_contiguous() \
+            or not slot_mapping.is_contiguous():
+        raise ValueError("pos and slot_mapping must be contiguous int64")
+    if kv_cache.dim() != 5 or not kv_cache.is_contiguous() or kv_cache.shape[0] != 2:
+        raise ValueError("kv_cache must be contiguous [2, num_blocks, block_size, n_kv_head, head_dim]")
+    if err_count is not None:
+        _cuda(err_count, "err_count")
+        if err_count.dtype != torch.int32:
+            raise ValueError("err_count must be int32")
+    T, n_head, hd = q.shape
+    n_kv = k.shape[1]
+    _, nb, bs, cn_kv, chd = kv_cache.shape
+    if k.shape != (T, n_kv, hd) or v.shape != (T, n_kv, hd) or (cn_kv, chd) != (n_kv, hd) \
+            or pos.numel() != T or slot_mapping.numel() != T:
+        raise ValueError("shape mismatch")
+    if max_pos is None:
+        max_pos = cos.shape[0]
+    if cos.shape[-1] != hd // 2 or sin.shape != cos.shape or max_pos > cos.shape[0]:
+        raise ValueError("cos / sin tables must be [>= max_pos, head_dim // 2]")
+    with torch.cuda.device(q.device):
+        st = lib().sra_rope_kv_store(q.data_ptr(), k.data_ptr(), v.data_ptr(), cos.data_ptr(), sin.data_ptr(),
+                                     pos.data_ptr(), slot_mapping.data_ptr(), kv_cache.data_ptr(), T, n_head,
+                                     n_kv, hd, _tok_stride(q, "q"), _tok_stride(k, "k"), _tok_stride(v, "v"),
+                                     int(max_pos), nb, bs,
+                                     err_count.data_ptr() if err_count is not None else None,
+                                     _dtype(q), _stream(q, stream))
+    _check("sra_rope_kv_store", st)
+
+
+def glu(gate_up: torch.Tensor, out: torch.Tensor | None = None, act: str = "silu", stream=None) -> torch.Tensor:
+    """out[t, j] = act(gate_up[t, j]) * gate_up[t, I + j] for act in {'silu', 'relu'}."""
+    _cuda(gate_up, "gate_up")
+    rows, W, is_ = _as_rows(gate_up, "gate_up")
+    if W % 2:
+        raise ValueError("gate_up width must be even (gate | up)")
+    I = W // 2
+    if out is None:
+        out = torch.empty(*gate_up.shape[:-1], I, dtype=gate_up.dtype, device=gate_up.device)
+    _cuda(out, "out")
+    _same_device(gate_up, out)
+    if out.dtype != gate_up.dtype:
+        raise ValueError("gate_up and out must share one dtype")
+    orows, oI, os_ = _as_rows(out, "out")
+    if (orows, oI) != (rows, I):
+        raise ValueError("shape mismatch")
+    if act not in ACT_CODE:
+        raise ValueError("act must be 'silu' or 'relu'")
+    with torch.cuda.device(gate_up.device):
+        st = lib().sra_glu(gate_up.data_ptr(), out.data_ptr(), rows, I, is_, os_, ACT_CODE[act],
+                           _dtype(gate_up), _stream(gate_up, stream))
+    _check("sra_glu", st)
+    return out
+
+
+def swiglu(gate_up: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """silu(gate) * up over a fused [.., 2I] gate_up."""
+    return glu(gate_up, out, "silu", stream)
+
+
+def reglu(gate_up: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """relu(gate) * up over a fused [.., 2I] gate_up."""
+    return glu(gate_up, out, "relu", stream)

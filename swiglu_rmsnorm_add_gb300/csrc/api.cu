@@ -1,0 +1,460 @@
+// C-ABI entry points (include/sra.h): argument validation, per-shape kernel
+// planning and launch on the caller's stream. Host code only.
+//
+// Validation happens entirely before the first CUDA runtime call, so a bad call
+// enqueues nothing and touches no device state. Planning is a pure function of
+// the sizes, the alignment of every pointer and stride, and the SM count.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstring>
+
+#include "internal.h"
+#include "sra.h"
+
+namespace sra {
+namespace {
+
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_smem_optin[kMaxDevices];
+std::atomic<int> g_force_norm{-1}, g_force_rope{-1}, g_force_glu{-1};
+
+// SM count of the current device (cached per device).
+int current_sm_count(int* dev_out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return -1;
+    }
+    if (dev_out) *dev_out = dev;
+    if (dev >= 0 && dev < kMaxDevices) {
+        int c = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return -1;
+    }
+    if (dev >= 0 && dev < kMaxDevices) g_sm_count[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+int smem_optin(int dev) {
+    if (dev >= 0 && dev < kMaxDevices) {
+        int c = g_smem_optin[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 48 * 1024;
+    }
+    if (dev >= 0 && dev < kMaxDevices) g_smem_optin[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+bool valid_dtype(int dt) { return dt == DT_F32 || dt == DT_F16 || dt == DT_BF16; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool stride_aligned16(int64_t stride_elems, int es) { return ((stride_elems * es) & 15) == 0; }
+
+// Byte span [lo, hi) of a strided [rows, width] region.
+struct Span {
+    uintptr_t lo, hi;
+};
+Span span_of(const void* p, int64_t rows, int64_t stride, int64_t width, int es) {
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    const int64_t n = rows <= 0 ? 0 : ((rows - 1) * stride + width);
+    return {lo, lo + static_cast<uintptr_t>(n) * static_cast<uintptr_t>(es)};
+}
+bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
+
+int ceil_div_i(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+int round_up32(int64_t v) { return static_cast<int>(((v + 31) / 32) * 32); }
+
+// ------------------------------------------------------------------ RMSNorm plan
+// Register capacity of each variant, in accesses of `vec` elements.
+constexpr int kWarpMaxNv = 8;
+constexpr int kCtaMaxAccesses = 2048;  // 256 threads x 8, 512 x 4, 1024 x 2
+
+int cta_max_threads_for_nv(int nv) { return nv >= 8 ? 256 : (nv >= 4 ? 512 : 1024); }
+
+bool plan_norm_variant(int variant, int64_t rows, int64_t D, int vec, int es, int num_sms, int smem_limit,
+                       NormPlan* p) {
+    const int64_t nacc = ceil_div(D, vec);  // accesses per row, tail included
+    p->variant = variant;
+    p->vec = vec;
+    p->smem = 0;
+    switch (variant) {
+        case NORM_WARP_ROWS: {
+            const int64_t per_lane = ceil_div(nacc, 32);
+            if (per_lane > kWarpMaxNv) return false;
+            int nv = 1;
+            while (nv < per_lane) nv <<= 1;
+            p->nv = nv;
+            // Warps per CTA: spread few rows over many SMs, pack many rows densely.
+            int wpc = 1;
+            if (rows >= 8LL * num_sms) wpc = 8;
+            else if (rows >= 4LL * num_sms) wpc = 4;
+            else if (rows >= 2LL * num_sms) wpc = 2;
+            p->threads = 32 * wpc;
+            const int64_t max_ctas = static_cast<int64_t>(num_sms) * (2048 / p->threads);
+            p->grid = std::max<int64_t>(1, std::min(ceil_div(rows, wpc), max_ctas));
+            return true;
+        }
+        case NORM_CTA_ROW: {
+            if (nacc > kCtaMaxAccesses) return false;
+            // Few rows (decode): spread a row over many threads, short per-thread
+            // chains. Many rows: fewer threads per row, more accesses each.
+            const bool few_rows = rows < 2LL * num_sms;
+            int nv = few_rows ? 1 : 4;
+            while (nv < 8 && ceil_div(nacc, nv) > cta_max_threads_for_nv(nv)) nv <<= 1;
+            while (nv > 1 && ceil_div(nacc, nv) < 64) nv >>= 1;
+            if (ceil_div(nacc, nv) > cta_max_threads_for_nv(nv)) return false;
+            p->nv = nv;
+            p->threads = std::max(32, round_up32(ceil_div(nacc, nv)));
+            const int64_t max_ctas = static_cast<int64_t>(num_sms) * std::max(1, 2048 / p->threads);
+            p->grid = std::max<int64_t>(1, std::min(rows, max_ctas));
+            return true;
+        }
+        case NORM_CTA_SMEM: {
+            const int64_t bytes = ceil_div(D, vec) * vec * es;
+            if (bytes > smem_limit - 1024) return false;
+            p->nv = 0;
+            p->smem = static_cast<size_t>(bytes);
+            p->threads = static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(nacc))));
+            const int per_sm = std::max<int64_t>(1, (smem_limit) / std::max<int64_t>(bytes, 1));
+            p->grid = std::max<int64_t>(1, std::min(rows, static_cast<int64_t>(num_sms) * per_sm));
+            return true;
+        }
+        case NORM_TWO_PASS: {
+            p->nv = 0;
+            p->threads = static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(nacc))));
+            const int64_t max_ctas = static_cast<int64_t>(num_sms) * std::max(1, 2048 / p->threads);
+            p->grid = std::max<int64_t>(1, std::min(rows, max_ctas));
+            return true;
+        }
+        default:
+            return false;
+    }
+}
+
+int auto_norm_variant(int64_t rows, int64_t D, int vec) {
+    const int64_t nacc = ceil_div(D, vec);
+    // Warp-per-row when the row fits a warp's registers and there are enough rows
+    // to keep the SMs busy; otherwise a CTA per row.
+    if (nacc <= 32 * kWarpMaxNv && (rows >= 256 || nacc <= 64)) return NORM_WARP_ROWS;
+    if (nacc <= kCtaMaxAccesses) return NORM_CTA_ROW;
+    return NORM_CTA_SMEM;
+}
+
+int norm_vec(int dt, const void* const* ptrs, int nptr, const int64_t* strides, int nstr) {
+    const int es = elem_bytes(dt);
+    bool ok = true;
+    for (int i = 0; i < nptr; ++i) ok = ok && aligned16(ptrs[i]);
+    for (int i = 0; i < nstr; ++i) ok = ok && stride_aligned16(strides[i], es);
+    return ok ? 16 / es : 1;
+}
+
+int plan_norm(int64_t rows, int64_t D, int dt, int vec, int num_sms, int smem_limit, NormPlan* p) {
+    const int es = elem_bytes(dt);
+    const int forced = g_force_norm.load(std::memory_order_relaxed);
+    if (forced >= 0) {
+        if (!plan_norm_variant(forced, rows, D, vec, es, num_sms, smem_limit, p)) return SRA_ERR_VARIANT;
+        return SRA_OK;
+    }
+    int v = auto_norm_variant(rows, D, vec);
+    if (v == NORM_CTA_SMEM && !plan_norm_variant(v, rows, D, vec, es, num_sms, smem_limit, p)) v = NORM_TWO_PASS;
+    if (!plan_norm_variant(v, rows, D, vec, es, num_sms, smem_limit, p)) return SRA_ERR_VARIANT;
+    return SRA_OK;
+}
+
+// ------------------------------------------------------------------ RoPE plan
+int plan_rope(int64_t T, int n_head, int n_kv, int head_dim, int pairs, int num_sms, RopePlan* p) {
+    const int forced = g_force_rope.load(std::memory_order_relaxed);
+    if (forced > 0) return SRA_ERR_VARIANT;
+    const int h = head_dim / 2;
+    const int64_t U = static_cast<int64_t>(n_head + 2 * n_kv) * (h / pairs);
+    p->variant = ROPE_TOKEN_CTA;
+    p->pairs = pairs;
+    p->threads = static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(U))));
+    const int64_t max_ctas = static_cast<int64_t>(num_sms) * std::max(1, 2048 / p->threads);
+    p->grid = std::max<int64_t>(1, std::min(T, max_ctas));
+    return SRA_OK;
+}
+
+// ------------------------------------------------------------------- GLU plan
+int plan_glu(int64_t T, int64_t I, int vec, int num_sms, GluPlan* p) {
+    const int forced = g_force_glu.load(std::memory_order_relaxed);
+    if (forced > 0) return SRA_ERR_VARIANT;
+    const int64_t nv = I / vec;
+    p->variant = GLU_COLS_ROWS;
+    p->vec = vec;
+    // Few rows: narrow CTAs spread the columns over many SMs. Many rows: 256 threads.
+    int threads = T >= 64 ? 256 : 128;
+    threads = static_cast<int>(std::min<int64_t>(threads, std::max(32, round_up32(nv))));
+    p->threads = threads;
+    p->grid_x = ceil_div(nv, threads);
+    const int64_t resident = static_cast<int64_t>(num_sms) * (2048 / threads);
+    const int64_t gy = std::max<int64_t>(1, resident / std::max<int64_t>(1, p->grid_x));
+    p->grid_y = std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(T, gy), 65535));
+    return SRA_OK;
+}
+
+// Largest power-of-two vector width (elements, <= 16 bytes) that divides I and
+// every stride and keeps every pointer aligned.
+int glu_vec(int dt, const void* gu, const void* out, int64_t I, int64_t is, int64_t os) {
+    const int es = elem_bytes(dt);
+    for (int bytes = 16; bytes >= es * 2; bytes >>= 1) {
+        const int vec = bytes / es;
+        if ((reinterpret_cast<uintptr_t>(gu) % bytes) == 0 && (reinterpret_cast<uintptr_t>(out) % bytes) == 0 &&
+            I % vec == 0 && is % vec == 0 && os % vec == 0)
+            return vec;
+    }
+    return 1;
+}
+
+int status_from(cudaError_t e) {
+    if (e == cudaSuccess) return SRA_OK;
+    cudaGetLastError();
+    return SRA_ERR_LAUNCH;
+}
+
+int norm_common(void* x, const void* res, const void* w, void* out, int64_t rows, int64_t D, int64_t xs,
+                int64_t rs, int64_t os, float eps, int dtype, void* stream, bool add) {
+    if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
+    if (rows < 0 || D <= 0) return SRA_ERR_SHAPE;
+    if (xs < D || os < D || (add && rs < D)) return SRA_ERR_STRIDE;
+    if (!(eps >= 0.0f) || !std::isfinite(eps)) return SRA_ERR_ARG;
+    if (rows == 0) return SRA_OK;
+    if (!x || !w || !out || (add && !res)) return SRA_ERR_NULL;
+    const int es = elem_bytes(dtype);
+    const Span sx = span_of(x, rows, xs, D, es), so = span_of(out, rows, os, D, es), sw = span_of(w, 1, D, D, es);
+    if (add) {
+        const Span sr = span_of(res, rows, rs, D, es);
+        if (overlap(so, sx) || overlap(so, sr) || overlap(so, sw) || overlap(sx, sw)) return SRA_ERR_ALIAS;
+        if (overlap(sx, sr) && !(res == x && rs == xs)) return SRA_ERR_ALIAS;
+    } else {
+        const bool in_place = out == x && os == xs;
+        if ((!in_place && overlap(so, sx)) || overlap(so, sw)) return SRA_ERR_ALIAS;
+    }
+    int dev = 0;
+    const int sms = current_sm_count(&dev);
+    if (sms <= 0) return SRA_ERR_DEVICE;
+    const void* ptrs[4] = {x, w, out, add ? res : x};
+    const int64_t strides[3] = {xs, os, add ? rs : xs};
+    const int vec = norm_vec(dtype, ptrs, 4, strides, 3);
+    NormPlan plan;
+    const int smem_limit = smem_optin(dev);
+    int st = plan_norm(rows, D, dtype, vec, sms, smem_limit, &plan);
+    if (st != SRA_OK) return st;
+    if (plan.variant == NORM_CTA_SMEM && plan.smem > 48 * 1024) {
+        if (norm_smem_prepare(dtype, add, vec, plan.smem) != cudaSuccess) return status_from(cudaErrorInvalidValue);
+    }
+    NormArgs a;
+    a.x = x;
+    a.res = res;
+    a.w = w;
+    a.out = out;
+    a.rows = rows;
+    a.D = D;
+    a.xs = xs;
+    a.rs = add ? rs : 0;
+    a.os = os;
+    a.eps = eps;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    return status_from(add ? launch_add_rmsnorm(a, plan, dtype, s) : launch_rmsnorm(a, plan, dtype, s));
+}
+
+std::atomic<int>* force_slot(const char* op) {
+    if (!op) return nullptr;
+    if (std::strcmp(op, "rmsnorm") == 0) return &g_force_norm;
+    if (std::strcmp(op, "rope_kv_store") == 0) return &g_force_rope;
+    if (std::strcmp(op, "glu") == 0) return &g_force_glu;
+    return nullptr;
+}
+
+int variant_count(const char* op) {
+    if (!op) return SRA_ERR_ARG;
+    if (std::strcmp(op, "rmsnorm") == 0) return NORM_NUM_VARIANTS;
+    if (std::strcmp(op, "rope_kv_store") == 0) return ROPE_NUM_VARIANTS;
+    if (std::strcmp(op, "glu") == 0) return GLU_NUM_VARIANTS;
+    return SRA_ERR_ARG;
+}
+
+}  // namespace
+}  // namespace sra
+
+using namespace sra;
+
+extern "C" {
+
+int sra_version(void) { return SRA_VERSION; }
+
+const char* sra_status_string(int status) {
+    switch (status) {
+        case SRA_OK: return "ok";
+        case SRA_ERR_NULL: return "a required pointer is NULL";
+        case SRA_ERR_SHAPE: return "a size is out of range";
+        case SRA_ERR_STRIDE: return "a stride is smaller than the row it must hold";
+        case SRA_ERR_DTYPE: return "unsupported dtype";
+        case SRA_ERR_ALIAS: return "an output overlaps an input in a way the operator forbids";
+        case SRA_ERR_ARG: return "invalid argument";
+        case SRA_ERR_VARIANT: return "the forced kernel variant cannot handle this call";
+        case SRA_ERR_LAUNCH: return "CUDA kernel launch failed";
+        case SRA_ERR_DEVICE: return "could not query the CUDA device";
+        default: return "unknown status";
+    }
+}
+
+int sra_rmsnorm(const void* x, const void* w, void* out, int64_t rows, int64_t D, int64_t x_row_stride,
+                int64_t out_row_stride, float eps, int dtype, void* stream) {
+    return norm_common(const_cast<void*>(x), nullptr, w, out, rows, D, x_row_stride, 0, out_row_stride, eps,
+                       dtype, stream, false);
+}
+
+int sra_add_rmsnorm(void* x, const void* res, const void* w, void* out, int64_t rows, int64_t D,
+                    int64_t x_row_stride, int64_t res_row_stride, int64_t out_row_stride, float eps, int dtype,
+                    void* stream) {
+    return norm_common(x, res, w, out, rows, D, x_row_stride, res_row_stride, out_row_stride, eps, dtype, stream,
+                       true);
+}
+
+int sra_rope_kv_store(void* q, const void* k, const void* v, const float* cos, const float* sin,
+                      const int64_t* pos, const int64_t* slot_mapping, void* kv_cache, int64_t T, int n_head,
+                      int n_kv_head, int head_dim, int64_t q_tok_stride, int64_t k_tok_stride,
+                      int64_t v_tok_stride, int64_t max_pos, int64_t num_blocks, int block_size,
+                      int32_t* err_count, int dtype, void* stream) {
+    if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
+    if (T < 0 || n_head <= 0 || n_kv_head <= 0 || n_head % n_kv_head != 0 || head_dim <= 0 || head_dim % 2 != 0 ||
+        block_size <= 0 || num_blocks < 0 || max_pos < 0)
+        return SRA_ERR_SHAPE;
+    const int64_t qw = static_cast<int64_t>(n_head) * head_dim, kw = static_cast<int64_t>(n_kv_head) * head_dim;
+    if (q_tok_stride < qw || k_tok_stride < kw || v_tok_stride < kw) return SRA_ERR_STRIDE;
+    if (T == 0) return SRA_OK;
+    if (!q || !k || !v || !cos || !sin || !pos || !slot_mapping || !kv_cache) return SRA_ERR_NULL;
+    const int es = elem_bytes(dtype);
+    const Span sq = span_of(q, T, q_tok_stride, qw, es), sk = span_of(k, T, k_tok_stride, kw, es),
+               sv = span_of(v, T, v_tok_stride, kw, es);
+    const Span sc = span_of(kv_cache, 1, 0, 2 * num_blocks * block_size * kw, es);
+    if (overlap(sq, sk) || overlap(sq, sv) || overlap(sc, sq) || overlap(sc, sk) || overlap(sc, sv))
+        return SRA_ERR_ALIAS;
+    int dev = 0;
+    const int sms = current_sm_count(&dev);
+    if (sms <= 0) return SRA_ERR_DEVICE;
+    const int h = head_dim / 2;
+    int pairs = 16 / es;
+    const bool vec_ok = h % pairs == 0 && h % 4 == 0 && aligned16(q) && aligned16(k) && aligned16(v) &&
+                        aligned16(kv_cache) && aligned16(cos) && aligned16(sin) &&
+                        stride_aligned16(q_tok_stride, es) && stride_aligned16(k_tok_stride, es) &&
+                        stride_aligned16(v_tok_stride, es);
+    if (!vec_ok) pairs = 1;
+    RopePlan plan;
+    int st = plan_rope(T, n_head, n_kv_head, head_dim, pairs, sms, &plan);
+    if (st != SRA_OK) return st;
+    RopeArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.cos = cos;
+    a.sin = sin;
+    a.pos = pos;
+    a.slot = slot_mapping;
+    a.cache = kv_cache;
+    a.err = err_count;
+    a.T = T;
+    a.n_head = n_head;
+    a.n_kv = n_kv_head;
+    a.head_dim = head_dim;
+    a.qs = q_tok_stride;
+    a.ks = k_tok_stride;
+    a.vs = v_tok_stride;
+    a.max_pos = max_pos;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    return status_from(launch_rope_kv_store(a, plan, dtype, static_cast<cudaStream_t>(stream)));
+}
+
+int sra_glu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row_stride, int64_t out_row_stride,
+            int act, int dtype, void* stream) {
+    if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
+    if (act != SRA_ACT_SILU && act != SRA_ACT_RELU) return SRA_ERR_ARG;
+    if (T < 0 || I <= 0) return SRA_ERR_SHAPE;
+    if (in_row_stride < 2 * I || out_row_stride < I) return SRA_ERR_STRIDE;
+    if (T == 0) return SRA_OK;
+    if (!gate_up || !out) return SRA_ERR_NULL;
+    const int es = elem_bytes(dtype);
+    if (overlap(span_of(gate_up, T, in_row_stride, 2 * I, es), span_of(out, T, out_row_stride, I, es)))
+        return SRA_ERR_ALIAS;
+    int dev = 0;
+    const int sms = current_sm_count(&dev);
+    if (sms <= 0) return SRA_ERR_DEVICE;
+    GluPlan plan;
+    int st = plan_glu(T, I, glu_vec(dtype, gate_up, out, I, in_row_stride, out_row_stride), sms, &plan);
+    if (st != SRA_OK) return st;
+    GluArgs a;
+    a.gate_up = gate_up;
+    a.out = out;
+    a.T = T;
+    a.I = I;
+    a.is = in_row_stride;
+    a.os = out_row_stride;
+    return status_from(launch_glu(a, plan, act, dtype, static_cast<cudaStream_t>(stream)));
+}
+
+int sra_swiglu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row_stride,
+               int64_t out_row_stride, int dtype, void* stream) {
+    return sra_glu(gate_up, out, T, I, in_row_stride, out_row_stride, SRA_ACT_SILU, dtype, stream);
+}
+
+int sra_force_variant(const char* op, int variant) {
+    std::atomic<int>* slot = force_slot(op);
+    if (!slot) return SRA_ERR_ARG;
+    if (variant < -1 || variant >= variant_count(op)) return SRA_ERR_ARG;
+    slot->store(variant, std::memory_order_relaxed);
+    return SRA_OK;
+}
+
+int sra_variant_count(const char* op) { return variant_count(op); }
+
+const char* sra_variant_name(const char* op, int variant) {
+    static const char* const norm_names[] = {"warp_rows", "cta_row", "cta_smem", "two_pass"};
+    static const char* const rope_names[] = {"token_cta"};
+    static const char* const glu_names[] = {"cols_rows"};
+    const int n = variant_count(op);
+    if (n < 0 || variant < 0 || variant >= n) return nullptr;
+    if (std::strcmp(op, "rmsnorm") == 0) return norm_names[variant];
+    if (std::strcmp(op, "rope_kv_store") == 0) return rope_names[variant];
+    return glu_names[variant];
+}
+
+int sra_pick_variant(const char* op, int64_t a, int64_t b, int64_t c, int64_t d, int dtype, int num_sms) {
+    if (!valid_dtype(dtype) || variant_count(op) < 0) return SRA_ERR_ARG;
+    int dev = 0;
+    if (num_sms <= 0) {
+        num_sms = current_sm_count(&dev);
+        if (num_sms <= 0) return SRA_ERR_DEVICE;
+    }
+    const int es = elem_bytes(dtype);
+    if (std::strcmp(op, "rmsnorm") == 0) {
+        if (a < 0 || b <= 0) return SRA_ERR_SHAPE;
+        NormPlan p;
+        const int st = plan_norm(a, b, dtype, 16 / es, num_sms, 227 * 1024, &p);
+        return st == SRA_OK ? p.variant : st;
+    }
+    if (std::strcmp(op, "rope_kv_store") == 0) {
+        if (a < 0 || b <= 0 || c <= 0 || d <= 0 || d % 2) return SRA_ERR_SHAPE;
+        RopePlan p;
+        const int st = plan_rope(a, static_cast<int>(b), static_cast<int>(c), static_cast<int>(d), 1, num_sms, &p);
+        return st == SRA_OK ? p.variant : st;
+    }
+    if (a < 0 || b <= 0) return SRA_ERR_SHAPE;
+    GluPlan p;
+    const int st = plan_glu(a, b, 16 / es, num_sms, &p);
+    return st == SRA_OK ? p.variant : st;
+}
+
+}  // extern "C"

@@ -1,0 +1,179 @@
+// Device helpers shared by the kernels: element formats, vector accesses,
+// reductions. Internal to the library (not part of the C ABI).
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+#include <string.h>
+
+namespace sra {
+
+// ---------------------------------------------------------------------------
+// Element formats: widen to fp32, narrow with round-to-nearest-even.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__half v) { return __half2float(v); }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __half from_f32<__half>(float v) { return __float2half_rn(v); }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// Round an fp32 value to T and back (the value a T store would hold).
+template <typename T> __device__ __forceinline__ float round_trip(float v) {
+    return to_f32(from_f32<T>(v));
+}
+
+// ---------------------------------------------------------------------------
+// Vector accesses of VEC elements (VEC * sizeof(T) in {2, 4, 8, 16} bytes).
+// ---------------------------------------------------------------------------
+template <int BYTES> struct RawOf;
+template <> struct RawOf<16> { using type = uint4; };
+template <> struct RawOf<8> { using type = uint2; };
+template <> struct RawOf<4> { using type = unsigned int; };
+template <> struct RawOf<2> { using type = unsigned short; };
+
+// 32-bit words of a raw vector.
+__device__ __forceinline__ uint32_t word(const uint4& r, int i) {
+    return i == 0 ? r.x : (i == 1 ? r.y : (i == 2 ? r.z : r.w));
+}
+__device__ __forceinline__ uint32_t word(const uint2& r, int i) { return i == 0 ? r.x : r.y; }
+__device__ __forceinline__ uint32_t word(const unsigned int& r, int) { return r; }
+__device__ __forceinline__ void set_word(uint4& r, int i, uint32_t v) {
+    if (i == 0) r.x = v; else if (i == 1) r.y = v; else if (i == 2) r.z = v; else r.w = v;
+}
+__device__ __forceinline__ void set_word(uint2& r, int i, uint32_t v) { if (i == 0) r.x = v; else r.y = v; }
+__device__ __forceinline__ void set_word(unsigned int& r, int, uint32_t v) { r = v; }
+
+// Per-format conversion of packed words (4 bytes) and 16-bit patterns.
+template <typename T> struct Elem;
+template <> struct Elem<float> {
+    __device__ __forceinline__ static void unpack_word(uint32_t w, float* f) { f[0] = __uint_as_float(w); }
+    __device__ __forceinline__ static uint32_t pack_word(const float* f) { return __float_as_uint(f[0]); }
+    __device__ __forceinline__ static float from_bits16(unsigned short) { return 0.0f; }  // unused
+    __device__ __forceinline__ static unsigned short to_bits16(float) { return 0; }      // unused
+};
+template <> struct Elem<__nv_bfloat16> {
+    __device__ __forceinline__ static void unpack_word(uint32_t w, float* f) {
+        f[0] = __uint_as_float(w << 16);
+        f[1] = __uint_as_float(w & 0xffff0000u);
+    }
+    __device__ __forceinline__ static uint32_t pack_word(const float* f) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(f[0], f[1]);  // RNE, .x = low half
+        uint32_t w;
+        memcpy(&w, &h, 4);
+        return w;
+    }
+    __device__ __forceinline__ static float from_bits16(unsigned short b) {
+        return __uint_as_float(static_cast<uint32_t>(b) << 16);
+    }
+    __device__ __forceinline__ static unsigned short to_bits16(float f) {
+        return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+    }
+};
+template <> struct Elem<__half> {
+    __device__ __forceinline__ static void unpack_word(uint32_t w, float* f) {
+        __half2 h;
+        memcpy(&h, &w, 4);
+        const float2 v = __half22float2(h);
+        f[0] = v.x;
+        f[1] = v.y;
+    }
+    __device__ __forceinline__ static uint32_t pack_word(const float* f) {
+        __half2 h = __floats2half2_rn(f[0], f[1]);
+        uint32_t w;
+        memcpy(&w, &h, 4);
+        return w;
+    }
+    __device__ __forceinline__ static float from_bits16(unsigned short b) {
+        return __half2float(__ushort_as_half(b));
+    }
+    __device__ __forceinline__ static unsigned short to_bits16(float f) {
+        return __half_as_ushort(__float2half_rn(f));
+    }
+};
+
+template <typename T, int VEC>
+struct Vec {
+    static constexpr int BYTES = VEC * int(sizeof(T));
+    using Raw = typename RawOf<BYTES>::type;
+
+    // Plain load (cached in L1 / L2).
+    __device__ __forceinline__ static Raw load(const T* p) { return *reinterpret_cast<const Raw*>(p); }
+    // Read-only streaming load: each byte is read once; evict first.
+    __device__ __forceinline__ static Raw load_stream(const T* p) {
+        return ldcs(reinterpret_cast<const Raw*>(p));
+    }
+    __device__ __forceinline__ static void store(T* p, Raw r) { *reinterpret_cast<Raw*>(p) = r; }
+    __device__ __forceinline__ static void store_stream(T* p, Raw r) {
+        stcs(reinterpret_cast<Raw*>(p), r);
+    }
+
+    __device__ __forceinline__ static void unpack(const Raw& r, float (&f)[VEC]) {
+        if constexpr (BYTES == 2) {
+            f[0] = Elem<T>::from_bits16(r);
+        } else {
+            constexpr int W = BYTES / 4, PER = 4 / int(sizeof(T));
+#pragma unroll
+            for (int i = 0; i < W; ++i) Elem<T>::unpack_word(word(r, i), f + i * PER);
+        }
+    }
+    __device__ __forceinline__ static Raw pack(const float (&f)[VEC]) {
+        Raw r;
+        if constexpr (BYTES == 2) {
+            r = Elem<T>::to_bits16(f[0]);
+        } else {
+            constexpr int W = BYTES / 4, PER = 4 / int(sizeof(T));
+#pragma unroll
+            for (int i = 0; i < W; ++i) set_word(r, i, Elem<T>::pack_word(f + i * PER));
+        }
+        return r;
+    }
+
+  private:
+    __device__ __forceinline__ static uint4 ldcs(const uint4* p) { return __ldcs(p); }
+    __device__ __forceinline__ static uint2 ldcs(const uint2* p) { return __ldcs(p); }
+    __device__ __forceinline__ static unsigned int ldcs(const unsigned int* p) { return __ldcs(p); }
+    __device__ __forceinline__ static unsigned short ldcs(const unsigned short* p) { return __ldcs(p); }
+    __device__ __forceinline__ static void stcs(uint4* p, uint4 v) { __stcs(p, v); }
+    __device__ __forceinline__ static void stcs(uint2* p, uint2 v) { __stcs(p, v); }
+    __device__ __forceinline__ static void stcs(unsigned int* p, unsigned int v) { __stcs(p, v); }
+    __device__ __forceinline__ static void stcs(unsigned short* p, unsigned short v) { __stcs(p, v); }
+};
+
+// Elements per 16-byte access.
+template <typename T> constexpr int vec16() { return 16 / int(sizeof(T)); }
+
+// ---------------------------------------------------------------------------
+// Reductions
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+// Sum over the whole CTA; every thread gets the total. `scratch` holds >= 33 floats
+// of shared memory. blockDim.x must be a multiple of 32.
+__device__ __forceinline__ float block_sum(float v, float* scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    v = warp_sum(v);
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        float s = lane < nwarps ? scratch[lane] : 0.0f;
+        s = warp_sum(s);
+        if (lane == 0) scratch[32] = s;
+    }
+    __syncthreads();
+    float total = scratch[32];
+    __syncthreads();  // scratch may be reused by the next row
+    return total;
+}
+
+}  // namespace sra

@@ -1,0 +1,14 @@
+// Residual-add + RMSNorm launchers (the ADD = true half of the family in norm_impl.cuh).
+#include "norm_impl.cuh"
+
+namespace sra {
+
+cudaError_t launch_add_rmsnorm(const NormArgs& a, const NormPlan& p, int dtype, cudaStream_t s) {
+    return norm::launch<true>(a, p, dtype, s);
+}
+
+cudaError_t norm_smem_prepare(int dtype, bool add, int vec, size_t bytes) {
+    return add ? norm::smem_prepare<true>(dtype, vec, bytes) : norm::smem_prepare<false>(dtype, vec, bytes);
+}
+
+}  // namespace sra

@@ -1,0 +1,10 @@
+// RMSNorm launchers (the ADD = false half of the family in norm_impl.cuh).
+#include "norm_impl.cuh"
+
+namespace sra {
+
+cudaError_t launch_rmsnorm(const NormArgs& a, const NormPlan& p, int dtype, cudaStream_t s) {
+    return norm::launch<false>(a, p, dtype, s);
+}
+
+}  // namespace sra

@@ -1,0 +1,146 @@
+// Fused neox RoPE + paged KV-cache store.
+//
+// koas-w.github.io "preformanceimprovement", section 1: Q, K, V, cos and sin
+// are read once; Q and K are rotated in registers; Q is written back in place;
+// K_rot and V go straight into the paged cache through slot_mapping, with no
+// temporary tensors. GQA is handled inside the kernel (each KV head is written
+// once per token; kv_head = head / (n_head / n_kv_head) is the read-side map).
+// Cache layout [2, num_blocks, block_size, n_kv_head, head_dim] (mer.dev
+// "AsyncT vllm 适配加速笔记（一）", section 1.1).
+//
+// Work decomposition: a token's work is U = (n_head + 2 * n_kv_head) * (h / P)
+// tasks of P rotation pairs each (h = head_dim / 2; P = 16 bytes of elements, or
+// 1). Task u of a token is fixed per thread (thread u of the CTA), so a thread
+// decodes its head and offset once; CTAs stride over tokens. With Qwen2.5-1.5B
+// shapes (12 Q + 2 K + 2 V heads, head_dim 128, bf16) a token is exactly 128
+// tasks: one 128-thread CTA per token, every access 16 bytes, a warp's
+// accesses to one head row fully coalesced.
+//
+// The rotation y = x_lo * c - x_hi * s (and x_hi * c + x_lo * s) is evaluated
+// with Kahan's fma-based difference of products, so its fp32 error is a few
+// ulps of the RESULT even under cancellation; one RNE to the dtype follows.
+#include "common.cuh"
+#include "internal.h"
+
+namespace sra {
+namespace rope {
+
+// a * b - c * d, accurate to a few ulps of the result (W. Kahan).
+__device__ __forceinline__ float diff_of_products(float a, float b, float c, float d) {
+    const float w = c * d;
+    const float e = fmaf(-c, d, w);  // w - c * d, exactly
+    const float f = fmaf(a, b, -w);
+    return f + e;
+}
+
+template <typename T, int P>
+__global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
+    using V = Vec<T, P>;
+    using R = typename V::Raw;
+    using C = Vec<float, (P >= 4 ? 4 : 1)>;  // cos / sin accesses
+    constexpr int CW = P >= 4 ? 4 : 1;
+
+    const int h = a.head_dim >> 1;
+    const int per_head = h / P;
+    const int n_units = a.n_head + 2 * a.n_kv;
+    const int U = n_units * per_head;
+    const int64_t capacity = a.num_blocks * static_cast<int64_t>(a.block_size);
+
+    for (int u = threadIdx.x; u < U; u += blockDim.x) {
+        const int unit = u / per_head;
+        const int i0 = (u - unit * per_head) * P;
+        // 0: Q head, 1: K head, 2: V head
+        const int kind = unit < a.n_head ? 0 : (unit < a.n_head + a.n_kv ? 1 : 2);
+        const int head = kind == 0 ? unit : (kind == 1 ? unit - a.n_head : unit - a.n_head - a.n_kv);
+
+        for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
+            const int64_t p = a.pos[t];
+            const bool pos_ok = p >= 0 && p < a.max_pos;
+            int64_t slot = -1;
+            if (kind != 0 || u == 0) slot = a.slot[t];
+            const bool slot_in_range = slot < capacity;
+
+            if (u == 0 && a.err != nullptr) {
+                const int bad = (pos_ok ? 0 : 1) + ((slot >= 0 && !slot_in_range) ? 1 : 0);
+                if (bad) atomicAdd(a.err, bad);
+            }
+            if (!pos_ok) continue;                       // q[t] unchanged, nothing cached
+            if (kind != 0 && (slot < 0 || !slot_in_range)) continue;  // padding / bad slot
+
+            const T* src;
+            T* dst;
+            if (kind == 0) {
+                T* qh = static_cast<T*>(a.q) + t * a.qs + static_cast<int64_t>(head) * a.head_dim;
+                src = qh;
+                dst = qh;
+            } else {
+                const int64_t blk = slot / a.block_size;
+                const int64_t off = slot - blk * a.block_size;
+                const int plane = kind == 1 ? 0 : 1;
+                dst = static_cast<T*>(a.cache) +
+                      (((plane * a.num_blocks + blk) * a.block_size + off) * a.n_kv + head) *
+                          static_cast<int64_t>(a.head_dim);
+                src = kind == 1 ? static_cast<const T*>(a.k) + t * a.ks + static_cast<int64_t>(head) * a.head_dim
+                                : static_cast<const T*>(a.v) + t * a.vs + static_cast<int64_t>(head) * a.head_dim;
+            }
+            const R lo_r = V::load(src + i0);
+            const R hi_r = V::load(src + h + i0);
+            if (kind == 2) {  // V: bit copy
+                V::store(dst + i0, lo_r);
+                V::store(dst + h + i0, hi_r);
+                continue;
+            }
+            float c[P], s[P];
+            const float* crow = a.cos + p * h + i0;
+            const float* srow = a.sin + p * h + i0;
+#pragma unroll
+            for (int j = 0; j < P; j += CW) {
+                float cf[CW], sf[CW];
+                C::unpack(C::load(crow + j), cf);
+                C::unpack(C::load(srow + j), sf);
+#pragma unroll
+                for (int q = 0; q < CW; ++q) {
+                    c[j + q] = cf[q];
+                    s[j + q] = sf[q];
+                }
+            }
+            float lo[P], hi[P], ylo[P], yhi[P];
+            V::unpack(lo_r, lo);
+            V::unpack(hi_r, hi);
+#pragma unroll
+            for (int j = 0; j < P; ++j) {
+                ylo[j] = diff_of_products(lo[j], c[j], hi[j], s[j]);
+                yhi[j] = diff_of_products(hi[j], c[j], -lo[j], s[j]);
+            }
+            V::store(dst + i0, V::pack(ylo));
+            V::store(dst + h + i0, V::pack(yhi));
+        }
+    }
+}
+
+template <typename T>
+cudaError_t launch_typed(const RopeArgs& a, const RopePlan& p, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>(p.grid)), block(p.threads);
+    if (p.pairs == vec16<T>()) {
+        token_cta_kernel<T, vec16<T>()><<<grid, block, 0, s>>>(a);
+    } else if (p.pairs == 1) {
+        token_cta_kernel<T, 1><<<grid, block, 0, s>>>(a);
+    } else {
+        return cudaErrorInvalidValue;
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace rope
+
+cudaError_t launch_rope_kv_store(const RopeArgs& a, const RopePlan& p, int dtype, cudaStream_t s) {
+    if (p.variant != ROPE_TOKEN_CTA) return cudaErrorInvalidValue;
+    switch (dtype) {
+        case DT_F32: return rope::launch_typed<float>(a, p, s);
+        case DT_F16: return rope::launch_typed<__half>(a, p, s);
+        case DT_BF16: return rope::launch_typed<__nv_bfloat16>(a, p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace sra

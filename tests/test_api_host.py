@@ -1,0 +1,166 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+The library must load, export every function include/sra.h declares, and
+reject every invalid argument with its status code before making any CUDA
+call. Fake addresses are only ever passed together with an argument that is
+invalid, so no call here can reach a kernel launch even on a GPU machine.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import swiglu_rmsnorm_add_gb300 as sra
+from swiglu_rmsnorm_add_gb300 import build as sra_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sra.h")
+
+OK, NULL, SHAPE, STRIDE, DTYPE, ALIAS, ARG, VARIANT = 0, -1, -2, -3, -4, -5, -6, -7
+BF16, F16, F32 = 2, 1, 0
+P = 0x10000  # a fake, never dereferenced device address
+
+
+@pytest.fixture(scope="module")
+def L():
+    sra_build.build()
+    return sra.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"SRA_API\s+[\w\s\*]*?\b(sra_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_api():
+    names = declared_functions()
+    for n in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_glu", "sra_swiglu"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    # and nothing else (the static CUDA runtime stays hidden)
+    import subprocess
+
+    out = subprocess.run(["nm", "-D", "--defined-only", sra_build.LIB], capture_output=True, text=True).stdout
+    exported = sorted(line.split()[-1] for line in out.splitlines() if line.strip())
+    assert exported == declared_functions()
+
+
+def test_version_and_strings(L):
+    assert L.sra_version() == 1
+    for code in range(-9, 1):
+        assert sra.status_string(code)
+    assert sra.status_string(-1234) == "unknown status"
+
+
+def test_rmsnorm_validation(L):
+    f = L.sra_rmsnorm
+    assert f(P, P, P + 4096, 4, 16, 16, 16, 1e-6, 7, None) == DTYPE
+    assert f(P, P, P + 4096, -1, 16, 16, 16, 1e-6, BF16, None) == SHAPE
+    assert f(P, P, P + 4096, 4, 0, 16, 16, 1e-6, BF16, None) == SHAPE
+    assert f(P, P, P + 4096, 4, 16, 15, 16, 1e-6, BF16, None) == STRIDE
+    assert f(P, P, P + 4096, 4, 16, 16, 8, 1e-6, BF16, None) == STRIDE
+    assert f(P, P, P + 4096, 4, 16, 16, 16, -1.0, BF16, None) == ARG
+    assert f(P, P, P + 4096, 4, 16, 16, 16, float("nan"), BF16, None) == ARG
+    assert f(None, P, P + 4096, 4, 16, 16, 16, 1e-6, BF16, None) == NULL
+    assert f(P, None, P + 4096, 4, 16, 16, 16, 1e-6, BF16, None) == NULL
+    assert f(P, P + 8192, None, 4, 16, 16, 16, 1e-6, BF16, None) == NULL
+    # zero rows: a valid no-op, even with NULL pointers
+    assert f(None, None, None, 0, 16, 16, 16, 1e-6, BF16, None) == OK
+    # out overlapping x without being x, and out overlapping w
+    assert f(P, P + 8192, P + 2, 4, 16, 16, 16, 1e-6, BF16, None) == ALIAS
+    assert f(P, P + 4096, P + 4096 + 16, 4, 16, 16, 16, 1e-6, BF16, None) == ALIAS
+    # in place with a different stride is not the same view
+    assert f(P, P + 8192, P, 4, 16, 16, 32, 1e-6, BF16, None) == ALIAS
+
+
+def test_add_rmsnorm_validation(L):
+    f = L.sra_add_rmsnorm
+    X, R, W, O = P, P + 4096, P + 8192, P + 12288
+    assert f(X, None, W, O, 4, 16, 16, 16, 16, 1e-6, BF16, None) == NULL
+    assert f(X, R, W, O, 4, 16, 16, 8, 16, 1e-6, BF16, None) == STRIDE
+    assert f(X, R, W, X, 4, 16, 16, 16, 16, 1e-6, BF16, None) == ALIAS       # out == x forbidden
+    assert f(X, R, W, R, 4, 16, 16, 16, 16, 1e-6, BF16, None) == ALIAS       # out == res
+    assert f(X, R, W, W, 4, 16, 16, 16, 16, 1e-6, BF16, None) == ALIAS       # out == w
+    assert f(X, X + 2, W, O, 4, 16, 16, 16, 16, 1e-6, BF16, None) == ALIAS   # res overlaps x
+    assert f(X, R, W, O, 0, 16, 16, 16, 16, 1e-6, BF16, None) == OK
+
+
+def test_rope_validation(L):
+    f = L.sra_rope_kv_store
+    Q, K, V, C, S, PO, SL, KV = (P + i * 0x100000 for i in range(8))
+
+    def call(**kw):
+        a = dict(q=Q, k=K, v=V, cos=C, sin=S, pos=PO, slot=SL, cache=KV, T=4, nh=12, nkv=2, hd=128,
+                 qs=1536, ks=256, vs=256, max_pos=32768, nb=16, bs=16, err=None, dt=BF16)
+        a.update(kw)
+        return f(a["q"], a["k"], a["v"], a["cos"], a["sin"], a["pos"], a["slot"], a["cache"], a["T"], a["nh"],
+                 a["nkv"], a["hd"], a["qs"], a["ks"], a["vs"], a["max_pos"], a["nb"], a["bs"], a["err"],
+                 a["dt"], None)
+
+    assert call(dt=3) == DTYPE
+    assert call(T=-1) == SHAPE
+    assert call(nh=12, nkv=5) == SHAPE
+    assert call(hd=127, qs=12 * 127, ks=2 * 127, vs=2 * 127) == SHAPE
+    assert call(bs=0) == SHAPE
+    assert call(nb=-1) == SHAPE
+    assert call(max_pos=-5) == SHAPE
+    assert call(qs=1535) == STRIDE
+    assert call(ks=255) == STRIDE
+    assert call(vs=100) == STRIDE
+    for name in ("q", "k", "v", "cos", "sin", "pos", "slot", "cache"):
+        assert call(**{name: None}) == NULL, name
+    assert call(T=0) == OK
+    assert call(k=Q + 64) == ALIAS                 # q overlaps k
+    assert call(cache=V + 2) == ALIAS              # cache overlaps v
+
+
+def test_glu_validation(L):
+    f = L.sra_glu
+    assert f(P, P + 0x100000, 4, 8, 16, 8, 0, 9, None) == DTYPE
+    assert f(P, P + 0x100000, 4, 8, 16, 8, 2, BF16, None) == ARG
+    assert f(P, P + 0x100000, -1, 8, 16, 8, 0, BF16, None) == SHAPE
+    assert f(P, P + 0x100000, 4, 0, 16, 8, 0, BF16, None) == SHAPE
+    assert f(P, P + 0x100000, 4, 8, 15, 8, 0, BF16, None) == STRIDE
+    assert f(P, P + 0x100000, 4, 8, 16, 7, 0, BF16, None) == STRIDE
+    assert f(None, P + 0x100000, 4, 8, 16, 8, 0, BF16, None) == NULL
+    assert f(P, P + 8, 4, 8, 16, 8, 0, BF16, None) == ALIAS
+    assert f(None, None, 0, 8, 16, 8, 1, BF16, None) == OK
+    assert L.sra_swiglu(P, P + 8, 4, 8, 16, 8, BF16, None) == ALIAS
+
+
+def test_variant_control(L):
+    assert sra.variant_count("rmsnorm") == 4
+    assert sra.variant_count("rope_kv_store") == 1
+    assert sra.variant_count("glu") == 1
+    assert sra.variant_count("nope") == ARG
+    assert [sra.variant_name("rmsnorm", i) for i in range(4)] == ["warp_rows", "cta_row", "cta_smem", "two_pass"]
+    assert sra.variant_name("rmsnorm", 4) is None
+    assert L.sra_force_variant(b"rmsnorm", 4) == ARG
+    assert L.sra_force_variant(b"bogus", 0) == ARG
+    assert L.sra_force_variant(b"rmsnorm", 2) == OK
+    assert sra.pick_variant("rmsnorm", 512, 1536, num_sms=152) == 2
+    assert L.sra_force_variant(b"rmsnorm", -1) == OK
+
+
+def test_dispatch_choices(L):
+    import torch
+
+    pick = sra.pick_variant
+    # short rows, many of them: one warp per row
+    assert pick("rmsnorm", 4096, 1536, dtype=torch.bfloat16, num_sms=152) == 0
+    # decode (few rows) of the 1536-wide hidden state: a CTA per row
+    assert pick("rmsnorm", 1, 1536, dtype=torch.bfloat16, num_sms=152) == 1
+    # a row past a warp's registers: CTA per row
+    assert pick("rmsnorm", 512, 8192, dtype=torch.float32, num_sms=152) == 1
+    # past the registers of a CTA: staged in shared memory
+    assert pick("rmsnorm", 64, 40000, dtype=torch.bfloat16, num_sms=152) == 2
+    # past shared memory: two-pass
+    assert pick("rmsnorm", 2, 10_000_000, dtype=torch.float32, num_sms=152) == 3
+    assert pick("glu", 4096, 14336, num_sms=152) == 0
+    assert pick("rope_kv_store", 2048, 12, 2, 128, num_sms=152) == 0
+    assert pick("rmsnorm", -1, 16, num_sms=152) == SHAPE

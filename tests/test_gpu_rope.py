@@ -1,0 +1,137 @@
+"""GPU parity: fused neox RoPE + paged KV-cache store vs the oracle.
+
+Workload: Qwen2.5-1.5B GQA (12 Q / 2 KV heads, head_dim 128, bf16), T in
+{1, 64, 2048}, positions uniform in [0, 32768), theta 1e6 tables, a
+[2, 4096, 16, 2, 128] cache prefilled with the 0xDEAD sentinel and distinct
+slots (koas-w.github.io "preformanceimprovement" section 1; cache layout of
+mer.dev "AsyncT vllm 适配加速笔记（一）" section 1.1).
+Q and K within 1 ulp; V copies, slot placement and every untouched cache byte
+bit-exact; error counts exact.
+"""
+import pytest
+import torch
+
+import oracle
+import swiglu_rmsnorm_add_gb300 as sra
+from swiglu_rmsnorm_add_gb300 import synthetic as syn
+from tests.parity import assert_bits_equal, assert_close, assert_values_equal
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+def run_both(inp, max_pos=None, expect_err=None):
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sra.rope_kv_store(d["q"], d["k"], d["v"], d["cos"], d["sin"], d["pos"], d["slot_mapping"], d["kv_cache"],
+                      err_count=err, max_pos=max_pos)
+    torch.cuda.synchronize()
+    n = oracle.rope_kv_store(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], inp["pos"],
+                             inp["slot_mapping"], inp["kv_cache"], max_pos=max_pos)
+    assert int(err.item()) == n
+    if expect_err is not None:
+        assert n == expect_err
+    return d
+
+
+def check(d, inp, what):
+    cache_g, cache_o = d["kv_cache"].cpu(), inp["kv_cache"]
+    assert_close(d["q"], inp["q"], f"{what}: q")
+    assert_close(cache_g[0], cache_o[0], f"{what}: K plane")
+    assert_bits_equal(cache_g[1], cache_o[1], f"{what}: V plane")
+    # placement: the set of slots whose K-plane bytes changed is the same on both
+    sent = syn.sentinel_cache(cache_o.shape[1:], cache_o.dtype)
+    iv = torch.int32 if cache_o.element_size() == 4 else torch.int16
+    touched_g = (cache_g[0].view(iv) != sent.view(iv)).flatten(2).any(-1)
+    touched_o = (cache_o[0].view(iv) != sent.view(iv)).flatten(2).any(-1)
+    assert torch.equal(touched_g, touched_o), f"{what}: slot placement"
+
+
+@pytest.mark.parametrize("T", syn.ROPE_T)
+def test_config_qwen25(T):
+    tables = syn.rope_tables(32768, 128, 1e6)
+    inp = syn.rope_inputs(T, 1002, tables=tables)
+    d = run_both(inp, expect_err=0)
+    check(d, inp, f"T={T}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("n_head,n_kv,hd", [(12, 2, 128), (8, 8, 64), (16, 1, 256), (4, 2, 32), (6, 3, 10)])
+def test_head_layouts_and_dtypes(dtype, n_head, n_kv, hd):
+    tables = syn.rope_tables(4096, hd, 1e4)
+    inp = syn.rope_inputs(37, 20, n_head=n_head, n_kv_head=n_kv, head_dim=hd, num_blocks=8, block_size=16,
+                          max_pos=4096, dtype=dtype, tables=tables)
+    d = run_both(inp)
+    check(d, inp, f"{n_head}/{n_kv}/{hd} {dtype}")
+
+
+def test_position_zero_identity_and_ninety_degrees():
+    inp = syn.rope_inputs(16, 21, num_blocks=4)
+    inp["pos"].zero_()
+    q0 = inp["q"].clone()
+    d = run_both(inp)
+    assert_values_equal(d["q"], q0, "pos 0 is the identity")
+    inp = syn.rope_inputs(16, 22, num_blocks=4)
+    cos = torch.zeros(32768, 64)
+    sin = torch.ones(32768, 64)
+    inp["cos"], inp["sin"] = cos, sin
+    q0 = inp["q"].clone()
+    d = run_both(inp)
+    assert_values_equal(d["q"][..., :64], -q0[..., 64:], "90 degrees, first half")
+    assert_values_equal(d["q"][..., 64:], q0[..., :64], "90 degrees, second half")
+
+
+def test_padding_bad_slots_and_positions():
+    inp = syn.rope_inputs(8, 23, num_blocks=4)   # 64 slots
+    inp["slot_mapping"] = torch.tensor([-1, 3, 64, 5, 1000, 7, -1, 9], dtype=torch.int64)
+    inp["pos"] = torch.tensor([1, 2, 3, -4, 5, 32768, 7, 8], dtype=torch.int64)
+    # errors: slot 64 and 1000 out of range (2), positions -4 and 32768 (2)
+    d = run_both(inp, expect_err=4)
+    check(d, inp, "padding / errors")
+
+
+def test_fused_qkv_views_and_misaligned_scalar_path():
+    T, nh, nkv, hd = 40, 12, 2, 128
+    W = (nh + 2 * nkv) * hd
+    qkv = syn.normal((T, W + 8), 0, 1, torch.bfloat16, 24, 1)   # padded rows
+    tables = syn.rope_tables(32768, hd, 1e6)
+    pos = syn.positions(T, 32768, 24, 2)
+    slot = syn.slots(T, 64 * 16, 24, 3)
+    for off in (0, 1):   # off = 1: every row 2-byte aligned -> scalar path
+        base = syn.normal((T * (W + 8) + 1,), 0, 1, torch.bfloat16, 24, 4)
+        buf = base[off:off + T * (W + 8)].view(T, W + 8)
+        q = buf[:, :nh * hd].view(T, nh, hd)
+        k = buf[:, nh * hd:(nh + nkv) * hd].view(T, nkv, hd)
+        v = buf[:, (nh + nkv) * hd:W].view(T, nkv, hd)
+        cache = syn.sentinel_cache((2, 64, 16, nkv, hd))
+        inp = dict(q=q.contiguous(), k=k.contiguous(), v=v.contiguous(), cos=tables[0], sin=tables[1], pos=pos,
+                   slot_mapping=slot, kv_cache=cache)
+        bd = base.to(DEV)
+        bufd = bd[off:off + T * (W + 8)].view(T, W + 8)
+        dq = bufd[:, :nh * hd].view(T, nh, hd)
+        dk = bufd[:, nh * hd:(nh + nkv) * hd].view(T, nkv, hd)
+        dv = bufd[:, (nh + nkv) * hd:W].view(T, nkv, hd)
+        dc = cache.to(DEV)
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        sra.rope_kv_store(dq, dk, dv, tables[0].to(DEV), tables[1].to(DEV), pos.to(DEV), slot.to(DEV), dc,
+                          err_count=err)
+        oracle.rope_kv_store(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], pos, slot, cache)
+        assert_close(dq, inp["q"], f"fused view q off={off}")
+        assert_close(dc.cpu()[0], cache[0], "K")
+        assert_bits_equal(dc.cpu()[1], cache[1], "V")
+        # k, v and the row padding are untouched
+        after = bufd.cpu()
+        assert_bits_equal(after[:, nh * hd:], buf[:, nh * hd:], "k, v, padding untouched")
+
+
+def test_duplicate_free_large_T_cache_untouched_elsewhere():
+    inp = syn.rope_inputs(2048, 25)
+    d = run_both(inp, expect_err=0)
+    check(d, inp, "T=2048 full cache")
+
+
+def test_zero_tokens():
+    inp = syn.rope_inputs(0, 26, num_blocks=2)
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    sra.rope_kv_store(d["q"], d["k"], d["v"], d["cos"], d["sin"], d["pos"], d["slot_mapping"], d["kv_cache"])
+    assert_bits_equal(d["kv_cache"], inp["kv_cache"], "no-op")
