@@ -11,14 +11,20 @@ One step = one pass of the whole hot path at its configured shapes:
                   batch 1 and 64 (Qwen2.5-1.5B shapes), each replayed from a CUDA graph
                   (2 x 112 launches)
 Every input is synthetic and seeded, resident in HBM before timing. L2 is
-flushed (a 256 MiB write) before every step. Each step is queued behind a
-short device-side delay so the host has enqueued the whole step before the
-GPU starts it; the timed region is the step alone (CUDA events on the
-launching stream). `value` = algorithmic bytes of the step / device time of
-the step, summed over ranks (each rank runs its own replica: weak scaling).
+flushed before every step (a 256 MiB write, then a read, so no dirty lines are
+left to write back inside the step). Each step is queued behind a short
+device-side delay so the host has enqueued the whole step before the GPU starts
+it; the timed region is the step alone (CUDA events on the launching stream),
+with one more event pair around the dominant kernel (the largest stream).
+Kernels are launched with programmatic dependent launch (--no-pdl turns it
+off). `value` = algorithmic bytes of the step / device time of the step, summed
+over ranks (each rank runs its own replica: weak scaling).
 
-Also measured: per-kernel GB/s and fraction of the measured HBM peak, rows/s
-at decode batch, row-scaled companion shapes (>= 256 MB of traffic), an
+Also measured, per kernel: the time of one launch alone (clean L2, one event
+pair: includes the event overhead) and the streaming rate (back-to-back
+launches over rotating copies of its buffers that exceed 4x L2, so every launch
+reads cold data) with its GB/s and fraction of the measured HBM peak; rows/s
+at decode batch; the launch latency of the smallest launches; row-scaled companion shapes (>= 256 MB of traffic), an
 end-to-end number through the same C ABI from pinned host buffers, and the CPU
 oracle on a bounded sample of the same step (rank 0, one GPU only).
 
@@ -27,7 +33,6 @@ oracle on a bounded sample of the same step (rank 0, one GPU only).
 from __future__ import annotations
 
 import argparse
-import ctypes
 import hashlib
 import json
 import os
@@ -44,6 +49,7 @@ METRIC = "achieved HBM GB/s and % of GB300 peak per kernel; rows/s at decode bat
 UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
+STREAM_BYTES = 512 << 20   # per-kernel streaming measurement: total bytes over the rotating copies
 WORKLOAD = ("decoder per-token hot path at the configured shapes: rmsnorm 512xD sweep (8 widths x fp32/fp16/bf16), "
             "add_rmsnorm bf16 Tx1536 T={1,16,256,4096}, rope_kv_store Qwen2.5-1.5B GQA T={1,64,2048}, "
             "swiglu+reglu Llama-3-8B gate_up T={1,64,512,4096}, 28-layer decode chain B={1,64}")
@@ -60,6 +66,7 @@ def parse():
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-companions", action="store_true")
+    p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-baseline duration")
     return p.parse_args()
 
@@ -80,6 +87,38 @@ class Entry:
         st = self.fn(*self.args)
         if st != 0:
             raise RuntimeError(f"{self.name}: status {st}")
+
+    def tensors(self):
+        k = self.keep
+        if isinstance(k, dict):
+            return list(k.values())
+        if isinstance(k, (list, tuple)):
+            return list(k)
+        return [k]
+
+    def replicas(self, n):
+        """n launch closures, each on its own device copy of every buffer the launch touches."""
+        import torch
+
+        out = []
+        for _ in range(n):
+            remap, hold = {}, []
+            for t in self.tensors():
+                c = torch.empty_like(t)
+                c.copy_(t)
+                remap[t.data_ptr()] = c.data_ptr()
+                hold.append(c)
+            args = tuple(remap.get(a, a) if isinstance(a, int) and not isinstance(a, bool) else a
+                         for a in self.args)
+            fn = self.fn
+
+            def call(args=args, hold=hold):
+                st = fn(*args)
+                if st != 0:
+                    raise RuntimeError(f"{self.name}: status {st}")
+
+            out.append(call)
+        return out
 
 
 def build_entries(dev, stream_handle, only=(), companions=False):
@@ -159,13 +198,12 @@ def build_entries(dev, stream_handle, only=(), companions=False):
             out = torch.empty(T, I, dtype=torch.bfloat16, device=dev)
             entries.append(Entry(name, an, T * (2 * I * 2 + I * 2), T, L.sra_glu,
                                  (gu.data_ptr(), out.data_ptr(), T, I, 2 * I, I, act, 2, stream_handle),
-                                 [gu] if act == 0 else [], [out]))
-            entries[-1].keep = gu
+                                 [gu] if act == 0 else [], [out], keep=(gu, out)))
     return entries
 
 
 class ChainEntry:
-    def __init__(self, B, dev):
+    def __init__(self, B, dev, pdl=True):
         from swiglu_rmsnorm_add_gb300.chain import DecodeChain
 
         self.name = f"chain:bf16:B{B}x28"
@@ -173,7 +211,7 @@ class ChainEntry:
         self.B = B
         self.rows = B
         self.chain = DecodeChain(B, device=dev)
-        self.chain.capture()
+        self.chain.capture(pdl=pdl)
         self.bytes_by_kind = self.chain.bytes_per_step()
         self.bytes = sum(self.bytes_by_kind.values())
         self.times = []
@@ -370,8 +408,16 @@ def cpu_sample_run(target_seconds, threads=None, fraction=None):
 
 
 # --------------------------------------------------------------------------- main (GPU)
+def order_entries(entries):
+    """Step order: the largest streams first (GLU, then add_rmsnorm, RoPE, the RMSNorm sweep)."""
+    rank = {"swiglu": 0, "reglu": 0, "add_rmsnorm": 1, "rope_kv_store": 2, "rmsnorm": 3, "chain": 4}
+    return sorted(entries, key=lambda e: (rank[e.op], -e.bytes, e.name))
+
+
 def run_gpu(args):
     import torch
+
+    import swiglu_rmsnorm_add_gb300 as sra
 
     rank, world, local = dist_setup(args)
     dev = torch.device(f"cuda:{local}")
@@ -383,46 +429,56 @@ def run_gpu(args):
     stream = torch.cuda.current_stream(dev)
     sh = int(stream.cuda_stream)
     only = [o for o in args.only.split(",") if o]
+    pdl = not args.no_pdl
+    sra.set_pdl(pdl)
 
-    entries = build_entries(dev, sh, only)
+    entries = order_entries(build_entries(dev, sh, only))
     if not args.no_chain and (not only or any(o.startswith("chain") for o in only)):
         for B in (1, 64):
-            entries.append(ChainEntry(B, dev))
+            entries.append(ChainEntry(B, dev, pdl))
     assert entries, "nothing selected"
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     bytes_per_step = sum(e.bytes for e in entries)
     launches_per_step = sum(112 if e.op == "chain" else 1 for e in entries)
+    kern = [i for i, e in enumerate(entries) if e.op != "chain"] or list(range(len(entries)))
+    dom = max(kern, key=lambda i: (entries[i].bytes, entries[i].op == "swiglu"))
 
-    def enqueue_step(evs=None):
-        if evs is not None:
-            evs[0].record(stream)
+    def clean_l2():
+        # write a buffer larger than L2 (evicts everything), then read it back so
+        # the lines left in L2 are clean and no write-back lands in the timed step
+        flush.fill_(1)
+        flush.sum()
+
+    def enqueue_step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
         for i, e in enumerate(entries):
-            if evs is not None:
-                evs[1 + 2 * i].record(stream)
+            if ev is not None and i == dom:
+                ev[1].record(stream)
             e.launch()
-            if evs is not None:
-                evs[2 + 2 * i].record(stream)
-        if evs is not None:
-            evs[-1].record(stream)
+            if ev is not None and i == dom:
+                ev[2].record(stream)
+        if ev is not None:
+            ev[3].record(stream)
 
-    # calibrate the host enqueue time -> device delay that keeps the GPU behind the host
+    # host enqueue time of one step -> a device-side delay that keeps the GPU behind the host
     torch.cuda.synchronize()
-    tmp = [torch.cuda.Event(enable_timing=True) for _ in range(2 + 2 * len(entries))]
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     t0 = time.perf_counter()
-    enqueue_step(tmp)
+    enqueue_step(evs)
     host_s = time.perf_counter() - t0
     torch.cuda.synchronize()
     delay_cycles = int(min(2e7, max(2e5, 3.0 * host_s * 2.0e9)))
 
-    def step(evs=None):
-        flush.zero_()
+    def step(ev=None):
+        clean_l2()
         torch.cuda._sleep(delay_cycles)
-        enqueue_step(evs)
+        enqueue_step(ev)
 
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2 + 2 * len(entries))] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     try:
         gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
     except Exception:
@@ -431,8 +487,6 @@ def run_gpu(args):
     clocks.start()
     time.sleep(0.3)
     if world > 1:
-        import torch.distributed as dist
-
         dist.barrier()
     torch.cuda.synchronize()
     w0 = time.perf_counter()
@@ -445,9 +499,8 @@ def run_gpu(args):
     time.sleep(0.25)
     clk = clocks.stop()
 
-    step_ms = [ev[k][0].elapsed_time(ev[k][-1]) for k in range(args.steps)]
-    for i, e in enumerate(entries):
-        e.times = [ev[k][1 + 2 * i].elapsed_time(ev[k][2 + 2 * i]) for k in range(args.steps)]
+    step_ms = [ev[k][0].elapsed_time(ev[k][3]) for k in range(args.steps)]
+    dom_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
     ms = statistics.fmean(step_ms)
     if world > 1:
         t = torch.tensor([ms], dtype=torch.float64, device=dev)
@@ -456,49 +509,124 @@ def run_gpu(args):
     value = world * bytes_per_step / (ms / 1e3) / 1e9
 
     peak, peak_src = measured_peak()
+    de = entries[dom]
+    d_us = statistics.fmean(dom_ms) * 1e3
+    achieved = de.bytes / (d_us * 1e-6) / 1e9
+    roofline = {"bound": "hbm", "kernel": de.name, "achieved": round(achieved, 1), "peak": peak,
+                "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "traffic": kernel_traffic(de.name), "algorithmic_bytes": de.bytes,
+                "us_per_launch": round(d_us, 3), "timed": "CUDA events around its launch in every timed step"}
+
+    # per-kernel table: each launch timed alone (clean L2, event pair), after the step loop
+    reps = max(10, min(50, args.steps))
+
+    def time_alone(fn, n):
+        out = []
+        for _ in range(n):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            clean_l2()
+            torch.cuda._sleep(200000)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            b.synchronize()
+            out.append(a.elapsed_time(b))
+        return out
+
+    def time_stream(e):
+        """Per-launch time of back-to-back launches, each on its own copy of the
+        buffers; the copies together exceed 4x L2, so every launch reads cold data."""
+        n = int(min(64, max(1, -(-STREAM_BYTES // max(1, e.bytes)))))
+        calls = e.replicas(n) if n > 1 else [e.launch]
+        rounds = max(2, 8 // len(calls)) if len(calls) < 8 else 3
+        for c in calls:
+            c()
+        per = []
+        for _ in range(rounds):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            clean_l2()
+            torch.cuda._sleep(200000)
+            a.record(stream)
+            for c in calls:
+                c()
+            b.record(stream)
+            b.synchronize()
+            per.append(a.elapsed_time(b) / len(calls))
+        del calls
+        return statistics.median(per), n
+
     per_kernel = []
     for e in entries:
-        us = statistics.fmean(e.times) * 1e3
-        rec = {"name": e.name, "bytes": e.bytes, "us": round(us, 3),
-               "us_p20": round(sorted(e.times)[len(e.times) // 5] * 1e3, 3),
-               "us_p80": round(sorted(e.times)[(4 * len(e.times)) // 5] * 1e3, 3),
-               "gbs": round(e.bytes / (us * 1e-6) / 1e9, 1), "frac_of_peak": round(e.bytes / (us * 1e-6) / 1e9 / peak, 4),
-               "rows_per_s": round(e.rows / (us * 1e-6), 1)}
+        times = time_alone(e.launch, reps)
+        us = statistics.fmean(times) * 1e3
+        srt = sorted(times)
+        rec = {"name": e.name, "bytes": e.bytes, "us_alone": round(us, 3),
+               "us_alone_p20": round(srt[len(srt) // 5] * 1e3, 3),
+               "us_alone_p80": round(srt[(4 * len(srt)) // 5] * 1e3, 3)}
+        if e.op != "chain":
+            st_ms, copies = time_stream(e)
+            su = st_ms * 1e3
+            rec.update({"us": round(su, 3), "copies": copies, "gbs": round(e.bytes / (su * 1e-6) / 1e9, 1),
+                        "frac_of_peak": round(e.bytes / (su * 1e-6) / 1e9 / peak, 4),
+                        "rows_per_s": round(e.rows / (su * 1e-6), 1)})
+        else:
+            rec.update({"us": round(us, 3), "gbs": round(e.bytes / (us * 1e-6) / 1e9, 1),
+                        "frac_of_peak": round(e.bytes / (us * 1e-6) / 1e9 / peak, 4),
+                        "rows_per_s": round(e.rows / (us * 1e-6), 1)})
         if e.op == "chain":
             rec["tokens_per_s"] = rec.pop("rows_per_s")
             rec["launches"] = 112
+            rec["us_per_launch"] = round(us / 112, 3)
+            rec["pdl"] = pdl
+            # A/B: the same chain captured without programmatic dependent launch
+            g_main = e.chain.graph
+            e.chain.capture(pdl=not pdl, warmup=False)
+            t_alt = time_alone(e.chain.replay, reps)
+            e.chain.graph = g_main
+            rec["us_other_pdl_setting"] = round(statistics.fmean(t_alt) * 1e3, 3)
         per_kernel.append(rec)
-    kern = [i for i, e in enumerate(entries) if e.op != "chain"] or list(range(len(entries)))
-    dom = max(kern, key=lambda i: statistics.fmean(entries[i].times))
-    de = entries[dom]
-    d_us = statistics.fmean(de.times) * 1e3
-    achieved = de.bytes / (d_us * 1e-6) / 1e9
-    traffic = kernel_traffic(de.name)
-    roofline = {"bound": "hbm", "kernel": de.name, "achieved": round(achieved, 1), "peak": peak,
-                "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": traffic, "algorithmic_bytes": de.bytes, "us_per_launch": round(d_us, 3)}
 
-    # companions (row-scaled shapes, >= 256 MB traffic), timed alone after the step loop
+    # launch latency: back-to-back launches of a one-row RMSNorm (1 x 128 bf16),
+    # queued behind a device delay so the host is ahead; with and without PDL
+    latency = {}
+    if not only:
+        from swiglu_rmsnorm_add_gb300 import synthetic as syn
+
+        xt, wt = syn.rms_inputs(1, 128, torch.bfloat16, 7)
+        xt, wt = xt.to(dev), wt.to(dev)
+        ot = torch.empty_like(xt)
+        L = sra.lib()
+        targs = (xt.data_ptr(), wt.data_ptr(), ot.data_ptr(), 1, 128, 128, 128, 1e-6, 2, sh)
+        for mode in (True, False):
+            prev = sra.set_pdl(mode)
+            n = 200
+            per = []
+            for _ in range(3):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                torch.cuda._sleep(int(2e6))
+                a.record(stream)
+                for _ in range(n):
+                    L.sra_rmsnorm(*targs)
+                b.record(stream)
+                b.synchronize()
+                per.append(a.elapsed_time(b) * 1e3 / n)
+            sra.set_pdl(prev)
+            latency["pdl" if mode else "no_pdl"] = round(statistics.median(per), 3)
+        latency["what"] = "us per launch, 200 back-to-back rmsnorm [1,128] bf16 launches"
+
+    # companions (row-scaled shapes, >= 256 MB traffic), timed alone
     companions = []
     if not args.no_companions and not only:
         comp = build_entries(dev, sh, companions=True)
         for e in comp:
-            times = []
-            for _ in range(max(3, args.warmup)):
-                flush.zero_()
+            for _ in range(3):
                 e.launch()
-            for _ in range(max(10, min(50, args.steps))):
-                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                flush.zero_()
-                torch.cuda._sleep(200000)
-                a.record(stream)
-                e.launch()
-                b.record(stream)
-                b.synchronize()
-                times.append(a.elapsed_time(b))
-            us = statistics.fmean(times) * 1e3
-            companions.append({"name": e.name, "bytes": e.bytes, "us": round(us, 2),
-                               "gbs": round(e.bytes / (us * 1e-6) / 1e9, 1),
+            times = time_alone(e.launch, reps)
+            ua = statistics.fmean(times) * 1e3
+            st_ms, copies = time_stream(e)
+            us = st_ms * 1e3
+            companions.append({"name": e.name, "bytes": e.bytes, "us_alone": round(ua, 2), "us": round(us, 2),
+                               "copies": copies, "gbs": round(e.bytes / (us * 1e-6) / 1e9, 1),
                                "frac_of_peak": round(e.bytes / (us * 1e-6) / 1e9 / peak, 4)})
         del comp
 
@@ -523,7 +651,7 @@ def run_gpu(args):
             enqueue_step()
             for d, h in pairs_out:
                 h.copy_(d, non_blocking=True)
-            torch.cuda.current_stream(dev).synchronize()
+            stream.synchronize()
 
         for _ in range(max(2, args.warmup)):
             e2e_step()
@@ -554,13 +682,14 @@ def run_gpu(args):
                 "vs_baseline": None, "dtype": "f32", "data": "synthetic (seeded host RNG, resident in HBM)",
                 "config": {"workload": WORKLOAD if not only else f"subset: {','.join(only)}",
                            "io_dtypes": "bf16 (rmsnorm sweep also fp32, fp16); arithmetic fp32",
-                           "l2": "flushed before every step by a 256 MiB device write",
+                           "l2": "flushed before every step: a 256 MiB device write, then a read of it",
                            "bytes_per_step": bytes_per_step, "launches_per_step": launches_per_step,
+                           "programmatic_dependent_launch": pdl,
                            "parallelism": f"replicas x{world} (no collective)",
                            "step_wall_ms_incl_flush_and_delay": round(wall / args.steps * 1e3, 3)},
                 "gpu_launches": launches_per_step * args.steps,
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clk,
-                "kernels": per_kernel, "companions": companions}
+                "launch_latency_us": latency, "kernels": per_kernel, "companions": companions}
         print(json.dumps(line), flush=True)
     if world > 1:
         dist.destroy_process_group()

@@ -190,6 +190,24 @@ SRA_API const char* sra_status_string(int status);
 SRA_API int sra_version(void);
 
 /*
+ * The cudaError_t value behind the most recent SRA_ERR_LAUNCH returned to the
+ * calling thread (0 if there has been none). Diagnostic only.
+ */
+SRA_API int sra_last_cuda_error(void);
+
+/*
+ * Programmatic dependent launch for the CALLING THREAD's subsequent calls
+ * (enable != 0: on; 0: off, the default). When on, each kernel is launched with
+ * programmatic stream serialization: the GPU may schedule it while the kernel
+ * before it in the stream is still finishing, which hides launch latency in
+ * chains of short kernels (e.g. a decode step). Every kernel of this library
+ * first waits for the preceding grid to complete and its writes to become
+ * visible, so results are identical either way. The setting is captured into
+ * CUDA graphs with the launches. Returns the previous setting.
+ */
+SRA_API int sra_set_pdl(int enable);
+
+/*
  * Kernel-variant control, for A/B measurement of the per-shape dispatch.
  * op: "rmsnorm" (also used by add_rmsnorm), "rope_kv_store", "glu".
  * variant: -1 = automatic per-shape choice (the default); otherwise an index

@@ -16,6 +16,7 @@ from ._binding import (  # noqa: F401
     reglu,
     rmsnorm,
     rope_kv_store,
+    set_pdl,
     status_string,
     swiglu,
     variant_count,
@@ -23,4 +24,4 @@ from ._binding import (  # noqa: F401
 )
 
 __all__ = ["rmsnorm", "add_rmsnorm", "rope_kv_store", "swiglu", "reglu", "glu", "lib", "SRAError",
-           "force_variant", "variant_count", "variant_name", "pick_variant", "status_string"]
+           "force_variant", "set_pdl", "variant_count", "variant_name", "pick_variant", "status_string"]

@@ -18,7 +18,10 @@ ACT_CODE = {"silu": 0, "relu": 1}
 
 class SRAError(RuntimeError):
     def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn}: {status_string(status)} (status {status})")
+        msg = f"{fn}: {status_string(status)} (status {status})"
+        if status == -8:
+            msg += f", cudaError {lib().sra_last_cuda_error()}"
+        super().__init__(msg)
         self.status = status
 
 
@@ -44,6 +47,9 @@ def lib() -> ctypes.CDLL:
             L.sra_status_string.argtypes = [i32]
             L.sra_status_string.restype = ctypes.c_char_p
             L.sra_version.restype = i32
+            L.sra_last_cuda_error.restype = i32
+            L.sra_set_pdl.argtypes = [i32]
+            L.sra_set_pdl.restype = i32
             L.sra_force_variant.argtypes = [ctypes.c_char_p, i32]
             L.sra_force_variant.restype = i32
             L.sra_variant_count.argtypes = [ctypes.c_char_p]
@@ -63,6 +69,11 @@ def status_string(status: int) -> str:
 def _check(fn: str, status: int) -> None:
     if status != 0:
         raise SRAError(fn, status)
+
+
+def set_pdl(enable: bool) -> bool:
+    """Programmatic dependent launch for this thread's later calls; returns the previous setting."""
+    return bool(lib().sra_set_pdl(1 if enable else 0))
 
 
 def force_variant(op: str, variant: int) -> None:
@@ -180,6 +191,8 @@ def add_rmsnorm(x: torch.Tensor, res: torch.Tensor, w: torch.Tensor, out: torch.
 def _tok_stride(t: torch.Tensor, name: str) -> int:
     if t.dim() != 3:
         raise ValueError(f"{name} must be [T, heads, head_dim]")
+    if t.numel() == 0:
+        return t.shape[1] * t.shape[2]
     if t.stride(-1) != 1 or (t.shape[1] > 1 and t.stride(1) != t.shape[2]):
         raise ValueError(f"{name}: heads must be contiguous within a token")
     return t.stride(0) if t.shape[0] > 1 else t.shape[1] * t.shape[2]

@@ -37,6 +37,7 @@ def nvcc() -> str:
 def _inputs() -> list[str]:
     files = [os.path.join(CSRC, s) for s in SOURCES]
     files += glob.glob(os.path.join(CSRC, "*.cuh")) + glob.glob(os.path.join(CSRC, "*.h"))
+    files += [os.path.join(CSRC, "exports.map")]
     files += glob.glob(os.path.join(INCLUDE, "*.h")) + [os.path.abspath(__file__)]
     return files
 
@@ -67,7 +68,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     with cf.ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, SOURCES))
     tmp = LIB + f".tmp{os.getpid()}"
-    cmd = [cc] + ARCH + ["-shared", "-Xlinker", "--exclude-libs,ALL", "-o", tmp] + objs
+    cmd = [cc] + ARCH + ["-shared", "-Xlinker", "--exclude-libs,ALL", "-Xlinker",
+                          "--version-script=" + os.path.join(CSRC, "exports.map"), "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")

@@ -83,16 +83,24 @@ class DecodeChain:
             for _, call in self.layer_calls(l):
                 call()
 
-    def capture(self) -> torch.cuda.CUDAGraph:
-        """Capture one step into a CUDA graph (warm up first, outside capture)."""
-        s = torch.cuda.Stream()
-        s.wait_stream(torch.cuda.current_stream())
-        with torch.cuda.stream(s):
-            self.step()
-        torch.cuda.current_stream().wait_stream(s)
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            self.step()
+    def capture(self, pdl: bool = True, warmup: bool = True) -> torch.cuda.CUDAGraph:
+        """Capture one step into a CUDA graph (after one eager warm-up step unless
+        warmup=False). With pdl, each launch is captured with programmatic
+        stream serialization, so a kernel's launch overlaps the tail of the one
+        before it."""
+        prev = sra.set_pdl(pdl)
+        try:
+            if warmup:
+                s = torch.cuda.Stream()
+                s.wait_stream(torch.cuda.current_stream())
+                with torch.cuda.stream(s):
+                    self.step()
+                torch.cuda.current_stream().wait_stream(s)
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                self.step()
+        finally:
+            sra.set_pdl(prev)
         self.graph = g
         return g
 

@@ -19,6 +19,7 @@ constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_smem_optin[kMaxDevices];
 std::atomic<int> g_force_norm{-1}, g_force_rope{-1}, g_force_glu{-1};
+thread_local bool g_pdl = false;  // programmatic dependent launch for this thread's calls
 
 // SM count of the current device (cached per device).
 int current_sm_count(int* dev_out) {
@@ -71,6 +72,21 @@ Span span_of(const void* p, int64_t rows, int64_t stride, int64_t width, int es)
 }
 bool overlap(Span a, Span b) { return a.lo < b.hi && b.lo < a.hi && a.lo != a.hi && b.lo != b.hi; }
 
+// Whether two strided row sets [p + r*stride, p + r*stride + width) (r < rows,
+// element units of size es) share a byte. Exact for equal strides (interleaved
+// views of one fused buffer, e.g. q / k / v of a fused QKV); otherwise the
+// conservative span test.
+bool rows_overlap(const void* p1, int64_t rows1, int64_t s1, int64_t w1, const void* p2, int64_t rows2, int64_t s2,
+                  int64_t w2, int es) {
+    const Span a = span_of(p1, rows1, s1, w1, es), b = span_of(p2, rows2, s2, w2, es);
+    if (!overlap(a, b)) return false;
+    if (s1 != s2 || rows1 <= 1 || rows2 <= 1 || s1 < w1 || s1 < w2) return true;
+    const int64_t S = s1 * es, W1 = w1 * es, W2 = w2 * es;
+    const int64_t d = static_cast<int64_t>(reinterpret_cast<intptr_t>(p2) - reinterpret_cast<intptr_t>(p1));
+    const int64_t dm = ((d % S) + S) % S;  // row 2's start within row 1's period
+    return dm < W1 || dm + W2 > S;
+}
+
 int ceil_div_i(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int round_up32(int64_t v) { return static_cast<int>(((v + 31) / 32) * 32); }
@@ -81,43 +97,78 @@ constexpr int kWarpMaxNv = 8;
 constexpr int kCtaMaxAccesses = 2048;  // 256 threads x 8, 512 x 4, 1024 x 2
 
 int cta_max_threads_for_nv(int nv) { return nv >= 8 ? 256 : (nv >= 4 ? 512 : 1024); }
+size_t round_up16(int64_t bytes) { return static_cast<size_t>((bytes + 15) / 16 * 16); }
+
+// NV (accesses per thread) and threads for `nacc` accesses spread over one CTA:
+// few rows favour many threads with short chains, many rows fewer threads with
+// more accesses each (smaller CTAs, more of them resident).
+bool cta_shape(int64_t nacc, bool few_rows, int* nv_out, int* threads_out) {
+    int nv = few_rows ? 1 : 8;
+    while (nv < 8 && ceil_div(nacc, nv) > cta_max_threads_for_nv(nv)) nv <<= 1;
+    while (nv > 1 && ceil_div(nacc, nv) < 64) nv >>= 1;
+    if (ceil_div(nacc, nv) > cta_max_threads_for_nv(nv)) return false;
+    *nv_out = nv;
+    *threads_out = std::max(32, round_up32(ceil_div(nacc, nv)));
+    return true;
+}
 
 bool plan_norm_variant(int variant, int64_t rows, int64_t D, int vec, int es, int num_sms, int smem_limit,
                        NormPlan* p) {
+    const int64_t nvec = D / vec;
     const int64_t nacc = ceil_div(D, vec);  // accesses per row, tail included
+    const bool few_rows = rows < 2LL * num_sms;
     p->variant = variant;
     p->vec = vec;
     p->smem = 0;
+    p->pdl = g_pdl;
+    p->num_sms = num_sms;
     switch (variant) {
         case NORM_WARP_ROWS: {
             const int64_t per_lane = ceil_div(nacc, 32);
             if (per_lane > kWarpMaxNv) return false;
-            int nv = 1;
-            while (nv < per_lane) nv <<= 1;
+            static const int kNv[] = {1, 2, 3, 4, 6, 8};
+            int nv = 8;
+            for (int c : kNv) {
+                if (c >= per_lane) {
+                    nv = c;
+                    break;
+                }
+            }
             p->nv = nv;
-            // Warps per CTA: spread few rows over many SMs, pack many rows densely.
-            int wpc = 1;
-            if (rows >= 8LL * num_sms) wpc = 8;
-            else if (rows >= 4LL * num_sms) wpc = 4;
-            else if (rows >= 2LL * num_sms) wpc = 2;
-            p->threads = 32 * wpc;
-            const int64_t max_ctas = static_cast<int64_t>(num_sms) * (2048 / p->threads);
-            p->grid = std::max<int64_t>(1, std::min(ceil_div(rows, wpc), max_ctas));
+            // Warps per CTA: the smallest per-SM row load when CTAs are dealt to
+            // SMs evenly (ties to larger CTAs).
+            int best = 8;
+            int64_t best_load = -1;
+            for (int wpc : {8, 4, 2, 1}) {
+                const int64_t load = ceil_div(ceil_div(rows, wpc), num_sms) * wpc;
+                if (best_load < 0 || load < best_load) {
+                    best_load = load;
+                    best = wpc;
+                }
+            }
+            p->threads = 32 * best;
+            p->grid = std::max<int64_t>(1, ceil_div(rows, best));
+            p->smem = round_up16(D * es);
             return true;
         }
         case NORM_CTA_ROW: {
             if (nacc > kCtaMaxAccesses) return false;
-            // Few rows (decode): spread a row over many threads, short per-thread
-            // chains. Many rows: fewer threads per row, more accesses each.
-            const bool few_rows = rows < 2LL * num_sms;
-            int nv = few_rows ? 1 : 4;
-            while (nv < 8 && ceil_div(nacc, nv) > cta_max_threads_for_nv(nv)) nv <<= 1;
-            while (nv > 1 && ceil_div(nacc, nv) < 64) nv >>= 1;
-            if (ceil_div(nacc, nv) > cta_max_threads_for_nv(nv)) return false;
+            if (!cta_shape(nacc, few_rows, &p->nv, &p->threads)) return false;
+            p->grid = std::max<int64_t>(1, rows);
+            p->smem = round_up16(D * es);
+            return true;
+        }
+        case NORM_CTA_PAIR: {
+            const int64_t half = norm_pair_half(nvec);
+            const int64_t per_cta = std::max<int64_t>(half, nacc - half);
+            if (per_cta > kCtaMaxAccesses) return false;
+            int nv = 0, threads = 0;
+            if (!cta_shape(per_cta, few_rows, &nv, &threads)) return false;
+            if (nv < 2) nv = 2, threads = std::max(32, round_up32(ceil_div(per_cta, 2)));
             p->nv = nv;
-            p->threads = std::max(32, round_up32(ceil_div(nacc, nv)));
-            const int64_t max_ctas = static_cast<int64_t>(num_sms) * std::max(1, 2048 / p->threads);
-            p->grid = std::max<int64_t>(1, std::min(rows, max_ctas));
+            p->threads = threads;
+            p->grid = 2 * std::max<int64_t>(1, rows);
+            p->smem = round_up16(std::max(half * vec, D - half * vec) * es);
             return true;
         }
         case NORM_CTA_SMEM: {
@@ -126,15 +177,13 @@ bool plan_norm_variant(int variant, int64_t rows, int64_t D, int vec, int es, in
             p->nv = 0;
             p->smem = static_cast<size_t>(bytes);
             p->threads = static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(nacc))));
-            const int per_sm = std::max<int64_t>(1, (smem_limit) / std::max<int64_t>(bytes, 1));
-            p->grid = std::max<int64_t>(1, std::min(rows, static_cast<int64_t>(num_sms) * per_sm));
+            p->grid = std::max<int64_t>(1, rows);
             return true;
         }
         case NORM_TWO_PASS: {
             p->nv = 0;
             p->threads = static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(nacc))));
-            const int64_t max_ctas = static_cast<int64_t>(num_sms) * std::max(1, 2048 / p->threads);
-            p->grid = std::max<int64_t>(1, std::min(rows, max_ctas));
+            p->grid = std::max<int64_t>(1, rows);
             return true;
         }
         default:
@@ -142,12 +191,17 @@ bool plan_norm_variant(int variant, int64_t rows, int64_t D, int vec, int es, in
     }
 }
 
-int auto_norm_variant(int64_t rows, int64_t D, int vec) {
+int auto_norm_variant(int64_t rows, int64_t D, int vec, int num_sms) {
     const int64_t nacc = ceil_div(D, vec);
     // Warp-per-row when the row fits a warp's registers and there are enough rows
-    // to keep the SMs busy; otherwise a CTA per row.
+    // to keep the SMs busy.
     if (nacc <= 32 * kWarpMaxNv && (rows >= 256 || nacc <= 64)) return NORM_WARP_ROWS;
+    // Wide rows, more rows than SMs but too few to spread evenly one per CTA:
+    // split each row over a CTA pair.
+    const bool pair_rows = rows >= 2LL * num_sms && rows < 16LL * num_sms;
+    if (nacc >= 1024 && nacc <= 2LL * kCtaMaxAccesses && pair_rows) return NORM_CTA_PAIR;
     if (nacc <= kCtaMaxAccesses) return NORM_CTA_ROW;
+    if (nacc <= 2LL * kCtaMaxAccesses && rows >= 2LL * num_sms) return NORM_CTA_PAIR;
     return NORM_CTA_SMEM;
 }
 
@@ -166,7 +220,7 @@ int plan_norm(int64_t rows, int64_t D, int dt, int vec, int num_sms, int smem_li
         if (!plan_norm_variant(forced, rows, D, vec, es, num_sms, smem_limit, p)) return SRA_ERR_VARIANT;
         return SRA_OK;
     }
-    int v = auto_norm_variant(rows, D, vec);
+    int v = auto_norm_variant(rows, D, vec, num_sms);
     if (v == NORM_CTA_SMEM && !plan_norm_variant(v, rows, D, vec, es, num_sms, smem_limit, p)) v = NORM_TWO_PASS;
     if (!plan_norm_variant(v, rows, D, vec, es, num_sms, smem_limit, p)) return SRA_ERR_VARIANT;
     return SRA_OK;
@@ -180,9 +234,10 @@ int plan_rope(int64_t T, int n_head, int n_kv, int head_dim, int pairs, int num_
     const int64_t U = static_cast<int64_t>(n_head + 2 * n_kv) * (h / pairs);
     p->variant = ROPE_TOKEN_CTA;
     p->pairs = pairs;
+    p->pdl = g_pdl;
+    p->num_sms = num_sms;
     p->threads = static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(U))));
-    const int64_t max_ctas = static_cast<int64_t>(num_sms) * std::max(1, 2048 / p->threads);
-    p->grid = std::max<int64_t>(1, std::min(T, max_ctas));
+    p->grid = std::max<int64_t>(1, T);
     return SRA_OK;
 }
 
@@ -193,6 +248,8 @@ int plan_glu(int64_t T, int64_t I, int vec, int num_sms, GluPlan* p) {
     const int64_t nv = I / vec;
     p->variant = GLU_COLS_ROWS;
     p->vec = vec;
+    p->pdl = g_pdl;
+    p->num_sms = num_sms;
     // Few rows: narrow CTAs spread the columns over many SMs. Many rows: 256 threads.
     int threads = T >= 64 ? 256 : 128;
     threads = static_cast<int>(std::min<int64_t>(threads, std::max(32, round_up32(nv))));
@@ -217,8 +274,11 @@ int glu_vec(int dt, const void* gu, const void* out, int64_t I, int64_t is, int6
     return 1;
 }
 
+thread_local int g_last_cuda_error = 0;
+
 int status_from(cudaError_t e) {
     if (e == cudaSuccess) return SRA_OK;
+    g_last_cuda_error = static_cast<int>(e);
     cudaGetLastError();
     return SRA_ERR_LAUNCH;
 }
@@ -232,14 +292,18 @@ int norm_common(void* x, const void* res, const void* w, void* out, int64_t rows
     if (rows == 0) return SRA_OK;
     if (!x || !w || !out || (add && !res)) return SRA_ERR_NULL;
     const int es = elem_bytes(dtype);
-    const Span sx = span_of(x, rows, xs, D, es), so = span_of(out, rows, os, D, es), sw = span_of(w, 1, D, D, es);
+    const Span sw = span_of(w, 1, D, D, es);
+    const Span sx = span_of(x, rows, xs, D, es), so = span_of(out, rows, os, D, es);
     if (add) {
         const Span sr = span_of(res, rows, rs, D, es);
-        if (overlap(so, sx) || overlap(so, sr) || overlap(so, sw) || overlap(sx, sw)) return SRA_ERR_ALIAS;
-        if (overlap(sx, sr) && !(res == x && rs == xs)) return SRA_ERR_ALIAS;
+        if (rows_overlap(out, rows, os, D, x, rows, xs, D, es) || rows_overlap(out, rows, os, D, res, rows, rs, D, es) ||
+            overlap(so, sw) || overlap(sx, sw))
+            return SRA_ERR_ALIAS;
+        if (!(res == x && rs == xs) && rows_overlap(x, rows, xs, D, res, rows, rs, D, es)) return SRA_ERR_ALIAS;
+        (void)sr;
     } else {
         const bool in_place = out == x && os == xs;
-        if ((!in_place && overlap(so, sx)) || overlap(so, sw)) return SRA_ERR_ALIAS;
+        if ((!in_place && rows_overlap(out, rows, os, D, x, rows, xs, D, es)) || overlap(so, sw)) return SRA_ERR_ALIAS;
     }
     int dev = 0;
     const int sms = current_sm_count(&dev);
@@ -251,9 +315,6 @@ int norm_common(void* x, const void* res, const void* w, void* out, int64_t rows
     const int smem_limit = smem_optin(dev);
     int st = plan_norm(rows, D, dtype, vec, sms, smem_limit, &plan);
     if (st != SRA_OK) return st;
-    if (plan.variant == NORM_CTA_SMEM && plan.smem > 48 * 1024) {
-        if (norm_smem_prepare(dtype, add, vec, plan.smem) != cudaSuccess) return status_from(cudaErrorInvalidValue);
-    }
     NormArgs a;
     a.x = x;
     a.res = res;
@@ -293,6 +354,14 @@ using namespace sra;
 extern "C" {
 
 int sra_version(void) { return SRA_VERSION; }
+
+int sra_last_cuda_error(void) { return g_last_cuda_error; }
+
+int sra_set_pdl(int enable) {
+    const int prev = g_pdl ? 1 : 0;
+    g_pdl = enable != 0;
+    return prev;
+}
 
 const char* sra_status_string(int status) {
     switch (status) {
@@ -340,7 +409,9 @@ int sra_rope_kv_store(void* q, const void* k, const void* v, const float* cos, c
     const Span sq = span_of(q, T, q_tok_stride, qw, es), sk = span_of(k, T, k_tok_stride, kw, es),
                sv = span_of(v, T, v_tok_stride, kw, es);
     const Span sc = span_of(kv_cache, 1, 0, 2 * num_blocks * block_size * kw, es);
-    if (overlap(sq, sk) || overlap(sq, sv) || overlap(sc, sq) || overlap(sc, sk) || overlap(sc, sv))
+    if (rows_overlap(q, T, q_tok_stride, qw, k, T, k_tok_stride, kw, es) ||
+        rows_overlap(q, T, q_tok_stride, qw, v, T, v_tok_stride, kw, es) || overlap(sc, sq) || overlap(sc, sk) ||
+        overlap(sc, sv))
         return SRA_ERR_ALIAS;
     int dev = 0;
     const int sms = current_sm_count(&dev);
@@ -387,8 +458,7 @@ int sra_glu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row
     if (T == 0) return SRA_OK;
     if (!gate_up || !out) return SRA_ERR_NULL;
     const int es = elem_bytes(dtype);
-    if (overlap(span_of(gate_up, T, in_row_stride, 2 * I, es), span_of(out, T, out_row_stride, I, es)))
-        return SRA_ERR_ALIAS;
+    if (rows_overlap(gate_up, T, in_row_stride, 2 * I, out, T, out_row_stride, I, es)) return SRA_ERR_ALIAS;
     int dev = 0;
     const int sms = current_sm_count(&dev);
     if (sms <= 0) return SRA_ERR_DEVICE;
@@ -421,7 +491,7 @@ int sra_force_variant(const char* op, int variant) {
 int sra_variant_count(const char* op) { return variant_count(op); }
 
 const char* sra_variant_name(const char* op, int variant) {
-    static const char* const norm_names[] = {"warp_rows", "cta_row", "cta_smem", "two_pass"};
+    static const char* const norm_names[] = {"warp_rows", "cta_row", "cta_smem", "two_pass", "cta_pair"};
     static const char* const rope_names[] = {"token_cta"};
     static const char* const glu_names[] = {"cols_rows"};
     const int n = variant_count(op);

@@ -8,7 +8,79 @@
 #include <stdint.h>
 #include <string.h>
 
+#include <mutex>
+#include <unordered_map>
+#include <utility>
+
 namespace sra {
+
+// Resident CTAs per SM of `kernel` at `threads` threads and `smem` bytes of
+// dynamic shared memory (occupancy of the exact function launched), cached per
+// (kernel, threads, smem). Persistent grids are sized from it so that every CTA
+// is resident at once and no partial second wave forms.
+template <typename... KArgs>
+inline int resident_ctas_per_sm(void (*kernel)(KArgs...), int threads, size_t smem) {
+    static std::mutex mu;
+    static std::unordered_map<uint64_t, int> cache;
+    const uint64_t key = (reinterpret_cast<uint64_t>(reinterpret_cast<void*>(kernel)) << 20) ^
+                         (static_cast<uint64_t>(threads) << 40) ^ static_cast<uint64_t>(smem);
+    {
+        std::lock_guard<std::mutex> g(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess) {
+        cudaGetLastError();
+        n = 1;
+    }
+    if (n < 1) n = 1;
+    std::lock_guard<std::mutex> g(mu);
+    cache[key] = n;
+    return n;
+}
+
+// A persistent grid: `needed` CTAs, capped at what is resident at once.
+template <typename... KArgs>
+inline unsigned persistent_grid(void (*kernel)(KArgs...), int threads, size_t smem, int num_sms, int64_t needed) {
+    const int64_t cap = static_cast<int64_t>(resident_ctas_per_sm(kernel, threads, smem)) * num_sms;
+    int64_t g = needed < cap ? needed : cap;
+    if (g < 1) g = 1;
+    if (g > 0x7fffffff) g = 0x7fffffff;
+    return static_cast<unsigned>(g);
+}
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch (sm_90 and later). Every kernel calls
+// pdl_enter() before its first global-memory access: it waits until the grid
+// that precedes it in the stream has completed and its writes are visible,
+// then allows the next grid in the stream to be scheduled. When a kernel was
+// launched without programmatic stream serialization both instructions are
+// no-ops, so the kernels are correct either way.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// Launch `kernel` on `stream`, with programmatic stream serialization when
+// `pdl` is set (the kernel may then be scheduled while the previous kernel in
+// the stream finishes; pdl_enter() orders its memory accesses after it).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                                 cudaStream_t stream, bool pdl, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = pdl ? attr : nullptr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // ---------------------------------------------------------------------------
 // Element formats: widen to fp32, narrow with round-to-nearest-even.

@@ -8,15 +8,16 @@
 // gate = columns [0, I) of a row, up = columns [I, 2I).
 //
 // Layout: a 2-D grid. Thread (x) owns one VEC-wide column group j of every row
-// it visits; CTA rows (y) stride over the T rows, two rows in flight per
-// thread. No index division anywhere; all accesses 16 bytes when the row
-// widths, strides and base pointers allow.
+// it visits; CTA rows (y) stride over the T rows. The loop is software-
+// pipelined: the loads of the next pair of rows are issued before the current
+// pair is computed and stored, so four 16-byte loads per thread stay in flight
+// while the activation runs. No index division anywhere; all accesses 16 bytes
+// when the row widths, strides and base pointers allow.
 //
-// SiLU: g * sigma(g) with sigma from one ex2 and one reciprocal (fast
-// intrinsics, relative error ~1e-6, far inside half an output ulp of bf16 or
-// fp16). For g < 0 sigma(g) = e^g / (1 + e^g) is used, so the exponential
-// never overflows; |g| > ~87 underflows e^-|g| to zero, where the true SiLU
-// magnitude is below 2^-119.
+// SiLU: g / (1 + e^-g) with one ex2 and one reciprocal (fast intrinsics,
+// relative error ~1e-6, far inside half an output ulp of bf16 or fp16). For
+// g < -87.3 the denominator leaves the reciprocal's range and the result is 0,
+// where the true SiLU magnitude is below 2^-119.
 #include "common.cuh"
 #include "internal.h"
 
@@ -26,10 +27,7 @@ namespace glu {
 template <int ACT>
 __device__ __forceinline__ float act(float g) {
     if constexpr (ACT == 0) {
-        const float e = __expf(-fabsf(g));            // e^-|g| in (0, 1]
-        const float r = __fdividef(1.0f, 1.0f + e);   // sigma(|g|); denominator in [1, 2]
-        const float sig = g >= 0.0f ? r : e * r;      // sigma(g)
-        return g * sig;
+        return __fdividef(g, 1.0f + __expf(-g));
     } else {
         return fmaxf(g, 0.0f);
     }
@@ -51,6 +49,7 @@ template <typename T, int VEC, int ACT>
 __global__ void __launch_bounds__(256) cols_rows_kernel(GluArgs a) {
     using V = Vec<T, VEC>;
     using R = typename V::Raw;
+    pdl_enter();
     const int64_t nv = a.I / VEC;
     const int64_t jv = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (jv >= nv) return;
@@ -58,38 +57,58 @@ __global__ void __launch_bounds__(256) cols_rows_kernel(GluArgs a) {
     T* __restrict__ ocol = static_cast<T*>(a.out) + jv * VEC;
     const int64_t step = gridDim.y;
     int64_t t = blockIdx.y;
-    // Two rows per iteration: four independent 16-byte loads in flight per thread.
-    for (; t + step < a.T; t += 2 * step) {
-        const T* g0 = gcol + t * a.is;
-        const T* g1 = gcol + (t + step) * a.is;
-        const R ga = V::load_stream(g0), ua = V::load_stream(g0 + a.I);
-        const R gb = V::load_stream(g1), ub = V::load_stream(g1 + a.I);
-        V::store_stream(ocol + t * a.os, combine<T, VEC, ACT>(ga, ua));
-        V::store_stream(ocol + (t + step) * a.os, combine<T, VEC, ACT>(gb, ub));
+    if (t >= a.T) return;
+    // current pair (t, t + step); the second row may not exist
+    bool have1 = t + step < a.T;
+    R ga = V::load_stream(gcol + t * a.is), ua = V::load_stream(gcol + t * a.is + a.I);
+    R gb = ga, ub = ua;
+    if (have1) {
+        gb = V::load_stream(gcol + (t + step) * a.is);
+        ub = V::load_stream(gcol + (t + step) * a.is + a.I);
     }
-    if (t < a.T) {
-        const T* g0 = gcol + t * a.is;
-        const R ga = V::load_stream(g0), ua = V::load_stream(g0 + a.I);
+    while (true) {
+        const int64_t tn = t + 2 * step;
+        const bool next0 = tn < a.T, next1 = tn + step < a.T;
+        R gc = ga, uc = ua, gd = gb, ud = ub;
+        if (next0) {
+            gc = V::load_stream(gcol + tn * a.is);
+            uc = V::load_stream(gcol + tn * a.is + a.I);
+        }
+        if (next1) {
+            gd = V::load_stream(gcol + (tn + step) * a.is);
+            ud = V::load_stream(gcol + (tn + step) * a.is + a.I);
+        }
         V::store_stream(ocol + t * a.os, combine<T, VEC, ACT>(ga, ua));
+        if (have1) V::store_stream(ocol + (t + step) * a.os, combine<T, VEC, ACT>(gb, ub));
+        if (!next0) break;
+        ga = gc, ua = uc, gb = gd, ub = ud;
+        have1 = next1;
+        t = tn;
     }
+}
+
+template <typename T, int VEC, int ACT>
+cudaError_t launch_vec(const GluArgs& a, const GluPlan& p, cudaStream_t s) {
+    auto kernel = cols_rows_kernel<T, VEC, ACT>;
+    // Rows are strided over grid_y; size it so that grid_x * grid_y CTAs are all
+    // resident at once (one wave, every CTA with the same number of rows +- 1).
+    const int64_t resident = static_cast<int64_t>(resident_ctas_per_sm(kernel, p.threads, 0)) * p.num_sms;
+    int64_t gy = resident / (p.grid_x > 0 ? p.grid_x : 1);
+    if (gy < 1) gy = 1;
+    if (gy > a.T) gy = a.T;
+    if (gy > 65535) gy = 65535;
+    const dim3 grid(static_cast<unsigned>(p.grid_x), static_cast<unsigned>(gy)), block(p.threads);
+    return launch_kernel(kernel, grid, block, 0, s, p.pdl, a);
 }
 
 template <typename T, int ACT>
 cudaError_t launch_act(const GluArgs& a, const GluPlan& p, cudaStream_t s) {
-    const dim3 grid(static_cast<unsigned>(p.grid_x), static_cast<unsigned>(p.grid_y)), block(p.threads);
     constexpr int V16 = vec16<T>();
-    if (p.vec == V16) {
-        cols_rows_kernel<T, V16, ACT><<<grid, block, 0, s>>>(a);
-    } else if (p.vec == V16 / 2) {
-        cols_rows_kernel<T, V16 / 2, ACT><<<grid, block, 0, s>>>(a);
-    } else if (p.vec == V16 / 4) {
-        cols_rows_kernel<T, V16 / 4, ACT><<<grid, block, 0, s>>>(a);
-    } else if (p.vec == 1) {
-        cols_rows_kernel<T, 1, ACT><<<grid, block, 0, s>>>(a);
-    } else {
-        return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+    if (p.vec == V16) return launch_vec<T, V16, ACT>(a, p, s);
+    if (p.vec == V16 / 2) return launch_vec<T, V16 / 2, ACT>(a, p, s);
+    if (p.vec == V16 / 4) return launch_vec<T, V16 / 4, ACT>(a, p, s);
+    if (p.vec == 1) return launch_vec<T, 1, ACT>(a, p, s);
+    return cudaErrorInvalidValue;
 }
 
 template <typename T>

@@ -27,22 +27,32 @@ enum NormVariant {
     NORM_CTA_ROW = 1,    // one CTA per row, row held in registers
     NORM_CTA_SMEM = 2,   // one CTA per row, row staged in shared memory
     NORM_TWO_PASS = 3,   // one CTA per row, second pass re-reads the row (any D)
-    NORM_NUM_VARIANTS = 4
+    NORM_CTA_PAIR = 4,   // a 2-CTA cluster per row, half the row in each CTA's registers
+    NORM_NUM_VARIANTS = 5
 };
+
+#ifdef __CUDACC__
+#define SRA_HD __host__ __device__
+#else
+#define SRA_HD
+#endif
+// Accesses of a row taken by rank 0 of a cta_pair cluster (rank 1 takes the rest
+// and the scalar tail).
+inline SRA_HD int64_t norm_pair_half(int64_t nvec) { return (nvec + 1) / 2; }
 
 struct NormPlan {
     int variant;
     int vec;        // elements per access: 16 bytes' worth, or 1
     int nv;         // accesses per thread held in registers (warp / cta variants)
     int threads;    // threads per CTA
-    int64_t grid;   // CTAs
+    int64_t grid;   // CTAs wanted; the launcher caps it at the resident count
     size_t smem;    // dynamic shared memory, bytes
+    bool pdl;       // launch with programmatic stream serialization
+    int num_sms;
 };
 
 cudaError_t launch_rmsnorm(const NormArgs& a, const NormPlan& p, int dtype, cudaStream_t s);
 cudaError_t launch_add_rmsnorm(const NormArgs& a, const NormPlan& p, int dtype, cudaStream_t s);
-// Largest dynamic shared memory the CTA_SMEM variant may request on this device.
-cudaError_t norm_smem_prepare(int dtype, bool add, int vec, size_t bytes);
 
 // ------------------------------------------------------------ RoPE + KV store
 struct RopeArgs {
@@ -68,7 +78,9 @@ struct RopePlan {
     int variant;
     int pairs;      // rotation pairs per task: 16 bytes of elements per half, or 1
     int threads;    // threads per CTA
-    int64_t grid;   // CTAs (tokens are strided over the grid)
+    int64_t grid;   // CTAs wanted (tokens are strided over the grid); capped at the resident count
+    bool pdl;
+    int num_sms;
 };
 
 cudaError_t launch_rope_kv_store(const RopeArgs& a, const RopePlan& p, int dtype, cudaStream_t s);
@@ -88,7 +100,9 @@ struct GluPlan {
     int vec;        // elements per access (power of two, <= 16 bytes)
     int threads;    // threads per CTA (x)
     int64_t grid_x; // CTAs across the column vectors
-    int64_t grid_y; // CTAs across rows (rows strided over grid_y)
+    int64_t grid_y; // CTAs across rows (rows strided over grid_y); the launcher sizes it from occupancy
+    bool pdl;
+    int num_sms;
 };
 
 cudaError_t launch_glu(const GluArgs& a, const GluPlan& p, int act, int dtype, cudaStream_t s);

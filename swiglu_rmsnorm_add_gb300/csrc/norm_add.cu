@@ -7,8 +7,4 @@ cudaError_t launch_add_rmsnorm(const NormArgs& a, const NormPlan& p, int dtype, 
     return norm::launch<true>(a, p, dtype, s);
 }
 
-cudaError_t norm_smem_prepare(int dtype, bool add, int vec, size_t bytes) {
-    return add ? norm::smem_prepare<true>(dtype, vec, bytes) : norm::smem_prepare<false>(dtype, vec, bytes);
-}
-
 }  // namespace sra

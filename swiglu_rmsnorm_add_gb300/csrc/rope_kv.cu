@@ -39,6 +39,7 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
     using R = typename V::Raw;
     using C = Vec<float, (P >= 4 ? 4 : 1)>;  // cos / sin accesses
     constexpr int CW = P >= 4 ? 4 : 1;
+    pdl_enter();
 
     const int h = a.head_dim >> 1;
     const int per_head = h / P;
@@ -120,15 +121,11 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
 
 template <typename T>
 cudaError_t launch_typed(const RopeArgs& a, const RopePlan& p, cudaStream_t s) {
-    const dim3 grid(static_cast<unsigned>(p.grid)), block(p.threads);
-    if (p.pairs == vec16<T>()) {
-        token_cta_kernel<T, vec16<T>()><<<grid, block, 0, s>>>(a);
-    } else if (p.pairs == 1) {
-        token_cta_kernel<T, 1><<<grid, block, 0, s>>>(a);
-    } else {
-        return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+    const dim3 block(p.threads);
+    auto kernel = p.pairs == 1 ? token_cta_kernel<T, 1> : token_cta_kernel<T, vec16<T>()>;
+    if (p.pairs != 1 && p.pairs != vec16<T>()) return cudaErrorInvalidValue;
+    const dim3 grid(persistent_grid(kernel, p.threads, 0, p.num_sms, p.grid));
+    return launch_kernel(kernel, grid, block, 0, s, p.pdl, a);
 }
 
 }  // namespace rope

@@ -134,13 +134,14 @@ def test_glu_validation(L):
 
 
 def test_variant_control(L):
-    assert sra.variant_count("rmsnorm") == 4
+    assert sra.variant_count("rmsnorm") == 5
     assert sra.variant_count("rope_kv_store") == 1
     assert sra.variant_count("glu") == 1
     assert sra.variant_count("nope") == ARG
-    assert [sra.variant_name("rmsnorm", i) for i in range(4)] == ["warp_rows", "cta_row", "cta_smem", "two_pass"]
-    assert sra.variant_name("rmsnorm", 4) is None
-    assert L.sra_force_variant(b"rmsnorm", 4) == ARG
+    assert [sra.variant_name("rmsnorm", i) for i in range(5)] == ["warp_rows", "cta_row", "cta_smem", "two_pass",
+                                                                  "cta_pair"]
+    assert sra.variant_name("rmsnorm", 5) is None
+    assert L.sra_force_variant(b"rmsnorm", 5) == ARG
     assert L.sra_force_variant(b"bogus", 0) == ARG
     assert L.sra_force_variant(b"rmsnorm", 2) == OK
     assert sra.pick_variant("rmsnorm", 512, 1536, num_sms=152) == 2
@@ -156,7 +157,9 @@ def test_dispatch_choices(L):
     # decode (few rows) of the 1536-wide hidden state: a CTA per row
     assert pick("rmsnorm", 1, 1536, dtype=torch.bfloat16, num_sms=152) == 1
     # a row past a warp's registers: CTA per row
-    assert pick("rmsnorm", 512, 8192, dtype=torch.float32, num_sms=152) == 1
+    assert pick("rmsnorm", 512, 2176, dtype=torch.float32, num_sms=152) == 1
+    # wide rows, 512 of them on 152 SMs: a 2-CTA cluster per row
+    assert pick("rmsnorm", 512, 8192, dtype=torch.float32, num_sms=152) == 4
     # past the registers of a CTA: staged in shared memory
     assert pick("rmsnorm", 64, 40000, dtype=torch.bfloat16, num_sms=152) == 2
     # past shared memory: two-pass
@@ -164,3 +167,28 @@ def test_dispatch_choices(L):
     assert pick("glu", 4096, 14336, num_sms=152) == 0
     assert pick("rope_kv_store", 2048, 12, 2, 128, num_sms=152) == 0
     assert pick("rmsnorm", -1, 16, num_sms=152) == SHAPE
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(), reason="would launch on fake pointers")
+def test_interleaved_views_are_not_aliases(L):
+    """q / k / v as interleaved views of one fused QKV buffer pass the alias check
+    (the call then stops at the device query on this GPU-less host)."""
+    DEVICE = -9
+    T, nh, nkv, hd = 8, 12, 2, 128
+    W = (nh + 2 * nkv) * hd   # token stride of the fused buffer, elements
+    base = 0x100000
+    q, k, v = base, base + nh * hd * 2, base + (nh + nkv) * hd * 2
+    cache = 0x10000000
+    args = lambda q_, k_, v_: (q_, k_, v_, 0x2000000, 0x3000000, 0x4000000, 0x5000000, cache, T, nh, nkv, hd,
+                                W, W, W, 32768, 16, 16, None, BF16, None)
+    assert L.sra_rope_kv_store(*args(q, k, v)) == DEVICE
+    # k starting inside q's row of the same token: a real overlap
+    assert L.sra_rope_kv_store(*args(q, q + 64, v)) == ALIAS
+    # gate_up and out interleaved in one buffer of stride 3I: disjoint
+    I = 64
+    assert L.sra_glu(base, base + 2 * I * 2, 4, I, 3 * I, 3 * I, 0, BF16, None) == DEVICE
+    assert L.sra_glu(base, base + I * 2, 4, I, 3 * I, 3 * I, 0, BF16, None) == ALIAS
+    # add_rmsnorm: x | res | out interleaved rows of one [rows, 3D] buffer
+    D = 32
+    assert L.sra_add_rmsnorm(base, base + D * 2, 0x900000, base + 2 * D * 2, 4, D, 3 * D, 3 * D, 3 * D, 1e-6,
+                             BF16, None) == DEVICE

@@ -60,13 +60,36 @@ def test_chain_per_kernel_and_end_to_end(B):
     assert_bits_equal(ch.x, x_oracle, "end-to-end residual stream after 56 updates")
 
 
-def test_graph_replay_equals_eager():
+@pytest.mark.parametrize("pdl", [False, True])
+def test_graph_replay_equals_eager(pdl):
     a = DecodeChain(4, layers=3, num_blocks=16)
     b = DecodeChain(4, layers=3, num_blocks=16)
     a.step()
-    b.capture()   # capture warms up with one eager step, so both have run one step
-    a.step()
-    b.replay()
+    b.capture(pdl=pdl)   # capture warms up with one eager step, so both have run one step
+    for _ in range(3):
+        a.step()
+        b.replay()
+    torch.cuda.synchronize()
+    assert_bits_equal(a.x, b.x, "x")
+    for la, lb in zip(a.layers, b.layers):
+        for key in ("h1", "h2", "act", "q", "kv_cache"):
+            assert_bits_equal(la[key], lb[key], key)
+
+
+def test_eager_pdl_calls_match():
+    """Back-to-back eager launches with programmatic dependent launch on."""
+    import swiglu_rmsnorm_add_gb300 as sra
+
+    a = DecodeChain(64, layers=4, num_blocks=256)
+    b = DecodeChain(64, layers=4, num_blocks=256)
+    prev = sra.set_pdl(True)
+    try:
+        for _ in range(2):
+            b.step()
+    finally:
+        sra.set_pdl(prev)
+    for _ in range(2):
+        a.step()
     torch.cuda.synchronize()
     assert_bits_equal(a.x, b.x, "x")
     for la, lb in zip(a.layers, b.layers):
