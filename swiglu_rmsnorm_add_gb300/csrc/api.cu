@@ -42,6 +42,21 @@ int current_sm_count(int* dev_out) {
     return n;
 }
 
+int smem_per_sm(int dev) {
+    static std::atomic<int> cache[kMaxDevices];
+    if (dev >= 0 && dev < kMaxDevices) {
+        int c = cache[dev].load(std::memory_order_relaxed);
+        if (c > 0) return c;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess || n <= 0) {
+        cudaGetLastError();
+        return 100 * 1024;
+    }
+    if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
 int smem_optin(int dev) {
     if (dev >= 0 && dev < kMaxDevices) {
         int c = g_smem_optin[dev].load(std::memory_order_relaxed);
@@ -92,117 +107,166 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int round_up32(int64_t v) { return static_cast<int>(((v + 31) / 32) * 32); }
 
 // ------------------------------------------------------------------ RMSNorm plan
-// Register capacity of each variant, in accesses of `vec` elements.
-constexpr int kWarpMaxNv = 8;
-constexpr int kCtaMaxAccesses = 2048;  // 256 threads x 8, 512 x 4, 1024 x 2
-
-int cta_max_threads_for_nv(int nv) { return nv >= 8 ? 256 : (nv >= 4 ? 512 : 1024); }
 size_t round_up16(int64_t bytes) { return static_cast<size_t>((bytes + 15) / 16 * 16); }
 
-// NV (accesses per thread) and threads for `nacc` accesses spread over one CTA:
-// few rows favour many threads with short chains, many rows fewer threads with
-// more accesses each (smaller CTAs, more of them resident).
-bool cta_shape(int64_t nacc, bool few_rows, int* nv_out, int* threads_out) {
-    int nv = few_rows ? 1 : 8;
-    while (nv < 8 && ceil_div(nacc, nv) > cta_max_threads_for_nv(nv)) nv <<= 1;
-    while (nv > 1 && ceil_div(nacc, nv) < 64) nv >>= 1;
-    if (ceil_div(nacc, nv) > cta_max_threads_for_nv(nv)) return false;
-    *nv_out = nv;
-    *threads_out = std::max(32, round_up32(ceil_div(nacc, nv)));
-    return true;
+// Shared memory the planner may use per CTA, and per SM (CTAs resident by memory).
+struct SmemBudget {
+    int per_cta;  // opt-in limit minus the kernels' static shared memory and a margin
+    int per_sm;   // shared memory of one SM
+};
+constexpr int kCtaReserve = 1024;  // per-CTA shared memory the system keeps
+
+int64_t resident_by_smem(const SmemBudget& b, size_t smem, int threads) {
+    const int64_t by_smem = b.per_sm / static_cast<int64_t>(smem + kCtaReserve + 256);
+    const int64_t by_threads = 2048 / threads;
+    return std::max<int64_t>(1, std::min<int64_t>(std::min<int64_t>(by_smem, by_threads), 32));
 }
 
-bool plan_norm_variant(int variant, int64_t rows, int64_t D, int vec, int es, int num_sms, int smem_limit,
-                       NormPlan* p) {
-    const int64_t nvec = D / vec;
-    const int64_t nacc = ceil_div(D, vec);  // accesses per row, tail included
-    const bool few_rows = rows < 2LL * num_sms;
-    p->variant = variant;
-    p->vec = vec;
-    p->smem = 0;
-    p->pdl = g_pdl;
-    p->num_sms = num_sms;
+// Scalar (unaligned) register kernels: warp NV in {1,2,4,8}; CTA NV in {1,2,4,8}.
+bool plan_norm_scalar(int variant, int64_t rows, int64_t D, int num_sms, NormPlan* p) {
     switch (variant) {
         case NORM_WARP_ROWS: {
-            const int64_t per_lane = ceil_div(nacc, 32);
-            if (per_lane > kWarpMaxNv) return false;
-            static const int kNv[] = {1, 2, 3, 4, 6, 8};
-            int nv = 8;
-            for (int c : kNv) {
-                if (c >= per_lane) {
-                    nv = c;
-                    break;
-                }
-            }
+            if (D > 256) return false;
+            int nv = 1;
+            while (nv * 32 < D) nv <<= 1;
             p->nv = nv;
-            // Warps per CTA: the smallest per-SM row load when CTAs are dealt to
-            // SMs evenly (ties to larger CTAs).
-            int best = 8;
-            int64_t best_load = -1;
-            for (int wpc : {8, 4, 2, 1}) {
-                const int64_t load = ceil_div(ceil_div(rows, wpc), num_sms) * wpc;
-                if (best_load < 0 || load < best_load) {
-                    best_load = load;
-                    best = wpc;
-                }
-            }
-            p->threads = 32 * best;
-            p->grid = std::max<int64_t>(1, ceil_div(rows, best));
-            p->smem = round_up16(D * es);
+            p->threads = rows >= 4LL * num_sms ? 128 : 32;
+            p->grid = std::max<int64_t>(1, ceil_div(rows, p->threads / 32));
             return true;
         }
         case NORM_CTA_ROW: {
-            if (nacc > kCtaMaxAccesses) return false;
-            if (!cta_shape(nacc, few_rows, &p->nv, &p->threads)) return false;
+            if (D > 8192) return false;
+            int nv = 1;
+            while (nv < 8 && ceil_div(D, nv) > 1024) nv <<= 1;
+            if (rows >= 2LL * num_sms) {
+                while (nv < 8 && ceil_div(D, nv) > 256) nv <<= 1;
+            }
+            p->nv = nv;
+            p->threads = std::max(32, round_up32(ceil_div(D, nv)));
             p->grid = std::max<int64_t>(1, rows);
-            p->smem = round_up16(D * es);
+            return true;
+        }
+        case NORM_TWO_PASS:
+            p->nv = 0;
+            p->threads = static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(D))));
+            p->grid = std::max<int64_t>(1, rows);
+            return true;
+        default:
+            return false;  // cta_smem and cta_pair need 16-byte layouts
+    }
+}
+
+// Threads for `acc` 16-byte accesses of one row slice: few rows (decode) get one
+// access per thread; many rows about four, so more rows are resident.
+int staged_threads(int64_t acc, bool few_rows) {
+    const int64_t per = few_rows ? 1 : 4;
+    return static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(ceil_div(acc, per)))));
+}
+
+bool plan_norm_staged(int variant, int64_t rows, int64_t D, int vec, int es, bool add, int num_sms,
+                      const SmemBudget& b, NormPlan* p) {
+    const int64_t nvec = D / vec;
+    const int copies = add ? 2 : 1;  // x (and res) slices per group
+    const bool few_rows = rows < 2LL * num_sms;
+    (void)es;
+    switch (variant) {
+        case NORM_WARP_ROWS: {
+            if (ceil_div(D, vec) > 256) return false;
+            const size_t slice = round_up16(nvec * 16);
+            // Warps per CTA: the smallest per-SM row load that is resident in one
+            // round (shared memory and the 64-warp limit); ties go to larger CTAs.
+            int best = 0;
+            int64_t best_load = 0, best_cap = 0;
+            for (int wpc : {8, 4, 2, 1}) {
+                const size_t smem = slice + wpc * slice * copies;
+                if (static_cast<int64_t>(smem) > b.per_cta) continue;
+                const int64_t cap = resident_by_smem(b, smem, 32 * wpc) * wpc;  // rows per SM in one round
+                const int64_t load = ceil_div(ceil_div(rows, wpc), num_sms) * wpc;
+                const bool fits = load <= cap;
+                const bool best_fits = best && best_load <= best_cap;
+                if (!best || (fits && (!best_fits || load < best_load)) || (!fits && !best_fits && cap > best_cap)) {
+                    best = wpc, best_load = load, best_cap = cap;
+                }
+            }
+            if (!best) return false;
+            p->nv = 0;
+            p->threads = 32 * best;
+            p->grid = std::max<int64_t>(1, ceil_div(rows, best));
+            p->smem = slice + best * slice * copies;
+            p->stage_w = 1;
+            return true;
+        }
+        case NORM_CTA_ROW:
+        case NORM_CTA_SMEM: {
+            const size_t slice = round_up16(nvec * 16);
+            const bool stage = variant == NORM_CTA_ROW;
+            const size_t smem = (stage ? slice : 0) + slice * copies;
+            if (static_cast<int64_t>(smem) > b.per_cta) return false;
+            p->nv = 0;
+            p->threads = staged_threads(nvec, few_rows);
+            p->grid = std::max<int64_t>(1, rows);
+            p->smem = smem;
+            p->stage_w = stage ? 1 : 0;
             return true;
         }
         case NORM_CTA_PAIR: {
+            if (nvec < 2) return false;
             const int64_t half = norm_pair_half(nvec);
-            const int64_t per_cta = std::max<int64_t>(half, nacc - half);
-            if (per_cta > kCtaMaxAccesses) return false;
-            int nv = 0, threads = 0;
-            if (!cta_shape(per_cta, few_rows, &nv, &threads)) return false;
-            if (nv < 2) nv = 2, threads = std::max(32, round_up32(ceil_div(per_cta, 2)));
-            p->nv = nv;
-            p->threads = threads;
+            const size_t slice = round_up16(half * 16);
+            const size_t smem = slice + slice * copies;
+            if (static_cast<int64_t>(smem) > b.per_cta) return false;
+            p->nv = 0;
+            p->threads = staged_threads(half, few_rows);
             p->grid = 2 * std::max<int64_t>(1, rows);
-            p->smem = round_up16(std::max(half * vec, D - half * vec) * es);
+            p->smem = smem;
+            p->stage_w = 1;
             return true;
         }
-        case NORM_CTA_SMEM: {
-            const int64_t bytes = ceil_div(D, vec) * vec * es;
-            if (bytes > smem_limit - 1024) return false;
+        case NORM_TWO_PASS:
             p->nv = 0;
-            p->smem = static_cast<size_t>(bytes);
-            p->threads = static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(nacc))));
+            p->threads = static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(ceil_div(D, vec)))));
             p->grid = std::max<int64_t>(1, rows);
             return true;
-        }
-        case NORM_TWO_PASS: {
-            p->nv = 0;
-            p->threads = static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(nacc))));
-            p->grid = std::max<int64_t>(1, rows);
-            return true;
-        }
         default:
             return false;
     }
 }
 
-int auto_norm_variant(int64_t rows, int64_t D, int vec, int num_sms) {
+bool plan_norm_variant(int variant, int64_t rows, int64_t D, int vec, int es, bool add, int num_sms,
+                       const SmemBudget& b, NormPlan* p) {
+    p->variant = variant;
+    p->vec = vec;
+    p->smem = 0;
+    p->pdl = g_pdl;
+    p->num_sms = num_sms;
+    p->stage_w = 0;
+    if (vec == 1) return plan_norm_scalar(variant, rows, D, num_sms, p);
+    return plan_norm_staged(variant, rows, D, vec, es, add, num_sms, b, p);
+}
+
+// Automatic choice, in order of preference for the shape.
+int plan_norm(int64_t rows, int64_t D, int dt, int vec, bool add, int num_sms, const SmemBudget& b, NormPlan* p) {
+    const int es = elem_bytes(dt);
+    const int forced = g_force_norm.load(std::memory_order_relaxed);
+    if (forced >= 0) {
+        if (!plan_norm_variant(forced, rows, D, vec, es, add, num_sms, b, p)) return SRA_ERR_VARIANT;
+        return SRA_OK;
+    }
     const int64_t nacc = ceil_div(D, vec);
-    // Warp-per-row when the row fits a warp's registers and there are enough rows
-    // to keep the SMs busy.
-    if (nacc <= 32 * kWarpMaxNv && (rows >= 256 || nacc <= 64)) return NORM_WARP_ROWS;
+    int order[5];
+    int n = 0;
+    // Short rows and many of them: a warp per row.
+    if (nacc <= 256 && (rows >= 256 || nacc <= 64)) order[n++] = NORM_WARP_ROWS;
     // Wide rows, more rows than SMs but too few to spread evenly one per CTA:
     // split each row over a CTA pair.
-    const bool pair_rows = rows >= 2LL * num_sms && rows < 16LL * num_sms;
-    if (nacc >= 1024 && nacc <= 2LL * kCtaMaxAccesses && pair_rows) return NORM_CTA_PAIR;
-    if (nacc <= kCtaMaxAccesses) return NORM_CTA_ROW;
-    if (nacc <= 2LL * kCtaMaxAccesses && rows >= 2LL * num_sms) return NORM_CTA_PAIR;
-    return NORM_CTA_SMEM;
+    if (nacc >= 1024 && rows >= 2LL * num_sms && rows < 16LL * num_sms) order[n++] = NORM_CTA_PAIR;
+    order[n++] = NORM_CTA_ROW;
+    order[n++] = NORM_CTA_SMEM;
+    order[n++] = NORM_TWO_PASS;
+    for (int i = 0; i < n; ++i) {
+        if (plan_norm_variant(order[i], rows, D, vec, es, add, num_sms, b, p)) return SRA_OK;
+    }
+    return SRA_ERR_VARIANT;
 }
 
 int norm_vec(int dt, const void* const* ptrs, int nptr, const int64_t* strides, int nstr) {
@@ -211,19 +275,6 @@ int norm_vec(int dt, const void* const* ptrs, int nptr, const int64_t* strides, 
     for (int i = 0; i < nptr; ++i) ok = ok && aligned16(ptrs[i]);
     for (int i = 0; i < nstr; ++i) ok = ok && stride_aligned16(strides[i], es);
     return ok ? 16 / es : 1;
-}
-
-int plan_norm(int64_t rows, int64_t D, int dt, int vec, int num_sms, int smem_limit, NormPlan* p) {
-    const int es = elem_bytes(dt);
-    const int forced = g_force_norm.load(std::memory_order_relaxed);
-    if (forced >= 0) {
-        if (!plan_norm_variant(forced, rows, D, vec, es, num_sms, smem_limit, p)) return SRA_ERR_VARIANT;
-        return SRA_OK;
-    }
-    int v = auto_norm_variant(rows, D, vec, num_sms);
-    if (v == NORM_CTA_SMEM && !plan_norm_variant(v, rows, D, vec, es, num_sms, smem_limit, p)) v = NORM_TWO_PASS;
-    if (!plan_norm_variant(v, rows, D, vec, es, num_sms, smem_limit, p)) return SRA_ERR_VARIANT;
-    return SRA_OK;
 }
 
 // ------------------------------------------------------------------ RoPE plan
@@ -312,8 +363,10 @@ int norm_common(void* x, const void* res, const void* w, void* out, int64_t rows
     const int64_t strides[3] = {xs, os, add ? rs : xs};
     const int vec = norm_vec(dtype, ptrs, 4, strides, 3);
     NormPlan plan;
-    const int smem_limit = smem_optin(dev);
-    int st = plan_norm(rows, D, dtype, vec, sms, smem_limit, &plan);
+    SmemBudget budget;
+    budget.per_cta = smem_optin(dev) - 1024;
+    budget.per_sm = smem_per_sm(dev);
+    int st = plan_norm(rows, D, dtype, vec, add, sms, budget, &plan);
     if (st != SRA_OK) return st;
     NormArgs a;
     a.x = x;
@@ -326,6 +379,7 @@ int norm_common(void* x, const void* res, const void* w, void* out, int64_t rows
     a.rs = add ? rs : 0;
     a.os = os;
     a.eps = eps;
+    a.stage_w = plan.stage_w;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return status_from(add ? launch_add_rmsnorm(a, plan, dtype, s) : launch_rmsnorm(a, plan, dtype, s));
 }
@@ -512,7 +566,10 @@ int sra_pick_variant(const char* op, int64_t a, int64_t b, int64_t c, int64_t d,
     if (std::strcmp(op, "rmsnorm") == 0) {
         if (a < 0 || b <= 0) return SRA_ERR_SHAPE;
         NormPlan p;
-        const int st = plan_norm(a, b, dtype, 16 / es, num_sms, 227 * 1024, &p);
+        SmemBudget budget;
+        budget.per_cta = 227 * 1024 - 1024;
+        budget.per_sm = 228 * 1024;
+        const int st = plan_norm(a, b, dtype, 16 / es, false, num_sms, budget, &p);
         return st == SRA_OK ? p.variant : st;
     }
     if (std::strcmp(op, "rope_kv_store") == 0) {

@@ -66,19 +66,31 @@ __device__ __forceinline__ void pdl_enter() {
 // Launch `kernel` on `stream`, with programmatic stream serialization when
 // `pdl` is set (the kernel may then be scheduled while the previous kernel in
 // the stream finishes; pdl_enter() orders its memory accesses after it).
+// `cluster` > 1 launches thread-block clusters of that many CTAs along x.
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
-                                 cudaStream_t stream, bool pdl, Args&&... args) {
+                                 cudaStream_t stream, bool pdl, int cluster, Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = pdl ? attr : nullptr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = static_cast<unsigned>(cluster);
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
+    cfg.attrs = n ? attr : nullptr;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
@@ -219,7 +231,7 @@ struct Vec {
 };
 
 // Elements per 16-byte access.
-template <typename T> constexpr int vec16() { return 16 / int(sizeof(T)); }
+template <typename T> __host__ __device__ constexpr int vec16() { return 16 / int(sizeof(T)); }
 
 // ---------------------------------------------------------------------------
 // Reductions

@@ -98,7 +98,7 @@ cudaError_t launch_vec(const GluArgs& a, const GluPlan& p, cudaStream_t s) {
     if (gy > a.T) gy = a.T;
     if (gy > 65535) gy = 65535;
     const dim3 grid(static_cast<unsigned>(p.grid_x), static_cast<unsigned>(gy)), block(p.threads);
-    return launch_kernel(kernel, grid, block, 0, s, p.pdl, a);
+    return launch_kernel(kernel, grid, block, 0, s, p.pdl, 1, a);
 }
 
 template <typename T, int ACT>

@@ -20,6 +20,7 @@ struct NormArgs {
     int64_t rows, D;
     int64_t xs, rs, os;  // row strides, elements
     float eps;
+    int stage_w;         // staged kernels: 1 = w slice staged in shared memory
 };
 
 enum NormVariant {
@@ -49,6 +50,7 @@ struct NormPlan {
     size_t smem;    // dynamic shared memory, bytes
     bool pdl;       // launch with programmatic stream serialization
     int num_sms;
+    int stage_w;    // staged kernels: stage the w slice in shared memory
 };
 
 cudaError_t launch_rmsnorm(const NormArgs& a, const NormPlan& p, int dtype, cudaStream_t s);

@@ -8,21 +8,27 @@
 // page, section 4) first stores x <- round(x + res) in place and normalises the
 // rounded sum, reading each row once and writing it twice.
 //
-// Per-shape variants, all with 16-byte vector accesses when the layout allows
-// and a predicated scalar tail (never a power-of-two padded width):
-//   warp_rows  one warp per row, the row held in registers (short rows)
-//   cta_row    one CTA per row, the row held in registers (long rows)
-//   cta_smem   one CTA per row staged in shared memory (rows past the registers)
-//   two_pass   one CTA per row, statistics pass then a re-reading scale pass (any D)
-//   cta_pair   a 2-CTA cluster per row: each CTA holds half the row in registers
-//              and the two partial sums of squares meet through distributed
-//              shared memory (wide rows when rows alone cannot fill the SMs evenly)
-// The register variants stage w once per CTA in shared memory with cp.async
-// (no registers held, no software wait), so the registers hold only the row.
-// Every variant keeps a row's elements with one thread across both passes, so
-// in-place use (out == x) is safe and no inter-thread hazard exists on the row.
-// Each translation unit instantiates one ADD value only (norm_rms.cu: false,
-// norm_add.cu: true), so no kernel is registered from two modules.
+// Variants (chosen per shape by the host planner):
+//   warp_rows  a warp per row              (short rows, many of them)
+//   cta_row    a CTA per row, w staged     (long rows, or few rows: decode)
+//   cta_smem   a CTA per row, w from L2    (rows too wide to stage w beside them)
+//   two_pass   a CTA per row, the scale pass re-reads the row (any width)
+//   cta_pair   a 2-CTA cluster per row: each CTA takes half the row and the two
+//              partial sums of squares meet through distributed shared memory
+//              (wide rows when one CTA per row cannot spread evenly over the SMs)
+//
+// 16-byte layouts (the normal case) use the staged kernel: every row lands in
+// shared memory through cp.async (16-byte asynchronous copies that hold no
+// registers while in flight; cp.async.wait_all is a hardware wait, not a
+// software spin). The copies of the weight slice and of the first row are
+// issued together, so a row costs one memory round trip; the resident row count
+// is then bounded by shared memory (about the row's bytes), not by registers.
+// Layouts that are not 16-byte aligned use register kernels with scalar access.
+// A predicated scalar tail covers D % VEC; nothing is padded to a power of two.
+// Every thread reads back and writes only its own elements, so in-place use
+// (out == x) is safe. Each translation unit instantiates one ADD value only
+// (norm_rms.cu: false, norm_add.cu: true), so no kernel is registered from two
+// modules.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -41,196 +47,228 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
 }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
-// Copy w[e0, e1) (elements) to ws[0, e1 - e0) with every thread of the CTA:
-// 16-byte asynchronous copies for whole vectors, plain loads for the rest.
-// e0 is a multiple of VEC.
-template <typename T, int VEC>
-__device__ __forceinline__ void stage_weights(const T* __restrict__ w, T* ws, int64_t e0, int64_t e1) {
-    if constexpr (VEC * sizeof(T) == 16) {
-        const int64_t nv = (e1 - e0) / VEC;
-        for (int64_t i = threadIdx.x; i < nv; i += blockDim.x) cp_async16(ws + i * VEC, w + e0 + i * VEC);
-        for (int64_t j = e0 + nv * VEC + threadIdx.x; j < e1; j += blockDim.x) ws[j - e0] = w[j];
-        cp_async_wait_all();
-    } else {
-        for (int64_t j = e0 + threadIdx.x; j < e1; j += blockDim.x) ws[j - e0] = w[j];
-    }
-    __syncthreads();
-}
-
-// How the row's sum of squares is reduced.
+// How a row's sum of squares is reduced, and which threads share a row.
 enum Reduce { RED_WARP = 0, RED_CTA = 1, RED_PAIR = 2 };
 
-// One row, held in registers. The caller's group (a warp, a CTA or a CTA of a
-// pair) covers accesses [a0, a1) of the row: thread tid owns
-// idx = a0 + v * threads + tid for v < NV. `tail_owner` marks the group that
-// also owns the D % VEC trailing elements. ws holds w from element a0 * VEC on.
-template <typename T, int VEC, int NV, bool ADD, int RED>
-__device__ __forceinline__ void row_in_registers(const NormArgs& a, int64_t r, int tid, int threads, int64_t a0,
-                                                 int64_t a1, bool tail_owner, const T* ws, float* scratch,
-                                                 float* pair_slot, int parity) {
-    using V = Vec<T, VEC>;
-    using R = typename V::Raw;
-    const int64_t nvec = a.D / VEC;
-    const int tail = tail_owner ? static_cast<int>(a.D - nvec * VEC) : 0;
-    T* xr = static_cast<T*>(a.x) + r * a.xs;
-    T* orow = static_cast<T*>(a.out) + r * a.os;
+__host__ __device__ constexpr size_t round16(size_t b) { return (b + 15) / 16 * 16; }
 
-    R xv[NV];
-    float xt = 0.0f;
-#pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        const int64_t idx = a0 + static_cast<int64_t>(v) * threads + tid;
-        if (idx < a1) xv[v] = V::load(xr + idx * VEC);
-    }
-    if (tid < tail) xt = to_f32(xr[nvec * VEC + tid]);
-
-    float ss = 0.0f;
-    if constexpr (ADD) {
-        const T* rr = static_cast<const T*>(a.res) + r * a.rs;
-        R rv[NV];
-        float rt = 0.0f;
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const int64_t idx = a0 + static_cast<int64_t>(v) * threads + tid;
-            if (idx < a1) rv[v] = V::load(rr + idx * VEC);
-        }
-        if (tid < tail) rt = to_f32(rr[nvec * VEC + tid]);
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const int64_t idx = a0 + static_cast<int64_t>(v) * threads + tid;
-            if (idx < a1) {
-                float xf[VEC], rf[VEC];
-                V::unpack(xv[v], xf);
-                V::unpack(rv[v], rf);
-#pragma unroll
-                for (int i = 0; i < VEC; ++i) xf[i] += rf[i];
-                xv[v] = V::pack(xf);  // the rounded sum
-                V::store(xr + idx * VEC, xv[v]);
-                V::unpack(xv[v], xf);
-#pragma unroll
-                for (int i = 0; i < VEC; ++i) ss = fmaf(xf[i], xf[i], ss);
-            }
-        }
-        if (tid < tail) {
-            const T s = from_f32<T>(xt + rt);
-            xr[nvec * VEC + tid] = s;
-            xt = to_f32(s);
-            ss = fmaf(xt, xt, ss);
-        }
-    } else {
-#pragma unroll
-        for (int v = 0; v < NV; ++v) {
-            const int64_t idx = a0 + static_cast<int64_t>(v) * threads + tid;
-            if (idx < a1) {
-                float xf[VEC];
-                V::unpack(xv[v], xf);
-#pragma unroll
-                for (int i = 0; i < VEC; ++i) ss = fmaf(xf[i], xf[i], ss);
-            }
-        }
-        if (tid < tail) ss = fmaf(xt, xt, ss);
-    }
-
+// Sum of squares of one row reduced over the group; every thread gets it.
+template <int RED>
+__device__ __forceinline__ float group_sum(float ss, float* scratch, float* pair_slot, int parity) {
     if constexpr (RED == RED_WARP) {
-        ss = warp_sum(ss);
+        return warp_sum(ss);
     } else if constexpr (RED == RED_CTA) {
-        ss = block_sum(ss, scratch);
+        return block_sum(ss, scratch);
     } else {
-        // Pair: each CTA's partial goes to its own slot (double-buffered by row
-        // parity), the cluster barrier publishes both, each CTA adds the peer's.
+        // Each CTA's partial goes to its own slot (double-buffered by row parity so
+        // the next row cannot overwrite a value the peer has yet to read); the
+        // cluster barrier publishes both; each CTA adds the peer's.
         const float part = block_sum(ss, scratch);
         cg::cluster_group cl = cg::this_cluster();
         if (threadIdx.x == 0) pair_slot[parity] = part;
         cl.sync();
         const float peer = *cl.map_shared_rank(pair_slot + parity, static_cast<int>(cl.block_rank()) ^ 1);
-        ss = part + peer;  // the same sum on both CTAs (addition commutes exactly)
+        return part + peer;  // the same value on both CTAs (addition commutes exactly)
     }
-    const float rinv = rsqrtf(ss / static_cast<float>(a.D) + a.eps);
+}
 
+// ------------------------------------------------------------------ staged
+// T with 16-byte accesses (VEC = 16 / sizeof(T)). Shared memory:
+//   [ws: the w slice if a.stage_w] [per group: x slice][per group: res slice (ADD)]
+// each slice round16(slice_accesses * 16) bytes.
+template <typename T, bool ADD, int RED>
+__global__ void __launch_bounds__(1024) staged_rows_kernel(NormArgs a) {
+    constexpr int VEC = vec16<T>();
+    using V = Vec<T, VEC>;
+    extern __shared__ __align__(16) unsigned char dyn_smem[];
+    __shared__ float scratch[33];
+    __shared__ float pair_slot[2];
+    pdl_enter();
+
+    const int64_t nvec = a.D / VEC;
+    int rank = 0;
+    if constexpr (RED == RED_PAIR) rank = static_cast<int>(cg::this_cluster().block_rank());
+    const int64_t half = norm_pair_half(nvec);
+    const int64_t a0 = (RED == RED_PAIR && rank == 1) ? half : 0;
+    const int64_t a1 = (RED == RED_PAIR && rank == 0) ? half : nvec;
+    const int64_t slice_max = RED == RED_PAIR ? half : nvec;
+    const size_t slice_bytes = round16(static_cast<size_t>(slice_max) * 16);
+    const int tail = (RED != RED_PAIR || rank == 1) ? static_cast<int>(a.D - nvec * VEC) : 0;
+
+    int tid, threads, group, groups;
+    if constexpr (RED == RED_WARP) {
+        tid = threadIdx.x & 31, threads = 32, group = threadIdx.x >> 5, groups = blockDim.x >> 5;
+    } else {
+        tid = threadIdx.x, threads = blockDim.x, group = 0, groups = 1;
+    }
+    int64_t r0, step;
+    if constexpr (RED == RED_WARP) {
+        r0 = static_cast<int64_t>(blockIdx.x) * groups + group, step = static_cast<int64_t>(gridDim.x) * groups;
+    } else if constexpr (RED == RED_CTA) {
+        r0 = blockIdx.x, step = gridDim.x;
+    } else {
+        r0 = blockIdx.x / 2, step = gridDim.x / 2;
+    }
+
+    const bool stage_w = a.stage_w != 0;
+    T* ws = reinterpret_cast<T*>(dyn_smem);
+    unsigned char* gbase = dyn_smem + (stage_w ? slice_bytes : 0) + group * slice_bytes * (ADD ? 2 : 1);
+    T* xs = reinterpret_cast<T*>(gbase);
+    T* rs = reinterpret_cast<T*>(gbase + slice_bytes);
+    const T* w = static_cast<const T*>(a.w);
+
+    auto issue_row = [&](int64_t r) {
+        const T* xr = static_cast<const T*>(a.x) + r * a.xs;
+        const T* rr = static_cast<const T*>(a.res) + r * a.rs;
+        for (int64_t idx = a0 + tid; idx < a1; idx += threads) {
+            cp_async16(xs + (idx - a0) * VEC, xr + idx * VEC);
+            if constexpr (ADD) cp_async16(rs + (idx - a0) * VEC, rr + idx * VEC);
+        }
+    };
+
+    // The D % VEC trailing elements travel by plain loads, issued with the copies.
+    float xt = 0.0f, rt = 0.0f, wt = 0.0f;
+    auto load_tail = [&](int64_t r) {
+        if (tid < tail) {
+            const int64_t j = nvec * VEC + tid;
+            xt = to_f32(static_cast<const T*>(a.x)[r * a.xs + j]);
+            if constexpr (ADD) rt = to_f32(static_cast<const T*>(a.res)[r * a.rs + j]);
+            wt = to_f32(w[j]);
+        }
+    };
+
+    // Prologue: the w slice and this group's first row are in flight together.
+    if (stage_w) {
+        for (int64_t i = threadIdx.x; i < a1 - a0; i += blockDim.x) cp_async16(ws + i * VEC, w + (a0 + i) * VEC);
+    }
+    if (r0 < a.rows) {
+        issue_row(r0);
+        load_tail(r0);
+    }
+    cp_async_wait_all();
+    __syncthreads();  // every thread's w chunks are visible to the whole CTA
+
+    int parity = 0;
+    for (int64_t r = r0; r < a.rows; r += step) {
+        if (r != r0) {
+            issue_row(r);
+            load_tail(r);
+            cp_async_wait_all();  // this thread's own chunks only: no barrier needed
+        }
+        T* xr = static_cast<T*>(a.x) + r * a.xs;
+        T* orow = static_cast<T*>(a.out) + r * a.os;
+
+        float ss = 0.0f;
+        for (int64_t idx = a0 + tid; idx < a1; idx += threads) {
+            float xf[VEC];
+            V::unpack(V::load(xs + (idx - a0) * VEC), xf);
+            if constexpr (ADD) {
+                float rf[VEC];
+                V::unpack(V::load(rs + (idx - a0) * VEC), rf);
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        const int64_t idx = a0 + static_cast<int64_t>(v) * threads + tid;
-        if (idx < a1) {
+                for (int i = 0; i < VEC; ++i) xf[i] += rf[i];
+                const typename V::Raw p = V::pack(xf);  // the rounded sum
+                V::store(xr + idx * VEC, p);
+                V::store(xs + (idx - a0) * VEC, p);
+                V::unpack(p, xf);
+            }
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) ss = fmaf(xf[i], xf[i], ss);
+        }
+        if (tid < tail) {
+            if constexpr (ADD) {
+                const T s = from_f32<T>(xt + rt);
+                xr[nvec * VEC + tid] = s;
+                xt = to_f32(s);
+            }
+            ss = fmaf(xt, xt, ss);
+        }
+        ss = group_sum<RED>(ss, scratch, pair_slot, parity);
+        parity ^= 1;
+        const float rinv = rsqrtf(ss / static_cast<float>(a.D) + a.eps);
+
+        for (int64_t idx = a0 + tid; idx < a1; idx += threads) {
             float xf[VEC], wf[VEC];
-            V::unpack(xv[v], xf);
-            V::unpack(V::load(ws + (idx - a0) * VEC), wf);
+            V::unpack(V::load(xs + (idx - a0) * VEC), xf);
+            V::unpack(stage_w ? V::load(ws + (idx - a0) * VEC) : V::load(w + idx * VEC), wf);
 #pragma unroll
             for (int i = 0; i < VEC; ++i) xf[i] = xf[i] * rinv * wf[i];
             V::store(orow + idx * VEC, V::pack(xf));
         }
+        if (tid < tail) orow[nvec * VEC + tid] = from_f32<T>(xt * rinv * wt);
     }
-    if (tid < tail) {
-        const int64_t j = nvec * VEC + tid;
-        orow[j] = from_f32<T>(xt * rinv * to_f32(ws[j - a0 * VEC]));
+    if constexpr (RED == RED_PAIR) {
+        cg::this_cluster().sync();  // no CTA exits while its peer may still read its pair_slot
     }
 }
 
-template <typename T, int VEC, int NV, bool ADD>
-__global__ void __launch_bounds__(256) warp_rows_kernel(NormArgs a) {
-    extern __shared__ __align__(16) unsigned char dyn_smem[];
-    T* ws = reinterpret_cast<T*>(dyn_smem);
+// ------------------------------------------------------------------ registers
+// Scalar accesses (layouts that are not 16-byte aligned): the row in registers,
+// NV elements per thread, w loaded beside it.
+template <typename T, int NV, bool ADD, int RED>
+__device__ __forceinline__ void scalar_row(const NormArgs& a, int64_t r, int tid, int threads, float* scratch) {
+    T* xr = static_cast<T*>(a.x) + r * a.xs;
+    const T* rr = static_cast<const T*>(a.res) + r * a.rs;
+    const T* w = static_cast<const T*>(a.w);
+    T* orow = static_cast<T*>(a.out) + r * a.os;
+    float xv[NV], wv[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int64_t j = static_cast<int64_t>(v) * threads + tid;
+        xv[v] = 0.0f;
+        if (j < a.D) {
+            xv[v] = to_f32(xr[j]);
+            if constexpr (ADD) xv[v] += to_f32(rr[j]);
+            wv[v] = to_f32(w[j]);
+        }
+    }
+    float ss = 0.0f;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int64_t j = static_cast<int64_t>(v) * threads + tid;
+        if (j < a.D) {
+            if constexpr (ADD) {
+                const T s = from_f32<T>(xv[v]);  // the rounded sum
+                xr[j] = s;
+                xv[v] = to_f32(s);
+            }
+            ss = fmaf(xv[v], xv[v], ss);
+        }
+    }
+    ss = group_sum<RED>(ss, scratch, nullptr, 0);
+    const float rinv = rsqrtf(ss / static_cast<float>(a.D) + a.eps);
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int64_t j = static_cast<int64_t>(v) * threads + tid;
+        if (j < a.D) orow[j] = from_f32<T>(xv[v] * rinv * wv[v]);
+    }
+}
+
+template <typename T, int NV, bool ADD>
+__global__ void __launch_bounds__(256) scalar_warp_kernel(NormArgs a) {
     pdl_enter();
-    stage_weights<T, VEC>(static_cast<const T*>(a.w), ws, 0, a.D);
-    const int warps_per_cta = blockDim.x >> 5;
-    const int64_t step = static_cast<int64_t>(gridDim.x) * warps_per_cta;
-    const int lane = threadIdx.x & 31;
-    const int64_t nvec = a.D / VEC;
-    for (int64_t r = static_cast<int64_t>(blockIdx.x) * warps_per_cta + (threadIdx.x >> 5); r < a.rows;
-         r += step) {
-        row_in_registers<T, VEC, NV, ADD, RED_WARP>(a, r, lane, 32, 0, nvec, true, ws, nullptr, nullptr, 0);
-    }
+    const int wpc = blockDim.x >> 5;
+    const int64_t step = static_cast<int64_t>(gridDim.x) * wpc;
+    for (int64_t r = static_cast<int64_t>(blockIdx.x) * wpc + (threadIdx.x >> 5); r < a.rows; r += step)
+        scalar_row<T, NV, ADD, RED_WARP>(a, r, threadIdx.x & 31, 32, nullptr);
 }
 
-// Largest CTA the register-resident CTA variants are compiled for, per NV.
-template <int NV> constexpr int cta_row_max_threads() { return NV >= 8 ? 256 : (NV >= 4 ? 512 : 1024); }
-
-template <typename T, int VEC, int NV, bool ADD>
-__global__ void __launch_bounds__(cta_row_max_threads<NV>()) cta_row_kernel(NormArgs a) {
+template <typename T, int NV, bool ADD>
+__global__ void __launch_bounds__(1024) scalar_cta_kernel(NormArgs a) {
     __shared__ float scratch[33];
-    extern __shared__ __align__(16) unsigned char dyn_smem[];
-    T* ws = reinterpret_cast<T*>(dyn_smem);
     pdl_enter();
-    stage_weights<T, VEC>(static_cast<const T*>(a.w), ws, 0, a.D);
-    const int64_t nvec = a.D / VEC;
-    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
-        row_in_registers<T, VEC, NV, ADD, RED_CTA>(a, r, threadIdx.x, blockDim.x, 0, nvec, true, ws, scratch,
-                                                   nullptr, 0);
-    }
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
+        scalar_row<T, NV, ADD, RED_CTA>(a, r, threadIdx.x, blockDim.x, scratch);
 }
 
-template <typename T, int VEC, int NV, bool ADD>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(cta_row_max_threads<NV>()) cta_pair_kernel(NormArgs a) {
-    __shared__ float scratch[33];
-    __shared__ float pair_slot[2];
-    extern __shared__ __align__(16) unsigned char dyn_smem[];
-    T* ws = reinterpret_cast<T*>(dyn_smem);
-    pdl_enter();
-    cg::cluster_group cl = cg::this_cluster();
-    const int rank = static_cast<int>(cl.block_rank());
-    const int64_t nvec = a.D / VEC;
-    const int64_t half = norm_pair_half(nvec);
-    const int64_t a0 = rank == 0 ? 0 : half;
-    const int64_t a1 = rank == 0 ? half : nvec;
-    stage_weights<T, VEC>(static_cast<const T*>(a.w), ws, a0 * VEC, rank == 0 ? half * VEC : a.D);
-    const int64_t pairs = gridDim.x / 2;
-    int parity = 0;
-    for (int64_t r = blockIdx.x / 2; r < a.rows; r += pairs) {
-        row_in_registers<T, VEC, NV, ADD, RED_PAIR>(a, r, threadIdx.x, blockDim.x, a0, a1, rank == 1, ws, scratch,
-                                                    pair_slot, parity);
-        parity ^= 1;
-    }
-    // No CTA may exit while its peer can still read its pair_slot.
-    cl.sync();
-}
-
-// Row staged in shared memory (STAGED) or re-read from global memory (two-pass).
-template <typename T, int VEC, bool ADD, bool STAGED>
-__global__ void __launch_bounds__(1024) cta_wide_kernel(NormArgs a) {
+// ------------------------------------------------------------------ two-pass
+// Any width: the statistics pass keeps nothing; the scale pass re-reads the
+// row (from L2). Each thread revisits only its own elements.
+template <typename T, int VEC, bool ADD>
+__global__ void __launch_bounds__(1024) two_pass_kernel(NormArgs a) {
     using V = Vec<T, VEC>;
     using R = typename V::Raw;
-    extern __shared__ __align__(16) unsigned char dyn_smem[];
     __shared__ float scratch[33];
-    T* row_s = reinterpret_cast<T*>(dyn_smem);
     pdl_enter();
     const int tid = threadIdx.x, threads = blockDim.x;
     const int64_t nvec = a.D / VEC;
@@ -255,7 +293,6 @@ __global__ void __launch_bounds__(1024) cta_wide_kernel(NormArgs a) {
                 V::store(xr + idx * VEC, xv);
                 V::unpack(xv, xf);
             }
-            if constexpr (STAGED) V::store(row_s + idx * VEC, xv);
 #pragma unroll
             for (int i = 0; i < VEC; ++i) ss = fmaf(xf[i], xf[i], ss);
         }
@@ -274,11 +311,7 @@ __global__ void __launch_bounds__(1024) cta_wide_kernel(NormArgs a) {
         const float rinv = rsqrtf(ss / static_cast<float>(a.D) + a.eps);
         for (int64_t idx = tid; idx < nvec; idx += threads) {
             float xf[VEC], wf[VEC];
-            if constexpr (STAGED) {
-                V::unpack(V::load(row_s + idx * VEC), xf);
-            } else {
-                V::unpack(V::load(xr + idx * VEC), xf);  // this thread's own element(s)
-            }
+            V::unpack(V::load(xr + idx * VEC), xf);
             V::unpack(V::load(w + idx * VEC), wf);
 #pragma unroll
             for (int i = 0; i < VEC; ++i) xf[i] = xf[i] * rinv * wf[i];
@@ -291,6 +324,7 @@ __global__ void __launch_bounds__(1024) cta_wide_kernel(NormArgs a) {
     }
 }
 
+// ------------------------------------------------------------------ launch
 template <typename KArgs>
 cudaError_t smem_opt_in(void (*kernel)(KArgs), size_t smem) {
     if (smem <= 48 * 1024) return cudaSuccess;
@@ -298,67 +332,58 @@ cudaError_t smem_opt_in(void (*kernel)(KArgs), size_t smem) {
 }
 
 template <typename KArgs>
-cudaError_t launch_persistent(void (*kernel)(KArgs), const NormArgs& a, const NormPlan& p, size_t smem,
+cudaError_t launch_persistent(void (*kernel)(KArgs), const NormArgs& a, const NormPlan& p, bool pairs,
                               cudaStream_t s) {
-    const cudaError_t e = smem_opt_in(kernel, smem);
+    const cudaError_t e = smem_opt_in(kernel, p.smem);
     if (e != cudaSuccess) return e;
-    const dim3 grid(persistent_grid(kernel, p.threads, smem, p.num_sms, p.grid)), block(p.threads);
-    return launch_kernel(kernel, grid, block, smem, s, p.pdl, a);
+    unsigned g = persistent_grid(kernel, p.threads, p.smem, p.num_sms, p.grid);
+    if (pairs) {
+        g &= ~1u;  // whole clusters only
+        if (g < 2) g = 2;
+    }
+    return launch_kernel(kernel, dim3(g), dim3(p.threads), p.smem, s, p.pdl, pairs ? 2 : 1, a);
 }
 
-template <typename KArgs>
-cudaError_t launch_pair(void (*kernel)(KArgs), const NormArgs& a, const NormPlan& p, size_t smem,
-                        cudaStream_t s) {
-    const cudaError_t e = smem_opt_in(kernel, smem);
-    if (e != cudaSuccess) return e;
-    // Whole pairs only, at most the CTAs resident at once.
-    unsigned g = persistent_grid(kernel, p.threads, smem, p.num_sms, p.grid);
-    g &= ~1u;
-    if (g < 2) g = 2;
-    return launch_kernel(kernel, dim3(g), dim3(p.threads), smem, s, p.pdl, a);
+template <typename T, bool ADD>
+cudaError_t launch_staged(const NormArgs& a, const NormPlan& p, cudaStream_t s) {
+    switch (p.variant) {
+        case NORM_WARP_ROWS: return launch_persistent(staged_rows_kernel<T, ADD, RED_WARP>, a, p, false, s);
+        case NORM_CTA_ROW:
+        case NORM_CTA_SMEM: return launch_persistent(staged_rows_kernel<T, ADD, RED_CTA>, a, p, false, s);
+        case NORM_CTA_PAIR: return launch_persistent(staged_rows_kernel<T, ADD, RED_PAIR>, a, p, true, s);
+        case NORM_TWO_PASS: return launch_persistent(two_pass_kernel<T, vec16<T>(), ADD>, a, p, false, s);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
-template <typename T, int VEC, bool ADD>
-cudaError_t launch_vec(const NormArgs& a, const NormPlan& p, cudaStream_t s) {
+template <typename T, bool ADD>
+cudaError_t launch_scalar(const NormArgs& a, const NormPlan& p, cudaStream_t s) {
     switch (p.variant) {
         case NORM_WARP_ROWS:
             switch (p.nv) {
-                case 1: return launch_persistent(warp_rows_kernel<T, VEC, 1, ADD>, a, p, p.smem, s);
-                case 2: return launch_persistent(warp_rows_kernel<T, VEC, 2, ADD>, a, p, p.smem, s);
-                case 3: return launch_persistent(warp_rows_kernel<T, VEC, 3, ADD>, a, p, p.smem, s);
-                case 4: return launch_persistent(warp_rows_kernel<T, VEC, 4, ADD>, a, p, p.smem, s);
-                case 6: return launch_persistent(warp_rows_kernel<T, VEC, 6, ADD>, a, p, p.smem, s);
-                case 8: return launch_persistent(warp_rows_kernel<T, VEC, 8, ADD>, a, p, p.smem, s);
+                case 1: return launch_persistent(scalar_warp_kernel<T, 1, ADD>, a, p, false, s);
+                case 2: return launch_persistent(scalar_warp_kernel<T, 2, ADD>, a, p, false, s);
+                case 4: return launch_persistent(scalar_warp_kernel<T, 4, ADD>, a, p, false, s);
+                case 8: return launch_persistent(scalar_warp_kernel<T, 8, ADD>, a, p, false, s);
                 default: return cudaErrorInvalidValue;
             }
         case NORM_CTA_ROW:
             switch (p.nv) {
-                case 1: return launch_persistent(cta_row_kernel<T, VEC, 1, ADD>, a, p, p.smem, s);
-                case 2: return launch_persistent(cta_row_kernel<T, VEC, 2, ADD>, a, p, p.smem, s);
-                case 4: return launch_persistent(cta_row_kernel<T, VEC, 4, ADD>, a, p, p.smem, s);
-                case 8: return launch_persistent(cta_row_kernel<T, VEC, 8, ADD>, a, p, p.smem, s);
+                case 1: return launch_persistent(scalar_cta_kernel<T, 1, ADD>, a, p, false, s);
+                case 2: return launch_persistent(scalar_cta_kernel<T, 2, ADD>, a, p, false, s);
+                case 4: return launch_persistent(scalar_cta_kernel<T, 4, ADD>, a, p, false, s);
+                case 8: return launch_persistent(scalar_cta_kernel<T, 8, ADD>, a, p, false, s);
                 default: return cudaErrorInvalidValue;
             }
-        case NORM_CTA_PAIR:
-            switch (p.nv) {
-                case 2: return launch_pair(cta_pair_kernel<T, VEC, 2, ADD>, a, p, p.smem, s);
-                case 4: return launch_pair(cta_pair_kernel<T, VEC, 4, ADD>, a, p, p.smem, s);
-                case 8: return launch_pair(cta_pair_kernel<T, VEC, 8, ADD>, a, p, p.smem, s);
-                default: return cudaErrorInvalidValue;
-            }
-        case NORM_CTA_SMEM:
-            return launch_persistent(cta_wide_kernel<T, VEC, ADD, true>, a, p, p.smem, s);
-        case NORM_TWO_PASS:
-            return launch_persistent(cta_wide_kernel<T, VEC, ADD, false>, a, p, 0, s);
-        default:
-            return cudaErrorInvalidValue;
+        case NORM_TWO_PASS: return launch_persistent(two_pass_kernel<T, 1, ADD>, a, p, false, s);
+        default: return cudaErrorInvalidValue;
     }
 }
 
 template <typename T, bool ADD>
 cudaError_t launch_typed(const NormArgs& a, const NormPlan& p, cudaStream_t s) {
-    if (p.vec == vec16<T>()) return launch_vec<T, vec16<T>(), ADD>(a, p, s);
-    if (p.vec == 1) return launch_vec<T, 1, ADD>(a, p, s);
+    if (p.vec == vec16<T>()) return launch_staged<T, ADD>(a, p, s);
+    if (p.vec == 1) return launch_scalar<T, ADD>(a, p, s);
     return cudaErrorInvalidValue;
 }
 

@@ -125,7 +125,7 @@ cudaError_t launch_typed(const RopeArgs& a, const RopePlan& p, cudaStream_t s) {
     auto kernel = p.pairs == 1 ? token_cta_kernel<T, 1> : token_cta_kernel<T, vec16<T>()>;
     if (p.pairs != 1 && p.pairs != vec16<T>()) return cudaErrorInvalidValue;
     const dim3 grid(persistent_grid(kernel, p.threads, 0, p.num_sms, p.grid));
-    return launch_kernel(kernel, grid, block, 0, s, p.pdl, a);
+    return launch_kernel(kernel, grid, block, 0, s, p.pdl, 1, a);
 }
 
 }  // namespace rope

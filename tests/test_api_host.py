@@ -160,8 +160,10 @@ def test_dispatch_choices(L):
     assert pick("rmsnorm", 512, 2176, dtype=torch.float32, num_sms=152) == 1
     # wide rows, 512 of them on 152 SMs: a 2-CTA cluster per row
     assert pick("rmsnorm", 512, 8192, dtype=torch.float32, num_sms=152) == 4
-    # past the registers of a CTA: staged in shared memory
-    assert pick("rmsnorm", 64, 40000, dtype=torch.bfloat16, num_sms=152) == 2
+    # a wide row and its weights both fit shared memory: CTA per row, w staged
+    assert pick("rmsnorm", 64, 40000, dtype=torch.bfloat16, num_sms=152) == 1
+    # the row fits shared memory, the row plus w does not: w read from L2
+    assert pick("rmsnorm", 64, 70000, dtype=torch.bfloat16, num_sms=152) == 2
     # past shared memory: two-pass
     assert pick("rmsnorm", 2, 10_000_000, dtype=torch.float32, num_sms=152) == 3
     assert pick("glu", 4096, 14336, num_sms=152) == 0
