@@ -67,6 +67,8 @@ def parse():
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--no-companions", action="store_true")
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
+    p.add_argument("--sweep-variants", action="store_true",
+                   help="A/B: time every RMSNorm variant on every norm shape (prints its own JSON)")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-baseline duration")
     return p.parse_args()
 
@@ -695,6 +697,61 @@ def run_gpu(args):
         dist.destroy_process_group()
 
 
+def run_sweep(args):
+    """Streaming time of every RMSNorm variant on every norm shape (dispatch evidence)."""
+    import torch
+
+    import swiglu_rmsnorm_add_gb300 as sra
+
+    dev = torch.device("cuda:0")
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = int(stream.cuda_stream)
+    sra.set_pdl(not args.no_pdl)
+    only = [o for o in args.only.split(",") if o] or ["rmsnorm", "add_rmsnorm"]
+    entries = [e for e in build_entries(dev, sh, only) if e.op in ("rmsnorm", "add_rmsnorm")]
+    if not args.only:
+        entries += [e for e in build_entries(dev, sh, companions=True) if e.op in ("rmsnorm", "add_rmsnorm")]
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
+    peak, _ = measured_peak()
+    nvar = sra.variant_count("rmsnorm")
+    table = []
+    for e in entries:
+        row = {"name": e.name, "bytes": e.bytes, "auto": None, "variants": {}}
+        n = int(min(64, max(1, -(-STREAM_BYTES // max(1, e.bytes)))))
+        calls = e.replicas(n) if n > 1 else [e.launch]
+        for v in [-1] + list(range(nvar)):
+            sra.force_variant("rmsnorm", v)
+            try:
+                for c in calls:
+                    c()
+            except RuntimeError:
+                continue
+            per = []
+            for _ in range(3):
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                flush.fill_(1)
+                flush.sum()
+                torch.cuda._sleep(200000)
+                a.record(stream)
+                for c in calls:
+                    c()
+                b.record(stream)
+                b.synchronize()
+                per.append(a.elapsed_time(b) * 1e3 / len(calls))
+            us = statistics.median(per)
+            rec = {"us": round(us, 3), "frac": round(e.bytes / (us * 1e-6) / 1e9 / peak, 4)}
+            if v < 0:
+                row["auto"] = rec
+            else:
+                row["variants"][sra.variant_name("rmsnorm", v)] = rec
+        sra.force_variant("rmsnorm", -1)
+        del calls
+        table.append(row)
+    print(json.dumps({"variant_sweep": table, "peak_gbs": peak, "timing": "back-to-back launches over rotating "
+                      "copies (>= 512 MiB), median of 3, us per launch"}), flush=True)
+
+
 def run_reference(args):
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
@@ -726,5 +783,7 @@ if __name__ == "__main__":
     a = parse()
     if a.impl == "reference":
         run_reference(a)
+    elif a.sweep_variants:
+        run_sweep(a)
     else:
         run_gpu(a)

@@ -156,66 +156,120 @@ bool plan_norm_scalar(int variant, int64_t rows, int64_t D, int num_sms, NormPla
     }
 }
 
-// Threads for `acc` 16-byte accesses of one row slice: few rows (decode) get one
-// access per thread; many rows about four, so more rows are resident.
+// Threads for `acc` 16-byte accesses of one row slice in the staged kernels: few
+// rows (decode) get one access per thread; many rows eight, so CTAs stay small
+// and many of them are resident.
 int staged_threads(int64_t acc, bool few_rows) {
-    const int64_t per = few_rows ? 1 : 4;
+    const int64_t per = few_rows ? 1 : 8;
     return static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(ceil_div(acc, per)))));
 }
 
-bool plan_norm_staged(int variant, int64_t rows, int64_t D, int vec, int es, bool add, int num_sms,
-                      const SmemBudget& b, NormPlan* p) {
+// Register kernels: NV accesses per thread and threads for `nacc` accesses over
+// one CTA. Few rows favour many threads with short chains; many rows four
+// accesses per thread.
+constexpr int kCtaMaxAccesses = 2048;  // 256 threads x 8, 512 x 4, 1024 x 2
+int cta_max_threads_for_nv(int nv) { return nv >= 8 ? 256 : (nv >= 4 ? 512 : 1024); }
+bool cta_shape(int64_t nacc, bool few_rows, int min_nv, int* nv_out, int* threads_out) {
+    int nv = std::max(min_nv, few_rows ? 1 : 4);
+    while (nv < 8 && ceil_div(nacc, nv) > cta_max_threads_for_nv(nv)) nv <<= 1;
+    while (nv > min_nv && ceil_div(nacc, nv) < 64) nv >>= 1;
+    if (ceil_div(nacc, nv) > cta_max_threads_for_nv(nv)) return false;
+    *nv_out = nv;
+    *threads_out = std::max(32, round_up32(ceil_div(nacc, nv)));
+    return true;
+}
+
+// Warps per CTA for warp-per-row kernels: the smallest per-SM row load when CTAs
+// are dealt evenly (ties to larger CTAs).
+int balanced_wpc(int64_t rows, int num_sms) {
+    int best = 8;
+    int64_t best_load = -1;
+    for (int wpc : {8, 4, 2, 1}) {
+        const int64_t load = ceil_div(ceil_div(rows, wpc), num_sms) * wpc;
+        if (best_load < 0 || load < best_load) best_load = load, best = wpc;
+    }
+    return best;
+}
+
+bool plan_norm_vector(int variant, int64_t rows, int64_t D, int vec, bool add, int num_sms, const SmemBudget& b,
+                      NormPlan* p) {
     const int64_t nvec = D / vec;
-    const int copies = add ? 2 : 1;  // x (and res) slices per group
+    const int64_t nacc = ceil_div(D, vec);  // accesses per row, tail included
+    const int copies = add ? 2 : 1;         // x (and res) slices per group, staged kernels
     const bool few_rows = rows < 2LL * num_sms;
-    (void)es;
     switch (variant) {
         case NORM_WARP_ROWS: {
-            if (ceil_div(D, vec) > 256) return false;
+            const int64_t per_lane = ceil_div(nacc, 32);
+            if (per_lane > 8) return false;
+            int nv = 8;
+            for (int c : {1, 2, 3, 4, 6, 8}) {
+                if (c >= per_lane) {
+                    nv = c;
+                    break;
+                }
+            }
+            const int wpc = balanced_wpc(rows, num_sms);
+            p->nv = nv;
+            p->threads = 32 * wpc;
+            p->grid = std::max<int64_t>(1, ceil_div(rows, wpc));
+            return true;
+        }
+        case NORM_CTA_ROW:
+            if (nacc > kCtaMaxAccesses) return false;
+            if (!cta_shape(nacc, few_rows, 1, &p->nv, &p->threads)) return false;
+            p->grid = std::max<int64_t>(1, rows);
+            return true;
+        case NORM_CTA_PAIR: {
+            if (nvec < 2) return false;
+            const int64_t half = norm_pair_half(nvec);
+            const int64_t per_cta = std::max<int64_t>(half, nacc - half);
+            if (per_cta > kCtaMaxAccesses) return false;
+            if (!cta_shape(per_cta, few_rows, 2, &p->nv, &p->threads)) return false;
+            p->grid = 2 * std::max<int64_t>(1, rows);
+            return true;
+        }
+        case NORM_WARP_SMEM: {
+            if (nacc > 256) return false;
             const size_t slice = round_up16(nvec * 16);
             // Warps per CTA: the smallest per-SM row load that is resident in one
-            // round (shared memory and the 64-warp limit); ties go to larger CTAs.
+            // round (shared memory, threads); ties go to larger CTAs.
             int best = 0;
             int64_t best_load = 0, best_cap = 0;
             for (int wpc : {8, 4, 2, 1}) {
                 const size_t smem = slice + wpc * slice * copies;
                 if (static_cast<int64_t>(smem) > b.per_cta) continue;
-                const int64_t cap = resident_by_smem(b, smem, 32 * wpc) * wpc;  // rows per SM in one round
+                const int64_t cap = resident_by_smem(b, smem, 32 * wpc) * wpc;
                 const int64_t load = ceil_div(ceil_div(rows, wpc), num_sms) * wpc;
                 const bool fits = load <= cap;
                 const bool best_fits = best && best_load <= best_cap;
-                if (!best || (fits && (!best_fits || load < best_load)) || (!fits && !best_fits && cap > best_cap)) {
+                if (!best || (fits && (!best_fits || load < best_load)) || (!fits && !best_fits && cap > best_cap))
                     best = wpc, best_load = load, best_cap = cap;
-                }
             }
             if (!best) return false;
-            p->nv = 0;
             p->threads = 32 * best;
             p->grid = std::max<int64_t>(1, ceil_div(rows, best));
             p->smem = slice + best * slice * copies;
             p->stage_w = 1;
             return true;
         }
-        case NORM_CTA_ROW:
         case NORM_CTA_SMEM: {
             const size_t slice = round_up16(nvec * 16);
-            const bool stage = variant == NORM_CTA_ROW;
+            // stage w beside the row when both fit, else read it from L2
+            const bool stage = static_cast<int64_t>(slice + slice * copies) <= b.per_cta;
             const size_t smem = (stage ? slice : 0) + slice * copies;
             if (static_cast<int64_t>(smem) > b.per_cta) return false;
-            p->nv = 0;
             p->threads = staged_threads(nvec, few_rows);
             p->grid = std::max<int64_t>(1, rows);
             p->smem = smem;
             p->stage_w = stage ? 1 : 0;
             return true;
         }
-        case NORM_CTA_PAIR: {
+        case NORM_PAIR_SMEM: {
             if (nvec < 2) return false;
             const int64_t half = norm_pair_half(nvec);
             const size_t slice = round_up16(half * 16);
             const size_t smem = slice + slice * copies;
             if (static_cast<int64_t>(smem) > b.per_cta) return false;
-            p->nv = 0;
             p->threads = staged_threads(half, few_rows);
             p->grid = 2 * std::max<int64_t>(1, rows);
             p->smem = smem;
@@ -223,8 +277,7 @@ bool plan_norm_staged(int variant, int64_t rows, int64_t D, int vec, int es, boo
             return true;
         }
         case NORM_TWO_PASS:
-            p->nv = 0;
-            p->threads = static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(ceil_div(D, vec)))));
+            p->threads = static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(nacc))));
             p->grid = std::max<int64_t>(1, rows);
             return true;
         default:
@@ -232,39 +285,37 @@ bool plan_norm_staged(int variant, int64_t rows, int64_t D, int vec, int es, boo
     }
 }
 
-bool plan_norm_variant(int variant, int64_t rows, int64_t D, int vec, int es, bool add, int num_sms,
-                       const SmemBudget& b, NormPlan* p) {
+bool plan_norm_variant(int variant, int64_t rows, int64_t D, int vec, bool add, int num_sms, const SmemBudget& b,
+                       NormPlan* p) {
     p->variant = variant;
     p->vec = vec;
+    p->nv = 0;
     p->smem = 0;
     p->pdl = g_pdl;
     p->num_sms = num_sms;
     p->stage_w = 0;
     if (vec == 1) return plan_norm_scalar(variant, rows, D, num_sms, p);
-    return plan_norm_staged(variant, rows, D, vec, es, add, num_sms, b, p);
+    return plan_norm_vector(variant, rows, D, vec, add, num_sms, b, p);
 }
 
-// Automatic choice, in order of preference for the shape.
-int plan_norm(int64_t rows, int64_t D, int dt, int vec, bool add, int num_sms, const SmemBudget& b, NormPlan* p) {
-    const int es = elem_bytes(dt);
+// Automatic choice: the preferred variants for the shape, in order.
+int plan_norm(int64_t rows, int64_t D, int vec, bool add, int num_sms, const SmemBudget& b, NormPlan* p) {
     const int forced = g_force_norm.load(std::memory_order_relaxed);
     if (forced >= 0) {
-        if (!plan_norm_variant(forced, rows, D, vec, es, add, num_sms, b, p)) return SRA_ERR_VARIANT;
+        if (!plan_norm_variant(forced, rows, D, vec, add, num_sms, b, p)) return SRA_ERR_VARIANT;
         return SRA_OK;
     }
     const int64_t nacc = ceil_div(D, vec);
-    int order[5];
+    const bool few_rows = rows < 2LL * num_sms;
+    int order[6];
     int n = 0;
-    // Short rows and many of them: a warp per row.
-    if (nacc <= 256 && (rows >= 256 || nacc <= 64)) order[n++] = NORM_WARP_ROWS;
-    // Wide rows, more rows than SMs but too few to spread evenly one per CTA:
-    // split each row over a CTA pair.
-    if (nacc >= 1024 && rows >= 2LL * num_sms && rows < 16LL * num_sms) order[n++] = NORM_CTA_PAIR;
+    if (!few_rows && nacc <= 256 && (rows >= 256 || nacc <= 64)) order[n++] = NORM_WARP_ROWS;
+    if (!few_rows && nacc >= 1024 && rows < 16LL * num_sms) order[n++] = NORM_CTA_PAIR;
     order[n++] = NORM_CTA_ROW;
     order[n++] = NORM_CTA_SMEM;
     order[n++] = NORM_TWO_PASS;
     for (int i = 0; i < n; ++i) {
-        if (plan_norm_variant(order[i], rows, D, vec, es, add, num_sms, b, p)) return SRA_OK;
+        if (plan_norm_variant(order[i], rows, D, vec, add, num_sms, b, p)) return SRA_OK;
     }
     return SRA_ERR_VARIANT;
 }
@@ -366,7 +417,7 @@ int norm_common(void* x, const void* res, const void* w, void* out, int64_t rows
     SmemBudget budget;
     budget.per_cta = smem_optin(dev) - 1024;
     budget.per_sm = smem_per_sm(dev);
-    int st = plan_norm(rows, D, dtype, vec, add, sms, budget, &plan);
+    int st = plan_norm(rows, D, vec, add, sms, budget, &plan);
     if (st != SRA_OK) return st;
     NormArgs a;
     a.x = x;
@@ -545,7 +596,8 @@ int sra_force_variant(const char* op, int variant) {
 int sra_variant_count(const char* op) { return variant_count(op); }
 
 const char* sra_variant_name(const char* op, int variant) {
-    static const char* const norm_names[] = {"warp_rows", "cta_row", "cta_smem", "two_pass", "cta_pair"};
+    static const char* const norm_names[] = {"warp_rows", "cta_row",   "cta_smem", "two_pass",
+                                             "cta_pair",  "warp_smem", "pair_smem"};
     static const char* const rope_names[] = {"token_cta"};
     static const char* const glu_names[] = {"cols_rows"};
     const int n = variant_count(op);
@@ -569,7 +621,7 @@ int sra_pick_variant(const char* op, int64_t a, int64_t b, int64_t c, int64_t d,
         SmemBudget budget;
         budget.per_cta = 227 * 1024 - 1024;
         budget.per_sm = 228 * 1024;
-        const int st = plan_norm(a, b, dtype, 16 / es, false, num_sms, budget, &p);
+        const int st = plan_norm(a, b, 16 / es, false, num_sms, budget, &p);
         return st == SRA_OK ? p.variant : st;
     }
     if (std::strcmp(op, "rope_kv_store") == 0) {

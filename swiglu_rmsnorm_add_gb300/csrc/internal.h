@@ -26,10 +26,12 @@ struct NormArgs {
 enum NormVariant {
     NORM_WARP_ROWS = 0,  // one warp per row, row held in registers
     NORM_CTA_ROW = 1,    // one CTA per row, row held in registers
-    NORM_CTA_SMEM = 2,   // one CTA per row, row staged in shared memory
+    NORM_CTA_SMEM = 2,   // one CTA per row, row landed in shared memory (cp.async)
     NORM_TWO_PASS = 3,   // one CTA per row, second pass re-reads the row (any D)
     NORM_CTA_PAIR = 4,   // a 2-CTA cluster per row, half the row in each CTA's registers
-    NORM_NUM_VARIANTS = 5
+    NORM_WARP_SMEM = 5,  // one warp per row, row landed in shared memory (cp.async)
+    NORM_PAIR_SMEM = 6,  // a 2-CTA cluster per row, half the row in each CTA's shared memory
+    NORM_NUM_VARIANTS = 7
 };
 
 #ifdef __CUDACC__

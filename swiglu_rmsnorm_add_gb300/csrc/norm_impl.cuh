@@ -8,22 +8,20 @@
 // page, section 4) first stores x <- round(x + res) in place and normalises the
 // rounded sum, reading each row once and writing it twice.
 //
-// Variants (chosen per shape by the host planner):
-//   warp_rows  a warp per row              (short rows, many of them)
-//   cta_row    a CTA per row, w staged     (long rows, or few rows: decode)
-//   cta_smem   a CTA per row, w from L2    (rows too wide to stage w beside them)
+// Variants (chosen per shape by the host planner; 16-byte layouts):
+//   warp_rows  a warp per row, the row in registers          (short rows, many)
+//   cta_row    a CTA per row, the row in registers           (long rows; decode)
+//   cta_pair   a 2-CTA cluster per row, half the row in each CTA's registers;
+//              the partial sums of squares meet through distributed shared
+//              memory (wide rows that one CTA per row cannot spread evenly)
+//   warp_smem, cta_smem, pair_smem
+//              the same three row groupings with the row landed in shared memory
+//              by cp.async (16-byte asynchronous copies that hold no registers in
+//              flight; cp.async.wait_all is a hardware wait, not a software spin),
+//              the weight slice copied in the same round trip; the resident row
+//              count is then bounded by shared memory instead of registers
 //   two_pass   a CTA per row, the scale pass re-reads the row (any width)
-//   cta_pair   a 2-CTA cluster per row: each CTA takes half the row and the two
-//              partial sums of squares meet through distributed shared memory
-//              (wide rows when one CTA per row cannot spread evenly over the SMs)
-//
-// 16-byte layouts (the normal case) use the staged kernel: every row lands in
-// shared memory through cp.async (16-byte asynchronous copies that hold no
-// registers while in flight; cp.async.wait_all is a hardware wait, not a
-// software spin). The copies of the weight slice and of the first row are
-// issued together, so a row costs one memory round trip; the resident row count
-// is then bounded by shared memory (about the row's bytes), not by registers.
-// Layouts that are not 16-byte aligned use register kernels with scalar access.
+// Layouts that are not 16-byte aligned use scalar register kernels.
 // A predicated scalar tail covers D % VEC; nothing is padded to a power of two.
 // Every thread reads back and writes only its own elements, so in-place use
 // (out == x) is safe. Each translation unit instantiates one ADD value only
@@ -103,7 +101,8 @@ __global__ void __launch_bounds__(1024) staged_rows_kernel(NormArgs a) {
     }
     int64_t r0, step;
     if constexpr (RED == RED_WARP) {
-        r0 = static_cast<int64_t>(blockIdx.x) * groups + group, step = static_cast<int64_t>(gridDim.x) * groups;
+        // rows dealt to CTAs round-robin: CTAs (and SMs) differ by one row at most
+        r0 = static_cast<int64_t>(group) * gridDim.x + blockIdx.x, step = static_cast<int64_t>(gridDim.x) * groups;
     } else if constexpr (RED == RED_CTA) {
         r0 = blockIdx.x, step = gridDim.x;
     } else {
@@ -200,6 +199,146 @@ __global__ void __launch_bounds__(1024) staged_rows_kernel(NormArgs a) {
     if constexpr (RED == RED_PAIR) {
         cg::this_cluster().sync();  // no CTA exits while its peer may still read its pair_slot
     }
+}
+
+// ------------------------------------------------------------------ registers
+// 16-byte accesses, the row (or the CTA's half of it) in registers: thread tid
+// of the group owns accesses idx = a0 + v * threads + tid, v < NV. The weights
+// are loaded once the residual sum is formed, so their latency hides behind
+// the reduction and their registers reuse the residual's.
+template <typename T, int NV, bool ADD, int RED>
+__device__ __forceinline__ void reg_row(const NormArgs& a, int64_t r, int tid, int threads, int64_t a0, int64_t a1,
+                                        bool tail_owner, float* scratch, float* pair_slot, int parity) {
+    constexpr int VEC = vec16<T>();
+    using V = Vec<T, VEC>;
+    using R = typename V::Raw;
+    const int64_t nvec = a.D / VEC;
+    const int tail = tail_owner ? static_cast<int>(a.D - nvec * VEC) : 0;
+    const T* w = static_cast<const T*>(a.w);
+    T* xr = static_cast<T*>(a.x) + r * a.xs;
+    T* orow = static_cast<T*>(a.out) + r * a.os;
+
+    R xv[NV];
+    float xt = 0.0f, wt = 0.0f;
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int64_t idx = a0 + static_cast<int64_t>(v) * threads + tid;
+        if (idx < a1) xv[v] = V::load(xr + idx * VEC);
+    }
+    if (tid < tail) xt = to_f32(xr[nvec * VEC + tid]);
+
+    float ss = 0.0f;
+    if constexpr (ADD) {
+        const T* rr = static_cast<const T*>(a.res) + r * a.rs;
+        R rv[NV];
+        float rt = 0.0f;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int64_t idx = a0 + static_cast<int64_t>(v) * threads + tid;
+            if (idx < a1) rv[v] = V::load(rr + idx * VEC);
+        }
+        if (tid < tail) rt = to_f32(rr[nvec * VEC + tid]);
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int64_t idx = a0 + static_cast<int64_t>(v) * threads + tid;
+            if (idx < a1) {
+                float xf[VEC], rf[VEC];
+                V::unpack(xv[v], xf);
+                V::unpack(rv[v], rf);
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) xf[i] += rf[i];
+                xv[v] = V::pack(xf);  // the rounded sum
+                V::store(xr + idx * VEC, xv[v]);
+                V::unpack(xv[v], xf);
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) ss = fmaf(xf[i], xf[i], ss);
+            }
+        }
+        if (tid < tail) {
+            const T s = from_f32<T>(xt + rt);
+            xr[nvec * VEC + tid] = s;
+            xt = to_f32(s);
+            ss = fmaf(xt, xt, ss);
+        }
+    } else {
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            const int64_t idx = a0 + static_cast<int64_t>(v) * threads + tid;
+            if (idx < a1) {
+                float xf[VEC];
+                V::unpack(xv[v], xf);
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) ss = fmaf(xf[i], xf[i], ss);
+            }
+        }
+        if (tid < tail) ss = fmaf(xt, xt, ss);
+    }
+
+    R wv[NV];
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int64_t idx = a0 + static_cast<int64_t>(v) * threads + tid;
+        if (idx < a1) wv[v] = V::load(w + idx * VEC);
+    }
+    if (tid < tail) wt = to_f32(w[nvec * VEC + tid]);
+
+    ss = group_sum<RED>(ss, scratch, pair_slot, parity);
+    const float rinv = rsqrtf(ss / static_cast<float>(a.D) + a.eps);
+
+#pragma unroll
+    for (int v = 0; v < NV; ++v) {
+        const int64_t idx = a0 + static_cast<int64_t>(v) * threads + tid;
+        if (idx < a1) {
+            float xf[VEC], wf[VEC];
+            V::unpack(xv[v], xf);
+            V::unpack(wv[v], wf);
+#pragma unroll
+            for (int i = 0; i < VEC; ++i) xf[i] = xf[i] * rinv * wf[i];
+            V::store(orow + idx * VEC, V::pack(xf));
+        }
+    }
+    if (tid < tail) orow[nvec * VEC + tid] = from_f32<T>(xt * rinv * wt);
+}
+
+template <typename T, int NV, bool ADD>
+__global__ void __launch_bounds__(256) reg_warp_kernel(NormArgs a) {
+    pdl_enter();
+    const int wpc = blockDim.x >> 5;
+    const int64_t nvec = a.D / vec16<T>();
+    // Rows are dealt to CTAs round-robin, so CTAs (and SMs) differ by one row at most.
+    const int64_t step = static_cast<int64_t>(gridDim.x) * wpc;
+    for (int64_t r = static_cast<int64_t>(threadIdx.x >> 5) * gridDim.x + blockIdx.x; r < a.rows; r += step)
+        reg_row<T, NV, ADD, RED_WARP>(a, r, threadIdx.x & 31, 32, 0, nvec, true, nullptr, nullptr, 0);
+}
+
+// Largest CTA the register-resident CTA variants are compiled for, per NV.
+template <int NV> constexpr int cta_row_max_threads() { return NV >= 8 ? 256 : (NV >= 4 ? 512 : 1024); }
+
+template <typename T, int NV, bool ADD>
+__global__ void __launch_bounds__(cta_row_max_threads<NV>()) reg_cta_kernel(NormArgs a) {
+    __shared__ float scratch[33];
+    pdl_enter();
+    const int64_t nvec = a.D / vec16<T>();
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
+        reg_row<T, NV, ADD, RED_CTA>(a, r, threadIdx.x, blockDim.x, 0, nvec, true, scratch, nullptr, 0);
+}
+
+template <typename T, int NV, bool ADD>
+__global__ void __launch_bounds__(cta_row_max_threads<NV>()) reg_pair_kernel(NormArgs a) {
+    __shared__ float scratch[33];
+    __shared__ float pair_slot[2];
+    pdl_enter();
+    const int rank = static_cast<int>(cg::this_cluster().block_rank());
+    const int64_t nvec = a.D / vec16<T>();
+    const int64_t half = norm_pair_half(nvec);
+    const int64_t a0 = rank == 0 ? 0 : half;
+    const int64_t a1 = rank == 0 ? half : nvec;
+    int parity = 0;
+    for (int64_t r = blockIdx.x / 2; r < a.rows; r += gridDim.x / 2) {
+        reg_row<T, NV, ADD, RED_PAIR>(a, r, threadIdx.x, blockDim.x, a0, a1, rank == 1, scratch, pair_slot, parity);
+        parity ^= 1;
+    }
+    cg::this_cluster().sync();  // no CTA exits while its peer may still read its pair_slot
 }
 
 // ------------------------------------------------------------------ registers
@@ -327,7 +466,8 @@ __global__ void __launch_bounds__(1024) two_pass_kernel(NormArgs a) {
 // ------------------------------------------------------------------ launch
 template <typename KArgs>
 cudaError_t smem_opt_in(void (*kernel)(KArgs), size_t smem) {
-    if (smem <= 48 * 1024) return cudaSuccess;
+    // The static shared memory counts against the 48 KB default too.
+    if (smem <= 32 * 1024) return cudaSuccess;
     return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
 }
 
@@ -345,12 +485,36 @@ cudaError_t launch_persistent(void (*kernel)(KArgs), const NormArgs& a, const No
 }
 
 template <typename T, bool ADD>
-cudaError_t launch_staged(const NormArgs& a, const NormPlan& p, cudaStream_t s) {
+cudaError_t launch_vector(const NormArgs& a, const NormPlan& p, cudaStream_t s) {
     switch (p.variant) {
-        case NORM_WARP_ROWS: return launch_persistent(staged_rows_kernel<T, ADD, RED_WARP>, a, p, false, s);
+        case NORM_WARP_ROWS:
+            switch (p.nv) {
+                case 1: return launch_persistent(reg_warp_kernel<T, 1, ADD>, a, p, false, s);
+                case 2: return launch_persistent(reg_warp_kernel<T, 2, ADD>, a, p, false, s);
+                case 3: return launch_persistent(reg_warp_kernel<T, 3, ADD>, a, p, false, s);
+                case 4: return launch_persistent(reg_warp_kernel<T, 4, ADD>, a, p, false, s);
+                case 6: return launch_persistent(reg_warp_kernel<T, 6, ADD>, a, p, false, s);
+                case 8: return launch_persistent(reg_warp_kernel<T, 8, ADD>, a, p, false, s);
+                default: return cudaErrorInvalidValue;
+            }
         case NORM_CTA_ROW:
+            switch (p.nv) {
+                case 1: return launch_persistent(reg_cta_kernel<T, 1, ADD>, a, p, false, s);
+                case 2: return launch_persistent(reg_cta_kernel<T, 2, ADD>, a, p, false, s);
+                case 4: return launch_persistent(reg_cta_kernel<T, 4, ADD>, a, p, false, s);
+                case 8: return launch_persistent(reg_cta_kernel<T, 8, ADD>, a, p, false, s);
+                default: return cudaErrorInvalidValue;
+            }
+        case NORM_CTA_PAIR:
+            switch (p.nv) {
+                case 2: return launch_persistent(reg_pair_kernel<T, 2, ADD>, a, p, true, s);
+                case 4: return launch_persistent(reg_pair_kernel<T, 4, ADD>, a, p, true, s);
+                case 8: return launch_persistent(reg_pair_kernel<T, 8, ADD>, a, p, true, s);
+                default: return cudaErrorInvalidValue;
+            }
+        case NORM_WARP_SMEM: return launch_persistent(staged_rows_kernel<T, ADD, RED_WARP>, a, p, false, s);
         case NORM_CTA_SMEM: return launch_persistent(staged_rows_kernel<T, ADD, RED_CTA>, a, p, false, s);
-        case NORM_CTA_PAIR: return launch_persistent(staged_rows_kernel<T, ADD, RED_PAIR>, a, p, true, s);
+        case NORM_PAIR_SMEM: return launch_persistent(staged_rows_kernel<T, ADD, RED_PAIR>, a, p, true, s);
         case NORM_TWO_PASS: return launch_persistent(two_pass_kernel<T, vec16<T>(), ADD>, a, p, false, s);
         default: return cudaErrorInvalidValue;
     }
@@ -382,7 +546,7 @@ cudaError_t launch_scalar(const NormArgs& a, const NormPlan& p, cudaStream_t s) 
 
 template <typename T, bool ADD>
 cudaError_t launch_typed(const NormArgs& a, const NormPlan& p, cudaStream_t s) {
-    if (p.vec == vec16<T>()) return launch_staged<T, ADD>(a, p, s);
+    if (p.vec == vec16<T>()) return launch_vector<T, ADD>(a, p, s);
     if (p.vec == 1) return launch_scalar<T, ADD>(a, p, s);
     return cudaErrorInvalidValue;
 }

@@ -134,14 +134,14 @@ def test_glu_validation(L):
 
 
 def test_variant_control(L):
-    assert sra.variant_count("rmsnorm") == 5
+    assert sra.variant_count("rmsnorm") == 7
     assert sra.variant_count("rope_kv_store") == 1
     assert sra.variant_count("glu") == 1
     assert sra.variant_count("nope") == ARG
-    assert [sra.variant_name("rmsnorm", i) for i in range(5)] == ["warp_rows", "cta_row", "cta_smem", "two_pass",
-                                                                  "cta_pair"]
-    assert sra.variant_name("rmsnorm", 5) is None
-    assert L.sra_force_variant(b"rmsnorm", 5) == ARG
+    assert [sra.variant_name("rmsnorm", i) for i in range(7)] == ["warp_rows", "cta_row", "cta_smem", "two_pass",
+                                                                  "cta_pair", "warp_smem", "pair_smem"]
+    assert sra.variant_name("rmsnorm", 7) is None
+    assert L.sra_force_variant(b"rmsnorm", 7) == ARG
     assert L.sra_force_variant(b"bogus", 0) == ARG
     assert L.sra_force_variant(b"rmsnorm", 2) == OK
     assert sra.pick_variant("rmsnorm", 512, 1536, num_sms=152) == 2
@@ -156,14 +156,13 @@ def test_dispatch_choices(L):
     assert pick("rmsnorm", 4096, 1536, dtype=torch.bfloat16, num_sms=152) == 0
     # decode (few rows) of the 1536-wide hidden state: a CTA per row
     assert pick("rmsnorm", 1, 1536, dtype=torch.bfloat16, num_sms=152) == 1
+    assert pick("rmsnorm", 64, 1536, dtype=torch.bfloat16, num_sms=152) == 1
     # a row past a warp's registers: CTA per row
     assert pick("rmsnorm", 512, 2176, dtype=torch.float32, num_sms=152) == 1
     # wide rows, 512 of them on 152 SMs: a 2-CTA cluster per row
     assert pick("rmsnorm", 512, 8192, dtype=torch.float32, num_sms=152) == 4
-    # a wide row and its weights both fit shared memory: CTA per row, w staged
-    assert pick("rmsnorm", 64, 40000, dtype=torch.bfloat16, num_sms=152) == 1
-    # the row fits shared memory, the row plus w does not: w read from L2
-    assert pick("rmsnorm", 64, 70000, dtype=torch.bfloat16, num_sms=152) == 2
+    # past a CTA's registers: the row landed in shared memory
+    assert pick("rmsnorm", 64, 40000, dtype=torch.bfloat16, num_sms=152) == 2
     # past shared memory: two-pass
     assert pick("rmsnorm", 2, 10_000_000, dtype=torch.float32, num_sms=152) == 3
     assert pick("glu", 4096, 14336, num_sms=152) == 0
