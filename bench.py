@@ -720,7 +720,14 @@ def run_sweep(args):
         row = {"name": e.name, "bytes": e.bytes, "auto": None, "variants": {}}
         n = int(min(64, max(1, -(-STREAM_BYTES // max(1, e.bytes)))))
         calls = e.replicas(n) if n > 1 else [e.launch]
-        for v in [-1] + list(range(nvar)):
+        settings = [(-1, "auto")]
+        for v in range(nvar):
+            nm = sra.variant_name("rmsnorm", v)
+            if nm in ("warp_rows", "cta_row", "cta_pair"):
+                settings += [(v | (nv << 8), f"{nm}/nv{nv}") for nv in (1, 2, 3, 4, 6, 8)]
+            else:
+                settings.append((v, nm))
+        for v, label in settings:
             sra.force_variant("rmsnorm", v)
             try:
                 for c in calls:
@@ -744,7 +751,7 @@ def run_sweep(args):
             if v < 0:
                 row["auto"] = rec
             else:
-                row["variants"][sra.variant_name("rmsnorm", v)] = rec
+                row["variants"][label] = rec
         sra.force_variant("rmsnorm", -1)
         del calls
         table.append(row)

@@ -211,8 +211,10 @@ SRA_API int sra_set_pdl(int enable);
  * Kernel-variant control, for A/B measurement of the per-shape dispatch.
  * op: "rmsnorm" (also used by add_rmsnorm), "rope_kv_store", "glu".
  * variant: -1 = automatic per-shape choice (the default); otherwise an index
- * < sra_variant_count(op). A forced variant that cannot serve a later call makes
- * that call return SRA_ERR_VARIANT without enqueueing anything.
+ * < sra_variant_count(op), optionally OR-ed with (nv << 8) to also force the
+ * number of 16-byte accesses each thread holds in the register variants of
+ * "rmsnorm" (nv in 1, 2, 3, 4, 6, 8). A forced setting that cannot serve a later
+ * call makes that call return SRA_ERR_VARIANT without enqueueing anything.
  * Returns SRA_OK, or SRA_ERR_ARG for an unknown op or out-of-range variant.
  */
 SRA_API int sra_force_variant(const char* op, int variant);

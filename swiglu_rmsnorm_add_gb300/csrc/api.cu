@@ -20,6 +20,7 @@ std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_smem_optin[kMaxDevices];
 std::atomic<int> g_force_norm{-1}, g_force_rope{-1}, g_force_glu{-1};
 thread_local bool g_pdl = false;  // programmatic dependent launch for this thread's calls
+thread_local int g_force_nv = 0;  // accesses per thread forced for A/B measurement (0 = planner's)
 
 // SM count of the current device (cached per device).
 int current_sm_count(int* dev_out) {
@@ -170,6 +171,13 @@ int staged_threads(int64_t acc, bool few_rows) {
 constexpr int kCtaMaxAccesses = 2048;  // 256 threads x 8, 512 x 4, 1024 x 2
 int cta_max_threads_for_nv(int nv) { return nv >= 8 ? 256 : (nv >= 4 ? 512 : 1024); }
 bool cta_shape(int64_t nacc, bool few_rows, int min_nv, int* nv_out, int* threads_out) {
+    if (g_force_nv) {
+        const int nv = g_force_nv;
+        if ((nv & (nv - 1)) || nv < min_nv || nv > 8 || ceil_div(nacc, nv) > cta_max_threads_for_nv(nv)) return false;
+        *nv_out = nv;
+        *threads_out = std::max(32, round_up32(ceil_div(nacc, nv)));
+        return true;
+    }
     int nv = std::max(min_nv, few_rows ? 1 : 4);
     while (nv < 8 && ceil_div(nacc, nv) > cta_max_threads_for_nv(nv)) nv <<= 1;
     while (nv > min_nv && ceil_div(nacc, nv) < 64) nv >>= 1;
@@ -203,11 +211,12 @@ bool plan_norm_vector(int variant, int64_t rows, int64_t D, int vec, bool add, i
             if (per_lane > 8) return false;
             int nv = 8;
             for (int c : {1, 2, 3, 4, 6, 8}) {
-                if (c >= per_lane) {
+                if (c >= per_lane && (g_force_nv == 0 || c == g_force_nv)) {
                     nv = c;
                     break;
                 }
             }
+            if (nv < per_lane || (g_force_nv && nv != g_force_nv)) return false;
             const int wpc = balanced_wpc(rows, num_sms);
             p->nv = nv;
             p->threads = 32 * wpc;
@@ -302,8 +311,10 @@ bool plan_norm_variant(int variant, int64_t rows, int64_t D, int vec, bool add, 
 int plan_norm(int64_t rows, int64_t D, int vec, bool add, int num_sms, const SmemBudget& b, NormPlan* p) {
     const int forced = g_force_norm.load(std::memory_order_relaxed);
     if (forced >= 0) {
-        if (!plan_norm_variant(forced, rows, D, vec, add, num_sms, b, p)) return SRA_ERR_VARIANT;
-        return SRA_OK;
+        g_force_nv = (forced >> 8) & 0xFF;
+        const bool ok = plan_norm_variant(forced & 0xFF, rows, D, vec, add, num_sms, b, p);
+        g_force_nv = 0;
+        return ok ? SRA_OK : SRA_ERR_VARIANT;
     }
     const int64_t nacc = ceil_div(D, vec);
     const bool few_rows = rows < 2LL * num_sms;
@@ -588,7 +599,7 @@ int sra_swiglu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_
 int sra_force_variant(const char* op, int variant) {
     std::atomic<int>* slot = force_slot(op);
     if (!slot) return SRA_ERR_ARG;
-    if (variant < -1 || variant >= variant_count(op)) return SRA_ERR_ARG;
+    if (variant < -1 || (variant & 0xFF) >= variant_count(op) || (variant >> 16) != 0) return SRA_ERR_ARG;
     slot->store(variant, std::memory_order_relaxed);
     return SRA_OK;
 }

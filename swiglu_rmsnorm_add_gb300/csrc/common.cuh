@@ -63,6 +63,24 @@ __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Hint the L2 to fetch [p, p + bytes) (p 16-byte aligned, bytes a multiple of 16;
+// anything else is ignored). Issued before pdl_enter() for a CTA's own input
+// rows: with programmatic dependent launch the CTA runs while the previous
+// kernel drains, so the first DRAM round trip overlaps that tail. The L2 is the
+// point of coherence and a prefetch has no semantic effect, so data the
+// previous kernel is still writing is read correctly after the wait.
+__device__ __forceinline__ void prefetch_l2(const void* p, int64_t bytes) {
+    if (bytes < 16 || (reinterpret_cast<uintptr_t>(p) & 15u) != 0) return;
+    bytes &= ~static_cast<int64_t>(15);
+    const char* c = static_cast<const char*>(p);
+    constexpr int64_t kMax = int64_t(1) << 20;  // one instruction per MiB
+    for (int64_t off = 0; off < bytes; off += kMax) {
+        const int64_t n = bytes - off < kMax ? bytes - off : kMax;
+        asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(c + off), "r"(static_cast<unsigned>(n))
+                     : "memory");
+    }
+}
+
 // Launch `kernel` on `stream`, with programmatic stream serialization when
 // `pdl` is set (the kernel may then be scheduled while the previous kernel in
 // the stream finishes; pdl_enter() orders its memory accesses after it).

@@ -49,8 +49,19 @@ template <typename T, int VEC, int ACT>
 __global__ void __launch_bounds__(256) cols_rows_kernel(GluArgs a) {
     using V = Vec<T, VEC>;
     using R = typename V::Raw;
-    pdl_enter();
     const int64_t nv = a.I / VEC;
+    if (threadIdx.x == 0) {
+        // this CTA's column segment of its first two rows, gate and up
+        const int64_t j0 = static_cast<int64_t>(blockIdx.x) * blockDim.x;
+        const int64_t cols = (nv - j0 < blockDim.x ? nv - j0 : blockDim.x) * VEC;
+        for (int64_t t = blockIdx.y; t < a.T && t < blockIdx.y + 2 * static_cast<int64_t>(gridDim.y);
+             t += gridDim.y) {
+            const T* g = static_cast<const T*>(a.gate_up) + t * a.is + j0 * VEC;
+            prefetch_l2(g, cols * static_cast<int64_t>(sizeof(T)));
+            prefetch_l2(g + a.I, cols * static_cast<int64_t>(sizeof(T)));
+        }
+    }
+    pdl_enter();
     const int64_t jv = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (jv >= nv) return;
     const T* __restrict__ gcol = static_cast<const T*>(a.gate_up) + jv * VEC;

@@ -300,8 +300,21 @@ __device__ __forceinline__ void reg_row(const NormArgs& a, int64_t r, int tid, i
     if (tid < tail) orow[nvec * VEC + tid] = from_f32<T>(xt * rinv * wt);
 }
 
+// Prefetch row r of x (and res) and, if `with_w`, w, into L2 (one thread).
+template <typename T, bool ADD>
+__device__ __forceinline__ void prefetch_row(const NormArgs& a, int64_t r, int64_t e0, int64_t e1, bool with_w) {
+    if (r >= a.rows) return;
+    const int64_t bytes = (e1 - e0) * static_cast<int64_t>(sizeof(T));
+    prefetch_l2(static_cast<const T*>(a.x) + r * a.xs + e0, bytes);
+    if constexpr (ADD) prefetch_l2(static_cast<const T*>(a.res) + r * a.rs + e0, bytes);
+    if (with_w) prefetch_l2(static_cast<const T*>(a.w) + e0, bytes);
+}
+
 template <typename T, int NV, bool ADD>
 __global__ void __launch_bounds__(256) reg_warp_kernel(NormArgs a) {
+    if ((threadIdx.x & 31) == 0)
+        prefetch_row<T, ADD>(a, static_cast<int64_t>(threadIdx.x >> 5) * gridDim.x + blockIdx.x, 0, a.D,
+                             threadIdx.x == 0);
     pdl_enter();
     const int wpc = blockDim.x >> 5;
     const int64_t nvec = a.D / vec16<T>();
@@ -317,6 +330,7 @@ template <int NV> constexpr int cta_row_max_threads() { return NV >= 8 ? 256 : (
 template <typename T, int NV, bool ADD>
 __global__ void __launch_bounds__(cta_row_max_threads<NV>()) reg_cta_kernel(NormArgs a) {
     __shared__ float scratch[33];
+    if (threadIdx.x == 0) prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true);
     pdl_enter();
     const int64_t nvec = a.D / vec16<T>();
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
@@ -327,12 +341,14 @@ template <typename T, int NV, bool ADD>
 __global__ void __launch_bounds__(cta_row_max_threads<NV>()) reg_pair_kernel(NormArgs a) {
     __shared__ float scratch[33];
     __shared__ float pair_slot[2];
-    pdl_enter();
     const int rank = static_cast<int>(cg::this_cluster().block_rank());
     const int64_t nvec = a.D / vec16<T>();
     const int64_t half = norm_pair_half(nvec);
     const int64_t a0 = rank == 0 ? 0 : half;
     const int64_t a1 = rank == 0 ? half : nvec;
+    if (threadIdx.x == 0)
+        prefetch_row<T, ADD>(a, blockIdx.x / 2, a0 * vec16<T>(), rank == 0 ? a1 * vec16<T>() : a.D, true);
+    pdl_enter();
     int parity = 0;
     for (int64_t r = blockIdx.x / 2; r < a.rows; r += gridDim.x / 2) {
         reg_row<T, NV, ADD, RED_PAIR>(a, r, threadIdx.x, blockDim.x, a0, a1, rank == 1, scratch, pair_slot, parity);
@@ -385,6 +401,9 @@ __device__ __forceinline__ void scalar_row(const NormArgs& a, int64_t r, int tid
 
 template <typename T, int NV, bool ADD>
 __global__ void __launch_bounds__(256) scalar_warp_kernel(NormArgs a) {
+    if ((threadIdx.x & 31) == 0)
+        prefetch_row<T, ADD>(a, static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5), 0, a.D,
+                             threadIdx.x == 0);
     pdl_enter();
     const int wpc = blockDim.x >> 5;
     const int64_t step = static_cast<int64_t>(gridDim.x) * wpc;
@@ -395,6 +414,7 @@ __global__ void __launch_bounds__(256) scalar_warp_kernel(NormArgs a) {
 template <typename T, int NV, bool ADD>
 __global__ void __launch_bounds__(1024) scalar_cta_kernel(NormArgs a) {
     __shared__ float scratch[33];
+    if (threadIdx.x == 0) prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true);
     pdl_enter();
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
         scalar_row<T, NV, ADD, RED_CTA>(a, r, threadIdx.x, blockDim.x, scratch);
@@ -408,6 +428,7 @@ __global__ void __launch_bounds__(1024) two_pass_kernel(NormArgs a) {
     using V = Vec<T, VEC>;
     using R = typename V::Raw;
     __shared__ float scratch[33];
+    if (threadIdx.x == 0) prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true);
     pdl_enter();
     const int tid = threadIdx.x, threads = blockDim.x;
     const int64_t nvec = a.D / VEC;

@@ -39,6 +39,12 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
     using R = typename V::Raw;
     using C = Vec<float, (P >= 4 ? 4 : 1)>;  // cos / sin accesses
     constexpr int CW = P >= 4 ? 4 : 1;
+    if (threadIdx.x == 0 && blockIdx.x < a.T) {
+        const int64_t t = blockIdx.x, es = static_cast<int64_t>(sizeof(T));
+        prefetch_l2(static_cast<const T*>(a.q) + t * a.qs, static_cast<int64_t>(a.n_head) * a.head_dim * es);
+        prefetch_l2(static_cast<const T*>(a.k) + t * a.ks, static_cast<int64_t>(a.n_kv) * a.head_dim * es);
+        prefetch_l2(static_cast<const T*>(a.v) + t * a.vs, static_cast<int64_t>(a.n_kv) * a.head_dim * es);
+    }
     pdl_enter();
 
     const int h = a.head_dim >> 1;
