@@ -599,7 +599,8 @@ int sra_swiglu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_
 int sra_force_variant(const char* op, int variant) {
     std::atomic<int>* slot = force_slot(op);
     if (!slot) return SRA_ERR_ARG;
-    if (variant < -1 || (variant & 0xFF) >= variant_count(op) || (variant >> 16) != 0) return SRA_ERR_ARG;
+    if (variant < -1 || (variant >= 0 && ((variant & 0xFF) >= variant_count(op) || (variant >> 16) != 0)))
+        return SRA_ERR_ARG;
     slot->store(variant, std::memory_order_relaxed);
     return SRA_OK;
 }
