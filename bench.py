@@ -50,6 +50,7 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_FLUSH_BYTES = 256 << 20
 STREAM_BYTES = 512 << 20   # per-kernel streaming measurement: total bytes over the rotating copies
+NVTX_STEP = "sra_timed_step"
 WORKLOAD = ("decoder per-token hot path at the configured shapes: rmsnorm 512xD sweep (8 widths x fp32/fp16/bf16), "
             "add_rmsnorm bf16 Tx1536 T={1,16,256,4096}, rope_kv_store Qwen2.5-1.5B GQA T={1,64,2048}, "
             "swiglu+reglu Llama-3-8B gate_up T={1,64,512,4096}, 28-layer decode chain B={1,64}")
@@ -475,7 +476,11 @@ def run_gpu(args):
     def step(ev=None):
         clean_l2()
         torch.cuda._sleep(delay_cycles)
+        if ev is not None:
+            torch.cuda.nvtx.range_push(NVTX_STEP)  # lets ncu --nvtx-include select the timed steps
         enqueue_step(ev)
+        if ev is not None:
+            torch.cuda.nvtx.range_pop()
 
     for _ in range(args.warmup):
         step()

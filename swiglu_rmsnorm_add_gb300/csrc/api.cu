@@ -170,6 +170,9 @@ int staged_threads(int64_t acc, bool few_rows) {
 // accesses per thread.
 constexpr int kCtaMaxAccesses = 2048;  // 256 threads x 8, 512 x 4, 1024 x 2
 int cta_max_threads_for_nv(int nv) { return nv >= 8 ? 256 : (nv >= 4 ? 512 : 1024); }
+// Measured on GB300 (bench.py --sweep-variants): one access per thread is best
+// for a few rows (decode latency); for hundreds of rows the smallest NV >= 2
+// that keeps the CTA at <= 512 threads.
 bool cta_shape(int64_t nacc, bool few_rows, int min_nv, int* nv_out, int* threads_out) {
     if (g_force_nv) {
         const int nv = g_force_nv;
@@ -178,8 +181,8 @@ bool cta_shape(int64_t nacc, bool few_rows, int min_nv, int* nv_out, int* thread
         *threads_out = std::max(32, round_up32(ceil_div(nacc, nv)));
         return true;
     }
-    int nv = std::max(min_nv, few_rows ? 1 : 4);
-    while (nv < 8 && ceil_div(nacc, nv) > cta_max_threads_for_nv(nv)) nv <<= 1;
+    int nv = std::max(min_nv, few_rows ? 1 : 2);
+    while (nv < 8 && ceil_div(nacc, nv) > (few_rows ? cta_max_threads_for_nv(nv) : 512)) nv <<= 1;
     while (nv > min_nv && ceil_div(nacc, nv) < 64) nv >>= 1;
     if (ceil_div(nacc, nv) > cta_max_threads_for_nv(nv)) return false;
     *nv_out = nv;
@@ -303,6 +306,7 @@ bool plan_norm_variant(int variant, int64_t rows, int64_t D, int vec, bool add, 
     p->pdl = g_pdl;
     p->num_sms = num_sms;
     p->stage_w = 0;
+    p->prefetch = rows <= 4LL * num_sms ? 1 : 0;
     if (vec == 1) return plan_norm_scalar(variant, rows, D, num_sms, p);
     return plan_norm_vector(variant, rows, D, vec, add, num_sms, b, p);
 }
@@ -318,10 +322,12 @@ int plan_norm(int64_t rows, int64_t D, int vec, bool add, int num_sms, const Sme
     }
     const int64_t nacc = ceil_div(D, vec);
     const bool few_rows = rows < 2LL * num_sms;
+    // Order from the variant sweep on GB300 (bench.py --sweep-variants): the
+    // register variants beat the shared-memory ones on every configured shape
+    // but one (within 2%), and a CTA per row beats the CTA pair.
     int order[6];
     int n = 0;
     if (!few_rows && nacc <= 256 && (rows >= 256 || nacc <= 64)) order[n++] = NORM_WARP_ROWS;
-    if (!few_rows && nacc >= 1024 && rows < 16LL * num_sms) order[n++] = NORM_CTA_PAIR;
     order[n++] = NORM_CTA_ROW;
     order[n++] = NORM_CTA_SMEM;
     order[n++] = NORM_TWO_PASS;
@@ -442,6 +448,7 @@ int norm_common(void* x, const void* res, const void* w, void* out, int64_t rows
     a.os = os;
     a.eps = eps;
     a.stage_w = plan.stage_w;
+    a.prefetch = plan.prefetch;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return status_from(add ? launch_add_rmsnorm(a, plan, dtype, s) : launch_rmsnorm(a, plan, dtype, s));
 }

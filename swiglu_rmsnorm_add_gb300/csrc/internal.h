@@ -21,6 +21,7 @@ struct NormArgs {
     int64_t xs, rs, os;  // row strides, elements
     float eps;
     int stage_w;         // staged kernels: 1 = w slice staged in shared memory
+    int prefetch;        // 1 = prefetch each CTA's first rows into L2 before the launch wait
 };
 
 enum NormVariant {
@@ -53,6 +54,7 @@ struct NormPlan {
     bool pdl;       // launch with programmatic stream serialization
     int num_sms;
     int stage_w;    // staged kernels: stage the w slice in shared memory
+    int prefetch;   // L2 prefetch of the first rows before the launch wait
 };
 
 cudaError_t launch_rmsnorm(const NormArgs& a, const NormPlan& p, int dtype, cudaStream_t s);

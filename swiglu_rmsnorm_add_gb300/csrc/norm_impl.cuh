@@ -301,9 +301,12 @@ __device__ __forceinline__ void reg_row(const NormArgs& a, int64_t r, int tid, i
 }
 
 // Prefetch row r of x (and res) and, if `with_w`, w, into L2 (one thread).
+// Worth it when few rows share an SM (decode batches, a few hundred rows): with
+// many small CTAs per SM the bulk requests queue behind each other, so the
+// planner turns it off there.
 template <typename T, bool ADD>
 __device__ __forceinline__ void prefetch_row(const NormArgs& a, int64_t r, int64_t e0, int64_t e1, bool with_w) {
-    if (r >= a.rows) return;
+    if (!a.prefetch || r >= a.rows) return;
     const int64_t bytes = (e1 - e0) * static_cast<int64_t>(sizeof(T));
     prefetch_l2(static_cast<const T*>(a.x) + r * a.xs + e0, bytes);
     if constexpr (ADD) prefetch_l2(static_cast<const T*>(a.res) + r * a.rs + e0, bytes);
