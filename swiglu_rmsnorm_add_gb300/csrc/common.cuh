@@ -63,6 +63,16 @@ __device__ __forceinline__ void pdl_enter() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Hint the L2 to fetch the 128-byte lines of [p, p + bytes), spread over `n`
+// cooperating threads (this one is number `i`): plain prefetch instructions, no
+// bulk-copy engine involved. Same semantics as prefetch_l2 below.
+__device__ __forceinline__ void prefetch_lines(const void* p, int64_t bytes, int i, int n) {
+    const char* c = static_cast<const char*>(p);
+    const int64_t first = -static_cast<int64_t>(reinterpret_cast<uintptr_t>(p) & 127u);  // line-aligned start
+    for (int64_t off = first + static_cast<int64_t>(i) * 128; off < bytes; off += static_cast<int64_t>(n) * 128)
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(c + off) : "memory");
+}
+
 // Hint the L2 to fetch [p, p + bytes) (p 16-byte aligned, bytes a multiple of 16;
 // anything else is ignored). Issued before pdl_enter() for a CTA's own input
 // rows: with programmatic dependent launch the CTA runs while the previous

@@ -301,23 +301,31 @@ __device__ __forceinline__ void reg_row(const NormArgs& a, int64_t r, int tid, i
 }
 
 // Prefetch row r of x (and res) and, if `with_w`, w, into L2 (one thread).
-// Worth it when few rows share an SM (decode batches, a few hundred rows): with
-// many small CTAs per SM the bulk requests queue behind each other, so the
-// planner turns it off there.
+// Few rows per SM (decode batches, a few hundred rows): one thread issues bulk
+// prefetches. Many rows per SM: bulk requests would queue behind each other, so
+// the group's threads prefetch the row's cache lines themselves.
 template <typename T, bool ADD>
-__device__ __forceinline__ void prefetch_row(const NormArgs& a, int64_t r, int64_t e0, int64_t e1, bool with_w) {
-    if (!a.prefetch || r >= a.rows) return;
+__device__ __forceinline__ void prefetch_row(const NormArgs& a, int64_t r, int64_t e0, int64_t e1, bool with_w,
+                                             int i, int n) {
+    if (r >= a.rows) return;
     const int64_t bytes = (e1 - e0) * static_cast<int64_t>(sizeof(T));
-    prefetch_l2(static_cast<const T*>(a.x) + r * a.xs + e0, bytes);
-    if constexpr (ADD) prefetch_l2(static_cast<const T*>(a.res) + r * a.rs + e0, bytes);
-    if (with_w) prefetch_l2(static_cast<const T*>(a.w) + e0, bytes);
+    const T* x = static_cast<const T*>(a.x) + r * a.xs + e0;
+    const T* res = static_cast<const T*>(a.res) + r * a.rs + e0;
+    if (a.prefetch) {
+        if (i != 0) return;
+        prefetch_l2(x, bytes);
+        if constexpr (ADD) prefetch_l2(res, bytes);
+        if (with_w) prefetch_l2(static_cast<const T*>(a.w) + e0, bytes);
+    } else {
+        prefetch_lines(x, bytes, i, n);
+        if constexpr (ADD) prefetch_lines(res, bytes, i, n);
+    }
 }
 
 template <typename T, int NV, bool ADD>
 __global__ void __launch_bounds__(256) reg_warp_kernel(NormArgs a) {
-    if ((threadIdx.x & 31) == 0)
-        prefetch_row<T, ADD>(a, static_cast<int64_t>(threadIdx.x >> 5) * gridDim.x + blockIdx.x, 0, a.D,
-                             threadIdx.x == 0);
+    prefetch_row<T, ADD>(a, static_cast<int64_t>(threadIdx.x >> 5) * gridDim.x + blockIdx.x, 0, a.D,
+                         threadIdx.x == 0, threadIdx.x & 31, 32);
     pdl_enter();
     const int wpc = blockDim.x >> 5;
     const int64_t nvec = a.D / vec16<T>();
@@ -333,7 +341,7 @@ template <int NV> constexpr int cta_row_max_threads() { return NV >= 8 ? 256 : (
 template <typename T, int NV, bool ADD>
 __global__ void __launch_bounds__(cta_row_max_threads<NV>()) reg_cta_kernel(NormArgs a) {
     __shared__ float scratch[33];
-    if (threadIdx.x == 0) prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true);
+    prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true, threadIdx.x, blockDim.x);
     pdl_enter();
     const int64_t nvec = a.D / vec16<T>();
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
@@ -349,8 +357,8 @@ __global__ void __launch_bounds__(cta_row_max_threads<NV>()) reg_pair_kernel(Nor
     const int64_t half = norm_pair_half(nvec);
     const int64_t a0 = rank == 0 ? 0 : half;
     const int64_t a1 = rank == 0 ? half : nvec;
-    if (threadIdx.x == 0)
-        prefetch_row<T, ADD>(a, blockIdx.x / 2, a0 * vec16<T>(), rank == 0 ? a1 * vec16<T>() : a.D, true);
+    prefetch_row<T, ADD>(a, blockIdx.x / 2, a0 * vec16<T>(), rank == 0 ? a1 * vec16<T>() : a.D, true, threadIdx.x,
+                         blockDim.x);
     pdl_enter();
     int parity = 0;
     for (int64_t r = blockIdx.x / 2; r < a.rows; r += gridDim.x / 2) {
@@ -404,9 +412,8 @@ __device__ __forceinline__ void scalar_row(const NormArgs& a, int64_t r, int tid
 
 template <typename T, int NV, bool ADD>
 __global__ void __launch_bounds__(256) scalar_warp_kernel(NormArgs a) {
-    if ((threadIdx.x & 31) == 0)
-        prefetch_row<T, ADD>(a, static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5), 0, a.D,
-                             threadIdx.x == 0);
+    prefetch_row<T, ADD>(a, static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5), 0, a.D,
+                         threadIdx.x == 0, threadIdx.x & 31, 32);
     pdl_enter();
     const int wpc = blockDim.x >> 5;
     const int64_t step = static_cast<int64_t>(gridDim.x) * wpc;
@@ -417,7 +424,7 @@ __global__ void __launch_bounds__(256) scalar_warp_kernel(NormArgs a) {
 template <typename T, int NV, bool ADD>
 __global__ void __launch_bounds__(1024) scalar_cta_kernel(NormArgs a) {
     __shared__ float scratch[33];
-    if (threadIdx.x == 0) prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true);
+    prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true, threadIdx.x, blockDim.x);
     pdl_enter();
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
         scalar_row<T, NV, ADD, RED_CTA>(a, r, threadIdx.x, blockDim.x, scratch);
@@ -431,7 +438,7 @@ __global__ void __launch_bounds__(1024) two_pass_kernel(NormArgs a) {
     using V = Vec<T, VEC>;
     using R = typename V::Raw;
     __shared__ float scratch[33];
-    if (threadIdx.x == 0) prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true);
+    prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true, threadIdx.x, blockDim.x);
     pdl_enter();
     const int tid = threadIdx.x, threads = blockDim.x;
     const int64_t nvec = a.D / VEC;
