@@ -311,6 +311,24 @@ def kernel_traffic(entry_name):
     return rec.get("dram_bytes_per_launch")
 
 
+def reduce_max(x: float, device) -> float:
+    """The maximum of x over all ranks (x itself when not distributed)."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_value(bytes_per_rank_step: int, ms_max: float, world: int) -> float:
+    """Whole-job GB/s of a weak-scaling step: every rank moves the same bytes; the
+    slowest rank's step time sets the pace."""
+    return world * bytes_per_rank_step / (ms_max / 1e3) / 1e9
+
+
 def dist_setup(args):
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -509,12 +527,8 @@ def run_gpu(args):
 
     step_ms = [ev[k][0].elapsed_time(ev[k][3]) for k in range(args.steps)]
     dom_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(args.steps)]
-    ms = statistics.fmean(step_ms)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
-    value = world * bytes_per_step / (ms / 1e3) / 1e9
+    ms = reduce_max(statistics.fmean(step_ms), dev)
+    value = weak_value(bytes_per_step, ms, world)
 
     peak, peak_src = measured_peak()
     de = entries[dom]
@@ -671,12 +685,8 @@ def run_gpu(args):
             e2e_step()
         if world > 1:
             dist.barrier()
-        e_s = (time.perf_counter() - t0) / n_e2e
-        if world > 1:
-            t = torch.tensor([e_s], dtype=torch.float64, device=dev)
-            dist.all_reduce(t, op=dist.ReduceOp.MAX)
-            e_s = float(t.item())
-        e2e = {"value": round(world * bytes_per_step / e_s / 1e9, 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e_s = reduce_max((time.perf_counter() - t0) / n_e2e, dev)
+        e2e = {"value": round(weak_value(bytes_per_step, e_s * 1e3, world), 2), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": round(e_s * 1e3, 3)}
 
     cpu = None
