@@ -307,6 +307,7 @@ bool plan_norm_variant(int variant, int64_t rows, int64_t D, int vec, bool add, 
     p->num_sms = num_sms;
     p->stage_w = 0;
     p->prefetch = rows <= 4LL * num_sms ? 1 : 0;
+    p->next_prefetch = rows <= 64LL * num_sms ? 1 : 0;
     if (vec == 1) return plan_norm_scalar(variant, rows, D, num_sms, p);
     return plan_norm_vector(variant, rows, D, vec, add, num_sms, b, p);
 }
@@ -449,6 +450,7 @@ int norm_common(void* x, const void* res, const void* w, void* out, int64_t rows
     a.eps = eps;
     a.stage_w = plan.stage_w;
     a.prefetch = plan.prefetch;
+    a.next_prefetch = plan.next_prefetch;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     return status_from(add ? launch_add_rmsnorm(a, plan, dtype, s) : launch_rmsnorm(a, plan, dtype, s));
 }

@@ -22,6 +22,7 @@ struct NormArgs {
     float eps;
     int stage_w;         // staged kernels: 1 = w slice staged in shared memory
     int prefetch;        // 1 = prefetch each CTA's first rows into L2 before the launch wait
+    int next_prefetch;   // 1 = prefetch a group's next row while it processes the current one
 };
 
 enum NormVariant {
@@ -55,6 +56,7 @@ struct NormPlan {
     int num_sms;
     int stage_w;    // staged kernels: stage the w slice in shared memory
     int prefetch;   // L2 prefetch of the first rows before the launch wait
+    int next_prefetch;  // L2 prefetch of each group's next row
 };
 
 cudaError_t launch_rmsnorm(const NormArgs& a, const NormPlan& p, int dtype, cudaStream_t s);

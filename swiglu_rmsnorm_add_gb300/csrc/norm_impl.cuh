@@ -322,6 +322,19 @@ __device__ __forceinline__ void prefetch_row(const NormArgs& a, int64_t r, int64
     }
 }
 
+// A group that will process another row after this one prefetches that row's
+// lines into L2 now, so the DRAM queue stays full across the boundary between
+// one round of resident rows and the next. Off when rows are so many that they
+// stream back to back anyway.
+template <typename T, bool ADD>
+__device__ __forceinline__ void next_row_prefetch(const NormArgs& a, int64_t r, int64_t e0, int64_t e1, int i,
+                                                  int n) {
+    if (!a.next_prefetch || r >= a.rows) return;
+    const int64_t bytes = (e1 - e0) * static_cast<int64_t>(sizeof(T));
+    prefetch_lines(static_cast<const T*>(a.x) + r * a.xs + e0, bytes, i, n);
+    if constexpr (ADD) prefetch_lines(static_cast<const T*>(a.res) + r * a.rs + e0, bytes, i, n);
+}
+
 template <typename T, int NV, bool ADD>
 __global__ void __launch_bounds__(256) reg_warp_kernel(NormArgs a) {
     prefetch_row<T, ADD>(a, static_cast<int64_t>(threadIdx.x >> 5) * gridDim.x + blockIdx.x, 0, a.D,
@@ -331,8 +344,10 @@ __global__ void __launch_bounds__(256) reg_warp_kernel(NormArgs a) {
     const int64_t nvec = a.D / vec16<T>();
     // Rows are dealt to CTAs round-robin, so CTAs (and SMs) differ by one row at most.
     const int64_t step = static_cast<int64_t>(gridDim.x) * wpc;
-    for (int64_t r = static_cast<int64_t>(threadIdx.x >> 5) * gridDim.x + blockIdx.x; r < a.rows; r += step)
+    for (int64_t r = static_cast<int64_t>(threadIdx.x >> 5) * gridDim.x + blockIdx.x; r < a.rows; r += step) {
+        next_row_prefetch<T, ADD>(a, r + step, 0, a.D, threadIdx.x & 31, 32);
         reg_row<T, NV, ADD, RED_WARP>(a, r, threadIdx.x & 31, 32, 0, nvec, true, nullptr, nullptr, 0);
+    }
 }
 
 // Largest CTA the register-resident CTA variants are compiled for, per NV.
@@ -344,8 +359,10 @@ __global__ void __launch_bounds__(cta_row_max_threads<NV>()) reg_cta_kernel(Norm
     prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true, threadIdx.x, blockDim.x);
     pdl_enter();
     const int64_t nvec = a.D / vec16<T>();
-    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        next_row_prefetch<T, ADD>(a, r + gridDim.x, 0, a.D, threadIdx.x, blockDim.x);
         reg_row<T, NV, ADD, RED_CTA>(a, r, threadIdx.x, blockDim.x, 0, nvec, true, scratch, nullptr, 0);
+    }
 }
 
 template <typename T, int NV, bool ADD>
@@ -362,6 +379,8 @@ __global__ void __launch_bounds__(cta_row_max_threads<NV>()) reg_pair_kernel(Nor
     pdl_enter();
     int parity = 0;
     for (int64_t r = blockIdx.x / 2; r < a.rows; r += gridDim.x / 2) {
+        next_row_prefetch<T, ADD>(a, r + gridDim.x / 2, a0 * vec16<T>(), rank == 0 ? a1 * vec16<T>() : a.D,
+                                  threadIdx.x, blockDim.x);
         reg_row<T, NV, ADD, RED_PAIR>(a, r, threadIdx.x, blockDim.x, a0, a1, rank == 1, scratch, pair_slot, parity);
         parity ^= 1;
     }
