@@ -307,7 +307,9 @@ bool plan_norm_variant(int variant, int64_t rows, int64_t D, int vec, bool add, 
     p->num_sms = num_sms;
     p->stage_w = 0;
     p->prefetch = rows <= 4LL * num_sms ? 1 : 0;
-    p->next_prefetch = rows <= 64LL * num_sms ? 1 : 0;
+    // groups with a next row exist only past one row per resident group; with very
+    // many rows they stream back to back anyway (measured: bench.py --sweep-variants)
+    p->next_prefetch = rows >= 2LL * num_sms && rows <= 64LL * num_sms ? 1 : 0;
     if (vec == 1) return plan_norm_scalar(variant, rows, D, num_sms, p);
     return plan_norm_vector(variant, rows, D, vec, add, num_sms, b, p);
 }

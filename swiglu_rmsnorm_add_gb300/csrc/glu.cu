@@ -77,24 +77,9 @@ __global__ void __launch_bounds__(256) cols_rows_kernel(GluArgs a) {
         gb = V::load_stream(gcol + (t + step) * a.is);
         ub = V::load_stream(gcol + (t + step) * a.is + a.I);
     }
-    // Lines of this CTA's column segment (gate and up) for a row: thread i takes line i.
-    const int64_t seg_bytes = ((nv - static_cast<int64_t>(blockIdx.x) * blockDim.x) < blockDim.x
-                                   ? (nv - static_cast<int64_t>(blockIdx.x) * blockDim.x)
-                                   : blockDim.x) * VEC * static_cast<int64_t>(sizeof(T));
-    const int seg_lines = static_cast<int>((seg_bytes + 127) / 128);
-    const T* seg = static_cast<const T*>(a.gate_up) + static_cast<int64_t>(blockIdx.x) * blockDim.x * VEC;
     while (true) {
         const int64_t tn = t + 2 * step;
         const bool next0 = tn < a.T, next1 = tn + step < a.T;
-        // rows two iterations ahead into L2, so the DRAM queue never drains between pairs
-        {
-            const int64_t tp = tn + 2 * step + (threadIdx.x >= 2 * seg_lines ? step : 0);
-            const int li = threadIdx.x % (2 * seg_lines);
-            if (threadIdx.x < 4 * seg_lines && tp < a.T) {
-                const char* base = reinterpret_cast<const char*>(seg + tp * a.is + (li >= seg_lines ? a.I : 0));
-                asm volatile("prefetch.global.L2 [%0];" ::"l"(base + (li % seg_lines) * 128) : "memory");
-            }
-        }
         R gc = ga, uc = ua, gd = gb, ud = ub;
         if (next0) {
             gc = V::load_stream(gcol + tn * a.is);

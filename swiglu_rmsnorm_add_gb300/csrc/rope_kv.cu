@@ -61,16 +61,6 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
         const int head = kind == 0 ? unit : (kind == 1 ? unit - a.n_head : unit - a.n_head - a.n_kv);
 
         for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
-            const int64_t tn = t + gridDim.x;  // this CTA's next token: its rows into L2 now
-            if (u == threadIdx.x && tn < a.T) {
-                const int64_t es = static_cast<int64_t>(sizeof(T));
-                prefetch_lines(static_cast<const T*>(a.q) + tn * a.qs, static_cast<int64_t>(a.n_head) * a.head_dim * es,
-                               threadIdx.x, blockDim.x);
-                prefetch_lines(static_cast<const T*>(a.k) + tn * a.ks, static_cast<int64_t>(a.n_kv) * a.head_dim * es,
-                               threadIdx.x, blockDim.x);
-                prefetch_lines(static_cast<const T*>(a.v) + tn * a.vs, static_cast<int64_t>(a.n_kv) * a.head_dim * es,
-                               threadIdx.x, blockDim.x);
-            }
             const int64_t p = a.pos[t];
             const bool pos_ok = p >= 0 && p < a.max_pos;
             int64_t slot = -1;
