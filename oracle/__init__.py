@@ -62,6 +62,8 @@ def lib() -> ctypes.CDLL:
             L.orc_rope_kv_store.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32,
                                             i64, i64, i64, i64, i64, i32, i32]
             L.orc_rope_kv_store.restype = i64
+            L.orc_rope_kv_store_style.argtypes = L.orc_rope_kv_store.argtypes + [i32]
+            L.orc_rope_kv_store_style.restype = i64
             L.orc_glu.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32]
             L.orc_glu.restype = i32
             _lib = L
@@ -120,9 +122,11 @@ def _tok_stride(t: torch.Tensor) -> int:
     return t.stride(0)
 
 
-def rope_kv_store(q, k, v, cos, sin, pos, slot_mapping, kv_cache, max_pos: int | None = None) -> int:
+def rope_kv_store(q, k, v, cos, sin, pos, slot_mapping, kv_cache, max_pos: int | None = None,
+                  style: str = "neox") -> int:
     """Rotate q in place, write rotated k and v into kv_cache through slot_mapping.
 
+    style: "neox" pairs (i, i + head_dim/2); "interleaved" (GPT-J) pairs (2i, 2i + 1).
     Returns the error count (bad positions plus out-of-range slots).
     """
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (cos, "cos"), (sin, "sin"), (pos, "pos"),
@@ -137,11 +141,11 @@ def rope_kv_store(q, k, v, cos, sin, pos, slot_mapping, kv_cache, max_pos: int |
     _, num_blocks, block_size, _, _ = kv_cache.shape
     if max_pos is None:
         max_pos = cos.shape[0]
-    n = lib().orc_rope_kv_store(q.data_ptr(), k.data_ptr(), v.data_ptr(), cos.data_ptr(),
-                                sin.data_ptr(), pos.data_ptr(), slot_mapping.data_ptr(),
-                                kv_cache.data_ptr(), T, n_head, n_kv, hd, _tok_stride(q),
-                                _tok_stride(k), _tok_stride(v), int(max_pos), num_blocks,
-                                block_size, _FMT[q.dtype])
+    n = lib().orc_rope_kv_store_style(q.data_ptr(), k.data_ptr(), v.data_ptr(), cos.data_ptr(),
+                                      sin.data_ptr(), pos.data_ptr(), slot_mapping.data_ptr(),
+                                      kv_cache.data_ptr(), T, n_head, n_kv, hd, _tok_stride(q),
+                                      _tok_stride(k), _tok_stride(v), int(max_pos), num_blocks,
+                                      block_size, _FMT[q.dtype], {"neox": 0, "interleaved": 1}[style])
     if n < 0:
         raise ValueError("oracle: bad rope_kv_store arguments or duplicate slots")
     return int(n)

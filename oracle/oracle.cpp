@@ -205,6 +205,21 @@ int orc_add_rmsnorm(void* x, const void* res, const void* w, void* out, int64_t 
     return 0;
 }
 
+// Rotation partner layout of a head of width head_dim, h = head_dim / 2, pair i < h:
+//   neox (style 0, [koas] section 1: slice halves, negate, concatenate): (i, i + h)
+//   interleaved (style 1, GPT-J; m.lsln.cn "21 个算子" section 2.3: even/odd
+//   partner d, d +- 1):                                                  (2i, 2i + 1)
+// Both use c = cos[p, i], s = sin[p, i] for pair i.
+static void pair_index(int style, int i, int h, int* lo, int* hi) {
+    if (style == 0) {
+        *lo = i;
+        *hi = i + h;
+    } else {
+        *lo = 2 * i;
+        *hi = 2 * i + 1;
+    }
+}
+
 // Neox half-rotation of every Q and K head at position pos[t], Q rotated in place,
 // K_rot and V written through slot_mapping into a paged cache ([koas] section 1;
 // cache layout [2, num_blocks, block_size, n_kv_head, head_dim] from [mer] 1.1).
@@ -215,14 +230,15 @@ int orc_add_rmsnorm(void* x, const void* res, const void* w, void* out, int64_t 
 // cache untouched; slot < 0 is a padding token (no cache write, no error); a slot
 // >= num_blocks * block_size counts one error and skips the cache write.
 // Returns the error count, or -1 on bad arguments or duplicate valid slots.
-int64_t orc_rope_kv_store(void* q, const void* k, const void* v, const float* cos_t,
-                          const float* sin_t, const int64_t* pos, const int64_t* slot_mapping,
-                          void* kv_cache, int64_t T, int n_head, int n_kv_head, int head_dim,
-                          int64_t q_tok_stride, int64_t k_tok_stride, int64_t v_tok_stride,
-                          int64_t max_pos, int64_t num_blocks, int block_size, int fmt) {
+int64_t orc_rope_kv_store_style(void* q, const void* k, const void* v, const float* cos_t,
+                                const float* sin_t, const int64_t* pos, const int64_t* slot_mapping,
+                                void* kv_cache, int64_t T, int n_head, int n_kv_head, int head_dim,
+                                int64_t q_tok_stride, int64_t k_tok_stride, int64_t v_tok_stride,
+                                int64_t max_pos, int64_t num_blocks, int block_size, int fmt, int style) {
     FormatSpec s;
     if (!format_spec(fmt, &s) || T < 0 || n_head <= 0 || n_kv_head <= 0 || head_dim <= 0 ||
-        head_dim % 2 != 0 || n_head % n_kv_head != 0 || block_size <= 0 || num_blocks < 0)
+        head_dim % 2 != 0 || n_head % n_kv_head != 0 || block_size <= 0 || num_blocks < 0 ||
+        (style != 0 && style != 1))
         return -1;
     const int h = head_dim / 2;
     const int64_t capacity = num_blocks * block_size;
@@ -251,8 +267,10 @@ int64_t orc_rope_kv_store(void* q, const void* k, const void* v, const float* co
             for (int d = 0; d < head_dim; ++d) xin[d] = load(q, base + d, fmt);
             for (int i = 0; i < h; ++i) {
                 const double c = c_row[i], sn = s_row[i];
-                store(q, base + i, xin[i] * c - xin[i + h] * sn, fmt);
-                store(q, base + i + h, xin[i + h] * c + xin[i] * sn, fmt);
+                int lo, hi;
+                pair_index(style, i, h, &lo, &hi);
+                store(q, base + lo, xin[lo] * c - xin[hi] * sn, fmt);
+                store(q, base + hi, xin[hi] * c + xin[lo] * sn, fmt);
             }
         }
         if (sl < 0 || !slot_in_range) continue;
@@ -269,8 +287,10 @@ int64_t orc_rope_kv_store(void* q, const void* k, const void* v, const float* co
             for (int d = 0; d < head_dim; ++d) xin[d] = load(k, k_src + d, fmt);
             for (int i = 0; i < h; ++i) {
                 const double c = c_row[i], sn = s_row[i];
-                store(kv_cache, k_dst + i, xin[i] * c - xin[i + h] * sn, fmt);
-                store(kv_cache, k_dst + i + h, xin[i + h] * c + xin[i] * sn, fmt);
+                int lo, hi;
+                pair_index(style, i, h, &lo, &hi);
+                store(kv_cache, k_dst + lo, xin[lo] * c - xin[hi] * sn, fmt);
+                store(kv_cache, k_dst + hi, xin[hi] * c + xin[lo] * sn, fmt);
             }
             // V is stored unchanged: copy the element bits.
             const int es = elem_size(fmt);
@@ -280,6 +300,17 @@ int64_t orc_rope_kv_store(void* q, const void* k, const void* v, const float* co
     }
     delete[] xin;
     return errors;
+}
+
+// The neox layout (style 0) of orc_rope_kv_store_style.
+int64_t orc_rope_kv_store(void* q, const void* k, const void* v, const float* cos_t, const float* sin_t,
+                          const int64_t* pos, const int64_t* slot_mapping, void* kv_cache, int64_t T,
+                          int n_head, int n_kv_head, int head_dim, int64_t q_tok_stride,
+                          int64_t k_tok_stride, int64_t v_tok_stride, int64_t max_pos, int64_t num_blocks,
+                          int block_size, int fmt) {
+    return orc_rope_kv_store_style(q, k, v, cos_t, sin_t, pos, slot_mapping, kv_cache, T, n_head,
+                                   n_kv_head, head_dim, q_tok_stride, k_tok_stride, v_tok_stride, max_pos,
+                                   num_blocks, block_size, fmt, 0);
 }
 
 // Gated linear unit over a fused gate_up tensor [T, 2I] (gate = columns [0, I),

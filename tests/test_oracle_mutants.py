@@ -25,14 +25,15 @@ MUTANTS = [
      "test_oracle_norm.py"),
     ("residual dropped", "load(x, r * x_row_stride + j, fmt) + load(res, r * res_row_stride + j, fmt)",
      "load(x, r * x_row_stride + j, fmt)", "test_oracle_norm.py"),
-    ("rope first-half sign", "store(q, base + i, xin[i] * c - xin[i + h] * sn, fmt);",
-     "store(q, base + i, xin[i] * c + xin[i + h] * sn, fmt);", "test_oracle_rope.py"),
-    ("rope partner transposed", "store(q, base + i + h, xin[i + h] * c + xin[i] * sn, fmt);",
-     "store(q, base + i + h, xin[i] * c + xin[i + h] * sn, fmt);", "test_oracle_rope.py"),
-    ("K rotation skipped", "store(kv_cache, k_dst + i, xin[i] * c - xin[i + h] * sn, fmt);",
-     "store(kv_cache, k_dst + i, xin[i], fmt);", "test_oracle_rope.py"),
-    ("cos and sin swapped", "const double c = c_row[i], sn = s_row[i];\n                store(q",
-     "const double c = s_row[i], sn = c_row[i];\n                store(q", "test_oracle_rope.py"),
+    ("rope first-half sign", "store(q, base + lo, xin[lo] * c - xin[hi] * sn, fmt);",
+     "store(q, base + lo, xin[lo] * c + xin[hi] * sn, fmt);", "test_oracle_rope.py"),
+    ("rope partner transposed", "store(q, base + hi, xin[hi] * c + xin[lo] * sn, fmt);",
+     "store(q, base + hi, xin[lo] * c + xin[hi] * sn, fmt);", "test_oracle_rope.py"),
+    ("K rotation skipped", "store(kv_cache, k_dst + lo, xin[lo] * c - xin[hi] * sn, fmt);",
+     "store(kv_cache, k_dst + lo, xin[lo], fmt);", "test_oracle_rope.py"),
+    ("interleaved partner as neox", "*hi = 2 * i + 1;", "*hi = i + h;", "test_oracle_rope.py"),
+    ("cos and sin swapped", "const double c = c_row[i], sn = s_row[i];",
+     "const double c = s_row[i], sn = c_row[i];", "test_oracle_rope.py"),
     ("K and V planes swapped", "(((0 * num_blocks + blk)", "(((1 * num_blocks + blk)",
      "test_oracle_rope.py"),
     ("slot offset from the quotient", "const int64_t off = sl % block_size;",

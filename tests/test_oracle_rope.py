@@ -206,3 +206,55 @@ def test_duplicate_slots_rejected():
     slot = torch.tensor([1, 1, 2], dtype=torch.int64)
     with pytest.raises(ValueError):
         oracle.rope_kv_store(q, k, v, cos, sin, pos, slot, cache)
+
+
+# ------------------------------------------------------------ interleaved (GPT-J) pairing
+# m.lsln.cn "21 个算子" section 2.3 pairs each even dimension with the next odd one.
+
+def test_interleaved_partner_is_the_next_dimension():
+    q, k, v, pos, slot, cache = _case(T=1, n_head=1, n_kv=1, hd=8)
+    q.zero_()
+    q[0, 0, 0] = 1.0
+    cos, sin = _tables(16, 4, 0.0, 1.0)
+    oracle.rope_kv_store(q, k, v, cos, sin, pos, slot, cache, style="interleaved")
+    want = torch.zeros(8, dtype=torch.bfloat16)
+    want[1] = 1.0   # e_0 rotates into dimension 1, not h = 4
+    assert torch.equal(q[0, 0], want)
+
+
+@pytest.mark.parametrize("fmt", [F32, F16, BF16])
+def test_interleaved_general_angle_exact(fmt):
+    q, k, v, pos, slot, cache = _case(fmt=fmt, T=3)
+    # per-pair angles: pair i uses table column i
+    cos = torch.tensor([[0.75, 0.5, -0.25, 1.0]] * 16, dtype=torch.float32)
+    sin = torch.tensor([[0.5, -0.125, 0.875, 0.0]] * 16, dtype=torch.float32)
+    q0, k0 = q.clone(), k.clone()
+    oracle.rope_kv_store(q, k, v, cos, sin, pos, slot, cache, style="interleaved")
+    qb, cb = tensor_bits(q), tensor_bits(cache)
+    for t in range(3):
+        for hd in range(q.shape[1]):
+            x = [Fraction(float(val)) for val in q0[t, hd].double()]
+            for i in range(4):
+                c, s = Fraction(float(cos[0, i])), Fraction(float(sin[0, i]))
+                assert qb[t, hd, 2 * i] == nearest_bits(x[2 * i] * c - x[2 * i + 1] * s, fmt)
+                assert qb[t, hd, 2 * i + 1] == nearest_bits(x[2 * i + 1] * c + x[2 * i] * s, fmt)
+        sl = int(slot[t])
+        for kvh in range(k.shape[1]):
+            x = [Fraction(float(val)) for val in k0[t, kvh].double()]
+            for i in range(4):
+                c, s = Fraction(float(cos[0, i])), Fraction(float(sin[0, i]))
+                assert cb[0, sl // 2, sl % 2, kvh, 2 * i] == nearest_bits(x[2 * i] * c - x[2 * i + 1] * s, fmt)
+
+
+def test_interleaved_is_a_permutation_of_neox():
+    """Interleaved RoPE equals neox RoPE applied to the even/odd de-interleaved head."""
+    T, nh, nkv, hd = 4, 3, 1, 16
+    q, k, v, pos, slot, cache = _case(T=T, n_head=nh, n_kv=nkv, hd=hd, max_pos=64, fmt=F32)
+    cos, sin = synthetic.rope_tables(64, hd, 1e4)
+    perm = torch.cat([torch.arange(0, hd, 2), torch.arange(1, hd, 2)])  # [evens | odds]
+    qa = q.clone()
+    oracle.rope_kv_store(qa, k.clone(), v.clone(), cos, sin, pos, slot, cache.clone(), style="interleaved")
+    qb = q[..., perm].contiguous()
+    oracle.rope_kv_store(qb, k[..., perm].contiguous(), v[..., perm].contiguous(), cos, sin, pos, slot,
+                         cache.clone())
+    assert torch.equal(qa[..., perm], qb)
