@@ -75,6 +75,11 @@ typedef enum sra_status {
     SRA_ERR_DEVICE = -9    /* the device could not be queried */
 } sra_status_t;
 
+typedef enum sra_rope_style {
+    SRA_ROPE_NEOX = 0,        /* pairs (i, i + head_dim/2): rotate halves       [koas] sec. 1 */
+    SRA_ROPE_INTERLEAVED = 1  /* pairs (2i, 2i + 1): GPT-J even/odd partners    [lsln] sec. 2.3 */
+} sra_rope_style_t;
+
 typedef enum sra_act {
     SRA_ACT_SILU = 0,  /* SwiGLU: silu(g) * u, silu(g) = g / (1 + e^-g)   [koas] sec. 2 */
     SRA_ACT_RELU = 1   /* ReGLU:  max(g, 0) * u                            [mer] sec. 3.3 */
@@ -162,6 +167,20 @@ SRA_API int sra_rope_kv_store(void* q, const void* k, const void* v, const float
                       int64_t k_tok_stride, int64_t v_tok_stride, int64_t max_pos,
                       int64_t num_blocks, int block_size, int32_t* err_count, int dtype,
                       void* stream);
+
+/*
+ * sra_rope_kv_store_ex — sra_rope_kv_store with the rotation pairing chosen by
+ * `style` (sra_rope_style_t). SRA_ROPE_INTERLEAVED rotates the pairs (2i, 2i + 1)
+ * with c = cos[p*h + i], s = sin[p*h + i] ([lsln] sec. 2.3: each even dimension and
+ * the next odd one form a pair); the tables, cache layout, token rules and errors
+ * are those of sra_rope_kv_store. An unknown style -> SRA_ERR_ARG.
+ */
+SRA_API int sra_rope_kv_store_ex(void* q, const void* k, const void* v, const float* cos, const float* sin,
+                                 const int64_t* pos, const int64_t* slot_mapping, void* kv_cache, int64_t T,
+                                 int n_head, int n_kv_head, int head_dim, int64_t q_tok_stride,
+                                 int64_t k_tok_stride, int64_t v_tok_stride, int64_t max_pos,
+                                 int64_t num_blocks, int block_size, int32_t* err_count, int style, int dtype,
+                                 void* stream);
 
 /*
  * sra_glu — [koas] sec. 2 (SwiGLU: gate and up loaded together, activation and

@@ -40,9 +40,11 @@ def lib() -> ctypes.CDLL:
             L.sra_add_rmsnorm.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, i32, vp]
             L.sra_rope_kv_store.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i64,
                                             i64, i64, i64, i32, vp, i32, vp]
+            L.sra_rope_kv_store_ex.argtypes = L.sra_rope_kv_store.argtypes[:19] + [i32, i32, vp]
             L.sra_glu.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, vp]
             L.sra_swiglu.argtypes = [vp, vp, i64, i64, i64, i64, i32, vp]
-            for fn in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_glu", "sra_swiglu"):
+            for fn in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_rope_kv_store_ex", "sra_glu",
+                       "sra_swiglu"):
                 getattr(L, fn).restype = i32
             L.sra_status_string.argtypes = [i32]
             L.sra_status_string.restype = ctypes.c_char_p
@@ -198,10 +200,18 @@ def _tok_stride(t: torch.Tensor, name: str) -> int:
     return t.stride(0) if t.shape[0] > 1 else t.shape[1] * t.shape[2]
 
 
+ROPE_STYLE = {"neox": 0, "interleaved": 1}
+
+
 def rope_kv_store(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor,
                   pos: torch.Tensor, slot_mapping: torch.Tensor, kv_cache: torch.Tensor,
-                  err_count: torch.Tensor | None = None, max_pos: int | None = None, stream=None) -> None:
-    """Rotate q in place; write rotated k and v into kv_cache[0/1, slot // bs, slot % bs]."""
+                  err_count: torch.Tensor | None = None, max_pos: int | None = None, stream=None,
+                  style: str = "neox") -> None:
+    """Rotate q in place; write rotated k and v into kv_cache[0/1, slot // bs, slot % bs].
+
+    style: "neox" pairs (i, i + head_dim/2); "interleaved" (GPT-J) pairs (2i, 2i + 1)."""
+    if style not in ROPE_STYLE:
+        raise ValueError("style must be 'neox' or 'interleaved'")
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (cos, "cos"), (sin, "sin"), (pos, "pos"),
                  (slot_mapping, "slot_mapping"), (kv_cache, "kv_cache")):
         _cuda(t, n)
@@ -231,13 +241,13 @@ def rope_kv_store(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.
     if cos.shape[-1] != hd // 2 or sin.shape != cos.shape or max_pos > cos.shape[0]:
         raise ValueError("cos / sin tables must be [>= max_pos, head_dim // 2]")
     with torch.cuda.device(q.device):
-        st = lib().sra_rope_kv_store(q.data_ptr(), k.data_ptr(), v.data_ptr(), cos.data_ptr(), sin.data_ptr(),
-                                     pos.data_ptr(), slot_mapping.data_ptr(), kv_cache.data_ptr(), T, n_head,
-                                     n_kv, hd, _tok_stride(q, "q"), _tok_stride(k, "k"), _tok_stride(v, "v"),
-                                     int(max_pos), nb, bs,
-                                     err_count.data_ptr() if err_count is not None else None,
-                                     _dtype(q), _stream(q, stream))
-    _check("sra_rope_kv_store", st)
+        st = lib().sra_rope_kv_store_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), cos.data_ptr(), sin.data_ptr(),
+                                        pos.data_ptr(), slot_mapping.data_ptr(), kv_cache.data_ptr(), T, n_head,
+                                        n_kv, hd, _tok_stride(q, "q"), _tok_stride(k, "k"), _tok_stride(v, "v"),
+                                        int(max_pos), nb, bs,
+                                        err_count.data_ptr() if err_count is not None else None,
+                                        ROPE_STYLE[style], _dtype(q), _stream(q, stream))
+    _check("sra_rope_kv_store_ex", st)
 
 
 def glu(gate_up: torch.Tensor, out: torch.Tensor | None = None, act: str = "silu", stream=None) -> torch.Tensor:

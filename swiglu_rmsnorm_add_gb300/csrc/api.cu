@@ -349,12 +349,13 @@ int norm_vec(int dt, const void* const* ptrs, int nptr, const int64_t* strides, 
 }
 
 // ------------------------------------------------------------------ RoPE plan
-int plan_rope(int64_t T, int n_head, int n_kv, int head_dim, int pairs, int num_sms, RopePlan* p) {
+int plan_rope(int64_t T, int n_head, int n_kv, int head_dim, int pairs, int style, int num_sms, RopePlan* p) {
     const int forced = g_force_rope.load(std::memory_order_relaxed);
     if (forced > 0) return SRA_ERR_VARIANT;
     const int h = head_dim / 2;
     const int64_t U = static_cast<int64_t>(n_head + 2 * n_kv) * (h / pairs);
     p->variant = ROPE_TOKEN_CTA;
+    p->style = style;
     p->pairs = pairs;
     p->pdl = g_pdl;
     p->num_sms = num_sms;
@@ -519,12 +520,13 @@ int sra_add_rmsnorm(void* x, const void* res, const void* w, void* out, int64_t 
                        true);
 }
 
-int sra_rope_kv_store(void* q, const void* k, const void* v, const float* cos, const float* sin,
-                      const int64_t* pos, const int64_t* slot_mapping, void* kv_cache, int64_t T, int n_head,
-                      int n_kv_head, int head_dim, int64_t q_tok_stride, int64_t k_tok_stride,
-                      int64_t v_tok_stride, int64_t max_pos, int64_t num_blocks, int block_size,
-                      int32_t* err_count, int dtype, void* stream) {
+int sra_rope_kv_store_ex(void* q, const void* k, const void* v, const float* cos, const float* sin,
+                         const int64_t* pos, const int64_t* slot_mapping, void* kv_cache, int64_t T, int n_head,
+                         int n_kv_head, int head_dim, int64_t q_tok_stride, int64_t k_tok_stride,
+                         int64_t v_tok_stride, int64_t max_pos, int64_t num_blocks, int block_size,
+                         int32_t* err_count, int style, int dtype, void* stream) {
     if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
+    if (style != SRA_ROPE_NEOX && style != SRA_ROPE_INTERLEAVED) return SRA_ERR_ARG;
     if (T < 0 || n_head <= 0 || n_kv_head <= 0 || n_head % n_kv_head != 0 || head_dim <= 0 || head_dim % 2 != 0 ||
         block_size <= 0 || num_blocks < 0 || max_pos < 0)
         return SRA_ERR_SHAPE;
@@ -544,6 +546,8 @@ int sra_rope_kv_store(void* q, const void* k, const void* v, const float* cos, c
     const int sms = current_sm_count(&dev);
     if (sms <= 0) return SRA_ERR_DEVICE;
     const int h = head_dim / 2;
+    // 16 / es pairs per task: two 16-byte accesses (one per half for neox, two
+    // consecutive ones for interleaved)
     int pairs = 16 / es;
     const bool vec_ok = h % pairs == 0 && h % 4 == 0 && aligned16(q) && aligned16(k) && aligned16(v) &&
                         aligned16(kv_cache) && aligned16(cos) && aligned16(sin) &&
@@ -551,7 +555,7 @@ int sra_rope_kv_store(void* q, const void* k, const void* v, const float* cos, c
                         stride_aligned16(v_tok_stride, es);
     if (!vec_ok) pairs = 1;
     RopePlan plan;
-    int st = plan_rope(T, n_head, n_kv_head, head_dim, pairs, sms, &plan);
+    int st = plan_rope(T, n_head, n_kv_head, head_dim, pairs, style, sms, &plan);
     if (st != SRA_OK) return st;
     RopeArgs a;
     a.q = q;
@@ -574,6 +578,16 @@ int sra_rope_kv_store(void* q, const void* k, const void* v, const float* cos, c
     a.num_blocks = num_blocks;
     a.block_size = block_size;
     return status_from(launch_rope_kv_store(a, plan, dtype, static_cast<cudaStream_t>(stream)));
+}
+
+int sra_rope_kv_store(void* q, const void* k, const void* v, const float* cos, const float* sin,
+                      const int64_t* pos, const int64_t* slot_mapping, void* kv_cache, int64_t T, int n_head,
+                      int n_kv_head, int head_dim, int64_t q_tok_stride, int64_t k_tok_stride,
+                      int64_t v_tok_stride, int64_t max_pos, int64_t num_blocks, int block_size,
+                      int32_t* err_count, int dtype, void* stream) {
+    return sra_rope_kv_store_ex(q, k, v, cos, sin, pos, slot_mapping, kv_cache, T, n_head, n_kv_head, head_dim,
+                                q_tok_stride, k_tok_stride, v_tok_stride, max_pos, num_blocks, block_size,
+                                err_count, SRA_ROPE_NEOX, dtype, stream);
 }
 
 int sra_glu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row_stride, int64_t out_row_stride,
@@ -650,7 +664,7 @@ int sra_pick_variant(const char* op, int64_t a, int64_t b, int64_t c, int64_t d,
     if (std::strcmp(op, "rope_kv_store") == 0) {
         if (a < 0 || b <= 0 || c <= 0 || d <= 0 || d % 2) return SRA_ERR_SHAPE;
         RopePlan p;
-        const int st = plan_rope(a, static_cast<int>(b), static_cast<int>(c), static_cast<int>(d), 1, num_sms, &p);
+        const int st = plan_rope(a, static_cast<int>(b), static_cast<int>(c), static_cast<int>(d), 1, 0, num_sms, &p);
         return st == SRA_OK ? p.variant : st;
     }
     if (a < 0 || b <= 0) return SRA_ERR_SHAPE;

@@ -84,7 +84,8 @@ enum RopeVariant { ROPE_TOKEN_CTA = 0, ROPE_NUM_VARIANTS = 1 };
 
 struct RopePlan {
     int variant;
-    int pairs;      // rotation pairs per task: 16 bytes of elements per half, or 1
+    int style;      // 0 = neox (i, i + h), 1 = interleaved (2i, 2i + 1)
+    int pairs;      // rotation pairs per task: 16 bytes of elements per access, or 1
     int threads;    // threads per CTA
     int64_t grid;   // CTAs wanted (tokens are strided over the grid); capped at the resident count
     bool pdl;

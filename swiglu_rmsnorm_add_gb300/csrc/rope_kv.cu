@@ -1,4 +1,4 @@
-// Fused neox RoPE + paged KV-cache store.
+// Fused RoPE (neox halves, or interleaved GPT-J pairs) + paged KV-cache store.
 //
 // koas-w.github.io "preformanceimprovement", section 1: Q, K, V, cos and sin
 // are read once; Q and K are rotated in registers; Q is written back in place;
@@ -33,12 +33,18 @@ __device__ __forceinline__ float diff_of_products(float a, float b, float c, flo
     return f + e;
 }
 
-template <typename T, int P>
+// P rotation pairs per task, two P-element accesses per task in both styles.
+// STYLE 0 (neox): the pairs (i, i + h); the accesses are [i0, i0 + P) and
+// [h + i0, h + i0 + P). STYLE 1 (interleaved, GPT-J): the pairs (2i, 2i + 1);
+// the accesses are the 2P contiguous elements [2 i0, 2 i0 + 2P), split in two.
+template <typename T, int P, int STYLE>
 __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
+    constexpr bool IL = STYLE == 1;
     using V = Vec<T, P>;
     using R = typename V::Raw;
-    using C = Vec<float, (P >= 4 ? 4 : 1)>;  // cos / sin accesses
-    constexpr int CW = P >= 4 ? 4 : 1;
+    constexpr int CW = P >= 4 ? 4 : 1;  // cos / sin floats per access
+    using C = Vec<float, CW>;
+    static_assert(P == 1 || P % 2 == 0, "interleaved pairs split evenly over two accesses");
     if (threadIdx.x == 0 && blockIdx.x < a.T) {
         const int64_t t = blockIdx.x, es = static_cast<int64_t>(sizeof(T));
         prefetch_l2(static_cast<const T*>(a.q) + t * a.qs, static_cast<int64_t>(a.n_head) * a.head_dim * es);
@@ -90,12 +96,29 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
                 src = kind == 1 ? static_cast<const T*>(a.k) + t * a.ks + static_cast<int64_t>(head) * a.head_dim
                                 : static_cast<const T*>(a.v) + t * a.vs + static_cast<int64_t>(head) * a.head_dim;
             }
-            const R lo_r = V::load(src + i0);
-            const R hi_r = V::load(src + h + i0);
+            // element offsets of the task's two accesses
+            const int o0 = IL ? 2 * i0 : i0;
+            const int o1 = IL ? 2 * i0 + P : h + i0;
+            const R r0 = V::load(src + o0);
+            const R r1 = V::load(src + o1);
             if (kind == 2) {  // V: bit copy
-                V::store(dst + i0, lo_r);
-                V::store(dst + h + i0, hi_r);
+                V::store(dst + o0, r0);
+                V::store(dst + o1, r1);
                 continue;
+            }
+            float lo[P], hi[P];
+            if constexpr (IL && P >= 2) {
+                float f0[P], f1[P];
+                V::unpack(r0, f0);
+                V::unpack(r1, f1);
+#pragma unroll
+                for (int j = 0; j < P / 2; ++j) {
+                    lo[j] = f0[2 * j], hi[j] = f0[2 * j + 1];
+                    lo[P / 2 + j] = f1[2 * j], hi[P / 2 + j] = f1[2 * j + 1];
+                }
+            } else {  // neox, or interleaved with one pair: (r0, r1) is (lo, hi)
+                V::unpack(r0, lo);
+                V::unpack(r1, hi);
             }
             float c[P], s[P];
             const float* crow = a.cos + p * h + i0;
@@ -111,16 +134,25 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
                     s[j + q] = sf[q];
                 }
             }
-            float lo[P], hi[P], ylo[P], yhi[P];
-            V::unpack(lo_r, lo);
-            V::unpack(hi_r, hi);
+            float ylo[P], yhi[P];
 #pragma unroll
             for (int j = 0; j < P; ++j) {
                 ylo[j] = diff_of_products(lo[j], c[j], hi[j], s[j]);
                 yhi[j] = diff_of_products(hi[j], c[j], -lo[j], s[j]);
             }
-            V::store(dst + i0, V::pack(ylo));
-            V::store(dst + h + i0, V::pack(yhi));
+            if constexpr (IL && P >= 2) {
+                float f0[P], f1[P];
+#pragma unroll
+                for (int j = 0; j < P / 2; ++j) {
+                    f0[2 * j] = ylo[j], f0[2 * j + 1] = yhi[j];
+                    f1[2 * j] = ylo[P / 2 + j], f1[2 * j + 1] = yhi[P / 2 + j];
+                }
+                V::store(dst + o0, V::pack(f0));
+                V::store(dst + o1, V::pack(f1));
+            } else {
+                V::store(dst + o0, V::pack(ylo));
+                V::store(dst + o1, V::pack(yhi));
+            }
         }
     }
 }
@@ -128,8 +160,15 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
 template <typename T>
 cudaError_t launch_typed(const RopeArgs& a, const RopePlan& p, cudaStream_t s) {
     const dim3 block(p.threads);
-    auto kernel = p.pairs == 1 ? token_cta_kernel<T, 1> : token_cta_kernel<T, vec16<T>()>;
-    if (p.pairs != 1 && p.pairs != vec16<T>()) return cudaErrorInvalidValue;
+    void (*kernel)(RopeArgs) = nullptr;
+    if (p.style == 0) {
+        if (p.pairs == 1) kernel = token_cta_kernel<T, 1, 0>;
+        if (p.pairs == vec16<T>()) kernel = token_cta_kernel<T, vec16<T>(), 0>;
+    } else {
+        if (p.pairs == 1) kernel = token_cta_kernel<T, 1, 1>;
+        if (p.pairs == vec16<T>()) kernel = token_cta_kernel<T, vec16<T>(), 1>;
+    }
+    if (!kernel) return cudaErrorInvalidValue;
     const dim3 grid(persistent_grid(kernel, p.threads, 0, p.num_sms, p.grid));
     return launch_kernel(kernel, grid, block, 0, s, p.pdl, 1, a);
 }

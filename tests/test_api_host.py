@@ -119,6 +119,26 @@ def test_rope_validation(L):
     assert call(cache=V + 2) == ALIAS              # cache overlaps v
 
 
+def test_rope_style_validation(L):
+    """sra_rope_kv_store_ex: the style is checked with the other arguments; the
+    neox entry point is the same call with style 0."""
+    f = L.sra_rope_kv_store_ex
+    Q, K, V, C, S, PO, SL, KV = (P + i * 0x100000 for i in range(8))
+
+    def call(style, T=4, dt=BF16, q=Q):
+        return f(q, K, V, C, S, PO, SL, KV, T, 12, 2, 128, 1536, 256, 256, 32768, 16, 16, None, style, dt, None)
+
+    for style in (-1, 2, 7):
+        assert call(style) == ARG, style
+    assert call(1, dt=3) == DTYPE
+    assert call(1, T=-1) == SHAPE
+    assert call(1, q=None) == NULL
+    assert call(1, T=0) == OK
+    assert call(0, T=0) == OK
+    with pytest.raises(ValueError):
+        sra.rope_kv_store(*([None] * 8), style="gptj")
+
+
 def test_glu_validation(L):
     f = L.sra_glu
     assert f(P, P + 0x100000, 4, 8, 16, 8, 0, 9, None) == DTYPE

@@ -1,4 +1,6 @@
-"""GPU parity: fused neox RoPE + paged KV-cache store vs the oracle.
+"""GPU parity: fused RoPE + paged KV-cache store vs the oracle, in both
+pairings: neox halves (i, i + head_dim/2) and interleaved GPT-J pairs
+(2i, 2i + 1) (m.lsln.cn 21-operator article, section 2.3).
 
 Workload: Qwen2.5-1.5B GQA (12 Q / 2 KV heads, head_dim 128, bf16), T in
 {1, 64, 2048}, positions uniform in [0, 32768), theta 1e6 tables, a
@@ -20,14 +22,17 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-def run_both(inp, max_pos=None, expect_err=None):
+STYLES = ["neox", "interleaved"]
+
+
+def run_both(inp, max_pos=None, expect_err=None, style="neox"):
     d = {k: v.to(DEV) for k, v in inp.items()}
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
     sra.rope_kv_store(d["q"], d["k"], d["v"], d["cos"], d["sin"], d["pos"], d["slot_mapping"], d["kv_cache"],
-                      err_count=err, max_pos=max_pos)
+                      err_count=err, max_pos=max_pos, style=style)
     torch.cuda.synchronize()
     n = oracle.rope_kv_store(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], inp["pos"],
-                             inp["slot_mapping"], inp["kv_cache"], max_pos=max_pos)
+                             inp["slot_mapping"], inp["kv_cache"], max_pos=max_pos, style=style)
     assert int(err.item()) == n
     if expect_err is not None:
         assert n == expect_err
@@ -47,22 +52,61 @@ def check(d, inp, what):
     assert torch.equal(touched_g, touched_o), f"{what}: slot placement"
 
 
+@pytest.mark.parametrize("style", STYLES)
 @pytest.mark.parametrize("T", syn.ROPE_T)
-def test_config_qwen25(T):
+def test_config_qwen25(T, style):
     tables = syn.rope_tables(32768, 128, 1e6)
     inp = syn.rope_inputs(T, 1002, tables=tables)
-    d = run_both(inp, expect_err=0)
-    check(d, inp, f"T={T}")
+    d = run_both(inp, expect_err=0, style=style)
+    check(d, inp, f"T={T} {style}")
 
 
+@pytest.mark.parametrize("style", STYLES)
 @pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
-@pytest.mark.parametrize("n_head,n_kv,hd", [(12, 2, 128), (8, 8, 64), (16, 1, 256), (4, 2, 32), (6, 3, 10)])
-def test_head_layouts_and_dtypes(dtype, n_head, n_kv, hd):
+@pytest.mark.parametrize("n_head,n_kv,hd", [(12, 2, 128), (8, 8, 64), (16, 1, 256), (4, 2, 32), (6, 3, 10),
+                                            (4, 4, 8), (2, 1, 2)])
+def test_head_layouts_and_dtypes(dtype, n_head, n_kv, hd, style):
     tables = syn.rope_tables(4096, hd, 1e4)
     inp = syn.rope_inputs(37, 20, n_head=n_head, n_kv_head=n_kv, head_dim=hd, num_blocks=8, block_size=16,
                           max_pos=4096, dtype=dtype, tables=tables)
-    d = run_both(inp)
-    check(d, inp, f"{n_head}/{n_kv}/{hd} {dtype}")
+    d = run_both(inp, style=style)
+    check(d, inp, f"{n_head}/{n_kv}/{hd} {dtype} {style}")
+
+
+def test_interleaved_ninety_degrees_and_identity():
+    """cos 0, sin 1 turns each pair (x[2i], x[2i+1]) into (-x[2i+1], x[2i]);
+    position 0 is the identity."""
+    inp = syn.rope_inputs(16, 27, num_blocks=4)
+    inp["cos"], inp["sin"] = torch.zeros(32768, 64), torch.ones(32768, 64)
+    q0 = inp["q"].clone()
+    d = run_both(inp, style="interleaved")
+    assert_values_equal(d["q"][..., 0::2], -q0[..., 1::2], "90 degrees, even dims")
+    assert_values_equal(d["q"][..., 1::2], q0[..., 0::2], "90 degrees, odd dims")
+    inp = syn.rope_inputs(16, 28, num_blocks=4)
+    inp["pos"].zero_()
+    q0 = inp["q"].clone()
+    d = run_both(inp, style="interleaved")
+    assert_values_equal(d["q"], q0, "pos 0 is the identity")
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16, torch.float32])
+def test_interleaved_is_neox_on_permuted_dims(dtype):
+    """Interleaved RoPE of x equals neox RoPE of x with its dimensions permuted
+    (evens first, then odds), permuted back: both kernels, bit for bit."""
+    inp = syn.rope_inputs(64, 29, num_blocks=8, dtype=dtype)
+    perm = torch.cat([torch.arange(0, 128, 2), torch.arange(1, 128, 2)])
+    inv = torch.argsort(perm)
+    a = {k: v.to(DEV) for k, v in inp.items()}
+    b = {k: v.to(DEV) for k, v in inp.items()}
+    for key in ("q", "k", "v"):
+        b[key] = b[key][..., perm].contiguous()
+    sra.rope_kv_store(a["q"], a["k"], a["v"], a["cos"], a["sin"], a["pos"], a["slot_mapping"], a["kv_cache"],
+                      style="interleaved")
+    sra.rope_kv_store(b["q"], b["k"], b["v"], b["cos"], b["sin"], b["pos"], b["slot_mapping"], b["kv_cache"])
+    torch.cuda.synchronize()
+    assert_bits_equal(a["q"], b["q"][..., inv], "q")
+    # untouched slots hold the sentinel in both, so the whole cache compares
+    assert_bits_equal(a["kv_cache"], b["kv_cache"][..., inv], "cache")
 
 
 def test_position_zero_identity_and_ninety_degrees():
@@ -81,16 +125,18 @@ def test_position_zero_identity_and_ninety_degrees():
     assert_values_equal(d["q"][..., 64:], q0[..., :64], "90 degrees, second half")
 
 
-def test_padding_bad_slots_and_positions():
+@pytest.mark.parametrize("style", STYLES)
+def test_padding_bad_slots_and_positions(style):
     inp = syn.rope_inputs(8, 23, num_blocks=4)   # 64 slots
     inp["slot_mapping"] = torch.tensor([-1, 3, 64, 5, 1000, 7, -1, 9], dtype=torch.int64)
     inp["pos"] = torch.tensor([1, 2, 3, -4, 5, 32768, 7, 8], dtype=torch.int64)
     # errors: slot 64 and 1000 out of range (2), positions -4 and 32768 (2)
-    d = run_both(inp, expect_err=4)
-    check(d, inp, "padding / errors")
+    d = run_both(inp, expect_err=4, style=style)
+    check(d, inp, f"padding / errors {style}")
 
 
-def test_fused_qkv_views_and_misaligned_scalar_path():
+@pytest.mark.parametrize("style", STYLES)
+def test_fused_qkv_views_and_misaligned_scalar_path(style):
     T, nh, nkv, hd = 40, 12, 2, 128
     W = (nh + 2 * nkv) * hd
     qkv = syn.normal((T, W + 8), 0, 1, torch.bfloat16, 24, 1)   # padded rows
@@ -114,8 +160,8 @@ def test_fused_qkv_views_and_misaligned_scalar_path():
         dc = cache.to(DEV)
         err = torch.zeros(1, dtype=torch.int32, device=DEV)
         sra.rope_kv_store(dq, dk, dv, tables[0].to(DEV), tables[1].to(DEV), pos.to(DEV), slot.to(DEV), dc,
-                          err_count=err)
-        oracle.rope_kv_store(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], pos, slot, cache)
+                          err_count=err, style=style)
+        oracle.rope_kv_store(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], pos, slot, cache, style=style)
         assert_close(dq, inp["q"], f"fused view q off={off}")
         assert_close(dc.cpu()[0], cache[0], "K")
         assert_bits_equal(dc.cpu()[1], cache[1], "V")
@@ -124,10 +170,11 @@ def test_fused_qkv_views_and_misaligned_scalar_path():
         assert_bits_equal(after[:, nh * hd:], buf[:, nh * hd:], "k, v, padding untouched")
 
 
-def test_duplicate_free_large_T_cache_untouched_elsewhere():
+@pytest.mark.parametrize("style", STYLES)
+def test_duplicate_free_large_T_cache_untouched_elsewhere(style):
     inp = syn.rope_inputs(2048, 25)
-    d = run_both(inp, expect_err=0)
-    check(d, inp, "T=2048 full cache")
+    d = run_both(inp, expect_err=0, style=style)
+    check(d, inp, f"T=2048 full cache {style}")
 
 
 def test_zero_tokens():
