@@ -66,6 +66,9 @@ def lib() -> ctypes.CDLL:
             L.orc_rope_kv_store_style.restype = i64
             L.orc_glu.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32]
             L.orc_glu.restype = i32
+            L.orc_uclip.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i32, i32, dbl, dbl,
+                                    i32]
+            L.orc_uclip.restype = i32
             _lib = L
     return _lib
 
@@ -167,3 +170,41 @@ def swiglu(gate_up, out):
 
 def reglu(gate_up, out):
     glu(gate_up, out, "relu")
+
+
+def _nhd(t: torch.Tensor, name: str):
+    """(N, H, D, n_stride, h_stride) of a [N, D] or [N, H, D] view with unit innermost stride."""
+    if t.stride(-1) != 1 and t.shape[-1] > 1:
+        raise ValueError(f"oracle: {name} innermost stride must be 1")
+    if t.dim() == 2:
+        return t.shape[0], 1, t.shape[1], t.stride(0), t.shape[1]
+    if t.dim() == 3:
+        return t.shape[0], t.shape[1], t.shape[2], t.stride(0), t.stride(1)
+    raise ValueError(f"oracle: {name} must be 2-D or 3-D")
+
+
+def uclip(x: torch.Tensor, alpha: torch.Tensor, gamma: torch.Tensor, out: torch.Tensor,
+          clip_min: float = -1.0, clip_max: float = 1.0) -> None:
+    """out <- clamp(alpha * x, clip_min, clip_max) * gamma over the last dimension.
+
+    x and out: [N, D] or [N, H, D] views of one dtype; alpha, gamma: fp32 with 1 (scalar)
+    or D (per-channel) entries."""
+    for t, n in ((x, "x"), (alpha, "alpha"), (gamma, "gamma"), (out, "out")):
+        _cpu(t, n)
+    if alpha.dtype != torch.float32 or gamma.dtype != torch.float32:
+        raise ValueError("oracle: alpha and gamma are fp32")
+    N, H, D, xn, xh = _nhd(x, "x")
+    oN, oH, oD, on, oh = _nhd(out, "out")
+    if (oN, oH, oD) != (N, H, D) or alpha.numel() not in (1, D) or gamma.numel() not in (1, D):
+        raise ValueError("oracle: bad uclip shapes")
+    a, g = alpha.contiguous(), gamma.contiguous()
+    rc = lib().orc_uclip(x.data_ptr(), a.data_ptr(), g.data_ptr(), out.data_ptr(), N, H, D, xn, xh, on, oh,
+                         int(alpha.numel() == D and D > 1), int(gamma.numel() == D and D > 1),
+                         float(clip_min), float(clip_max), _FMT[x.dtype])
+    if rc != 0:
+        raise ValueError("oracle: bad uclip arguments")
+
+
+def dyht(x, alpha, gamma, out):
+    """DyHT: gamma * clamp(alpha * x, -1, 1)."""
+    uclip(x, alpha, gamma, out, -1.0, 1.0)

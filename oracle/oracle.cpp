@@ -1,5 +1,5 @@
 // Plain CPU oracle for the fused per-token decoder path (RMSNorm, residual-add +
-// RMSNorm, neox RoPE with paged KV-cache store, SwiGLU/ReGLU).
+// RMSNorm, RoPE with paged KV-cache store, SwiGLU/ReGLU, UClip/DyHT).
 //
 // TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check and the bench's
 // CPU-baseline leg load this file's library. The CUDA library never links,
@@ -18,9 +18,9 @@
 //           in place, normed result returned).
 //   [lsln]  m.lsln.cn/news/61269, section 2.3 (RMSNorm in fp32, y.to(dtype) once;
 //           precomputed cos/sin caches).
-//   [mer]   mer.dev "AsyncT vllm ..." section 1.1 (KV cache layout
-//           [2, num_blocks, block_size, num_kv_heads, head_size]) and section 3.3
-//           (relu_and_mul for ReGLU).
+//   [mer]   mer.dev "AsyncT vllm ..." section 0 (DyHT replacing RMSNorm), section 1.1
+//           (KV cache layout [2, num_blocks, block_size, num_kv_heads, head_size]) and
+//           section 3.3 (relu_and_mul for ReGLU; the uclip kernel; 3-D Q/K views).
 //   [csdn]  agent.csdn.net "使用Triton实现RMSNorm算子" (rsqrt(sum/D + eps) per row).
 //
 // Parity pins: every function here is pinned by the CPU tests (closed forms,
@@ -331,6 +331,34 @@ int orc_glu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row
                 a = g > 0.0 ? g : 0.0;
             }
             store(out, t * out_row_stride + j, a * u, fmt);
+        }
+    }
+    return 0;
+}
+
+// UClip / DyHT "norm" over rows of D channels: out = clamp(a * x, lo, hi) * g
+// ([mer] section 0: DyHT(x) = y * clamp(a x, -1, 1), replacing every RMSNorm;
+// section 3.3: the uclip kernel's per-channel or scalar alpha and gamma and its
+// clip bounds). x and out are [N, H, D] with element strides (n_stride, h_stride, 1)
+// each, so narrow Q/K views of a fused QKV buffer are read in place. alpha and
+// gamma are fp32, D entries each when per-channel, else one entry. The clamp lets
+// NaN through (a comparison with NaN is false); lo > hi or a NaN bound is an error.
+int orc_uclip(const void* x, const float* alpha, const float* gamma, void* out, int64_t N, int64_t H,
+              int64_t D, int64_t x_n_stride, int64_t x_h_stride, int64_t out_n_stride, int64_t out_h_stride,
+              int alpha_per_channel, int gamma_per_channel, double lo, double hi, int fmt) {
+    FormatSpec s;
+    if (!format_spec(fmt, &s) || N < 0 || H < 0 || D <= 0) return -1;
+    if (std::isnan(lo) || std::isnan(hi) || lo > hi) return -1;
+    for (int64_t n = 0; n < N; ++n) {
+        for (int64_t hh = 0; hh < H; ++hh) {
+            for (int64_t d = 0; d < D; ++d) {
+                const double a = alpha[alpha_per_channel ? d : 0];
+                const double g = gamma[gamma_per_channel ? d : 0];
+                double v = a * load(x, n * x_n_stride + hh * x_h_stride + d, fmt);
+                if (v < lo) v = lo;
+                if (v > hi) v = hi;
+                store(out, n * out_n_stride + hh * out_h_stride + d, v * g, fmt);
+            }
         }
     }
     return 0;
