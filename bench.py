@@ -191,6 +191,28 @@ def build_entries(dev, stream_handle, only=(), companions=False):
                               16, None, style, 2, stream_handle),
                              [inp["q"], inp["k"], inp["v"], inp["pos"], inp["slot_mapping"]], [inp["q"]],
                              keep=inp))
+    if companions:
+        # UClip / DyHT: in place of the hidden-row RMSNorm (scalar alpha, per-channel gamma),
+        # and the Q-head norm in place on a fused QKV buffer (per-channel alpha and gamma)
+        for T in (4096, 65536):
+            name = f"dyht:bf16:{T}x1536"
+            if not want(name):
+                continue
+            x = syn.normal((T, 1536), 0.0, 1.0, torch.bfloat16, 1005, 1).to(dev)
+            a, g = (p.to(dev) for p in syn.uclip_params(1536, False, True, 1005))
+            out = torch.empty_like(x)
+            entries.append(Entry(name, "uclip", 2 * T * 1536 * 2 + 1536 * 4 + 4, T, L.sra_uclip,
+                                 (x.data_ptr(), a.data_ptr(), g.data_ptr(), out.data_ptr(), T, 1, 1536, 1536, 1536,
+                                  1536, 1536, 0, 1, -1.0, 1.0, 2, stream_handle), [x], [out], keep=(x, a, g, out)))
+        T = 32768
+        name = f"uclip_q:bf16:T{T}"
+        if want(name):
+            qkv = syn.qkv_inputs(T, 12, 2, 128, torch.bfloat16, 1006).to(dev)
+            a, g = (p.to(dev) for p in syn.uclip_params(128, True, True, 1006))
+            W = 16 * 128
+            entries.append(Entry(name, "uclip", 2 * T * 12 * 128 * 2 + 2 * 128 * 4, T * 12, L.sra_uclip,
+                                 (qkv.data_ptr(), a.data_ptr(), g.data_ptr(), qkv.data_ptr(), T, 12, 128, W, 128, W,
+                                  128, 1, 1, -1.0, 1.0, 2, stream_handle), [qkv], [qkv], keep=(qkv, a, g)))
     I = syn.LLAMA3_8B_MLP["intermediate"]
     for T in Ts_glu:
         gu = None

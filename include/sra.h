@@ -1,13 +1,15 @@
 /*
  * sra.h — C ABI of the GB300 (sm_103a) per-token decoder-path library.
  *
- * Four bandwidth-bound operators of a transformer decoder layer, each a
+ * Bandwidth-bound operators of a transformer decoder layer, each a
  * hand-written CUDA kernel chosen per shape:
  *
  *   sra_rmsnorm        row-wise RMSNorm, fp32 accumulation
  *   sra_add_rmsnorm    residual add (in place) + RMSNorm
  *   sra_rope_kv_store  neox RoPE of Q and K + paged KV-cache store through slot_mapping (GQA)
+ *                      (sra_rope_kv_store_ex: also the interleaved GPT-J pairing)
  *   sra_glu            SwiGLU silu(gate) * up, or ReGLU relu(gate) * up, over a fused gate_up
+ *   sra_uclip          UClip / DyHT clamp(alpha * x, lo, hi) * gamma over [N, H, D] views
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -35,8 +37,9 @@
  *  [koas] koas-w.github.io "preformanceimprovement": sec. 1 fused RoPE + paged KV
  *         cache store; sec. 2 fused SwiGLU; sec. 3 Triton RMSNorm; sec. 4 fused add + norm.
  *  [lsln] m.lsln.cn/news/61269 "21 个算子": sec. 2.3 RMSNorm and RoPE details.
- *  [mer]  mer.dev "AsyncT vllm 适配加速笔记（一）": sec. 1.1 KV-cache layout;
- *         sec. 3.3 kernel fusion (ReGLU as relu_and_mul; stride-aware kernels).
+ *  [mer]  mer.dev "AsyncT vllm 适配加速笔记（一）": sec. 0 DyHT replacing RMSNorm;
+ *         sec. 1.1 KV-cache layout; sec. 3.3 kernel fusion (ReGLU as relu_and_mul;
+ *         the UClip kernel; stride-aware Q/K views).
  *  [csdn] agent.csdn.net "使用Triton实现RMSNorm算子": RMSNorm kernels and pitfalls.
  */
 #ifndef SRA_H_
@@ -198,9 +201,40 @@ SRA_API int sra_rope_kv_store_ex(void* q, const void* k, const void* v, const fl
 SRA_API int sra_glu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row_stride,
             int64_t out_row_stride, int act, int dtype, void* stream);
 
-/* sra_swiglu — sra_glu with act = SRA_ACT_SILU (the spec call swiglu(gate_up, out, T, I)). */
+/* sra_swiglu — sra_glu with act = SRA_ACT_SILU (the call swiglu(gate_up, out, T, I) on contiguous rows). */
 SRA_API int sra_swiglu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row_stride,
                int64_t out_row_stride, int dtype, void* stream);
+
+/*
+ * sra_uclip — [mer] sec. 0 (DyHT(x) = y * clamp(a x, -1, 1) in place of every
+ * RMSNorm) and sec. 3.3 (one kernel: clamp(alpha * x, clip_min, clip_max) * gamma
+ * with a scalar or per-channel alpha and gamma; Q/K norms on narrow 3-D views of
+ * a fused QKV projection, whose head stride is free).
+ *
+ *   out[n, h, d] = clamp(alpha_d * x[n, h, d], clip_min, clip_max) * gamma_d
+ *
+ * computed in fp32 and rounded once (RNE) to the dtype. DyHT is clip_min = -1,
+ * clip_max = 1. NaN in x passes through the clamp (a comparison with NaN is
+ * false); +-inf clips to a bound.
+ *
+ * x:      [N, H, D] of `dtype`, element strides (x_n_stride, x_h_stride, 1); a
+ *         2-D [rows, D] tensor is N = rows, H = 1. Read only.
+ * alpha:  fp32, D entries if alpha_per_channel (1) else 1 entry (0). Read only.
+ * gamma:  fp32, D entries if gamma_per_channel (1) else 1 entry (0). Read only.
+ * out:    [N, H, D] of `dtype`, strides (out_n_stride, out_h_stride, 1); its rows
+ *         must be pairwise disjoint. out == x with equal strides (in place) is
+ *         allowed; any other overlap of out with x, alpha or gamma is not.
+ * The stride of a dimension of size 1 is ignored.
+ * Errors: unknown dtype -> SRA_ERR_DTYPE; N < 0, H < 0, H >= 2^31 or D <= 0 -> SRA_ERR_SHAPE;
+ * a per-channel flag other than 0 / 1, a NaN bound or clip_min > clip_max ->
+ * SRA_ERR_ARG; a negative stride or out rows that overlap one another ->
+ * SRA_ERR_STRIDE; NULL -> SRA_ERR_NULL; overlap -> SRA_ERR_ALIAS. N * H == 0 is
+ * a no-op.
+ */
+SRA_API int sra_uclip(const void* x, const float* alpha, const float* gamma, void* out, int64_t N, int64_t H,
+                      int64_t D, int64_t x_n_stride, int64_t x_h_stride, int64_t out_n_stride,
+                      int64_t out_h_stride, int alpha_per_channel, int gamma_per_channel, float clip_min,
+                      float clip_max, int dtype, void* stream);
 
 /* Static text for a status code (never NULL). */
 SRA_API const char* sra_status_string(int status);

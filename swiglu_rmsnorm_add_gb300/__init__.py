@@ -1,5 +1,5 @@
 """GB300-native fused per-token decoder path: RMSNorm, residual-add + RMSNorm,
-neox RoPE with paged KV-cache store, SwiGLU / ReGLU.
+RoPE (neox or interleaved) with paged KV-cache store, SwiGLU / ReGLU, UClip / DyHT.
 
 Every operator runs in the hand-written sm_103a CUDA kernels of ``libsra.so``
 (C ABI in ``include/sra.h``). This module only marshals torch tensors into that
@@ -9,6 +9,7 @@ no CPU or PyTorch fallback: without the built library every call raises.
 from ._binding import (  # noqa: F401
     SRAError,
     add_rmsnorm,
+    dyht,
     force_variant,
     glu,
     lib,
@@ -19,9 +20,10 @@ from ._binding import (  # noqa: F401
     set_pdl,
     status_string,
     swiglu,
+    uclip,
     variant_count,
     variant_name,
 )
 
-__all__ = ["rmsnorm", "add_rmsnorm", "rope_kv_store", "swiglu", "reglu", "glu", "lib", "SRAError",
+__all__ = ["rmsnorm", "add_rmsnorm", "rope_kv_store", "swiglu", "reglu", "glu", "uclip", "dyht", "lib", "SRAError",
            "force_variant", "set_pdl", "variant_count", "variant_name", "pick_variant", "status_string"]

@@ -43,8 +43,10 @@ def lib() -> ctypes.CDLL:
             L.sra_rope_kv_store_ex.argtypes = L.sra_rope_kv_store.argtypes[:19] + [i32, i32, vp]
             L.sra_glu.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, vp]
             L.sra_swiglu.argtypes = [vp, vp, i64, i64, i64, i64, i32, vp]
+            L.sra_uclip.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i32, i32, f32, f32, i32,
+                                    vp]
             for fn in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_rope_kv_store_ex", "sra_glu",
-                       "sra_swiglu"):
+                       "sra_swiglu", "sra_uclip"):
                 getattr(L, fn).restype = i32
             L.sra_status_string.argtypes = [i32]
             L.sra_status_string.restype = ctypes.c_char_p
@@ -283,3 +285,52 @@ def swiglu(gate_up: torch.Tensor, out: torch.Tensor | None = None, stream=None) 
 def reglu(gate_up: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """relu(gate) * up over a fused [.., 2I] gate_up."""
     return glu(gate_up, out, "relu", stream)
+
+
+def _nhd(t: torch.Tensor, name: str) -> tuple[int, int, int, int, int]:
+    """(N, H, D, n_stride, h_stride) of a [N, D] or [N, H, D] view with unit innermost stride."""
+    if t.shape[-1] > 1 and t.stride(-1) != 1:
+        raise ValueError(f"{name}: innermost stride must be 1")
+    if t.dim() == 2:
+        return t.shape[0], 1, t.shape[1], t.stride(0), t.shape[1]
+    if t.dim() == 3:
+        return t.shape[0], t.shape[1], t.shape[2], t.stride(0), t.stride(1)
+    raise ValueError(f"{name} must be 2-D [N, D] or 3-D [N, H, D]")
+
+
+def uclip(x: torch.Tensor, alpha: torch.Tensor, gamma: torch.Tensor, out: torch.Tensor | None = None,
+          clip_min: float = -1.0, clip_max: float = 1.0, stream=None) -> torch.Tensor:
+    """out = clamp(alpha * x, clip_min, clip_max) * gamma over the last dimension.
+
+    x, out: [N, D] or [N, H, D] views (any token and head strides; out may be x for
+    in place). alpha, gamma: fp32 with 1 entry (scalar) or D entries (per channel)."""
+    _cuda(x, "x")
+    _cuda(alpha, "alpha")
+    _cuda(gamma, "gamma")
+    if out is None:
+        out = torch.empty(x.shape, dtype=x.dtype, device=x.device)
+    _cuda(out, "out")
+    _same_device(x, alpha, gamma, out)
+    if out.dtype != x.dtype:
+        raise ValueError("x and out must share one dtype")
+    if alpha.dtype != torch.float32 or gamma.dtype != torch.float32:
+        raise ValueError("alpha and gamma must be float32")
+    N, H, D, xn, xh = _nhd(x, "x")
+    oN, oH, oD, on, oh = _nhd(out, "out")
+    if (oN, oH, oD) != (N, H, D):
+        raise ValueError("shape mismatch")
+    for p, name in ((alpha, "alpha"), (gamma, "gamma")):
+        if p.numel() not in (1, D) or (p.numel() > 1 and p.dim() > 0 and p.stride(-1) != 1):
+            raise ValueError(f"{name} must hold 1 or D contiguous entries")
+    with torch.cuda.device(x.device):
+        st = lib().sra_uclip(x.data_ptr(), alpha.data_ptr(), gamma.data_ptr(), out.data_ptr(), N, H, D, xn, xh,
+                             on, oh, int(alpha.numel() == D and D > 1), int(gamma.numel() == D and D > 1),
+                             float(clip_min), float(clip_max), _dtype(x), _stream(x, stream))
+    _check("sra_uclip", st)
+    return out
+
+
+def dyht(x: torch.Tensor, alpha: torch.Tensor, gamma: torch.Tensor, out: torch.Tensor | None = None,
+         stream=None) -> torch.Tensor:
+    """DyHT: gamma * clamp(alpha * x, -1, 1)."""
+    return uclip(x, alpha, gamma, out, -1.0, 1.0, stream)

@@ -474,6 +474,46 @@ int variant_count(const char* op) {
     return SRA_ERR_ARG;
 }
 
+// ------------------------------------------------------------------- UClip plan
+
+// Whether the rows of an [N, H, D] view (element strides n_s, h_s, 1) are
+// pairwise disjoint: heads nested inside tokens, or tokens inside heads.
+// A dimension of size 1 places no constraint through its stride.
+bool rows_disjoint(int64_t N, int64_t H, int64_t D, int64_t n_s, int64_t h_s) {
+    const bool heads_ok = H <= 1 || h_s >= D;
+    const int64_t tok_w = H <= 1 ? D : (H - 1) * h_s + D;
+    if (heads_ok && (N <= 1 || n_s >= tok_w)) return true;
+    const bool toks_ok = N <= 1 || n_s >= D;
+    const int64_t head_w = N <= 1 ? D : (N - 1) * n_s + D;
+    return toks_ok && (H <= 1 || h_s >= head_w);
+}
+
+int uclip_vec(int dt, const UclipArgs& a) {
+    const int es = elem_bytes(dt);
+    for (int bytes = 16; bytes >= es * 2; bytes >>= 1) {
+        const int vec = bytes / es;
+        const int pbytes = 4 * (vec >= 4 ? 4 : vec);
+        bool ok = reinterpret_cast<uintptr_t>(a.x) % bytes == 0 && reinterpret_cast<uintptr_t>(a.out) % bytes == 0 &&
+                  a.D % vec == 0 && (a.N <= 1 || (a.xn % vec == 0 && a.on % vec == 0)) &&
+                  (a.H <= 1 || (a.xh % vec == 0 && a.oh % vec == 0));
+        ok = ok && (!a.alpha_pc || reinterpret_cast<uintptr_t>(a.alpha) % pbytes == 0);
+        ok = ok && (!a.gamma_pc || reinterpret_cast<uintptr_t>(a.gamma) % pbytes == 0);
+        if (ok) return vec;
+    }
+    return 1;
+}
+
+void plan_uclip(int64_t rows, int64_t D, int vec, int num_sms, UclipPlan* p) {
+    const int64_t nv = D / vec;
+    p->vec = vec;
+    p->bx = static_cast<int>(std::min<int64_t>(nv, 256));
+    p->by = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(256 / p->bx, rows)));
+    p->grid_x = ceil_div(nv, p->bx);
+    p->grid_y = std::max<int64_t>(1, ceil_div(rows, p->by));
+    p->pdl = g_pdl;
+    p->num_sms = num_sms;
+}
+
 }  // namespace
 }  // namespace sra
 
@@ -619,6 +659,54 @@ int sra_glu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row
 int sra_swiglu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row_stride,
                int64_t out_row_stride, int dtype, void* stream) {
     return sra_glu(gate_up, out, T, I, in_row_stride, out_row_stride, SRA_ACT_SILU, dtype, stream);
+}
+
+// ------------------------------------------------------------------- UClip
+int sra_uclip(const void* x, const float* alpha, const float* gamma, void* out, int64_t N, int64_t H, int64_t D,
+              int64_t x_n_stride, int64_t x_h_stride, int64_t out_n_stride, int64_t out_h_stride,
+              int alpha_per_channel, int gamma_per_channel, float clip_min, float clip_max, int dtype, void* stream) {
+    if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
+    if (N < 0 || H < 0 || H > INT32_MAX || D <= 0) return SRA_ERR_SHAPE;
+    if ((alpha_per_channel != 0 && alpha_per_channel != 1) || (gamma_per_channel != 0 && gamma_per_channel != 1) ||
+        std::isnan(clip_min) || std::isnan(clip_max) || clip_min > clip_max)
+        return SRA_ERR_ARG;
+    if (x_n_stride < 0 || x_h_stride < 0 || out_n_stride < 0 || out_h_stride < 0 ||
+        !rows_disjoint(N, H, D, out_n_stride, out_h_stride))
+        return SRA_ERR_STRIDE;
+    if (N == 0 || H == 0) return SRA_OK;
+    if (!x || !alpha || !gamma || !out) return SRA_ERR_NULL;
+    const int es = elem_bytes(dtype);
+    // tokens as rows of width (H - 1) * h_stride + D: exact for the equal token
+    // strides of views into one fused buffer, conservative otherwise
+    const int64_t xw = H <= 1 ? D : (H - 1) * x_h_stride + D, ow = H <= 1 ? D : (H - 1) * out_h_stride + D;
+    const bool in_place = out == x && (N <= 1 || out_n_stride == x_n_stride) && (H <= 1 || out_h_stride == x_h_stride);
+    const Span so = span_of(out, N, out_n_stride, ow, es);
+    const Span sa = span_of(alpha, 1, 0, alpha_per_channel ? D : 1, 4), sg = span_of(gamma, 1, 0, gamma_per_channel ? D : 1, 4);
+    if ((!in_place && rows_overlap(out, N, out_n_stride, ow, x, N, x_n_stride, xw, es)) || overlap(so, sa) ||
+        overlap(so, sg))
+        return SRA_ERR_ALIAS;
+    int dev = 0;
+    const int sms = current_sm_count(&dev);
+    if (sms <= 0) return SRA_ERR_DEVICE;
+    UclipArgs a;
+    a.x = x;
+    a.alpha = alpha;
+    a.gamma = gamma;
+    a.out = out;
+    a.N = N;
+    a.H = H;
+    a.D = D;
+    a.xn = N <= 1 ? 0 : x_n_stride;
+    a.xh = H <= 1 ? 0 : x_h_stride;
+    a.on = N <= 1 ? 0 : out_n_stride;
+    a.oh = H <= 1 ? 0 : out_h_stride;
+    a.alpha_pc = alpha_per_channel != 0;
+    a.gamma_pc = gamma_per_channel != 0;
+    a.lo = clip_min;
+    a.hi = clip_max;
+    UclipPlan plan;
+    plan_uclip(N * H, D, uclip_vec(dtype, a), sms, &plan);
+    return status_from(launch_uclip(a, plan, dtype, static_cast<cudaStream_t>(stream)));
 }
 
 int sra_force_variant(const char* op, int variant) {

@@ -116,4 +116,27 @@ struct GluPlan {
 
 cudaError_t launch_glu(const GluArgs& a, const GluPlan& p, int act, int dtype, cudaStream_t s);
 
+// ------------------------------------------------------------------- UClip
+struct UclipArgs {
+    const void* x;       // [N, H, D], strides (xn, xh, 1)
+    const float* alpha;  // D entries if alpha_pc, else 1
+    const float* gamma;  // D entries if gamma_pc, else 1
+    void* out;           // [N, H, D], strides (on, oh, 1)
+    int64_t N, H, D;
+    int64_t xn, xh, on, oh;  // elements
+    bool alpha_pc, gamma_pc;
+    float lo, hi;
+};
+
+struct UclipPlan {
+    int vec;         // elements per access (power of two, <= 16 bytes)
+    int bx, by;      // CTA shape: column groups x rows
+    int64_t grid_x;  // CTAs across the column groups
+    int64_t grid_y;  // CTAs across rows (upper bound; the launcher caps it at one resident wave)
+    bool pdl;
+    int num_sms;
+};
+
+cudaError_t launch_uclip(const UclipArgs& a, const UclipPlan& p, int dtype, cudaStream_t s);
+
 }  // namespace sra

@@ -113,3 +113,24 @@ def rope_inputs(T: int, seed: int, n_head: int = 12, n_kv_head: int = 2, head_di
 
 def glu_inputs(T: int, I: int, dtype: torch.dtype, seed: int):
     return normal((T, 2 * I), 0.0, 1.0, dtype, seed, 21)
+
+
+def uniform(shape, lo: float, hi: float, seed: int, stream: int) -> torch.Tensor:
+    """An fp32 CPU tensor with U(lo, hi) entries."""
+    a = rng(seed, stream).uniform(lo, hi, size=tuple(shape)).astype(np.float32)
+    return torch.from_numpy(a)
+
+
+def uclip_params(D: int, alpha_per_channel: bool, gamma_per_channel: bool, seed: int):
+    """fp32 alpha ~ U(0.25, 1) and gamma ~ N(1, 0.1), D entries each or one.
+
+    With x ~ N(0, 1) a fraction of alpha * x lies outside [-1, 1], so both the
+    clipped and the linear part of the clamp are exercised."""
+    alpha = uniform((D if alpha_per_channel else 1,), 0.25, 1.0, seed, 31)
+    gamma = normal((D if gamma_per_channel else 1,), 1.0, 0.1, torch.float32, seed, 32)
+    return alpha, gamma
+
+
+def qkv_inputs(T: int, n_head: int, n_kv_head: int, head_dim: int, dtype: torch.dtype, seed: int) -> torch.Tensor:
+    """A fused QKV projection output [T, n_head + 2 * n_kv_head, head_dim] ~ N(0, 1)."""
+    return normal((T, n_head + 2 * n_kv_head, head_dim), 0.0, 1.0, dtype, seed, 33)

@@ -35,7 +35,8 @@ def declared_functions():
 
 def test_header_declares_the_api():
     names = declared_functions()
-    for n in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_glu", "sra_swiglu"):
+    for n in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_rope_kv_store_ex", "sra_glu",
+              "sra_swiglu", "sra_uclip"):
         assert n in names
 
 
@@ -139,6 +140,42 @@ def test_rope_style_validation(L):
         sra.rope_kv_store(*([None] * 8), style="gptj")
 
 
+def test_uclip_validation(L):
+    f = L.sra_uclip
+    X, A, G, O = (P + i * 0x100000 for i in range(4))
+
+    def call(**kw):
+        a = dict(x=X, al=A, ga=G, out=O, N=4, H=3, D=64, xn=192, xh=64, on=192, oh=64, apc=1, gpc=0, lo=-1.0,
+                 hi=1.0, dt=BF16)
+        a.update(kw)
+        return f(a["x"], a["al"], a["ga"], a["out"], a["N"], a["H"], a["D"], a["xn"], a["xh"], a["on"], a["oh"],
+                 a["apc"], a["gpc"], a["lo"], a["hi"], a["dt"], None)
+
+    assert call(dt=5) == DTYPE
+    assert call(N=-1) == SHAPE
+    assert call(H=-1) == SHAPE
+    assert call(D=0) == SHAPE
+    assert call(apc=2) == ARG
+    assert call(gpc=-1) == ARG
+    assert call(lo=1.0, hi=-1.0) == ARG
+    assert call(lo=float("nan")) == ARG
+    assert call(hi=float("nan")) == ARG
+    assert call(oh=63) == STRIDE                 # heads of out overlap
+    assert call(on=100) == STRIDE                # tokens of out overlap
+    assert call(xn=-1) == STRIDE
+    for name in ("x", "al", "ga", "out"):
+        assert call(**{name: None}) == NULL, name
+    # heads-outer layout and size-1 dimensions pass the stride check (stopped at NULL)
+    assert call(x=None, on=64, oh=256) == NULL
+    assert call(x=None, H=1, oh=0, xh=0) == NULL
+    assert call(x=None, N=1, on=0, xn=0) == NULL
+    assert call(N=0) == OK
+    assert call(H=0) == OK
+    assert call(out=X + 2) == ALIAS              # x and out overlap, not in place
+    assert call(al=O + 4) == ALIAS               # alpha inside out
+    assert call(ga=O + 4) == ALIAS
+
+
 def test_glu_validation(L):
     f = L.sra_glu
     assert f(P, P + 0x100000, 4, 8, 16, 8, 0, 9, None) == DTYPE
@@ -209,6 +246,10 @@ def test_interleaved_views_are_not_aliases(L):
     I = 64
     assert L.sra_glu(base, base + 2 * I * 2, 4, I, 3 * I, 3 * I, 0, BF16, None) == DEVICE
     assert L.sra_glu(base, base + I * 2, 4, I, 3 * I, 3 * I, 0, BF16, None) == ALIAS
+    # uclip in place on the K heads of a fused QKV buffer
+    assert L.sra_uclip(k, 0x2000000, 0x3000000, k, T, nkv, hd, W, hd, W, hd, 1, 1, -1.0, 1.0, BF16, None) == DEVICE
+    # uclip from the Q heads into the K heads of the same buffer: disjoint
+    assert L.sra_uclip(q, 0x2000000, 0x3000000, k, T, nkv, hd, W, hd, W, hd, 1, 1, -1.0, 1.0, BF16, None) == DEVICE
     # add_rmsnorm: x | res | out interleaved rows of one [rows, 3D] buffer
     D = 32
     assert L.sra_add_rmsnorm(base, base + D * 2, 0x900000, base + 2 * D * 2, 4, D, 3 * D, 3 * D, 3 * D, 1e-6,
