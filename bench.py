@@ -173,10 +173,14 @@ def build_entries(dev, stream_handle, only=(), companions=False):
                              (x.data_ptr(), r.data_ptr(), w.data_ptr(), out.data_ptr(), T, 1536, 1536, 1536, 1536,
                               syn.EPS, 2, stream_handle), [x, r], [x, out], keep=(x, r, w, out)))
     tables = None
-    # (style, T): the neox shapes of the step; the interleaved (GPT-J) pairing as companions
-    ropes = [(0, T) for T in Ts_rope] + ([(1, 2048), (1, 32768)] if companions else [])
-    for style, T in ropes:
-        name = f"rope_kv_store:bf16:T{T}" if style == 0 else f"rope_kv_store_interleaved:bf16:T{T}"
+    # (style, Q/K UClip fused, T): the neox shapes of the step; the interleaved (GPT-J) pairing
+    # and the fused Q/K norm as companions
+    ropes = [(0, False, T) for T in Ts_rope]
+    if companions:
+        ropes += [(1, False, 2048), (1, False, 32768), (0, True, 2048), (0, True, 32768)]
+    for style, qk, T in ropes:
+        kind = ("rope_kv_store" if style == 0 else "rope_kv_store_interleaved") + ("_qk_uclip" if qk else "")
+        name = f"{kind}:bf16:T{T}"
         if not want(name):
             continue
         if tables is None:
@@ -184,11 +188,17 @@ def build_entries(dev, stream_handle, only=(), companions=False):
         nb = max(4096, (T + 15) // 16)
         inp = {k: v.to(dev) for k, v in syn.rope_inputs(T, 1002, num_blocks=nb, tables=tables).items()}
         per_tok = 2 * 12 * 128 * 2 + 2 * 128 * 2 * 2 + 2 * 64 * 4 + 16 + 2 * 2 * 128 * 2
-        entries.append(Entry(name, "rope_kv_store", per_tok * T, T, L.sra_rope_kv_store_ex,
-                             (inp["q"].data_ptr(), inp["k"].data_ptr(), inp["v"].data_ptr(), inp["cos"].data_ptr(),
-                              inp["sin"].data_ptr(), inp["pos"].data_ptr(), inp["slot_mapping"].data_ptr(),
-                              inp["kv_cache"].data_ptr(), T, 12, 2, 128, 12 * 128, 2 * 128, 2 * 128, 32768, nb,
-                              16, None, style, 2, stream_handle),
+        common = (inp["q"].data_ptr(), inp["k"].data_ptr(), inp["v"].data_ptr(), inp["cos"].data_ptr(),
+                  inp["sin"].data_ptr(), inp["pos"].data_ptr(), inp["slot_mapping"].data_ptr(),
+                  inp["kv_cache"].data_ptr(), T, 12, 2, 128, 12 * 128, 2 * 128, 2 * 128, 32768, nb, 16, None, style)
+        if qk:
+            params = [p.to(dev) for i in range(4) for p in (syn.uclip_params(128, True, True, 1002 + i)[i % 2],)]
+            inp = dict(inp, **{f"p{i}": p for i, p in enumerate(params)})
+            fn, args = L.sra_rope_kv_store_qk_uclip, common + tuple(p.data_ptr() for p in params) + (-1.0, 1.0)
+            nbytes = per_tok * T + 4 * 128 * 4
+        else:
+            fn, args, nbytes = L.sra_rope_kv_store_ex, common, per_tok * T
+        entries.append(Entry(name, "rope_kv_store", nbytes, T, fn, args + (2, stream_handle),
                              [inp["q"], inp["k"], inp["v"], inp["pos"], inp["slot_mapping"]], [inp["q"]],
                              keep=inp))
     if companions:

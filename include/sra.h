@@ -7,7 +7,8 @@
  *   sra_rmsnorm        row-wise RMSNorm, fp32 accumulation
  *   sra_add_rmsnorm    residual add (in place) + RMSNorm
  *   sra_rope_kv_store  neox RoPE of Q and K + paged KV-cache store through slot_mapping (GQA)
- *                      (sra_rope_kv_store_ex: also the interleaved GPT-J pairing)
+ *                      (sra_rope_kv_store_ex: also the interleaved GPT-J pairing;
+ *                      sra_rope_kv_store_qk_uclip: with the Q/K UClip norms fused in)
  *   sra_glu            SwiGLU silu(gate) * up, or ReGLU relu(gate) * up, over a fused gate_up
  *   sra_uclip          UClip / DyHT clamp(alpha * x, lo, hi) * gamma over [N, H, D] views
  *
@@ -184,6 +185,29 @@ SRA_API int sra_rope_kv_store_ex(void* q, const void* k, const void* v, const fl
                                  int64_t k_tok_stride, int64_t v_tok_stride, int64_t max_pos,
                                  int64_t num_blocks, int block_size, int32_t* err_count, int style, int dtype,
                                  void* stream);
+
+/*
+ * sra_rope_kv_store_qk_uclip — sra_rope_kv_store_ex with the Q and K norms of
+ * [mer] sec. 3.3 fused into the load: every Q head and every K head is first
+ * replaced by UClip clamp(alpha_d * x_d, clip_min, clip_max) * gamma_d (fp32,
+ * rounded once to the dtype, exactly as sra_uclip would store it) and then rotated;
+ * the normed, rotated K goes to the cache, q holds the normed, rotated Q. V is
+ * copied unchanged. A token whose position is out of range is left as it is (q
+ * not normed either) and counted, as in sra_rope_kv_store.
+ * q_alpha, q_gamma, k_alpha, k_gamma: fp32 device arrays of head_dim entries,
+ * shared by all heads of their kind (pass head_dim copies for a scalar).
+ * Errors: those of sra_rope_kv_store_ex; a NULL parameter -> SRA_ERR_NULL; a NaN
+ * bound or clip_min > clip_max -> SRA_ERR_ARG; a parameter array overlapping q or
+ * the cache -> SRA_ERR_ALIAS.
+ */
+SRA_API int sra_rope_kv_store_qk_uclip(void* q, const void* k, const void* v, const float* cos, const float* sin,
+                                       const int64_t* pos, const int64_t* slot_mapping, void* kv_cache, int64_t T,
+                                       int n_head, int n_kv_head, int head_dim, int64_t q_tok_stride,
+                                       int64_t k_tok_stride, int64_t v_tok_stride, int64_t max_pos,
+                                       int64_t num_blocks, int block_size, int32_t* err_count, int style,
+                                       const float* q_alpha, const float* q_gamma, const float* k_alpha,
+                                       const float* k_gamma, float clip_min, float clip_max, int dtype,
+                                       void* stream);
 
 /*
  * sra_glu — [koas] sec. 2 (SwiGLU: gate and up loaded together, activation and

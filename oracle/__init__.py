@@ -208,3 +208,26 @@ def uclip(x: torch.Tensor, alpha: torch.Tensor, gamma: torch.Tensor, out: torch.
 def dyht(x, alpha, gamma, out):
     """DyHT: gamma * clamp(alpha * x, -1, 1)."""
     uclip(x, alpha, gamma, out, -1.0, 1.0)
+
+
+def qk_uclip_rope_kv_store(q, k, v, cos, sin, pos, slot_mapping, kv_cache, q_alpha, q_gamma, k_alpha, k_gamma,
+                           clip_min: float = -1.0, clip_max: float = 1.0, max_pos: int | None = None,
+                           style: str = "neox") -> int:
+    """The Q/K norm followed by RoPE + KV store, as the two oracle operators in sequence.
+
+    Tokens whose position lies in [0, max_pos) get q <- uclip(q) (rounded to the dtype)
+    and a normed copy of k; the others are left to rope_kv_store, which leaves their q
+    unchanged, caches nothing and counts them. k itself is not modified."""
+    if max_pos is None:
+        max_pos = cos.shape[0]
+    ok = (pos >= 0) & (pos < max_pos)
+    kn = k.clone()
+    if bool(ok.any()):
+        idx = ok.nonzero().flatten()
+        qs = q[idx].clone()
+        uclip(qs, q_alpha, q_gamma, qs, clip_min, clip_max)
+        q[idx] = qs
+        ks = kn[idx].clone()
+        uclip(ks, k_alpha, k_gamma, ks, clip_min, clip_max)
+        kn[idx] = ks
+    return rope_kv_store(q, kn, v, cos, sin, pos, slot_mapping, kv_cache, max_pos=max_pos, style=style)

@@ -343,21 +343,30 @@ int orc_glu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row
 // each, so narrow Q/K views of a fused QKV buffer are read in place. alpha and
 // gamma are fp32, D entries each when per-channel, else one entry. The clamp lets
 // NaN through (a comparison with NaN is false); lo > hi or a NaN bound is an error.
+//
+// Precision: the page's kernel fixes it. It converts x to float and evaluates
+// a * x and the product with g in float, so this function does the same: two
+// fp32 roundings (a * x, then * g) around the clamp, with the bounds taken as
+// fp32 values, then one RNE to the output format.
 int orc_uclip(const void* x, const float* alpha, const float* gamma, void* out, int64_t N, int64_t H,
               int64_t D, int64_t x_n_stride, int64_t x_h_stride, int64_t out_n_stride, int64_t out_h_stride,
               int alpha_per_channel, int gamma_per_channel, double lo, double hi, int fmt) {
     FormatSpec s;
     if (!format_spec(fmt, &s) || N < 0 || H < 0 || D <= 0) return -1;
     if (std::isnan(lo) || std::isnan(hi) || lo > hi) return -1;
+    const float lo32 = static_cast<float>(lo), hi32 = static_cast<float>(hi);
     for (int64_t n = 0; n < N; ++n) {
         for (int64_t hh = 0; hh < H; ++hh) {
             for (int64_t d = 0; d < D; ++d) {
-                const double a = alpha[alpha_per_channel ? d : 0];
-                const double g = gamma[gamma_per_channel ? d : 0];
-                double v = a * load(x, n * x_n_stride + hh * x_h_stride + d, fmt);
-                if (v < lo) v = lo;
-                if (v > hi) v = hi;
-                store(out, n * out_n_stride + hh * out_h_stride + d, v * g, fmt);
+                const float a = alpha[alpha_per_channel ? d : 0];
+                const float g = gamma[gamma_per_channel ? d : 0];
+                // a value of any of the three formats is exact in float
+                const float xf = static_cast<float>(load(x, n * x_n_stride + hh * x_h_stride + d, fmt));
+                float v = a * xf;
+                if (v < lo32) v = lo32;
+                if (v > hi32) v = hi32;
+                const float y = v * g;
+                store(out, n * out_n_stride + hh * out_h_stride + d, static_cast<double>(y), fmt);
             }
         }
     }

@@ -41,12 +41,14 @@ def lib() -> ctypes.CDLL:
             L.sra_rope_kv_store.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i64,
                                             i64, i64, i64, i32, vp, i32, vp]
             L.sra_rope_kv_store_ex.argtypes = L.sra_rope_kv_store.argtypes[:19] + [i32, i32, vp]
+            L.sra_rope_kv_store_qk_uclip.argtypes = L.sra_rope_kv_store.argtypes[:19] + [i32, vp, vp, vp, vp, f32,
+                                                                                        f32, i32, vp]
             L.sra_glu.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, vp]
             L.sra_swiglu.argtypes = [vp, vp, i64, i64, i64, i64, i32, vp]
             L.sra_uclip.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i32, i32, f32, f32, i32,
                                     vp]
             for fn in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_rope_kv_store_ex", "sra_glu",
-                       "sra_swiglu", "sra_uclip"):
+                       "sra_swiglu", "sra_uclip", "sra_rope_kv_store_qk_uclip"):
                 getattr(L, fn).restype = i32
             L.sra_status_string.argtypes = [i32]
             L.sra_status_string.restype = ctypes.c_char_p
@@ -208,10 +210,13 @@ ROPE_STYLE = {"neox": 0, "interleaved": 1}
 def rope_kv_store(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.Tensor, sin: torch.Tensor,
                   pos: torch.Tensor, slot_mapping: torch.Tensor, kv_cache: torch.Tensor,
                   err_count: torch.Tensor | None = None, max_pos: int | None = None, stream=None,
-                  style: str = "neox") -> None:
+                  style: str = "neox", qk_uclip=None, clip: tuple[float, float] = (-1.0, 1.0)) -> None:
     """Rotate q in place; write rotated k and v into kv_cache[0/1, slot // bs, slot % bs].
 
-    style: "neox" pairs (i, i + head_dim/2); "interleaved" (GPT-J) pairs (2i, 2i + 1)."""
+    style: "neox" pairs (i, i + head_dim/2); "interleaved" (GPT-J) pairs (2i, 2i + 1).
+    qk_uclip: None, or (q_alpha, q_gamma, k_alpha, k_gamma), fp32 [head_dim] tensors: Q and K
+    heads first become clamp(alpha * x, *clip) * gamma (DyHT for the default clip), fused into
+    the same kernel."""
     if style not in ROPE_STYLE:
         raise ValueError("style must be 'neox' or 'interleaved'")
     for t, n in ((q, "q"), (k, "k"), (v, "v"), (cos, "cos"), (sin, "sin"), (pos, "pos"),
@@ -242,14 +247,27 @@ def rope_kv_store(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, cos: torch.
         max_pos = cos.shape[0]
     if cos.shape[-1] != hd // 2 or sin.shape != cos.shape or max_pos > cos.shape[0]:
         raise ValueError("cos / sin tables must be [>= max_pos, head_dim // 2]")
+    args = (q.data_ptr(), k.data_ptr(), v.data_ptr(), cos.data_ptr(), sin.data_ptr(), pos.data_ptr(),
+            slot_mapping.data_ptr(), kv_cache.data_ptr(), T, n_head, n_kv, hd, _tok_stride(q, "q"),
+            _tok_stride(k, "k"), _tok_stride(v, "v"), int(max_pos), nb, bs,
+            err_count.data_ptr() if err_count is not None else None, ROPE_STYLE[style])
+    if qk_uclip is None:
+        with torch.cuda.device(q.device):
+            st = lib().sra_rope_kv_store_ex(*args, _dtype(q), _stream(q, stream))
+        _check("sra_rope_kv_store_ex", st)
+        return
+    params = tuple(qk_uclip)
+    if len(params) != 4:
+        raise ValueError("qk_uclip is (q_alpha, q_gamma, k_alpha, k_gamma)")
+    for t, n in zip(params, ("q_alpha", "q_gamma", "k_alpha", "k_gamma")):
+        _cuda(t, n)
+        if t.dtype != torch.float32 or t.numel() != hd or not t.is_contiguous():
+            raise ValueError(f"{n} must be a contiguous float32 tensor of head_dim entries")
+    _same_device(q, *params)
     with torch.cuda.device(q.device):
-        st = lib().sra_rope_kv_store_ex(q.data_ptr(), k.data_ptr(), v.data_ptr(), cos.data_ptr(), sin.data_ptr(),
-                                        pos.data_ptr(), slot_mapping.data_ptr(), kv_cache.data_ptr(), T, n_head,
-                                        n_kv, hd, _tok_stride(q, "q"), _tok_stride(k, "k"), _tok_stride(v, "v"),
-                                        int(max_pos), nb, bs,
-                                        err_count.data_ptr() if err_count is not None else None,
-                                        ROPE_STYLE[style], _dtype(q), _stream(q, stream))
-    _check("sra_rope_kv_store_ex", st)
+        st = lib().sra_rope_kv_store_qk_uclip(*args, *(t.data_ptr() for t in params), float(clip[0]),
+                                              float(clip[1]), _dtype(q), _stream(q, stream))
+    _check("sra_rope_kv_store_qk_uclip", st)
 
 
 def glu(gate_up: torch.Tensor, out: torch.Tensor | None = None, act: str = "silu", stream=None) -> torch.Tensor:

@@ -356,6 +356,7 @@ int plan_rope(int64_t T, int n_head, int n_kv, int head_dim, int pairs, int styl
     const int64_t U = static_cast<int64_t>(n_head + 2 * n_kv) * (h / pairs);
     p->variant = ROPE_TOKEN_CTA;
     p->style = style;
+    p->qk_norm = false;
     p->pairs = pairs;
     p->pdl = g_pdl;
     p->num_sms = num_sms;
@@ -514,6 +515,88 @@ void plan_uclip(int64_t rows, int64_t D, int vec, int num_sms, UclipPlan* p) {
     p->num_sms = num_sms;
 }
 
+// RoPE + KV store, optionally with the UClip of Q and K (norm != nullptr: qa, qg,
+// ka, kg per-channel fp32 parameters of head_dim entries, then the clip bounds).
+struct QkNorm {
+    const float *qa, *qg, *ka, *kg;
+    float lo, hi;
+};
+
+int rope_impl(void* q, const void* k, const void* v, const float* cos, const float* sin, const int64_t* pos,
+              const int64_t* slot_mapping, void* kv_cache, int64_t T, int n_head, int n_kv_head, int head_dim,
+              int64_t q_tok_stride, int64_t k_tok_stride, int64_t v_tok_stride, int64_t max_pos, int64_t num_blocks,
+              int block_size, int32_t* err_count, int style, const QkNorm* norm, int dtype, void* stream) {
+    if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
+    if (style != SRA_ROPE_NEOX && style != SRA_ROPE_INTERLEAVED) return SRA_ERR_ARG;
+    if (T < 0 || n_head <= 0 || n_kv_head <= 0 || n_head % n_kv_head != 0 || head_dim <= 0 || head_dim % 2 != 0 ||
+        block_size <= 0 || num_blocks < 0 || max_pos < 0)
+        return SRA_ERR_SHAPE;
+    const int64_t qw = static_cast<int64_t>(n_head) * head_dim, kw = static_cast<int64_t>(n_kv_head) * head_dim;
+    if (q_tok_stride < qw || k_tok_stride < kw || v_tok_stride < kw) return SRA_ERR_STRIDE;
+    if (T == 0) return SRA_OK;
+    if (!q || !k || !v || !cos || !sin || !pos || !slot_mapping || !kv_cache) return SRA_ERR_NULL;
+    if (norm && (!norm->qa || !norm->qg || !norm->ka || !norm->kg)) return SRA_ERR_NULL;
+    const int es = elem_bytes(dtype);
+    const Span sq = span_of(q, T, q_tok_stride, qw, es), sk = span_of(k, T, k_tok_stride, kw, es),
+               sv = span_of(v, T, v_tok_stride, kw, es);
+    const Span sc = span_of(kv_cache, 1, 0, 2 * num_blocks * block_size * kw, es);
+    if (rows_overlap(q, T, q_tok_stride, qw, k, T, k_tok_stride, kw, es) ||
+        rows_overlap(q, T, q_tok_stride, qw, v, T, v_tok_stride, kw, es) || overlap(sc, sq) || overlap(sc, sk) ||
+        overlap(sc, sv))
+        return SRA_ERR_ALIAS;
+    if (norm) {
+        // the parameters are read while q and the cache are written
+        const float* ps[4] = {norm->qa, norm->qg, norm->ka, norm->kg};
+        for (const float* pp : ps) {
+            const Span sp = span_of(pp, 1, 0, head_dim, 4);
+            if (overlap(sp, sq) || overlap(sp, sc)) return SRA_ERR_ALIAS;
+        }
+    }
+    int dev = 0;
+    const int sms = current_sm_count(&dev);
+    if (sms <= 0) return SRA_ERR_DEVICE;
+    const int h = head_dim / 2;
+    // 16 / es pairs per task: two 16-byte accesses (one per half for neox, two
+    // consecutive ones for interleaved)
+    int pairs = 16 / es;
+    const bool vec_ok = h % pairs == 0 && h % 4 == 0 && aligned16(q) && aligned16(k) && aligned16(v) &&
+                        aligned16(kv_cache) && aligned16(cos) && aligned16(sin) &&
+                        stride_aligned16(q_tok_stride, es) && stride_aligned16(k_tok_stride, es) &&
+                        stride_aligned16(v_tok_stride, es) &&
+                        (!norm || (aligned16(norm->qa) && aligned16(norm->qg) && aligned16(norm->ka) &&
+                                   aligned16(norm->kg)));
+    if (!vec_ok) pairs = 1;
+    RopePlan plan;
+    int st = plan_rope(T, n_head, n_kv_head, head_dim, pairs, style, sms, &plan);
+    if (st != SRA_OK) return st;
+    plan.qk_norm = norm != nullptr;
+    RopeArgs a;
+    a.q = q;
+    a.k = k;
+    a.v = v;
+    a.cos = cos;
+    a.sin = sin;
+    a.pos = pos;
+    a.slot = slot_mapping;
+    a.cache = kv_cache;
+    a.err = err_count;
+    a.T = T;
+    a.n_head = n_head;
+    a.n_kv = n_kv_head;
+    a.head_dim = head_dim;
+    a.qs = q_tok_stride;
+    a.ks = k_tok_stride;
+    a.vs = v_tok_stride;
+    a.max_pos = max_pos;
+    a.num_blocks = num_blocks;
+    a.block_size = block_size;
+    if (norm) {
+        a.qa = norm->qa, a.qg = norm->qg, a.ka = norm->ka, a.kg = norm->kg;
+        a.clip_lo = norm->lo, a.clip_hi = norm->hi;
+    }
+    return status_from(launch_rope_kv_store(a, plan, dtype, static_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 }  // namespace sra
 
@@ -565,59 +648,23 @@ int sra_rope_kv_store_ex(void* q, const void* k, const void* v, const float* cos
                          int n_kv_head, int head_dim, int64_t q_tok_stride, int64_t k_tok_stride,
                          int64_t v_tok_stride, int64_t max_pos, int64_t num_blocks, int block_size,
                          int32_t* err_count, int style, int dtype, void* stream) {
-    if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
-    if (style != SRA_ROPE_NEOX && style != SRA_ROPE_INTERLEAVED) return SRA_ERR_ARG;
-    if (T < 0 || n_head <= 0 || n_kv_head <= 0 || n_head % n_kv_head != 0 || head_dim <= 0 || head_dim % 2 != 0 ||
-        block_size <= 0 || num_blocks < 0 || max_pos < 0)
-        return SRA_ERR_SHAPE;
-    const int64_t qw = static_cast<int64_t>(n_head) * head_dim, kw = static_cast<int64_t>(n_kv_head) * head_dim;
-    if (q_tok_stride < qw || k_tok_stride < kw || v_tok_stride < kw) return SRA_ERR_STRIDE;
-    if (T == 0) return SRA_OK;
-    if (!q || !k || !v || !cos || !sin || !pos || !slot_mapping || !kv_cache) return SRA_ERR_NULL;
-    const int es = elem_bytes(dtype);
-    const Span sq = span_of(q, T, q_tok_stride, qw, es), sk = span_of(k, T, k_tok_stride, kw, es),
-               sv = span_of(v, T, v_tok_stride, kw, es);
-    const Span sc = span_of(kv_cache, 1, 0, 2 * num_blocks * block_size * kw, es);
-    if (rows_overlap(q, T, q_tok_stride, qw, k, T, k_tok_stride, kw, es) ||
-        rows_overlap(q, T, q_tok_stride, qw, v, T, v_tok_stride, kw, es) || overlap(sc, sq) || overlap(sc, sk) ||
-        overlap(sc, sv))
-        return SRA_ERR_ALIAS;
-    int dev = 0;
-    const int sms = current_sm_count(&dev);
-    if (sms <= 0) return SRA_ERR_DEVICE;
-    const int h = head_dim / 2;
-    // 16 / es pairs per task: two 16-byte accesses (one per half for neox, two
-    // consecutive ones for interleaved)
-    int pairs = 16 / es;
-    const bool vec_ok = h % pairs == 0 && h % 4 == 0 && aligned16(q) && aligned16(k) && aligned16(v) &&
-                        aligned16(kv_cache) && aligned16(cos) && aligned16(sin) &&
-                        stride_aligned16(q_tok_stride, es) && stride_aligned16(k_tok_stride, es) &&
-                        stride_aligned16(v_tok_stride, es);
-    if (!vec_ok) pairs = 1;
-    RopePlan plan;
-    int st = plan_rope(T, n_head, n_kv_head, head_dim, pairs, style, sms, &plan);
-    if (st != SRA_OK) return st;
-    RopeArgs a;
-    a.q = q;
-    a.k = k;
-    a.v = v;
-    a.cos = cos;
-    a.sin = sin;
-    a.pos = pos;
-    a.slot = slot_mapping;
-    a.cache = kv_cache;
-    a.err = err_count;
-    a.T = T;
-    a.n_head = n_head;
-    a.n_kv = n_kv_head;
-    a.head_dim = head_dim;
-    a.qs = q_tok_stride;
-    a.ks = k_tok_stride;
-    a.vs = v_tok_stride;
-    a.max_pos = max_pos;
-    a.num_blocks = num_blocks;
-    a.block_size = block_size;
-    return status_from(launch_rope_kv_store(a, plan, dtype, static_cast<cudaStream_t>(stream)));
+    return rope_impl(q, k, v, cos, sin, pos, slot_mapping, kv_cache, T, n_head, n_kv_head, head_dim, q_tok_stride,
+                     k_tok_stride, v_tok_stride, max_pos, num_blocks, block_size, err_count, style, nullptr, dtype,
+                     stream);
+}
+
+int sra_rope_kv_store_qk_uclip(void* q, const void* k, const void* v, const float* cos, const float* sin,
+                               const int64_t* pos, const int64_t* slot_mapping, void* kv_cache, int64_t T,
+                               int n_head, int n_kv_head, int head_dim, int64_t q_tok_stride, int64_t k_tok_stride,
+                               int64_t v_tok_stride, int64_t max_pos, int64_t num_blocks, int block_size,
+                               int32_t* err_count, int style, const float* q_alpha, const float* q_gamma,
+                               const float* k_alpha, const float* k_gamma, float clip_min, float clip_max,
+                               int dtype, void* stream) {
+    if (std::isnan(clip_min) || std::isnan(clip_max) || clip_min > clip_max) return SRA_ERR_ARG;
+    const QkNorm norm{q_alpha, q_gamma, k_alpha, k_gamma, clip_min, clip_max};
+    return rope_impl(q, k, v, cos, sin, pos, slot_mapping, kv_cache, T, n_head, n_kv_head, head_dim, q_tok_stride,
+                     k_tok_stride, v_tok_stride, max_pos, num_blocks, block_size, err_count, style, &norm, dtype,
+                     stream);
 }
 
 int sra_rope_kv_store(void* q, const void* k, const void* v, const float* cos, const float* sin,

@@ -78,6 +78,12 @@ struct RopeArgs {
     int64_t qs, ks, vs;  // token strides, elements
     int64_t max_pos, num_blocks;
     int block_size;
+    // optional UClip of Q and K before the rotation (per-channel fp32, head_dim entries)
+    const float* qa = nullptr;
+    const float* qg = nullptr;
+    const float* ka = nullptr;
+    const float* kg = nullptr;
+    float clip_lo = 0.0f, clip_hi = 0.0f;
 };
 
 enum RopeVariant { ROPE_TOKEN_CTA = 0, ROPE_NUM_VARIANTS = 1 };
@@ -85,6 +91,7 @@ enum RopeVariant { ROPE_TOKEN_CTA = 0, ROPE_NUM_VARIANTS = 1 };
 struct RopePlan {
     int variant;
     int style;      // 0 = neox (i, i + h), 1 = interleaved (2i, 2i + 1)
+    bool qk_norm;   // UClip Q and K heads before rotating (RopeArgs::qa..kg)
     int pairs;      // rotation pairs per task: 16 bytes of elements per access, or 1
     int threads;    // threads per CTA
     int64_t grid;   // CTAs wanted (tokens are strided over the grid); capped at the resident count

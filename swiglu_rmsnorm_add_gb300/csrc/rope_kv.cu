@@ -33,11 +33,54 @@ __device__ __forceinline__ float diff_of_products(float a, float b, float c, flo
     return f + e;
 }
 
+// The per-channel parameters of the dimensions a task's lo[j] / hi[j] hold:
+// neox lo = i0 + j, hi = h + i0 + j; interleaved lo = 2 (i0 + j), hi = lo + 1.
+template <int P, bool IL>
+__device__ __forceinline__ void load_pair_params(const float* p, int i0, int h, float (&lo)[P], float (&hi)[P]) {
+    constexpr int CW = P >= 4 ? 4 : 1;
+    using C = Vec<float, CW>;
+    if constexpr (IL && P >= 2) {
+#pragma unroll
+        for (int j = 0; j < 2 * P; j += CW) {
+            float f[CW];
+            C::unpack(C::load(p + 2 * i0 + j), f);
+#pragma unroll
+            for (int q = 0; q < CW; ++q) {
+                if ((j + q) % 2 == 0) lo[(j + q) / 2] = f[q];
+                else hi[(j + q) / 2] = f[q];
+            }
+        }
+    } else {
+        const float* plo = IL ? p + 2 * i0 : p + i0;
+        const float* phi = IL ? p + 2 * i0 + 1 : p + h + i0;
+#pragma unroll
+        for (int j = 0; j < P; j += CW) {
+            float fl[CW], fh[CW];
+            C::unpack(C::load(plo + j), fl);
+            C::unpack(C::load(phi + j), fh);
+#pragma unroll
+            for (int q = 0; q < CW; ++q) lo[j + q] = fl[q], hi[j + q] = fh[q];
+        }
+    }
+}
+
+__device__ __forceinline__ float uclip1(float x, float a, float g, float lo, float hi) {
+    float v = a * x;
+    v = v < lo ? lo : v;
+    v = v > hi ? hi : v;
+    return v * g;
+}
+
 // P rotation pairs per task, two P-element accesses per task in both styles.
 // STYLE 0 (neox): the pairs (i, i + h); the accesses are [i0, i0 + P) and
 // [h + i0, h + i0 + P). STYLE 1 (interleaved, GPT-J): the pairs (2i, 2i + 1);
 // the accesses are the 2P contiguous elements [2 i0, 2 i0 + 2P), split in two.
-template <typename T, int P, int STYLE>
+//
+// NORM: Q and K heads first go through UClip clamp(a x, lo, hi) * g with
+// per-channel parameters (mer.dev "AsyncT vllm 适配加速笔记（一）", section 3.3: the
+// Q/K norms of the fused QKV output), rounded to T as the separate norm kernel
+// would store them, then rotated. A token with a bad position is left as is.
+template <typename T, int P, int STYLE, bool NORM>
 __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
     constexpr bool IL = STYLE == 1;
     using V = Vec<T, P>;
@@ -120,6 +163,17 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
                 V::unpack(r0, lo);
                 V::unpack(r1, hi);
             }
+            if constexpr (NORM) {
+                // parameters from L1: 4P floats per task, the same for every token
+                float alo[P], ahi[P], glo[P], ghi[P];
+                load_pair_params<P, IL>(kind == 0 ? a.qa : a.ka, i0, h, alo, ahi);
+                load_pair_params<P, IL>(kind == 0 ? a.qg : a.kg, i0, h, glo, ghi);
+#pragma unroll
+                for (int j = 0; j < P; ++j) {
+                    lo[j] = round_to<T>(uclip1(lo[j], alo[j], glo[j], a.clip_lo, a.clip_hi));
+                    hi[j] = round_to<T>(uclip1(hi[j], ahi[j], ghi[j], a.clip_lo, a.clip_hi));
+                }
+            }
             float c[P], s[P];
             const float* crow = a.cos + p * h + i0;
             const float* srow = a.sin + p * h + i0;
@@ -157,16 +211,27 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
     }
 }
 
+template <typename T, bool NORM>
+void (*pick(const RopePlan& p))(RopeArgs) {
+    constexpr int V = vec16<T>();
+    if (p.style == 0) {
+        if (p.pairs == 1) return token_cta_kernel<T, 1, 0, NORM>;
+        if (p.pairs == V) return token_cta_kernel<T, V, 0, NORM>;
+    } else {
+        if (p.pairs == 1) return token_cta_kernel<T, 1, 1, NORM>;
+        if (p.pairs == V) return token_cta_kernel<T, V, 1, NORM>;
+    }
+    return nullptr;
+}
+
 template <typename T>
 cudaError_t launch_typed(const RopeArgs& a, const RopePlan& p, cudaStream_t s) {
     const dim3 block(p.threads);
     void (*kernel)(RopeArgs) = nullptr;
-    if (p.style == 0) {
-        if (p.pairs == 1) kernel = token_cta_kernel<T, 1, 0>;
-        if (p.pairs == vec16<T>()) kernel = token_cta_kernel<T, vec16<T>(), 0>;
+    if (p.qk_norm) {
+        kernel = pick<T, true>(p);
     } else {
-        if (p.pairs == 1) kernel = token_cta_kernel<T, 1, 1>;
-        if (p.pairs == vec16<T>()) kernel = token_cta_kernel<T, vec16<T>(), 1>;
+        kernel = pick<T, false>(p);
     }
     if (!kernel) return cudaErrorInvalidValue;
     const dim3 grid(persistent_grid(kernel, p.threads, 0, p.num_sms, p.grid));

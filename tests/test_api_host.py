@@ -140,6 +140,27 @@ def test_rope_style_validation(L):
         sra.rope_kv_store(*([None] * 8), style="gptj")
 
 
+def test_rope_qk_uclip_validation(L):
+    f = L.sra_rope_kv_store_qk_uclip
+    Q, K, V, C, S, PO, SL, KV, QA, QG, KA, KG = (P + i * 0x100000 for i in range(12))
+
+    def call(**kw):
+        a = dict(q=Q, cache=KV, T=4, style=0, qa=QA, qg=QG, ka=KA, kg=KG, lo=-1.0, hi=1.0, dt=BF16)
+        a.update(kw)
+        return f(a["q"], K, V, C, S, PO, SL, a["cache"], a["T"], 12, 2, 128, 1536, 256, 256, 32768, 16, 16, None,
+                 a["style"], a["qa"], a["qg"], a["ka"], a["kg"], a["lo"], a["hi"], a["dt"], None)
+
+    assert call(lo=1.0, hi=0.0) == ARG
+    assert call(hi=float("nan")) == ARG
+    assert call(style=3) == ARG
+    assert call(dt=9) == DTYPE
+    for name in ("qa", "qg", "ka", "kg"):
+        assert call(**{name: None}) == NULL, name
+    assert call(qa=Q + 64) == ALIAS              # a parameter array inside q
+    assert call(kg=KV + 64) == ALIAS             # ... or inside the cache
+    assert call(T=0) == OK
+
+
 def test_uclip_validation(L):
     f = L.sra_uclip
     X, A, G, O = (P + i * 0x100000 for i in range(4))

@@ -182,3 +182,90 @@ def test_zero_tokens():
     d = {k: v.to(DEV) for k, v in inp.items()}
     sra.rope_kv_store(d["q"], d["k"], d["v"], d["cos"], d["sin"], d["pos"], d["slot_mapping"], d["kv_cache"])
     assert_bits_equal(d["kv_cache"], inp["kv_cache"], "no-op")
+
+
+# ------------------------------------------------ Q/K UClip fused into the load
+def _qk_params(hd, seed):
+    return tuple(syn.uclip_params(hd, True, True, seed + i)[i % 2] for i in range(4))
+
+
+@pytest.mark.parametrize("style", STYLES)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("T,n_head,n_kv,hd", [(64, 12, 2, 128), (2048, 12, 2, 128), (37, 8, 8, 64), (29, 6, 3, 10),
+                                              (5, 16, 1, 256)])
+def test_qk_uclip_fused_vs_oracle(style, dtype, T, n_head, n_kv, hd):
+    """Fused Q/K norm + RoPE + store vs the oracle's uclip-then-rope composition."""
+    max_pos = 32768 if hd == 128 else 4096
+    tables = syn.rope_tables(max_pos, hd, 1e6 if hd == 128 else 1e4)
+    inp = syn.rope_inputs(T, 30, n_head=n_head, n_kv_head=n_kv, head_dim=hd,
+                          num_blocks=max(8, (T + 15) // 16), max_pos=max_pos, dtype=dtype, tables=tables)
+    params = _qk_params(hd, 30)
+    d = {k: v.to(DEV) for k, v in inp.items()}
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sra.rope_kv_store(d["q"], d["k"], d["v"], d["cos"], d["sin"], d["pos"], d["slot_mapping"], d["kv_cache"],
+                      err_count=err, style=style, qk_uclip=tuple(p.to(DEV) for p in params), clip=(-0.9, 1.1))
+    torch.cuda.synchronize()
+    n = oracle.qk_uclip_rope_kv_store(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], inp["pos"],
+                                      inp["slot_mapping"], inp["kv_cache"], *params, clip_min=-0.9, clip_max=1.1,
+                                      style=style)
+    assert int(err.item()) == n == 0
+    check(d, inp, f"qk_uclip {style} {dtype} {n_head}/{n_kv}/{hd}")
+
+
+@pytest.mark.parametrize("style", STYLES)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_qk_uclip_fused_equals_separate_kernels(style, dtype):
+    """The fused kernel is bit-identical to sra.uclip on the Q and K heads followed by
+    the plain rope_kv_store on the fused QKV views (same fp32 steps, same roundings)."""
+    T, nh, nkv, hd = 512, 12, 2, 128
+    qkv = syn.qkv_inputs(T, nh, nkv, hd, dtype, 31).to(DEV)
+    tables = [t.to(DEV) for t in syn.rope_tables(32768, hd, 1e6)]
+    pos = syn.positions(T, 32768, 31, 2).to(DEV)
+    slot = syn.slots(T, 64 * 16, 31, 3).to(DEV)
+    qa, qg, ka, kg = (p.to(DEV) for p in _qk_params(hd, 31))
+    a, b = qkv.clone(), qkv.clone()
+    ca = syn.sentinel_cache((2, 64, 16, nkv, hd), dtype).to(DEV)
+    cb = ca.clone()
+    sra.rope_kv_store(a[:, :nh], a[:, nh:nh + nkv], a[:, nh + nkv:], *tables, pos, slot, ca, style=style,
+                      qk_uclip=(qa, qg, ka, kg))
+    kn = torch.empty(T, nkv, hd, dtype=dtype, device=DEV)
+    sra.dyht(b[:, :nh], qa, qg, b[:, :nh])
+    sra.dyht(b[:, nh:nh + nkv], ka, kg, kn)
+    sra.rope_kv_store(b[:, :nh], kn, b[:, nh + nkv:], *tables, pos, slot, cb, style=style)
+    torch.cuda.synchronize()
+    assert_bits_equal(a[:, :nh], b[:, :nh], "q")
+    assert_bits_equal(a[:, nh:], qkv[:, nh:], "k and v inputs untouched")
+    assert_bits_equal(ca, cb, "cache")
+
+
+def test_qk_uclip_bad_positions_and_scalar_path():
+    """Bad positions leave q raw and count; a 2-byte-misaligned fused view takes the scalar path."""
+    T, nh, nkv, hd = 24, 4, 2, 64
+    inp = syn.rope_inputs(T, 32, n_head=nh, n_kv_head=nkv, head_dim=hd, num_blocks=4, max_pos=4096,
+                          tables=syn.rope_tables(4096, hd, 1e4))
+    inp["pos"][3] = -2
+    inp["pos"][9] = 4096
+    params = _qk_params(hd, 32)
+    W = (nh + 2 * nkv) * hd
+    base = syn.normal((T * W + 1,), 0, 1, torch.bfloat16, 32, 9)
+    buf = base[1:].view(T, W)
+    q = buf[:, :nh * hd].view(T, nh, hd)
+    k = buf[:, nh * hd:(nh + nkv) * hd].view(T, nkv, hd)
+    v = buf[:, (nh + nkv) * hd:].view(T, nkv, hd)
+    bd = base.to(DEV)
+    bufd = bd[1:].view(T, W)
+    dq = bufd[:, :nh * hd].view(T, nh, hd)
+    dk = bufd[:, nh * hd:(nh + nkv) * hd].view(T, nkv, hd)
+    dv = bufd[:, (nh + nkv) * hd:].view(T, nkv, hd)
+    dc = inp["kv_cache"].to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sra.rope_kv_store(dq, dk, dv, inp["cos"].to(DEV), inp["sin"].to(DEV), inp["pos"].to(DEV),
+                      inp["slot_mapping"].to(DEV), dc, err_count=err, qk_uclip=tuple(p.to(DEV) for p in params))
+    qo = q.contiguous()
+    n = oracle.qk_uclip_rope_kv_store(qo, k.contiguous(), v.contiguous(), inp["cos"], inp["sin"], inp["pos"],
+                                      inp["slot_mapping"], inp["kv_cache"], *params)
+    assert int(err.item()) == n == 2
+    assert_close(dq, qo, "q")
+    assert_close(dc.cpu()[0], inp["kv_cache"][0], "K")
+    assert_bits_equal(dc.cpu()[1], inp["kv_cache"][1], "V")
+    assert_bits_equal(dq[3], q[3], "bad position: q raw")

@@ -45,16 +45,17 @@ MUTANTS = [
     ("silu with e^+g", "a = g / (1.0 + std::exp(-g));", "a = g / (1.0 + std::exp(g));",
      "test_oracle_glu.py"),
     ("relu passes negatives", "a = g > 0.0 ? g : 0.0;", "a = g;", "test_oracle_glu.py"),
-    ("uclip gamma dropped", "v * g, fmt);", "v, fmt);", "test_oracle_uclip.py"),
-    ("uclip lower bound clips to the upper", "if (v < lo) v = lo;", "if (v < lo) v = hi;",
+    ("uclip gamma dropped", "const float y = v * g;", "const float y = v;", "test_oracle_uclip.py"),
+    ("uclip lower bound clips to the upper", "if (v < lo32) v = lo32;", "if (v < lo32) v = hi32;",
      "test_oracle_uclip.py"),
-    ("uclip NaN clamped", "if (v < lo) v = lo;", "if (!(v >= lo)) v = lo;", "test_oracle_uclip.py"),
+    ("uclip NaN clamped", "if (v < lo32) v = lo32;", "if (!(v >= lo32)) v = lo32;", "test_oracle_uclip.py"),
+    ("uclip in double", "float v = a * xf;", "double v = static_cast<double>(a) * xf;", "test_oracle_uclip.py"),
     ("uclip alpha indexed by head", "alpha[alpha_per_channel ? d : 0]", "alpha[alpha_per_channel ? hh : 0]",
      "test_oracle_uclip.py"),
     ("uclip per-channel gamma read as scalar", "gamma[gamma_per_channel ? d : 0]", "gamma[0]",
      "test_oracle_uclip.py"),
     ("uclip middle stride ignored", "hh * x_h_stride + d", "hh * D + d", "test_oracle_uclip.py"),
-    ("uclip gamma inside the clamp", "double v = a * load(", "double v = a * g * load(", "test_oracle_uclip.py"),
+    ("uclip gamma inside the clamp", "float v = a * xf;", "float v = a * g * xf;", "test_oracle_uclip.py"),
     ("ties away from zero", "(frac > 0.5 || (frac == 0.5 && std::fmod(fl, 2.0) != 0.0))",
      "(frac >= 0.5)", "test_oracle_rounding.py"),
     ("no overflow to infinity", "if (r > maxfin) r = INFINITY;", "", "test_oracle_rounding.py"),

@@ -6,10 +6,13 @@ DyHT(x) = y * clamp(a x, -1, 1) replaces every RMSNorm of the AsyncT model
 a scalar or per-channel alpha and gamma, over 3-D [N, H, D] views whose middle
 stride is free (narrow Q/K views of a fused QKV projection).
 
-The pins: exhaustive identity and plain-clip cases checked against torch's own
-clamp, closed forms for power-of-two scales, the special values, exact-rational
-brute force with per-channel parameters and asymmetric bounds, and stride
-invariance on narrow views.
+The page's kernel evaluates in float, so the oracle keeps its two fp32
+roundings (a * x, then * g) and fp32 bounds. The pins: exhaustive identity and
+plain-clip cases checked against torch's own clamp, closed forms for
+power-of-two scales, the special values, exact-rational brute force of the
+kernel's steps (fp32 roundings by search) with per-channel parameters and
+asymmetric bounds, a case where the fp32 rounding of a * x decides the output,
+and stride invariance on narrow views.
 """
 import math
 from fractions import Fraction
@@ -19,7 +22,7 @@ import pytest
 import torch
 
 import oracle
-from tests.exact import BF16, F16, F32, TORCH_DT, from_bits, nearest_bits, tensor_bits
+from tests.exact import BF16, F16, F32, TORCH_DT, bits_value, from_bits, nearest_bits, tensor_bits
 
 FMTS = [F32, F16, BF16]
 
@@ -95,20 +98,27 @@ def test_special_values(fmt):
         _run(x, _scalar(1.0), _scalar(1.0), math.nan, 1.0)
 
 
+def _f32(v: Fraction) -> Fraction:
+    """v rounded to fp32 by the brute-force nearest search."""
+    return Fraction(bits_value(nearest_bits(v, F32), F32))
+
+
 def _exact_bits(x, alpha, gamma, lo, hi, fmt):
-    """Exact rational clamp(a x, lo, hi) * g rounded by the brute-force search."""
+    """The page's kernel steps on exact rationals: fp32(a x), the clamp against
+    fp32 bounds, fp32(* g), then the nearest value of the format."""
     N, H, D = x.shape
     xs = x.double().numpy()
     a = alpha.double().numpy()
     g = gamma.double().numpy()
-    flo, fhi = Fraction(lo), Fraction(hi)
+    flo, fhi = _f32(Fraction(lo)), _f32(Fraction(hi))
     bits = np.zeros((N, H, D), dtype=np.int64)
     for n in range(N):
         for h in range(H):
             for d in range(D):
-                v = Fraction(float(a[d if a.size > 1 else 0])) * Fraction(float(xs[n, h, d]))
+                v = _f32(Fraction(float(a[d if a.size > 1 else 0])) * Fraction(float(xs[n, h, d])))
                 v = min(max(v, flo), fhi)
-                bits[n, h, d] = nearest_bits(v * Fraction(float(g[d if g.size > 1 else 0])), fmt)
+                y = _f32(v * Fraction(float(g[d if g.size > 1 else 0])))
+                bits[n, h, d] = nearest_bits(y, fmt)
     return bits
 
 
@@ -169,3 +179,17 @@ def test_narrow_views_match_contiguous(fmt):
 
 def tensor_bits_t(t):
     return torch.from_numpy(tensor_bits(t))
+
+
+def test_fp32_product_rounding_is_kept():
+    """Inputs (found by search) where the kernel's two fp32 roundings move the fp16
+    result by one ulp against a single rounding of the exact a * x * g: the oracle
+    must give the fp32-step value 0xb838, not the exact value's 0xb837."""
+    x = torch.tensor([[-1.8701171875]], dtype=torch.float16)
+    a = torch.tensor([0.280250608921051], dtype=torch.float32)
+    g = torch.tensor([1.0057204961776733], dtype=torch.float32)
+    exact = Fraction(float(a[0])) * Fraction(float(x[0, 0])) * Fraction(float(g[0]))
+    assert nearest_bits(exact, F16) == 0xB837
+    out = _run(x, a, g, -math.inf, math.inf)
+    assert int(tensor_bits(out)[0, 0]) == 0xB838
+    assert int(tensor_bits(out)[0, 0]) == int(_exact_bits(x.reshape(1, 1, 1), a, g, -4.0, 4.0, F16)[0, 0, 0])
