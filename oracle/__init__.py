@@ -69,6 +69,9 @@ def lib() -> ctypes.CDLL:
             L.orc_uclip.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i32, i32, dbl, dbl,
                                     i32]
             L.orc_uclip.restype = i32
+            L.orc_paged_decode_attention.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i64, i64, i32,
+                                                     i64, dbl, i32]
+            L.orc_paged_decode_attention.restype = i64
             _lib = L
     return _lib
 
@@ -231,3 +234,29 @@ def qk_uclip_rope_kv_store(q, k, v, cos, sin, pos, slot_mapping, kv_cache, q_alp
         uclip(ks, k_alpha, k_gamma, ks, clip_min, clip_max)
         kn[idx] = ks
     return rope_kv_store(q, kn, v, cos, sin, pos, slot_mapping, kv_cache, max_pos=max_pos, style=style)
+
+
+def paged_decode_attention(q, kv_cache, block_table, seq_lens, out, scale: float | None = None) -> int:
+    """out[b, h] = softmax(scale * q[b, h] . K) V over request b's cached tokens.
+
+    q, out: [B, n_head, head_dim] (token stride free, heads contiguous); kv_cache:
+    contiguous [2, num_blocks, block_size, n_kv_head, head_dim]; block_table: int32
+    [B, max_blocks]; seq_lens: int32 [B]. scale defaults to 1 / sqrt(head_dim).
+    Returns the count of skipped bad entries."""
+    for t, n in ((q, "q"), (kv_cache, "kv_cache"), (block_table, "block_table"), (seq_lens, "seq_lens"),
+                 (out, "out")):
+        _cpu(t, n)
+    assert kv_cache.is_contiguous() and block_table.is_contiguous() and seq_lens.is_contiguous()
+    assert block_table.dtype == torch.int32 and seq_lens.dtype == torch.int32
+    B, n_head, hd = q.shape
+    _, num_blocks, block_size, n_kv, _ = kv_cache.shape
+    if scale is None:
+        scale = 1.0 / float(hd) ** 0.5
+    n = lib().orc_paged_decode_attention(q.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(),
+                                         seq_lens.data_ptr(), out.data_ptr(), B, n_head, n_kv, hd,
+                                         _tok_stride(q), _tok_stride(out), num_blocks, block_size,
+                                         block_table.shape[1] if block_table.dim() == 2 else 0, float(scale),
+                                         _FMT[q.dtype])
+    if n < 0:
+        raise ValueError("oracle: bad paged_decode_attention arguments")
+    return int(n)

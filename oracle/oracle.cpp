@@ -1,5 +1,6 @@
 // Plain CPU oracle for the fused per-token decoder path (RMSNorm, residual-add +
-// RMSNorm, RoPE with paged KV-cache store, SwiGLU/ReGLU, UClip/DyHT).
+// RMSNorm, RoPE with paged KV-cache store, SwiGLU/ReGLU, UClip/DyHT) and the
+// decode-attention read of the paged cache.
 //
 // TEST INFRASTRUCTURE ONLY. Only the test suite, the smoke check and the bench's
 // CPU-baseline leg load this file's library. The CUDA library never links,
@@ -31,7 +32,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <set>
+#include <vector>
 
 namespace {
 
@@ -371,6 +374,75 @@ int orc_uclip(const void* x, const float* alpha, const float* gamma, void* out, 
         }
     }
     return 0;
+}
+
+// Decode attention over a paged KV cache: for request b and query head h,
+//   s_t = scale * sum_d q[b, h, d] * K_t[d],   o = sum_t softmax(s)_t * V_t,
+// over the request's first seq_lens[b] tokens, token t living in cache block
+// block_table[b, t / block_size] at offset t % block_size, kv head h / (n_head /
+// n_kv_head) ([mer] section 1.1: cache [2, num_blocks, block_size, n_kv, head]
+// with a block table and seq lens per request; section 3.1: the decode kernel
+// reads that layout through the block table; [lsln] section 2.1: qk_score,
+// scale + softmax and pv_agg as one attention read of the cache). Softmax is
+// taken with its maximum subtracted (the same function, written stably).
+// Bad inputs are skipped and counted: a seq_len outside [0, max_blocks *
+// block_size] is clamped into it (one error per request); a block id outside
+// [0, num_blocks) drops that block's tokens (one error per block entry used). A
+// request with no token left gets o = 0. Returns the error count, or -1 for bad
+// arguments.
+int64_t orc_paged_decode_attention(const void* q, const void* kv_cache, const int32_t* block_table,
+                                   const int32_t* seq_lens, void* out, int64_t B, int n_head, int n_kv_head,
+                                   int head_dim, int64_t q_tok_stride, int64_t out_tok_stride, int64_t num_blocks,
+                                   int block_size, int64_t max_blocks, double scale, int fmt) {
+    FormatSpec spec;
+    if (!format_spec(fmt, &spec) || B < 0 || n_head <= 0 || n_kv_head <= 0 || n_head % n_kv_head != 0 ||
+        head_dim <= 0 || block_size <= 0 || max_blocks < 0 || num_blocks < 0)
+        return -1;
+    const int group = n_head / n_kv_head;
+    int64_t errors = 0;
+    std::vector<double> s, qd(head_dim), acc(head_dim);
+    std::vector<int64_t> rows;  // element offset of each valid token's K row (kv head 0)
+    for (int64_t b = 0; b < B; ++b) {
+        int64_t L = seq_lens[b];
+        if (L < 0 || L > max_blocks * block_size) {
+            ++errors;
+            L = L < 0 ? 0 : max_blocks * block_size;
+        }
+        rows.clear();
+        for (int64_t j = 0; j * block_size < L; ++j) {
+            const int64_t blk = block_table[b * max_blocks + j];
+            if (blk < 0 || blk >= num_blocks) {
+                ++errors;
+                continue;
+            }
+            for (int64_t off = 0; off < block_size && j * block_size + off < L; ++off)
+                rows.push_back((blk * block_size + off) * n_kv_head * static_cast<int64_t>(head_dim));
+        }
+        const int64_t v_plane = num_blocks * block_size * n_kv_head * static_cast<int64_t>(head_dim);
+        for (int h = 0; h < n_head; ++h) {
+            const int64_t kvh_off = static_cast<int64_t>(h / group) * head_dim;
+            for (int d = 0; d < head_dim; ++d) qd[d] = load(q, b * q_tok_stride + static_cast<int64_t>(h) * head_dim + d, fmt);
+            s.assign(rows.size(), 0.0);
+            double m = -INFINITY;
+            for (size_t t = 0; t < rows.size(); ++t) {
+                double dot = 0.0;
+                for (int d = 0; d < head_dim; ++d) dot += qd[d] * load(kv_cache, rows[t] + kvh_off + d, fmt);
+                s[t] = scale * dot;
+                if (s[t] > m) m = s[t];
+            }
+            double denom = 0.0;
+            std::fill(acc.begin(), acc.end(), 0.0);
+            for (size_t t = 0; t < rows.size(); ++t) {
+                const double p = std::exp(s[t] - m);
+                denom += p;
+                for (int d = 0; d < head_dim; ++d) acc[d] += p * load(kv_cache, v_plane + rows[t] + kvh_off + d, fmt);
+            }
+            for (int d = 0; d < head_dim; ++d)
+                store(out, b * out_tok_stride + static_cast<int64_t>(h) * head_dim + d,
+                      rows.empty() ? 0.0 : acc[d] / denom, fmt);
+        }
+    }
+    return errors;
 }
 
 }  // extern "C"

@@ -56,6 +56,21 @@ MUTANTS = [
      "test_oracle_uclip.py"),
     ("uclip middle stride ignored", "hh * x_h_stride + d", "hh * D + d", "test_oracle_uclip.py"),
     ("uclip gamma inside the clamp", "float v = a * xf;", "float v = a * g * xf;", "test_oracle_uclip.py"),
+    ("attention without the max shift", "const double p = std::exp(s[t] - m);", "const double p = std::exp(s[t]);",
+     "test_oracle_attention.py"),
+    ("attention scale dropped", "s[t] = scale * dot;", "s[t] = dot;", "test_oracle_attention.py"),
+    ("attention kv head by modulo", "static_cast<int64_t>(h / group) * head_dim", "static_cast<int64_t>(h % n_kv_head) * head_dim",
+     "test_oracle_attention.py"),
+    ("attention V read from the K plane", "load(kv_cache, v_plane + rows[t] + kvh_off + d, fmt)",
+     "load(kv_cache, rows[t] + kvh_off + d, fmt)", "test_oracle_attention.py"),
+    ("attention offset within the block dropped", "rows.push_back((blk * block_size + off)",
+     "rows.push_back((blk * block_size)", "test_oracle_attention.py"),
+    ("attention block table row ignored", "block_table[b * max_blocks + j]", "block_table[j]",
+     "test_oracle_attention.py"),
+    ("attention one token past seq_len", "j * block_size + off < L;", "j * block_size + off <= L;",
+     "test_oracle_attention.py"),
+    ("attention denominator dropped", "rows.empty() ? 0.0 : acc[d] / denom", "rows.empty() ? 0.0 : acc[d]",
+     "test_oracle_attention.py"),
     ("ties away from zero", "(frac > 0.5 || (frac == 0.5 && std::fmod(fl, 2.0) != 0.0))",
      "(frac >= 0.5)", "test_oracle_rounding.py"),
     ("no overflow to infinity", "if (r > maxfin) r = INFINITY;", "", "test_oracle_rounding.py"),
