@@ -223,6 +223,22 @@ def build_entries(dev, stream_handle, only=(), companions=False):
             entries.append(Entry(name, "uclip", 2 * T * 12 * 128 * 2 + 2 * 128 * 4, T * 12, L.sra_uclip,
                                  (qkv.data_ptr(), a.data_ptr(), g.data_ptr(), qkv.data_ptr(), T, 12, 128, W, 128, W,
                                   128, 1, 1, -1.0, 1.0, 2, stream_handle), [qkv], [qkv], keep=(qkv, a, g)))
+    if companions:
+        # decode attention over the paged cache (Qwen2.5-1.5B heads): the read side of rope_kv_store
+        for B, ctx in ((1, 32768), (32, syn.ATTN_CTX), (64, syn.ATTN_CTX)):
+            name = f"decode_attention:bf16:B{B}xctx{ctx}"
+            if not want(name):
+                continue
+            nb = max(4096, B * ((ctx + 15) // 16))
+            q, cache, table, seq = (t.to(dev) for t in syn.attention_inputs(B, ctx, 12, 2, 128, 16, nb,
+                                                                             torch.bfloat16, 1012))
+            out = torch.empty_like(q)
+            nblk = (ctx + 15) // 16
+            nbytes = 2 * B * ctx * 2 * 128 * 2 + 2 * B * 12 * 128 * 2 + 4 * (B * nblk + B)
+            entries.append(Entry(name, "decode_attention", nbytes, B, L.sra_paged_decode_attention,
+                                 (q.data_ptr(), cache.data_ptr(), table.data_ptr(), seq.data_ptr(), out.data_ptr(),
+                                  B, 12, 2, 128, 12 * 128, 12 * 128, nb, 16, table.shape[1], 128 ** -0.5, None, 2,
+                                  stream_handle), [q, table, seq], [out], keep=(q, cache, table, seq, out)))
     I = syn.LLAMA3_8B_MLP["intermediate"]
     for T in Ts_glu:
         gu = None

@@ -11,6 +11,7 @@
  *                      sra_rope_kv_store_qk_uclip: with the Q/K UClip norms fused in)
  *   sra_glu            SwiGLU silu(gate) * up, or ReGLU relu(gate) * up, over a fused gate_up
  *   sra_uclip          UClip / DyHT clamp(alpha * x, lo, hi) * gamma over [N, H, D] views
+ *   sra_paged_decode_attention  softmax decode attention read through the paged cache's block table
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -228,6 +229,50 @@ SRA_API int sra_glu(const void* gate_up, void* out, int64_t T, int64_t I, int64_
 /* sra_swiglu — sra_glu with act = SRA_ACT_SILU (the call swiglu(gate_up, out, T, I) on contiguous rows). */
 SRA_API int sra_swiglu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row_stride,
                int64_t out_row_stride, int dtype, void* stream);
+
+/*
+ * sra_paged_decode_attention — the read side of the paged cache: [mer] sec. 1.1
+ * (cache [2, num_blocks, block_size, n_kv, head] with a block table and seq lens
+ * per request), sec. 2.2 (the K/V load is the cost; query heads sharing a KV head
+ * share its load) and sec. 3.1 (a decode kernel reading that layout through the
+ * block table); [lsln] sec. 2.1 and 5.3 (qk_score, scale + softmax and pv_agg over
+ * cache_kv_read) and sec. 3.2 (a split reduction merged through each part's max
+ * and sum of exponentials).
+ *
+ *   out[b, h, :] = sum_{t < seq_lens[b]} softmax_t(scale * q[b, h, :] . K_t) V_t
+ *
+ * with K_t / V_t the rows of kv head h / (n_head / n_kv_head) at block
+ * block_table[b, t / block_size], offset t % block_size. fp32 arithmetic (scores
+ * in base 2, an online softmax per split, the splits merged in fp32), one RNE to
+ * the dtype.
+ *
+ * q:           [B, n_head, head_dim] of `dtype`, heads contiguous, token stride
+ *              q_tok_stride. Read only.
+ * kv_cache:    [2, num_blocks, block_size, n_kv_head, head_dim] of `dtype`,
+ *              contiguous and 16-byte aligned; plane 0 = K, plane 1 = V (what
+ *              sra_rope_kv_store writes). Read only.
+ * block_table: int32 [B, max_blocks_per_seq], row-major. Read only.
+ * seq_lens:    int32 [B]. Read only.
+ * out:         [B, n_head, head_dim] of `dtype`, token stride out_tok_stride; it
+ *              must not overlap q, the cache, the table or seq_lens.
+ * scale:       any finite float (1 / sqrt(head_dim) for the usual attention).
+ * err_count:   nullable device int32, incremented (atomically) once per request
+ *              whose seq_len lies outside [0, max_blocks_per_seq * block_size]
+ *              (it is clamped into that range) and once per used block entry
+ *              outside [0, num_blocks) (that block's tokens are skipped). A request
+ *              left with no token gets zeros.
+ * Supported shapes: head_dim 64, 128 or 256; block_size 8, 16 or 32; n_head /
+ * n_kv_head <= 8. Others -> SRA_ERR_SHAPE.
+ * Errors: unknown dtype -> SRA_ERR_DTYPE; bad sizes -> SRA_ERR_SHAPE; a token
+ * stride below n_head * head_dim -> SRA_ERR_STRIDE; a non-finite scale or a cache
+ * not 16-byte aligned -> SRA_ERR_ARG; NULL -> SRA_ERR_NULL; overlap ->
+ * SRA_ERR_ALIAS. B == 0 is a no-op.
+ */
+SRA_API int sra_paged_decode_attention(const void* q, const void* kv_cache, const int32_t* block_table,
+                                       const int32_t* seq_lens, void* out, int64_t B, int n_head, int n_kv_head,
+                                       int head_dim, int64_t q_tok_stride, int64_t out_tok_stride,
+                                       int64_t num_blocks, int block_size, int64_t max_blocks_per_seq, float scale,
+                                       int32_t* err_count, int dtype, void* stream);
 
 /*
  * sra_uclip — [mer] sec. 0 (DyHT(x) = y * clamp(a x, -1, 1) in place of every

@@ -1,5 +1,6 @@
 """GB300-native fused per-token decoder path: RMSNorm, residual-add + RMSNorm,
-RoPE (neox or interleaved) with paged KV-cache store, SwiGLU / ReGLU, UClip / DyHT.
+RoPE (neox or interleaved) with paged KV-cache store, SwiGLU / ReGLU, UClip / DyHT,
+and the decode-attention read of the paged cache.
 
 Every operator runs in the hand-written sm_103a CUDA kernels of ``libsra.so``
 (C ABI in ``include/sra.h``). This module only marshals torch tensors into that
@@ -13,6 +14,7 @@ from ._binding import (  # noqa: F401
     force_variant,
     glu,
     lib,
+    paged_decode_attention,
     pick_variant,
     reglu,
     rmsnorm,
@@ -25,5 +27,6 @@ from ._binding import (  # noqa: F401
     variant_name,
 )
 
-__all__ = ["rmsnorm", "add_rmsnorm", "rope_kv_store", "swiglu", "reglu", "glu", "uclip", "dyht", "lib", "SRAError",
+__all__ = ["rmsnorm", "add_rmsnorm", "rope_kv_store", "swiglu", "reglu", "glu", "uclip", "dyht", "paged_decode_attention", "lib",
+           "SRAError",
            "force_variant", "set_pdl", "variant_count", "variant_name", "pick_variant", "status_string"]

@@ -43,12 +43,14 @@ def lib() -> ctypes.CDLL:
             L.sra_rope_kv_store_ex.argtypes = L.sra_rope_kv_store.argtypes[:19] + [i32, i32, vp]
             L.sra_rope_kv_store_qk_uclip.argtypes = L.sra_rope_kv_store.argtypes[:19] + [i32, vp, vp, vp, vp, f32,
                                                                                         f32, i32, vp]
+            L.sra_paged_decode_attention.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i64, i64, i32,
+                                                     i64, f32, vp, i32, vp]
             L.sra_glu.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, vp]
             L.sra_swiglu.argtypes = [vp, vp, i64, i64, i64, i64, i32, vp]
             L.sra_uclip.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i32, i32, f32, f32, i32,
                                     vp]
             for fn in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_rope_kv_store_ex", "sra_glu",
-                       "sra_swiglu", "sra_uclip", "sra_rope_kv_store_qk_uclip"):
+                       "sra_swiglu", "sra_uclip", "sra_rope_kv_store_qk_uclip", "sra_paged_decode_attention"):
                 getattr(L, fn).restype = i32
             L.sra_status_string.argtypes = [i32]
             L.sra_status_string.restype = ctypes.c_char_p
@@ -352,3 +354,46 @@ def dyht(x: torch.Tensor, alpha: torch.Tensor, gamma: torch.Tensor, out: torch.T
          stream=None) -> torch.Tensor:
     """DyHT: gamma * clamp(alpha * x, -1, 1)."""
     return uclip(x, alpha, gamma, out, -1.0, 1.0, stream)
+
+
+def paged_decode_attention(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                           seq_lens: torch.Tensor, out: torch.Tensor | None = None, scale: float | None = None,
+                           err_count: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """out[b, h] = softmax(scale * q[b, h] . K) V over request b's cached tokens.
+
+    q: [B, n_head, head_dim]; kv_cache: [2, num_blocks, block_size, n_kv_head, head_dim] (the
+    layout rope_kv_store writes); block_table: int32 [B, max_blocks]; seq_lens: int32 [B];
+    scale defaults to 1 / sqrt(head_dim)."""
+    for t, n in ((q, "q"), (kv_cache, "kv_cache"), (block_table, "block_table"), (seq_lens, "seq_lens")):
+        _cuda(t, n)
+    if out is None:
+        out = torch.empty(q.shape, dtype=q.dtype, device=q.device)
+    _cuda(out, "out")
+    _same_device(q, kv_cache, block_table, seq_lens, out, err_count)
+    if not (q.dtype == kv_cache.dtype == out.dtype):
+        raise ValueError("q, kv_cache and out must share one dtype")
+    if kv_cache.dim() != 5 or not kv_cache.is_contiguous() or kv_cache.shape[0] != 2:
+        raise ValueError("kv_cache must be contiguous [2, num_blocks, block_size, n_kv_head, head_dim]")
+    if block_table.dtype != torch.int32 or block_table.dim() != 2 or not block_table.is_contiguous():
+        raise ValueError("block_table must be a contiguous int32 [B, max_blocks] tensor")
+    if seq_lens.dtype != torch.int32 or not seq_lens.is_contiguous():
+        raise ValueError("seq_lens must be contiguous int32")
+    if err_count is not None:
+        _cuda(err_count, "err_count")
+        if err_count.dtype != torch.int32:
+            raise ValueError("err_count must be int32")
+    B, n_head, hd = q.shape
+    _, nb, bs, n_kv, chd = kv_cache.shape
+    if chd != hd or out.shape != q.shape or block_table.shape[0] != B or seq_lens.numel() != B:
+        raise ValueError("shape mismatch")
+    if scale is None:
+        scale = 1.0 / float(hd) ** 0.5
+    with torch.cuda.device(q.device):
+        st = lib().sra_paged_decode_attention(q.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(),
+                                              seq_lens.data_ptr(), out.data_ptr(), B, n_head, n_kv, hd,
+                                              _tok_stride(q, "q"), _tok_stride(out, "out"), nb, bs,
+                                              block_table.shape[1], float(scale),
+                                              err_count.data_ptr() if err_count is not None else None,
+                                              _dtype(q), _stream(q, stream))
+    _check("sra_paged_decode_attention", st)
+    return out

@@ -708,6 +708,71 @@ int sra_swiglu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_
     return sra_glu(gate_up, out, T, I, in_row_stride, out_row_stride, SRA_ACT_SILU, dtype, stream);
 }
 
+// ------------------------------------------------------------------- decode attention
+int sra_paged_decode_attention(const void* q, const void* kv_cache, const int32_t* block_table,
+                               const int32_t* seq_lens, void* out, int64_t B, int n_head, int n_kv_head,
+                               int head_dim, int64_t q_tok_stride, int64_t out_tok_stride, int64_t num_blocks,
+                               int block_size, int64_t max_blocks_per_seq, float scale, int32_t* err_count,
+                               int dtype, void* stream) {
+    if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
+    if (B < 0 || n_head <= 0 || n_kv_head <= 0 || n_head % n_kv_head != 0 || n_head / n_kv_head > 8 ||
+        (head_dim != 64 && head_dim != 128 && head_dim != 256) ||
+        (block_size != 8 && block_size != 16 && block_size != 32) || num_blocks < 0 || max_blocks_per_seq < 0)
+        return SRA_ERR_SHAPE;
+    const int64_t w = static_cast<int64_t>(n_head) * head_dim;
+    if (q_tok_stride < w || out_tok_stride < w) return SRA_ERR_STRIDE;
+    if (!std::isfinite(scale)) return SRA_ERR_ARG;
+    if (B == 0) return SRA_OK;
+    if (!q || !kv_cache || !block_table || !seq_lens || !out) return SRA_ERR_NULL;
+    if (!aligned16(kv_cache)) return SRA_ERR_ARG;
+    const int es = elem_bytes(dtype);
+    const Span so = span_of(out, B, out_tok_stride, w, es);
+    const Span sc = span_of(kv_cache, 1, 0, 2 * num_blocks * block_size * static_cast<int64_t>(n_kv_head) * head_dim, es);
+    const Span st = span_of(block_table, 1, 0, B * max_blocks_per_seq, 4), sl = span_of(seq_lens, 1, 0, B, 4);
+    if (rows_overlap(out, B, out_tok_stride, w, q, B, q_tok_stride, w, es) || overlap(so, sc) || overlap(so, st) ||
+        overlap(so, sl))
+        return SRA_ERR_ALIAS;
+    int dev = 0;
+    const int sms = current_sm_count(&dev);
+    if (sms <= 0) return SRA_ERR_DEVICE;
+    const int group = n_head / n_kv_head;
+    AttnPlan plan;
+    plan.head_dim = head_dim;
+    plan.threads = 128;
+    plan.pdl = g_pdl;
+    plan.num_sms = sms;
+    // splits of one (request, kv head): a cluster of up to 8 CTAs, enough CTAs for two per SM,
+    // and at least 4 cache blocks per split
+    const int64_t groups = B * n_kv_head;
+    int splits = 1;
+    while (splits < 8 && groups * splits < 2 * static_cast<int64_t>(sms) && max_blocks_per_seq >= 4 * splits)
+        splits *= 2;
+    plan.splits = splits;
+    const int64_t limit = smem_optin(dev) - 1024;
+    plan.stages = 4;
+    if (static_cast<int64_t>(decode_attention_smem(group, head_dim, block_size, 4, es)) > limit) plan.stages = 2;
+    plan.smem = decode_attention_smem(group, head_dim, block_size, plan.stages, es);
+    if (static_cast<int64_t>(plan.smem) > limit) return SRA_ERR_SHAPE;
+    AttnArgs a;
+    a.q = q;
+    a.cache = kv_cache;
+    a.table = block_table;
+    a.seq_lens = seq_lens;
+    a.out = out;
+    a.err = err_count;
+    a.B = B;
+    a.qs = q_tok_stride;
+    a.os = out_tok_stride;
+    a.num_blocks = num_blocks;
+    a.max_blocks = max_blocks_per_seq;
+    a.n_head = n_head;
+    a.n_kv = n_kv_head;
+    a.group = group;
+    a.block_size = block_size;
+    a.scale_log2 = scale * 1.4426950408889634f;
+    return status_from(launch_decode_attention(a, plan, dtype, static_cast<cudaStream_t>(stream)));
+}
+
 // ------------------------------------------------------------------- UClip
 int sra_uclip(const void* x, const float* alpha, const float* gamma, void* out, int64_t N, int64_t H, int64_t D,
               int64_t x_n_stride, int64_t x_h_stride, int64_t out_n_stride, int64_t out_h_stride,

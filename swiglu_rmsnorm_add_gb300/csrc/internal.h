@@ -123,6 +123,32 @@ struct GluPlan {
 
 cudaError_t launch_glu(const GluArgs& a, const GluPlan& p, int act, int dtype, cudaStream_t s);
 
+// ------------------------------------------------------------------- decode attention
+struct AttnArgs {
+    const void* q;             // [B, n_head, head_dim], token stride qs
+    const void* cache;         // [2, num_blocks, block_size, n_kv, head_dim]
+    const int32_t* table;      // [B, max_blocks]
+    const int32_t* seq_lens;   // [B]
+    void* out;                 // [B, n_head, head_dim], token stride os
+    int32_t* err;              // nullable
+    int64_t B, qs, os, num_blocks, max_blocks;
+    int n_head, n_kv, group, block_size;
+    float scale_log2;          // softmax scale * log2(e)
+};
+
+struct AttnPlan {
+    int head_dim;  // 64, 128 or 256 (template)
+    int splits;    // CTAs per (request, kv head): the cluster size
+    int threads;
+    int stages;    // K/V tiles in flight per CTA
+    size_t smem;
+    bool pdl;
+    int num_sms;
+};
+
+cudaError_t launch_decode_attention(const AttnArgs& a, const AttnPlan& p, int dtype, cudaStream_t s);
+size_t decode_attention_smem(int group, int head_dim, int block_size, int stages, int es);
+
 // ------------------------------------------------------------------- UClip
 struct UclipArgs {
     const void* x;       // [N, H, D], strides (xn, xh, 1)

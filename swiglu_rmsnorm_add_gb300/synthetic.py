@@ -134,3 +134,28 @@ def uclip_params(D: int, alpha_per_channel: bool, gamma_per_channel: bool, seed:
 def qkv_inputs(T: int, n_head: int, n_kv_head: int, head_dim: int, dtype: torch.dtype, seed: int) -> torch.Tensor:
     """A fused QKV projection output [T, n_head + 2 * n_kv_head, head_dim] ~ N(0, 1)."""
     return normal((T, n_head + 2 * n_kv_head, head_dim), 0.0, 1.0, dtype, seed, 33)
+
+
+def attention_inputs(B: int, lens, n_head: int, n_kv_head: int, head_dim: int, block_size: int,
+                     num_blocks: int, dtype: torch.dtype, seed: int, max_blocks: int | None = None):
+    """A decode batch over a paged cache: q [B, n_head, head_dim] ~ N(0, 1), a cache
+    [2, num_blocks, block_size, n_kv_head, head_dim] ~ N(0, 1) (K and V), int32 seq_lens
+    (`lens`: one length for every request or a sequence of B lengths), and an int32
+    block table that gives each request its own blocks, drawn from a seeded permutation
+    of the cache's blocks (unused table entries hold further blocks of the permutation)."""
+    lens = [int(lens)] * B if np.isscalar(lens) else [int(x) for x in lens]
+    need = max([(L + block_size - 1) // block_size for L in lens] + [1])
+    if max_blocks is None:
+        max_blocks = need
+    if B * max_blocks > num_blocks:
+        raise ValueError("cache too small for the requests' blocks")
+    q = normal((B, n_head, head_dim), 0.0, 1.0, dtype, seed, 41)
+    cache = normal((2, num_blocks, block_size, n_kv_head, head_dim), 0.0, 1.0, dtype, seed, 42)
+    perm = rng(seed, 43).permutation(num_blocks)[:B * max_blocks].reshape(B, max_blocks)
+    table = torch.from_numpy(perm.astype(np.int32))
+    seq = torch.tensor(lens, dtype=torch.int32)
+    return q, cache, table, seq
+
+
+ATTN_B = (1, 32, 64)        # decode batch sizes
+ATTN_CTX = 1024             # context length of the decode-attention micro-benchmark

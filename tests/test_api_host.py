@@ -36,7 +36,7 @@ def declared_functions():
 def test_header_declares_the_api():
     names = declared_functions()
     for n in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_rope_kv_store_ex", "sra_glu",
-              "sra_swiglu", "sra_uclip"):
+              "sra_swiglu", "sra_uclip", "sra_paged_decode_attention", "sra_rope_kv_store_qk_uclip"):
         assert n in names
 
 
@@ -159,6 +159,38 @@ def test_rope_qk_uclip_validation(L):
     assert call(qa=Q + 64) == ALIAS              # a parameter array inside q
     assert call(kg=KV + 64) == ALIAS             # ... or inside the cache
     assert call(T=0) == OK
+
+
+def test_paged_decode_attention_validation(L):
+    f = L.sra_paged_decode_attention
+    Q, C, TB, SL, O, E = (P + i * 0x1000000 for i in range(6))
+
+    def call(**kw):
+        a = dict(q=Q, c=C, tb=TB, sl=SL, o=O, B=4, nh=12, nkv=2, hd=128, qs=1536, os=1536, nb=64, bs=16, mb=8,
+                 scale=0.088, dt=BF16)
+        a.update(kw)
+        return f(a["q"], a["c"], a["tb"], a["sl"], a["o"], a["B"], a["nh"], a["nkv"], a["hd"], a["qs"], a["os"],
+                 a["nb"], a["bs"], a["mb"], a["scale"], None, a["dt"], None)
+
+    assert call(dt=4) == DTYPE
+    assert call(B=-1) == SHAPE
+    assert call(nh=12, nkv=5) == SHAPE
+    assert call(nh=18, nkv=2) == SHAPE            # 9 query heads per kv head
+    assert call(hd=96, qs=12 * 96, os=12 * 96) == SHAPE
+    assert call(bs=12) == SHAPE
+    assert call(nb=-1) == SHAPE
+    assert call(mb=-1) == SHAPE
+    assert call(qs=1535) == STRIDE
+    assert call(os=100) == STRIDE
+    assert call(scale=float("inf")) == ARG
+    assert call(scale=float("nan")) == ARG
+    for name in ("q", "c", "tb", "sl", "o"):
+        assert call(**{name: None}) == NULL, name
+    assert call(c=C + 8) == ARG                   # cache not 16-byte aligned
+    assert call(o=Q + 64) == ALIAS               # out overlapping q
+    assert call(o=C + 1024) == ALIAS             # out inside the cache
+    assert call(o=TB) == ALIAS
+    assert call(B=0) == OK
 
 
 def test_uclip_validation(L):

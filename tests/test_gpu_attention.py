@@ -1,0 +1,166 @@
+"""GPU parity: decode attention over the paged KV cache vs the oracle.
+
+Workload: Qwen2.5-1.5B attention (12 query / 2 KV heads, head_dim 128, bf16),
+cache blocks of 16 tokens; the decode micro-benchmark of mer.dev "AsyncT vllm
+适配加速笔记（一）" section 3.1 (batch 32, 1024 cached tokens per request), batch 64
+with mixed lengths, and batch 1 with a 32 768-token context; q and the cache
+~N(0, 1), per-request blocks from a seeded permutation.
+
+Tolerance. The kernel evaluates in fp32: score errors of about 1e-6 (absolute,
+in the exponent) become relative errors of the probabilities, and the sums of
+p * V over up to 32 768 tokens add about sqrt(T) * 2^-24 relative to
+sum p |V| / sum p <= max |V|. An output near zero therefore carries an
+absolute error set by max |V|, not by its own size. The bound: within 1 ulp of
+the oracle's rounded value (bf16 / fp16) or 1e-5 relative (fp32), plus
+3e-5 * max |V| over the request's tokens of that kv head.
+"""
+import pytest
+import torch
+
+import oracle
+import swiglu_rmsnorm_add_gb300 as sra
+from swiglu_rmsnorm_add_gb300 import synthetic as syn
+from tests.parity import ulp_distance
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+ATOL_V = 3e-5
+
+
+def vmax(cache, table, seq, b, kvh):
+    bs = cache.shape[2]
+    L = int(seq[b])
+    nblk = (L + bs - 1) // bs
+    blocks = [int(x) for x in table[b, :nblk] if 0 <= int(x) < cache.shape[1]]
+    if not blocks:
+        return 0.0
+    return float(cache[1, blocks, :, kvh].float().abs().max())
+
+
+def assert_attention_close(got, want, cache, table, seq, what):
+    got, want = got.cpu(), want.cpu()
+    B, n_head, hd = want.shape
+    G = n_head // cache.shape[3]
+    for b in range(B):
+        for kvh in range(cache.shape[3]):
+            hs = slice(kvh * G, kvh * G + G)
+            g, w = got[b, hs], want[b, hs]
+            atol = ATOL_V * vmax(cache, table, seq, b, kvh)
+            err = (g.double() - w.double()).abs()
+            if w.dtype == torch.float32:
+                bad = err > 1e-5 * w.double().abs() + atol
+            else:
+                bad = (ulp_distance(g, w) > 1) & (err > atol)
+            assert not bool(bad.any()), (
+                f"{what}: request {b} kv head {kvh}: {int(bad.sum())} outputs off, max err {float(err.max()):.3g}")
+
+
+def run_both(q, cache, table, seq, scale=None, expect_err=None):
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    got = sra.paged_decode_attention(q.to(DEV), cache.to(DEV), table.to(DEV), seq.to(DEV), scale=scale,
+                                     err_count=err)
+    torch.cuda.synchronize()
+    want = torch.empty_like(q)
+    n = oracle.paged_decode_attention(q, cache, table, seq, want, scale)
+    assert int(err.item()) == n
+    if expect_err is not None:
+        assert n == expect_err
+    return got.cpu(), want
+
+
+@pytest.mark.parametrize("B", [1, 32])
+def test_config_qwen25_ctx1024(B):
+    q, cache, table, seq = syn.attention_inputs(B, syn.ATTN_CTX, 12, 2, 128, 16, 4096, torch.bfloat16, 1012)
+    got, want = run_both(q, cache, table, seq, expect_err=0)
+    assert_attention_close(got, want, cache, table, seq, f"B={B} ctx=1024")
+
+
+def test_config_qwen25_batch64_mixed_lengths():
+    lens = syn.rng(1013, 5).integers(1, 1025, size=64)
+    q, cache, table, seq = syn.attention_inputs(64, lens, 12, 2, 128, 16, 4096, torch.bfloat16, 1013,
+                                                max_blocks=64)
+    got, want = run_both(q, cache, table, seq, expect_err=0)
+    assert_attention_close(got, want, cache, table, seq, "B=64 mixed")
+
+
+def test_config_qwen25_long_context():
+    q, cache, table, seq = syn.attention_inputs(1, 32768, 12, 2, 128, 16, 2048, torch.bfloat16, 1014)
+    got, want = run_both(q, cache, table, seq, expect_err=0)
+    assert_attention_close(got, want, cache, table, seq, "B=1 ctx=32768")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("hd", [64, 128, 256])
+@pytest.mark.parametrize("n_head,n_kv", [(8, 8), (8, 4), (12, 2), (32, 4), (8, 1)])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_shapes_dtypes(dtype, hd, n_head, n_kv, bs):
+    lens = [1, 5, bs, bs + 1, 3 * bs - 1, 200]
+    q, cache, table, seq = syn.attention_inputs(6, lens, n_head, n_kv, hd, bs, 6 * (200 // bs + 2), dtype,
+                                                1015 + hd + bs)
+    got, want = run_both(q, cache, table, seq, expect_err=0)
+    assert_attention_close(got, want, cache, table, seq, f"{dtype} hd={hd} {n_head}/{n_kv} bs={bs}")
+
+
+def test_bad_entries_empty_requests_and_clamping():
+    q, cache, table, seq = syn.attention_inputs(4, 64, 12, 2, 128, 16, 64, torch.bfloat16, 1016, max_blocks=5)
+    table[0, 1] = 64          # out of range: block 1 of request 0 skipped
+    table[1, 0] = -3          # negative
+    seq[2] = 0                # empty request -> zeros
+    seq[3] = 81               # past 5 blocks of 16: clamped to 80
+    got, want = run_both(q, cache, table, seq, expect_err=3)
+    assert_attention_close(got, want, cache, table, seq, "bad entries")
+    assert bool((got[2] == 0).all())
+
+
+def test_dominant_key_and_scale():
+    q, cache, table, seq = syn.attention_inputs(2, 300, 12, 2, 128, 16, 64, torch.bfloat16, 1017)
+    q.zero_()
+    q[:, :, 0] = 1.0
+    for b in range(2):
+        cache[0, int(table[b, 7]), 3, :, 0] = 1000.0   # token 7 * 16 + 3 dominates
+    got, want = run_both(q, cache, table, seq, scale=1.0)
+    assert_attention_close(got, want, cache, table, seq, "dominant key")
+    got, want = run_both(q, cache, table, seq, scale=0.01)
+    assert_attention_close(got, want, cache, table, seq, "small scale")
+
+
+def test_q_and_out_views_of_fused_buffers():
+    """q read from a fused [B, 16 * 128] QKV row, out written into a padded buffer."""
+    B = 8
+    q, cache, table, seq = syn.attention_inputs(B, 100, 12, 2, 128, 16, 64, torch.bfloat16, 1018)
+    qkv = syn.normal((B, 16, 128), 0, 1, torch.bfloat16, 1018, 7)
+    qkv[:, :12] = q
+    dq = qkv.to(DEV)[:, :12]
+    obuf = torch.full((B, 13, 128), 5.0, dtype=torch.bfloat16, device=DEV)
+    out = obuf[:, :12]
+    sra.paged_decode_attention(dq, cache.to(DEV), table.to(DEV), seq.to(DEV), out)
+    want = torch.empty_like(q)
+    oracle.paged_decode_attention(q, cache, table, seq, want)
+    assert_attention_close(out, want, cache, table, seq, "views")
+    assert bool((obuf[:, 12].cpu() == 5.0).all())
+
+
+def test_reads_what_rope_kv_store_wrote():
+    """One decode step: rope_kv_store writes this token's K/V into the cache, then the
+    attention of the rotated q over the request's 257 cached tokens reads it back."""
+    B, nh, nkv, hd, bs = 4, 12, 2, 128, 16
+    q, cache, table, seq = syn.attention_inputs(B, 257, nh, nkv, hd, bs, 128, torch.bfloat16, 1019)
+    pos = (seq - 1).to(torch.int64)
+    slot = (table[torch.arange(B), pos // bs].to(torch.int64) * bs + pos % bs)
+    k = syn.normal((B, nkv, hd), 0, 1, torch.bfloat16, 1019, 8)
+    v = syn.normal((B, nkv, hd), 0, 1, torch.bfloat16, 1019, 9)
+    cos, sin = syn.rope_tables(4096, hd, 1e6)
+    d = dict(q=q.to(DEV), k=k.to(DEV), v=v.to(DEV), cos=cos.to(DEV), sin=sin.to(DEV), pos=pos.to(DEV),
+             slot=slot.to(DEV), cache=cache.to(DEV))
+    sra.rope_kv_store(d["q"], d["k"], d["v"], d["cos"], d["sin"], d["pos"], d["slot"], d["cache"])
+    got = sra.paged_decode_attention(d["q"], d["cache"], table.to(DEV), seq.to(DEV))
+    # the store itself is checked against the oracle's store elsewhere; here the attention
+    # is checked on the bytes the store left (the oracle applied to the kernel's actual inputs)
+    qg, cg = d["q"].cpu(), d["cache"].cpu()
+    want = torch.empty_like(q)
+    oracle.paged_decode_attention(qg, cg, table, seq, want)
+    assert_attention_close(got, want, cg, table, seq, "after rope_kv_store")
+    # the new token's V row sits where the table says
+    for b in range(B):
+        s = int(slot[b])
+        assert torch.equal(cg[1, s // bs, s % bs], v[b])
