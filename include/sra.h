@@ -331,7 +331,9 @@ SRA_API int sra_set_pdl(int enable);
 
 /*
  * Kernel-variant control, for A/B measurement of the per-shape dispatch.
- * op: "rmsnorm" (also used by add_rmsnorm), "rope_kv_store", "glu".
+ * op: "rmsnorm" (also used by add_rmsnorm), "rope_kv_store", "glu",
+ * "decode_attention" (0 = CUDA-core kernel, 1 = mma.sync kernel for bf16 / fp16
+ * with head_dim 64 or 128).
  * variant: -1 = automatic per-shape choice (the default); otherwise an index
  * < sra_variant_count(op), optionally OR-ed with (nv << 8) to also force the
  * number of 16-byte accesses each thread holds in the register variants of
@@ -347,7 +349,8 @@ SRA_API const char* sra_variant_name(const char* op, int variant);
  * The variant the automatic dispatch would pick for a call with these sizes and
  * all pointers and strides 16-byte aligned, on a GPU with num_sms SMs
  * (num_sms <= 0: query the current device). rmsnorm: a = rows, b = D;
- * rope_kv_store: a = T, b = n_head, c = n_kv_head, d = head_dim; glu: a = T, b = I.
+ * rope_kv_store: a = T, b = n_head, c = n_kv_head, d = head_dim; glu: a = T, b = I;
+ * decode_attention: a = B, b = n_head, c = n_kv_head, d = head_dim.
  * Negative sra_status on bad arguments. Enqueues nothing.
  */
 SRA_API int sra_pick_variant(const char* op, int64_t a, int64_t b, int64_t c, int64_t d, int dtype,

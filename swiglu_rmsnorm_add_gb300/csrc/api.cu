@@ -18,7 +18,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_smem_optin[kMaxDevices];
-std::atomic<int> g_force_norm{-1}, g_force_rope{-1}, g_force_glu{-1};
+std::atomic<int> g_force_norm{-1}, g_force_rope{-1}, g_force_glu{-1}, g_force_attn{-1};
 thread_local bool g_pdl = false;  // programmatic dependent launch for this thread's calls
 thread_local int g_force_nv = 0;  // accesses per thread forced for A/B measurement (0 = planner's)
 
@@ -464,6 +464,7 @@ std::atomic<int>* force_slot(const char* op) {
     if (std::strcmp(op, "rmsnorm") == 0) return &g_force_norm;
     if (std::strcmp(op, "rope_kv_store") == 0) return &g_force_rope;
     if (std::strcmp(op, "glu") == 0) return &g_force_glu;
+    if (std::strcmp(op, "decode_attention") == 0) return &g_force_attn;
     return nullptr;
 }
 
@@ -472,6 +473,7 @@ int variant_count(const char* op) {
     if (std::strcmp(op, "rmsnorm") == 0) return NORM_NUM_VARIANTS;
     if (std::strcmp(op, "rope_kv_store") == 0) return ROPE_NUM_VARIANTS;
     if (std::strcmp(op, "glu") == 0) return GLU_NUM_VARIANTS;
+    if (std::strcmp(op, "decode_attention") == 0) return 2;  // CUDA cores, mma.sync
     return SRA_ERR_ARG;
 }
 
@@ -744,14 +746,31 @@ int sra_paged_decode_attention(const void* q, const void* kv_cache, const int32_
     // splits of one (request, kv head): a cluster of up to 8 CTAs, enough CTAs for two per SM,
     // and at least 4 cache blocks per split
     const int64_t groups = B * n_kv_head;
-    int splits = 1;
-    while (splits < 8 && groups * splits < 2 * static_cast<int64_t>(sms) && max_blocks_per_seq >= 4 * splits)
-        splits *= 2;
-    plan.splits = splits;
     const int64_t limit = smem_optin(dev) - 1024;
+    // tensor cores for 16-bit data when q rows allow 4-byte fragment loads
+    plan.tensor_cores = dtype != DT_F32 && (head_dim == 64 || head_dim == 128) &&
+                        (reinterpret_cast<uintptr_t>(q) & 3u) == 0 && q_tok_stride % 2 == 0 &&
+                        num_blocks * block_size < (int64_t(1) << 31) &&
+                        static_cast<int64_t>(decode_attention_mma_smem(head_dim)) <= limit;
+    const int forced = g_force_attn.load(std::memory_order_relaxed);
+    if (forced == 1 && !plan.tensor_cores) return SRA_ERR_VARIANT;
+    if (forced == 0) plan.tensor_cores = false;
+    int splits = 1;
+    if (plan.tensor_cores) {
+        // one 8-warp CTA per SM at most (its K/V rings fill the SM's shared memory), and at
+        // least 256 tokens (two 16-token tiles per warp) per split
+        while (splits < 16 && groups * splits * 2 <= static_cast<int64_t>(sms) &&
+               max_blocks_per_seq * block_size >= 256 * static_cast<int64_t>(splits) * 2)
+            splits *= 2;
+    } else {
+        while (splits < 8 && groups * splits < 2 * static_cast<int64_t>(sms) && max_blocks_per_seq >= 4 * splits)
+            splits *= 2;
+    }
+    plan.splits = splits;
     plan.stages = 4;
     if (static_cast<int64_t>(decode_attention_smem(group, head_dim, block_size, 4, es)) > limit) plan.stages = 2;
-    plan.smem = decode_attention_smem(group, head_dim, block_size, plan.stages, es);
+    plan.smem = plan.tensor_cores ? decode_attention_mma_smem(head_dim)
+                                  : decode_attention_smem(group, head_dim, block_size, plan.stages, es);
     if (static_cast<int64_t>(plan.smem) > limit) return SRA_ERR_SHAPE;
     AttnArgs a;
     a.q = q;
@@ -837,10 +856,12 @@ const char* sra_variant_name(const char* op, int variant) {
                                              "cta_pair",  "warp_smem", "pair_smem"};
     static const char* const rope_names[] = {"token_cta"};
     static const char* const glu_names[] = {"cols_rows"};
+    static const char* const attn_names[] = {"cuda_cores", "mma_sync"};
     const int n = variant_count(op);
     if (n < 0 || variant < 0 || variant >= n) return nullptr;
     if (std::strcmp(op, "rmsnorm") == 0) return norm_names[variant];
     if (std::strcmp(op, "rope_kv_store") == 0) return rope_names[variant];
+    if (std::strcmp(op, "decode_attention") == 0) return attn_names[variant];
     return glu_names[variant];
 }
 
@@ -866,6 +887,11 @@ int sra_pick_variant(const char* op, int64_t a, int64_t b, int64_t c, int64_t d,
         RopePlan p;
         const int st = plan_rope(a, static_cast<int>(b), static_cast<int>(c), static_cast<int>(d), 1, 0, num_sms, &p);
         return st == SRA_OK ? p.variant : st;
+    }
+    if (std::strcmp(op, "decode_attention") == 0) {
+        if (a < 0 || b <= 0 || c <= 0 || b % c || b / c > 8 || (d != 64 && d != 128 && d != 256))
+            return SRA_ERR_SHAPE;
+        return dtype != DT_F32 && d <= 128 ? 1 : 0;
     }
     if (a < 0 || b <= 0) return SRA_ERR_SHAPE;
     GluPlan p;

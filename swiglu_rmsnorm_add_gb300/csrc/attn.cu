@@ -12,6 +12,11 @@
 // pv_agg fused over cache_kv_read) and section 3.2 (split the reduction and
 // merge the parts through their (max, sum of exponentials)).
 //
+// Two kernels. bf16 / fp16 with head_dim 64 or 128 run on the tensor cores
+// (decode_mma_kernel below: warp-level mma.sync, each warp streaming its own
+// 16-token tiles); fp32 and head_dim 256 run on the CUDA cores (decode_kernel,
+// described next). Both share the split / cluster-merge structure.
+//
 // Work: a CTA owns one (request, kv head, split). All G query heads of the kv
 // head are computed together, so every K/V byte is read from HBM once. The
 // request's cache blocks are dealt to the splits in contiguous ranges; a split
@@ -263,6 +268,368 @@ __global__ void __launch_bounds__(kThreads) decode_kernel(AttnArgs a) {
     cluster.sync();  // keep every CTA's shared memory alive until the merge has read it
 }
 
+// ------------------------------------------------------------------------------------------
+// Tensor-core path (bf16 / fp16, head_dim 64 or 128): warp-level mma.sync m16n8k16.
+//
+// The contraction per 16-token tile is S[16 x 16] = Q[16 x HD] K^T and
+// O[16 x HD] += P[16 x 16] V with the G <= 8 query heads of the kv head as the
+// rows 0..7 of the 16-row operands (rows 8..15 are zero). Each warp owns its
+// own 16-token tiles and its own cp.async ring (K and V tiles of 16 rows,
+// 16-byte chunks XOR-swizzled by row so ldmatrix reads are conflict-free;
+// rows of tokens past the end or in a bad block are zero-filled and masked).
+// Q stays in registers as A fragments for the whole kernel; K tiles feed the
+// B operand directly (ldmatrix), V tiles through ldmatrix.trans. The
+// probabilities are split into a T-rounded high part and a T-rounded residual,
+// two MMAs per V fragment, so p keeps about 16 significant bits instead of the
+// 8 (bf16) a single rounding would leave. Warps merge their (m, l, O) in
+// shared memory, then the CTAs of the cluster as in the fp32 path.
+// 2^x by the ex2.approx instruction (PTX ISA: about 2^-22 relative error); 2^-inf = 0.
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+template <typename T>
+struct Mma;
+template <>
+struct Mma<__nv_bfloat16> {
+    __device__ __forceinline__ static void run(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+    }
+};
+template <>
+struct Mma<__half> {
+    __device__ __forceinline__ static void run(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+    }
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(s));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t (&r)[4], const void* p) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(s));
+}
+// 16-byte copy; src_bytes = 0 fills the destination with zeros and reads nothing.
+__device__ __forceinline__ void cp_async16_zfill(void* smem_dst, const void* gmem_src, int src_bytes) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(s), "l"(gmem_src), "r"(src_bytes) : "memory");
+}
+
+// Two values rounded to T, packed (first value in the low half).
+template <typename T>
+__device__ __forceinline__ uint32_t pack2(float x, float y) {
+    float f[2] = {x, y};
+    return Elem<T>::pack_word(f);
+}
+template <typename T>
+__device__ __forceinline__ float2 unpack2(uint32_t w) {
+    float f[2];
+    Elem<T>::unpack_word(w, f);
+    return make_float2(f[0], f[1]);
+}
+
+constexpr int kMmaWarps = 8;
+constexpr int kMmaTile = 16;    // tokens per warp tile
+constexpr int kMmaStages = 3;   // tiles per warp ring
+
+__host__ __device__ inline size_t mma_ring_bytes(int HD) {
+    const size_t ring = static_cast<size_t>(kMmaWarps) * kMmaStages * 2 * kMmaTile * HD * 2;
+    const size_t merge = (static_cast<size_t>(kMmaWarps) * 8 * (HD + 2) + 8 * (HD + 2)) * 4;
+    return ring > merge ? ring : merge;
+}
+__host__ __device__ inline size_t mma_smem(int HD) {
+    return mma_ring_bytes(HD) + static_cast<size_t>(kMmaWarps) * kMmaStages * 4;  // + per-slot row masks
+}
+
+template <typename T, int HD>
+__global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) {
+    constexpr int CPR = HD * 2 / 16;      // 16-byte chunks per row
+    constexpr int KS = HD / 16;           // k-steps of Q K^T
+    constexpr int NB = HD / 8;            // 8-dim blocks of O
+    constexpr int TE = kMmaTile * HD;     // elements of one K or V tile
+    extern __shared__ __align__(16) unsigned char smem[];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int S = static_cast<int>(cluster.num_blocks());
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int64_t grp = blockIdx.x / S;
+    const int64_t b = grp / a.n_kv;
+    const int kvh = static_cast<int>(grp - b * a.n_kv);
+    const int G = a.group, BS = a.block_size;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int fg = lane >> 2, ft = lane & 3;  // fragment row group and thread-in-group
+    T* ring = reinterpret_cast<T*>(smem) + static_cast<size_t>(warp) * kMmaStages * 2 * TE;
+
+    pdl_enter();
+    int64_t len = a.seq_lens[b];
+    const int64_t cap = a.max_blocks * BS;
+    if ((len < 0 || len > cap) && kvh == 0 && rank == 0 && threadIdx.x == 0 && a.err) atomicAdd(a.err, 1);
+    len = len < 0 ? 0 : (len > cap ? cap : len);
+    // static split of the table's capacity (not of seq_len), so the block-table reads of the
+    // first tiles need not wait for seq_len; tokens at or past seq_len are masked
+    const int64_t per = ((cap + S - 1) / S + kMmaTile - 1) / kMmaTile * kMmaTile;
+    const int64_t t_begin = rank * per < cap ? rank * per : cap;
+    const int64_t t_lim = t_begin + per < cap ? t_begin + per : cap;
+    const int64_t t_end = len < t_begin ? t_begin : (len < t_lim ? len : t_lim);
+    const int32_t* table = a.table + b * a.max_blocks;
+    auto block_ok = [&](int32_t blk) { return blk >= 0 && blk < a.num_blocks; };
+    const int64_t tok_stride = static_cast<int64_t>(a.n_kv) * HD;
+    const int64_t v_plane = a.num_blocks * BS * tok_stride;
+    const T* cache = static_cast<const T*>(a.cache);
+    const int64_t n_tiles = (t_end - t_begin + kMmaTile - 1) / kMmaTile;
+    const int64_t n_static = (t_lim - t_begin + kMmaTile - 1) / kMmaTile;
+    const int bs_log2 = __ffs(BS) - 1;  // block_size is a power of two
+    unsigned* vmask = reinterpret_cast<unsigned*>(smem + mma_ring_bytes(HD)) + warp * kMmaStages;
+    const unsigned FULL = 0xffffffffu;
+    // This warp's tile u into ring slot (u / warps) % stages: lane r < 16 finds token r's row
+    // once; the 16-byte copies then go row by row, LPR lanes per row (contiguous), and each
+    // lane's destination offsets in a slot are fixed, computed once. Chunks are XOR-swizzled
+    // by row so the 8 rows one ldmatrix reads sit in 8 different bank groups. Rows past
+    // seq_len or in a bad block are zero-filled (no read) and masked.
+    constexpr int LPR = CPR < 32 ? CPR : 32;  // lanes per row
+    constexpr int RPI = 32 / LPR;              // rows per instruction
+    const int col = lane % LPR, rr0 = lane / LPR;
+    const int64_t kvh_off = static_cast<int64_t>(kvh) * HD;
+    int dst_off[kMmaTile / RPI][CPR / LPR];
+#pragma unroll
+    for (int i = 0; i < kMmaTile / RPI; ++i)
+#pragma unroll
+        for (int cc = 0; cc < CPR / LPR; ++cc) {
+            const int r = rr0 + RPI * i, ch = col + cc * LPR;
+            dst_off[i][cc] = r * HD + ((ch ^ (r & 7)) * 8);
+        }
+    auto issue = [&](int64_t u) {
+        const int slot = static_cast<int>((u / kMmaWarps) % kMmaStages);
+        T* dst = ring + static_cast<size_t>(slot) * 2 * TE;
+        int64_t off = -1;  // element offset of token `lane`'s K row in the cache, -1: no row
+        if (lane < kMmaTile) {
+            const int64_t tok = t_begin + u * kMmaTile + lane;
+            const int32_t blk = tok < t_lim ? table[tok >> bs_log2] : 0;
+            if (tok < t_end) {
+                if (block_ok(blk)) {
+                    off = ((static_cast<int64_t>(blk) << bs_log2) + (tok & (BS - 1))) * tok_stride + kvh_off;
+                } else if (kvh == 0 && (tok & (BS - 1)) == 0 && a.err) {
+                    atomicAdd(a.err, 1);  // a bad block entry, counted once (kv head 0, its first token)
+                }
+            }
+        }
+        const unsigned valid = __ballot_sync(FULL, off >= 0) & 0xffffu;
+        if (lane == 0) vmask[slot] = valid;
+#pragma unroll
+        for (int i = 0; i < kMmaTile / RPI; ++i) {
+            const int64_t ro = __shfl_sync(FULL, off, rr0 + RPI * i);
+            const T* src = ro >= 0 ? cache + ro + col * 8 : cache;
+            const int n = ro >= 0 ? 16 : 0;
+#pragma unroll
+            for (int cc = 0; cc < CPR / LPR; ++cc) {
+                T* d = dst + dst_off[i][cc];
+                cp_async16_zfill(d, src + cc * LPR * 8, n);
+                cp_async16_zfill(d + TE, ro >= 0 ? src + cc * LPR * 8 + v_plane : cache, n);
+            }
+        }
+    };
+    for (int k = 0; k < kMmaStages - 1; ++k) {
+        const int64_t u = warp + static_cast<int64_t>(k) * kMmaWarps;
+        if (u < n_static) issue(u);
+        cp_async_commit();
+    }
+    // Q as A fragments (loaded while the first tiles are in flight): rows = query heads
+    // (zero past G), columns = dims of k-step s
+    uint32_t qa[KS][2];
+    {
+        const T* qrow = static_cast<const T*>(a.q) + b * a.qs + static_cast<int64_t>(kvh * G + fg) * HD;
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+            qa[s][0] = fg < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * s + 2 * ft) : 0u;
+            qa[s][1] = fg < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * s + 8 + 2 * ft) : 0u;
+        }
+    }
+
+    float o[NB][4];  // C fragments of O; rows fg + 8 (c2, c3) stay zero
+#pragma unroll
+    for (int d = 0; d < NB; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.0f;
+    float m = -INFINITY, l = 0.0f;
+    for (int64_t u = warp, k = 0; u < n_tiles; u += kMmaWarps, ++k) {
+        cp_async_wait<kMmaStages - 2>();
+        __syncwarp();
+        if (u + (kMmaStages - 1) * kMmaWarps < n_tiles) issue(u + (kMmaStages - 1) * kMmaWarps);
+        cp_async_commit();
+        const T* Ks = ring + static_cast<size_t>(k % kMmaStages) * 2 * TE;
+        const T* Vs = Ks + TE;
+        const unsigned valid = vmask[k % kMmaStages];
+
+        // S = Q K^T: two 8-token blocks
+        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        {
+            const int mi = lane >> 3, rr = lane & 7;
+            const int tok = 8 * (mi >> 1) + rr;
+#pragma unroll
+            for (int s = 0; s < KS; ++s) {
+                uint32_t kb[4];
+                const int chunk = 2 * s + (mi & 1);
+                ldsm_x4(kb, Ks + tok * HD + ((chunk ^ (tok & 7)) * 8));
+                Mma<T>::run(sc[0], qa[s][0], qa[s][1], kb[0], kb[1]);
+                Mma<T>::run(sc[1], qa[s][0], qa[s][1], kb[2], kb[3]);
+            }
+        }
+        // online softmax on row fg (this thread's tokens: 8 nb + 2 ft + e)
+        float v[2][2];
+        float mx = -INFINITY;
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                v[nb][e] = (valid >> (8 * nb + 2 * ft + e)) & 1u ? sc[nb][e] * a.scale_log2 : -INFINITY;
+                mx = fmaxf(mx, v[nb][e]);
+            }
+        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
+        const float m_new = fmaxf(m, mx);
+        const float corr = m_new == -INFINITY ? 1.0f : ex2(m - m_new);
+        float p[2][2];
+        float ps = 0.0f;
+#pragma unroll
+        for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                p[nb][e] = v[nb][e] == -INFINITY ? 0.0f : ex2(v[nb][e] - m_new);
+                ps += p[nb][e];
+            }
+        l = l * corr + ps;
+        m = m_new;
+        // P as A fragments, high part and residual
+        uint32_t ph0 = pack2<T>(p[0][0], p[0][1]), ph1 = pack2<T>(p[1][0], p[1][1]);
+        const float2 h0 = unpack2<T>(ph0), h1 = unpack2<T>(ph1);
+        uint32_t pl0 = pack2<T>(p[0][0] - h0.x, p[0][1] - h0.y), pl1 = pack2<T>(p[1][0] - h1.x, p[1][1] - h1.y);
+        // O = O * corr + P V (the rescale only when some row's max moved)
+        if (__any_sync(FULL, corr != 1.0f)) {
+#pragma unroll
+            for (int d = 0; d < NB; ++d) o[d][0] *= corr, o[d][1] *= corr;
+        }
+        {
+            const int mi = lane >> 3, rr = lane & 7;
+            const int tok = 8 * (mi & 1) + rr;
+#pragma unroll
+            for (int d2 = 0; d2 < NB / 2; ++d2) {
+                uint32_t vb[4];
+                const int chunk = 2 * d2 + (mi >> 1);
+                ldsm_x4_trans(vb, Vs + tok * HD + ((chunk ^ (tok & 7)) * 8));
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    Mma<T>::run(o[2 * d2 + h], ph0, ph1, vb[2 * h], vb[2 * h + 1]);
+                    Mma<T>::run(o[2 * d2 + h], pl0, pl1, vb[2 * h], vb[2 * h + 1]);
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
+    l += __shfl_xor_sync(FULL, l, 1);
+    l += __shfl_xor_sync(FULL, l, 2);
+
+    // warp partials into shared memory (over the rings, which are done)
+    __syncthreads();
+    float* wm = reinterpret_cast<float*>(smem);          // [warps][8]
+    float* wl = wm + kMmaWarps * 8;                      // [warps][8]
+    float* wo = wl + kMmaWarps * 8;                      // [warps][8][HD]
+    float* pm = wo + kMmaWarps * 8 * HD;                 // [8]  CTA partials for the cluster merge
+    float* pl = pm + 8;                                  // [8]
+    float* pacc = pl + 8;                                // [8][HD]
+    if (ft == 0) {
+        wm[warp * 8 + fg] = m;
+        wl[warp * 8 + fg] = l;
+    }
+#pragma unroll
+    for (int d = 0; d < NB; ++d) {
+        wo[(warp * 8 + fg) * HD + 8 * d + 2 * ft] = o[d][0];
+        wo[(warp * 8 + fg) * HD + 8 * d + 2 * ft + 1] = o[d][1];
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
+        const int gg = idx / HD, d = idx - gg * HD;
+        float M = -INFINITY;
+        for (int w = 0; w < kMmaWarps; ++w) M = fmaxf(M, wm[w * 8 + gg]);
+        float num = 0.0f, den = 0.0f;
+        if (M != -INFINITY) {
+            for (int w = 0; w < kMmaWarps; ++w) {
+                const float mw = wm[w * 8 + gg];
+                if (mw == -INFINITY) continue;
+                const float sw = exp2f(mw - M);
+                num = fmaf(sw, wo[(w * 8 + gg) * HD + d], num);
+                den = fmaf(sw, wl[w * 8 + gg], den);
+            }
+        }
+        pacc[idx] = num;
+        if (d == 0) pm[gg] = M, pl[gg] = den;
+    }
+    cluster.sync();
+    T* out = static_cast<T*>(a.out) + b * a.os + static_cast<int64_t>(kvh * G) * HD;
+    for (int idx = rank * blockDim.x + threadIdx.x; idx < G * HD; idx += S * blockDim.x) {
+        const int gg = idx / HD;
+        float M = -INFINITY;
+        for (int r = 0; r < S; ++r) M = fmaxf(M, cluster.map_shared_rank(pm, r)[gg]);
+        float num = 0.0f, den = 0.0f;
+        if (M != -INFINITY) {
+            for (int r = 0; r < S; ++r) {
+                const float mr = cluster.map_shared_rank(pm, r)[gg];
+                if (mr == -INFINITY) continue;
+                const float w = exp2f(mr - M);
+                num = fmaf(w, cluster.map_shared_rank(pacc, r)[idx], num);
+                den = fmaf(w, cluster.map_shared_rank(pl, r)[gg], den);
+            }
+        }
+        out[idx] = from_f32<T>(den > 0.0f ? num / den : 0.0f);
+    }
+    cluster.sync();
+}
+
+template <typename T, int HD>
+cudaError_t launch_mma(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
+    auto kernel = decode_mma_kernel<T, HD>;
+    const size_t smem = mma_smem(HD);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int splits = p.splits;
+    if (splits > 8) {
+        // a 16-CTA cluster is a non-portable size: use it only where the device can place one
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        int clusters = 0;
+        if (e == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = static_cast<unsigned>(splits);
+            attr.val.clusterDim.y = attr.val.clusterDim.z = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(splits));
+            cfg.blockDim = dim3(kMmaWarps * 32);
+            cfg.dynamicSmemBytes = smem;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+        }
+        if (e != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            splits = 8;
+        }
+    }
+    const dim3 grid(static_cast<unsigned>(a.B * a.n_kv * splits)), block(kMmaWarps * 32);
+    return launch_kernel(kernel, grid, block, smem, s, p.pdl, splits, a);
+}
+
 template <typename T, int HD, int STAGES>
 cudaError_t launch_hd(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
     auto kernel = decode_kernel<T, HD, STAGES>;
@@ -288,10 +655,15 @@ cudaError_t launch_stages(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) 
 
 template <typename T>
 cudaError_t launch_typed(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
+    if constexpr (sizeof(T) == 2) {
+        if (p.tensor_cores) return p.head_dim == 64 ? launch_mma<T, 64>(a, p, s) : launch_mma<T, 128>(a, p, s);
+    }
     return p.stages >= 4 ? launch_stages<T, 4>(a, p, s) : launch_stages<T, 2>(a, p, s);
 }
 
 }  // namespace attn
+
+size_t decode_attention_mma_smem(int head_dim) { return attn::mma_smem(head_dim); }
 
 size_t decode_attention_smem(int group, int head_dim, int block_size, int stages, int es) {
     return attn::layout(group, head_dim, block_size, stages, es).total;

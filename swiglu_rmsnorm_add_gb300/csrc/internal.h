@@ -140,7 +140,8 @@ struct AttnPlan {
     int head_dim;  // 64, 128 or 256 (template)
     int splits;    // CTAs per (request, kv head): the cluster size
     int threads;
-    int stages;    // K/V tiles in flight per CTA
+    int stages;    // K/V tiles in flight per CTA (CUDA-core path)
+    bool tensor_cores;  // bf16 / fp16, head_dim 64 or 128: the mma.sync path
     size_t smem;
     bool pdl;
     int num_sms;
@@ -148,6 +149,7 @@ struct AttnPlan {
 
 cudaError_t launch_decode_attention(const AttnArgs& a, const AttnPlan& p, int dtype, cudaStream_t s);
 size_t decode_attention_smem(int group, int head_dim, int block_size, int stages, int es);
+size_t decode_attention_mma_smem(int head_dim);
 
 // ------------------------------------------------------------------- UClip
 struct UclipArgs {

@@ -247,6 +247,8 @@ def test_variant_control(L):
     assert sra.variant_count("rmsnorm") == 7
     assert sra.variant_count("rope_kv_store") == 1
     assert sra.variant_count("glu") == 1
+    assert sra.variant_count("decode_attention") == 2
+    assert [sra.variant_name("decode_attention", i) for i in range(2)] == ["cuda_cores", "mma_sync"]
     assert sra.variant_count("nope") == ARG
     assert [sra.variant_name("rmsnorm", i) for i in range(7)] == ["warp_rows", "cta_row", "cta_smem", "two_pass",
                                                                   "cta_pair", "warp_smem", "pair_smem"]
@@ -277,6 +279,11 @@ def test_dispatch_choices(L):
     assert pick("rmsnorm", 2, 10_000_000, dtype=torch.float32, num_sms=152) == 3
     assert pick("glu", 4096, 14336, num_sms=152) == 0
     assert pick("rope_kv_store", 2048, 12, 2, 128, num_sms=152) == 0
+    # decode attention: tensor cores for 16-bit data up to head_dim 128, CUDA cores otherwise
+    assert pick("decode_attention", 32, 12, 2, 128, dtype=torch.bfloat16, num_sms=152) == 1
+    assert pick("decode_attention", 32, 12, 2, 256, dtype=torch.bfloat16, num_sms=152) == 0
+    assert pick("decode_attention", 32, 12, 2, 128, dtype=torch.float32, num_sms=152) == 0
+    assert pick("decode_attention", 32, 18, 2, 128, num_sms=152) == SHAPE
     assert pick("rmsnorm", -1, 16, num_sms=152) == SHAPE
 
 

@@ -89,19 +89,49 @@ def test_config_qwen25_long_context():
     assert_attention_close(got, want, cache, table, seq, "B=1 ctx=32768")
 
 
+@pytest.fixture(params=["auto", "cuda_cores"])
+def attn_variant(request):
+    """Run under the automatic choice and with the CUDA-core kernel forced."""
+    sra.force_variant("decode_attention", -1 if request.param == "auto" else 0)
+    yield request.param
+    sra.force_variant("decode_attention", -1)
+
+
 @pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
 @pytest.mark.parametrize("hd", [64, 128, 256])
 @pytest.mark.parametrize("n_head,n_kv", [(8, 8), (8, 4), (12, 2), (32, 4), (8, 1)])
 @pytest.mark.parametrize("bs", [8, 16, 32])
-def test_shapes_dtypes(dtype, hd, n_head, n_kv, bs):
+def test_shapes_dtypes(dtype, hd, n_head, n_kv, bs, attn_variant):
     lens = [1, 5, bs, bs + 1, 3 * bs - 1, 200]
     q, cache, table, seq = syn.attention_inputs(6, lens, n_head, n_kv, hd, bs, 6 * (200 // bs + 2), dtype,
                                                 1015 + hd + bs)
     got, want = run_both(q, cache, table, seq, expect_err=0)
-    assert_attention_close(got, want, cache, table, seq, f"{dtype} hd={hd} {n_head}/{n_kv} bs={bs}")
+    assert_attention_close(got, want, cache, table, seq, f"{dtype} hd={hd} {n_head}/{n_kv} bs={bs} {attn_variant}")
 
 
-def test_bad_entries_empty_requests_and_clamping():
+@pytest.mark.parametrize("B,ctx", [(1, 32768), (32, 1024), (3, 4097)])
+def test_cuda_core_kernel_on_the_configs(B, ctx):
+    sra.force_variant("decode_attention", 0)
+    try:
+        q, cache, table, seq = syn.attention_inputs(B, ctx, 12, 2, 128, 16, max(64, B * (ctx // 16 + 1)),
+                                                    torch.bfloat16, 1020)
+        got, want = run_both(q, cache, table, seq, expect_err=0)
+        assert_attention_close(got, want, cache, table, seq, f"cuda cores B={B} ctx={ctx}")
+    finally:
+        sra.force_variant("decode_attention", -1)
+
+
+def test_forcing_the_mma_kernel_where_it_cannot_run():
+    q, cache, table, seq = syn.attention_inputs(2, 40, 8, 2, 256, 16, 16, torch.bfloat16, 1021)
+    sra.force_variant("decode_attention", 1)
+    try:
+        with pytest.raises(sra.SRAError):
+            sra.paged_decode_attention(q.to(DEV), cache.to(DEV), table.to(DEV), seq.to(DEV))
+    finally:
+        sra.force_variant("decode_attention", -1)
+
+
+def test_bad_entries_empty_requests_and_clamping(attn_variant):
     q, cache, table, seq = syn.attention_inputs(4, 64, 12, 2, 128, 16, 64, torch.bfloat16, 1016, max_blocks=5)
     table[0, 1] = 64          # out of range: block 1 of request 0 skipped
     table[1, 0] = -3          # negative
@@ -112,7 +142,7 @@ def test_bad_entries_empty_requests_and_clamping():
     assert bool((got[2] == 0).all())
 
 
-def test_dominant_key_and_scale():
+def test_dominant_key_and_scale(attn_variant):
     q, cache, table, seq = syn.attention_inputs(2, 300, 12, 2, 128, 16, 64, torch.bfloat16, 1017)
     q.zero_()
     q[:, :, 0] = 1.0
