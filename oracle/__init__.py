@@ -72,6 +72,8 @@ def lib() -> ctypes.CDLL:
             L.orc_paged_decode_attention.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i64, i64, i32,
                                                      i64, dbl, i32]
             L.orc_paged_decode_attention.restype = i64
+            L.orc_linear.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32]
+            L.orc_linear.restype = i32
             _lib = L
     return _lib
 
@@ -260,3 +262,33 @@ def paged_decode_attention(q, kv_cache, block_table, seq_lens, out, scale: float
     if n < 0:
         raise ValueError("oracle: bad paged_decode_attention arguments")
     return int(n)
+
+
+def linear(h: torch.Tensor, W: torch.Tensor, y: torch.Tensor) -> None:
+    """y[b, n] = sum_k h[b, k] * W[n, k]: h [B, K], W [N, K] contiguous (nn.Linear), y [B, N]."""
+    for t, n in ((h, "h"), (W, "W"), (y, "y")):
+        _cpu(t, n)
+    assert W.is_contiguous()
+    B, K = h.shape
+    N = W.shape[0]
+    rc = lib().orc_linear(h.data_ptr(), W.data_ptr(), y.data_ptr(), B, K, N, _row_stride(h), _row_stride(y),
+                          _FMT[h.dtype])
+    if rc != 0:
+        raise ValueError("oracle: bad linear arguments")
+
+
+def rmsnorm_linear(x, w_ln, W, y, eps: float) -> None:
+    """The norm as the projection's prologue: y = rmsnorm(x) * w_ln @ W^T, with the normed
+    rows rounded to the dtype as the separate norm kernel stores them."""
+    h = torch.empty(x.shape, dtype=x.dtype)
+    rmsnorm(x, w_ln, h, eps)
+    linear(h, W, y)
+
+
+def glu_linear(gate_up, W, y, act: str = "silu") -> None:
+    """The GLU as the down projection's prologue: y = (act(gate) * up) @ W^T, the activation
+    rounded to the dtype as the separate GLU kernel stores it."""
+    B, W2 = gate_up.shape
+    h = torch.empty(B, W2 // 2, dtype=gate_up.dtype)
+    glu(gate_up, h, act)
+    linear(h, W, y)

@@ -445,4 +445,25 @@ int64_t orc_paged_decode_attention(const void* q, const void* kv_cache, const in
     return errors;
 }
 
+// The linear layer of a decoder (nn.Linear's layout): y[b, n] = sum_k h[b, k] * W[n, k]
+// with W [N, K] row-major, accumulated in double and rounded once ([lsln] section
+// 2.2: ln1 feeds qkv_proj; the norm's output h is what the separate norm kernel
+// stores, in the same format). Used after rmsnorm (norm as the GEMV's prologue) and
+// after the GLU (the activation fused into the down projection).
+int orc_linear(const void* h, const void* W, void* y, int64_t B, int64_t K, int64_t N, int64_t h_row_stride,
+               int64_t y_row_stride, int fmt) {
+    FormatSpec s;
+    if (!format_spec(fmt, &s) || B < 0 || K <= 0 || N <= 0) return -1;
+    std::vector<double> hb(K);
+    for (int64_t b = 0; b < B; ++b) {
+        for (int64_t k = 0; k < K; ++k) hb[k] = load(h, b * h_row_stride + k, fmt);
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k) acc += hb[k] * load(W, n * K + k, fmt);
+            store(y, b * y_row_stride + n, acc, fmt);
+        }
+    }
+    return 0;
+}
+
 }  // extern "C"

@@ -71,6 +71,10 @@ MUTANTS = [
      "test_oracle_attention.py"),
     ("attention denominator dropped", "rows.empty() ? 0.0 : acc[d] / denom", "rows.empty() ? 0.0 : acc[d]",
      "test_oracle_attention.py"),
+    ("linear weight transposed", "acc += hb[k] * load(W, n * K + k, fmt);", "acc += hb[k] * load(W, k * N + n, fmt);",
+     "test_oracle_linear.py"),
+    ("linear accumulates in float", "double acc = 0.0;\n            for (int64_t k = 0; k < K; ++k) acc += hb[k]",
+     "float acc = 0.0f;\n            for (int64_t k = 0; k < K; ++k) acc += hb[k]", "test_oracle_linear.py"),
     ("ties away from zero", "(frac > 0.5 || (frac == 0.5 && std::fmod(fl, 2.0) != 0.0))",
      "(frac >= 0.5)", "test_oracle_rounding.py"),
     ("no overflow to infinity", "if (r > maxfin) r = INFINITY;", "", "test_oracle_rounding.py"),
