@@ -239,6 +239,31 @@ def build_entries(dev, stream_handle, only=(), companions=False):
                                  (q.data_ptr(), cache.data_ptr(), table.data_ptr(), seq.data_ptr(), out.data_ptr(),
                                   B, 12, 2, 128, 12 * 128, 12 * 128, nb, 16, table.shape[1], 128 ** -0.5, None, 2,
                                   stream_handle), [q, table, seq], [out], keep=(q, cache, table, seq, out)))
+    if companions:
+        # RMSNorm / SwiGLU fused into the projection they feed (Qwen2.5-1.5B: ln1 + qkv_proj,
+        # silu(gate) * up + down_proj), decode batch 1 and 64
+        for B in (1, 64):
+            K, N = syn.QWEN25_QKV["K"], syn.QWEN25_QKV["N"]
+            name = f"rmsnorm_linear:bf16:B{B}x{K}x{N}"
+            if want(name):
+                x = syn.normal((B, K), 0.0, 1.0, torch.bfloat16, 1030, 1).to(dev)
+                w = syn.normal((K,), 1.0, 0.1, torch.bfloat16, 1030, 2).to(dev)
+                W = syn.linear_weight(N, K, torch.bfloat16, 1030).to(dev)
+                y = torch.empty(B, N, dtype=torch.bfloat16, device=dev)
+                nbytes = (N * K + B * K + K + B * N) * 2
+                entries.append(Entry(name, "linear", nbytes, B, L.sra_rmsnorm_linear,
+                                     (x.data_ptr(), w.data_ptr(), W.data_ptr(), y.data_ptr(), B, K, N, K, N, syn.EPS,
+                                      2, stream_handle), [x], [y], keep=(x, w, W, y)))
+            I, N = syn.QWEN25_DOWN["I"], syn.QWEN25_DOWN["N"]
+            name = f"swiglu_linear:bf16:B{B}x{I}x{N}"
+            if want(name):
+                gu = syn.normal((B, 2 * I), 0.0, 1.0, torch.bfloat16, 1031, 3).to(dev)
+                W = syn.linear_weight(N, I, torch.bfloat16, 1031).to(dev)
+                y = torch.empty(B, N, dtype=torch.bfloat16, device=dev)
+                nbytes = (N * I + B * 2 * I + B * N) * 2
+                entries.append(Entry(name, "linear", nbytes, B, L.sra_glu_linear,
+                                     (gu.data_ptr(), W.data_ptr(), y.data_ptr(), B, I, N, 2 * I, N, 0, 2,
+                                      stream_handle), [gu], [y], keep=(gu, W, y)))
     I = syn.LLAMA3_8B_MLP["intermediate"]
     for T in Ts_glu:
         gu = None

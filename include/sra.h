@@ -12,6 +12,7 @@
  *   sra_glu            SwiGLU silu(gate) * up, or ReGLU relu(gate) * up, over a fused gate_up
  *   sra_uclip          UClip / DyHT clamp(alpha * x, lo, hi) * gamma over [N, H, D] views
  *   sra_paged_decode_attention  softmax decode attention read through the paged cache's block table
+ *   sra_rmsnorm_linear / sra_glu_linear  RMSNorm / GLU fused into the projection they feed
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -38,7 +39,8 @@
  * Sources. The operators are those of these web pages (cited by title and section):
  *  [koas] koas-w.github.io "preformanceimprovement": sec. 1 fused RoPE + paged KV
  *         cache store; sec. 2 fused SwiGLU; sec. 3 Triton RMSNorm; sec. 4 fused add + norm.
- *  [lsln] m.lsln.cn/news/61269 "21 个算子": sec. 2.3 RMSNorm and RoPE details.
+ *  [lsln] m.lsln.cn/news/61269 "21 个算子": sec. 2.2 fusion choices (ln1 + qkv_proj);
+ *         sec. 2.3 RMSNorm and RoPE details; sec. 3 split reductions; sec. 5.3 cache read.
  *  [mer]  mer.dev "AsyncT vllm 适配加速笔记（一）": sec. 0 DyHT replacing RMSNorm;
  *         sec. 1.1 KV-cache layout; sec. 3.3 kernel fusion (ReGLU as relu_and_mul;
  *         the UClip kernel; stride-aware Q/K views).
@@ -273,6 +275,44 @@ SRA_API int sra_paged_decode_attention(const void* q, const void* kv_cache, cons
                                        int head_dim, int64_t q_tok_stride, int64_t out_tok_stride,
                                        int64_t num_blocks, int block_size, int64_t max_blocks_per_seq, float scale,
                                        int32_t* err_count, int dtype, void* stream);
+
+/*
+ * sra_rmsnorm_linear — RMSNorm as the prologue of the projection it feeds
+ * ([lsln] sec. 2.2: ln1 + qkv_proj fused, the normed rows never stored):
+ *
+ *   h[b, :] = RNE(x[b, :] * rsqrt(mean_k x[b, k]^2 + eps) * w_ln[:])   (as sra_rmsnorm)
+ *   y[b, n] = RNE(sum_k h[b, k] * W[n, k])
+ *
+ * x:    [B, K] of `dtype`, row stride x_row_stride (>= K). Read only.
+ * w_ln: [K] RMSNorm weight of `dtype`. Read only.
+ * W:    [N, K] of `dtype`, row-major (nn.Linear's [out, in] layout). Read only.
+ * y:    [B, N] of `dtype`, row stride y_row_stride (>= N); must not overlap x, w_ln or W.
+ * bf16 / fp16 with K and N multiples of 64 and 16-byte aligned x, w_ln, W (x_row_stride a
+ * multiple of 8) run on the tensor cores (fp32 accumulation); other layouts and fp32 run
+ * a CUDA-core kernel with the same result up to the order of the fp32 sums.
+ * Errors: unknown dtype -> SRA_ERR_DTYPE; B < 0, K <= 0 or N <= 0 (or K too long for
+ * one CTA's shared memory on the CUDA-core path) -> SRA_ERR_SHAPE; short strides ->
+ * SRA_ERR_STRIDE; eps negative or not finite -> SRA_ERR_ARG; NULL -> SRA_ERR_NULL;
+ * overlap -> SRA_ERR_ALIAS. B == 0 is a no-op.
+ */
+SRA_API int sra_rmsnorm_linear(const void* x, const void* w_ln, const void* W, void* y, int64_t B, int64_t K,
+                               int64_t N, int64_t x_row_stride, int64_t y_row_stride, float eps, int dtype,
+                               void* stream);
+
+/*
+ * sra_glu_linear — the gated activation as the prologue of the down projection
+ * ([lsln] sec. 2.2 applied to the MLP; [koas] sec. 2 / [mer] sec. 3.3 for the
+ * activation):
+ *
+ *   h[b, i] = RNE(act(gate_up[b, i]) * gate_up[b, I + i])   (as sra_glu)
+ *   y[b, n] = RNE(sum_i h[b, i] * W[n, i])
+ *
+ * gate_up: [B, 2I] of `dtype`, row stride in_row_stride (>= 2I). W: [N, I] row-major.
+ * y: [B, N], row stride y_row_stride. act: sra_act_t. Layout rules, paths and errors
+ * as sra_rmsnorm_linear (an unknown act -> SRA_ERR_ARG).
+ */
+SRA_API int sra_glu_linear(const void* gate_up, const void* W, void* y, int64_t B, int64_t I, int64_t N,
+                           int64_t in_row_stride, int64_t y_row_stride, int act, int dtype, void* stream);
 
 /*
  * sra_uclip — [mer] sec. 0 (DyHT(x) = y * clamp(a x, -1, 1) in place of every

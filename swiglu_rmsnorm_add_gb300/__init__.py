@@ -1,6 +1,7 @@
 """GB300-native fused per-token decoder path: RMSNorm, residual-add + RMSNorm,
 RoPE (neox or interleaved) with paged KV-cache store, SwiGLU / ReGLU, UClip / DyHT,
-and the decode-attention read of the paged cache.
+the decode-attention read of the paged cache, and RMSNorm / GLU fused into the
+projection they feed.
 
 Every operator runs in the hand-written sm_103a CUDA kernels of ``libsra.so``
 (C ABI in ``include/sra.h``). This module only marshals torch tensors into that
@@ -13,11 +14,13 @@ from ._binding import (  # noqa: F401
     dyht,
     force_variant,
     glu,
+    glu_linear,
     lib,
     paged_decode_attention,
     pick_variant,
     reglu,
     rmsnorm,
+    rmsnorm_linear,
     rope_kv_store,
     set_pdl,
     status_string,
@@ -27,6 +30,7 @@ from ._binding import (  # noqa: F401
     variant_name,
 )
 
-__all__ = ["rmsnorm", "add_rmsnorm", "rope_kv_store", "swiglu", "reglu", "glu", "uclip", "dyht", "paged_decode_attention", "lib",
+__all__ = ["rmsnorm", "add_rmsnorm", "rope_kv_store", "swiglu", "reglu", "glu", "uclip", "dyht", "paged_decode_attention",
+           "rmsnorm_linear", "glu_linear", "lib",
            "SRAError",
            "force_variant", "set_pdl", "variant_count", "variant_name", "pick_variant", "status_string"]

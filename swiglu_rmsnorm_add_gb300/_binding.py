@@ -45,12 +45,15 @@ def lib() -> ctypes.CDLL:
                                                                                         f32, i32, vp]
             L.sra_paged_decode_attention.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i64, i64, i32,
                                                      i64, f32, vp, i32, vp]
+            L.sra_rmsnorm_linear.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, i32, vp]
+            L.sra_glu_linear.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, vp]
             L.sra_glu.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, vp]
             L.sra_swiglu.argtypes = [vp, vp, i64, i64, i64, i64, i32, vp]
             L.sra_uclip.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i32, i32, f32, f32, i32,
                                     vp]
             for fn in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_rope_kv_store_ex", "sra_glu",
-                       "sra_swiglu", "sra_uclip", "sra_rope_kv_store_qk_uclip", "sra_paged_decode_attention"):
+                       "sra_swiglu", "sra_uclip", "sra_rope_kv_store_qk_uclip", "sra_paged_decode_attention",
+                       "sra_rmsnorm_linear", "sra_glu_linear"):
                 getattr(L, fn).restype = i32
             L.sra_status_string.argtypes = [i32]
             L.sra_status_string.restype = ctypes.c_char_p
@@ -397,3 +400,63 @@ def paged_decode_attention(q: torch.Tensor, kv_cache: torch.Tensor, block_table:
                                               _dtype(q), _stream(q, stream))
     _check("sra_paged_decode_attention", st)
     return out
+
+
+def _linear_check(x, W, y, B, K, N):
+    _cuda(W, "W")
+    if W.dim() != 2 or tuple(W.shape) != (N, K) or not W.is_contiguous():
+        raise ValueError("W must be a contiguous [N, K] tensor (nn.Linear's weight)")
+    if W.dtype != x.dtype or (y is not None and y.dtype != x.dtype):
+        raise ValueError("x, W and y must share one dtype")
+
+
+def rmsnorm_linear(x: torch.Tensor, w_ln: torch.Tensor, W: torch.Tensor, y: torch.Tensor | None = None,
+                   eps: float = 1e-6, stream=None) -> torch.Tensor:
+    """y = rmsnorm(x) * w_ln @ W^T with the norm fused in as the projection's prologue.
+    x: [B, K]; w_ln: [K]; W: [N, K] (nn.Linear); y: [B, N]."""
+    _cuda(x, "x")
+    _cuda(w_ln, "w_ln")
+    B, K, xs = _as_rows(x, "x")
+    N = W.shape[0]
+    _linear_check(x, W, y, B, K, N)
+    if w_ln.numel() != K or w_ln.dtype != x.dtype or not w_ln.is_contiguous():
+        raise ValueError("w_ln must be a contiguous [K] tensor of x's dtype")
+    if y is None:
+        y = torch.empty(*x.shape[:-1], N, dtype=x.dtype, device=x.device)
+    _cuda(y, "y")
+    _same_device(x, w_ln, W, y)
+    yr, yn, ys = _as_rows(y, "y")
+    if (yr, yn) != (B, N):
+        raise ValueError("shape mismatch")
+    with torch.cuda.device(x.device):
+        st = lib().sra_rmsnorm_linear(x.data_ptr(), w_ln.data_ptr(), W.data_ptr(), y.data_ptr(), B, K, N, xs, ys,
+                                      float(eps), _dtype(x), _stream(x, stream))
+    _check("sra_rmsnorm_linear", st)
+    return y
+
+
+def glu_linear(gate_up: torch.Tensor, W: torch.Tensor, y: torch.Tensor | None = None, act: str = "silu",
+               stream=None) -> torch.Tensor:
+    """y = (act(gate) * up) @ W^T with the activation fused in as the down projection's prologue.
+    gate_up: [B, 2I]; W: [N, I] (nn.Linear); y: [B, N]."""
+    _cuda(gate_up, "gate_up")
+    B, W2, xs = _as_rows(gate_up, "gate_up")
+    if W2 % 2:
+        raise ValueError("gate_up width must be even (gate | up)")
+    I = W2 // 2
+    N = W.shape[0]
+    _linear_check(gate_up, W, y, B, I, N)
+    if act not in ACT_CODE:
+        raise ValueError("act must be 'silu' or 'relu'")
+    if y is None:
+        y = torch.empty(*gate_up.shape[:-1], N, dtype=gate_up.dtype, device=gate_up.device)
+    _cuda(y, "y")
+    _same_device(gate_up, W, y)
+    yr, yn, ys = _as_rows(y, "y")
+    if (yr, yn) != (B, N):
+        raise ValueError("shape mismatch")
+    with torch.cuda.device(gate_up.device):
+        st = lib().sra_glu_linear(gate_up.data_ptr(), W.data_ptr(), y.data_ptr(), B, I, N, xs, ys, ACT_CODE[act],
+                                  _dtype(gate_up), _stream(gate_up, stream))
+    _check("sra_glu_linear", st)
+    return y

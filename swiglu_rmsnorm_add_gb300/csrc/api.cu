@@ -792,6 +792,73 @@ int sra_paged_decode_attention(const void* q, const void* kv_cache, const int32_
     return status_from(launch_decode_attention(a, plan, dtype, static_cast<cudaStream_t>(stream)));
 }
 
+// ------------------------------------------------------------------- fused linear
+static int linear_common(const void* x, const void* w_ln, const void* W, void* y, int64_t B, int64_t K, int64_t N,
+                      int64_t xs, int64_t ys, float eps, int prologue, int dtype, void* stream) {
+    if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
+    if (B < 0 || K <= 0 || N <= 0) return SRA_ERR_SHAPE;
+    const int64_t xw = prologue == 0 ? K : 2 * K;
+    if (xs < xw || ys < N) return SRA_ERR_STRIDE;
+    if (prologue == 0 && (!(eps >= 0.0f) || !std::isfinite(eps))) return SRA_ERR_ARG;
+    if (B == 0) return SRA_OK;
+    if (!x || !W || !y || (prologue == 0 && !w_ln)) return SRA_ERR_NULL;
+    const int es = elem_bytes(dtype);
+    const Span sy = span_of(y, B, ys, N, es);
+    if (rows_overlap(y, B, ys, N, x, B, xs, xw, es) || overlap(sy, span_of(W, 1, 0, N * K, es)) ||
+        (prologue == 0 && overlap(sy, span_of(w_ln, 1, 0, K, es))))
+        return SRA_ERR_ALIAS;
+    int dev = 0;
+    const int sms = current_sm_count(&dev);
+    if (sms <= 0) return SRA_ERR_DEVICE;
+    const int64_t limit = smem_optin(dev) - 1024;
+    LinPlan plan;
+    plan.prologue = prologue;
+    plan.pdl = g_pdl;
+    plan.mt = B <= 16 ? 1 : (B <= 32 ? 2 : 4);
+    plan.tensor_cores = dtype != DT_F32 && K % 64 == 0 && N % 64 == 0 && aligned16(x) && aligned16(W) &&
+                        xs % 8 == 0 && (prologue != 0 || aligned16(w_ln));
+    plan.splits = 1;
+    if (plan.tensor_cores) {
+        // about one CTA per SM: 64-column slices x row blocks x K splits (a cluster)
+        // two CTAs per SM fit (about 80 KB each); aim for one wave of 1-2 CTAs per SM with at
+        // least two W tiles per CTA
+        const int64_t slices = (N / 64) * ((B + plan.mt * 16 - 1) / (plan.mt * 16));
+        const int64_t KT = K / 64;
+        while (plan.splits < 8 && slices * plan.splits * 2 <= 2 * static_cast<int64_t>(sms) &&
+               KT >= 4 * plan.splits)
+            plan.splits *= 2;
+        if (static_cast<int64_t>(linear_smem(plan.mt)) > limit) plan.tensor_cores = false;
+    }
+    if (!plan.tensor_cores) {
+        plan.splits = 1;
+        if (K * 4 > limit) return SRA_ERR_SHAPE;
+    }
+    LinArgs a;
+    a.x = x;
+    a.w_ln = w_ln;
+    a.W = W;
+    a.y = y;
+    a.B = B;
+    a.K = K;
+    a.N = N;
+    a.xs = xs;
+    a.ys = ys;
+    a.eps = eps;
+    return status_from(launch_linear(a, plan, dtype, static_cast<cudaStream_t>(stream)));
+}
+
+int sra_rmsnorm_linear(const void* x, const void* w_ln, const void* W, void* y, int64_t B, int64_t K, int64_t N,
+                       int64_t x_row_stride, int64_t y_row_stride, float eps, int dtype, void* stream) {
+    return linear_common(x, w_ln, W, y, B, K, N, x_row_stride, y_row_stride, eps, 0, dtype, stream);
+}
+
+int sra_glu_linear(const void* gate_up, const void* W, void* y, int64_t B, int64_t I, int64_t N,
+                   int64_t in_row_stride, int64_t y_row_stride, int act, int dtype, void* stream) {
+    if (act != SRA_ACT_SILU && act != SRA_ACT_RELU) return valid_dtype(dtype) ? SRA_ERR_ARG : SRA_ERR_DTYPE;
+    return linear_common(gate_up, nullptr, W, y, B, I, N, in_row_stride, y_row_stride, 0.0f, 1 + act, dtype,
+                             stream);
+}
+
 // ------------------------------------------------------------------- UClip
 int sra_uclip(const void* x, const float* alpha, const float* gamma, void* out, int64_t N, int64_t H, int64_t D,
               int64_t x_n_stride, int64_t x_h_stride, int64_t out_n_stride, int64_t out_h_stride,

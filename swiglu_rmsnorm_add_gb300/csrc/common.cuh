@@ -210,16 +210,6 @@ template <> struct Elem<__half> {
     }
 };
 
-// v rounded to T (RNE) and widened back: the value a store of v as T would hold.
-template <typename T>
-__device__ __forceinline__ float round_to(float v) {
-    if constexpr (sizeof(T) == 4) {
-        return v;
-    } else {
-        return Elem<T>::from_bits16(Elem<T>::to_bits16(v));
-    }
-}
-
 template <typename T, int VEC>
 struct Vec {
     static constexpr int BYTES = VEC * int(sizeof(T));

@@ -151,6 +151,27 @@ cudaError_t launch_decode_attention(const AttnArgs& a, const AttnPlan& p, int dt
 size_t decode_attention_smem(int group, int head_dim, int block_size, int stages, int es);
 size_t decode_attention_mma_smem(int head_dim);
 
+// ------------------------------------------------------------------- fused linear
+struct LinArgs {
+    const void* x;     // [B, K] (RMSNorm prologue) or gate_up [B, 2K] (GLU prologue), row stride xs
+    const void* w_ln;  // [K] RMSNorm weight (RMSNorm prologue only)
+    const void* W;     // [N, K] row-major (nn.Linear)
+    void* y;           // [B, N], row stride ys
+    int64_t B, K, N, xs, ys;
+    float eps;
+};
+
+struct LinPlan {
+    int prologue;       // 0 RMSNorm, 1 SwiGLU, 2 ReGLU
+    bool tensor_cores;  // bf16 / fp16, K and N multiples of 64, 16-byte aligned layouts
+    int mt;             // 16-row m-tiles per CTA (1, 2 or 4)
+    int splits;         // CTAs per cluster along K
+    bool pdl;
+};
+
+cudaError_t launch_linear(const LinArgs& a, const LinPlan& p, int dtype, cudaStream_t s);
+size_t linear_smem(int mt);
+
 // ------------------------------------------------------------------- UClip
 struct UclipArgs {
     const void* x;       // [N, H, D], strides (xn, xh, 1)

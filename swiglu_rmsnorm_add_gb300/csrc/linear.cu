@@ -1,0 +1,388 @@
+// The decoder's projections with their elementwise producer fused in as a
+// prologue: y = prologue(x) @ W^T, W in nn.Linear's [N, K] layout.
+//
+// m.lsln.cn 21-operator article, section 2.2: the RMSNorm before the
+// attention feeds qkv_proj directly, so the norm runs inside the projection
+// and its output never goes to memory (3-5 % of the step); the same holds for
+// the activation before the MLP's down projection (silu(gate) * up, or relu).
+// The prologue's rows are rounded to the dtype, as the separate kernel would
+// store them, before they meet W.
+//
+// At decode batch sizes the cost is the weight read (N * K * 2 bytes per call),
+// so the layout streams W once: a CTA owns a 64-column slice of y for up to 64
+// rows, the K dimension is split over the CTAs of a thread-block cluster, and
+// the partial products are summed through distributed shared memory (no global
+// scratch). Inside a CTA, W tiles of 64 x 64 stream through an 8-deep cp.async
+// ring, and h is produced tile by tile next to them: the inputs of the next
+// tile are loaded into registers while the current one is multiplied, then
+// normed (or activated), rounded to T and stored into the other of two h
+// buffers. For the RMSNorm each CTA first sums the squares of its K range and
+// the cluster exchanges the partial sums, so every row's statistic is complete
+// before the first tile. The products run on the tensor cores
+// as mma.sync m16n8k16 with fp32 accumulators (h as the A operand through
+// ldmatrix, W tiles as the B operand through ldmatrix, 16-byte chunks
+// XOR-swizzled by row against bank conflicts).
+#include <cooperative_groups.h>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace cg = cooperative_groups;
+
+namespace sra {
+namespace lin {
+
+constexpr int kWarps = 4;
+constexpr int kNT = 64;      // columns of y per CTA
+constexpr int kKT = 64;      // K per W tile
+constexpr int kStages = 8;   // W tiles in flight (64 KB)
+
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(s), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t (&r)[4], const void* p) {
+    const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(p));
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(s));
+}
+
+template <typename T>
+struct Mma;
+template <>
+struct Mma<__nv_bfloat16> {
+    __device__ __forceinline__ static void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+};
+template <>
+struct Mma<__half> {
+    __device__ __forceinline__ static void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+        asm volatile(
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+            "{%0,%1,%2,%3};"
+            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+            : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+    }
+};
+
+template <typename T>
+__device__ __forceinline__ T to_t(float v) {
+    const unsigned short b = Elem<T>::to_bits16(v);
+    T r;
+    memcpy(&r, &b, 2);
+    return r;
+}
+
+// Shared memory: the W ring [stages][64][64] (the epilogue's partial tile reuses it once
+// drained), two h tiles [MT*16][64] (built while the other is multiplied), row statistics.
+__host__ __device__ inline size_t ring_bytes() { return static_cast<size_t>(kStages) * kNT * kKT * 2; }
+__host__ __device__ inline size_t htile_bytes(int MT) { return static_cast<size_t>(MT) * 16 * kKT * 2; }
+__host__ __device__ inline size_t smem_bytes(int MT) {
+    const size_t part = static_cast<size_t>(MT) * 16 * kNT * 4;
+    return (ring_bytes() > part ? ring_bytes() : part) + 2 * htile_bytes(MT) + static_cast<size_t>(MT) * 16 * 4;
+}
+
+// 16-byte chunk c of row r of a row-major tile whose rows hold `cpr` chunks.
+__device__ __forceinline__ int swz(int r, int c) { return c ^ (r & 7); }
+
+template <int ACT>
+__device__ __forceinline__ float glu_act(float g) {
+    if constexpr (ACT == 0) {
+        return __fdividef(g, 1.0f + __expf(-g));
+    } else {
+        return fmaxf(g, 0.0f);
+    }
+}
+
+// PRO: 0 = RMSNorm prologue, 1 = SwiGLU, 2 = ReGLU.
+template <typename T, int MT, int PRO>
+__global__ void __launch_bounds__(kWarps * 32) linear_kernel(LinArgs a) {
+    using V8 = Vec<T, 8>;
+    using R8 = typename V8::Raw;
+    extern __shared__ __align__(16) unsigned char smem[];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int SK = static_cast<int>(cluster.num_blocks());
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t n0 = (blockIdx.x / SK) * static_cast<int64_t>(kNT);
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * MT * 16;
+    const int rows = static_cast<int>(a.B - r0 < MT * 16 ? a.B - r0 : MT * 16);
+    const int KT = static_cast<int>(a.K / kKT);
+    const int per = (KT + SK - 1) / SK;
+    const int kt0 = rank * per < KT ? rank * per : KT;
+    const int kt1 = kt0 + per < KT ? kt0 + per : KT;
+    const int ntiles = kt1 - kt0;
+    const int64_t kbase = static_cast<int64_t>(kt0) * kKT;
+    T* ring = reinterpret_cast<T*>(smem);
+    float* part = reinterpret_cast<float*>(smem);  // the epilogue's partial tile, after the ring drains
+    const size_t ring_area = ring_bytes() > static_cast<size_t>(MT) * 16 * kNT * 4
+                                 ? ring_bytes()
+                                 : static_cast<size_t>(MT) * 16 * kNT * 4;
+    T* hbuf = reinterpret_cast<T*>(smem + ring_area);                         // [2][MT*16][64]
+    float* stat = reinterpret_cast<float*>(smem + ring_area + 2 * htile_bytes(MT));
+    const T* W = static_cast<const T*>(a.W);
+    const T* X = static_cast<const T*>(a.x);
+
+    // W tile t (columns (kt0 + t) * 64 .. of rows n0 .. n0 + 63) into ring slot t % stages
+    auto issue = [&](int t) {
+        T* dst = ring + static_cast<size_t>(t % kStages) * kNT * kKT;
+        const T* src = W + n0 * a.K + (kbase + static_cast<int64_t>(t) * kKT);
+        for (int c = threadIdx.x; c < kNT * 8; c += kWarps * 32) {
+            const int r = c >> 3, ch = c & 7;
+            cp_async16(dst + r * kKT + swz(r, ch) * 8, src + static_cast<int64_t>(r) * a.K + ch * 8);
+        }
+    };
+    pdl_enter();
+    for (int t = 0; t < kStages - 1; ++t) {
+        if (t < ntiles) issue(t);
+        cp_async_commit();
+    }
+
+    // h tiles: thread owns chunks c = tid + 128 i (i < MT) of the [MT*16][64] tile: row c / 8,
+    // 8-element chunk c % 8. The inputs of tile t + 1 are loaded into registers while tile t
+    // is multiplied, then turned into h (rounded to T) in the other buffer.
+    R8 xa[MT], xb[MT];  // x (or gate) and w_ln (or up) chunks
+    auto prefetch = [&](int t) {
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            const int c = threadIdx.x + kWarps * 32 * i, r = c >> 3, ch = c & 7;
+            if (r < rows) {
+                const int64_t k = kbase + static_cast<int64_t>(t) * kKT + ch * 8;
+                const T* xr = X + (r0 + r) * a.xs + k;
+                xa[i] = V8::load(xr);
+                xb[i] = PRO == 0 ? V8::load(static_cast<const T*>(a.w_ln) + k) : V8::load(xr + a.K);
+            }
+        }
+    };
+    __shared__ float inv[64];
+    auto build = [&](int t) {
+        T* hb = hbuf + static_cast<size_t>(t & 1) * MT * 16 * kKT;
+#pragma unroll
+        for (int i = 0; i < MT; ++i) {
+            const int c = threadIdx.x + kWarps * 32 * i, r = c >> 3, ch = c & 7;
+            float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if (r < rows) {
+                float g[8];
+                V8::unpack(xa[i], f);
+                V8::unpack(xb[i], g);
+                if constexpr (PRO == 0) {
+                    const float iv = inv[r];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = f[e] * iv * g[e];
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = glu_act<PRO - 1>(f[e]) * g[e];
+                }
+            }
+            *reinterpret_cast<R8*>(hb + r * kKT + swz(r, ch) * 8) = V8::pack(f);
+        }
+    };
+    if (ntiles > 0) prefetch(0);
+    if constexpr (PRO == 0) {
+        // each rank sums the squares of its K range; the cluster exchanges the partial sums
+        for (int r = warp; r < MT * 16; r += kWarps) {
+            float ss = 0.0f;
+            if (r < rows) {
+                const T* xr = X + (r0 + r) * a.xs + kbase;
+                for (int k = lane * 8; k < ntiles * kKT; k += 256) {
+                    float f[8];
+                    V8::unpack(V8::load(xr + k), f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+                }
+                ss = warp_sum(ss);
+            }
+            if (lane == 0) stat[r] = ss;
+        }
+        cluster.sync();  // every rank's partial sums are in its shared memory
+        for (int r = threadIdx.x; r < MT * 16; r += kWarps * 32) {
+            float tot = 0.0f;
+            for (int q = 0; q < SK; ++q) tot += cluster.map_shared_rank(stat, q)[r];
+            inv[r] = rsqrtf(tot / static_cast<float>(a.K) + a.eps);
+        }
+        __syncthreads();
+    }
+    if (ntiles > 0) build(0);
+
+    constexpr int NGROUPS = kWarps / MT;   // warps sharing an m-tile split its 64 columns
+    constexpr int NBW = 8 / NGROUPS;       // n8 blocks per warp
+    const int mt = warp % MT, ng = warp / MT;
+    float acc[NBW][4];
+#pragma unroll
+    for (int j = 0; j < NBW; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+    const int li = lane & 7, lm = lane >> 3;  // ldmatrix: row within a matrix, matrix index
+    for (int t = 0; t < ntiles; ++t) {
+        if (t + 1 < ntiles) prefetch(t + 1);
+        cp_async_wait<kStages - 2>();
+        __syncthreads();  // W tile t landed, h tile t built; the slot of tile t - 1 is free
+        if (t + kStages - 1 < ntiles) issue(t + kStages - 1);
+        cp_async_commit();
+        const T* wt = ring + static_cast<size_t>(t % kStages) * kNT * kKT;
+        const T* ht = hbuf + static_cast<size_t>(t & 1) * MT * 16 * kKT;
+#pragma unroll
+        for (int ks = 0; ks < kKT / 16; ++ks) {
+            uint32_t af[4];
+            {
+                const int r = mt * 16 + (lm & 1) * 8 + li;
+                ldsm_x4(af, ht + r * kKT + swz(r, ks * 2 + (lm >> 1)) * 8);
+            }
+#pragma unroll
+            for (int j = 0; j < NBW; j += 2) {
+                uint32_t bf[4];
+                const int n = (ng * NBW + j) * 8 + (lm >> 1) * 8 + li;
+                ldsm_x4(bf, wt + n * kKT + swz(n, ks * 2 + (lm & 1)) * 8);
+                Mma<T>::run(acc[j], af, bf[0], bf[1]);
+                Mma<T>::run(acc[j + 1], af, bf[2], bf[3]);
+            }
+        }
+        if (t + 1 < ntiles) build(t + 1);
+    }
+    cp_async_wait<0>();
+    __syncthreads();  // the ring is drained: its space takes the partial tile
+
+    // ---- epilogue: partial tile into shared memory, then summed over the cluster
+    {
+        const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+        for (int j = 0; j < NBW; ++j) {
+            const int col = (ng * NBW + j) * 8 + 2 * q;
+            const int row = mt * 16 + g;
+            part[row * kNT + col] = acc[j][0];
+            part[row * kNT + col + 1] = acc[j][1];
+            part[(row + 8) * kNT + col] = acc[j][2];
+            part[(row + 8) * kNT + col + 1] = acc[j][3];
+        }
+    }
+    cluster.sync();
+    T* y = static_cast<T*>(a.y);
+    for (int idx = rank * kWarps * 32 + threadIdx.x; idx < rows * kNT; idx += SK * kWarps * 32) {
+        const int r = idx / kNT, c = idx - r * kNT;
+        float sum = 0.0f;
+        for (int q = 0; q < SK; ++q) sum += cluster.map_shared_rank(part, q)[r * kNT + c];
+        y[(r0 + r) * a.ys + n0 + c] = to_t<T>(sum);
+    }
+    cluster.sync();
+}
+
+template <typename T, int MT, int PRO>
+cudaError_t launch_mt(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
+    auto kernel = linear_kernel<T, MT, PRO>;
+    const size_t smem = smem_bytes(MT);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>(a.N / kNT * p.splits), static_cast<unsigned>((a.B + MT * 16 - 1) / (MT * 16)));
+    return launch_kernel(kernel, grid, dim3(kWarps * 32), smem, s, p.pdl, p.splits, a);
+}
+
+template <typename T, int PRO>
+cudaError_t launch_pro(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
+    switch (p.mt) {
+        case 1: return launch_mt<T, 1, PRO>(a, p, s);
+        case 2: return launch_mt<T, 2, PRO>(a, p, s);
+        case 4: return launch_mt<T, 4, PRO>(a, p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+template <typename T>
+cudaError_t launch_typed(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
+    switch (p.prologue) {
+        case 0: return launch_pro<T, 0>(a, p, s);
+        case 1: return launch_pro<T, 1>(a, p, s);
+        case 2: return launch_pro<T, 2>(a, p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+// ---- the general path (fp32, unaligned layouts, K or N not a multiple of 64): CUDA cores.
+// CTA (column chunk, row): the row's h (rounded to T) in shared memory as fp32, then one
+// warp per output column, lanes striding over K.
+template <typename T, int PRO>
+__global__ void __launch_bounds__(128) linear_simple_kernel(LinArgs a) {
+    extern __shared__ __align__(16) unsigned char smem[];
+    float* h = reinterpret_cast<float*>(smem);
+    __shared__ float red[33];
+    const int64_t b = blockIdx.y;
+    const T* xr = static_cast<const T*>(a.x) + b * a.xs;
+    pdl_enter();
+    if constexpr (PRO == 0) {
+        float ss = 0.0f;
+        for (int64_t k = threadIdx.x; k < a.K; k += blockDim.x) {
+            const float v = to_f32(xr[k]);
+            ss = fmaf(v, v, ss);
+        }
+        ss = block_sum(ss, red);
+        const float iv = rsqrtf(ss / static_cast<float>(a.K) + a.eps);
+        const T* wl = static_cast<const T*>(a.w_ln);
+        for (int64_t k = threadIdx.x; k < a.K; k += blockDim.x)
+            h[k] = round_trip<T>(to_f32(xr[k]) * iv * to_f32(wl[k]));
+    } else {
+        for (int64_t k = threadIdx.x; k < a.K; k += blockDim.x)
+            h[k] = round_trip<T>(glu_act<PRO - 1>(to_f32(xr[k])) * to_f32(xr[k + a.K]));
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const T* W = static_cast<const T*>(a.W);
+    for (int64_t n = blockIdx.x * 128 + warp; n < a.N && n < (blockIdx.x + 1) * 128; n += 4) {
+        float acc = 0.0f;
+        for (int64_t k = lane; k < a.K; k += 32) acc = fmaf(h[k], to_f32(W[n * a.K + k]), acc);
+        acc = warp_sum(acc);
+        if (lane == 0) static_cast<T*>(a.y)[b * a.ys + n] = from_f32<T>(acc);
+    }
+}
+
+template <typename T, int PRO>
+cudaError_t launch_simple(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
+    auto kernel = linear_simple_kernel<T, PRO>;
+    const size_t smem = static_cast<size_t>(a.K) * 4;
+    if (smem > 48 * 1024) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    const dim3 grid(static_cast<unsigned>((a.N + 127) / 128), static_cast<unsigned>(a.B));
+    return launch_kernel(kernel, grid, dim3(128), smem, s, p.pdl, 1, a);
+}
+
+template <typename T>
+cudaError_t launch_simple_typed(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
+    switch (p.prologue) {
+        case 0: return launch_simple<T, 0>(a, p, s);
+        case 1: return launch_simple<T, 1>(a, p, s);
+        case 2: return launch_simple<T, 2>(a, p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace lin
+
+size_t linear_smem(int mt) { return lin::smem_bytes(mt); }
+
+cudaError_t launch_linear(const LinArgs& a, const LinPlan& p, int dtype, cudaStream_t s) {
+    if (!p.tensor_cores) {
+        switch (dtype) {
+            case DT_F32: return lin::launch_simple_typed<float>(a, p, s);
+            case DT_F16: return lin::launch_simple_typed<__half>(a, p, s);
+            case DT_BF16: return lin::launch_simple_typed<__nv_bfloat16>(a, p, s);
+            default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (dtype) {
+        case DT_F16: return lin::launch_typed<__half>(a, p, s);
+        case DT_BF16: return lin::launch_typed<__nv_bfloat16>(a, p, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace sra

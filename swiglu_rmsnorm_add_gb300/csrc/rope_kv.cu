@@ -170,8 +170,8 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
                 load_pair_params<P, IL>(kind == 0 ? a.qg : a.kg, i0, h, glo, ghi);
 #pragma unroll
                 for (int j = 0; j < P; ++j) {
-                    lo[j] = round_to<T>(uclip1(lo[j], alo[j], glo[j], a.clip_lo, a.clip_hi));
-                    hi[j] = round_to<T>(uclip1(hi[j], ahi[j], ghi[j], a.clip_lo, a.clip_hi));
+                    lo[j] = round_trip<T>(uclip1(lo[j], alo[j], glo[j], a.clip_lo, a.clip_hi));
+                    hi[j] = round_trip<T>(uclip1(hi[j], ahi[j], ghi[j], a.clip_lo, a.clip_hi));
                 }
             }
             float c[P], s[P];

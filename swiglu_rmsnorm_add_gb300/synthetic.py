@@ -159,3 +159,13 @@ def attention_inputs(B: int, lens, n_head: int, n_kv_head: int, head_dim: int, b
 
 ATTN_B = (1, 32, 64)        # decode batch sizes
 ATTN_CTX = 1024             # context length of the decode-attention micro-benchmark
+
+
+def linear_weight(N: int, K: int, dtype: torch.dtype, seed: int, stream: int = 51) -> torch.Tensor:
+    """A projection weight [N, K] (nn.Linear's layout) ~ N(0, 0.02), the usual initialisation scale."""
+    return normal((N, K), 0.0, 0.02, dtype, seed, stream)
+
+
+QWEN25_QKV = dict(K=1536, N=2048)     # ln1 -> qkv_proj: hidden 1536 -> (12 + 2 + 2) * 128
+QWEN25_DOWN = dict(I=8960, N=1536)    # silu(gate) * up -> down_proj
+LINEAR_B = (1, 16, 64)                # decode batch sizes

@@ -36,7 +36,8 @@ def declared_functions():
 def test_header_declares_the_api():
     names = declared_functions()
     for n in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_rope_kv_store_ex", "sra_glu",
-              "sra_swiglu", "sra_uclip", "sra_paged_decode_attention", "sra_rope_kv_store_qk_uclip"):
+              "sra_swiglu", "sra_uclip", "sra_paged_decode_attention", "sra_rope_kv_store_qk_uclip",
+              "sra_rmsnorm_linear", "sra_glu_linear"):
         assert n in names
 
 
@@ -191,6 +192,29 @@ def test_paged_decode_attention_validation(L):
     assert call(o=C + 1024) == ALIAS             # out inside the cache
     assert call(o=TB) == ALIAS
     assert call(B=0) == OK
+
+
+def test_linear_validation(L):
+    X, WL, W, Y = (P + i * 0x1000000 for i in range(4))
+    f = L.sra_rmsnorm_linear
+    assert f(X, WL, W, Y, 4, 64, 64, 64, 64, 1e-6, 7, None) == DTYPE
+    assert f(X, WL, W, Y, -1, 64, 64, 64, 64, 1e-6, BF16, None) == SHAPE
+    assert f(X, WL, W, Y, 4, 0, 64, 64, 64, 1e-6, BF16, None) == SHAPE
+    assert f(X, WL, W, Y, 4, 64, 0, 64, 64, 1e-6, BF16, None) == SHAPE
+    assert f(X, WL, W, Y, 4, 64, 64, 63, 64, 1e-6, BF16, None) == STRIDE
+    assert f(X, WL, W, Y, 4, 64, 64, 64, 63, 1e-6, BF16, None) == STRIDE
+    assert f(X, WL, W, Y, 4, 64, 64, 64, 64, -1.0, BF16, None) == ARG
+    assert f(X, None, W, Y, 4, 64, 64, 64, 64, 1e-6, BF16, None) == NULL
+    assert f(X, WL, None, Y, 4, 64, 64, 64, 64, 1e-6, BF16, None) == NULL
+    assert f(X, WL, W, X + 64, 4, 64, 64, 64, 64, 1e-6, BF16, None) == ALIAS
+    assert f(X, WL, W, W + 64, 4, 64, 64, 64, 64, 1e-6, BF16, None) == ALIAS
+    assert f(X, WL, W, Y, 0, 64, 64, 64, 64, 1e-6, BF16, None) == OK
+    g = L.sra_glu_linear
+    assert g(X, W, Y, 4, 64, 64, 128, 64, 2, BF16, None) == ARG
+    assert g(X, W, Y, 4, 64, 64, 127, 64, 0, BF16, None) == STRIDE
+    assert g(X, W, X + 200, 4, 64, 64, 128, 64, 0, BF16, None) == ALIAS
+    assert g(None, W, Y, 4, 64, 64, 128, 64, 0, BF16, None) == NULL
+    assert g(X, W, Y, 0, 64, 64, 128, 64, 1, BF16, None) == OK
 
 
 def test_uclip_validation(L):

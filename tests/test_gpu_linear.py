@@ -1,0 +1,122 @@
+"""GPU parity: RMSNorm / GLU fused as the prologue of the projection they feed.
+
+m.lsln.cn 21-operator article section 2.2 (ln1 fused into qkv_proj); the same
+fusion of the MLP's activation into its down projection. Workloads: the
+Qwen2.5-1.5B projections at decode batch sizes 1, 16 and 64: ln1 + qkv_proj
+(K = 1536, N = 2048) and silu(gate) * up + down_proj (I = 8960, N = 1536);
+x ~ N(0, 1), RMSNorm weight ~ N(1, 0.1), W ~ N(0, 0.02).
+
+Tolerance. The kernels accumulate in fp32 and round the normed (or activated)
+rows to the dtype before the product, as the oracle does; an h element whose
+fp32 value lands on the other side of a rounding midpoint than the oracle's
+moves y by one ulp of h times |W_nk|, and the fp32 sums add about
+sqrt(K) * 2^-24 of S[b, n] = sum_k |h[b, k]| |W[n, k]|. The bound: within 1 ulp
+of the oracle (bf16 / fp16), or within 1e-5 * S + 4u * max_k |h_k W_nk| (two
+such h elements, u the dtype's unit roundoff); fp32: 1e-5 relative + 1e-6 * S.
+"""
+import pytest
+import torch
+
+import oracle
+import swiglu_rmsnorm_add_gb300 as sra
+from swiglu_rmsnorm_add_gb300 import synthetic as syn
+from tests.parity import ulp_distance
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+UNIT = {torch.bfloat16: 2.0 ** -8, torch.float16: 2.0 ** -11, torch.float32: 2.0 ** -24}
+
+
+def assert_linear_close(got, want, h, W, what):
+    got, want = got.cpu(), want.cpu()
+    Ha, Wa = h.double().abs(), W.double().abs()
+    S = Ha @ Wa.T
+    M = (Ha[:, None, :] * Wa[None, :, :]).amax(-1) if h.shape[1] * W.shape[0] * h.shape[0] <= 2 ** 26 else S
+    # two h elements on the other side of a rounding midpoint: 2 * 2u * max_k |h_k W_nk|
+    atol = 1e-5 * S + 4 * UNIT[want.dtype] * M
+    err = (got.double() - want.double()).abs()
+    if want.dtype == torch.float32:
+        bad = err > 1e-5 * want.double().abs() + 1e-6 * S
+    else:
+        bad = (ulp_distance(got, want) > 1) & (err > atol)
+    assert not bool(bad.any()), f"{what}: {int(bad.sum())} of {bad.numel()} outputs off (max err {float(err.max()):.3g})"
+
+
+def norm_case(B, K, N, dtype, seed, rows=None):
+    x = syn.normal((B, K), 0, 1, dtype, seed, 1)
+    w = syn.normal((K,), 1, 0.1, dtype, seed, 2)
+    W = syn.linear_weight(N, K, dtype, seed)
+    got = sra.rmsnorm_linear(x.to(DEV), w.to(DEV), W.to(DEV)).cpu()
+    sel = torch.arange(B) if rows is None else rows
+    h = torch.empty(len(sel), K, dtype=dtype)
+    oracle.rmsnorm(x[sel].contiguous(), w, h, 1e-6)
+    want = torch.empty(len(sel), N, dtype=dtype)
+    oracle.linear(h, W, want)
+    return got[sel], want, h, W
+
+
+def glu_case(B, I, N, dtype, seed, act="silu", rows=None):
+    gu = syn.normal((B, 2 * I), 0, 1, dtype, seed, 3)
+    W = syn.linear_weight(N, I, dtype, seed)
+    got = sra.glu_linear(gu.to(DEV), W.to(DEV), act=act).cpu()
+    sel = torch.arange(B) if rows is None else rows
+    h = torch.empty(len(sel), I, dtype=dtype)
+    oracle.glu(gu[sel].contiguous(), h, act)
+    want = torch.empty(len(sel), N, dtype=dtype)
+    oracle.linear(h, W, want)
+    return got[sel], want, h, W
+
+
+@pytest.mark.parametrize("B", syn.LINEAR_B)
+def test_config_qwen25_ln1_qkv(B):
+    got, want, h, W = norm_case(B, syn.QWEN25_QKV["K"], syn.QWEN25_QKV["N"], torch.bfloat16, 1030)
+    assert_linear_close(got, want, h, W, f"ln1+qkv B={B}")
+
+
+@pytest.mark.parametrize("B", syn.LINEAR_B)
+def test_config_qwen25_swiglu_down(B):
+    rows = None if B <= 16 else torch.arange(0, B, 7)
+    got, want, h, W = glu_case(B, syn.QWEN25_DOWN["I"], syn.QWEN25_DOWN["N"], torch.bfloat16, 1031, rows=rows)
+    assert_linear_close(got, want, h, W, f"swiglu+down B={B}")
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("B", [1, 5, 16, 17, 33, 64, 100])
+@pytest.mark.parametrize("K,N", [(64, 64), (640, 192), (128, 1024), (100, 40), (1536, 2048)])
+def test_norm_shapes_dtypes(dtype, B, K, N):
+    got, want, h, W = norm_case(B, K, N, dtype, 1032 + K + B)
+    assert_linear_close(got, want, h, W, f"norm {dtype} B={B} K={K} N={N}")
+
+
+@pytest.mark.parametrize("act", ["silu", "relu"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("B,I,N", [(1, 64, 64), (7, 960, 128), (64, 512, 256), (3, 72, 40)])
+def test_glu_shapes_dtypes(act, dtype, B, I, N):
+    got, want, h, W = glu_case(B, I, N, dtype, 1033 + I + B, act)
+    assert_linear_close(got, want, h, W, f"{act} {dtype} B={B} I={I} N={N}")
+
+
+def test_strided_rows_and_outputs():
+    """x rows padded (row stride K + 64), y written into a wider buffer: guard columns untouched."""
+    B, K, N = 20, 512, 256
+    base = syn.normal((B, K + 64), 0, 1, torch.bfloat16, 1034, 1)
+    x = base[:, :K]
+    w = syn.normal((K,), 1, 0.1, torch.bfloat16, 1034, 2)
+    W = syn.linear_weight(N, K, torch.bfloat16, 1034)
+    ybuf = torch.full((B, N + 8), 3.0, dtype=torch.bfloat16, device=DEV)
+    sra.rmsnorm_linear(base.to(DEV)[:, :K], w.to(DEV), W.to(DEV), ybuf[:, :N])
+    h = torch.empty(B, K, dtype=torch.bfloat16)
+    oracle.rmsnorm(x.contiguous(), w, h, 1e-6)
+    want = torch.empty(B, N, dtype=torch.bfloat16)
+    oracle.linear(h, W, want)
+    assert_linear_close(ybuf[:, :N], want, h, W, "strided")
+    assert bool((ybuf[:, N:].cpu() == 3.0).all())
+
+
+def test_llama3_8b_down_sampled():
+    """The Llama-3-8B down projection (I = 14336, N = 4096) at batch 64, sampled rows."""
+    rows = torch.tensor([0, 13, 40, 63])
+    got, want, h, W = glu_case(64, 14336, 4096, torch.bfloat16, 1035, rows=rows)
+    assert_linear_close(got, want, h, W, "llama3 down")
