@@ -507,7 +507,8 @@ def cpu_sample_run(target_seconds, threads=None, fraction=None):
 def order_entries(entries):
     """Step order: the largest streams first (SwiGLU T=4096, the dominant kernel, opens the step
     right after the L2 clean-up), then GLU, add_rmsnorm, RoPE, the RMSNorm sweep, the chains."""
-    rank = {"swiglu": 0, "reglu": 0, "add_rmsnorm": 1, "rope_kv_store": 2, "rmsnorm": 3, "chain": 4}
+    rank = {"swiglu": 0, "reglu": 0, "add_rmsnorm": 1, "rope_kv_store": 2, "rmsnorm": 3, "chain": 4,
+            "uclip": 5, "decode_attention": 6, "linear": 7}
     return sorted(entries, key=lambda e: (rank[e.op], -e.bytes, e.op != "swiglu", e.name))
 
 
@@ -529,7 +530,10 @@ def run_gpu(args):
     pdl = not args.no_pdl
     sra.set_pdl(pdl)
 
-    entries = order_entries(build_entries(dev, sh, only))
+    entries = build_entries(dev, sh, only)
+    if only:  # a companion shape named on the command line is timed as a step entry of its own
+        entries += build_entries(dev, sh, only, companions=True)
+    entries = order_entries(entries)
     if not args.no_chain and (not only or any(o.startswith("chain") for o in only)):
         for B in (1, 64):
             entries.append(ChainEntry(B, dev, pdl))
