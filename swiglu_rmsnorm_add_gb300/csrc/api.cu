@@ -817,11 +817,15 @@ static int linear_common(const void* x, const void* w_ln, const void* W, void* y
     plan.mt = B <= 16 ? 1 : (B <= 32 ? 2 : 4);
     plan.tensor_cores = dtype != DT_F32 && K % 64 == 0 && N % 64 == 0 && aligned16(x) && aligned16(W) &&
                         xs % 8 == 0 && (prologue != 0 || aligned16(w_ln));
+    plan.narrow = false;
     plan.splits = 1;
-    if (plan.tensor_cores) {
-        // about one CTA per SM: 64-column slices x row blocks x K splits (a cluster)
-        // two CTAs per SM fit (about 80 KB each); aim for one wave of 1-2 CTAs per SM with at
-        // least two W tiles per CTA
+    // decode batches: 16-column CTAs over all of K, no cluster, when the B rows of h for all of
+    // K fit in shared memory beside the W rings
+    plan.narrow = plan.tensor_cores && B <= 16 &&
+                  static_cast<int64_t>(linear16_smem(static_cast<int>(B), K)) <= std::min<int64_t>(limit, 200 * 1024);
+    if (plan.tensor_cores && !plan.narrow) {
+        // 64-column slices x row blocks x K splits (a cluster); two CTAs per SM fit (about 80 KB
+        // each): aim for one wave of 1-2 CTAs per SM with at least four W tiles per CTA
         const int64_t slices = (N / 64) * ((B + plan.mt * 16 - 1) / (plan.mt * 16));
         const int64_t KT = K / 64;
         while (plan.splits < 8 && slices * plan.splits * 2 <= 2 * static_cast<int64_t>(sms) &&

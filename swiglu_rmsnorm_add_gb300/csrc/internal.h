@@ -164,6 +164,7 @@ struct LinArgs {
 struct LinPlan {
     int prologue;       // 0 RMSNorm, 1 SwiGLU, 2 ReGLU
     bool tensor_cores;  // bf16 / fp16, K and N multiples of 64, 16-byte aligned layouts
+    bool narrow;        // B <= 16: CTAs of 16 columns over all of K, no cluster
     int mt;             // 16-row m-tiles per CTA (1, 2 or 4)
     int splits;         // CTAs per cluster along K
     bool pdl;
@@ -171,6 +172,7 @@ struct LinPlan {
 
 cudaError_t launch_linear(const LinArgs& a, const LinPlan& p, int dtype, cudaStream_t s);
 size_t linear_smem(int mt);
+size_t linear16_smem(int rows, int64_t K);
 
 // ------------------------------------------------------------------- UClip
 struct UclipArgs {

@@ -275,6 +275,151 @@ __global__ void __launch_bounds__(kWarps * 32) linear_kernel(LinArgs a) {
     cluster.sync();
 }
 
+// ---- decode batches: a CTA owns 16 columns of y over the whole of K; its eight warps
+// split K between them (each streaming its own W tiles through a private cp.async ring)
+// and meet only at the end, in shared memory: no cluster, no exchange. h for all of K
+// is built once, up front, while the first W tiles are in flight: the RMSNorm
+// normalises the full rows itself (B x K values), the GLU activates them. Only the B
+// real rows are stored; the A fragments of the padding rows read one zero row.
+constexpr int kNW16 = 8;       // warps
+constexpr int kStages16 = 6;   // W tiles in flight per warp
+constexpr int kTile16 = 16 * kKT;  // elements of a W tile (16 columns x 64 of K)
+
+__host__ __device__ inline size_t ring16_bytes() {
+    const size_t ring = static_cast<size_t>(kNW16) * kStages16 * kTile16 * 2;
+    const size_t part = static_cast<size_t>(kNW16) * 16 * 16 * 4;
+    return ring > part ? ring : part;
+}
+__host__ __device__ inline size_t smem16_bytes(int rows, int64_t K) {
+    return ring16_bytes() + static_cast<size_t>(rows + 1) * K * 2 + 64 * 4;
+}
+
+template <typename T, int PRO>
+__global__ void __launch_bounds__(kNW16 * 32) linear16_kernel(LinArgs a) {
+    using V8 = Vec<T, 8>;
+    using R8 = typename V8::Raw;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 16;
+    const int rows = static_cast<int>(a.B < 16 ? a.B : 16);
+    const int KT = static_cast<int>(a.K / kKT);
+    T* ring = reinterpret_cast<T*>(smem) + static_cast<size_t>(warp) * kStages16 * kTile16;
+    float* part = reinterpret_cast<float*>(smem);  // [warps][16][16], after the rings drain
+    T* hsm = reinterpret_cast<T*>(smem + ring16_bytes());  // [rows][K], then one zero row
+    T* zrow = hsm + static_cast<int64_t>(rows) * a.K;
+    float* inv = reinterpret_cast<float*>(smem + ring16_bytes() + static_cast<size_t>(rows + 1) * a.K * 2);
+    const T* W = static_cast<const T*>(a.W);
+    const T* X = static_cast<const T*>(a.x);
+    // this warp's tiles: t = warp, warp + 8, ...; j-th of them into ring slot j % stages
+    const int mine = KT > warp ? (KT - warp + kNW16 - 1) / kNW16 : 0;
+    auto issue = [&](int j) {
+        const int t = warp + j * kNW16;
+        T* dst = ring + static_cast<size_t>(j % kStages16) * kTile16;
+        const T* src = W + n0 * a.K + static_cast<int64_t>(t) * kKT;
+#pragma unroll
+        for (int c = lane; c < 16 * 8; c += 32) {
+            const int r = c >> 3, ch = c & 7;
+            cp_async16(dst + r * kKT + swz(r, ch) * 8, src + static_cast<int64_t>(r) * a.K + ch * 8);
+        }
+    };
+    pdl_enter();
+    for (int j = 0; j < kStages16 - 1; ++j) {
+        if (j < mine) issue(j);
+        cp_async_commit();
+    }
+
+    const int cpr = static_cast<int>(a.K / 8);
+    for (int c = threadIdx.x; c < cpr; c += kNW16 * 32) reinterpret_cast<uint4*>(zrow)[c] = make_uint4(0, 0, 0, 0);
+    if constexpr (PRO == 0) {
+        // full-row sums of squares: a warp per row
+        for (int r = warp; r < rows; r += kNW16) {
+            const T* xr = X + r * a.xs;
+            float ss = 0.0f;
+            for (int64_t k = lane * 8; k < a.K; k += 256) {
+                float f[8];
+                V8::unpack(V8::load(xr + k), f);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+            }
+            ss = warp_sum(ss);
+            if (lane == 0) inv[r] = rsqrtf(ss / static_cast<float>(a.K) + a.eps);
+        }
+        __syncthreads();
+    }
+    for (int c = threadIdx.x; c < rows * cpr; c += kNW16 * 32) {
+        const int r = c / cpr, ch = c - r * cpr;
+        const T* xr = X + r * a.xs + ch * 8;
+        float f[8], g[8];
+        V8::unpack(V8::load(xr), f);
+        if constexpr (PRO == 0) {
+            V8::unpack(V8::load(static_cast<const T*>(a.w_ln) + ch * 8), g);
+            const float iv = inv[r];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = f[e] * iv * g[e];
+        } else {
+            V8::unpack(V8::load(xr + a.K), g);
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = glu_act<PRO - 1>(f[e]) * g[e];
+        }
+        *reinterpret_cast<R8*>(hsm + static_cast<int64_t>(r) * a.K + swz(r, ch) * 8) = V8::pack(f);
+    }
+    __syncthreads();
+
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    const int li = lane & 7, lm = lane >> 3;
+    const int ar = (lm & 1) * 8 + li;  // this lane's A row in ldmatrix
+    const T* arow = ar < rows ? hsm + static_cast<int64_t>(ar) * a.K : zrow;
+    for (int j = 0; j < mine; ++j) {
+        const int t = warp + j * kNW16;
+        cp_async_wait<kStages16 - 2>();
+        __syncwarp();
+        if (j + kStages16 - 1 < mine) issue(j + kStages16 - 1);
+        cp_async_commit();
+        const T* wt = ring + static_cast<size_t>(j % kStages16) * kTile16;
+#pragma unroll
+        for (int ks = 0; ks < kKT / 16; ++ks) {
+            uint32_t af[4], bf[4];
+            const int ach = (t * kKT + ks * 16) / 8 + (lm >> 1);
+            ldsm_x4(af, arow + (ar < rows ? swz(ar, ach) : ach) * 8);
+            const int n = (lm >> 1) * 8 + li;
+            ldsm_x4(bf, wt + n * kKT + swz(n, ks * 2 + (lm & 1)) * 8);
+            Mma<T>::run(acc[0], af, bf[0], bf[1]);
+            Mma<T>::run(acc[1], af, bf[2], bf[3]);
+        }
+    }
+    cp_async_wait<0>();
+    __syncthreads();  // every warp is done with its ring: the space takes the partial tiles
+    {
+        const int g = lane >> 2, q = lane & 3;
+        float* pw = part + warp * 256;
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            pw[g * 16 + j * 8 + 2 * q] = acc[j][0];
+            pw[g * 16 + j * 8 + 2 * q + 1] = acc[j][1];
+            pw[(g + 8) * 16 + j * 8 + 2 * q] = acc[j][2];
+            pw[(g + 8) * 16 + j * 8 + 2 * q + 1] = acc[j][3];
+        }
+    }
+    __syncthreads();
+    T* y = static_cast<T*>(a.y);
+    for (int idx = threadIdx.x; idx < rows * 16; idx += kNW16 * 32) {
+        float sum = 0.0f;
+#pragma unroll
+        for (int w = 0; w < kNW16; ++w) sum += part[w * 256 + idx];
+        y[(idx >> 4) * a.ys + n0 + (idx & 15)] = to_t<T>(sum);
+    }
+}
+
+template <typename T, int PRO>
+cudaError_t launch16(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
+    auto kernel = linear16_kernel<T, PRO>;
+    const size_t smem = smem16_bytes(static_cast<int>(a.B < 16 ? a.B : 16), a.K);
+    const cudaError_t e =
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    return launch_kernel(kernel, dim3(static_cast<unsigned>(a.N / 16)), dim3(kNW16 * 32), smem, s, p.pdl, 1, a);
+}
+
 template <typename T, int MT, int PRO>
 cudaError_t launch_mt(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
     auto kernel = linear_kernel<T, MT, PRO>;
@@ -297,6 +442,14 @@ cudaError_t launch_pro(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
 
 template <typename T>
 cudaError_t launch_typed(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
+    if (p.narrow) {
+        switch (p.prologue) {
+            case 0: return launch16<T, 0>(a, p, s);
+            case 1: return launch16<T, 1>(a, p, s);
+            case 2: return launch16<T, 2>(a, p, s);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (p.prologue) {
         case 0: return launch_pro<T, 0>(a, p, s);
         case 1: return launch_pro<T, 1>(a, p, s);
@@ -368,6 +521,7 @@ cudaError_t launch_simple_typed(const LinArgs& a, const LinPlan& p, cudaStream_t
 }  // namespace lin
 
 size_t linear_smem(int mt) { return lin::smem_bytes(mt); }
+size_t linear16_smem(int rows, int64_t K) { return lin::smem16_bytes(rows, K); }
 
 cudaError_t launch_linear(const LinArgs& a, const LinPlan& p, int dtype, cudaStream_t s) {
     if (!p.tensor_cores) {
