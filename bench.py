@@ -503,6 +503,59 @@ def cpu_sample_run(target_seconds, threads=None, fraction=None):
             "seconds": dt, "bytes": b, "fraction": fraction}
 
 
+def cpu_rows_run():
+    """The oracle timed beside each widened row (one thread, a small sample of the row's
+    companion workload); returns {companion name prefix: {"gbs", "bytes", "seconds", "sample"}}."""
+    import torch
+
+    import oracle
+    from swiglu_rmsnorm_add_gb300 import synthetic as syn
+
+    tables = syn.rope_tables(32768, 128, 1e6)
+    out = {}
+
+    def timed(name, nbytes, sample, fn):
+        n, t0 = 0, time.perf_counter()
+        while True:  # repeat the sample for at least a quarter of a second
+            fn()
+            n += 1
+            dt = time.perf_counter() - t0
+            if dt >= 0.25:
+                break
+        out[name] = {"gbs": round(n * nbytes / dt / 1e9, 4), "bytes": n * nbytes, "seconds": round(dt, 3),
+                     "sample": f"{sample}, {n} runs"}
+
+    T = 256
+    inp = syn.rope_inputs(T, 1002, tables=tables, num_blocks=64)
+    timed("rope_kv_store_interleaved", 8720 * T, f"T={T}", lambda: oracle.rope_kv_store(**inp, style="interleaved"))
+    inp = syn.rope_inputs(T, 1002, tables=tables, num_blocks=64)
+    ps = tuple(syn.uclip_params(128, True, True, 1002 + i)[i % 2] for i in range(4))
+    timed("rope_kv_store_qk_uclip", 8720 * T, f"T={T}",
+          lambda: oracle.qk_uclip_rope_kv_store(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], inp["pos"],
+                                                inp["slot_mapping"], inp["kv_cache"], *ps))
+    x = syn.normal((512, 1536), 0.0, 1.0, torch.bfloat16, 1005, 1)
+    a, g = syn.uclip_params(1536, False, True, 1005)
+    y = torch.empty_like(x)
+    timed("dyht", 2 * 512 * 1536 * 2, "512 x 1536", lambda: oracle.dyht(x, a, g, y))
+    B, ctx = 4, 1024
+    q, cache, table, seq = syn.attention_inputs(B, ctx, 12, 2, 128, 16, 4096, torch.bfloat16, 1012)
+    o = torch.empty_like(q)
+    timed("decode_attention", 2 * B * ctx * 2 * 128 * 2, f"B={B} x {ctx} tokens",
+          lambda: oracle.paged_decode_attention(q, cache, table, seq, o))
+    K, N = syn.QWEN25_QKV["K"], syn.QWEN25_QKV["N"]
+    x = syn.normal((1, K), 0.0, 1.0, torch.bfloat16, 1030, 1)
+    w = syn.normal((K,), 1.0, 0.1, torch.bfloat16, 1030, 2)
+    W = syn.linear_weight(N, K, torch.bfloat16, 1030)
+    y = torch.empty(1, N, dtype=torch.bfloat16)
+    timed("rmsnorm_linear", N * K * 2, "B=1", lambda: oracle.rmsnorm_linear(x, w, W, y, syn.EPS))
+    I, N = syn.QWEN25_DOWN["I"], syn.QWEN25_DOWN["N"]
+    gu = syn.normal((1, 2 * I), 0.0, 1.0, torch.bfloat16, 1031, 3)
+    W = syn.linear_weight(N, I, torch.bfloat16, 1031)
+    y = torch.empty(1, N, dtype=torch.bfloat16)
+    timed("swiglu_linear", N * I * 2, "B=1", lambda: oracle.glu_linear(gu, W, y, "silu"))
+    return out
+
+
 # --------------------------------------------------------------------------- main (GPU)
 def order_entries(entries):
     """Step order: the largest streams first (SwiGLU T=4096, the dominant kernel, opens the step
@@ -772,6 +825,15 @@ def run_gpu(args):
     if rank == 0 and world == 1 and not args.no_cpu and not only:
         cpu = cpu_sample_run(args.cpu_seconds)
         cpu = {k: (round(v, 4) if isinstance(v, float) else v) for k, v in cpu.items()}
+        if companions:
+            # the oracle beside each widened row: one thread on a small sample of the row's workload
+            rows_cpu = cpu_rows_run()
+            for c in companions:
+                for prefix, r in rows_cpu.items():
+                    if c["name"].startswith(prefix + ":"):
+                        c["cpu_oracle_gbs"] = r["gbs"]
+                        c["cpu_oracle_sample"] = f"{r['sample']}, 1 thread, {r['seconds']} s"
+            cpu["rows"] = rows_cpu
 
     if rank == 0:
         line = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
