@@ -375,6 +375,27 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
     const int fg = lane >> 2, ft = lane & 3;  // fragment row group and thread-in-group
     T* ring = reinterpret_cast<T*>(smem) + static_cast<size_t>(warp) * kMmaStages * 2 * TE;
 
+    {
+        // Before the dependency wait: warm the K and V rows of this warp's first tile. The
+        // split is a static slice of the table's capacity, so the tile's tokens are known;
+        // their block ids are read relaxed (the previous kernel may still be writing them) and
+        // only steer prefetches. Everything used below is read again after the wait.
+        const int64_t cap0 = a.max_blocks * BS;
+        const int64_t per0 = ((cap0 + S - 1) / S + kMmaTile - 1) / kMmaTile * kMmaTile;
+        const int64_t tok = rank * per0 + warp * kMmaTile + (lane & (kMmaTile - 1));
+        if (tok < cap0 && tok < (rank + 1) * per0) {
+            int blk;
+            asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];"
+                         : "=r"(blk)
+                         : "l"(a.table + b * a.max_blocks + tok / BS));
+            if (blk >= 0 && blk < a.num_blocks) {
+                const T* row = static_cast<const T*>(a.cache) +
+                               ((static_cast<int64_t>(blk) * BS + tok % BS) * a.n_kv + kvh) * HD +
+                               (lane >= kMmaTile ? a.num_blocks * BS * static_cast<int64_t>(a.n_kv) * HD : 0);
+                prefetch_lines(row, HD * 2, 0, 1);
+            }
+        }
+    }
     pdl_enter();
     int64_t len = a.seq_lens[b];
     const int64_t cap = a.max_blocks * BS;

@@ -94,6 +94,18 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
         prefetch_l2(static_cast<const T*>(a.k) + t * a.ks, static_cast<int64_t>(a.n_kv) * a.head_dim * es);
         prefetch_l2(static_cast<const T*>(a.v) + t * a.vs, static_cast<int64_t>(a.n_kv) * a.head_dim * es);
     }
+    if (threadIdx.x == blockDim.x - 1 && blockIdx.x < a.T) {
+        // Warm the first token's cos / sin rows. The position is read before the dependency
+        // wait (a relaxed read: the previous kernel may still be writing it), so it only
+        // steers a prefetch; the position used below is read again after the wait.
+        int64_t p;
+        asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(p) : "l"(a.pos + blockIdx.x));
+        if (p >= 0 && p < a.max_pos) {
+            const int64_t half = a.head_dim >> 1;
+            prefetch_l2(a.cos + p * half, half * 4);
+            prefetch_l2(a.sin + p * half, half * 4);
+        }
+    }
     pdl_enter();
 
     const int h = a.head_dim >> 1;
