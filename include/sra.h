@@ -277,6 +277,40 @@ SRA_API int sra_paged_decode_attention(const void* q, const void* kv_cache, cons
                                        int32_t* err_count, int dtype, void* stream);
 
 /*
+ * sra_paged_decode_attention_ws — sra_paged_decode_attention with a caller-owned
+ * workspace. When few (request, kv head) pairs meet a long context (the case a
+ * cluster of up to 16 splits cannot spread over the GPU, e.g. one request with
+ * 32 k cached tokens), the tensor-core kernel splits every pair over many
+ * independent CTAs ([lsln] sec. 3: split the reduction, then merge the parts by
+ * their max and sum of exponentials); each writes its partial result into the
+ * workspace and the last to finish merges them. Otherwise the workspace is
+ * unused and the call is sra_paged_decode_attention.
+ * workspace: device memory of at least
+ *   sra_paged_decode_attention_workspace_size(B, n_head, n_kv_head, head_dim,
+ *                                             max_blocks_per_seq, block_size, dtype)
+ *   bytes, 16-byte aligned, zero-filled by the caller once before its first use;
+ *   every call leaves it ready for the next (its counters back at zero). It must
+ *   not overlap any other argument, and calls that share a workspace must not run
+ *   concurrently (same stream, or ordered by events).
+ * Errors: those of sra_paged_decode_attention; workspace_bytes below the size the
+ * shape needs, a negative size or a misaligned workspace -> SRA_ERR_ARG.
+ */
+SRA_API int sra_paged_decode_attention_ws(const void* q, const void* kv_cache, const int32_t* block_table,
+                                          const int32_t* seq_lens, void* out, int64_t B, int n_head,
+                                          int n_kv_head, int head_dim, int64_t q_tok_stride,
+                                          int64_t out_tok_stride, int64_t num_blocks, int block_size,
+                                          int64_t max_blocks_per_seq, float scale, void* workspace,
+                                          int64_t workspace_bytes, int32_t* err_count, int dtype, void* stream);
+
+/*
+ * Workspace bytes sra_paged_decode_attention_ws needs for this shape on the
+ * current device (0: the shape takes the cluster kernel and needs none); a
+ * negative sra_status for sizes sra_paged_decode_attention would reject.
+ */
+SRA_API int64_t sra_paged_decode_attention_workspace_size(int64_t B, int n_head, int n_kv_head, int head_dim,
+                                                          int64_t max_blocks_per_seq, int block_size, int dtype);
+
+/*
  * sra_rmsnorm_linear — RMSNorm as the prologue of the projection it feeds
  * ([lsln] sec. 2.2: ln1 + qkv_proj fused, the normed rows never stored):
  *

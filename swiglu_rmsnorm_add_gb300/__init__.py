@@ -11,6 +11,7 @@ no CPU or PyTorch fallback: without the built library every call raises.
 from ._binding import (  # noqa: F401
     SRAError,
     add_rmsnorm,
+    decode_attention_workspace,
     dyht,
     force_variant,
     glu,
@@ -31,6 +32,7 @@ from ._binding import (  # noqa: F401
 )
 
 __all__ = ["rmsnorm", "add_rmsnorm", "rope_kv_store", "swiglu", "reglu", "glu", "uclip", "dyht", "paged_decode_attention",
+           "decode_attention_workspace",
            "rmsnorm_linear", "glu_linear", "lib",
            "SRAError",
            "force_variant", "set_pdl", "variant_count", "variant_name", "pick_variant", "status_string"]

@@ -45,6 +45,10 @@ def lib() -> ctypes.CDLL:
                                                                                         f32, i32, vp]
             L.sra_paged_decode_attention.argtypes = [vp, vp, vp, vp, vp, i64, i32, i32, i32, i64, i64, i64, i32,
                                                      i64, f32, vp, i32, vp]
+            L.sra_paged_decode_attention_ws.argtypes = L.sra_paged_decode_attention.argtypes[:15] + [vp, i64, vp,
+                                                                                                    i32, vp]
+            L.sra_paged_decode_attention_workspace_size.argtypes = [i64, i32, i32, i32, i64, i32, i32]
+            L.sra_paged_decode_attention_workspace_size.restype = i64
             L.sra_rmsnorm_linear.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, i32, vp]
             L.sra_glu_linear.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, vp]
             L.sra_glu.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, vp]
@@ -53,7 +57,7 @@ def lib() -> ctypes.CDLL:
                                     vp]
             for fn in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_rope_kv_store_ex", "sra_glu",
                        "sra_swiglu", "sra_uclip", "sra_rope_kv_store_qk_uclip", "sra_paged_decode_attention",
-                       "sra_rmsnorm_linear", "sra_glu_linear"):
+                       "sra_rmsnorm_linear", "sra_glu_linear", "sra_paged_decode_attention_ws"):
                 getattr(L, fn).restype = i32
             L.sra_status_string.argtypes = [i32]
             L.sra_status_string.restype = ctypes.c_char_p
@@ -359,9 +363,21 @@ def dyht(x: torch.Tensor, alpha: torch.Tensor, gamma: torch.Tensor, out: torch.T
     return uclip(x, alpha, gamma, out, -1.0, 1.0, stream)
 
 
+def decode_attention_workspace(B: int, n_head: int, n_kv_head: int, head_dim: int, max_blocks: int,
+                               block_size: int, dtype=torch.bfloat16, device="cuda") -> torch.Tensor | None:
+    """A zero-filled workspace for paged_decode_attention(..., workspace=...), or None when the
+    shape does not use one. Reuse it across calls (the kernel leaves it zeroed)."""
+    n = lib().sra_paged_decode_attention_workspace_size(B, n_head, n_kv_head, head_dim, max_blocks, block_size,
+                                                       DTYPE_CODE[dtype])
+    if n < 0:
+        _check("sra_paged_decode_attention_workspace_size", int(n))
+    return torch.zeros(int(n), dtype=torch.uint8, device=device) if n > 0 else None
+
+
 def paged_decode_attention(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
                            seq_lens: torch.Tensor, out: torch.Tensor | None = None, scale: float | None = None,
-                           err_count: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+                           err_count: torch.Tensor | None = None, stream=None,
+                           workspace: torch.Tensor | None = None) -> torch.Tensor:
     """out[b, h] = softmax(scale * q[b, h] . K) V over request b's cached tokens.
 
     q: [B, n_head, head_dim]; kv_cache: [2, num_blocks, block_size, n_kv_head, head_dim] (the
@@ -391,14 +407,19 @@ def paged_decode_attention(q: torch.Tensor, kv_cache: torch.Tensor, block_table:
         raise ValueError("shape mismatch")
     if scale is None:
         scale = 1.0 / float(hd) ** 0.5
+    args = (q.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(), seq_lens.data_ptr(), out.data_ptr(), B,
+            n_head, n_kv, hd, _tok_stride(q, "q"), _tok_stride(out, "out"), nb, bs, block_table.shape[1],
+            float(scale))
+    err = err_count.data_ptr() if err_count is not None else None
     with torch.cuda.device(q.device):
-        st = lib().sra_paged_decode_attention(q.data_ptr(), kv_cache.data_ptr(), block_table.data_ptr(),
-                                              seq_lens.data_ptr(), out.data_ptr(), B, n_head, n_kv, hd,
-                                              _tok_stride(q, "q"), _tok_stride(out, "out"), nb, bs,
-                                              block_table.shape[1], float(scale),
-                                              err_count.data_ptr() if err_count is not None else None,
-                                              _dtype(q), _stream(q, stream))
-    _check("sra_paged_decode_attention", st)
+        if workspace is None:
+            st = lib().sra_paged_decode_attention(*args, err, _dtype(q), _stream(q, stream))
+        else:
+            _cuda(workspace, "workspace")
+            st = lib().sra_paged_decode_attention_ws(*args, workspace.data_ptr(),
+                                                     workspace.numel() * workspace.element_size(), err,
+                                                     _dtype(q), _stream(q, stream))
+    _check("sra_paged_decode_attention" if workspace is None else "sra_paged_decode_attention_ws", st)
     return out
 
 

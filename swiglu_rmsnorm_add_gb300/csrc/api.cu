@@ -600,6 +600,23 @@ int rope_impl(void* q, const void* k, const void* v, const float* cos, const flo
 }
 
 }  // namespace
+
+// Global splits of a decode-attention call: used when the cluster splits cannot give every SM
+// work (fewer than SMs / 16 (request, kv head) pairs) and the context is long enough for more
+// than 16 splits of at least 512 tokens; one CTA per SM at most.
+int decode_attention_gsplits(int64_t B, int n_kv, int64_t max_blocks, int block_size, int num_sms) {
+    const int64_t groups = B * n_kv;
+    if (groups <= 0 || groups * 16 >= num_sms) return 0;
+    const int64_t gs = std::min<int64_t>({num_sms / groups, max_blocks * block_size / 512, kMaxGsplits});
+    return gs > 16 ? static_cast<int>(gs) : 0;
+}
+
+int64_t decode_attention_ws_bytes(int64_t B, int n_kv, int head_dim, int gsplits) {
+    if (gsplits <= 0) return 0;
+    const int64_t groups = B * n_kv;
+    return (groups * 4 + 255) / 256 * 256 + groups * gsplits * (16 + 8 * static_cast<int64_t>(head_dim)) * 4;
+}
+
 }  // namespace sra
 
 using namespace sra;
@@ -711,11 +728,11 @@ int sra_swiglu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_
 }
 
 // ------------------------------------------------------------------- decode attention
-int sra_paged_decode_attention(const void* q, const void* kv_cache, const int32_t* block_table,
-                               const int32_t* seq_lens, void* out, int64_t B, int n_head, int n_kv_head,
-                               int head_dim, int64_t q_tok_stride, int64_t out_tok_stride, int64_t num_blocks,
-                               int block_size, int64_t max_blocks_per_seq, float scale, int32_t* err_count,
-                               int dtype, void* stream) {
+static int attention_impl(const void* q, const void* kv_cache, const int32_t* block_table, const int32_t* seq_lens,
+                          void* out, int64_t B, int n_head, int n_kv_head, int head_dim, int64_t q_tok_stride,
+                          int64_t out_tok_stride, int64_t num_blocks, int block_size, int64_t max_blocks_per_seq,
+                          float scale, void* workspace, int64_t workspace_bytes, int32_t* err_count, int dtype,
+                          void* stream) {
     if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
     if (B < 0 || n_head <= 0 || n_kv_head <= 0 || n_head % n_kv_head != 0 || n_head / n_kv_head > 8 ||
         (head_dim != 64 && head_dim != 128 && head_dim != 256) ||
@@ -789,7 +806,58 @@ int sra_paged_decode_attention(const void* q, const void* kv_cache, const int32_
     a.group = group;
     a.block_size = block_size;
     a.scale_log2 = scale * 1.4426950408889634f;
+    if (workspace && plan.tensor_cores && forced != 0) {
+        const int gs = decode_attention_gsplits(B, n_kv_head, max_blocks_per_seq, block_size, sms);
+        const int64_t need = decode_attention_ws_bytes(B, n_kv_head, head_dim, gs);
+        if (gs > 0) {
+            if (workspace_bytes < need || !aligned16(workspace)) return SRA_ERR_ARG;
+            const Span sws = span_of(workspace, 1, 0, need, 1);
+            if (overlap(sws, so) || overlap(sws, sc) || overlap(sws, st) || overlap(sws, sl) ||
+                overlap(sws, span_of(q, B, q_tok_stride, w, es)))
+                return SRA_ERR_ALIAS;
+            a.gsplits = gs;
+            a.ws_count = static_cast<int32_t*>(workspace);
+            a.ws_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((B * n_kv_head * 4 + 255) / 256) * 256);
+        }
+    }
     return status_from(launch_decode_attention(a, plan, dtype, static_cast<cudaStream_t>(stream)));
+}
+
+
+int sra_paged_decode_attention(const void* q, const void* kv_cache, const int32_t* block_table,
+                               const int32_t* seq_lens, void* out, int64_t B, int n_head, int n_kv_head,
+                               int head_dim, int64_t q_tok_stride, int64_t out_tok_stride, int64_t num_blocks,
+                               int block_size, int64_t max_blocks_per_seq, float scale, int32_t* err_count,
+                               int dtype, void* stream) {
+    return attention_impl(q, kv_cache, block_table, seq_lens, out, B, n_head, n_kv_head, head_dim, q_tok_stride,
+                          out_tok_stride, num_blocks, block_size, max_blocks_per_seq, scale, nullptr, 0, err_count,
+                          dtype, stream);
+}
+
+int64_t sra_paged_decode_attention_workspace_size(int64_t B, int n_head, int n_kv_head, int head_dim,
+                                                  int64_t max_blocks_per_seq, int block_size, int dtype) {
+    if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
+    if (B < 0 || n_head <= 0 || n_kv_head <= 0 || n_head % n_kv_head != 0 || n_head / n_kv_head > 8 ||
+        (head_dim != 64 && head_dim != 128 && head_dim != 256) ||
+        (block_size != 8 && block_size != 16 && block_size != 32) || max_blocks_per_seq < 0)
+        return SRA_ERR_SHAPE;
+    if (dtype == DT_F32 || head_dim > 128 || B == 0) return 0;
+    int dev = 0;
+    const int sms = current_sm_count(&dev);
+    if (sms <= 0) return SRA_ERR_DEVICE;
+    return decode_attention_ws_bytes(B, n_kv_head, head_dim,
+                                     decode_attention_gsplits(B, n_kv_head, max_blocks_per_seq, block_size, sms));
+}
+
+int sra_paged_decode_attention_ws(const void* q, const void* kv_cache, const int32_t* block_table,
+                                  const int32_t* seq_lens, void* out, int64_t B, int n_head, int n_kv_head,
+                                  int head_dim, int64_t q_tok_stride, int64_t out_tok_stride, int64_t num_blocks,
+                                  int block_size, int64_t max_blocks_per_seq, float scale, void* workspace,
+                                  int64_t workspace_bytes, int32_t* err_count, int dtype, void* stream) {
+    if (workspace_bytes < 0) return SRA_ERR_ARG;
+    return attention_impl(q, kv_cache, block_table, seq_lens, out, B, n_head, n_kv_head, head_dim, q_tok_stride,
+                          out_tok_stride, num_blocks, block_size, max_blocks_per_seq, scale, workspace,
+                          workspace_bytes, err_count, dtype, stream);
 }
 
 // ------------------------------------------------------------------- fused linear

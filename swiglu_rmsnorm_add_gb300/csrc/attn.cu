@@ -357,7 +357,11 @@ __host__ __device__ inline size_t mma_smem(int HD) {
     return mma_ring_bytes(HD) + static_cast<size_t>(kMmaWarps) * kMmaStages * 4;  // + per-slot row masks
 }
 
-template <typename T, int HD>
+// GMERGE: the splits of a (request, kv head) are independent CTAs (a.gsplits of them, more
+// than a cluster holds): each writes its (max, sum, partial output) to the workspace, and the
+// CTA that finishes last (an atomic count per (request, kv head)) merges them and resets the
+// count to zero for the next call.
+template <typename T, int HD, bool GMERGE>
 __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) {
     constexpr int CPR = HD * 2 / 16;      // 16-byte chunks per row
     constexpr int KS = HD / 16;           // k-steps of Q K^T
@@ -365,8 +369,8 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
     constexpr int TE = kMmaTile * HD;     // elements of one K or V tile
     extern __shared__ __align__(16) unsigned char smem[];
     cg::cluster_group cluster = cg::this_cluster();
-    const int S = static_cast<int>(cluster.num_blocks());
-    const int rank = static_cast<int>(cluster.block_rank());
+    const int S = GMERGE ? a.gsplits : static_cast<int>(cluster.num_blocks());
+    const int rank = GMERGE ? static_cast<int>(blockIdx.x % a.gsplits) : static_cast<int>(cluster.block_rank());
     const int64_t grp = blockIdx.x / S;
     const int64_t b = grp / a.n_kv;
     const int kvh = static_cast<int>(grp - b * a.n_kv);
@@ -395,6 +399,11 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
                 prefetch_lines(row, HD * 2, 0, 1);
             }
         }
+        // and this split's whole slice of the block table, so the later tiles' table reads
+        // hit the L2 and each tile costs one DRAM round trip, not two
+        const int64_t s0 = rank * per0, s1 = cap0 < s0 + per0 ? cap0 : s0 + per0;
+        if (warp == kMmaWarps - 1 && s0 < s1)
+            prefetch_lines(a.table + b * a.max_blocks + s0 / BS, ((s1 - 1) / BS - s0 / BS + 1) * 4, lane, 32);
     }
     pdl_enter();
     int64_t len = a.seq_lens[b];
@@ -597,8 +606,80 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
         pacc[idx] = num;
         if (d == 0) pm[gg] = M, pl[gg] = den;
     }
-    cluster.sync();
     T* out = static_cast<T*>(a.out) + b * a.os + static_cast<int64_t>(kvh * G) * HD;
+    if constexpr (GMERGE) {
+        // this split's partial into the workspace: [8 max][8 sum][8 x HD output]
+        float* slot = a.ws_part + (static_cast<int64_t>(grp) * S + rank) * (16 + 8 * HD);
+        __syncthreads();
+        for (int i = threadIdx.x; i < G * HD; i += blockDim.x) slot[16 + i] = pacc[i];
+        if (threadIdx.x < G) slot[threadIdx.x] = pm[threadIdx.x], slot[8 + threadIdx.x] = pl[threadIdx.x];
+        __threadfence();
+        __syncthreads();
+        __shared__ int last;
+        if (threadIdx.x == 0) last = atomicAdd(a.ws_count + grp, 1) == S - 1;
+        __syncthreads();
+        if (!last) return;
+        __threadfence();  // the other splits' partials are visible past their counts
+        const float* parts = a.ws_part + static_cast<int64_t>(grp) * S * (16 + 8 * HD);
+        constexpr int PS = 16 + 8 * HD;  // floats per split's partial
+        constexpr int CH = 16;           // splits one thread sums with its loads all in flight
+        // the splits' maxima and sums into shared memory (over the drained rings), one
+        // 16-byte load per thread and quarter header, all independent
+        float* hm = reinterpret_cast<float*>(smem);        // [S][16]: 8 maxima, 8 sums
+        float* wr = hm + static_cast<size_t>(S) * 16;      // [S][8] merge weights
+        float* den = wr + static_cast<size_t>(S) * 8;      // [8]
+        float* part = den + 8;                             // [nq][G * HD] partial numerators
+        for (int i = threadIdx.x; i < S * 4; i += blockDim.x)
+            reinterpret_cast<float4*>(hm)[i] = __ldcg(reinterpret_cast<const float4*>(parts + (i >> 2) * PS) + (i & 3));
+        __syncthreads();
+        // warp gg: M over the splits, the weights 2^(m_r - M) and the denominator
+        if (warp < G) {
+            const int gg = warp;
+            float M = -INFINITY;
+            for (int r = lane; r < S; r += 32) M = fmaxf(M, hm[r * 16 + gg]);
+            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
+            float d = 0.0f;
+            for (int r = lane; r < S; r += 32) {
+                const float mr = hm[r * 16 + gg];
+                const float w = (M == -INFINITY || mr == -INFINITY) ? 0.0f : exp2f(mr - M);
+                wr[r * 8 + gg] = w;
+                d = fmaf(w, hm[r * 16 + 8 + gg], d);
+            }
+            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(FULL, d, o);
+            if (lane == 0) den[gg] = d;
+        }
+        __syncthreads();
+        // numerators: a task is 4 output columns over a chunk of CH splits, its CH loads
+        // issued together; the chunks' sums meet in shared memory
+        const int nslots = G * HD / 4, nq = (S + CH - 1) / CH;
+        for (int t = threadIdx.x; t < nslots * nq; t += blockDim.x) {
+            const int sl = t % nslots, q = t / nslots, gg = 4 * sl / HD;
+            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+            for (int j = 0; j < CH; ++j) {
+                const int r = q * CH + j;
+                if (r < S) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(parts + r * PS + 16) + sl);
+                    const float w = wr[r * 8 + gg];
+                    acc.x = fmaf(w, v.x, acc.x);
+                    acc.y = fmaf(w, v.y, acc.y);
+                    acc.z = fmaf(w, v.z, acc.z);
+                    acc.w = fmaf(w, v.w, acc.w);
+                }
+            }
+            reinterpret_cast<float4*>(part + static_cast<size_t>(q) * G * HD)[sl] = acc;
+        }
+        __syncthreads();
+        for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
+            const int gg = idx / HD;
+            float num = 0.0f;
+            for (int q = 0; q < nq; ++q) num += part[q * G * HD + idx];
+            out[idx] = from_f32<T>(den[gg] > 0.0f ? num / den[gg] : 0.0f);
+        }
+        if (threadIdx.x == 0) a.ws_count[grp] = 0;  // ready for the next call
+        return;
+    }
+    cluster.sync();
     for (int idx = rank * blockDim.x + threadIdx.x; idx < G * HD; idx += S * blockDim.x) {
         const int gg = idx / HD;
         float M = -INFINITY;
@@ -620,8 +701,16 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
 
 template <typename T, int HD>
 cudaError_t launch_mma(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
-    auto kernel = decode_mma_kernel<T, HD>;
     const size_t smem = mma_smem(HD);
+    if (a.gsplits > 0) {
+        auto kg = decode_mma_kernel<T, HD, true>;
+        const cudaError_t eg =
+            cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (eg != cudaSuccess) return eg;
+        const dim3 grid(static_cast<unsigned>(a.B * a.n_kv * a.gsplits)), block(kMmaWarps * 32);
+        return launch_kernel(kg, grid, block, smem, s, p.pdl, 1, a);
+    }
+    auto kernel = decode_mma_kernel<T, HD, false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int splits = p.splits;

@@ -134,6 +134,11 @@ struct AttnArgs {
     int64_t B, qs, os, num_blocks, max_blocks;
     int n_head, n_kv, group, block_size;
     float scale_log2;          // softmax scale * log2(e)
+    // global split (tensor-core kernel): gsplits > 0 CTAs per (request, kv head), merged
+    // through the workspace by the last one to finish
+    int gsplits = 0;
+    float* ws_part = nullptr;     // [B * n_kv][gsplits][16 + 8 * head_dim]
+    int32_t* ws_count = nullptr;  // [B * n_kv], zero between calls
 };
 
 struct AttnPlan {
@@ -150,6 +155,12 @@ struct AttnPlan {
 cudaError_t launch_decode_attention(const AttnArgs& a, const AttnPlan& p, int dtype, cudaStream_t s);
 size_t decode_attention_smem(int group, int head_dim, int block_size, int stages, int es);
 size_t decode_attention_mma_smem(int head_dim);
+// Global-split plan of a decode-attention call: splits per (request, kv head) (0: none) and the
+// workspace bytes it needs.
+// at most this many global splits: the last CTA's merge buffers fit over its drained rings
+constexpr int kMaxGsplits = 256;
+int decode_attention_gsplits(int64_t B, int n_kv, int64_t max_blocks, int block_size, int num_sms);
+int64_t decode_attention_ws_bytes(int64_t B, int n_kv, int head_dim, int gsplits);
 
 // ------------------------------------------------------------------- fused linear
 struct LinArgs {

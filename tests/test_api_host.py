@@ -37,7 +37,8 @@ def test_header_declares_the_api():
     names = declared_functions()
     for n in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_rope_kv_store_ex", "sra_glu",
               "sra_swiglu", "sra_uclip", "sra_paged_decode_attention", "sra_rope_kv_store_qk_uclip",
-              "sra_rmsnorm_linear", "sra_glu_linear"):
+              "sra_rmsnorm_linear", "sra_glu_linear", "sra_paged_decode_attention_ws",
+              "sra_paged_decode_attention_workspace_size"):
         assert n in names
 
 
@@ -215,6 +216,22 @@ def test_linear_validation(L):
     assert g(X, W, X + 200, 4, 64, 64, 128, 64, 0, BF16, None) == ALIAS
     assert g(None, W, Y, 4, 64, 64, 128, 64, 0, BF16, None) == NULL
     assert g(X, W, Y, 0, 64, 64, 128, 64, 1, BF16, None) == OK
+
+
+def test_attention_workspace_validation(L):
+    f = L.sra_paged_decode_attention_workspace_size
+    assert f(1, 12, 2, 128, 2048, 16, 9) == DTYPE
+    assert f(-1, 12, 2, 128, 2048, 16, BF16) == SHAPE
+    assert f(1, 18, 2, 128, 2048, 16, BF16) == SHAPE
+    assert f(1, 12, 2, 96, 2048, 16, BF16) == SHAPE
+    assert f(1, 12, 2, 128, 2048, 16, F32) == 0          # the fp32 kernel takes no workspace
+    assert f(1, 12, 2, 256, 2048, 16, BF16) == 0         # nor head_dim 256
+    assert f(0, 12, 2, 128, 2048, 16, BF16) == 0
+    g = L.sra_paged_decode_attention_ws
+    Q, C, TB, SL, O = (P + i * 0x1000000 for i in range(5))
+    assert g(Q, C, TB, SL, O, 4, 12, 2, 128, 1536, 1536, 64, 16, 8, 0.088, None, -1, None, BF16, None) == ARG
+    assert g(Q, C, TB, SL, O, 4, 12, 2, 128, 1536, 1536, 64, 16, 8, 0.088, None, 0, None, 7, None) == DTYPE
+    assert g(Q, C, TB, SL, O, 0, 12, 2, 128, 1536, 1536, 64, 16, 8, 0.088, None, 0, None, BF16, None) == OK
 
 
 def test_uclip_validation(L):

@@ -194,3 +194,45 @@ def test_reads_what_rope_kv_store_wrote():
     for b in range(B):
         s = int(slot[b])
         assert torch.equal(cg[1, s // bs, s % bs], v[b])
+
+
+# ----------------------------------------------- global split through a workspace
+@pytest.mark.parametrize("B,ctx,n_head,n_kv,hd", [(1, 32768, 12, 2, 128), (2, 16384, 8, 1, 64), (1, 12000, 32, 4, 128),
+                                                  (3, 9000, 12, 2, 128)])
+def test_workspace_split_matches_the_oracle_twice(B, ctx, n_head, n_kv, hd):
+    """Long contexts over few (request, kv head) pairs take the workspace path; two calls in a
+    row give the same bytes (the kernel leaves the workspace ready for the next call)."""
+    nb = B * ((ctx + 15) // 16) + 8
+    q, cache, table, seq = syn.attention_inputs(B, ctx, n_head, n_kv, hd, 16, nb, torch.bfloat16, 1022 + B)
+    seq[0] = ctx - 7 if B > 1 else seq[0]
+    ws = sra.decode_attention_workspace(B, n_head, n_kv, hd, table.shape[1], 16, torch.bfloat16, DEV)
+    assert ws is not None and ws.numel() > 0
+    dq, dc, dt, ds = q.to(DEV), cache.to(DEV), table.to(DEV), seq.to(DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    a = sra.paged_decode_attention(dq, dc, dt, ds, workspace=ws, err_count=err)
+    b = sra.paged_decode_attention(dq, dc, dt, ds, workspace=ws, err_count=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    assert torch.equal(a, b)
+    assert int(ws[:4 * B * n_kv].view(torch.int32).abs().sum()) == 0   # counters back at zero
+    want = torch.empty_like(q)
+    oracle.paged_decode_attention(q, cache, table, seq, want)
+    assert_attention_close(a, want, cache, table, seq, f"workspace B={B} ctx={ctx}")
+
+
+def test_workspace_rules():
+    q, cache, table, seq = syn.attention_inputs(1, 32768, 12, 2, 128, 16, 2056, torch.bfloat16, 1026)
+    ws = sra.decode_attention_workspace(1, 12, 2, 128, table.shape[1], 16, torch.bfloat16, DEV)
+    dq, dc, dt, ds = q.to(DEV), cache.to(DEV), table.to(DEV), seq.to(DEV)
+    with pytest.raises(sra.SRAError):        # too small
+        sra.paged_decode_attention(dq, dc, dt, ds, workspace=ws[:64])
+    # shapes that take the cluster kernel need none; a workspace given anyway is not used
+    assert sra.decode_attention_workspace(32, 12, 2, 128, 64, 16, torch.bfloat16, DEV) is None
+    assert sra.decode_attention_workspace(1, 12, 2, 128, 2048, 16, torch.float32, DEV) is None
+    q2, cache2, table2, seq2 = syn.attention_inputs(4, 300, 12, 2, 128, 16, 128, torch.bfloat16, 1027)
+    junk = torch.full((1024,), 7, dtype=torch.uint8, device=DEV)
+    got = sra.paged_decode_attention(q2.to(DEV), cache2.to(DEV), table2.to(DEV), seq2.to(DEV), workspace=junk)
+    want = torch.empty_like(q2)
+    oracle.paged_decode_attention(q2, cache2, table2, seq2, want)
+    assert_attention_close(got, want, cache2, table2, seq2, "workspace unused")
+    assert bool((junk.cpu() == 7).all())
