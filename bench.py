@@ -239,6 +239,26 @@ def build_entries(dev, stream_handle, only=(), companions=False):
                                  (q.data_ptr(), cache.data_ptr(), table.data_ptr(), seq.data_ptr(), out.data_ptr(),
                                   B, 12, 2, 128, 12 * 128, 12 * 128, nb, 16, table.shape[1], 128 ** -0.5, None, 2,
                                   stream_handle), [q, table, seq], [out], keep=(q, cache, table, seq, out)))
+        # few (request, kv head) pairs over a long context: split over up to one CTA per SM, the
+        # partials merged through a caller workspace
+        for B, ctx in ((1, 32768), (2, 16384)):
+            name = f"decode_attention_ws:bf16:B{B}xctx{ctx}"
+            if not want(name):
+                continue
+            nb = max(4096, B * ((ctx + 15) // 16))
+            q, cache, table, seq = (t.to(dev) for t in syn.attention_inputs(B, ctx, 12, 2, 128, 16, nb,
+                                                                             torch.bfloat16, 1013))
+            out = torch.empty_like(q)
+            ws = sra.decode_attention_workspace(B, 12, 2, 128, table.shape[1], 16, torch.bfloat16, dev)
+            if ws is None:
+                raise RuntimeError(f"{name}: the shape takes no workspace split")
+            nblk = (ctx + 15) // 16
+            nbytes = 2 * B * ctx * 2 * 128 * 2 + 2 * B * 12 * 128 * 2 + 4 * (B * nblk + B)
+            entries.append(Entry(name, "decode_attention", nbytes, B, L.sra_paged_decode_attention_ws,
+                                 (q.data_ptr(), cache.data_ptr(), table.data_ptr(), seq.data_ptr(), out.data_ptr(),
+                                  B, 12, 2, 128, 12 * 128, 12 * 128, nb, 16, table.shape[1], 128 ** -0.5,
+                                  ws.data_ptr(), ws.numel(), None, 2, stream_handle), [q, table, seq], [out],
+                                 keep=(q, cache, table, seq, out, ws)))
     if companions:
         # RMSNorm / SwiGLU fused into the projection they feed (Qwen2.5-1.5B: ln1 + qkv_proj,
         # silu(gate) * up + down_proj), decode batch 1 and 64
@@ -542,6 +562,7 @@ def cpu_rows_run():
     o = torch.empty_like(q)
     timed("decode_attention", 2 * B * ctx * 2 * 128 * 2, f"B={B} x {ctx} tokens",
           lambda: oracle.paged_decode_attention(q, cache, table, seq, o))
+    out["decode_attention_ws"] = out["decode_attention"]  # same result; the workspace only splits the work
     K, N = syn.QWEN25_QKV["K"], syn.QWEN25_QKV["N"]
     x = syn.normal((1, K), 0.0, 1.0, torch.bfloat16, 1030, 1)
     w = syn.normal((K,), 1.0, 0.1, torch.bfloat16, 1030, 2)
