@@ -311,6 +311,37 @@ SRA_API int64_t sra_paged_decode_attention_workspace_size(int64_t B, int n_head,
                                                           int64_t max_blocks_per_seq, int block_size, int dtype);
 
 /*
+ * sra_paged_decode_attention_noalloc — sra_paged_decode_attention_ws for callers
+ * that cannot allocate device memory: a library running inside a serving stack
+ * whose allocator owns all of the GPU's memory, a plugin that must not call
+ * cudaMalloc behind its host framework's back, or a decode loop that cannot take
+ * the device-wide synchronisation cudaMalloc / cudaFree may cause. The pages this
+ * library follows have no counterpart to it: it exists only for such callers.
+ * Its scratch is one library-owned device array of SRA_NOALLOC_SCRATCH_BYTES,
+ * present (and held until the process exits) on every GPU that loads the
+ * library; the call allocates nothing and calls no allocating routine.
+ * Arguments, layout and results are those of sra_paged_decode_attention; on this
+ * library's planning the result equals sra_paged_decode_attention_ws's.
+ * Set-up: the first call on a device looks up the array's device address on that
+ * device (with it current); make that first call before any stream capture.
+ * Every call clears the array's counters on `stream` before its kernel runs.
+ * Races: all calls on a device share the one array, so two calls that may run at
+ * the same time on the GPU (different streams without an event between them, or
+ * different host threads) corrupt each other's partial results; order them on one
+ * stream. Shapes that need no scratch run the cluster kernel and share nothing.
+ * Errors: those of sra_paged_decode_attention_ws; a shape whose scratch would
+ * exceed SRA_NOALLOC_SCRATCH_BYTES -> SRA_ERR_SHAPE (none does on a GPU of up to
+ * 252 SMs); the array's address not available -> SRA_ERR_DEVICE.
+ */
+#define SRA_NOALLOC_SCRATCH_BYTES (1 << 20)
+SRA_API int sra_paged_decode_attention_noalloc(const void* q, const void* kv_cache, const int32_t* block_table,
+                                               const int32_t* seq_lens, void* out, int64_t B, int n_head,
+                                               int n_kv_head, int head_dim, int64_t q_tok_stride,
+                                               int64_t out_tok_stride, int64_t num_blocks, int block_size,
+                                               int64_t max_blocks_per_seq, float scale, int32_t* err_count,
+                                               int dtype, void* stream);
+
+/*
  * sra_rmsnorm_linear — RMSNorm as the prologue of the projection it feeds
  * ([lsln] sec. 2.2: ln1 + qkv_proj fused, the normed rows never stored):
  *

@@ -18,6 +18,7 @@ from ._binding import (  # noqa: F401
     glu_linear,
     lib,
     paged_decode_attention,
+    paged_decode_attention_noalloc,
     pick_variant,
     reglu,
     rmsnorm,
@@ -32,7 +33,7 @@ from ._binding import (  # noqa: F401
 )
 
 __all__ = ["rmsnorm", "add_rmsnorm", "rope_kv_store", "swiglu", "reglu", "glu", "uclip", "dyht", "paged_decode_attention",
-           "decode_attention_workspace",
+           "paged_decode_attention_noalloc", "decode_attention_workspace",
            "rmsnorm_linear", "glu_linear", "lib",
            "SRAError",
            "force_variant", "set_pdl", "variant_count", "variant_name", "pick_variant", "status_string"]

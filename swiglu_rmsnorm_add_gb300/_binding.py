@@ -47,6 +47,7 @@ def lib() -> ctypes.CDLL:
                                                      i64, f32, vp, i32, vp]
             L.sra_paged_decode_attention_ws.argtypes = L.sra_paged_decode_attention.argtypes[:15] + [vp, i64, vp,
                                                                                                     i32, vp]
+            L.sra_paged_decode_attention_noalloc.argtypes = L.sra_paged_decode_attention.argtypes
             L.sra_paged_decode_attention_workspace_size.argtypes = [i64, i32, i32, i32, i64, i32, i32]
             L.sra_paged_decode_attention_workspace_size.restype = i64
             L.sra_rmsnorm_linear.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, i32, vp]
@@ -57,7 +58,8 @@ def lib() -> ctypes.CDLL:
                                     vp]
             for fn in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_rope_kv_store_ex", "sra_glu",
                        "sra_swiglu", "sra_uclip", "sra_rope_kv_store_qk_uclip", "sra_paged_decode_attention",
-                       "sra_rmsnorm_linear", "sra_glu_linear", "sra_paged_decode_attention_ws"):
+                       "sra_rmsnorm_linear", "sra_glu_linear", "sra_paged_decode_attention_ws",
+                       "sra_paged_decode_attention_noalloc"):
                 getattr(L, fn).restype = i32
             L.sra_status_string.argtypes = [i32]
             L.sra_status_string.restype = ctypes.c_char_p
@@ -374,15 +376,8 @@ def decode_attention_workspace(B: int, n_head: int, n_kv_head: int, head_dim: in
     return torch.zeros(int(n), dtype=torch.uint8, device=device) if n > 0 else None
 
 
-def paged_decode_attention(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
-                           seq_lens: torch.Tensor, out: torch.Tensor | None = None, scale: float | None = None,
-                           err_count: torch.Tensor | None = None, stream=None,
-                           workspace: torch.Tensor | None = None) -> torch.Tensor:
-    """out[b, h] = softmax(scale * q[b, h] . K) V over request b's cached tokens.
-
-    q: [B, n_head, head_dim]; kv_cache: [2, num_blocks, block_size, n_kv_head, head_dim] (the
-    layout rope_kv_store writes); block_table: int32 [B, max_blocks]; seq_lens: int32 [B];
-    scale defaults to 1 / sqrt(head_dim)."""
+def _attention_args(q, kv_cache, block_table, seq_lens, out, scale, err_count):
+    """Checks and C arguments shared by the decode-attention entry points."""
     for t, n in ((q, "q"), (kv_cache, "kv_cache"), (block_table, "block_table"), (seq_lens, "seq_lens")):
         _cuda(t, n)
     if out is None:
@@ -411,6 +406,19 @@ def paged_decode_attention(q: torch.Tensor, kv_cache: torch.Tensor, block_table:
             n_head, n_kv, hd, _tok_stride(q, "q"), _tok_stride(out, "out"), nb, bs, block_table.shape[1],
             float(scale))
     err = err_count.data_ptr() if err_count is not None else None
+    return out, args, err
+
+
+def paged_decode_attention(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                           seq_lens: torch.Tensor, out: torch.Tensor | None = None, scale: float | None = None,
+                           err_count: torch.Tensor | None = None, stream=None,
+                           workspace: torch.Tensor | None = None) -> torch.Tensor:
+    """out[b, h] = softmax(scale * q[b, h] . K) V over request b's cached tokens.
+
+    q: [B, n_head, head_dim]; kv_cache: [2, num_blocks, block_size, n_kv_head, head_dim] (the
+    layout rope_kv_store writes); block_table: int32 [B, max_blocks]; seq_lens: int32 [B];
+    scale defaults to 1 / sqrt(head_dim)."""
+    out, args, err = _attention_args(q, kv_cache, block_table, seq_lens, out, scale, err_count)
     with torch.cuda.device(q.device):
         if workspace is None:
             st = lib().sra_paged_decode_attention(*args, err, _dtype(q), _stream(q, stream))
@@ -420,6 +428,24 @@ def paged_decode_attention(q: torch.Tensor, kv_cache: torch.Tensor, block_table:
                                                      workspace.numel() * workspace.element_size(), err,
                                                      _dtype(q), _stream(q, stream))
     _check("sra_paged_decode_attention" if workspace is None else "sra_paged_decode_attention_ws", st)
+    return out
+
+
+def paged_decode_attention_noalloc(q: torch.Tensor, kv_cache: torch.Tensor, block_table: torch.Tensor,
+                                   seq_lens: torch.Tensor, out: torch.Tensor, scale: float | None = None,
+                                   err_count: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """paged_decode_attention for callers that cannot allocate device memory (a serving
+    stack whose allocator owns the GPU, a plugin inside another framework): the long-context
+    split keeps its partial results in one device array the library holds, so the call
+    allocates nothing; `out` is therefore required. Calls on one device share that array:
+    order them on one stream. The first call on a device looks up the array's address; make
+    it before any stream capture."""
+    if out is None:
+        raise ValueError("out is required: this entry point allocates nothing")
+    out, args, err = _attention_args(q, kv_cache, block_table, seq_lens, out, scale, err_count)
+    with torch.cuda.device(q.device):
+        st = lib().sra_paged_decode_attention_noalloc(*args, err, _dtype(q), _stream(q, stream))
+    _check("sra_paged_decode_attention_noalloc", st)
     return out
 
 

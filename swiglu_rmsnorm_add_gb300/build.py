@@ -21,7 +21,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libsra.so")
 
-SOURCES = ["api.cu", "norm_rms.cu", "norm_add.cu", "rope_kv.cu", "glu.cu", "uclip.cu", "attn.cu", "linear.cu"]
+SOURCES = ["api.cu", "norm_rms.cu", "norm_add.cu", "rope_kv.cu", "glu.cu", "uclip.cu", "attn.cu", "attn_noalloc.cu", "linear.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-Wall,-fvisibility=hidden", "-I" + INCLUDE,
                  "-I" + CSRC]

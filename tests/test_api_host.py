@@ -38,7 +38,7 @@ def test_header_declares_the_api():
     for n in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_rope_kv_store_ex", "sra_glu",
               "sra_swiglu", "sra_uclip", "sra_paged_decode_attention", "sra_rope_kv_store_qk_uclip",
               "sra_rmsnorm_linear", "sra_glu_linear", "sra_paged_decode_attention_ws",
-              "sra_paged_decode_attention_workspace_size"):
+              "sra_paged_decode_attention_workspace_size", "sra_paged_decode_attention_noalloc"):
         assert n in names
 
 
@@ -232,6 +232,17 @@ def test_attention_workspace_validation(L):
     assert g(Q, C, TB, SL, O, 4, 12, 2, 128, 1536, 1536, 64, 16, 8, 0.088, None, -1, None, BF16, None) == ARG
     assert g(Q, C, TB, SL, O, 4, 12, 2, 128, 1536, 1536, 64, 16, 8, 0.088, None, 0, None, 7, None) == DTYPE
     assert g(Q, C, TB, SL, O, 0, 12, 2, 128, 1536, 1536, 64, 16, 8, 0.088, None, 0, None, BF16, None) == OK
+
+
+def test_attention_noalloc_validation(L):
+    # the library-held scratch variant rejects what the other entry points reject, before
+    # touching a device
+    h = L.sra_paged_decode_attention_noalloc
+    Q, C, TB, SL, O = (P + i * 0x1000000 for i in range(5))
+    assert h(Q, C, TB, SL, O, 4, 12, 2, 128, 1536, 1536, 64, 16, 8, 0.088, None, 7, None) == DTYPE
+    assert h(Q, C, TB, SL, O, 4, 18, 2, 128, 1536, 1536, 64, 16, 8, 0.088, None, BF16, None) == SHAPE
+    assert h(Q, C, TB, SL, O, -1, 12, 2, 128, 1536, 1536, 64, 16, 8, 0.088, None, BF16, None) == SHAPE
+    assert h(Q, C, TB, SL, O, 0, 12, 2, 128, 1536, 1536, 64, 16, 8, 0.088, None, BF16, None) == OK
 
 
 def test_uclip_validation(L):
