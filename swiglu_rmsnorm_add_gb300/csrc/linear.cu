@@ -190,20 +190,34 @@ __global__ void __launch_bounds__(kWarps * 32) linear_kernel(LinArgs a) {
     };
     if (ntiles > 0) prefetch(0);
     if constexpr (PRO == 0) {
-        // each rank sums the squares of its K range; the cluster exchanges the partial sums
-        for (int r = warp; r < MT * 16; r += kWarps) {
-            float ss = 0.0f;
-            if (r < rows) {
-                const T* xr = X + (r0 + r) * a.xs + kbase;
-                for (int k = lane * 8; k < ntiles * kKT; k += 256) {
-                    float f[8];
-                    V8::unpack(V8::load(xr + k), f);
+        // each rank sums the squares of its K range; the cluster exchanges the partial sums.
+        // A warp owns rows warp, warp + 4, ...: the loads of all its rows go out together,
+        // one 16-byte chunk per lane and row per 256 columns
+        constexpr int RPW = MT * 16 / kWarps;
+        float ss[RPW];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
-                }
-                ss = warp_sum(ss);
+        for (int i = 0; i < RPW; ++i) ss[i] = 0.0f;
+        for (int k = lane * 8; k < ntiles * kKT; k += 256) {
+            R8 v[RPW];
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                const int r = warp + kWarps * i;
+                if (r < rows) v[i] = V8::load(X + (r0 + r) * a.xs + kbase + k);
             }
-            if (lane == 0) stat[r] = ss;
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                if (warp + kWarps * i < rows) {
+                    float f[8];
+                    V8::unpack(v[i], f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) ss[i] = fmaf(f[e], f[e], ss[i]);
+                }
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < RPW; ++i) {
+            const float t = warp_sum(ss[i]);
+            if (lane == 0) stat[warp + kWarps * i] = t;
         }
         cluster.sync();  // every rank's partial sums are in its shared memory
         for (int r = threadIdx.x; r < MT * 16; r += kWarps * 32) {
@@ -331,37 +345,64 @@ __global__ void __launch_bounds__(kNW16 * 32) linear16_kernel(LinArgs a) {
     const int cpr = static_cast<int>(a.K / 8);
     for (int c = threadIdx.x; c < cpr; c += kNW16 * 32) reinterpret_cast<uint4*>(zrow)[c] = make_uint4(0, 0, 0, 0);
     if constexpr (PRO == 0) {
-        // full-row sums of squares: a warp per row
+        // full-row sums of squares: a warp per row, four 16-byte loads per lane in flight
         for (int r = warp; r < rows; r += kNW16) {
             const T* xr = X + r * a.xs;
             float ss = 0.0f;
-            for (int64_t k = lane * 8; k < a.K; k += 256) {
-                float f[8];
-                V8::unpack(V8::load(xr + k), f);
+            for (int64_t k0 = lane * 8; k0 < a.K; k0 += 4 * 256) {
+                R8 v[4];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+                for (int u = 0; u < 4; ++u)
+                    if (k0 + u * 256 < a.K) v[u] = V8::load(xr + k0 + u * 256);
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (k0 + u * 256 < a.K) {
+                        float f[8];
+                        V8::unpack(v[u], f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) ss = fmaf(f[e], f[e], ss);
+                    }
+                }
             }
             ss = warp_sum(ss);
             if (lane == 0) inv[r] = rsqrtf(ss / static_cast<float>(a.K) + a.eps);
         }
         __syncthreads();
     }
-    for (int c = threadIdx.x; c < rows * cpr; c += kNW16 * 32) {
-        const int r = c / cpr, ch = c - r * cpr;
-        const T* xr = X + r * a.xs + ch * 8;
-        float f[8], g[8];
-        V8::unpack(V8::load(xr), f);
-        if constexpr (PRO == 0) {
-            V8::unpack(V8::load(static_cast<const T*>(a.w_ln) + ch * 8), g);
-            const float iv = inv[r];
+    // h for all of K: thread chunks c = tid + 256 u, the inputs of HB chunks loaded together
+    constexpr int HB = 8;
+    const int total = rows * cpr;
+    for (int c0 = threadIdx.x; c0 < total; c0 += HB * kNW16 * 32) {
+        R8 xv[HB], gv[HB];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = f[e] * iv * g[e];
-        } else {
-            V8::unpack(V8::load(xr + a.K), g);
-#pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = glu_act<PRO - 1>(f[e]) * g[e];
+        for (int u = 0; u < HB; ++u) {
+            const int c = c0 + u * kNW16 * 32;
+            if (c < total) {
+                const int r = c / cpr, ch = c - r * cpr;
+                const T* xr = X + r * a.xs + ch * 8;
+                xv[u] = V8::load(xr);
+                gv[u] = PRO == 0 ? V8::load(static_cast<const T*>(a.w_ln) + ch * 8) : V8::load(xr + a.K);
+            }
         }
-        *reinterpret_cast<R8*>(hsm + static_cast<int64_t>(r) * a.K + swz(r, ch) * 8) = V8::pack(f);
+#pragma unroll
+        for (int u = 0; u < HB; ++u) {
+            const int c = c0 + u * kNW16 * 32;
+            if (c < total) {
+                const int r = c / cpr, ch = c - r * cpr;
+                float f[8], g[8];
+                V8::unpack(xv[u], f);
+                V8::unpack(gv[u], g);
+                if constexpr (PRO == 0) {
+                    const float iv = inv[r];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = f[e] * iv * g[e];
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = glu_act<PRO - 1>(f[e]) * g[e];
+                }
+                *reinterpret_cast<R8*>(hsm + static_cast<int64_t>(r) * a.K + swz(r, ch) * 8) = V8::pack(f);
+            }
+        }
     }
     __syncthreads();
 
