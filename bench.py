@@ -901,7 +901,7 @@ def run_sweep(args):
         settings = [(-1, "auto")]
         for v in range(nvar):
             nm = sra.variant_name("rmsnorm", v)
-            if nm in ("warp_rows", "cta_row", "cta_pair"):
+            if nm in ("warp_rows", "cta_row", "cta_pair", "cta_lean"):
                 settings += [(v | (nv << 8), f"{nm}/nv{nv}") for nv in (1, 2, 3, 4, 6, 8)]
             else:
                 settings.append((v, nm))

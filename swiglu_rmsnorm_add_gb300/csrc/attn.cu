@@ -443,13 +443,18 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
             const int r = rr0 + RPI * i, ch = col + cc * LPR;
             dst_off[i][cc] = r * HD + ((ch ^ (r & 7)) * 8);
         }
-    auto issue = [&](int64_t u) {
+    // Block-table entry of token `lane` of tile u (lanes < 16; 0 past the static range). It is
+    // read one tile ahead of its use, so the copy issue never waits on the table's latency.
+    auto load_blk = [&](int64_t u) -> int32_t {
+        const int64_t tok = t_begin + u * kMmaTile + lane;
+        return lane < kMmaTile && tok < t_lim ? table[tok >> bs_log2] : 0;
+    };
+    auto issue = [&](int64_t u, int32_t blk) {
         const int slot = static_cast<int>((u / kMmaWarps) % kMmaStages);
         T* dst = ring + static_cast<size_t>(slot) * 2 * TE;
         int64_t off = -1;  // element offset of token `lane`'s K row in the cache, -1: no row
         if (lane < kMmaTile) {
             const int64_t tok = t_begin + u * kMmaTile + lane;
-            const int32_t blk = tok < t_lim ? table[tok >> bs_log2] : 0;
             if (tok < t_end) {
                 if (block_ok(blk)) {
                     off = ((static_cast<int64_t>(blk) << bs_log2) + (tok & (BS - 1))) * tok_stride + kvh_off;
@@ -473,11 +478,18 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
             }
         }
     };
-    for (int k = 0; k < kMmaStages - 1; ++k) {
-        const int64_t u = warp + static_cast<int64_t>(k) * kMmaWarps;
-        if (u < n_static) issue(u);
-        cp_async_commit();
+    {
+        int32_t blk0[kMmaStages - 1];
+#pragma unroll
+        for (int k = 0; k < kMmaStages - 1; ++k) blk0[k] = load_blk(warp + static_cast<int64_t>(k) * kMmaWarps);
+#pragma unroll
+        for (int k = 0; k < kMmaStages - 1; ++k) {
+            const int64_t u = warp + static_cast<int64_t>(k) * kMmaWarps;
+            if (u < n_static) issue(u, blk0[k]);
+            cp_async_commit();
+        }
     }
+    int32_t blk_next = load_blk(warp + static_cast<int64_t>(kMmaStages - 1) * kMmaWarps);
     // Q as A fragments (loaded while the first tiles are in flight): rows = query heads
     // (zero past G), columns = dims of k-step s
     uint32_t qa[KS][2];
@@ -497,7 +509,10 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
     for (int64_t u = warp, k = 0; u < n_tiles; u += kMmaWarps, ++k) {
         cp_async_wait<kMmaStages - 2>();
         __syncwarp();
-        if (u + (kMmaStages - 1) * kMmaWarps < n_tiles) issue(u + (kMmaStages - 1) * kMmaWarps);
+        if (u + (kMmaStages - 1) * kMmaWarps < n_tiles) {
+            issue(u + (kMmaStages - 1) * kMmaWarps, blk_next);
+            blk_next = load_blk(u + kMmaStages * kMmaWarps);
+        }
         cp_async_commit();
         const T* Ks = ring + static_cast<size_t>(k % kMmaStages) * 2 * TE;
         const T* Vs = Ks + TE;

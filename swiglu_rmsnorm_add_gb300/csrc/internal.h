@@ -33,7 +33,8 @@ enum NormVariant {
     NORM_CTA_PAIR = 4,   // a 2-CTA cluster per row, half the row in each CTA's registers
     NORM_WARP_SMEM = 5,  // one warp per row, row landed in shared memory (cp.async)
     NORM_PAIR_SMEM = 6,  // a 2-CTA cluster per row, half the row in each CTA's shared memory
-    NORM_NUM_VARIANTS = 7
+    NORM_CTA_LEAN = 7,   // one CTA (<= 256 threads) per row, row in registers, w read in the scale loop
+    NORM_NUM_VARIANTS = 8
 };
 
 #ifdef __CUDACC__

@@ -143,6 +143,15 @@ __global__ void __launch_bounds__(kWarps * 32) linear_kernel(LinArgs a) {
             cp_async16(dst + r * kKT + swz(r, ch) * 8, src + static_cast<int64_t>(r) * a.K + ch * 8);
         }
     };
+    // Before the dependency wait: this CTA's slice of W (64 rows x its K range) and of the
+    // prologue's input into L2 (hints only; both are read again after the wait).
+    if (threadIdx.x < kNT && n0 + threadIdx.x < a.N)
+        prefetch_l2(W + (n0 + threadIdx.x) * a.K + kbase, static_cast<int64_t>(ntiles) * kKT * 2);
+    else if (threadIdx.x >= kNT && threadIdx.x - kNT < rows) {
+        const T* xr = X + (r0 + threadIdx.x - kNT) * a.xs + kbase;
+        prefetch_l2(xr, static_cast<int64_t>(ntiles) * kKT * 2);
+        if (PRO != 0) prefetch_l2(xr + a.K, static_cast<int64_t>(ntiles) * kKT * 2);
+    }
     pdl_enter();
     for (int t = 0; t < kStages - 1; ++t) {
         if (t < ntiles) issue(t);
@@ -336,6 +345,12 @@ __global__ void __launch_bounds__(kNW16 * 32) linear16_kernel(LinArgs a) {
             cp_async16(dst + r * kKT + swz(r, ch) * 8, src + static_cast<int64_t>(r) * a.K + ch * 8);
         }
     };
+    // Before the dependency wait: this CTA's 16 rows of W and the prologue's input rows
+    // into L2 (hints only; both are read again after the wait).
+    if (threadIdx.x < 16)
+        prefetch_l2(W + (n0 + threadIdx.x) * a.K, a.K * 2);
+    else if (threadIdx.x >= 32 && threadIdx.x - 32 < rows)
+        prefetch_l2(X + (threadIdx.x - 32) * a.xs, (PRO == 0 ? 1 : 2) * a.K * 2);
     pdl_enter();
     for (int j = 0; j < kStages16 - 1; ++j) {
         if (j < mine) issue(j);

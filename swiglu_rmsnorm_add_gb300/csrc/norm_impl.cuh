@@ -206,7 +206,10 @@ __global__ void __launch_bounds__(1024) staged_rows_kernel(NormArgs a) {
 // of the group owns accesses idx = a0 + v * threads + tid, v < NV. The weights
 // are loaded once the residual sum is formed, so their latency hides behind
 // the reduction and their registers reuse the residual's.
-template <typename T, int NV, bool ADD, int RED>
+// LEAN: w is read in the scale loop, one access at a time, instead of being
+// held in registers across the reduction; fewer registers, so more CTAs are
+// resident.
+template <typename T, int NV, bool ADD, int RED, bool LEAN = false>
 __device__ __forceinline__ void reg_row(const NormArgs& a, int64_t r, int tid, int threads, int64_t a0, int64_t a1,
                                         bool tail_owner, float* scratch, float* pair_slot, int parity) {
     constexpr int VEC = vec16<T>();
@@ -274,11 +277,13 @@ __device__ __forceinline__ void reg_row(const NormArgs& a, int64_t r, int tid, i
         if (tid < tail) ss = fmaf(xt, xt, ss);
     }
 
-    R wv[NV];
+    R wv[LEAN ? 1 : NV];
+    if constexpr (!LEAN) {
 #pragma unroll
-    for (int v = 0; v < NV; ++v) {
-        const int64_t idx = a0 + static_cast<int64_t>(v) * threads + tid;
-        if (idx < a1) wv[v] = V::load(w + idx * VEC);
+        for (int v = 0; v < NV; ++v) {
+            const int64_t idx = a0 + static_cast<int64_t>(v) * threads + tid;
+            if (idx < a1) wv[v] = V::load(w + idx * VEC);
+        }
     }
     if (tid < tail) wt = to_f32(w[nvec * VEC + tid]);
 
@@ -291,7 +296,7 @@ __device__ __forceinline__ void reg_row(const NormArgs& a, int64_t r, int tid, i
         if (idx < a1) {
             float xf[VEC], wf[VEC];
             V::unpack(xv[v], xf);
-            V::unpack(wv[v], wf);
+            V::unpack(LEAN ? V::load(w + idx * VEC) : wv[LEAN ? 0 : v], wf);
 #pragma unroll
             for (int i = 0; i < VEC; ++i) xf[i] = xf[i] * rinv * wf[i];
             V::store(orow + idx * VEC, V::pack(xf));
@@ -362,6 +367,22 @@ __global__ void __launch_bounds__(cta_row_max_threads<NV>()) reg_cta_kernel(Norm
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
         next_row_prefetch<T, ADD>(a, r + gridDim.x, 0, a.D, threadIdx.x, blockDim.x);
         reg_row<T, NV, ADD, RED_CTA>(a, r, threadIdx.x, blockDim.x, 0, nvec, true, scratch, nullptr, 0);
+    }
+}
+
+// A CTA per row like reg_cta_kernel, with w read in the scale loop and at most
+// 256 threads held to 64 registers, so four CTAs (rows) or more share an SM:
+// 4 x 152 = 608 rows resident at once, and a second launch's CTAs can become
+// resident beside a first one's while it drains.
+template <typename T, int NV, bool ADD>
+__global__ void __launch_bounds__(256, 4) reg_lean_kernel(NormArgs a) {
+    __shared__ float scratch[33];
+    prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true, threadIdx.x, blockDim.x);
+    pdl_enter();
+    const int64_t nvec = a.D / vec16<T>();
+    for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x) {
+        next_row_prefetch<T, ADD>(a, r + gridDim.x, 0, a.D, threadIdx.x, blockDim.x);
+        reg_row<T, NV, ADD, RED_CTA, true>(a, r, threadIdx.x, blockDim.x, 0, nvec, true, scratch, nullptr, 0);
     }
 }
 
@@ -553,6 +574,13 @@ cudaError_t launch_vector(const NormArgs& a, const NormPlan& p, cudaStream_t s) 
                 case 2: return launch_persistent(reg_cta_kernel<T, 2, ADD>, a, p, false, s);
                 case 4: return launch_persistent(reg_cta_kernel<T, 4, ADD>, a, p, false, s);
                 case 8: return launch_persistent(reg_cta_kernel<T, 8, ADD>, a, p, false, s);
+                default: return cudaErrorInvalidValue;
+            }
+        case NORM_CTA_LEAN:
+            switch (p.nv) {
+                case 2: return launch_persistent(reg_lean_kernel<T, 2, ADD>, a, p, false, s);
+                case 4: return launch_persistent(reg_lean_kernel<T, 4, ADD>, a, p, false, s);
+                case 8: return launch_persistent(reg_lean_kernel<T, 8, ADD>, a, p, false, s);
                 default: return cudaErrorInvalidValue;
             }
         case NORM_CTA_PAIR:

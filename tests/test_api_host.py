@@ -296,16 +296,16 @@ def test_glu_validation(L):
 
 
 def test_variant_control(L):
-    assert sra.variant_count("rmsnorm") == 7
+    assert sra.variant_count("rmsnorm") == 8
     assert sra.variant_count("rope_kv_store") == 1
     assert sra.variant_count("glu") == 1
     assert sra.variant_count("decode_attention") == 2
     assert [sra.variant_name("decode_attention", i) for i in range(2)] == ["cuda_cores", "mma_sync"]
     assert sra.variant_count("nope") == ARG
-    assert [sra.variant_name("rmsnorm", i) for i in range(7)] == ["warp_rows", "cta_row", "cta_smem", "two_pass",
-                                                                  "cta_pair", "warp_smem", "pair_smem"]
-    assert sra.variant_name("rmsnorm", 7) is None
-    assert L.sra_force_variant(b"rmsnorm", 7) == ARG
+    assert [sra.variant_name("rmsnorm", i) for i in range(8)] == ["warp_rows", "cta_row", "cta_smem", "two_pass",
+                                                                  "cta_pair", "warp_smem", "pair_smem", "cta_lean"]
+    assert sra.variant_name("rmsnorm", 8) is None
+    assert L.sra_force_variant(b"rmsnorm", 8) == ARG
     assert L.sra_force_variant(b"bogus", 0) == ARG
     assert L.sra_force_variant(b"rmsnorm", 2) == OK
     assert sra.pick_variant("rmsnorm", 512, 1536, num_sms=152) == 2

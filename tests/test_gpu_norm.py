@@ -89,7 +89,7 @@ def test_ragged_widths(dtype, D, rows):
     assert_close(out, ref, f"add_rmsnorm [{rows},{D}] {dtype}")
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 6])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 6, 7])
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("rows,D", [(3, 1536), (700, 1536), (64, 2176), (40, 8192), (5, 333), (1, 1),
                                     (333, 4095), (512, 8192)])
