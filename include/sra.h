@@ -423,6 +423,18 @@ SRA_API int sra_version(void);
 SRA_API int sra_last_cuda_error(void);
 
 /*
+ * Bounded device waits that gave up, on the current device, since the library was
+ * loaded. Kernels that stream tiles with tensor-memory-access copies
+ * (sra_rmsnorm_linear, sra_glu_linear) wait on shared-memory barriers for those
+ * copies; each wait is bounded (about a second), and a wait that runs out is
+ * counted here and the kernel goes on, so a copy that never completes cannot hang
+ * the GPU (that call's output is then not valid). Reads the counter synchronously
+ * (cudaMemcpyFromSymbol); 0 on a device that ran none of those kernels. No paper
+ * section defines this; it is the library's own failure report.
+ */
+SRA_API unsigned int sra_wait_timeouts(void);
+
+/*
  * Programmatic dependent launch for the CALLING THREAD's subsequent calls
  * (enable != 0: on; 0: off, the default). When on, each kernel is launched with
  * programmatic stream serialization: the GPU may schedule it while the kernel

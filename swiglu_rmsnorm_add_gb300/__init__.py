@@ -30,10 +30,12 @@ from ._binding import (  # noqa: F401
     uclip,
     variant_count,
     variant_name,
+    wait_timeouts,
 )
 
 __all__ = ["rmsnorm", "add_rmsnorm", "rope_kv_store", "swiglu", "reglu", "glu", "uclip", "dyht", "paged_decode_attention",
            "paged_decode_attention_noalloc", "decode_attention_workspace",
            "rmsnorm_linear", "glu_linear", "lib",
            "SRAError",
-           "force_variant", "set_pdl", "variant_count", "variant_name", "pick_variant", "status_string"]
+           "force_variant", "set_pdl", "variant_count", "variant_name", "pick_variant", "status_string",
+           "wait_timeouts"]

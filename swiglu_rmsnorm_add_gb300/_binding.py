@@ -65,6 +65,8 @@ def lib() -> ctypes.CDLL:
             L.sra_status_string.restype = ctypes.c_char_p
             L.sra_version.restype = i32
             L.sra_last_cuda_error.restype = i32
+            L.sra_wait_timeouts.argtypes = []
+            L.sra_wait_timeouts.restype = ctypes.c_uint
             L.sra_set_pdl.argtypes = [i32]
             L.sra_set_pdl.restype = i32
             L.sra_force_variant.argtypes = [ctypes.c_char_p, i32]
@@ -86,6 +88,11 @@ def status_string(status: int) -> str:
 def _check(fn: str, status: int) -> None:
     if status != 0:
         raise SRAError(fn, status)
+
+
+def wait_timeouts() -> int:
+    """Bounded device waits that ran out on the current device since the library was loaded."""
+    return int(lib().sra_wait_timeouts())
 
 
 def set_pdl(enable: bool) -> bool:

@@ -645,6 +645,8 @@ int sra_version(void) { return SRA_VERSION; }
 
 int sra_last_cuda_error(void) { return g_last_cuda_error; }
 
+unsigned int sra_wait_timeouts(void) { return linear_wait_timeouts(); }
+
 int sra_set_pdl(int enable) {
     const int prev = g_pdl ? 1 : 0;
     g_pdl = enable != 0;
@@ -916,14 +918,14 @@ static int linear_common(const void* x, const void* w_ln, const void* W, void* y
     plan.narrow = plan.tensor_cores && B <= 16 &&
                   static_cast<int64_t>(linear16_smem(static_cast<int>(B), K)) <= std::min<int64_t>(limit, 200 * 1024);
     if (plan.tensor_cores && !plan.narrow) {
-        // 64-column slices x row blocks x K splits (a cluster); two CTAs per SM fit (about 80 KB
+        // 64-column slices x row blocks x K splits (a cluster); two CTAs per SM fit (45 to 113 KB
         // each): aim for one wave of 1-2 CTAs per SM with at least four W tiles per CTA
         const int64_t slices = (N / 64) * ((B + plan.mt * 16 - 1) / (plan.mt * 16));
         const int64_t KT = K / 64;
         while (plan.splits < 8 && slices * plan.splits * 2 <= 2 * static_cast<int64_t>(sms) &&
                KT >= 4 * plan.splits)
             plan.splits *= 2;
-        if (static_cast<int64_t>(linear_smem(plan.mt)) > limit) plan.tensor_cores = false;
+        if (static_cast<int64_t>(linear_smem(plan.mt, prologue)) > limit) plan.tensor_cores = false;
     }
     if (!plan.tensor_cores) {
         plan.splits = 1;

@@ -380,30 +380,38 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
     T* ring = reinterpret_cast<T*>(smem) + static_cast<size_t>(warp) * kMmaStages * 2 * TE;
 
     {
-        // Before the dependency wait: warm the K and V rows of this warp's first tile. The
-        // split is a static slice of the table's capacity, so the tile's tokens are known;
-        // their block ids are read relaxed (the previous kernel may still be writing them) and
-        // only steer prefetches. Everything used below is read again after the wait.
+        // Before the dependency wait: warm what the first tiles need. First the loads that
+        // depend on nothing: this request's seq_len and this split's whole slice of the block
+        // table (so the later tiles' table reads hit the L2 and each tile costs one DRAM round
+        // trip, not two). Then the K and V rows of this warp's first two tiles: the split is a
+        // static slice of the table's capacity, so the tiles' tokens are known; their block ids
+        // are read relaxed (the previous kernel may still be writing them) and only steer
+        // prefetches. Everything used below is read again after the wait.
         const int64_t cap0 = a.max_blocks * BS;
         const int64_t per0 = ((cap0 + S - 1) / S + kMmaTile - 1) / kMmaTile * kMmaTile;
-        const int64_t tok = rank * per0 + warp * kMmaTile + (lane & (kMmaTile - 1));
-        if (tok < cap0 && tok < (rank + 1) * per0) {
-            int blk;
-            asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];"
-                         : "=r"(blk)
-                         : "l"(a.table + b * a.max_blocks + tok / BS));
-            if (blk >= 0 && blk < a.num_blocks) {
+        const int64_t s0 = rank * per0, s1 = cap0 < s0 + per0 ? cap0 : s0 + per0;
+        if (warp == 0 && lane == 0) prefetch_lines(a.seq_lens + b, 4, 0, 1);
+        if (warp == kMmaWarps - 1 && s0 < s1)
+            prefetch_lines(a.table + b * a.max_blocks + s0 / BS, ((s1 - 1) / BS - s0 / BS + 1) * 4, lane, 32);
+        int blk[2] = {-1, -1};
+        int64_t tok[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            tok[j] = s0 + (warp + j * kMmaWarps) * kMmaTile + (lane & (kMmaTile - 1));
+            if (tok[j] < s1)
+                asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];"
+                             : "=r"(blk[j])
+                             : "l"(a.table + b * a.max_blocks + tok[j] / BS));
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (tok[j] < s1 && blk[j] >= 0 && blk[j] < a.num_blocks) {
                 const T* row = static_cast<const T*>(a.cache) +
-                               ((static_cast<int64_t>(blk) * BS + tok % BS) * a.n_kv + kvh) * HD +
+                               ((static_cast<int64_t>(blk[j]) * BS + tok[j] % BS) * a.n_kv + kvh) * HD +
                                (lane >= kMmaTile ? a.num_blocks * BS * static_cast<int64_t>(a.n_kv) * HD : 0);
                 prefetch_lines(row, HD * 2, 0, 1);
             }
         }
-        // and this split's whole slice of the block table, so the later tiles' table reads
-        // hit the L2 and each tile costs one DRAM round trip, not two
-        const int64_t s0 = rank * per0, s1 = cap0 < s0 + per0 ? cap0 : s0 + per0;
-        if (warp == kMmaWarps - 1 && s0 < s1)
-            prefetch_lines(a.table + b * a.max_blocks + s0 / BS, ((s1 - 1) / BS - s0 / BS + 1) * 4, lane, 32);
     }
     pdl_enter();
     int64_t len = a.seq_lens[b];

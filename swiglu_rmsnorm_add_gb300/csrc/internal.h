@@ -183,7 +183,8 @@ struct LinPlan {
 };
 
 cudaError_t launch_linear(const LinArgs& a, const LinPlan& p, int dtype, cudaStream_t s);
-size_t linear_smem(int mt);
+size_t linear_smem(int mt, int prologue);
+unsigned int linear_wait_timeouts();  // bounded waits of the fused-projection kernel that ran out
 size_t linear16_smem(int rows, int64_t K);
 
 // ------------------------------------------------------------------- UClip

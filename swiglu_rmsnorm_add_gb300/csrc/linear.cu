@@ -24,18 +24,20 @@
 // XOR-swizzled by row against bank conflicts).
 #include <cooperative_groups.h>
 
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace cg = cooperative_groups;
 
 namespace sra {
 namespace lin {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 4;   // warps of a CTA for 16 rows; 32 or 64 rows take warps_for(MT)
 constexpr int kNT = 64;      // columns of y per CTA
 constexpr int kKT = 64;      // K per W tile
-constexpr int kStages = 8;   // W tiles in flight (64 KB)
 
 __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
     const unsigned s = static_cast<unsigned>(__cvta_generic_to_shared(smem_dst));
@@ -84,13 +86,32 @@ __device__ __forceinline__ T to_t(float v) {
     return r;
 }
 
-// Shared memory: the W ring [stages][64][64] (the epilogue's partial tile reuses it once
-// drained), two h tiles [MT*16][64] (built while the other is multiplied), row statistics.
-__host__ __device__ inline size_t ring_bytes() { return static_cast<size_t>(kStages) * kNT * kKT * 2; }
-__host__ __device__ inline size_t htile_bytes(int MT) { return static_cast<size_t>(MT) * 16 * kKT * 2; }
-__host__ __device__ inline size_t smem_bytes(int MT) {
-    const size_t part = static_cast<size_t>(MT) * 16 * kNT * 4;
-    return (ring_bytes() > part ? ring_bytes() : part) + 2 * htile_bytes(MT) + static_cast<size_t>(MT) * 16 * 4;
+// Shared memory (from a 1024-byte aligned base, as the 128-byte swizzle of the tile copies
+// needs): two rings. The W ring holds W tiles [64][64]; it runs far ahead (its tiles come
+// from DRAM). The input ring holds, for the same 64 columns of K, the prologue's input tile:
+// x [MT*16][64] and the norm weight's 64 entries (RMSNorm), or gate and up [2][MT*16][64]
+// (GLU); its tiles are re-read by every column slice, so they come from L2 and a short ring
+// covers them. Tiles are swizzled (16-byte chunk c of row r at c ^ (r % 8)). Then two h tiles
+// [MT*16][64] (built while the other is multiplied). The epilogue's partial tile reuses the
+// rings once they have drained. Sizes keep two CTAs per SM.
+__host__ __device__ constexpr int warps_for(int MT) { return MT == 1 ? 4 : 8; }
+__host__ __device__ constexpr int wstages_for(int MT, int PRO) { return MT == 4 && PRO != 0 ? 5 : 8; }
+__host__ __device__ constexpr int xstages_for(int MT, int PRO) { return 3; }
+__host__ __device__ constexpr size_t wtile_bytes() { return static_cast<size_t>(kNT) * kKT * 2; }
+__host__ __device__ constexpr size_t xtile_bytes(int MT) { return static_cast<size_t>(MT) * 16 * kKT * 2; }
+__host__ __device__ constexpr size_t xstage_bytes(int MT, int PRO) {
+    return (static_cast<size_t>(PRO == 0 ? 1 : 2) * xtile_bytes(MT) + (PRO == 0 ? kKT * 2 : 0) + 1023) / 1024 * 1024;
+}
+__host__ __device__ constexpr size_t rings_bytes(int MT, int PRO) {
+    return wstages_for(MT, PRO) * wtile_bytes() + xstages_for(MT, PRO) * xstage_bytes(MT, PRO);
+}
+__host__ __device__ constexpr size_t htile_bytes(int MT) { return static_cast<size_t>(MT) * 16 * kKT * 2; }
+__host__ __device__ constexpr size_t ring_area(int MT, int PRO) {
+    return rings_bytes(MT, PRO) > static_cast<size_t>(MT) * 16 * kNT * 4 ? rings_bytes(MT, PRO)
+                                                                           : static_cast<size_t>(MT) * 16 * kNT * 4;
+}
+__host__ __device__ constexpr size_t smem_bytes(int MT, int PRO) {
+    return 1024 + ring_area(MT, PRO) + 2 * htile_bytes(MT);  // + the alignment slack
 }
 
 // 16-byte chunk c of row r of a row-major tile whose rows hold `cpr` chunks.
@@ -105,44 +126,77 @@ __device__ __forceinline__ float glu_act(float g) {
     }
 }
 
-// PRO: 0 = RMSNorm prologue, 1 = SwiGLU, 2 = ReGLU.
+// PRO: 0 = RMSNorm prologue, 1 = SwiGLU, 2 = ReGLU. The tensor maps: tmW over W [N][K] and
+// tmX over the input rows [B][K] (GLU: [B][2K]), both with 64 x 64 (rows: MT*16) boxes and the
+// 128-byte swizzle; tmN over the norm weight [K], 64-entry boxes (RMSNorm only).
 template <typename T, int MT, int PRO>
-__global__ void __launch_bounds__(kWarps * 32) linear_kernel(LinArgs a) {
+__global__ void __launch_bounds__(warps_for(MT) * 32) linear_kernel(LinArgs a, const __grid_constant__ CUtensorMap tmW,
+                                                              const __grid_constant__ CUtensorMap tmX,
+                                                              const __grid_constant__ CUtensorMap tmN) {
     using V8 = Vec<T, 8>;
     using R8 = typename V8::Raw;
-    extern __shared__ __align__(16) unsigned char smem[];
+    constexpr int XR = MT * 16;                  // rows of an input / h tile
+    constexpr int NW = warps_for(MT);            // warps
+    constexpr int SW = wstages_for(MT, PRO);  // W ring stages
+    constexpr int SX = xstages_for(MT, PRO);  // input ring stages
+    constexpr size_t XB = xstage_bytes(MT, PRO);
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    __shared__ uint64_t wfull[SW];  // W tile t lands in slot t % SW and completes on wfull[t % SW]
+    __shared__ uint64_t xfull[SX];  // input tile t: slot t % SX, xfull[t % SX]
+    __shared__ float stat[64];
+    __shared__ float inv[64];
     cg::cluster_group cluster = cg::this_cluster();
     const int SK = static_cast<int>(cluster.num_blocks());
     const int rank = static_cast<int>(cluster.block_rank());
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t n0 = (blockIdx.x / SK) * static_cast<int64_t>(kNT);
-    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * MT * 16;
-    const int rows = static_cast<int>(a.B - r0 < MT * 16 ? a.B - r0 : MT * 16);
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * XR;
+    const int rows = static_cast<int>(a.B - r0 < XR ? a.B - r0 : XR);
     const int KT = static_cast<int>(a.K / kKT);
     const int per = (KT + SK - 1) / SK;
     const int kt0 = rank * per < KT ? rank * per : KT;
     const int kt1 = kt0 + per < KT ? kt0 + per : KT;
     const int ntiles = kt1 - kt0;
     const int64_t kbase = static_cast<int64_t>(kt0) * kKT;
-    T* ring = reinterpret_cast<T*>(smem);
     float* part = reinterpret_cast<float*>(smem);  // the epilogue's partial tile, after the ring drains
-    const size_t ring_area = ring_bytes() > static_cast<size_t>(MT) * 16 * kNT * 4
-                                 ? ring_bytes()
-                                 : static_cast<size_t>(MT) * 16 * kNT * 4;
-    T* hbuf = reinterpret_cast<T*>(smem + ring_area);                         // [2][MT*16][64]
-    float* stat = reinterpret_cast<float*>(smem + ring_area + 2 * htile_bytes(MT));
+    T* hbuf = reinterpret_cast<T*>(smem + ring_area(MT, PRO));  // [2][XR][64]
     const T* W = static_cast<const T*>(a.W);
     const T* X = static_cast<const T*>(a.x);
+    auto wslot = [&](int t) { return reinterpret_cast<T*>(smem + static_cast<size_t>(t % SW) * wtile_bytes()); };
+    auto xslot = [&](int t) {
+        return reinterpret_cast<T*>(smem + SW * wtile_bytes() + static_cast<size_t>(t % SX) * XB);
+    };
 
-    // W tile t (columns (kt0 + t) * 64 .. of rows n0 .. n0 + 63) into ring slot t % stages
-    auto issue = [&](int t) {
-        T* dst = ring + static_cast<size_t>(t % kStages) * kNT * kKT;
-        const T* src = W + n0 * a.K + (kbase + static_cast<int64_t>(t) * kKT);
-        for (int c = threadIdx.x; c < kNT * 8; c += kWarps * 32) {
-            const int r = c >> 3, ch = c & 7;
-            cp_async16(dst + r * kKT + swz(r, ch) * 8, src + static_cast<int64_t>(r) * a.K + ch * 8);
+    // Thread 0 issues the tile copies. W tile t: W's 64 x 64 tile at columns (kt0 + t) * 64 of
+    // rows n0 ..; input tile t: the input rows' same 64 columns of K (x; or gate and up) and,
+    // for the RMSNorm, the norm weight's 64 entries. Rows past B arrive as zeros.
+    constexpr uint32_t kXTx =
+        static_cast<uint32_t>((PRO == 0 ? 1 : 2) * xtile_bytes(MT) + (PRO == 0 ? kKT * 2 : 0));
+    auto issue_w = [&](int t) {
+        uint64_t* bar = &wfull[t % SW];
+        fence_proxy_async();  // the slot's earlier reads come before the copy
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(wtile_bytes()));
+        tma_load_2d(wslot(t), &tmW, static_cast<int>(kbase) + t * kKT, static_cast<int>(n0), bar);
+    };
+    auto issue_x = [&](int t) {
+        uint64_t* bar = &xfull[t % SX];
+        const int k0 = static_cast<int>(kbase) + t * kKT;
+        T* xd = xslot(t);
+        fence_proxy_async();
+        mbar_arrive_expect_tx(bar, kXTx);
+        tma_load_2d(xd, &tmX, k0, static_cast<int>(r0), bar);
+        if constexpr (PRO != 0) {
+            tma_load_2d(xd + XR * kKT, &tmX, static_cast<int>(a.K) + k0, static_cast<int>(r0), bar);
+        } else {
+            tma_load_1d(xd + XR * kKT, &tmN, k0, bar);
         }
     };
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < SW; ++i) mbar_init(&wfull[i], 1);
+        for (int i = 0; i < SX; ++i) mbar_init(&xfull[i], 1);
+        mbar_init_fence();
+    }
     // Before the dependency wait: this CTA's slice of W (64 rows x its K range) and of the
     // prologue's input into L2 (hints only; both are read again after the wait).
     if (threadIdx.x < kNT && n0 + threadIdx.x < a.N)
@@ -152,44 +206,32 @@ __global__ void __launch_bounds__(kWarps * 32) linear_kernel(LinArgs a) {
         prefetch_l2(xr, static_cast<int64_t>(ntiles) * kKT * 2);
         if (PRO != 0) prefetch_l2(xr + a.K, static_cast<int64_t>(ntiles) * kKT * 2);
     }
+    __syncthreads();  // the barriers are initialised
     pdl_enter();
-    for (int t = 0; t < kStages - 1; ++t) {
-        if (t < ntiles) issue(t);
-        cp_async_commit();
+    if (threadIdx.x == 0) {
+        for (int t = 0; t < SX && t < ntiles; ++t) issue_x(t);
+        for (int t = 0; t < SW - 1 && t < ntiles; ++t) issue_w(t);
     }
 
-    // h tiles: thread owns chunks c = tid + 128 i (i < MT) of the [MT*16][64] tile: row c / 8,
-    // 8-element chunk c % 8. The inputs of tile t + 1 are loaded into registers while tile t
-    // is multiplied, then turned into h (rounded to T) in the other buffer.
-    R8 xa[MT], xb[MT];  // x (or gate) and w_ln (or up) chunks
-    auto prefetch = [&](int t) {
-#pragma unroll
-        for (int i = 0; i < MT; ++i) {
-            const int c = threadIdx.x + kWarps * 32 * i, r = c >> 3, ch = c & 7;
-            if (r < rows) {
-                const int64_t k = kbase + static_cast<int64_t>(t) * kKT + ch * 8;
-                const T* xr = X + (r0 + r) * a.xs + k;
-                xa[i] = V8::load(xr);
-                xb[i] = PRO == 0 ? V8::load(static_cast<const T*>(a.w_ln) + k) : V8::load(xr + a.K);
-            }
-        }
-    };
-    __shared__ float inv[64];
+    // h tile t from input tile t: thread owns chunks c = tid + 32 NW i of the [XR][64] tile:
+    // row c / 8, 8-element chunk c % 8; rows past B are zero.
     auto build = [&](int t) {
-        T* hb = hbuf + static_cast<size_t>(t & 1) * MT * 16 * kKT;
+        T* hb = hbuf + static_cast<size_t>(t & 1) * XR * kKT;
+        const T* xs = xslot(t);
 #pragma unroll
-        for (int i = 0; i < MT; ++i) {
-            const int c = threadIdx.x + kWarps * 32 * i, r = c >> 3, ch = c & 7;
+        for (int i = 0; i < XR * 8 / (NW * 32); ++i) {
+            const int c = threadIdx.x + NW * 32 * i, r = c >> 3, ch = c & 7;
             float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
             if (r < rows) {
                 float g[8];
-                V8::unpack(xa[i], f);
-                V8::unpack(xb[i], g);
+                V8::unpack(*reinterpret_cast<const R8*>(xs + r * kKT + swz(r, ch) * 8), f);
                 if constexpr (PRO == 0) {
+                    V8::unpack(*reinterpret_cast<const R8*>(xs + XR * kKT + ch * 8), g);
                     const float iv = inv[r];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) f[e] = f[e] * iv * g[e];
                 } else {
+                    V8::unpack(*reinterpret_cast<const R8*>(xs + (XR + r) * kKT + swz(r, ch) * 8), g);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) f[e] = glu_act<PRO - 1>(f[e]) * g[e];
                 }
@@ -197,12 +239,11 @@ __global__ void __launch_bounds__(kWarps * 32) linear_kernel(LinArgs a) {
             *reinterpret_cast<R8*>(hb + r * kKT + swz(r, ch) * 8) = V8::pack(f);
         }
     };
-    if (ntiles > 0) prefetch(0);
     if constexpr (PRO == 0) {
         // each rank sums the squares of its K range; the cluster exchanges the partial sums.
         // A warp owns rows warp, warp + 4, ...: the loads of all its rows go out together,
         // one 16-byte chunk per lane and row per 256 columns
-        constexpr int RPW = MT * 16 / kWarps;
+        constexpr int RPW = MT * 16 / NW;
         float ss[RPW];
 #pragma unroll
         for (int i = 0; i < RPW; ++i) ss[i] = 0.0f;
@@ -210,12 +251,12 @@ __global__ void __launch_bounds__(kWarps * 32) linear_kernel(LinArgs a) {
             R8 v[RPW];
 #pragma unroll
             for (int i = 0; i < RPW; ++i) {
-                const int r = warp + kWarps * i;
+                const int r = warp + NW * i;
                 if (r < rows) v[i] = V8::load(X + (r0 + r) * a.xs + kbase + k);
             }
 #pragma unroll
             for (int i = 0; i < RPW; ++i) {
-                if (warp + kWarps * i < rows) {
+                if (warp + NW * i < rows) {
                     float f[8];
                     V8::unpack(v[i], f);
 #pragma unroll
@@ -226,19 +267,22 @@ __global__ void __launch_bounds__(kWarps * 32) linear_kernel(LinArgs a) {
 #pragma unroll
         for (int i = 0; i < RPW; ++i) {
             const float t = warp_sum(ss[i]);
-            if (lane == 0) stat[warp + kWarps * i] = t;
+            if (lane == 0) stat[warp + NW * i] = t;
         }
         cluster.sync();  // every rank's partial sums are in its shared memory
-        for (int r = threadIdx.x; r < MT * 16; r += kWarps * 32) {
+        for (int r = threadIdx.x; r < MT * 16; r += NW * 32) {
             float tot = 0.0f;
             for (int q = 0; q < SK; ++q) tot += cluster.map_shared_rank(stat, q)[r];
             inv[r] = rsqrtf(tot / static_cast<float>(a.K) + a.eps);
         }
-        __syncthreads();
+        __syncthreads();  // inv complete before the first h tile
     }
-    if (ntiles > 0) build(0);
+    if (ntiles > 0) {
+        mbar_wait(&xfull[0], 0);
+        build(0);
+    }
 
-    constexpr int NGROUPS = kWarps / MT;   // warps sharing an m-tile split its 64 columns
+    constexpr int NGROUPS = NW / MT;   // warps sharing an m-tile split its 64 columns
     constexpr int NBW = 8 / NGROUPS;       // n8 blocks per warp
     const int mt = warp % MT, ng = warp / MT;
     float acc[NBW][4];
@@ -246,13 +290,20 @@ __global__ void __launch_bounds__(kWarps * 32) linear_kernel(LinArgs a) {
     for (int j = 0; j < NBW; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
     const int li = lane & 7, lm = lane >> 3;  // ldmatrix: row within a matrix, matrix index
     for (int t = 0; t < ntiles; ++t) {
-        if (t + 1 < ntiles) prefetch(t + 1);
-        cp_async_wait<kStages - 2>();
-        __syncthreads();  // W tile t landed, h tile t built; the slot of tile t - 1 is free
-        if (t + kStages - 1 < ntiles) issue(t + kStages - 1);
-        cp_async_commit();
-        const T* wt = ring + static_cast<size_t>(t % kStages) * kNT * kKT;
-        const T* ht = hbuf + static_cast<size_t>(t & 1) * MT * 16 * kKT;
+        // W tile t landed (for this iteration's products), input tile t + 1 landed (for h
+        // tile t + 1, built at the end of this iteration)
+        mbar_wait(&wfull[t % SW], static_cast<uint32_t>((t / SW) & 1));
+        if (t + 1 < ntiles) mbar_wait(&xfull[(t + 1) % SX], static_cast<uint32_t>(((t + 1) / SX) & 1));
+        // h tile t is built and every warp is done with tile t - 1 and input tile t: W tile
+        // t - 1's slot takes W tile t + SW - 1, input tile t's slot takes input tile t + SX,
+        // h tile t - 1's buffer takes h tile t + 1
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            if (t + SW - 1 < ntiles) issue_w(t + SW - 1);
+            if (t + SX < ntiles) issue_x(t + SX);
+        }
+        const T* wt = wslot(t);
+        const T* ht = hbuf + static_cast<size_t>(t & 1) * XR * kKT;
 #pragma unroll
         for (int ks = 0; ks < kKT / 16; ++ks) {
             uint32_t af[4];
@@ -271,8 +322,7 @@ __global__ void __launch_bounds__(kWarps * 32) linear_kernel(LinArgs a) {
         }
         if (t + 1 < ntiles) build(t + 1);
     }
-    cp_async_wait<0>();
-    __syncthreads();  // the ring is drained: its space takes the partial tile
+    __syncthreads();  // every warp is done with the ring: its space takes the partial tile
 
     // ---- epilogue: partial tile into shared memory, then summed over the cluster
     {
@@ -289,7 +339,7 @@ __global__ void __launch_bounds__(kWarps * 32) linear_kernel(LinArgs a) {
     }
     cluster.sync();
     T* y = static_cast<T*>(a.y);
-    for (int idx = rank * kWarps * 32 + threadIdx.x; idx < rows * kNT; idx += SK * kWarps * 32) {
+    for (int idx = rank * NW * 32 + threadIdx.x; idx < rows * kNT; idx += SK * NW * 32) {
         const int r = idx / kNT, c = idx - r * kNT;
         float sum = 0.0f;
         for (int q = 0; q < SK; ++q) sum += cluster.map_shared_rank(part, q)[r * kNT + c];
@@ -477,21 +527,32 @@ cudaError_t launch16(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
 }
 
 template <typename T, int MT, int PRO>
-cudaError_t launch_mt(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
+cudaError_t launch_mt(const LinArgs& a, const LinPlan& p, cudaStream_t s, const CUtensorMap& tmW,
+                      const CUtensorMap& tmX, const CUtensorMap& tmN) {
     auto kernel = linear_kernel<T, MT, PRO>;
-    const size_t smem = smem_bytes(MT);
+    const size_t smem = smem_bytes(MT, PRO);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const dim3 grid(static_cast<unsigned>(a.N / kNT * p.splits), static_cast<unsigned>((a.B + MT * 16 - 1) / (MT * 16)));
-    return launch_kernel(kernel, grid, dim3(kWarps * 32), smem, s, p.pdl, p.splits, a);
+    return launch_kernel(kernel, grid, dim3(warps_for(MT) * 32), smem, s, p.pdl, p.splits, a, tmW, tmX, tmN);
 }
 
 template <typename T, int PRO>
 cudaError_t launch_pro(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
+    // tensor maps: W [N][K] and the input rows [B][K or 2K] in 64 x (64 or MT*16) boxes with the
+    // 128-byte swizzle, the norm weight [K] in 64-entry boxes
+    const bool bf16 = sizeof(T) == 2 && std::is_same<T, __nv_bfloat16>::value;
+    const uint32_t xr = static_cast<uint32_t>(p.mt) * 16;
+    CUtensorMap tmW, tmX, tmN;
+    memset(&tmN, 0, sizeof(tmN));
+    if (!encode_tmap_16(&tmW, a.W, 2, a.K, a.N, a.K * 2, kKT, kNT, bf16, true) ||
+        !encode_tmap_16(&tmX, a.x, 2, PRO == 0 ? a.K : 2 * a.K, a.B, a.xs * 2, kKT, xr, bf16, true) ||
+        (PRO == 0 && !encode_tmap_16(&tmN, a.w_ln, 1, a.K, 1, 0, kKT, 1, bf16, false)))
+        return cudaErrorNotSupported;
     switch (p.mt) {
-        case 1: return launch_mt<T, 1, PRO>(a, p, s);
-        case 2: return launch_mt<T, 2, PRO>(a, p, s);
-        case 4: return launch_mt<T, 4, PRO>(a, p, s);
+        case 1: return launch_mt<T, 1, PRO>(a, p, s, tmW, tmX, tmN);
+        case 2: return launch_mt<T, 2, PRO>(a, p, s, tmW, tmX, tmN);
+        case 4: return launch_mt<T, 4, PRO>(a, p, s, tmW, tmX, tmN);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -576,7 +637,43 @@ cudaError_t launch_simple_typed(const LinArgs& a, const LinPlan& p, cudaStream_t
 
 }  // namespace lin
 
-size_t linear_smem(int mt) { return lin::smem_bytes(mt); }
+bool encode_tmap_16(CUtensorMap* map, const void* base, int rank, uint64_t dim0, uint64_t dim1, uint64_t stride1,
+                    uint32_t box0, uint32_t box1, bool bf16, bool swizzle128) {
+    using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+    static const Encode encode = [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return static_cast<Encode>(nullptr);
+        }
+        return reinterpret_cast<Encode>(fn);
+    }();
+    if (!encode || rank < 1 || rank > 2) return false;
+    const cuuint64_t dims[2] = {dim0, dim1};
+    const cuuint64_t strides[1] = {stride1};
+    const cuuint32_t box[2] = {box0, box1};
+    const cuuint32_t estr[2] = {1, 1};
+    return encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                  static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+unsigned int linear_wait_timeouts() {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return v;
+}
+
+size_t linear_smem(int mt, int prologue) { return lin::smem_bytes(mt, prologue); }
 size_t linear16_smem(int rows, int64_t K) { return lin::smem16_bytes(rows, K); }
 
 cudaError_t launch_linear(const LinArgs& a, const LinPlan& p, int dtype, cudaStream_t s) {

@@ -120,3 +120,13 @@ def test_llama3_8b_down_sampled():
     rows = torch.tensor([0, 13, 40, 63])
     got, want, h, W = glu_case(64, 14336, 4096, torch.bfloat16, 1035, rows=rows)
     assert_linear_close(got, want, h, W, "llama3 down")
+
+
+def test_no_wait_ran_out():
+    """The tile copies of every call above landed within their bounded waits."""
+    x = syn.normal((64, 1536), 0.0, 1.0, torch.bfloat16, 77, 1).to(DEV)
+    w = syn.normal((1536,), 1.0, 0.1, torch.bfloat16, 77, 2).to(DEV)
+    W = syn.linear_weight(2048, 1536, torch.bfloat16, 77).to(DEV)
+    sra.rmsnorm_linear(x, w, W, eps=syn.EPS)
+    torch.cuda.synchronize()
+    assert sra.wait_timeouts() == 0
