@@ -23,7 +23,10 @@ over ranks (each rank runs its own replica: weak scaling).
 Also measured, per kernel: the time of one launch alone (clean L2, one event
 pair: includes the event overhead) and the streaming rate (back-to-back
 launches over rotating copies of its buffers that exceed 4x L2, so every launch
-reads cold data) with its GB/s and fraction of the measured HBM peak; rows/s
+reads cold data, replayed from a CUDA graph so the host's enqueue rate cannot pace
+them) with its GB/s and fraction of the measured HBM peak, and the fraction of
+the launch's floor in a dependent chain (its bytes at that peak plus the measured
+per-launch latency) that it reaches; rows/s
 at decode batch; the launch latency of the smallest launches; row-scaled companion shapes (>= 256 MB of traffic), an
 end-to-end number through the same C ABI from pinned host buffers, and the CPU
 oracle on a bounded sample of the same step (rank 0, one GPU only).
@@ -99,8 +102,9 @@ class Entry:
             return list(k)
         return [k]
 
-    def replicas(self, n):
-        """n launch closures, each on its own device copy of every buffer the launch touches."""
+    def replicas(self, n, stream_handle=None):
+        """n launch closures, each on its own device copy of every buffer the launch touches
+        (and, if given, on another stream: the stream is every call's last argument)."""
         import torch
 
         out = []
@@ -113,6 +117,8 @@ class Entry:
                 hold.append(c)
             args = tuple(remap.get(a, a) if isinstance(a, int) and not isinstance(a, bool) else a
                          for a in self.args)
+            if stream_handle is not None:
+                args = args[:-1] + (stream_handle,)
             fn = self.fn
 
             def call(args=args, hold=hold):
@@ -708,26 +714,40 @@ def run_gpu(args):
             out.append(a.elapsed_time(b))
         return out
 
+    cap_stream = torch.cuda.Stream(dev)
+
+    def graph_of(calls):
+        """The calls (launched on cap_stream) captured into one CUDA graph, so a replay
+        measures the device alone: the host's enqueue rate cannot pace the launches."""
+        with torch.cuda.stream(cap_stream):
+            for c in calls:
+                c()
+        cap_stream.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=cap_stream):
+            for c in calls:
+                c()
+        return g
+
     def time_stream(e):
         """Per-launch time of back-to-back launches, each on its own copy of the
-        buffers; the copies together exceed 4x L2, so every launch reads cold data."""
+        buffers (the copies together exceed 4x L2, so every launch reads cold data),
+        replayed from a CUDA graph."""
         n = int(min(64, max(1, -(-STREAM_BYTES // max(1, e.bytes)))))
-        calls = e.replicas(n) if n > 1 else [e.launch]
+        calls = e.replicas(n, int(cap_stream.cuda_stream))
+        g = graph_of(calls)
         rounds = max(2, 8 // len(calls)) if len(calls) < 8 else 3
-        for c in calls:
-            c()
         per = []
         for _ in range(rounds):
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             clean_l2()
             torch.cuda._sleep(200000)
             a.record(stream)
-            for c in calls:
-                c()
+            g.replay()
             b.record(stream)
             b.synchronize()
             per.append(a.elapsed_time(b) / len(calls))
-        del calls
+        del g, calls
         return statistics.median(per), n
 
     per_kernel = []
@@ -771,23 +791,34 @@ def run_gpu(args):
         xt, wt = xt.to(dev), wt.to(dev)
         ot = torch.empty_like(xt)
         L = sra.lib()
-        targs = (xt.data_ptr(), wt.data_ptr(), ot.data_ptr(), 1, 128, 128, 128, 1e-6, 2, sh)
+        targs = (xt.data_ptr(), wt.data_ptr(), ot.data_ptr(), 1, 128, 128, 128, 1e-6, 2,
+                 int(cap_stream.cuda_stream))
         for mode in (True, False):
             prev = sra.set_pdl(mode)
             n = 200
+            g = graph_of([lambda: L.sra_rmsnorm(*targs)] * n)
             per = []
             for _ in range(3):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                torch.cuda._sleep(int(2e6))
+                torch.cuda._sleep(200000)
                 a.record(stream)
-                for _ in range(n):
-                    L.sra_rmsnorm(*targs)
+                g.replay()
                 b.record(stream)
                 b.synchronize()
                 per.append(a.elapsed_time(b) * 1e3 / n)
             sra.set_pdl(prev)
+            del g
             latency["pdl" if mode else "no_pdl"] = round(statistics.median(per), 3)
-        latency["what"] = "us per launch, 200 back-to-back rmsnorm [1,128] bf16 launches"
+        latency["what"] = ("us per launch, 200 back-to-back rmsnorm [1,128] bf16 launches replayed from a CUDA graph "
+                           "(the per-launch floor of a dependent kernel chain)")
+        # per kernel: the time the launch could take at best in such a chain (its bytes at the
+        # measured copy bandwidth plus that per-launch floor), and the fraction of it reached
+        if pdl:
+            for rec in per_kernel:
+                if "frac_of_peak" in rec and not rec["name"].startswith("chain"):
+                    floor = rec["bytes"] / peak / 1e3 + latency["pdl"]
+                    rec["floor_us"] = round(floor, 3)
+                    rec["frac_of_floor"] = round(floor / rec["us"], 4)
 
     # companions (row-scaled shapes, >= 256 MB traffic), timed alone
     companions = []
