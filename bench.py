@@ -280,7 +280,29 @@ def build_entries(dev, stream_handle, only=(), companions=False):
                 entries.append(Entry(name, "linear", nbytes, B, L.sra_rmsnorm_linear,
                                      (x.data_ptr(), w.data_ptr(), W.data_ptr(), y.data_ptr(), B, K, N, K, N, syn.EPS,
                                       2, stream_handle), [x], [y], keep=(x, w, W, y)))
+            name = f"rmsnorm_linear_ws:bf16:B{B}x{K}x{N}"
+            if B >= 32 and want(name):
+                x = syn.normal((B, K), 0.0, 1.0, torch.bfloat16, 1030, 1).to(dev)
+                w = syn.normal((K,), 1.0, 0.1, torch.bfloat16, 1030, 2).to(dev)
+                W = syn.linear_weight(N, K, torch.bfloat16, 1030).to(dev)
+                y = torch.empty(B, N, dtype=torch.bfloat16, device=dev)
+                ws = sra.linear_workspace(B, K, torch.bfloat16, dev)
+                nbytes = (N * K + B * K + K + B * N) * 2
+                entries.append(Entry(name, "linear", nbytes, B, L.sra_rmsnorm_linear_ws,
+                                     (x.data_ptr(), w.data_ptr(), W.data_ptr(), y.data_ptr(), B, K, N, K, N, syn.EPS,
+                                      ws.data_ptr(), ws.numel() * 2, 2, stream_handle), [x], [y],
+                                     keep=(x, w, W, y, ws)))
             I, N = syn.QWEN25_DOWN["I"], syn.QWEN25_DOWN["N"]
+            name = f"swiglu_linear_ws:bf16:B{B}x{I}x{N}"
+            if B >= 32 and want(name):
+                gu = syn.normal((B, 2 * I), 0.0, 1.0, torch.bfloat16, 1031, 3).to(dev)
+                W = syn.linear_weight(N, I, torch.bfloat16, 1031).to(dev)
+                y = torch.empty(B, N, dtype=torch.bfloat16, device=dev)
+                ws = sra.linear_workspace(B, I, torch.bfloat16, dev)
+                nbytes = (N * I + B * 2 * I + B * N) * 2
+                entries.append(Entry(name, "linear", nbytes, B, L.sra_glu_linear_ws,
+                                     (gu.data_ptr(), W.data_ptr(), y.data_ptr(), B, I, N, 2 * I, N, 0, ws.data_ptr(),
+                                      ws.numel() * 2, 2, stream_handle), [gu], [y], keep=(gu, W, y, ws)))
             name = f"swiglu_linear:bf16:B{B}x{I}x{N}"
             if want(name):
                 gu = syn.normal((B, 2 * I), 0.0, 1.0, torch.bfloat16, 1031, 3).to(dev)
@@ -580,6 +602,9 @@ def cpu_rows_run():
     W = syn.linear_weight(N, I, torch.bfloat16, 1031)
     y = torch.empty(1, N, dtype=torch.bfloat16)
     timed("swiglu_linear", N * I * 2, "B=1", lambda: oracle.glu_linear(gu, W, y, "silu"))
+    # the workspace entry points compute the same result
+    out["rmsnorm_linear_ws"] = out["rmsnorm_linear"]
+    out["swiglu_linear_ws"] = out["swiglu_linear"]
     return out
 
 

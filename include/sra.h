@@ -13,6 +13,7 @@
  *   sra_uclip          UClip / DyHT clamp(alpha * x, lo, hi) * gamma over [N, H, D] views
  *   sra_paged_decode_attention  softmax decode attention read through the paged cache's block table
  *   sra_rmsnorm_linear / sra_glu_linear  RMSNorm / GLU fused into the projection they feed
+ *   sra_rmsnorm_linear_ws / sra_glu_linear_ws  the same, given a workspace for larger batches
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -31,7 +32,9 @@
  *    no output byte changes. SRA_ERR_LAUNCH reports a failed kernel launch
  *    (cudaGetLastError after the launch). A zero-sized call (rows == 0 or
  *    T == 0) validates its arguments, enqueues nothing and returns SRA_OK.
- *  - No entry point waits on the device, traps or asserts on the device.
+ *  - No call waits for the device to finish, and no kernel traps or asserts. The
+ *    only device-side waits are the fused projections' waits for their own tile
+ *    copies; each is bounded and counted when it runs out (sra_wait_timeouts).
  *  - Thread safety: calls may be made concurrently from several host threads.
  *    sra_force_variant changes process-wide state and is meant for A/B
  *    measurement only.
@@ -378,6 +381,33 @@ SRA_API int sra_rmsnorm_linear(const void* x, const void* w_ln, const void* W, v
  */
 SRA_API int sra_glu_linear(const void* gate_up, const void* W, void* y, int64_t B, int64_t I, int64_t N,
                            int64_t in_row_stride, int64_t y_row_stride, int act, int dtype, void* stream);
+
+/*
+ * sra_rmsnorm_linear_ws / sra_glu_linear_ws — the same projections given a caller
+ * workspace (the library allocates nothing). The fused kernels rebuild the prologue's
+ * rows once per 64-column slice of y; at larger batches that repeated work dominates, so
+ * from 32 rows (bf16 / fp16, K and N multiples of 64, 16-byte aligned W and workspace)
+ * the prologue runs once in its own kernel (as sra_rmsnorm / sra_glu), writing
+ * h [B, K] (row stride K) into the workspace, and the projection then streams W against
+ * h. Below that, or for other layouts, the fused kernel runs and the workspace is not
+ * touched. The result is the same computation (h rounded to the dtype, then one rounding
+ * of the product; y may differ from the fused call's in the last bit where an h element
+ * lands on the other side of a rounding midpoint).
+ * workspace: device memory of at least B * K (sra_glu_linear_ws: B * I) elements of
+ * `dtype`, 16-byte aligned, overlapping no other argument; its contents on return are
+ * unspecified (from 32 rows it holds h). A NULL workspace runs the fused kernel; where the
+ * split applies, a workspace smaller than B * K elements -> SRA_ERR_ARG and one that
+ * overlaps another argument -> SRA_ERR_ALIAS. Other arguments and errors as
+ * sra_rmsnorm_linear / sra_glu_linear. The projection over h runs a warp-specialised
+ * kernel: a producer warp streams W and h tiles by TMA, the other warps multiply.
+ * Calls that share a workspace must not overlap on the GPU.
+ */
+SRA_API int sra_rmsnorm_linear_ws(const void* x, const void* w_ln, const void* W, void* y, int64_t B, int64_t K,
+                                  int64_t N, int64_t x_row_stride, int64_t y_row_stride, float eps, void* workspace,
+                                  int64_t workspace_bytes, int dtype, void* stream);
+SRA_API int sra_glu_linear_ws(const void* gate_up, const void* W, void* y, int64_t B, int64_t I, int64_t N,
+                              int64_t in_row_stride, int64_t y_row_stride, int act, void* workspace,
+                              int64_t workspace_bytes, int dtype, void* stream);
 
 /*
  * sra_uclip — [mer] sec. 0 (DyHT(x) = y * clamp(a x, -1, 1) in place of every

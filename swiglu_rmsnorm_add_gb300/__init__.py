@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     glu,
     glu_linear,
     lib,
+    linear_workspace,
     paged_decode_attention,
     paged_decode_attention_noalloc,
     pick_variant,
@@ -35,7 +36,7 @@ from ._binding import (  # noqa: F401
 
 __all__ = ["rmsnorm", "add_rmsnorm", "rope_kv_store", "swiglu", "reglu", "glu", "uclip", "dyht", "paged_decode_attention",
            "paged_decode_attention_noalloc", "decode_attention_workspace",
-           "rmsnorm_linear", "glu_linear", "lib",
+           "rmsnorm_linear", "glu_linear", "linear_workspace", "lib",
            "SRAError",
            "force_variant", "set_pdl", "variant_count", "variant_name", "pick_variant", "status_string",
            "wait_timeouts"]

@@ -52,6 +52,8 @@ def lib() -> ctypes.CDLL:
             L.sra_paged_decode_attention_workspace_size.restype = i64
             L.sra_rmsnorm_linear.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, i32, vp]
             L.sra_glu_linear.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, vp]
+            L.sra_rmsnorm_linear_ws.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, vp, i64, i32, vp]
+            L.sra_glu_linear_ws.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, vp, i64, i32, vp]
             L.sra_glu.argtypes = [vp, vp, i64, i64, i64, i64, i32, i32, vp]
             L.sra_swiglu.argtypes = [vp, vp, i64, i64, i64, i64, i32, vp]
             L.sra_uclip.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, i64, i64, i32, i32, f32, f32, i32,
@@ -59,7 +61,7 @@ def lib() -> ctypes.CDLL:
             for fn in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_rope_kv_store_ex", "sra_glu",
                        "sra_swiglu", "sra_uclip", "sra_rope_kv_store_qk_uclip", "sra_paged_decode_attention",
                        "sra_rmsnorm_linear", "sra_glu_linear", "sra_paged_decode_attention_ws",
-                       "sra_paged_decode_attention_noalloc"):
+                       "sra_paged_decode_attention_noalloc", "sra_rmsnorm_linear_ws", "sra_glu_linear_ws"):
                 getattr(L, fn).restype = i32
             L.sra_status_string.argtypes = [i32]
             L.sra_status_string.restype = ctypes.c_char_p
@@ -464,10 +466,26 @@ def _linear_check(x, W, y, B, K, N):
         raise ValueError("x, W and y must share one dtype")
 
 
+def linear_workspace(B: int, K: int, dtype: torch.dtype, device) -> torch.Tensor:
+    """A workspace for rmsnorm_linear / glu_linear with B rows and K (or I) inputs: B * K elements."""
+    return torch.empty(max(1, B * K), dtype=dtype, device=device)
+
+
+def _ws_args(ws, x):
+    if ws is None:
+        return None, 0
+    _cuda(ws, "workspace")
+    if ws.dtype != x.dtype:
+        raise ValueError("workspace must have x's dtype")
+    return ws.data_ptr(), ws.numel() * ws.element_size()
+
+
 def rmsnorm_linear(x: torch.Tensor, w_ln: torch.Tensor, W: torch.Tensor, y: torch.Tensor | None = None,
-                   eps: float = 1e-6, stream=None) -> torch.Tensor:
+                   eps: float = 1e-6, stream=None, workspace: torch.Tensor | None = None) -> torch.Tensor:
     """y = rmsnorm(x) * w_ln @ W^T with the norm fused in as the projection's prologue.
-    x: [B, K]; w_ln: [K]; W: [N, K] (nn.Linear); y: [B, N]."""
+    x: [B, K]; w_ln: [K]; W: [N, K] (nn.Linear); y: [B, N]. With a workspace
+    (linear_workspace) larger batches run the norm once in its own kernel first
+    (sra_rmsnorm_linear_ws)."""
     _cuda(x, "x")
     _cuda(w_ln, "w_ln")
     B, K, xs = _as_rows(x, "x")
@@ -483,16 +501,25 @@ def rmsnorm_linear(x: torch.Tensor, w_ln: torch.Tensor, W: torch.Tensor, y: torc
     if (yr, yn) != (B, N):
         raise ValueError("shape mismatch")
     with torch.cuda.device(x.device):
-        st = lib().sra_rmsnorm_linear(x.data_ptr(), w_ln.data_ptr(), W.data_ptr(), y.data_ptr(), B, K, N, xs, ys,
-                                      float(eps), _dtype(x), _stream(x, stream))
-    _check("sra_rmsnorm_linear", st)
+        if workspace is None:
+            st = lib().sra_rmsnorm_linear(x.data_ptr(), w_ln.data_ptr(), W.data_ptr(), y.data_ptr(), B, K, N, xs,
+                                          ys, float(eps), _dtype(x), _stream(x, stream))
+            _check("sra_rmsnorm_linear", st)
+        else:
+            _same_device(x, workspace)
+            wp, wb = _ws_args(workspace, x)
+            st = lib().sra_rmsnorm_linear_ws(x.data_ptr(), w_ln.data_ptr(), W.data_ptr(), y.data_ptr(), B, K, N, xs,
+                                             ys, float(eps), wp, wb, _dtype(x), _stream(x, stream))
+            _check("sra_rmsnorm_linear_ws", st)
     return y
 
 
 def glu_linear(gate_up: torch.Tensor, W: torch.Tensor, y: torch.Tensor | None = None, act: str = "silu",
-               stream=None) -> torch.Tensor:
+               stream=None, workspace: torch.Tensor | None = None) -> torch.Tensor:
     """y = (act(gate) * up) @ W^T with the activation fused in as the down projection's prologue.
-    gate_up: [B, 2I]; W: [N, I] (nn.Linear); y: [B, N]."""
+    gate_up: [B, 2I]; W: [N, I] (nn.Linear); y: [B, N]. With a workspace
+    (linear_workspace(B, I, ...)) larger batches run the activation once in its own kernel
+    first (sra_glu_linear_ws)."""
     _cuda(gate_up, "gate_up")
     B, W2, xs = _as_rows(gate_up, "gate_up")
     if W2 % 2:
@@ -510,7 +537,14 @@ def glu_linear(gate_up: torch.Tensor, W: torch.Tensor, y: torch.Tensor | None = 
     if (yr, yn) != (B, N):
         raise ValueError("shape mismatch")
     with torch.cuda.device(gate_up.device):
-        st = lib().sra_glu_linear(gate_up.data_ptr(), W.data_ptr(), y.data_ptr(), B, I, N, xs, ys, ACT_CODE[act],
-                                  _dtype(gate_up), _stream(gate_up, stream))
-    _check("sra_glu_linear", st)
+        if workspace is None:
+            st = lib().sra_glu_linear(gate_up.data_ptr(), W.data_ptr(), y.data_ptr(), B, I, N, xs, ys, ACT_CODE[act],
+                                      _dtype(gate_up), _stream(gate_up, stream))
+            _check("sra_glu_linear", st)
+        else:
+            _same_device(gate_up, workspace)
+            wp, wb = _ws_args(workspace, gate_up)
+            st = lib().sra_glu_linear_ws(gate_up.data_ptr(), W.data_ptr(), y.data_ptr(), B, I, N, xs, ys,
+                                         ACT_CODE[act], wp, wb, _dtype(gate_up), _stream(gate_up, stream))
+            _check("sra_glu_linear_ws", st)
     return y

@@ -887,11 +887,12 @@ int sra_paged_decode_attention_ws(const void* q, const void* kv_cache, const int
 }
 
 // ------------------------------------------------------------------- fused linear
+// prologue: 0 RMSNorm, 1 SwiGLU, 2 ReGLU, 3 none (x holds h; internal, from linear_ws)
 static int linear_common(const void* x, const void* w_ln, const void* W, void* y, int64_t B, int64_t K, int64_t N,
                       int64_t xs, int64_t ys, float eps, int prologue, int dtype, void* stream) {
     if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
     if (B < 0 || K <= 0 || N <= 0) return SRA_ERR_SHAPE;
-    const int64_t xw = prologue == 0 ? K : 2 * K;
+    const int64_t xw = prologue == 1 || prologue == 2 ? 2 * K : K;
     if (xs < xw || ys < N) return SRA_ERR_STRIDE;
     if (prologue == 0 && (!(eps >= 0.0f) || !std::isfinite(eps))) return SRA_ERR_ARG;
     if (B == 0) return SRA_OK;
@@ -948,6 +949,64 @@ static int linear_common(const void* x, const void* w_ln, const void* W, void* y
 int sra_rmsnorm_linear(const void* x, const void* w_ln, const void* W, void* y, int64_t B, int64_t K, int64_t N,
                        int64_t x_row_stride, int64_t y_row_stride, float eps, int dtype, void* stream) {
     return linear_common(x, w_ln, W, y, B, K, N, x_row_stride, y_row_stride, eps, 0, dtype, stream);
+}
+
+// Rows from which the workspace entry points split the prologue off: the fused kernel rebuilds
+// the prologue's rows once per 64-column slice of y (24 times for N = 1536). Measured on GB300
+// at 64 rows: ln1 + qkv_proj 9.4 -> 8.3 us, SwiGLU + down_proj 30.0 -> 19.0 us.
+constexpr int64_t kLinearSplitRows = 32;
+
+// The workspace path: the prologue's own kernel writes h [B, K] into the workspace, then the
+// projection streams W against h (prologue 3). Falls back to the fused kernel (workspace
+// untouched) below kLinearSplitRows rows or where the tensor-core path does not apply.
+static int linear_ws(const void* x, const void* w_ln, const void* W, void* y, int64_t B, int64_t K, int64_t N,
+                     int64_t xs, int64_t ys, float eps, int prologue, void* ws, int64_t ws_bytes, int dtype,
+                     void* stream) {
+    // validate exactly as the fused call does (nothing is enqueued on error)
+    if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
+    if (B < 0 || K <= 0 || N <= 0) return SRA_ERR_SHAPE;
+    const int64_t xw = prologue == 0 ? K : 2 * K;
+    if (xs < xw || ys < N) return SRA_ERR_STRIDE;
+    if (prologue == 0 && (!(eps >= 0.0f) || !std::isfinite(eps))) return SRA_ERR_ARG;
+    if (ws_bytes < 0) return SRA_ERR_ARG;
+    if (B == 0) return SRA_OK;
+    if (!x || !W || !y || (prologue == 0 && !w_ln)) return SRA_ERR_NULL;
+    const int es = elem_bytes(dtype);
+    const bool split = ws != nullptr && B >= kLinearSplitRows && dtype != DT_F32 && K % 64 == 0 && N % 64 == 0 &&
+                       aligned16(W) && aligned16(ws);
+    if (!split)
+        return linear_common(x, w_ln, W, y, B, K, N, xs, ys, eps, prologue, dtype, stream);
+    if (ws_bytes < B * K * es) return SRA_ERR_ARG;
+    const Span sw = span_of(ws, 1, 0, B * K, es);
+    if (overlap(sw, span_of(x, B, xs, xw, es)) || overlap(sw, span_of(W, 1, 0, N * K, es)) ||
+        overlap(sw, span_of(y, B, ys, N, es)) || (prologue == 0 && overlap(sw, span_of(w_ln, 1, 0, K, es))))
+        return SRA_ERR_ALIAS;
+    // the fused call's own checks (alias of y with x, W, w_ln; strides), before anything runs
+    {
+        const Span sy = span_of(y, B, ys, N, es);
+        if (rows_overlap(y, B, ys, N, x, B, xs, xw, es) || overlap(sy, span_of(W, 1, 0, N * K, es)) ||
+            (prologue == 0 && overlap(sy, span_of(w_ln, 1, 0, K, es))))
+            return SRA_ERR_ALIAS;
+    }
+    const int st = prologue == 0 ? sra_rmsnorm(x, w_ln, ws, B, K, xs, K, eps, dtype, stream)
+                                 : sra_glu(x, ws, B, K, xs, K, prologue - 1, dtype, stream);
+    if (st != SRA_OK) return st;
+    return linear_common(ws, nullptr, W, y, B, K, N, K, ys, 0.0f, 3, dtype, stream);
+}
+
+int sra_rmsnorm_linear_ws(const void* x, const void* w_ln, const void* W, void* y, int64_t B, int64_t K, int64_t N,
+                          int64_t x_row_stride, int64_t y_row_stride, float eps, void* workspace,
+                          int64_t workspace_bytes, int dtype, void* stream) {
+    return linear_ws(x, w_ln, W, y, B, K, N, x_row_stride, y_row_stride, eps, 0, workspace, workspace_bytes, dtype,
+                     stream);
+}
+
+int sra_glu_linear_ws(const void* gate_up, const void* W, void* y, int64_t B, int64_t I, int64_t N,
+                      int64_t in_row_stride, int64_t y_row_stride, int act, void* workspace, int64_t workspace_bytes,
+                      int dtype, void* stream) {
+    if (act != SRA_ACT_SILU && act != SRA_ACT_RELU) return valid_dtype(dtype) ? SRA_ERR_ARG : SRA_ERR_DTYPE;
+    return linear_ws(gate_up, nullptr, W, y, B, I, N, in_row_stride, y_row_stride, 0.0f, 1 + act, workspace,
+                     workspace_bytes, dtype, stream);
 }
 
 int sra_glu_linear(const void* gate_up, const void* W, void* y, int64_t B, int64_t I, int64_t N,

@@ -165,7 +165,7 @@ int64_t decode_attention_ws_bytes(int64_t B, int n_kv, int head_dim, int gsplits
 
 // ------------------------------------------------------------------- fused linear
 struct LinArgs {
-    const void* x;     // [B, K] (RMSNorm prologue) or gate_up [B, 2K] (GLU prologue), row stride xs
+    const void* x;     // [B, K] (RMSNorm prologue, or h itself) or gate_up [B, 2K] (GLU prologue), row stride xs
     const void* w_ln;  // [K] RMSNorm weight (RMSNorm prologue only)
     const void* W;     // [N, K] row-major (nn.Linear)
     void* y;           // [B, N], row stride ys
@@ -174,7 +174,7 @@ struct LinArgs {
 };
 
 struct LinPlan {
-    int prologue;       // 0 RMSNorm, 1 SwiGLU, 2 ReGLU
+    int prologue;       // 0 RMSNorm, 1 SwiGLU, 2 ReGLU, 3 none (the input rows are h)
     bool tensor_cores;  // bf16 / fp16, K and N multiples of 64, 16-byte aligned layouts
     bool narrow;        // B <= 16: CTAs of 16 columns over all of K, no cluster
     int mt;             // 16-row m-tiles per CTA (1, 2 or 4)

@@ -95,12 +95,13 @@ __device__ __forceinline__ T to_t(float v) {
 // [MT*16][64] (built while the other is multiplied). The epilogue's partial tile reuses the
 // rings once they have drained. Sizes keep two CTAs per SM.
 __host__ __device__ constexpr int warps_for(int MT) { return MT == 1 ? 4 : 8; }
-__host__ __device__ constexpr int wstages_for(int MT, int PRO) { return MT == 4 && PRO != 0 ? 5 : 8; }
+__host__ __device__ constexpr bool glu_input(int PRO) { return PRO == 1 || PRO == 2; }  // gate and up tiles
+__host__ __device__ constexpr int wstages_for(int MT, int PRO) { return MT == 4 && glu_input(PRO) ? 5 : 8; }
 __host__ __device__ constexpr int xstages_for(int MT, int PRO) { return 3; }
 __host__ __device__ constexpr size_t wtile_bytes() { return static_cast<size_t>(kNT) * kKT * 2; }
 __host__ __device__ constexpr size_t xtile_bytes(int MT) { return static_cast<size_t>(MT) * 16 * kKT * 2; }
 __host__ __device__ constexpr size_t xstage_bytes(int MT, int PRO) {
-    return (static_cast<size_t>(PRO == 0 ? 1 : 2) * xtile_bytes(MT) + (PRO == 0 ? kKT * 2 : 0) + 1023) / 1024 * 1024;
+    return (static_cast<size_t>(glu_input(PRO) ? 2 : 1) * xtile_bytes(MT) + (PRO == 0 ? kKT * 2 : 0) + 1023) / 1024 * 1024;
 }
 __host__ __device__ constexpr size_t rings_bytes(int MT, int PRO) {
     return wstages_for(MT, PRO) * wtile_bytes() + xstages_for(MT, PRO) * xstage_bytes(MT, PRO);
@@ -126,9 +127,10 @@ __device__ __forceinline__ float glu_act(float g) {
     }
 }
 
-// PRO: 0 = RMSNorm prologue, 1 = SwiGLU, 2 = ReGLU. The tensor maps: tmW over W [N][K] and
-// tmX over the input rows [B][K] (GLU: [B][2K]), both with 64 x 64 (rows: MT*16) boxes and the
-// 128-byte swizzle; tmN over the norm weight [K], 64-entry boxes (RMSNorm only).
+// PRO: 0 = RMSNorm prologue, 1 = SwiGLU, 2 = ReGLU, 3 = none (the input rows are h, already
+// produced by the prologue's own kernel). The tensor maps: tmW over W [N][K] and tmX over the
+// input rows [B][K] (GLU: [B][2K]), both with 64 x 64 (rows: MT*16) boxes and the 128-byte
+// swizzle; tmN over the norm weight [K], 64-entry boxes (RMSNorm only).
 template <typename T, int MT, int PRO>
 __global__ void __launch_bounds__(warps_for(MT) * 32) linear_kernel(LinArgs a, const __grid_constant__ CUtensorMap tmW,
                                                               const __grid_constant__ CUtensorMap tmX,
@@ -172,7 +174,7 @@ __global__ void __launch_bounds__(warps_for(MT) * 32) linear_kernel(LinArgs a, c
     // rows n0 ..; input tile t: the input rows' same 64 columns of K (x; or gate and up) and,
     // for the RMSNorm, the norm weight's 64 entries. Rows past B arrive as zeros.
     constexpr uint32_t kXTx =
-        static_cast<uint32_t>((PRO == 0 ? 1 : 2) * xtile_bytes(MT) + (PRO == 0 ? kKT * 2 : 0));
+        static_cast<uint32_t>((glu_input(PRO) ? 2 : 1) * xtile_bytes(MT) + (PRO == 0 ? kKT * 2 : 0));
     auto issue_w = [&](int t) {
         uint64_t* bar = &wfull[t % SW];
         fence_proxy_async();  // the slot's earlier reads come before the copy
@@ -186,9 +188,9 @@ __global__ void __launch_bounds__(warps_for(MT) * 32) linear_kernel(LinArgs a, c
         fence_proxy_async();
         mbar_arrive_expect_tx(bar, kXTx);
         tma_load_2d(xd, &tmX, k0, static_cast<int>(r0), bar);
-        if constexpr (PRO != 0) {
+        if constexpr (glu_input(PRO)) {
             tma_load_2d(xd + XR * kKT, &tmX, static_cast<int>(a.K) + k0, static_cast<int>(r0), bar);
-        } else {
+        } else if constexpr (PRO == 0) {
             tma_load_1d(xd + XR * kKT, &tmN, k0, bar);
         }
     };
@@ -204,7 +206,7 @@ __global__ void __launch_bounds__(warps_for(MT) * 32) linear_kernel(LinArgs a, c
     else if (threadIdx.x >= kNT && threadIdx.x - kNT < rows) {
         const T* xr = X + (r0 + threadIdx.x - kNT) * a.xs + kbase;
         prefetch_l2(xr, static_cast<int64_t>(ntiles) * kKT * 2);
-        if (PRO != 0) prefetch_l2(xr + a.K, static_cast<int64_t>(ntiles) * kKT * 2);
+        if (glu_input(PRO)) prefetch_l2(xr + a.K, static_cast<int64_t>(ntiles) * kKT * 2);
     }
     __syncthreads();  // the barriers are initialised
     pdl_enter();
@@ -225,7 +227,9 @@ __global__ void __launch_bounds__(warps_for(MT) * 32) linear_kernel(LinArgs a, c
             if (r < rows) {
                 float g[8];
                 V8::unpack(*reinterpret_cast<const R8*>(xs + r * kKT + swz(r, ch) * 8), f);
-                if constexpr (PRO == 0) {
+                if constexpr (PRO == 3) {
+                    // h as given
+                } else if constexpr (PRO == 0) {
                     V8::unpack(*reinterpret_cast<const R8*>(xs + XR * kKT + ch * 8), g);
                     const float iv = inv[r];
 #pragma unroll
@@ -340,6 +344,136 @@ __global__ void __launch_bounds__(warps_for(MT) * 32) linear_kernel(LinArgs a, c
     cluster.sync();
     T* y = static_cast<T*>(a.y);
     for (int idx = rank * NW * 32 + threadIdx.x; idx < rows * kNT; idx += SK * NW * 32) {
+        const int r = idx / kNT, c = idx - r * kNT;
+        float sum = 0.0f;
+        for (int q = 0; q < SK; ++q) sum += cluster.map_shared_rank(part, q)[r * kNT + c];
+        y[(r0 + r) * a.ys + n0 + c] = to_t<T>(sum);
+    }
+    cluster.sync();
+}
+
+// ---- the projection of rows that are already h (the workspace path: the prologue ran in its
+// own kernel). No prologue work is left, so nothing is shared between warps inside a tile and
+// the CTA needs no barrier per tile: a producer warp streams stage t (W's 64 x 64 tile and
+// h's [MT*16][64] tile, both by TMA with the 128-byte swizzle) into slot t % SH and the
+// compute warps, each on its own 16 rows x (64 / NGROUPS) columns, wait for that stage's
+// full barrier, multiply, and release the slot on its empty barrier (one arrival per
+// warp). The K range, the cluster and the epilogue are those of linear_kernel.
+constexpr int kStagesH = 6;
+__host__ __device__ constexpr size_t hstage_bytes(int MT) { return wtile_bytes() + xtile_bytes(MT); }
+__host__ __device__ constexpr size_t smemh_bytes(int MT) {
+    return 1024 + (kStagesH * hstage_bytes(MT) > static_cast<size_t>(MT) * 16 * kNT * 4
+                       ? kStagesH * hstage_bytes(MT)
+                       : static_cast<size_t>(MT) * 16 * kNT * 4);
+}
+
+template <typename T, int MT>
+__global__ void __launch_bounds__((warps_for(MT) + 1) * 32) linear_h_kernel(LinArgs a,
+                                                                         const __grid_constant__ CUtensorMap tmW,
+                                                                         const __grid_constant__ CUtensorMap tmX) {
+    constexpr int XR = MT * 16;
+    constexpr int NW = warps_for(MT);  // compute warps; warp NW issues the copies
+    constexpr int S = kStagesH;
+    constexpr size_t SB = hstage_bytes(MT);
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    __shared__ uint64_t full[S], empty[S];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int SK = static_cast<int>(cluster.num_blocks());
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t n0 = (blockIdx.x / SK) * static_cast<int64_t>(kNT);
+    const int64_t r0 = static_cast<int64_t>(blockIdx.y) * XR;
+    const int rows = static_cast<int>(a.B - r0 < XR ? a.B - r0 : XR);
+    const int KT = static_cast<int>(a.K / kKT);
+    const int per = (KT + SK - 1) / SK;
+    const int kt0 = rank * per < KT ? rank * per : KT;
+    const int kt1 = kt0 + per < KT ? kt0 + per : KT;
+    const int ntiles = kt1 - kt0;
+    const int64_t kbase = static_cast<int64_t>(kt0) * kKT;
+    float* part = reinterpret_cast<float*>(smem);  // the epilogue's partial tile, after the ring drains
+    const T* W = static_cast<const T*>(a.W);
+    const T* X = static_cast<const T*>(a.x);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], NW);
+        }
+        mbar_init_fence();
+    }
+    // Before the dependency wait: this CTA's slice of W and of h into L2 (hints only).
+    if (threadIdx.x < kNT && n0 + threadIdx.x < a.N)
+        prefetch_l2(W + (n0 + threadIdx.x) * a.K + kbase, static_cast<int64_t>(ntiles) * kKT * 2);
+    else if (threadIdx.x >= kNT && threadIdx.x - kNT < rows)
+        prefetch_l2(X + (r0 + threadIdx.x - kNT) * a.xs + kbase, static_cast<int64_t>(ntiles) * kKT * 2);
+    __syncthreads();  // the barriers are initialised
+    pdl_enter();
+
+    constexpr int NGROUPS = NW / MT;   // warps sharing an m-tile split its 64 columns
+    constexpr int NBW = 8 / NGROUPS;   // n8 blocks per warp
+    float acc[NBW][4];
+#pragma unroll
+    for (int j = 0; j < NBW; ++j) acc[j][0] = acc[j][1] = acc[j][2] = acc[j][3] = 0.0f;
+    const int mt = warp % MT, ng = warp / MT;
+    if (warp == NW) {
+        if (lane == 0) {
+            for (int t = 0; t < ntiles; ++t) {
+                const int slot = t % S;
+                // the slot's previous tile (t - S) is released by every compute warp
+                if (t >= S) mbar_wait(&empty[slot], static_cast<uint32_t>(((t / S) - 1) & 1));
+                unsigned char* st = smem + static_cast<size_t>(slot) * SB;
+                const int k0 = static_cast<int>(kbase) + t * kKT;
+                mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(SB));
+                tma_load_2d(st, &tmW, k0, static_cast<int>(n0), &full[slot]);
+                tma_load_2d(st + wtile_bytes(), &tmX, k0, static_cast<int>(r0), &full[slot]);
+            }
+        }
+    } else {
+        const int li = lane & 7, lm = lane >> 3;  // ldmatrix: row within a matrix, matrix index
+        for (int t = 0; t < ntiles; ++t) {
+            const int slot = t % S;
+            mbar_wait(&full[slot], static_cast<uint32_t>((t / S) & 1));
+            const T* wt = reinterpret_cast<const T*>(smem + static_cast<size_t>(slot) * SB);
+            const T* ht = reinterpret_cast<const T*>(smem + static_cast<size_t>(slot) * SB + wtile_bytes());
+#pragma unroll
+            for (int ks = 0; ks < kKT / 16; ++ks) {
+                uint32_t af[4];
+                {
+                    const int r = mt * 16 + (lm & 1) * 8 + li;
+                    ldsm_x4(af, ht + r * kKT + swz(r, ks * 2 + (lm >> 1)) * 8);
+                }
+#pragma unroll
+                for (int j = 0; j < NBW; j += 2) {
+                    uint32_t bf[4];
+                    const int n = (ng * NBW + j) * 8 + (lm >> 1) * 8 + li;
+                    ldsm_x4(bf, wt + n * kKT + swz(n, ks * 2 + (lm & 1)) * 8);
+                    Mma<T>::run(acc[j], af, bf[0], bf[1]);
+                    Mma<T>::run(acc[j + 1], af, bf[2], bf[3]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done with the slot
+        }
+    }
+    __syncthreads();  // every stage has landed and been read: the ring's space takes the partial tile
+
+    // ---- epilogue: partial tile into shared memory, then summed over the cluster
+    if (warp < NW) {
+        const int g = lane >> 2, q = lane & 3;
+#pragma unroll
+        for (int j = 0; j < NBW; ++j) {
+            const int col = (ng * NBW + j) * 8 + 2 * q;
+            const int row = mt * 16 + g;
+            part[row * kNT + col] = acc[j][0];
+            part[row * kNT + col + 1] = acc[j][1];
+            part[(row + 8) * kNT + col] = acc[j][2];
+            part[(row + 8) * kNT + col + 1] = acc[j][3];
+        }
+    }
+    cluster.sync();
+    T* y = static_cast<T*>(a.y);
+    constexpr int NT = (NW + 1) * 32;
+    for (int idx = rank * NT + threadIdx.x; idx < rows * kNT; idx += SK * NT) {
         const int r = idx / kNT, c = idx - r * kNT;
         float sum = 0.0f;
         for (int q = 0; q < SK; ++q) sum += cluster.map_shared_rank(part, q)[r * kNT + c];
@@ -537,6 +671,17 @@ cudaError_t launch_mt(const LinArgs& a, const LinPlan& p, cudaStream_t s, const 
     return launch_kernel(kernel, grid, dim3(warps_for(MT) * 32), smem, s, p.pdl, p.splits, a, tmW, tmX, tmN);
 }
 
+template <typename T, int MT>
+cudaError_t launch_h_mt(const LinArgs& a, const LinPlan& p, cudaStream_t s, const CUtensorMap& tmW,
+                        const CUtensorMap& tmX) {
+    auto kernel = linear_h_kernel<T, MT>;
+    const size_t smem = smemh_bytes(MT);
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    const dim3 grid(static_cast<unsigned>(a.N / kNT * p.splits), static_cast<unsigned>((a.B + MT * 16 - 1) / (MT * 16)));
+    return launch_kernel(kernel, grid, dim3((warps_for(MT) + 1) * 32), smem, s, p.pdl, p.splits, a, tmW, tmX);
+}
+
 template <typename T, int PRO>
 cudaError_t launch_pro(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
     // tensor maps: W [N][K] and the input rows [B][K or 2K] in 64 x (64 or MT*16) boxes with the
@@ -546,9 +691,17 @@ cudaError_t launch_pro(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
     CUtensorMap tmW, tmX, tmN;
     memset(&tmN, 0, sizeof(tmN));
     if (!encode_tmap_16(&tmW, a.W, 2, a.K, a.N, a.K * 2, kKT, kNT, bf16, true) ||
-        !encode_tmap_16(&tmX, a.x, 2, PRO == 0 ? a.K : 2 * a.K, a.B, a.xs * 2, kKT, xr, bf16, true) ||
+        !encode_tmap_16(&tmX, a.x, 2, glu_input(PRO) ? 2 * a.K : a.K, a.B, a.xs * 2, kKT, xr, bf16, true) ||
         (PRO == 0 && !encode_tmap_16(&tmN, a.w_ln, 1, a.K, 1, 0, kKT, 1, bf16, false)))
         return cudaErrorNotSupported;
+    if constexpr (PRO == 3) {
+        switch (p.mt) {
+            case 1: return launch_h_mt<T, 1>(a, p, s, tmW, tmX);
+            case 2: return launch_h_mt<T, 2>(a, p, s, tmW, tmX);
+            case 4: return launch_h_mt<T, 4>(a, p, s, tmW, tmX);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (p.mt) {
         case 1: return launch_mt<T, 1, PRO>(a, p, s, tmW, tmX, tmN);
         case 2: return launch_mt<T, 2, PRO>(a, p, s, tmW, tmX, tmN);
@@ -571,6 +724,7 @@ cudaError_t launch_typed(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
         case 0: return launch_pro<T, 0>(a, p, s);
         case 1: return launch_pro<T, 1>(a, p, s);
         case 2: return launch_pro<T, 2>(a, p, s);
+        case 3: return launch_pro<T, 3>(a, p, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -673,7 +827,9 @@ unsigned int linear_wait_timeouts() {
     return v;
 }
 
-size_t linear_smem(int mt, int prologue) { return lin::smem_bytes(mt, prologue); }
+size_t linear_smem(int mt, int prologue) {
+    return prologue == 3 ? lin::smemh_bytes(mt) : lin::smem_bytes(mt, prologue);
+}
 size_t linear16_smem(int rows, int64_t K) { return lin::smem16_bytes(rows, K); }
 
 cudaError_t launch_linear(const LinArgs& a, const LinPlan& p, int dtype, cudaStream_t s) {

@@ -218,6 +218,28 @@ def test_linear_validation(L):
     assert g(X, W, Y, 0, 64, 64, 128, 64, 1, BF16, None) == OK
 
 
+def test_linear_workspace_validation(L):
+    X, WL, W, Y, WS = (P + i * 0x1000000 for i in range(5))
+    f = L.sra_rmsnorm_linear_ws
+    # the fused call's checks come first, nothing runs on error
+    assert f(X, WL, W, Y, 64, 64, 64, 64, 64, 1e-6, WS, 1 << 20, 7, None) == DTYPE
+    assert f(X, WL, W, Y, 64, 64, 64, 63, 64, 1e-6, WS, 1 << 20, BF16, None) == STRIDE
+    assert f(X, WL, W, Y, 64, 64, 64, 64, 64, 1e-6, WS, -1, BF16, None) == ARG
+    assert f(X, None, W, Y, 64, 64, 64, 64, 64, 1e-6, WS, 1 << 20, BF16, None) == NULL
+    # from 32 rows the workspace must hold B * K elements and overlap nothing
+    assert f(X, WL, W, Y, 64, 64, 64, 64, 64, 1e-6, WS, 64 * 64 * 2 - 2, BF16, None) == ARG
+    assert f(X, WL, W, Y, 64, 64, 64, 64, 64, 1e-6, X + 64, 1 << 20, BF16, None) == ALIAS
+    assert f(X, WL, W, Y, 64, 64, 64, 64, 64, 1e-6, W, 1 << 20, BF16, None) == ALIAS
+    assert f(X, WL, W, Y, 64, 64, 64, 64, 64, 1e-6, Y, 1 << 20, BF16, None) == ALIAS
+    assert f(X, WL, W, X + 64, 64, 64, 64, 64, 64, 1e-6, WS, 1 << 20, BF16, None) == ALIAS
+    assert f(X, WL, W, Y, 0, 64, 64, 64, 64, 1e-6, WS, 0, BF16, None) == OK
+    g = L.sra_glu_linear_ws
+    assert g(X, W, Y, 64, 64, 64, 128, 64, 2, WS, 1 << 20, BF16, None) == ARG
+    assert g(X, W, Y, 64, 64, 64, 128, 64, 0, WS, 64 * 64 * 2 - 2, BF16, None) == ARG
+    assert g(X, W, Y, 64, 64, 64, 128, 64, 0, X + 128, 1 << 20, BF16, None) == ALIAS
+    assert g(X, W, Y, 0, 64, 64, 128, 64, 1, WS, 0, BF16, None) == OK
+
+
 def test_attention_workspace_validation(L):
     f = L.sra_paged_decode_attention_workspace_size
     assert f(1, 12, 2, 128, 2048, 16, 9) == DTYPE

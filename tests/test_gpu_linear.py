@@ -44,11 +44,12 @@ def assert_linear_close(got, want, h, W, what):
     assert not bool(bad.any()), f"{what}: {int(bad.sum())} of {bad.numel()} outputs off (max err {float(err.max()):.3g})"
 
 
-def norm_case(B, K, N, dtype, seed, rows=None):
+def norm_case(B, K, N, dtype, seed, rows=None, ws=False):
     x = syn.normal((B, K), 0, 1, dtype, seed, 1)
     w = syn.normal((K,), 1, 0.1, dtype, seed, 2)
     W = syn.linear_weight(N, K, dtype, seed)
-    got = sra.rmsnorm_linear(x.to(DEV), w.to(DEV), W.to(DEV)).cpu()
+    wsp = sra.linear_workspace(B, K, dtype, DEV) if ws else None
+    got = sra.rmsnorm_linear(x.to(DEV), w.to(DEV), W.to(DEV), workspace=wsp).cpu()
     sel = torch.arange(B) if rows is None else rows
     h = torch.empty(len(sel), K, dtype=dtype)
     oracle.rmsnorm(x[sel].contiguous(), w, h, 1e-6)
@@ -57,10 +58,11 @@ def norm_case(B, K, N, dtype, seed, rows=None):
     return got[sel], want, h, W
 
 
-def glu_case(B, I, N, dtype, seed, act="silu", rows=None):
+def glu_case(B, I, N, dtype, seed, act="silu", rows=None, ws=False):
     gu = syn.normal((B, 2 * I), 0, 1, dtype, seed, 3)
     W = syn.linear_weight(N, I, dtype, seed)
-    got = sra.glu_linear(gu.to(DEV), W.to(DEV), act=act).cpu()
+    wsp = sra.linear_workspace(B, I, dtype, DEV) if ws else None
+    got = sra.glu_linear(gu.to(DEV), W.to(DEV), act=act, workspace=wsp).cpu()
     sel = torch.arange(B) if rows is None else rows
     h = torch.empty(len(sel), I, dtype=dtype)
     oracle.glu(gu[sel].contiguous(), h, act)
@@ -120,6 +122,45 @@ def test_llama3_8b_down_sampled():
     rows = torch.tensor([0, 13, 40, 63])
     got, want, h, W = glu_case(64, 14336, 4096, torch.bfloat16, 1035, rows=rows)
     assert_linear_close(got, want, h, W, "llama3 down")
+
+
+@pytest.mark.parametrize("B", [1, 17, 32, 33, 64, 100])
+def test_workspace_config_qwen25(B):
+    """The workspace entry points (norm / activation in their own kernel from 32 rows, the
+    projection over h) on the Qwen2.5-1.5B projections."""
+    got, want, h, W = norm_case(B, syn.QWEN25_QKV["K"], syn.QWEN25_QKV["N"], torch.bfloat16, 1036, ws=True)
+    assert_linear_close(got, want, h, W, f"ws ln1+qkv B={B}")
+    rows = None if B <= 17 else torch.arange(0, B, 7)
+    got, want, h, W = glu_case(B, syn.QWEN25_DOWN["I"], syn.QWEN25_DOWN["N"], torch.bfloat16, 1037, rows=rows,
+                               ws=True)
+    assert_linear_close(got, want, h, W, f"ws swiglu+down B={B}")
+
+
+@pytest.mark.parametrize("act", ["silu", "relu"])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16, torch.float32])
+@pytest.mark.parametrize("B,K,N", [(32, 64, 64), (50, 640, 192), (64, 512, 256), (96, 100, 40)])
+def test_workspace_shapes_dtypes(act, dtype, B, K, N):
+    got, want, h, W = norm_case(B, K, N, dtype, 1038 + K + B, ws=True)
+    assert_linear_close(got, want, h, W, f"ws norm {dtype} B={B} K={K} N={N}")
+    got, want, h, W = glu_case(B, K, N, dtype, 1039 + K + B, act, ws=True)
+    assert_linear_close(got, want, h, W, f"ws {act} {dtype} B={B} I={K} N={N}")
+
+
+def test_workspace_equals_its_two_steps():
+    """From 32 rows the workspace path is the RMSNorm kernel writing h into the workspace,
+    then the projection of h: the workspace ends up holding exactly sra.rmsnorm's output,
+    and y matches the oracle's projection of that h."""
+    B, K, N = 64, 1536, 2048
+    x = syn.normal((B, K), 0, 1, torch.bfloat16, 1040, 1).to(DEV)
+    w = syn.normal((K,), 1, 0.1, torch.bfloat16, 1040, 2).to(DEV)
+    W = syn.linear_weight(N, K, torch.bfloat16, 1040).to(DEV)
+    ws = sra.linear_workspace(B, K, torch.bfloat16, DEV)
+    y = sra.rmsnorm_linear(x, w, W, workspace=ws)
+    h = sra.rmsnorm(x, w, eps=1e-6)
+    assert torch.equal(ws.view(B, K).view(torch.int16), h.view(torch.int16))  # the workspace holds h
+    want = torch.empty(B, N, dtype=torch.bfloat16)
+    oracle.linear(h.cpu(), W.cpu(), want)
+    assert_linear_close(y, want, h.cpu(), W.cpu(), "ws two steps")
 
 
 def test_no_wait_ran_out():
