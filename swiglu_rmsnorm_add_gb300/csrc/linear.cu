@@ -435,24 +435,29 @@ __global__ void __launch_bounds__((warps_for(MT) + 1) * 32) linear_h_kernel(LinA
             mbar_wait(&full[slot], static_cast<uint32_t>((t / S) & 1));
             const T* wt = reinterpret_cast<const T*>(smem + static_cast<size_t>(slot) * SB);
             const T* ht = reinterpret_cast<const T*>(smem + static_cast<size_t>(slot) * SB + wtile_bytes());
+            // every fragment of the tile first, then the products: the shared-memory loads
+            // overlap instead of each waiting for the products before it
+            uint32_t af[kKT / 16][4], bf[kKT / 16][NBW / 2][4];
 #pragma unroll
             for (int ks = 0; ks < kKT / 16; ++ks) {
-                uint32_t af[4];
-                {
-                    const int r = mt * 16 + (lm & 1) * 8 + li;
-                    ldsm_x4(af, ht + r * kKT + swz(r, ks * 2 + (lm >> 1)) * 8);
-                }
+                const int r = mt * 16 + (lm & 1) * 8 + li;
+                ldsm_x4(af[ks], ht + r * kKT + swz(r, ks * 2 + (lm >> 1)) * 8);
 #pragma unroll
                 for (int j = 0; j < NBW; j += 2) {
-                    uint32_t bf[4];
                     const int n = (ng * NBW + j) * 8 + (lm >> 1) * 8 + li;
-                    ldsm_x4(bf, wt + n * kKT + swz(n, ks * 2 + (lm & 1)) * 8);
-                    Mma<T>::run(acc[j], af, bf[0], bf[1]);
-                    Mma<T>::run(acc[j + 1], af, bf[2], bf[3]);
+                    ldsm_x4(bf[ks][j / 2], wt + n * kKT + swz(n, ks * 2 + (lm & 1)) * 8);
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);  // this warp is done with the slot
+            if (lane == 0) mbar_arrive(&empty[slot]);  // the fragments are in registers: the slot is free
+#pragma unroll
+            for (int ks = 0; ks < kKT / 16; ++ks) {
+#pragma unroll
+                for (int j = 0; j < NBW; j += 2) {
+                    Mma<T>::run(acc[j], af[ks], bf[ks][j / 2][0], bf[ks][j / 2][1]);
+                    Mma<T>::run(acc[j + 1], af[ks], bf[ks][j / 2][2], bf[ks][j / 2][3]);
+                }
+            }
         }
     }
     __syncthreads();  // every stage has landed and been read: the ring's space takes the partial tile
