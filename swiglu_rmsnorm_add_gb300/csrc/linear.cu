@@ -9,19 +9,24 @@
 // store them, before they meet W.
 //
 // At decode batch sizes the cost is the weight read (N * K * 2 bytes per call),
-// so the layout streams W once: a CTA owns a 64-column slice of y for up to 64
-// rows, the K dimension is split over the CTAs of a thread-block cluster, and
-// the partial products are summed through distributed shared memory (no global
-// scratch). Inside a CTA, W tiles of 64 x 64 stream through an 8-deep cp.async
-// ring, and h is produced tile by tile next to them: the inputs of the next
-// tile are loaded into registers while the current one is multiplied, then
-// normed (or activated), rounded to T and stored into the other of two h
-// buffers. For the RMSNorm each CTA first sums the squares of its K range and
-// the cluster exchanges the partial sums, so every row's statistic is complete
-// before the first tile. The products run on the tensor cores
-// as mma.sync m16n8k16 with fp32 accumulators (h as the A operand through
-// ldmatrix, W tiles as the B operand through ldmatrix, 16-byte chunks
-// XOR-swizzled by row against bank conflicts).
+// so W is streamed once. Three kernels:
+//  - linear16_kernel (up to 16 rows): a CTA owns 16 columns of y over the whole
+//    of K; its warps split K, stream their W tiles through private cp.async
+//    rings, and h for all of K is built once up front.
+//  - linear_kernel (more rows): a CTA owns a 64-column slice of y for 16, 32 or
+//    64 rows, K is split over the CTAs of a thread-block cluster and the partial
+//    products are summed through distributed shared memory (no global scratch).
+//    W tiles and the prologue's input tiles arrive by TMA tensor copies (128-byte
+//    swizzle) into two mbarrier rings, W's deep (from DRAM) and the input's short
+//    (from L2); h is built tile by tile from the input tiles into one of two h
+//    buffers while the other is multiplied. For the RMSNorm each CTA first sums
+//    the squares of its K range and the cluster exchanges the partial sums.
+//  - linear_h_kernel (the workspace path, where the prologue ran in its own
+//    kernel): a producer warp streams W and h tiles by TMA, the other warps
+//    multiply and release each slot on an empty barrier; no CTA barrier per tile.
+// The products run on the tensor cores as mma.sync m16n8k16 with fp32
+// accumulators (h as the A operand, W tiles as the B operand, both through
+// ldmatrix from swizzled shared memory).
 #include <cooperative_groups.h>
 
 #include <type_traits>
