@@ -465,6 +465,14 @@ SRA_API int sra_last_cuda_error(void);
 SRA_API unsigned int sra_wait_timeouts(void);
 
 /*
+ * Self-test of that bound: one GPU thread waits on a shared-memory barrier that nothing
+ * completes. The wait gives up after about a second, the kernel writes 0 to *result
+ * (device int32; 1 would mean the barrier completed) and sra_wait_timeouts() grows by
+ * one. Enqueued on `stream`; NULL result -> SRA_ERR_NULL. No paper section defines it.
+ */
+SRA_API int sra_wait_selftest(int32_t* result, void* stream);
+
+/*
  * Programmatic dependent launch for the CALLING THREAD's subsequent calls
  * (enable != 0: on; 0: off, the default). When on, each kernel is launched with
  * programmatic stream serialization: the GPU may schedule it while the kernel

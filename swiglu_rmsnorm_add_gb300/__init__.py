@@ -31,6 +31,7 @@ from ._binding import (  # noqa: F401
     uclip,
     variant_count,
     variant_name,
+    wait_selftest,
     wait_timeouts,
 )
 
@@ -39,4 +40,4 @@ __all__ = ["rmsnorm", "add_rmsnorm", "rope_kv_store", "swiglu", "reglu", "glu", 
            "rmsnorm_linear", "glu_linear", "linear_workspace", "lib",
            "SRAError",
            "force_variant", "set_pdl", "variant_count", "variant_name", "pick_variant", "status_string",
-           "wait_timeouts"]
+           "wait_timeouts", "wait_selftest"]

@@ -69,6 +69,8 @@ def lib() -> ctypes.CDLL:
             L.sra_last_cuda_error.restype = i32
             L.sra_wait_timeouts.argtypes = []
             L.sra_wait_timeouts.restype = ctypes.c_uint
+            L.sra_wait_selftest.argtypes = [vp, vp]
+            L.sra_wait_selftest.restype = i32
             L.sra_set_pdl.argtypes = [i32]
             L.sra_set_pdl.restype = i32
             L.sra_force_variant.argtypes = [ctypes.c_char_p, i32]
@@ -90,6 +92,15 @@ def status_string(status: int) -> str:
 def _check(fn: str, status: int) -> None:
     if status != 0:
         raise SRAError(fn, status)
+
+
+def wait_selftest(device="cuda:0") -> int:
+    """Run the bounded-wait self-test (about a second) and return what the kernel wrote: 0
+    when the wait gave up as it should."""
+    r = torch.full((1,), -1, dtype=torch.int32, device=device)
+    with torch.cuda.device(r.device):
+        _check("sra_wait_selftest", lib().sra_wait_selftest(r.data_ptr(), _stream(r, None)))
+    return int(r.item())
 
 
 def wait_timeouts() -> int:

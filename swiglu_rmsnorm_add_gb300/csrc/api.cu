@@ -647,6 +647,11 @@ int sra_last_cuda_error(void) { return g_last_cuda_error; }
 
 unsigned int sra_wait_timeouts(void) { return linear_wait_timeouts(); }
 
+int sra_wait_selftest(int32_t* result, void* stream) {
+    if (!result) return SRA_ERR_NULL;
+    return status_from(launch_wait_selftest(result, static_cast<cudaStream_t>(stream)));
+}
+
 int sra_set_pdl(int enable) {
     const int prev = g_pdl ? 1 : 0;
     g_pdl = enable != 0;

@@ -185,6 +185,7 @@ struct LinPlan {
 cudaError_t launch_linear(const LinArgs& a, const LinPlan& p, int dtype, cudaStream_t s);
 size_t linear_smem(int mt, int prologue);
 unsigned int linear_wait_timeouts();  // bounded waits of the fused-projection kernel that ran out
+cudaError_t launch_wait_selftest(int32_t* out, cudaStream_t s);  // a wait on a barrier nothing completes
 size_t linear16_smem(int rows, int64_t K);
 
 // ------------------------------------------------------------------- UClip

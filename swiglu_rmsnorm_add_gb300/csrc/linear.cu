@@ -828,6 +828,25 @@ bool encode_tmap_16(CUtensorMap* map, const void* base, int rank, uint64_t dim0,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+namespace lin {
+// One thread waits on a barrier that nothing arrives at: the bounded wait has to give up,
+// count the timeout and return, leaving the GPU usable.
+__global__ void wait_selftest_kernel(int32_t* out) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) out[0] = mbar_wait(&bar, 0) ? 1 : 0;
+}
+}  // namespace lin
+
+cudaError_t launch_wait_selftest(int32_t* out, cudaStream_t s) {
+    lin::wait_selftest_kernel<<<1, 32, 0, s>>>(out);
+    return cudaGetLastError();
+}
+
 unsigned int linear_wait_timeouts() {
     unsigned int v = 0;
     if (cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof(v)) != cudaSuccess) {

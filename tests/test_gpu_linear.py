@@ -163,6 +163,9 @@ def test_workspace_equals_its_two_steps():
     assert_linear_close(y, want, h.cpu(), W.cpu(), "ws two steps")
 
 
+_SELFTEST_TIMEOUTS = [0]  # timeouts the self-test below causes on purpose
+
+
 def test_no_wait_ran_out():
     """The tile copies of every call above landed within their bounded waits."""
     x = syn.normal((64, 1536), 0.0, 1.0, torch.bfloat16, 77, 1).to(DEV)
@@ -170,4 +173,16 @@ def test_no_wait_ran_out():
     W = syn.linear_weight(2048, 1536, torch.bfloat16, 77).to(DEV)
     sra.rmsnorm_linear(x, w, W, eps=syn.EPS)
     torch.cuda.synchronize()
-    assert sra.wait_timeouts() == 0
+    assert sra.wait_timeouts() == _SELFTEST_TIMEOUTS[0]
+
+
+def test_bounded_wait_gives_up():
+    """A wait on a barrier that nothing completes gives up after its bound, is counted, and
+    leaves the GPU usable (the calls after it run and match the oracle)."""
+    before = sra.wait_timeouts()
+    assert sra.wait_selftest(DEV) == 0
+    torch.cuda.synchronize()
+    _SELFTEST_TIMEOUTS[0] += 1
+    assert sra.wait_timeouts() == before + 1
+    got, want, h, W = norm_case(64, 1536, 2048, torch.bfloat16, 1041)
+    assert_linear_close(got, want, h, W, "after the self-test")
