@@ -804,6 +804,9 @@ def run_gpu(args):
             t_alt = time_alone(e.chain.replay, reps)
             e.chain.graph = g_main
             rec["us_other_pdl_setting"] = round(statistics.fmean(t_alt) * 1e3, 3)
+            # A/B: the same step launched eagerly from the host (112 C-ABI calls through the binding)
+            t_eager = time_alone(e.chain.step, max(5, reps // 4))
+            rec["us_eager"] = round(statistics.fmean(t_eager) * 1e3, 3)
         per_kernel.append(rec)
 
     # launch latency: back-to-back launches of a one-row RMSNorm (1 x 128 bf16),
