@@ -345,10 +345,12 @@ int plan_norm(int64_t rows, int64_t D, int vec, bool add, int num_sms, const Sme
     // but one (within 2%), and a CTA per row beats the CTA pair.
     int order[7];
     int n = 0;
-    if (!few_rows && nacc <= 256 && (rows >= 256 || nacc <= 64)) order[n++] = NORM_WARP_ROWS;
-    // 16-bit rows of more than 512 and up to 1024 accesses (8192 elements), hundreds of rows:
-    // the lean CTA (w read in the scale loop) measured 2-4 % faster than cta_row
-    if (!few_rows && vec == 8 && nacc > 512 && nacc <= 1024) order[n++] = NORM_CTA_LEAN;
+    // a warp per row from 256 rows (add_rmsnorm [256, 1536]: 15 % faster than a CTA per row), or
+    // for short rows once every SM has two
+    if (nacc <= 256 && (rows >= 256 || (!few_rows && nacc <= 64))) order[n++] = NORM_WARP_ROWS;
+    // 16-bit rows of 512 to 1024 accesses (4096 to 8192 elements), hundreds of rows: the lean
+    // CTA (w read in the scale loop) measured 3-4 % faster than cta_row
+    if (!few_rows && vec == 8 && nacc >= 512 && nacc <= 1024) order[n++] = NORM_CTA_LEAN;
     order[n++] = NORM_CTA_ROW;
     order[n++] = NORM_CTA_SMEM;
     order[n++] = NORM_TWO_PASS;
