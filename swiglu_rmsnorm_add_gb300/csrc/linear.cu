@@ -350,8 +350,13 @@ __global__ void __launch_bounds__(warps_for(MT) * 32) linear_kernel(LinArgs a, c
     T* y = static_cast<T*>(a.y);
     for (int idx = rank * NW * 32 + threadIdx.x; idx < rows * kNT; idx += SK * NW * 32) {
         const int r = idx / kNT, c = idx - r * kNT;
+        // every rank's value requested before the first add (the cluster holds at most 8 ranks)
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = q < SK ? cluster.map_shared_rank(part, q)[r * kNT + c] : 0.0f;
         float sum = 0.0f;
-        for (int q = 0; q < SK; ++q) sum += cluster.map_shared_rank(part, q)[r * kNT + c];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sum += v[q];
         y[(r0 + r) * a.ys + n0 + c] = to_t<T>(sum);
     }
     cluster.sync();
@@ -485,8 +490,13 @@ __global__ void __launch_bounds__((warps_for(MT) + 1) * 32) linear_h_kernel(LinA
     constexpr int NT = (NW + 1) * 32;
     for (int idx = rank * NT + threadIdx.x; idx < rows * kNT; idx += SK * NT) {
         const int r = idx / kNT, c = idx - r * kNT;
+        // every rank's value requested before the first add (the cluster holds at most 8 ranks)
+        float v[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) v[q] = q < SK ? cluster.map_shared_rank(part, q)[r * kNT + c] : 0.0f;
         float sum = 0.0f;
-        for (int q = 0; q < SK; ++q) sum += cluster.map_shared_rank(part, q)[r * kNT + c];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) sum += v[q];
         y[(r0 + r) * a.ys + n0 + c] = to_t<T>(sum);
     }
     cluster.sync();
