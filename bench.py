@@ -989,7 +989,8 @@ def run_sweep(args):
         for v in range(nvar):
             nm = sra.variant_name("rmsnorm", v)
             if nm in ("warp_rows", "cta_row", "cta_pair", "cta_lean"):
-                settings += [(v | (nv << 8), f"{nm}/nv{nv}") for nv in (1, 2, 3, 4, 6, 8)]
+                nvs = (1, 2, 3, 4, 6, 8, 12, 16) if nm == "warp_rows" else (1, 2, 3, 4, 6, 8)
+                settings += [(v | (nv << 8), f"{nm}/nv{nv}") for nv in nvs]
             else:
                 settings.append((v, nm))
         for v, label in settings:

@@ -486,13 +486,15 @@ SRA_API int sra_set_pdl(int enable);
 
 /*
  * Kernel-variant control, for A/B measurement of the per-shape dispatch.
- * op: "rmsnorm" (also used by add_rmsnorm), "rope_kv_store", "glu",
- * "decode_attention" (0 = CUDA-core kernel, 1 = mma.sync kernel for bf16 / fp16
- * with head_dim 64 or 128).
+ * op: "rmsnorm" (also used by add_rmsnorm), "rope_kv_store" (0 = one task of a
+ * token per thread, 1 = two tasks per thread sharing one cos / sin load, for an
+ * even n_head + 2 * n_kv_head), "glu", "decode_attention" (0 = CUDA-core kernel,
+ * 1 = mma.sync kernel for bf16 / fp16 with head_dim 64 or 128).
  * variant: -1 = automatic per-shape choice (the default); otherwise an index
  * < sra_variant_count(op), optionally OR-ed with (nv << 8) to also force the
  * number of 16-byte accesses each thread holds in the register variants of
- * "rmsnorm" (nv in 1, 2, 3, 4, 6, 8). A forced setting that cannot serve a later
+ * "rmsnorm" (nv in 1, 2, 3, 4, 6, 8; also 12 and 16 for the warp-per-row
+ * variant). A forced setting that cannot serve a later
  * call makes that call return SRA_ERR_VARIANT without enqueueing anything.
  * Returns SRA_OK, or SRA_ERR_ARG for an unknown op or out-of-range variant.
  */

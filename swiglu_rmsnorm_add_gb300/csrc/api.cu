@@ -211,9 +211,9 @@ bool plan_norm_vector(int variant, int64_t rows, int64_t D, int vec, bool add, i
     switch (variant) {
         case NORM_WARP_ROWS: {
             const int64_t per_lane = ceil_div(nacc, 32);
-            if (per_lane > 8) return false;
-            int nv = 8;
-            for (int c : {1, 2, 3, 4, 6, 8}) {
+            if (per_lane > 16) return false;
+            int nv = 16;
+            for (int c : {1, 2, 3, 4, 6, 8, 12, 16}) {
                 if (c >= per_lane && (g_force_nv == 0 || c == g_force_nv)) {
                     nv = c;
                     break;
@@ -346,8 +346,11 @@ int plan_norm(int64_t rows, int64_t D, int vec, bool add, int num_sms, const Sme
     int order[7];
     int n = 0;
     // a warp per row from 256 rows (add_rmsnorm [256, 1536]: 15 % faster than a CTA per row), or
-    // for short rows once every SM has two
+    // for short rows once every SM has two. Rows of 257 to 512 accesses (12 or 16 per lane) take
+    // a warp each at a few hundred rows: 512 rows of fp32 1536 / 2048, 16-bit 2176 / 4096 measured
+    // 35 / 28 / 21 / 9 % faster than the CTA variants
     if (nacc <= 256 && (rows >= 256 || (!few_rows && nacc <= 64))) order[n++] = NORM_WARP_ROWS;
+    else if (nacc <= 512 && rows >= 256 && rows <= 8LL * num_sms) order[n++] = NORM_WARP_ROWS;
     // 16-bit rows of 512 to 1024 accesses (4096 to 8192 elements), hundreds of rows: the lean
     // CTA (w read in the scale loop) measured 3-4 % faster than cta_row
     if (!few_rows && vec == 8 && nacc >= 512 && nacc <= 1024) order[n++] = NORM_CTA_LEAN;
@@ -369,18 +372,33 @@ int norm_vec(int dt, const void* const* ptrs, int nptr, const int64_t* strides, 
 }
 
 // ------------------------------------------------------------------ RoPE plan
-int plan_rope(int64_t T, int n_head, int n_kv, int head_dim, int pairs, int style, int num_sms, RopePlan* p) {
+int plan_rope(int64_t T, int n_head, int n_kv, int head_dim, int pairs, int style, bool qk_norm, int num_sms,
+              RopePlan* p) {
     const int forced = g_force_rope.load(std::memory_order_relaxed);
-    if (forced > 0) return SRA_ERR_VARIANT;
     const int h = head_dim / 2;
-    const int64_t U = static_cast<int64_t>(n_head + 2 * n_kv) * (h / pairs);
-    p->variant = ROPE_TOKEN_CTA;
+    const int n_units = n_head + 2 * n_kv;
+    // two tasks per thread need the token's tasks to split into two equal sets of whole heads
+    const bool two_ok = n_units % 2 == 0;
+    // Two tasks per thread once the tokens outnumber what one round of the one-task kernel holds
+    // (about 9 tokens per SM at Qwen2.5-1.5B bf16 shapes). Measured on GB300, bf16, 12 / 2 heads:
+    // T = 2048 and 32768 faster (neox and interleaved), T = 1 and 64 slower; with the Q/K UClip
+    // fused the two-task kernel runs out of registers and is slower at every T.
+    int variant = two_ok && !qk_norm && T > 8LL * num_sms ? ROPE_TOKEN_CTA2 : ROPE_TOKEN_CTA;
+    if (forced >= 0) {
+        if (forced >= ROPE_NUM_VARIANTS) return SRA_ERR_VARIANT;  // no accesses-per-thread setting here
+        variant = forced;
+    }
+    if (variant == ROPE_TOKEN_CTA2 && !two_ok) return SRA_ERR_VARIANT;
+    const int64_t U = static_cast<int64_t>(n_units) * (h / pairs) / (variant == ROPE_TOKEN_CTA2 ? 2 : 1);
+    p->variant = variant;
     p->style = style;
-    p->qk_norm = false;
+    p->qk_norm = qk_norm;
     p->pairs = pairs;
     p->pdl = g_pdl;
     p->num_sms = num_sms;
-    p->threads = static_cast<int>(std::min<int64_t>(1024, std::max(32, round_up32(U))));
+    // the two-task kernel is compiled for at most 512 threads (its tasks loop past them)
+    const int64_t max_threads = variant == ROPE_TOKEN_CTA2 ? 512 : 1024;
+    p->threads = static_cast<int>(std::min<int64_t>(max_threads, std::max(32, round_up32(U))));
     p->grid = std::max<int64_t>(1, T);
     return SRA_OK;
 }
@@ -589,9 +607,8 @@ int rope_impl(void* q, const void* k, const void* v, const float* cos, const flo
                                    aligned16(norm->kg)));
     if (!vec_ok) pairs = 1;
     RopePlan plan;
-    int st = plan_rope(T, n_head, n_kv_head, head_dim, pairs, style, sms, &plan);
+    int st = plan_rope(T, n_head, n_kv_head, head_dim, pairs, style, norm != nullptr, sms, &plan);
     if (st != SRA_OK) return st;
-    plan.qk_norm = norm != nullptr;
     RopeArgs a;
     a.q = q;
     a.k = k;
@@ -1085,7 +1102,7 @@ int sra_variant_count(const char* op) { return variant_count(op); }
 const char* sra_variant_name(const char* op, int variant) {
     static const char* const norm_names[] = {"warp_rows", "cta_row",   "cta_smem",  "two_pass",
                                              "cta_pair",  "warp_smem", "pair_smem", "cta_lean"};
-    static const char* const rope_names[] = {"token_cta"};
+    static const char* const rope_names[] = {"token_cta", "token_cta2"};
     static const char* const glu_names[] = {"cols_rows"};
     static const char* const attn_names[] = {"cuda_cores", "mma_sync"};
     const int n = variant_count(op);
@@ -1116,7 +1133,8 @@ int sra_pick_variant(const char* op, int64_t a, int64_t b, int64_t c, int64_t d,
     if (std::strcmp(op, "rope_kv_store") == 0) {
         if (a < 0 || b <= 0 || c <= 0 || d <= 0 || d % 2) return SRA_ERR_SHAPE;
         RopePlan p;
-        const int st = plan_rope(a, static_cast<int>(b), static_cast<int>(c), static_cast<int>(d), 1, 0, num_sms, &p);
+        const int st =
+            plan_rope(a, static_cast<int>(b), static_cast<int>(c), static_cast<int>(d), 1, 0, false, num_sms, &p);
         return st == SRA_OK ? p.variant : st;
     }
     if (std::strcmp(op, "decode_attention") == 0) {

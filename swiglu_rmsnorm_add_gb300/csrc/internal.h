@@ -87,7 +87,9 @@ struct RopeArgs {
     float clip_lo = 0.0f, clip_hi = 0.0f;
 };
 
-enum RopeVariant { ROPE_TOKEN_CTA = 0, ROPE_NUM_VARIANTS = 1 };
+// TOKEN_CTA: one task of P pairs per thread; TOKEN_CTA2: two tasks per thread sharing one
+// cos / sin load (needs an even number of head units, n_head + 2 n_kv_head)
+enum RopeVariant { ROPE_TOKEN_CTA = 0, ROPE_TOKEN_CTA2 = 1, ROPE_NUM_VARIANTS = 2 };
 
 struct RopePlan {
     int variant;

@@ -566,6 +566,8 @@ cudaError_t launch_vector(const NormArgs& a, const NormPlan& p, cudaStream_t s) 
                 case 4: return launch_persistent(reg_warp_kernel<T, 4, ADD>, a, p, false, s);
                 case 6: return launch_persistent(reg_warp_kernel<T, 6, ADD>, a, p, false, s);
                 case 8: return launch_persistent(reg_warp_kernel<T, 8, ADD>, a, p, false, s);
+                case 12: return launch_persistent(reg_warp_kernel<T, 12, ADD>, a, p, false, s);
+                case 16: return launch_persistent(reg_warp_kernel<T, 16, ADD>, a, p, false, s);
                 default: return cudaErrorInvalidValue;
             }
         case NORM_CTA_ROW:

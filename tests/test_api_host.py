@@ -319,7 +319,7 @@ def test_glu_validation(L):
 
 def test_variant_control(L):
     assert sra.variant_count("rmsnorm") == 8
-    assert sra.variant_count("rope_kv_store") == 1
+    assert sra.variant_count("rope_kv_store") == 2
     assert sra.variant_count("glu") == 1
     assert sra.variant_count("decode_attention") == 2
     assert [sra.variant_name("decode_attention", i) for i in range(2)] == ["cuda_cores", "mma_sync"]
@@ -345,8 +345,14 @@ def test_dispatch_choices(L):
     assert pick("rmsnorm", 64, 1536, dtype=torch.bfloat16, num_sms=152) == 1
     # from 256 rows of 1536: one warp per row (measured 15 % faster at 256 rows)
     assert pick("rmsnorm", 256, 1536, dtype=torch.bfloat16, num_sms=152) == 0
-    # 16-bit rows of 4096 and 8192 elements, 512 of them: the lean CTA per row
-    assert pick("rmsnorm", 512, 4096, dtype=torch.bfloat16, num_sms=152) == 7
+    # rows of 257 to 512 16-byte accesses, a few hundred of them: a warp per row (12 or 16
+    # accesses per lane); more rows keep the CTA variants
+    assert pick("rmsnorm", 512, 4096, dtype=torch.bfloat16, num_sms=152) == 0
+    assert pick("rmsnorm", 512, 2176, dtype=torch.bfloat16, num_sms=152) == 0
+    assert pick("rmsnorm", 512, 1536, dtype=torch.float32, num_sms=152) == 0
+    assert pick("rmsnorm", 512, 2048, dtype=torch.float32, num_sms=152) == 0
+    assert pick("rmsnorm", 4096, 4096, dtype=torch.bfloat16, num_sms=152) == 7
+    # 16-bit rows of 8192 elements, 512 of them: the lean CTA per row
     assert pick("rmsnorm", 512, 8192, dtype=torch.float16, num_sms=152) == 7
     # a row past a warp's registers: CTA per row
     assert pick("rmsnorm", 512, 2176, dtype=torch.float32, num_sms=152) == 1
@@ -357,7 +363,12 @@ def test_dispatch_choices(L):
     # past shared memory: two-pass
     assert pick("rmsnorm", 2, 10_000_000, dtype=torch.float32, num_sms=152) == 3
     assert pick("glu", 4096, 14336, num_sms=152) == 0
-    assert pick("rope_kv_store", 2048, 12, 2, 128, num_sms=152) == 0
+    # RoPE: one task per thread up to 8 tokens per SM, two tasks per thread past that (an even
+    # number of head units); an odd number keeps one task per thread
+    assert pick("rope_kv_store", 64, 12, 2, 128, num_sms=152) == 0
+    assert pick("rope_kv_store", 1216, 12, 2, 128, num_sms=152) == 0
+    assert pick("rope_kv_store", 2048, 12, 2, 128, num_sms=152) == 1
+    assert pick("rope_kv_store", 2048, 3, 1, 64, num_sms=152) == 0
     # decode attention: tensor cores for 16-bit data up to head_dim 128, CUDA cores otherwise
     assert pick("decode_attention", 32, 12, 2, 128, dtype=torch.bfloat16, num_sms=152) == 1
     assert pick("decode_attention", 32, 12, 2, 256, dtype=torch.bfloat16, num_sms=152) == 0

@@ -269,3 +269,56 @@ def test_qk_uclip_bad_positions_and_scalar_path():
     assert_close(dc.cpu()[0], inp["kv_cache"][0], "K")
     assert_bits_equal(dc.cpu()[1], inp["kv_cache"][1], "V")
     assert_bits_equal(dq[3], q[3], "bad position: q raw")
+
+
+# ------------------------------------------------ forced kernel variants
+@pytest.mark.parametrize("variant", [0, 1])
+@pytest.mark.parametrize("style", STYLES)
+@pytest.mark.parametrize("dtype", [torch.float32, torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("T,n_head,n_kv,hd", [(2048, 12, 2, 128), (1, 12, 2, 128), (37, 8, 8, 64), (29, 16, 1, 256),
+                                              (37, 6, 3, 10), (5, 2, 1, 2), (7, 3, 1, 64)])
+def test_forced_variants(variant, style, dtype, T, n_head, n_kv, hd):
+    """One task per thread (0) and two tasks per thread sharing a cos / sin load (1); the
+    second needs an even number of head units and refuses the rest."""
+    max_pos = 32768 if hd == 128 else 4096
+    tables = syn.rope_tables(max_pos, hd, 1e6 if hd == 128 else 1e4)
+    inp = syn.rope_inputs(T, 31, n_head=n_head, n_kv_head=n_kv, head_dim=hd,
+                          num_blocks=max(8, (T + 15) // 16), max_pos=max_pos, dtype=dtype, tables=tables)
+    sra.force_variant("rope_kv_store", variant)
+    try:
+        try:
+            d = run_both(inp, expect_err=0, style=style)
+        except sra.SRAError as e:
+            assert variant == 1 and (n_head + 2 * n_kv) % 2 == 1 and e.status == -7
+            return
+        assert variant == 0 or (n_head + 2 * n_kv) % 2 == 0
+        check(d, inp, f"variant {variant} {style} {dtype} T={T} {n_head}/{n_kv}/{hd}")
+    finally:
+        sra.force_variant("rope_kv_store", -1)
+
+
+@pytest.mark.parametrize("style", STYLES)
+def test_two_tasks_per_thread_padding_bad_slots_and_uclip(style):
+    sra.force_variant("rope_kv_store", 1)
+    try:
+        inp = syn.rope_inputs(8, 23, num_blocks=4)   # 64 slots
+        inp["slot_mapping"] = torch.tensor([-1, 3, 64, 5, 1000, 7, -1, 9], dtype=torch.int64)
+        inp["pos"] = torch.tensor([1, 2, 3, -4, 5, 32768, 7, 8], dtype=torch.int64)
+        d = run_both(inp, expect_err=4, style=style)
+        check(d, inp, f"two tasks per thread, padding / errors {style}")
+
+        tables = syn.rope_tables(32768, 128, 1e6)
+        inp = syn.rope_inputs(2048, 32, tables=tables)
+        params = _qk_params(128, 32)
+        d = {k: v.to(DEV) for k, v in inp.items()}
+        err = torch.zeros(1, dtype=torch.int32, device=DEV)
+        sra.rope_kv_store(d["q"], d["k"], d["v"], d["cos"], d["sin"], d["pos"], d["slot_mapping"], d["kv_cache"],
+                          err_count=err, style=style, qk_uclip=tuple(p.to(DEV) for p in params), clip=(-0.9, 1.1))
+        torch.cuda.synchronize()
+        n = oracle.qk_uclip_rope_kv_store(inp["q"], inp["k"], inp["v"], inp["cos"], inp["sin"], inp["pos"],
+                                          inp["slot_mapping"], inp["kv_cache"], *params, clip_min=-0.9,
+                                          clip_max=1.1, style=style)
+        assert int(err.item()) == n == 0
+        check(d, inp, f"two tasks per thread, qk_uclip {style}")
+    finally:
+        sra.force_variant("rope_kv_store", -1)
