@@ -487,8 +487,8 @@ SRA_API int sra_set_pdl(int enable);
 /*
  * Kernel-variant control, for A/B measurement of the per-shape dispatch.
  * op: "rmsnorm" (also used by add_rmsnorm), "rope_kv_store" (0 = one task of a
- * token per thread, 1 = two tasks per thread sharing one cos / sin load, for an
- * even n_head + 2 * n_kv_head), "glu", "decode_attention" (0 = CUDA-core kernel,
+ * token per thread, 1 = two tasks per thread that read the same cos / sin chunk,
+ * for an even n_head + 2 * n_kv_head), "glu", "decode_attention" (0 = CUDA-core kernel,
  * 1 = mma.sync kernel for bf16 / fp16 with head_dim 64 or 128).
  * variant: -1 = automatic per-shape choice (the default); otherwise an index
  * < sra_variant_count(op), optionally OR-ed with (nv << 8) to also force the
