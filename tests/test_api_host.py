@@ -369,6 +369,16 @@ def test_dispatch_choices(L):
     assert pick("rope_kv_store", 1216, 12, 2, 128, num_sms=152) == 0
     assert pick("rope_kv_store", 2048, 12, 2, 128, num_sms=152) == 1
     assert pick("rope_kv_store", 2048, 3, 1, 64, num_sms=152) == 0
+    # the threshold follows the SM count: past 8 tokens per SM
+    assert pick("rope_kv_store", 800, 12, 2, 128, num_sms=100) == 0
+    assert pick("rope_kv_store", 801, 12, 2, 128, num_sms=100) == 1
+    # warp rows of 257-512 accesses only between 256 rows and 8 rows per SM
+    assert pick("rmsnorm", 255, 1536, dtype=torch.float32, num_sms=152) == 1
+    assert pick("rmsnorm", 256, 1536, dtype=torch.float32, num_sms=152) == 0
+    assert pick("rmsnorm", 1216, 1536, dtype=torch.float32, num_sms=152) == 0
+    assert pick("rmsnorm", 1217, 1536, dtype=torch.float32, num_sms=152) == 1
+    # past 512 accesses (fp32 2176: 544) a warp cannot hold the row
+    assert pick("rmsnorm", 512, 2176, dtype=torch.float32, num_sms=152) == 1
     # decode attention: tensor cores for 16-bit data up to head_dim 128, CUDA cores otherwise
     assert pick("decode_attention", 32, 12, 2, 128, dtype=torch.bfloat16, num_sms=152) == 1
     assert pick("decode_attention", 32, 12, 2, 256, dtype=torch.bfloat16, num_sms=152) == 0
