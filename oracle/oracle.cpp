@@ -344,8 +344,9 @@ int orc_glu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row
 // section 3.3: the uclip kernel's per-channel or scalar alpha and gamma and its
 // clip bounds). x and out are [N, H, D] with element strides (n_stride, h_stride, 1)
 // each, so narrow Q/K views of a fused QKV buffer are read in place. alpha and
-// gamma are fp32, D entries each when per-channel, else one entry. The clamp lets
-// NaN through (a comparison with NaN is false); lo > hi or a NaN bound is an error.
+// gamma are fp32, D entries each when per-channel, else one entry. The page's
+// kernel clamps with fmaxf then fminf, which return the non-NaN operand, so a NaN
+// a * x becomes the lower bound; lo > hi or a NaN bound is an error.
 //
 // Precision: the page's kernel fixes it. It converts x to float and evaluates
 // a * x and the product with g in float, so this function does the same: two
@@ -366,6 +367,7 @@ int orc_uclip(const void* x, const float* alpha, const float* gamma, void* out, 
                 // a value of any of the three formats is exact in float
                 const float xf = static_cast<float>(load(x, n * x_n_stride + hh * x_h_stride + d, fmt));
                 float v = a * xf;
+                if (std::isnan(v)) v = lo32;  // the page's fmaxf keeps the bound when a * x is NaN
                 if (v < lo32) v = lo32;
                 if (v > hi32) v = hi32;
                 const float y = v * g;

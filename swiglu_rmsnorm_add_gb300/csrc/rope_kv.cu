@@ -65,11 +65,10 @@ __device__ __forceinline__ void load_pair_params(const float* p, int i0, int h, 
     }
 }
 
+// clamp(a x, lo, hi) * g in fp32; a NaN product takes the lower bound (fmaxf
+// returns its non-NaN operand), as in the separate UClip kernel.
 __device__ __forceinline__ float uclip1(float x, float a, float g, float lo, float hi) {
-    float v = a * x;
-    v = v < lo ? lo : v;
-    v = v > hi ? hi : v;
-    return v * g;
+    return fminf(fmaxf(a * x, lo), hi) * g;
 }
 
 // One Q or K task: unpack the two accesses (r0, r1) into the pair halves, UClip

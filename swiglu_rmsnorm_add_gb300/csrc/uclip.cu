@@ -16,8 +16,8 @@
 // four 16-byte loads are in flight per thread. An element is read and written
 // by the same thread only, so out == x (in place) is safe.
 //
-// Arithmetic: fp32 a * x, the clamp (NaN passes through: both comparisons are
-// false), then * g, one RNE to the dtype.
+// Arithmetic: fp32 a * x, the clamp (a NaN product becomes the lower bound, as
+// in the page's fminf(fmaxf(..)) form), then * g, one RNE to the dtype.
 #include "common.cuh"
 #include "internal.h"
 
@@ -26,10 +26,9 @@ namespace uclip {
 
 constexpr int kRowsInFlight = 4;
 
-__device__ __forceinline__ float clip(float v, float lo, float hi) {
-    v = v < lo ? lo : v;
-    return v > hi ? hi : v;
-}
+// fmaxf returns its other operand when one is NaN, so a NaN product takes the
+// lower bound, as the page's kernel (fmaxf, then fminf) has it.
+__device__ __forceinline__ float clip(float v, float lo, float hi) { return fminf(fmaxf(v, lo), hi); }
 
 // VEC consecutive fp32 parameters starting at p + col (per channel), or p[0] repeated.
 template <int VEC, bool PER_CHANNEL>

@@ -48,7 +48,7 @@ MUTANTS = [
     ("uclip gamma dropped", "const float y = v * g;", "const float y = v;", "test_oracle_uclip.py"),
     ("uclip lower bound clips to the upper", "if (v < lo32) v = lo32;", "if (v < lo32) v = hi32;",
      "test_oracle_uclip.py"),
-    ("uclip NaN clamped", "if (v < lo32) v = lo32;", "if (!(v >= lo32)) v = lo32;", "test_oracle_uclip.py"),
+    ("uclip NaN passes the clamp", "if (std::isnan(v)) v = lo32;", "", "test_oracle_uclip.py"),
     ("uclip in double", "float v = a * xf;", "double v = static_cast<double>(a) * xf;", "test_oracle_uclip.py"),
     ("uclip alpha indexed by head", "alpha[alpha_per_channel ? d : 0]", "alpha[alpha_per_channel ? hh : 0]",
      "test_oracle_uclip.py"),

@@ -87,11 +87,11 @@ def test_special_values(fmt):
     dt = TORCH_DT[fmt]
     x = torch.tensor([math.nan, math.inf, -math.inf, 0.0, -0.0], dtype=dt).reshape(1, -1)
     out = _run(x, _scalar(3.0), _scalar(-2.0), -1.0, 1.0)
-    assert math.isnan(out[0, 0])                      # NaN passes through the clamp
+    assert out[0, 0].item() == -1.0 * -2.0            # a NaN product takes the lower bound, times g
     assert out[0, 1].item() == -2.0 and out[0, 2].item() == 2.0   # +-inf clip to the bounds, times g
     assert out[0, 3].item() == 0.0 and out[0, 4].item() == 0.0
-    z = _run(x[:, 1:3], _scalar(0.0), _scalar(1.0), -1.0, 1.0)   # 0 * inf = NaN
-    assert torch.isnan(z).all()
+    z = _run(x[:, 1:3], _scalar(0.0), _scalar(0.5), -1.0, 1.0)   # 0 * inf = NaN -> the lower bound
+    assert (z == -0.5).all()
     with pytest.raises(ValueError):
         _run(x, _scalar(1.0), _scalar(1.0), 1.0, -1.0)   # lo > hi
     with pytest.raises(ValueError):
