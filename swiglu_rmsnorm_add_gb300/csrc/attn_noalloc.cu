@@ -10,10 +10,11 @@
 // them the same kernel with its scratch in one fixed device array that the library
 // itself holds.
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 
-#include <atomic>
 #include <cstdint>
+#include <mutex>
 
 #include "sra.h"
 
@@ -29,20 +30,62 @@ static __device__ __align__(256) unsigned char g_attn_scratch[kScratchBytes];
 namespace {
 
 constexpr int kMaxDevices = 64;
-std::atomic<void*> g_scratch_addr[kMaxDevices];
 
-// Device address of the array on the current device. Host code sees only a host-side
-// stand-in for g_attn_scratch, so the address comes from the runtime, once per device,
-// with that device current. Returns nullptr when the runtime cannot give it.
+// The context a cached address belongs to: the driver's process-unique context id
+// (cuCtxGetId; a handle value can be reused by a context created after a reset, an
+// id never is). 0 when the driver cannot tell, and then nothing is cached.
+unsigned long long current_context_id() {
+    using GetCurrent = CUresult (*)(CUcontext*);
+    using GetId = CUresult (*)(CUcontext, unsigned long long*);
+    static const GetCurrent get_current = [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return static_cast<GetCurrent>(nullptr);
+        }
+        return reinterpret_cast<GetCurrent>(fn);
+    }();
+    static const GetId get_id = [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess) {
+            cudaGetLastError();
+            return static_cast<GetId>(nullptr);
+        }
+        return reinterpret_cast<GetId>(fn);
+    }();
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx || get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
+
+std::mutex g_mu;
+unsigned long long g_ctx_id[kMaxDevices];
+void* g_addr[kMaxDevices];
+
+// Device address of the array in the current device's context. Host code sees only a
+// host-side stand-in for g_attn_scratch, so the address comes from the runtime, with the
+// device current: once per device, and again whenever that device's context has
+// changed since (after cudaDeviceReset the array lives in a new context). A call made
+// before the runtime has made the device's context current is answered but not cached.
+// Returns nullptr when the runtime cannot give the address.
 void* scratch_on_current_device(int dev) {
     if (dev < 0 || dev >= kMaxDevices) return nullptr;
-    void* p = g_scratch_addr[dev].load(std::memory_order_acquire);
-    if (p) return p;
+    const unsigned long long id = current_context_id();
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (id != 0 && g_ctx_id[dev] == id && g_addr[dev]) return g_addr[dev];
+    void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_attn_scratch) != cudaSuccess || !p) {
         cudaGetLastError();
         return nullptr;
     }
-    g_scratch_addr[dev].store(p, std::memory_order_release);
+    g_ctx_id[dev] = id;
+    g_addr[dev] = id != 0 ? p : nullptr;
     return p;
 }
 

@@ -9,7 +9,8 @@ entry points with a caller-owned workspace (or none) give, call after call: the
 array keeps the previous call's contents, so each test makes two calls in a row
 on different inputs of one shape and compares both with the existing entry
 point, within the attention tests' tolerance (the same kernel runs on both
-sides, so the results are expected to agree exactly).
+sides, so the results are expected to agree exactly), and with the CPU oracle
+at that tolerance, so a defect the two entry points share cannot pass.
 
 This file is collected last, so a run that stops at its first failure has
 already run every other test; it also passes alone in a fresh process.
@@ -17,6 +18,7 @@ already run every other test; it also passes alone in a fresh process.
 import pytest
 import torch
 
+import oracle
 import swiglu_rmsnorm_add_gb300 as sra
 from swiglu_rmsnorm_add_gb300 import synthetic as syn
 from tests.test_gpu_attention import assert_attention_close
@@ -54,6 +56,9 @@ def test_noalloc_matches_existing_entry_twice(B, ctx, n_head, n_kv, hd, dtype):
         torch.cuda.synchronize()
         assert int(err_a.item()) == int(err_b.item()) == 0
         assert_attention_close(got, want, cache, table, seq, f"no-alloc call {call + 1} B={B} ctx={ctx}")
+        ref = torch.empty_like(q)
+        assert oracle.paged_decode_attention(q, cache, table, seq, ref) == 0
+        assert_attention_close(got, ref, cache, table, seq, f"no-alloc vs oracle, call {call + 1} B={B} ctx={ctx}")
 
 
 def test_noalloc_requires_out():
