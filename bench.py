@@ -72,7 +72,7 @@ def parse():
     p.add_argument("--no-companions", action="store_true")
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--sweep-variants", action="store_true",
-                   help="A/B: time every RMSNorm variant on every norm shape (prints its own JSON)")
+                   help="A/B: time every RMSNorm / GLU variant on every norm / GLU shape (prints its own JSON)")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-baseline duration")
     return p.parse_args()
 
@@ -312,6 +312,24 @@ def build_entries(dev, stream_handle, only=(), companions=False):
                 entries.append(Entry(name, "linear", nbytes, B, L.sra_glu_linear,
                                      (gu.data_ptr(), W.data_ptr(), y.data_ptr(), B, I, N, 2 * I, N, 0, 2,
                                       stream_handle), [gu], [y], keep=(gu, W, y)))
+    if companions:
+        # the decode chain's own batch-64 shapes, standalone (Qwen2.5-1.5B: hidden 1536, intermediate 8960)
+        name = "add_rmsnorm:bf16:64x1536"
+        if want(name):
+            x, r, w = syn.add_rms_inputs(64, 1536, torch.bfloat16, 1004)
+            x, r, w = x.to(dev), r.to(dev), w.to(dev)
+            out = torch.empty_like(x)
+            entries.append(Entry(name, "add_rmsnorm", 4 * 64 * 1536 * 2 + 1536 * 2, 64, L.sra_add_rmsnorm,
+                                 (x.data_ptr(), r.data_ptr(), w.data_ptr(), out.data_ptr(), 64, 1536, 1536, 1536,
+                                  1536, syn.EPS, 2, stream_handle), [x, r], [x, out], keep=(x, r, w, out)))
+        I5 = syn.QWEN25_DOWN["I"]
+        name = f"swiglu:bf16:64x{I5}"
+        if want(name):
+            gu = syn.glu_inputs(64, I5, torch.bfloat16, 1004).to(dev)
+            out = torch.empty(64, I5, dtype=torch.bfloat16, device=dev)
+            entries.append(Entry(name, "swiglu", 64 * (2 * I5 * 2 + I5 * 2), 64, L.sra_glu,
+                                 (gu.data_ptr(), out.data_ptr(), 64, I5, 2 * I5, I5, 0, 2, stream_handle), [gu],
+                                 [out], keep=(gu, out)))
     I = syn.LLAMA3_8B_MLP["intermediate"]
     for T in Ts_glu:
         gu = None
@@ -807,6 +825,21 @@ def run_gpu(args):
             # A/B: the same step launched eagerly from the host (112 C-ABI calls through the binding)
             t_eager = time_alone(e.chain.step, max(5, reps // 4))
             rec["us_eager"] = round(statistics.fmean(t_eager) * 1e3, 3)
+            # per kernel kind inside the chain: a graph of only that kind's launches, in chain order
+            # on the chain's buffers (each launch waits for the one before, as in the step)
+            kinds = {}
+            nl = e.chain.launches_per_step()
+            for kind, kb in e.bytes_by_kind.items():
+                gk = e.chain.capture_kind(kind, pdl)
+                tk = statistics.fmean(time_alone(gk.replay, reps)) * 1e3
+                del gk
+                kinds[kind] = {"launches": nl[kind], "bytes": kb, "us": round(tk, 3),
+                               "us_per_launch": round(tk / nl[kind], 3),
+                               "gbs": round(kb / (tk * 1e-6) / 1e9, 1),
+                               "frac_of_peak": round(kb / (tk * 1e-6) / 1e9 / peak, 4)}
+            rec["kinds"] = kinds
+            rec["kinds_what"] = ("each kernel kind of the step alone: a CUDA graph of its launches in chain order "
+                                 "on the chain's own buffers, replayed (clean L2 before each replay)")
         per_kernel.append(rec)
 
     # launch latency: back-to-back launches of a one-row RMSNorm (1 x 128 bf16),
@@ -963,7 +996,8 @@ def run_gpu(args):
 
 
 def run_sweep(args):
-    """Streaming time of every RMSNorm variant on every norm shape (dispatch evidence)."""
+    """Streaming time of every RMSNorm variant on every norm shape, and of every GLU
+    variant on the GLU shapes (dispatch evidence)."""
     import torch
 
     import swiglu_rmsnorm_add_gb300 as sra
@@ -973,28 +1007,31 @@ def run_sweep(args):
     stream = torch.cuda.current_stream(dev)
     sh = int(stream.cuda_stream)
     sra.set_pdl(not args.no_pdl)
-    only = [o for o in args.only.split(",") if o] or ["rmsnorm", "add_rmsnorm"]
-    entries = [e for e in build_entries(dev, sh, only) if e.op in ("rmsnorm", "add_rmsnorm")]
+    swept = ("rmsnorm", "add_rmsnorm", "swiglu", "reglu")
+    only = [o for o in args.only.split(",") if o] or list(swept)
+    entries = [e for e in build_entries(dev, sh, only) if e.op in swept]
     if not args.only:
-        entries += [e for e in build_entries(dev, sh, companions=True) if e.op in ("rmsnorm", "add_rmsnorm")]
+        entries += [e for e in build_entries(dev, sh, companions=True) if e.op in swept]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     peak, _ = measured_peak()
-    nvar = sra.variant_count("rmsnorm")
     table = []
     for e in entries:
         row = {"name": e.name, "bytes": e.bytes, "auto": None, "variants": {}}
         n = int(min(64, max(1, -(-STREAM_BYTES // max(1, e.bytes)))))
         calls = e.replicas(n) if n > 1 else [e.launch]
+        op = "glu" if e.op in ("swiglu", "reglu") else "rmsnorm"
         settings = [(-1, "auto")]
-        for v in range(nvar):
-            nm = sra.variant_name("rmsnorm", v)
+        for v in range(sra.variant_count(op)):
+            nm = sra.variant_name(op, v)
             if nm in ("warp_rows", "cta_row", "cta_pair", "cta_lean"):
                 nvs = (1, 2, 3, 4, 6, 8, 12, 16) if nm == "warp_rows" else (1, 2, 3, 4, 6, 8)
                 settings += [(v | (nv << 8), f"{nm}/nv{nv}") for nv in nvs]
+            elif nm == "warps_row":
+                settings += [(v | (nv << 8) | (g << 16), f"{nm}/g{g}nv{nv}") for g in (2, 4, 8) for nv in (8, 16)]
             else:
                 settings.append((v, nm))
         for v, label in settings:
-            sra.force_variant("rmsnorm", v)
+            sra.force_variant(op, v)
             try:
                 for c in calls:
                     c()
@@ -1018,7 +1055,7 @@ def run_sweep(args):
                 row["auto"] = rec
             else:
                 row["variants"][label] = rec
-        sra.force_variant("rmsnorm", -1)
+        sra.force_variant(op, -1)
         del calls
         table.append(row)
     print(json.dumps({"variant_sweep": table, "peak_gbs": peak, "timing": "back-to-back launches over rotating "

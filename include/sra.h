@@ -20,6 +20,10 @@
  *  - Pointers to tensors are DEVICE pointers (any memory the current device can
  *    load from and store to). The caller owns every buffer; the library never
  *    allocates, frees, zero-fills or keeps a pointer after the call returns.
+ *    Two exceptions, both library-owned device arrays in the library's own
+ *    module: the scratch array of sra_paged_decode_attention_noalloc (whose
+ *    counters that call clears, and whose address it keeps per device), and the
+ *    counter of bounded device waits that ran out (sra_wait_timeouts).
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream). Every call only enqueues work on that stream and returns at once;
  *    results are visible after the stream is synchronised. The kernel runs on
@@ -326,7 +330,9 @@ SRA_API int64_t sra_paged_decode_attention_workspace_size(int64_t B, int n_head,
  * Arguments, layout and results are those of sra_paged_decode_attention; on this
  * library's planning the result equals sra_paged_decode_attention_ws's.
  * Set-up: the first call on a device looks up the array's device address on that
- * device (with it current); make that first call before any stream capture.
+ * device (with it current); make that first call before any stream capture. The
+ * address is kept per device and looked up again when the device's context has
+ * changed (a call after cudaDeviceReset finds the array in the new context).
  * Every call clears the array's counters on `stream` before its kernel runs.
  * Races: all calls on a device share the one array, so two calls that may run at
  * the same time on the GPU (different streams without an event between them, or
@@ -418,8 +424,8 @@ SRA_API int sra_glu_linear_ws(const void* gate_up, const void* W, void* y, int64
  *   out[n, h, d] = clamp(alpha_d * x[n, h, d], clip_min, clip_max) * gamma_d
  *
  * computed in fp32 and rounded once (RNE) to the dtype. DyHT is clip_min = -1,
- * clip_max = 1. NaN in x passes through the clamp (a comparison with NaN is
- * false); +-inf clips to a bound.
+ * clip_max = 1. A NaN alpha * x becomes clip_min (the page's kernel clamps with
+ * fmaxf then fminf, which keep the non-NaN operand); +-inf clips to a bound.
  *
  * x:      [N, H, D] of `dtype`, element strides (x_n_stride, x_h_stride, 1); a
  *         2-D [rows, D] tensor is N = rows, H = 1. Read only.
@@ -488,13 +494,16 @@ SRA_API int sra_set_pdl(int enable);
  * Kernel-variant control, for A/B measurement of the per-shape dispatch.
  * op: "rmsnorm" (also used by add_rmsnorm), "rope_kv_store" (0 = one task of a
  * token per thread, 1 = two tasks per thread that read the same cos / sin chunk,
- * for an even n_head + 2 * n_kv_head), "glu", "decode_attention" (0 = CUDA-core kernel,
+ * for an even n_head + 2 * n_kv_head), "glu" (0 = columns over threads and rows over
+ * CTAs at 48 registers a thread, 1 = the same kernel with the registers the compiler
+ * picks), "decode_attention" (0 = CUDA-core kernel,
  * 1 = mma.sync kernel for bf16 / fp16 with head_dim 64 or 128).
  * variant: -1 = automatic per-shape choice (the default); otherwise an index
  * < sra_variant_count(op), optionally OR-ed with (nv << 8) to also force the
  * number of 16-byte accesses each thread holds in the register variants of
  * "rmsnorm" (nv in 1, 2, 3, 4, 6, 8; also 12 and 16 for the warp-per-row
- * variant). A forced setting that cannot serve a later
+ * variant; 8 or 16 for warps_row), and with (g << 16) to force the warps per row
+ * of warps_row (g in 2, 4, 8). A forced setting that cannot serve a later
  * call makes that call return SRA_ERR_VARIANT without enqueueing anything.
  * Returns SRA_OK, or SRA_ERR_ARG for an unknown op or out-of-range variant.
  */
@@ -506,7 +515,8 @@ SRA_API const char* sra_variant_name(const char* op, int variant);
  * The variant the automatic dispatch would pick for a call with these sizes and
  * all pointers and strides 16-byte aligned, on a GPU with num_sms SMs
  * (num_sms <= 0: query the current device). rmsnorm: a = rows, b = D;
- * rope_kv_store: a = T, b = n_head, c = n_kv_head, d = head_dim; glu: a = T, b = I;
+ * rope_kv_store: a = T, b = n_head, c = n_kv_head, d = head_dim; glu: a = T, b = I,
+ * c = act (0 = SiLU, 1 = ReLU);
  * decode_attention: a = B, b = n_head, c = n_kv_head, d = head_dim.
  * Negative sra_status on bad arguments. Enqueues nothing.
  */

@@ -107,6 +107,25 @@ class DecodeChain:
     def replay(self) -> None:
         self.graph.replay()
 
+    def capture_kind(self, kind: str, pdl: bool = True) -> torch.cuda.CUDAGraph:
+        """A CUDA graph of only the step's calls of one kernel kind ("add_rmsnorm",
+        "rope_kv_store" or "swiglu"), in chain order on the chain's own buffers: the
+        per-launch time of that kind inside a dependent chain, for per-kernel
+        accounting of the step."""
+        prev = sra.set_pdl(pdl)
+        try:
+            calls = [c for l in range(self.L) for k, c in self.layer_calls(l) if k == kind]
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                for c in calls:
+                    c()
+        finally:
+            sra.set_pdl(prev)
+        return g
+
+    def launches_per_step(self) -> dict:
+        return {"add_rmsnorm": 2 * self.L, "rope_kv_store": self.L, "swiglu": self.L}
+
     # ------------------------------------------------------------ accounting
     def bytes_per_step(self) -> dict:
         """Algorithmic HBM bytes of one step, per kernel kind (weights counted once)."""

@@ -21,6 +21,7 @@ std::atomic<int> g_smem_optin[kMaxDevices];
 std::atomic<int> g_force_norm{-1}, g_force_rope{-1}, g_force_glu{-1}, g_force_attn{-1};
 thread_local bool g_pdl = false;  // programmatic dependent launch for this thread's calls
 thread_local int g_force_nv = 0;  // accesses per thread forced for A/B measurement (0 = planner's)
+thread_local int g_force_g = 0;   // warps per row forced for warps_row A/B measurement (0 = planner's)
 
 // SM count of the current device (cached per device).
 int current_sm_count(int* dev_out) {
@@ -246,6 +247,35 @@ bool plan_norm_vector(int variant, int64_t rows, int64_t D, int vec, bool add, i
             p->grid = std::max<int64_t>(1, rows);
             return true;
         }
+        case NORM_WARPS_ROW: {
+            // G warps per row with NV (8 or 16) accesses per lane: the fewest warps that hold
+            // the row, then the fewest accesses per lane
+            int G = 0, nv = 0;
+            for (int g : {2, 4, 8}) {
+                if (g_force_g && g != g_force_g) continue;
+                for (int c : {8, 16}) {
+                    if (g_force_nv && c != g_force_nv) continue;
+                    if (32LL * g * c >= nacc) {
+                        G = g, nv = c;
+                        break;
+                    }
+                }
+                if (G) break;
+            }
+            if (!G || nacc <= 32 * 16 / 2) return false;  // rows a single warp holds take warp_rows
+            // groups per CTA (<= 256 threads): the smallest per-SM row load, ties to larger CTAs
+            int best = 1;
+            int64_t best_load = -1;
+            for (int gpc = 8 / G; gpc >= 1; gpc >>= 1) {
+                const int64_t load = ceil_div(ceil_div(rows, gpc), num_sms) * gpc;
+                if (best_load < 0 || load < best_load) best_load = load, best = gpc;
+            }
+            p->nv = nv;
+            p->group_warps = G;
+            p->threads = 32 * G * best;
+            p->grid = std::max<int64_t>(1, ceil_div(rows, best));
+            return true;
+        }
         case NORM_CTA_PAIR: {
             if (nvec < 2) return false;
             const int64_t half = norm_pair_half(nvec);
@@ -321,6 +351,7 @@ bool plan_norm_variant(int variant, int64_t rows, int64_t D, int vec, bool add, 
     p->pdl = g_pdl;
     p->num_sms = num_sms;
     p->stage_w = 0;
+    p->group_warps = 0;
     p->prefetch = rows <= 4LL * num_sms ? 1 : 0;
     // groups with a next row exist only past one row per resident group; with very
     // many rows they stream back to back anyway (measured: bench.py --sweep-variants)
@@ -334,8 +365,10 @@ int plan_norm(int64_t rows, int64_t D, int vec, bool add, int num_sms, const Sme
     const int forced = g_force_norm.load(std::memory_order_relaxed);
     if (forced >= 0) {
         g_force_nv = (forced >> 8) & 0xFF;
+        g_force_g = (forced >> 16) & 0xFF;
         const bool ok = plan_norm_variant(forced & 0xFF, rows, D, vec, add, num_sms, b, p);
         g_force_nv = 0;
+        g_force_g = 0;
         return ok ? SRA_OK : SRA_ERR_VARIANT;
     }
     const int64_t nacc = ceil_div(D, vec);
@@ -404,11 +437,13 @@ int plan_rope(int64_t T, int n_head, int n_kv, int head_dim, int pairs, int styl
 }
 
 // ------------------------------------------------------------------- GLU plan
-int plan_glu(int64_t T, int64_t I, int vec, int num_sms, GluPlan* p) {
+int plan_glu(int64_t T, int64_t I, int vec, int act, int num_sms, GluPlan* p) {
     const int forced = g_force_glu.load(std::memory_order_relaxed);
-    if (forced > 0) return SRA_ERR_VARIANT;
     const int64_t nv = I / vec;
-    p->variant = GLU_COLS_ROWS;
+    // Measured on GB300 (bench.py --sweep-variants, streaming): SiLU runs faster with the
+    // registers the compiler picks (58 on 16-byte vectors, four CTAs per SM: T = 4096 53.2 against
+    // 55.2 us, T = 512 8.2 against 8.8 us); ReLU at 48 (51.2 against 52.2 us at T = 4096)
+    p->variant = forced >= 0 ? forced : (act == 0 ? GLU_COLS_ROWS_REGS : GLU_COLS_ROWS);
     p->vec = vec;
     p->pdl = g_pdl;
     p->num_sms = num_sms;
@@ -754,7 +789,7 @@ int sra_glu(const void* gate_up, void* out, int64_t T, int64_t I, int64_t in_row
     const int sms = current_sm_count(&dev);
     if (sms <= 0) return SRA_ERR_DEVICE;
     GluPlan plan;
-    int st = plan_glu(T, I, glu_vec(dtype, gate_up, out, I, in_row_stride, out_row_stride), sms, &plan);
+    int st = plan_glu(T, I, glu_vec(dtype, gate_up, out, I, in_row_stride, out_row_stride), act, sms, &plan);
     if (st != SRA_OK) return st;
     GluArgs a;
     a.gate_up = gate_up;
@@ -1091,7 +1126,7 @@ int sra_uclip(const void* x, const float* alpha, const float* gamma, void* out, 
 int sra_force_variant(const char* op, int variant) {
     std::atomic<int>* slot = force_slot(op);
     if (!slot) return SRA_ERR_ARG;
-    if (variant < -1 || (variant >= 0 && ((variant & 0xFF) >= variant_count(op) || (variant >> 16) != 0)))
+    if (variant < -1 || (variant >= 0 && ((variant & 0xFF) >= variant_count(op) || (variant >> 24) != 0)))
         return SRA_ERR_ARG;
     slot->store(variant, std::memory_order_relaxed);
     return SRA_OK;
@@ -1100,10 +1135,10 @@ int sra_force_variant(const char* op, int variant) {
 int sra_variant_count(const char* op) { return variant_count(op); }
 
 const char* sra_variant_name(const char* op, int variant) {
-    static const char* const norm_names[] = {"warp_rows", "cta_row",   "cta_smem",  "two_pass",
-                                             "cta_pair",  "warp_smem", "pair_smem", "cta_lean"};
+    static const char* const norm_names[] = {"warp_rows", "cta_row",   "cta_smem",  "two_pass", "cta_pair",
+                                             "warp_smem", "pair_smem", "cta_lean",  "warps_row"};
     static const char* const rope_names[] = {"token_cta", "token_cta2"};
-    static const char* const glu_names[] = {"cols_rows"};
+    static const char* const glu_names[] = {"cols_rows", "cols_rows_regs"};
     static const char* const attn_names[] = {"cuda_cores", "mma_sync"};
     const int n = variant_count(op);
     if (n < 0 || variant < 0 || variant >= n) return nullptr;
@@ -1144,7 +1179,7 @@ int sra_pick_variant(const char* op, int64_t a, int64_t b, int64_t c, int64_t d,
     }
     if (a < 0 || b <= 0) return SRA_ERR_SHAPE;
     GluPlan p;
-    const int st = plan_glu(a, b, 16 / es, num_sms, &p);
+    const int st = plan_glu(a, b, 16 / es, c == 1 ? 1 : 0, num_sms, &p);
     return st == SRA_OK ? p.variant : st;
 }
 

@@ -262,6 +262,89 @@ struct Vec {
 template <typename T> __host__ __device__ constexpr int vec16() { return 16 / int(sizeof(T)); }
 
 // ---------------------------------------------------------------------------
+// Gated linear units: act(g) * u in fp32, act = SiLU (ACT 0) or ReLU (ACT 1).
+//
+// SiLU as g / (1 + e^-g) with one ex2 and one fast reciprocal; the fast
+// reciprocal returns 0 once its divisor passes 2^126 (g below -87.3), and the
+// true value there is still a normal number of bf16 and fp32 (silu(-88) is about
+// -5e-37). So gates below -64 take another form: there e^g < 2^-92, so 1 + e^g
+// rounds to 1 in fp32 and silu(g) * u = g * u * e^g to far below an fp32 ulp.
+// e^g itself leaves fp32's normal range below -87.3, so it is applied as four
+// equal factors e^(g/4) (g/4 is exact), the operand u scaled down first: every
+// intermediate is a normal fp32 number whenever the result is one, and the
+// result is within a few fp32 ulps of the exact product (expf is CUDA's accurate
+// exponential). A NaN gate stays NaN; -inf gives NaN, as g / (1 + e^-g) does.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float silu_mul_far(float g, float u) {
+    const float e = expf(0.25f * g);
+    return (((u * e) * g) * e) * e * e;
+}
+
+constexpr float kSiluFar = -64.0f;  // gates below take silu_mul_far
+
+// act(g) * u in the fast form: g / (1 + e^-g) (one ex2, one fast reciprocal),
+// times u. Exact to a few fp32 ulps for gates at or above kSiluFar, except that
+// for a gate below 2^-64 in size g * sigma can be an fp32 subnormal whose lost
+// digits a large u would scale back into view; glu_mul covers both cases.
+template <int ACT>
+__device__ __forceinline__ float glu_mul_fast(float g, float u) {
+    if constexpr (ACT == 0) {
+        return __fdividef(g, 1.0f + __expf(-g)) * u;
+    } else {
+        return fmaxf(g, 0.0f) * u;
+    }
+}
+
+// act(g) * u for every gate. Below kSiluFar: silu_mul_far. Otherwise sigma(g) =
+// 1 / (1 + e^-g) first and then g * u * sigma in the order that keeps the
+// partial product normal: g * u first for |g| < 1 (no overflow there: |g u| <
+// |u|), g * sigma first otherwise (at least 64 e^-64 in size, and g * u could
+// overflow where the result does not).
+template <int ACT>
+__device__ __forceinline__ float glu_mul(float g, float u) {
+    if constexpr (ACT == 0) {
+        if (g < kSiluFar) return silu_mul_far(g, u);
+        const float sig = __fdividef(1.0f, 1.0f + __expf(-g));
+        return fabsf(g) < 1.0f ? (g * u) * sig : (g * sig) * u;
+    } else {
+        return fmaxf(g, 0.0f) * u;
+    }
+}
+
+// Whether a raw vector of gates needs glu_mul's careful forms (never on the
+// configured inputs): a gate below -64 — a negative value's bit pattern grows with
+// its magnitude, so that is an unsigned compare of each element's bits with those
+// of -64 (negative NaNs compare above it too; glu_mul keeps them NaN) — or, in
+// fp32, a nonzero gate below 2^-64 in size, whose g * sigma could be subnormal.
+// In bf16 and fp16 the smallest gate, halved, is still an fp32 number with 15 or
+// more significant bits, so only the far-negative test applies there.
+template <typename T> struct FarBits;
+template <> struct FarBits<__nv_bfloat16> { static constexpr uint32_t v = 0xC280u; };
+template <> struct FarBits<__half> { static constexpr uint32_t v = 0xD400u; };
+template <> struct FarBits<float> { static constexpr uint32_t v = 0xC2800000u; };
+
+template <typename T, int VEC>
+__device__ __forceinline__ bool needs_careful(const typename Vec<T, VEC>::Raw& gr) {
+    constexpr int BYTES = VEC * int(sizeof(T));
+    if constexpr (BYTES == 2) {
+        return static_cast<uint32_t>(gr) > FarBits<T>::v;
+    } else {
+        uint32_t hit = 0;
+#pragma unroll
+        for (int i = 0; i < BYTES / 4; ++i) {
+            const uint32_t w = word(gr, i);
+            if constexpr (sizeof(T) == 4) {
+                const uint32_t m = w & 0x7fffffffu;
+                hit |= (w > FarBits<T>::v || (m != 0u && m < 0x1f800000u)) ? 1u : 0u;  // 2^-64
+            } else {
+                hit |= __vcmpgtu2(w, FarBits<T>::v * 0x10001u);
+            }
+        }
+        return hit != 0;
+    }
+}
+
+// ---------------------------------------------------------------------------
 // Reductions
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ float warp_sum(float v) {
@@ -286,6 +369,58 @@ __device__ __forceinline__ float block_sum(float v, float* scratch) {
     float total = scratch[32];
     __syncthreads();  // scratch may be reused by the next row
     return total;
+}
+
+// Double-precision sum over a warp / a CTA (for the rare rows whose fp32 sum of
+// squares leaves fp32's range). `scratch` holds >= 33 doubles of shared memory.
+__device__ __forceinline__ double warp_sum_d(double v) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ double block_sum_d(double v, double* scratch) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    v = warp_sum_d(v);
+    if (lane == 0) scratch[warp] = v;
+    __syncthreads();
+    if (warp == 0) {
+        double s = lane < nwarps ? scratch[lane] : 0.0;
+        s = warp_sum_d(s);
+        if (lane == 0) scratch[32] = s;
+    }
+    __syncthreads();
+    const double total = scratch[32];
+    __syncthreads();
+    return total;
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm scale outside fp32's comfortable range.
+//
+// The sum of squares is accumulated in fp32. It overflows for rows with
+// elements of about 1.8e19 and up (bf16 and fp32 hold up to 3.4e38), and once
+// sum / D + eps falls below 2^-64, squares in fp32's subnormal range have lost
+// digits that then matter. Rows in either case (never the configured inputs)
+// are summed again in double, and the factor 1 / sqrt(mean + eps) is split
+// into a power of two `pre` and an fp32 `rinv`: out = ((x * pre) * rinv) * w,
+// every factor finite and normal (the factor itself can exceed fp32's range,
+// up to about 2^155 for rows of fp32 subnormals with eps = 0). A NaN sum stays
+// on the ordinary path (every output is NaN either way).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool ss_in_range(float ss, int64_t D, float eps) {
+    return !(ss > 3.40282347e38f) && !(ss / static_cast<float>(D) + eps < 0x1p-64f);
+}
+
+struct WideScale {
+    float pre, rinv;
+};
+
+__device__ __forceinline__ WideScale wide_scale(double sd, int64_t D, float eps) {
+    const double rd = 1.0 / sqrt(sd / static_cast<double>(D) + static_cast<double>(eps));
+    if (rd > 0x1p64) return {0x1p64f, static_cast<float>(rd * 0x1p-64)};
+    if (rd < 0x1p-64) return {0x1p-64f, static_cast<float>(rd * 0x1p64)};
+    return {1.0f, static_cast<float>(rd)};
 }
 
 }  // namespace sra

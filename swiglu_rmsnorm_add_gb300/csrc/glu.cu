@@ -15,23 +15,14 @@
 // when the row widths, strides and base pointers allow.
 //
 // SiLU: g / (1 + e^-g) with one ex2 and one reciprocal (fast intrinsics,
-// relative error ~1e-6, far inside half an output ulp of bf16 or fp16). For
-// g < -87.3 the denominator leaves the reciprocal's range and the result is 0,
-// where the true SiLU magnitude is below 2^-119.
+// relative error ~1e-6, far inside half an output ulp of bf16 or fp16); gates
+// below -64 take the scaled form of glu_mul (common.cuh), which stays accurate
+// down to the smallest outputs the formats hold.
 #include "common.cuh"
 #include "internal.h"
 
 namespace sra {
 namespace glu {
-
-template <int ACT>
-__device__ __forceinline__ float act(float g) {
-    if constexpr (ACT == 0) {
-        return __fdividef(g, 1.0f + __expf(-g));
-    } else {
-        return fmaxf(g, 0.0f);
-    }
-}
 
 template <typename T, int VEC, int ACT>
 __device__ __forceinline__ typename Vec<T, VEC>::Raw combine(const typename Vec<T, VEC>::Raw& gr,
@@ -41,12 +32,36 @@ __device__ __forceinline__ typename Vec<T, VEC>::Raw combine(const typename Vec<
     V::unpack(gr, g);
     V::unpack(ur, u);
 #pragma unroll
-    for (int i = 0; i < VEC; ++i) g[i] = act<ACT>(g[i]) * u[i];
+    for (int i = 0; i < VEC; ++i) g[i] = glu_mul_fast<ACT>(g[i], u[i]);
     return V::pack(g);
 }
 
+// Output vector t of this thread through glu_mul one element at a time, re-read
+// from memory (the rare vectors needs_careful finds; kept scalar and rolled so the
+// common path keeps its registers).
 template <typename T, int VEC, int ACT>
-__global__ void __launch_bounds__(256) cols_rows_kernel(GluArgs a) {
+__device__ __forceinline__ void careful_vec(const T* g, T* o, int64_t I) {
+#pragma unroll 1
+    for (int i = 0; i < VEC; ++i) o[i] = from_f32<T>(glu_mul<ACT>(to_f32(g[i]), to_f32(g[i + I])));
+}
+
+// Store the result of row t's vector: the fast form, or careful_vec.
+template <typename T, int VEC, int ACT>
+__device__ __forceinline__ void emit(const typename Vec<T, VEC>::Raw& gr, const typename Vec<T, VEC>::Raw& ur,
+                                     const T* g, T* o, int64_t I) {
+    using V = Vec<T, VEC>;
+    if (ACT == 0 && __builtin_expect(needs_careful<T, VEC>(gr), 0)) {
+        careful_vec<T, VEC, ACT>(g, o, I);
+    } else {
+        V::store_stream(o, combine<T, VEC, ACT>(gr, ur));
+    }
+}
+
+// MINB: the CTAs of 256 threads each SM should hold (the launch bound): 5 caps the
+// kernel at 48 registers a thread (variant cols_rows, the default), 1 lets the
+// compiler take the registers it wants (variant cols_rows_regs, for A/B).
+template <typename T, int VEC, int ACT, int MINB>
+__global__ void __launch_bounds__(256, MINB) cols_rows_kernel(GluArgs a) {
     using V = Vec<T, VEC>;
     using R = typename V::Raw;
     const int64_t nv = a.I / VEC;
@@ -89,8 +104,8 @@ __global__ void __launch_bounds__(256) cols_rows_kernel(GluArgs a) {
             gd = V::load_stream(gcol + (tn + step) * a.is);
             ud = V::load_stream(gcol + (tn + step) * a.is + a.I);
         }
-        V::store_stream(ocol + t * a.os, combine<T, VEC, ACT>(ga, ua));
-        if (have1) V::store_stream(ocol + (t + step) * a.os, combine<T, VEC, ACT>(gb, ub));
+        emit<T, VEC, ACT>(ga, ua, gcol + t * a.is, ocol + t * a.os, a.I);
+        if (have1) emit<T, VEC, ACT>(gb, ub, gcol + (t + step) * a.is, ocol + (t + step) * a.os, a.I);
         if (!next0) break;
         ga = gc, ua = uc, gb = gd, ub = ud;
         have1 = next1;
@@ -100,7 +115,7 @@ __global__ void __launch_bounds__(256) cols_rows_kernel(GluArgs a) {
 
 template <typename T, int VEC, int ACT>
 cudaError_t launch_vec(const GluArgs& a, const GluPlan& p, cudaStream_t s) {
-    auto kernel = cols_rows_kernel<T, VEC, ACT>;
+    auto kernel = p.variant == GLU_COLS_ROWS_REGS ? cols_rows_kernel<T, VEC, ACT, 1> : cols_rows_kernel<T, VEC, ACT, 5>;
     // Rows are strided over grid_y; size it so that grid_x * grid_y CTAs are all
     // resident at once (one wave, every CTA with the same number of rows +- 1).
     const int64_t resident = static_cast<int64_t>(resident_ctas_per_sm(kernel, p.threads, 0)) * p.num_sms;
@@ -130,7 +145,7 @@ cudaError_t launch_typed(const GluArgs& a, const GluPlan& p, int act_kind, cudaS
 }  // namespace glu
 
 cudaError_t launch_glu(const GluArgs& a, const GluPlan& p, int act, int dtype, cudaStream_t s) {
-    if (p.variant != GLU_COLS_ROWS) return cudaErrorInvalidValue;
+    if (p.variant != GLU_COLS_ROWS && p.variant != GLU_COLS_ROWS_REGS) return cudaErrorInvalidValue;
     switch (dtype) {
         case DT_F32: return glu::launch_typed<float>(a, p, act, s);
         case DT_F16: return glu::launch_typed<__half>(a, p, act, s);

@@ -34,7 +34,9 @@ enum NormVariant {
     NORM_WARP_SMEM = 5,  // one warp per row, row landed in shared memory (cp.async)
     NORM_PAIR_SMEM = 6,  // a 2-CTA cluster per row, half the row in each CTA's shared memory
     NORM_CTA_LEAN = 7,   // one CTA (<= 256 threads) per row, row in registers, w read in the scale loop
-    NORM_NUM_VARIANTS = 8
+    NORM_WARPS_ROW = 8,  // 2, 4 or 8 warps per row, row in registers, w read in the scale loop;
+                         // the warps' partial sums meet behind a named barrier of just those warps
+    NORM_NUM_VARIANTS = 9
 };
 
 #ifdef __CUDACC__
@@ -58,6 +60,7 @@ struct NormPlan {
     int stage_w;    // staged kernels: stage the w slice in shared memory
     int prefetch;   // L2 prefetch of the first rows before the launch wait
     int next_prefetch;  // L2 prefetch of each group's next row
+    int group_warps;    // warps_row: warps per row (2, 4 or 8)
 };
 
 cudaError_t launch_rmsnorm(const NormArgs& a, const NormPlan& p, int dtype, cudaStream_t s);
@@ -112,7 +115,11 @@ struct GluArgs {
     int64_t is, os;       // row strides, elements
 };
 
-enum GluVariant { GLU_COLS_ROWS = 0, GLU_NUM_VARIANTS = 1 };
+enum GluVariant {
+    GLU_COLS_ROWS = 0,       // columns over threads, rows over CTAs; 48 registers (five 256-thread CTAs per SM)
+    GLU_COLS_ROWS_REGS = 1,  // the same kernel with the registers the compiler wants (A/B)
+    GLU_NUM_VARIANTS = 2
+};
 
 struct GluPlan {
     int variant;

@@ -123,15 +123,6 @@ __host__ __device__ constexpr size_t smem_bytes(int MT, int PRO) {
 // 16-byte chunk c of row r of a row-major tile whose rows hold `cpr` chunks.
 __device__ __forceinline__ int swz(int r, int c) { return c ^ (r & 7); }
 
-template <int ACT>
-__device__ __forceinline__ float glu_act(float g) {
-    if constexpr (ACT == 0) {
-        return __fdividef(g, 1.0f + __expf(-g));
-    } else {
-        return fmaxf(g, 0.0f);
-    }
-}
-
 // PRO: 0 = RMSNorm prologue, 1 = SwiGLU, 2 = ReGLU, 3 = none (the input rows are h, already
 // produced by the prologue's own kernel). The tensor maps: tmW over W [N][K] and tmX over the
 // input rows [B][K] (GLU: [B][2K]), both with 64 x 64 (rows: MT*16) boxes and the 128-byte
@@ -153,6 +144,8 @@ __global__ void __launch_bounds__(warps_for(MT) * 32) linear_kernel(LinArgs a, c
     __shared__ uint64_t xfull[SX];  // input tile t: slot t % SX, xfull[t % SX]
     __shared__ float stat[64];
     __shared__ float inv[64];
+    __shared__ float pre[64];     // RMSNorm rows past fp32's sum range: a power-of-two pre-scale
+    __shared__ double dstat[64];  // ... and their sums of squares again, in double
     cg::cluster_group cluster = cg::this_cluster();
     const int SK = static_cast<int>(cluster.num_blocks());
     const int rank = static_cast<int>(cluster.block_rank());
@@ -229,6 +222,20 @@ __global__ void __launch_bounds__(warps_for(MT) * 32) linear_kernel(LinArgs a, c
         for (int i = 0; i < XR * 8 / (NW * 32); ++i) {
             const int c = threadIdx.x + NW * 32 * i, r = c >> 3, ch = c & 7;
             float f[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+            if constexpr (PRO == 1) {
+                // a chunk holding a gate below -64 (never on the configured inputs): each
+                // element through glu_mul, scalar, straight into the h tile
+                if (r < rows && __builtin_expect(needs_careful<T, 8>(
+                                                     *reinterpret_cast<const R8*>(xs + r * kKT + swz(r, ch) * 8)),
+                                                 0)) {
+                    const T* gp = xs + r * kKT + swz(r, ch) * 8;
+                    const T* up = xs + (XR + r) * kKT + swz(r, ch) * 8;
+                    T* hp = hb + r * kKT + swz(r, ch) * 8;
+#pragma unroll 1
+                    for (int e = 0; e < 8; ++e) hp[e] = to_t<T>(glu_mul<0>(to_f32(gp[e]), to_f32(up[e])));
+                    continue;
+                }
+            }
             if (r < rows) {
                 float g[8];
                 V8::unpack(*reinterpret_cast<const R8*>(xs + r * kKT + swz(r, ch) * 8), f);
@@ -236,13 +243,13 @@ __global__ void __launch_bounds__(warps_for(MT) * 32) linear_kernel(LinArgs a, c
                     // h as given
                 } else if constexpr (PRO == 0) {
                     V8::unpack(*reinterpret_cast<const R8*>(xs + XR * kKT + ch * 8), g);
-                    const float iv = inv[r];
+                    const float iv = inv[r], pv = pre[r];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = f[e] * iv * g[e];
+                    for (int e = 0; e < 8; ++e) f[e] = f[e] * pv * iv * g[e];
                 } else {
                     V8::unpack(*reinterpret_cast<const R8*>(xs + (XR + r) * kKT + swz(r, ch) * 8), g);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = glu_act<PRO - 1>(f[e]) * g[e];
+                    for (int e = 0; e < 8; ++e) f[e] = glu_mul_fast<PRO - 1>(f[e], g[e]);
                 }
             }
             *reinterpret_cast<R8*>(hb + r * kKT + swz(r, ch) * 8) = V8::pack(f);
@@ -279,12 +286,47 @@ __global__ void __launch_bounds__(warps_for(MT) * 32) linear_kernel(LinArgs a, c
             if (lane == 0) stat[warp + NW * i] = t;
         }
         cluster.sync();  // every rank's partial sums are in its shared memory
+        int wide = 0;
         for (int r = threadIdx.x; r < MT * 16; r += NW * 32) {
             float tot = 0.0f;
             for (int q = 0; q < SK; ++q) tot += cluster.map_shared_rank(stat, q)[r];
             inv[r] = rsqrtf(tot / static_cast<float>(a.K) + a.eps);
+            pre[r] = 1.0f;
+            wide |= r < rows && !ss_in_range(tot, a.K, a.eps);
         }
-        __syncthreads();  // inv complete before the first h tile
+        // inv complete before the first h tile. Every rank adds the same partials in the
+        // same order, so `wide` is the same on all ranks of the cluster.
+        if (__syncthreads_or(wide)) {
+            // rows whose fp32 sum left fp32's range: each rank sums its K range again in
+            // double, and the cluster exchanges those sums
+#pragma unroll
+            for (int i = 0; i < RPW; ++i) {
+                const int r = warp + NW * i;
+                double sd = 0.0;
+                if (r < rows) {
+                    for (int k = lane * 8; k < ntiles * kKT; k += 256) {
+                        float f[8];
+                        V8::unpack(V8::load(X + (r0 + r) * a.xs + kbase + k), f);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) sd += static_cast<double>(f[e]) * static_cast<double>(f[e]);
+                    }
+                }
+                sd = warp_sum_d(sd);
+                if (lane == 0) dstat[r] = sd;
+            }
+            cluster.sync();
+            for (int r = threadIdx.x; r < rows; r += NW * 32) {
+                float tot = 0.0f;
+                for (int q = 0; q < SK; ++q) tot += cluster.map_shared_rank(stat, q)[r];
+                if (!ss_in_range(tot, a.K, a.eps)) {
+                    double sd = 0.0;
+                    for (int q = 0; q < SK; ++q) sd += cluster.map_shared_rank(dstat, q)[r];
+                    const WideScale sc = wide_scale(sd, a.K, a.eps);
+                    inv[r] = sc.rinv, pre[r] = sc.pre;
+                }
+            }
+            __syncthreads();
+        }
     }
     if (ntiles > 0) {
         mbar_wait(&xfull[0], 0);
@@ -518,7 +560,7 @@ __host__ __device__ inline size_t ring16_bytes() {
     return ring > part ? ring : part;
 }
 __host__ __device__ inline size_t smem16_bytes(int rows, int64_t K) {
-    return ring16_bytes() + static_cast<size_t>(rows + 1) * K * 2 + 64 * 4;
+    return ring16_bytes() + static_cast<size_t>(rows + 1) * K * 2 + 2 * 64 * 4;
 }
 
 template <typename T, int PRO>
@@ -535,6 +577,7 @@ __global__ void __launch_bounds__(kNW16 * 32) linear16_kernel(LinArgs a) {
     T* hsm = reinterpret_cast<T*>(smem + ring16_bytes());  // [rows][K], then one zero row
     T* zrow = hsm + static_cast<int64_t>(rows) * a.K;
     float* inv = reinterpret_cast<float*>(smem + ring16_bytes() + static_cast<size_t>(rows + 1) * a.K * 2);
+    float* pre = inv + 64;  // RMSNorm rows past fp32's sum range: a power-of-two pre-scale
     const T* W = static_cast<const T*>(a.W);
     const T* X = static_cast<const T*>(a.x);
     // this warp's tiles: t = warp, warp + 8, ...; j-th of them into ring slot j % stages
@@ -584,7 +627,19 @@ __global__ void __launch_bounds__(kNW16 * 32) linear16_kernel(LinArgs a) {
                 }
             }
             ss = warp_sum(ss);
-            if (lane == 0) inv[r] = rsqrtf(ss / static_cast<float>(a.K) + a.eps);
+            float iv = rsqrtf(ss / static_cast<float>(a.K) + a.eps), pv = 1.0f;
+            if (!ss_in_range(ss, a.K, a.eps)) {  // the row again, in double
+                double sd = 0.0;
+                for (int64_t k0 = lane * 8; k0 < a.K; k0 += 256) {
+                    float f[8];
+                    V8::unpack(V8::load(xr + k0), f);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) sd += static_cast<double>(f[e]) * static_cast<double>(f[e]);
+                }
+                const WideScale sc = wide_scale(warp_sum_d(sd), a.K, a.eps);
+                iv = sc.rinv, pv = sc.pre;
+            }
+            if (lane == 0) inv[r] = iv, pre[r] = pv;
         }
         __syncthreads();
     }
@@ -608,16 +663,27 @@ __global__ void __launch_bounds__(kNW16 * 32) linear16_kernel(LinArgs a) {
             const int c = c0 + u * kNW16 * 32;
             if (c < total) {
                 const int r = c / cpr, ch = c - r * cpr;
+                if constexpr (PRO == 1) {
+                    // a chunk holding a gate below -64 (never on the configured inputs): each
+                    // element through glu_mul, scalar, re-read from x
+                    if (__builtin_expect(needs_careful<T, 8>(xv[u]), 0)) {
+                        const T* xr = X + r * a.xs + ch * 8;
+                        T* hp = hsm + static_cast<int64_t>(r) * a.K + swz(r, ch) * 8;
+#pragma unroll 1
+                        for (int e = 0; e < 8; ++e) hp[e] = to_t<T>(glu_mul<0>(to_f32(xr[e]), to_f32(xr[e + a.K])));
+                        continue;
+                    }
+                }
                 float f[8], g[8];
                 V8::unpack(xv[u], f);
                 V8::unpack(gv[u], g);
                 if constexpr (PRO == 0) {
-                    const float iv = inv[r];
+                    const float iv = inv[r], pv = pre[r];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = f[e] * iv * g[e];
+                    for (int e = 0; e < 8; ++e) f[e] = f[e] * pv * iv * g[e];
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) f[e] = glu_act<PRO - 1>(f[e]) * g[e];
+                    for (int e = 0; e < 8; ++e) f[e] = glu_mul_fast<PRO - 1>(f[e], g[e]);
                 }
                 *reinterpret_cast<R8*>(hsm + static_cast<int64_t>(r) * a.K + swz(r, ch) * 8) = V8::pack(f);
             }
@@ -757,6 +823,7 @@ __global__ void __launch_bounds__(128) linear_simple_kernel(LinArgs a) {
     extern __shared__ __align__(16) unsigned char smem[];
     float* h = reinterpret_cast<float*>(smem);
     __shared__ float red[33];
+    __shared__ double dred[33];
     const int64_t b = blockIdx.y;
     const T* xr = static_cast<const T*>(a.x) + b * a.xs;
     pdl_enter();
@@ -767,13 +834,22 @@ __global__ void __launch_bounds__(128) linear_simple_kernel(LinArgs a) {
             ss = fmaf(v, v, ss);
         }
         ss = block_sum(ss, red);
-        const float iv = rsqrtf(ss / static_cast<float>(a.K) + a.eps);
+        float iv = rsqrtf(ss / static_cast<float>(a.K) + a.eps), pv = 1.0f;
+        if (!ss_in_range(ss, a.K, a.eps)) {  // the row again, in double
+            double sd = 0.0;
+            for (int64_t k = threadIdx.x; k < a.K; k += blockDim.x) {
+                const double v = to_f32(xr[k]);
+                sd += v * v;
+            }
+            const WideScale sc = wide_scale(block_sum_d(sd, dred), a.K, a.eps);
+            iv = sc.rinv, pv = sc.pre;
+        }
         const T* wl = static_cast<const T*>(a.w_ln);
         for (int64_t k = threadIdx.x; k < a.K; k += blockDim.x)
-            h[k] = round_trip<T>(to_f32(xr[k]) * iv * to_f32(wl[k]));
+            h[k] = round_trip<T>(to_f32(xr[k]) * pv * iv * to_f32(wl[k]));
     } else {
         for (int64_t k = threadIdx.x; k < a.K; k += blockDim.x)
-            h[k] = round_trip<T>(glu_act<PRO - 1>(to_f32(xr[k])) * to_f32(xr[k + a.K]));
+            h[k] = round_trip<T>(glu_mul<PRO - 1>(to_f32(xr[k]), to_f32(xr[k + a.K])));
     }
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;

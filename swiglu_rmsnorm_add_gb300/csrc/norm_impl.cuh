@@ -21,12 +21,21 @@
 //              the weight slice copied in the same round trip; the resident row
 //              count is then bounded by shared memory instead of registers
 //   two_pass   a CTA per row, the scale pass re-reads the row (any width)
+//   warps_row  G = 2, 4 or 8 warps per row, the row in registers and w read in
+//              the scale loop; the warps' partial sums meet in shared memory
+//              behind a named barrier of just those G warps (rows of 513 to
+//              2048 accesses at a few hundred rows: no CTA-wide barrier, and
+//              the rows dealt evenly over all SMs)
 // Layouts that are not 16-byte aligned use scalar register kernels.
 // A predicated scalar tail covers D % VEC; nothing is padded to a power of two.
 // Every thread reads back and writes only its own elements, so in-place use
-// (out == x) is safe. Each translation unit instantiates one ADD value only
-// (norm_rms.cu: false, norm_add.cu: true), so no kernel is registered from two
-// modules.
+// (out == x) is safe. A row whose fp32 sum of squares overflows, or is too small
+// for fp32 to hold its digits (ss_in_range, common.cuh), is summed again in
+// double from the values the thread already holds, and scaled by wide_scale's
+// power of two `pre` and fp32 `rinv` (out = ((x * pre) * rinv) * w; pre is 1 on
+// every other row): the same result the exact formula gives, for every finite
+// input. Each translation unit instantiates one ADD value only (norm_rms.cu:
+// false, norm_add.cu: true), so no kernel is registered from two modules.
 #pragma once
 
 #include <cooperative_groups.h>
@@ -46,15 +55,35 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // How a row's sum of squares is reduced, and which threads share a row.
-enum Reduce { RED_WARP = 0, RED_CTA = 1, RED_PAIR = 2 };
+enum Reduce { RED_WARP = 0, RED_CTA = 1, RED_PAIR = 2, RED_GROUP = 3 };
+
+// Barrier of the G warps of this warp's group (id 1 + group; id 0 is the CTA's).
+template <int G>
+__device__ __forceinline__ void group_barrier() {
+    asm volatile("bar.sync %0, %1;" ::"r"(1 + static_cast<int>(threadIdx.x >> 5) / G), "r"(32 * G) : "memory");
+}
 
 __host__ __device__ constexpr size_t round16(size_t b) { return (b + 15) / 16 * 16; }
 
 // Sum of squares of one row reduced over the group; every thread gets it.
-template <int RED>
+// RED_GROUP (G warps per row): each warp's sum goes to its slot of the row's
+// parity, scratch[32 * parity + warp]; one barrier of the group publishes them.
+// The next row writes the other parity's slots, and the row after that can only
+// reach its own writes once every warp of the group has passed the next row's
+// barrier, i.e. has read this row's slots: one barrier per row suffices.
+template <int RED, int G = 1>
 __device__ __forceinline__ float group_sum(float ss, float* scratch, float* pair_slot, int parity) {
     if constexpr (RED == RED_WARP) {
         return warp_sum(ss);
+    } else if constexpr (RED == RED_GROUP) {
+        const int warp = static_cast<int>(threadIdx.x >> 5), first = warp / G * G;
+        ss = warp_sum(ss);
+        if ((threadIdx.x & 31) == 0) scratch[32 * parity + warp] = ss;
+        group_barrier<G>();
+        float tot = 0.0f;
+#pragma unroll
+        for (int i = 0; i < G; ++i) tot += scratch[32 * parity + first + i];  // the same order in every warp
+        return tot;
     } else if constexpr (RED == RED_CTA) {
         return block_sum(ss, scratch);
     } else {
@@ -70,6 +99,41 @@ __device__ __forceinline__ float group_sum(float ss, float* scratch, float* pair
     }
 }
 
+// The same in double (rare rows only). `scratch` is the float scratch of
+// group_sum, 8-byte aligned and >= 66 floats; `pair_slot` >= 6 floats (the
+// doubles live in its floats 2..5, double-buffered by row parity).
+// RED_GROUP: `pair_slot` holds 32 doubles, one per warp; the next use of a slot
+// comes after at least one more group_sum barrier, which every warp passes only
+// after reading this one.
+template <int RED, int G = 1>
+__device__ __forceinline__ double group_sum_d(double v, float* scratch, float* pair_slot, int parity) {
+    if constexpr (RED == RED_WARP) {
+        return warp_sum_d(v);
+    } else if constexpr (RED == RED_GROUP) {
+        double* slot = reinterpret_cast<double*>(pair_slot);
+        const int warp = static_cast<int>(threadIdx.x >> 5), first = warp / G * G;
+        v = warp_sum_d(v);
+        if ((threadIdx.x & 31) == 0) slot[warp] = v;
+        group_barrier<G>();
+        double tot = 0.0;
+#pragma unroll
+        for (int i = 0; i < G; ++i) tot += slot[first + i];
+        return tot;
+    } else if constexpr (RED == RED_CTA) {
+        return block_sum_d(v, reinterpret_cast<double*>(scratch));
+    } else {
+        const double part = block_sum_d(v, reinterpret_cast<double*>(scratch));
+        double* slot = reinterpret_cast<double*>(pair_slot + 2);
+        cg::cluster_group cl = cg::this_cluster();
+        if (threadIdx.x == 0) slot[parity] = part;
+        cl.sync();
+        const double peer = *cl.map_shared_rank(slot + parity, static_cast<int>(cl.block_rank()) ^ 1);
+        return part + peer;
+    }
+}
+
+__device__ __forceinline__ double sq_d(float v) { return static_cast<double>(v) * static_cast<double>(v); }
+
 // ------------------------------------------------------------------ staged
 // T with 16-byte accesses (VEC = 16 / sizeof(T)). Shared memory:
 //   [ws: the w slice if a.stage_w] [per group: x slice][per group: res slice (ADD)]
@@ -79,8 +143,8 @@ __global__ void __launch_bounds__(1024) staged_rows_kernel(NormArgs a) {
     constexpr int VEC = vec16<T>();
     using V = Vec<T, VEC>;
     extern __shared__ __align__(16) unsigned char dyn_smem[];
-    __shared__ float scratch[33];
-    __shared__ float pair_slot[2];
+    __shared__ __align__(8) float scratch[66];
+    __shared__ __align__(8) float pair_slot[6];
     pdl_enter();
 
     const int64_t nvec = a.D / VEC;
@@ -183,18 +247,29 @@ __global__ void __launch_bounds__(1024) staged_rows_kernel(NormArgs a) {
             ss = fmaf(xt, xt, ss);
         }
         ss = group_sum<RED>(ss, scratch, pair_slot, parity);
+        float rinv = rsqrtf(ss / static_cast<float>(a.D) + a.eps), pre = 1.0f;
+        if (__builtin_expect(!ss_in_range(ss, a.D, a.eps), 0)) {
+            double sd = tid < tail ? sq_d(xt) : 0.0;
+            for (int64_t idx = a0 + tid; idx < a1; idx += threads) {
+                float xf[VEC];
+                V::unpack(V::load(xs + (idx - a0) * VEC), xf);
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) sd += sq_d(xf[i]);
+            }
+            const WideScale sc = wide_scale(group_sum_d<RED>(sd, scratch, pair_slot, parity), a.D, a.eps);
+            pre = sc.pre, rinv = sc.rinv;
+        }
         parity ^= 1;
-        const float rinv = rsqrtf(ss / static_cast<float>(a.D) + a.eps);
 
         for (int64_t idx = a0 + tid; idx < a1; idx += threads) {
             float xf[VEC], wf[VEC];
             V::unpack(V::load(xs + (idx - a0) * VEC), xf);
             V::unpack(stage_w ? V::load(ws + (idx - a0) * VEC) : V::load(w + idx * VEC), wf);
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) xf[i] = xf[i] * rinv * wf[i];
+            for (int i = 0; i < VEC; ++i) xf[i] = xf[i] * pre * rinv * wf[i];
             V::store(orow + idx * VEC, V::pack(xf));
         }
-        if (tid < tail) orow[nvec * VEC + tid] = from_f32<T>(xt * rinv * wt);
+        if (tid < tail) orow[nvec * VEC + tid] = from_f32<T>(xt * pre * rinv * wt);
     }
     if constexpr (RED == RED_PAIR) {
         cg::this_cluster().sync();  // no CTA exits while its peer may still read its pair_slot
@@ -209,7 +284,7 @@ __global__ void __launch_bounds__(1024) staged_rows_kernel(NormArgs a) {
 // LEAN: w is read in the scale loop, one access at a time, instead of being
 // held in registers across the reduction; fewer registers, so more CTAs are
 // resident.
-template <typename T, int NV, bool ADD, int RED, bool LEAN = false>
+template <typename T, int NV, bool ADD, int RED, bool LEAN = false, int G = 1>
 __device__ __forceinline__ void reg_row(const NormArgs& a, int64_t r, int tid, int threads, int64_t a0, int64_t a1,
                                         bool tail_owner, float* scratch, float* pair_slot, int parity) {
     constexpr int VEC = vec16<T>();
@@ -287,8 +362,22 @@ __device__ __forceinline__ void reg_row(const NormArgs& a, int64_t r, int tid, i
     }
     if (tid < tail) wt = to_f32(w[nvec * VEC + tid]);
 
-    ss = group_sum<RED>(ss, scratch, pair_slot, parity);
-    const float rinv = rsqrtf(ss / static_cast<float>(a.D) + a.eps);
+    ss = group_sum<RED, G>(ss, scratch, pair_slot, parity);
+    float rinv = rsqrtf(ss / static_cast<float>(a.D) + a.eps), pre = 1.0f;
+    if (__builtin_expect(!ss_in_range(ss, a.D, a.eps), 0)) {
+        double sd = tid < tail ? sq_d(xt) : 0.0;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) {
+            if (a0 + static_cast<int64_t>(v) * threads + tid < a1) {
+                float xf[VEC];
+                V::unpack(xv[v], xf);
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) sd += sq_d(xf[i]);
+            }
+        }
+        const WideScale sc = wide_scale(group_sum_d<RED, G>(sd, scratch, pair_slot, parity), a.D, a.eps);
+        pre = sc.pre, rinv = sc.rinv;
+    }
 
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
@@ -298,11 +387,11 @@ __device__ __forceinline__ void reg_row(const NormArgs& a, int64_t r, int tid, i
             V::unpack(xv[v], xf);
             V::unpack(LEAN ? V::load(w + idx * VEC) : wv[LEAN ? 0 : v], wf);
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) xf[i] = xf[i] * rinv * wf[i];
+            for (int i = 0; i < VEC; ++i) xf[i] = xf[i] * pre * rinv * wf[i];
             V::store(orow + idx * VEC, V::pack(xf));
         }
     }
-    if (tid < tail) orow[nvec * VEC + tid] = from_f32<T>(xt * rinv * wt);
+    if (tid < tail) orow[nvec * VEC + tid] = from_f32<T>(xt * pre * rinv * wt);
 }
 
 // Prefetch row r of x (and res) and, if `with_w`, w, into L2 (one thread).
@@ -360,7 +449,7 @@ template <int NV> constexpr int cta_row_max_threads() { return NV >= 8 ? 256 : (
 
 template <typename T, int NV, bool ADD>
 __global__ void __launch_bounds__(cta_row_max_threads<NV>()) reg_cta_kernel(NormArgs a) {
-    __shared__ float scratch[33];
+    __shared__ __align__(8) float scratch[66];
     prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true, threadIdx.x, blockDim.x);
     pdl_enter();
     const int64_t nvec = a.D / vec16<T>();
@@ -376,7 +465,7 @@ __global__ void __launch_bounds__(cta_row_max_threads<NV>()) reg_cta_kernel(Norm
 // resident beside a first one's while it drains.
 template <typename T, int NV, bool ADD>
 __global__ void __launch_bounds__(256, 4) reg_lean_kernel(NormArgs a) {
-    __shared__ float scratch[33];
+    __shared__ __align__(8) float scratch[66];
     prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true, threadIdx.x, blockDim.x);
     pdl_enter();
     const int64_t nvec = a.D / vec16<T>();
@@ -386,10 +475,34 @@ __global__ void __launch_bounds__(256, 4) reg_lean_kernel(NormArgs a) {
     }
 }
 
+// G warps per row (warps_row): the CTA's warps form groups of G, each group takes
+// rows dealt round-robin over all groups of the grid (CTAs, and so SMs, differ by
+// one row at most), thread tid = 32 * (warp % G) + lane of its group owns accesses
+// idx = tid + v * 32 G. w is read in the scale loop, as in the lean CTA kernel.
+template <typename T, int NV, bool ADD, int G>
+__global__ void __launch_bounds__(256) reg_group_kernel(NormArgs a) {
+    __shared__ __align__(8) float scratch[66];    // [parity][warp] partial sums
+    __shared__ __align__(8) float dslots[66];     // [warp] double partial sums (rare rows)
+    const int warp = static_cast<int>(threadIdx.x >> 5);
+    const int gpc = static_cast<int>(blockDim.x >> 5) / G;  // groups per CTA
+    const int tid = static_cast<int>(threadIdx.x) - warp / G * G * 32;
+    const int64_t step = static_cast<int64_t>(gridDim.x) * gpc;
+    const int64_t r0 = static_cast<int64_t>(warp / G) * gridDim.x + blockIdx.x;
+    prefetch_row<T, ADD>(a, r0, 0, a.D, tid == 0, tid, 32 * G);
+    pdl_enter();
+    const int64_t nvec = a.D / vec16<T>();
+    int parity = 0;
+    for (int64_t r = r0; r < a.rows; r += step) {
+        next_row_prefetch<T, ADD>(a, r + step, 0, a.D, tid, 32 * G);
+        reg_row<T, NV, ADD, RED_GROUP, true, G>(a, r, tid, 32 * G, 0, nvec, true, scratch, dslots, parity);
+        parity ^= 1;
+    }
+}
+
 template <typename T, int NV, bool ADD>
 __global__ void __launch_bounds__(cta_row_max_threads<NV>()) reg_pair_kernel(NormArgs a) {
-    __shared__ float scratch[33];
-    __shared__ float pair_slot[2];
+    __shared__ __align__(8) float scratch[66];
+    __shared__ __align__(8) float pair_slot[6];
     const int rank = static_cast<int>(cg::this_cluster().block_rank());
     const int64_t nvec = a.D / vec16<T>();
     const int64_t half = norm_pair_half(nvec);
@@ -442,11 +555,18 @@ __device__ __forceinline__ void scalar_row(const NormArgs& a, int64_t r, int tid
         }
     }
     ss = group_sum<RED>(ss, scratch, nullptr, 0);
-    const float rinv = rsqrtf(ss / static_cast<float>(a.D) + a.eps);
+    float rinv = rsqrtf(ss / static_cast<float>(a.D) + a.eps), pre = 1.0f;
+    if (__builtin_expect(!ss_in_range(ss, a.D, a.eps), 0)) {
+        double sd = 0.0;
+#pragma unroll
+        for (int v = 0; v < NV; ++v) sd += sq_d(xv[v]);  // xv is 0 past the row's end
+        const WideScale sc = wide_scale(group_sum_d<RED>(sd, scratch, nullptr, 0), a.D, a.eps);
+        pre = sc.pre, rinv = sc.rinv;
+    }
 #pragma unroll
     for (int v = 0; v < NV; ++v) {
         const int64_t j = static_cast<int64_t>(v) * threads + tid;
-        if (j < a.D) orow[j] = from_f32<T>(xv[v] * rinv * wv[v]);
+        if (j < a.D) orow[j] = from_f32<T>(xv[v] * pre * rinv * wv[v]);
     }
 }
 
@@ -463,7 +583,7 @@ __global__ void __launch_bounds__(256) scalar_warp_kernel(NormArgs a) {
 
 template <typename T, int NV, bool ADD>
 __global__ void __launch_bounds__(1024) scalar_cta_kernel(NormArgs a) {
-    __shared__ float scratch[33];
+    __shared__ __align__(8) float scratch[66];
     prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true, threadIdx.x, blockDim.x);
     pdl_enter();
     for (int64_t r = blockIdx.x; r < a.rows; r += gridDim.x)
@@ -477,7 +597,7 @@ template <typename T, int VEC, bool ADD>
 __global__ void __launch_bounds__(1024) two_pass_kernel(NormArgs a) {
     using V = Vec<T, VEC>;
     using R = typename V::Raw;
-    __shared__ float scratch[33];
+    __shared__ __align__(8) float scratch[66];
     prefetch_row<T, ADD>(a, blockIdx.x, 0, a.D, true, threadIdx.x, blockDim.x);
     pdl_enter();
     const int tid = threadIdx.x, threads = blockDim.x;
@@ -518,18 +638,30 @@ __global__ void __launch_bounds__(1024) two_pass_kernel(NormArgs a) {
             ss = fmaf(xt, xt, ss);
         }
         ss = block_sum(ss, scratch);
-        const float rinv = rsqrtf(ss / static_cast<float>(a.D) + a.eps);
+        float rinv = rsqrtf(ss / static_cast<float>(a.D) + a.eps), pre = 1.0f;
+        if (__builtin_expect(!ss_in_range(ss, a.D, a.eps), 0)) {
+            // the statistics pass again in double (each thread its own, already updated, elements)
+            double sd = tid < tail ? sq_d(xt) : 0.0;
+            for (int64_t idx = tid; idx < nvec; idx += threads) {
+                float xf[VEC];
+                V::unpack(V::load(xr + idx * VEC), xf);
+#pragma unroll
+                for (int i = 0; i < VEC; ++i) sd += sq_d(xf[i]);
+            }
+            const WideScale sc = wide_scale(block_sum_d(sd, reinterpret_cast<double*>(scratch)), a.D, a.eps);
+            pre = sc.pre, rinv = sc.rinv;
+        }
         for (int64_t idx = tid; idx < nvec; idx += threads) {
             float xf[VEC], wf[VEC];
             V::unpack(V::load(xr + idx * VEC), xf);
             V::unpack(V::load(w + idx * VEC), wf);
 #pragma unroll
-            for (int i = 0; i < VEC; ++i) xf[i] = xf[i] * rinv * wf[i];
+            for (int i = 0; i < VEC; ++i) xf[i] = xf[i] * pre * rinv * wf[i];
             V::store(orow + idx * VEC, V::pack(xf));
         }
         if (tid < tail) {
             const int64_t j = nvec * VEC + tid;
-            orow[j] = from_f32<T>(xt * rinv * to_f32(w[j]));
+            orow[j] = from_f32<T>(xt * pre * rinv * to_f32(w[j]));
         }
     }
 }
@@ -583,6 +715,16 @@ cudaError_t launch_vector(const NormArgs& a, const NormPlan& p, cudaStream_t s) 
                 case 2: return launch_persistent(reg_lean_kernel<T, 2, ADD>, a, p, false, s);
                 case 4: return launch_persistent(reg_lean_kernel<T, 4, ADD>, a, p, false, s);
                 case 8: return launch_persistent(reg_lean_kernel<T, 8, ADD>, a, p, false, s);
+                default: return cudaErrorInvalidValue;
+            }
+        case NORM_WARPS_ROW:
+            switch (p.nv * 16 + p.group_warps) {
+                case 8 * 16 + 2: return launch_persistent(reg_group_kernel<T, 8, ADD, 2>, a, p, false, s);
+                case 8 * 16 + 4: return launch_persistent(reg_group_kernel<T, 8, ADD, 4>, a, p, false, s);
+                case 8 * 16 + 8: return launch_persistent(reg_group_kernel<T, 8, ADD, 8>, a, p, false, s);
+                case 16 * 16 + 2: return launch_persistent(reg_group_kernel<T, 16, ADD, 2>, a, p, false, s);
+                case 16 * 16 + 4: return launch_persistent(reg_group_kernel<T, 16, ADD, 4>, a, p, false, s);
+                case 16 * 16 + 8: return launch_persistent(reg_group_kernel<T, 16, ADD, 8>, a, p, false, s);
                 default: return cudaErrorInvalidValue;
             }
         case NORM_CTA_PAIR:

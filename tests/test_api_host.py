@@ -318,16 +318,20 @@ def test_glu_validation(L):
 
 
 def test_variant_control(L):
-    assert sra.variant_count("rmsnorm") == 8
+    assert sra.variant_count("rmsnorm") == 9
     assert sra.variant_count("rope_kv_store") == 2
-    assert sra.variant_count("glu") == 1
+    assert sra.variant_count("glu") == 2
+    assert [sra.variant_name("glu", i) for i in range(2)] == ["cols_rows", "cols_rows_regs"]
     assert sra.variant_count("decode_attention") == 2
     assert [sra.variant_name("decode_attention", i) for i in range(2)] == ["cuda_cores", "mma_sync"]
     assert sra.variant_count("nope") == ARG
-    assert [sra.variant_name("rmsnorm", i) for i in range(8)] == ["warp_rows", "cta_row", "cta_smem", "two_pass",
-                                                                  "cta_pair", "warp_smem", "pair_smem", "cta_lean"]
-    assert sra.variant_name("rmsnorm", 8) is None
-    assert L.sra_force_variant(b"rmsnorm", 8) == ARG
+    assert [sra.variant_name("rmsnorm", i) for i in range(9)] == ["warp_rows", "cta_row", "cta_smem", "two_pass",
+                                                                  "cta_pair", "warp_smem", "pair_smem", "cta_lean",
+                                                                  "warps_row"]
+    assert sra.variant_name("rmsnorm", 9) is None
+    assert L.sra_force_variant(b"rmsnorm", 9) == ARG
+    assert L.sra_force_variant(b"rmsnorm", 8 | (16 << 8) | (4 << 16)) == OK   # warps_row, 16 accesses, 4 warps
+    assert L.sra_force_variant(b"rmsnorm", 1 << 24) == ARG
     assert L.sra_force_variant(b"bogus", 0) == ARG
     assert L.sra_force_variant(b"rmsnorm", 2) == OK
     assert sra.pick_variant("rmsnorm", 512, 1536, num_sms=152) == 2
@@ -362,7 +366,9 @@ def test_dispatch_choices(L):
     assert pick("rmsnorm", 64, 40000, dtype=torch.bfloat16, num_sms=152) == 2
     # past shared memory: two-pass
     assert pick("rmsnorm", 2, 10_000_000, dtype=torch.float32, num_sms=152) == 3
-    assert pick("glu", 4096, 14336, num_sms=152) == 0
+    # SiLU with the registers the compiler picks, ReLU held to 48 (measured)
+    assert pick("glu", 4096, 14336, num_sms=152) == 1
+    assert pick("glu", 4096, 14336, 1, num_sms=152) == 0
     # RoPE: one task per thread up to 8 tokens per SM, two tasks per thread past that (an even
     # number of head units); an odd number keeps one task per thread
     assert pick("rope_kv_store", 64, 12, 2, 128, num_sms=152) == 0

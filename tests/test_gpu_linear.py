@@ -186,3 +186,34 @@ def test_bounded_wait_gives_up():
     assert sra.wait_timeouts() == before + 1
     got, want, h, W = norm_case(64, 1536, 2048, torch.bfloat16, 1041)
     assert_linear_close(got, want, h, W, "after the self-test")
+
+
+@pytest.mark.parametrize("eps", [0.0, 1e-6])
+@pytest.mark.parametrize("dtype,B,K,N,ws", [
+    (torch.bfloat16, 1, 1536, 2048, False),     # decode-batch kernel
+    (torch.bfloat16, 16, 1536, 2048, False),
+    (torch.bfloat16, 64, 1536, 2048, False),    # cluster kernel
+    (torch.bfloat16, 64, 1536, 2048, True),     # prologue kernel into a workspace
+    (torch.float16, 33, 640, 192, False),
+    (torch.float32, 5, 640, 192, False),        # CUDA-core kernel
+    (torch.bfloat16, 3, 100, 40, False),
+])
+def test_norm_rows_beyond_the_fp32_sum_range(eps, dtype, B, K, N, ws):
+    """RMSNorm prologue rows whose fp32 sum of squares overflows (elements of 2^100)
+    or loses its digits (2^-60 and 2^-130 with eps = 0) beside ordinary rows: the
+    fused projection equals the oracle's rmsnorm then linear, as on any row."""
+    x = syn.normal((B, K), 0, 1, torch.float32, 1035, 1).double()
+    scales = [2.0 ** 100, 2.0 ** -130, 1.0, 2.0 ** -60] if dtype != torch.float16 else [2.0 ** 12, 2.0 ** -10, 1.0]
+    for b in range(B):
+        x[b] *= scales[b % len(scales)]
+    x = x.to(dtype)
+    w = syn.normal((K,), 1, 0.1, dtype, 1035, 2)
+    W = syn.linear_weight(N, K, dtype, 1035)
+    wsp = sra.linear_workspace(B, K, dtype, DEV) if ws else None
+    got = sra.rmsnorm_linear(x.to(DEV), w.to(DEV), W.to(DEV), eps=eps, workspace=wsp).cpu()
+    h = torch.empty(B, K, dtype=dtype)
+    oracle.rmsnorm(x, w, h, eps)
+    assert bool(torch.isfinite(h.float()).all())
+    want = torch.empty(B, N, dtype=dtype)
+    oracle.linear(h, W, want)
+    assert_linear_close(got, want, h, W, f"norm range {dtype} B={B} K={K} eps={eps} ws={ws}")

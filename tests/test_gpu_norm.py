@@ -89,7 +89,7 @@ def test_ragged_widths(dtype, D, rows):
     assert_close(out, ref, f"add_rmsnorm [{rows},{D}] {dtype}")
 
 
-@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("variant", [0, 1, 2, 3, 4, 5, 6, 7, 8])
 @pytest.mark.parametrize("dtype", DTYPES)
 @pytest.mark.parametrize("rows,D", [(3, 1536), (700, 1536), (64, 2176), (40, 8192), (5, 333), (1, 1),
                                     (333, 4095), (512, 8192)])
@@ -190,3 +190,108 @@ def test_companion_large_rows_sampled():
     ref = torch.empty(len(idx), D, dtype=torch.bfloat16)
     oracle.rmsnorm(x[idx].contiguous(), w, ref, syn.EPS)
     assert_close(out[idx], ref, "sampled rows")
+
+
+def _range_rows(D, dtype, seed):
+    """Rows whose fp32 sum of squares overflows or underflows, beside ordinary rows.
+
+    The pages accumulate in fp32 to keep bf16 from overflowing
+    (koas-w.github.io "preformanceimprovement", section 3); the result asked for
+    is still the exact formula, so these rows are compared with the fp64 oracle
+    like any other: elements of 2^100 (the sum of squares passes fp32's range),
+    one element of 2^120 in an ordinary row, rows of 2^-60 and 2^-130 (bf16 /
+    fp32 subnormals), an ordinary row, a zero row, and a row holding one
+    infinity. fp16 cannot reach the first four, so its rows stay in range.
+    """
+    g = syn.normal((8, D), 0, 1, torch.float32, seed, 1).double()
+    big, one, tiny, sub = (2.0 ** 100, 2.0 ** 120, 2.0 ** -60, 2.0 ** -130)
+    if dtype == torch.float16:
+        big, one, tiny, sub = (2.0 ** 12, 2.0 ** 15, 2.0 ** -10, 2.0 ** -20)
+    rows = [g[0] * big, g[1].clone(), g[2] * tiny, g[3] * sub, g[4], torch.zeros(D, dtype=torch.float64),
+            g[6].clone(), -g[7] * big]
+    rows[1][D // 3] = one
+    rows[6][D // 2] = float("inf")
+    return torch.stack(rows).to(dtype)
+
+
+@pytest.mark.parametrize("variant", [-1, 0, 1, 2, 3, 4, 5, 6, 7, 8])
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("D", [1536, 333, 8192])
+@pytest.mark.parametrize("eps", [0.0, syn.EPS])
+def test_rows_beyond_the_fp32_sum_range(variant, dtype, D, eps):
+    """Every variant (and the planner's choice) on rows whose squares overflow or
+    underflow fp32: within 1 ulp of the oracle, NaN where the formula gives
+    0 * inf (a zero row with eps = 0, an infinite element)."""
+    sra.force_variant("rmsnorm", variant)
+    try:
+        x = _range_rows(D, dtype, 17)
+        w = syn.normal((D,), 1, 0.1, dtype, 17, 2)
+        try:
+            got, ref = run_rms(x, w, eps)
+        except sra.SRAError as e:
+            assert e.status == -7 and variant >= 0  # this variant cannot hold the row in registers
+            return
+        assert_close(got, ref, f"rmsnorm variant {variant} [{8},{D}] {dtype} eps={eps}")
+        # the fused add: the stored sum is the same big / tiny row
+        res = (x.double() * 2.0 ** -8).to(dtype)
+        xd = x.to(DEV)
+        out = sra.add_rmsnorm(xd, res.to(DEV), w.to(DEV), eps=eps)
+        xr, ref = x.clone(), torch.empty_like(x)
+        oracle.add_rmsnorm(xr, res, w, ref, eps)
+        assert_bits_equal(xd, xr, "residual")
+        assert_close(out, ref, f"add_rmsnorm variant {variant} [{8},{D}] {dtype} eps={eps}")
+    finally:
+        sra.force_variant("rmsnorm", -1)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("g,nv", [(2, 8), (2, 16), (4, 8), (4, 16), (8, 8), (8, 16)])
+@pytest.mark.parametrize("rows,D", [(512, 4096), (512, 8192), (300, 6000), (1, 8192), (777, 2056), (9, 5000)])
+def test_warps_row_every_group(dtype, g, nv, rows, D):
+    """warps_row forced to each (warps per row, accesses per lane) that can hold the row:
+    rows of several groups per CTA, fewer rows than groups; rmsnorm and add_rmsnorm
+    against the oracle."""
+    sra.force_variant("rmsnorm", 8 | (nv << 8) | (g << 16))
+    try:
+        x, w = syn.rms_inputs(rows, D, dtype, 18)
+        try:
+            got, ref = run_rms(x, w)
+        except sra.SRAError as e:
+            assert e.status == -7 and 32 * g * nv < -(-D // (16 // x.element_size()))
+            return
+        assert_close(got, ref, f"warps_row g{g} nv{nv} [{rows},{D}] {dtype}")
+        xa, ra, wa = syn.add_rms_inputs(rows, D, dtype, 19)
+        xd = xa.to(DEV)
+        buf, out = guarded(xa.shape, dtype)
+        sra.add_rmsnorm(xd, ra.to(DEV), wa.to(DEV), out, syn.EPS)
+        torch.cuda.synchronize()
+        check_guards(buf)
+        ref = torch.empty_like(xa)
+        oracle.add_rmsnorm(xa, ra, wa, ref, syn.EPS)
+        assert_bits_equal(xd, xa, "residual")
+        assert_close(out, ref, f"add warps_row g{g} nv{nv} [{rows},{D}] {dtype}")
+    finally:
+        sra.force_variant("rmsnorm", -1)
+
+
+@pytest.mark.parametrize("dtype", DTYPES)
+@pytest.mark.parametrize("D", [4100, 8190, 2053])
+def test_warps_row_ragged_tail(dtype, D):
+    """Rows padded to a 16-byte stride with D % (16 / element size) != 0: the scalar
+    tail of warps_row (the first threads of the group own one element each)."""
+    stride = -(-D // 8) * 8
+    rows = 300
+    base = syn.normal((rows, stride), 0, 1, dtype, 20, 1)
+    x = base[:, :D]
+    w = syn.normal((D,), 1, 0.1, dtype, 20, 2)
+    sra.force_variant("rmsnorm", 8)
+    try:
+        xd = base.to(DEV)[:, :D]
+        obuf = torch.full((rows, stride), 9.0, dtype=dtype, device=DEV)
+        sra.rmsnorm(xd, w.to(DEV), obuf[:, :D], syn.EPS)
+        ref = torch.empty(rows, D, dtype=dtype)
+        oracle.rmsnorm(x.contiguous(), w, ref, syn.EPS)
+        assert_close(obuf[:, :D], ref, f"warps_row tail [{rows},{D}] {dtype}")
+        assert bool((obuf[:, D:].cpu().double() == 9).all())
+    finally:
+        sra.force_variant("rmsnorm", -1)
