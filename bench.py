@@ -73,6 +73,8 @@ def parse():
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--sweep-variants", action="store_true",
                    help="A/B: time every RMSNorm / GLU variant on every norm / GLU shape (prints its own JSON)")
+    p.add_argument("--sweep-cps", action="store_true",
+                   help="with --sweep-variants: also cap the register RMSNorm variants at 1-6 CTAs per SM")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-baseline duration")
     return p.parse_args()
 
@@ -160,14 +162,19 @@ def build_entries(dev, stream_handle, only=(), companions=False):
         Ts_add, Ts_rope, Ts_glu = syn.ADD_RMS_T, syn.ROPE_T, syn.GLU_T
     else:
         Ts_add, Ts_rope, Ts_glu = (32768,), (32768,), ()
-        name = "rmsnorm:bf16:65536x1536"
-        if want(name):
-            x, w = syn.rms_inputs(65536, 1536, torch.bfloat16, 1001)
-            x, w = x.to(dev), w.to(dev)
-            out = torch.empty_like(x)
-            entries.append(Entry(name, "rmsnorm", 2 * 65536 * 1536 * 2 + 1536 * 2, 65536, L.sra_rmsnorm,
-                                 (x.data_ptr(), w.data_ptr(), out.data_ptr(), 65536, 1536, 1536, 1536, syn.EPS, 2,
-                                  stream_handle), [x], [out], keep=(x, w, out)))
+        # row-scaled companions of the RMSNorm widths: the Qwen2.5-1.5B hidden row in bf16, and
+        # the fp32 rows of 8192 and 4096 whose 512-row configured shapes are dominated by the
+        # fixed cost of a launch (>= 256 MB each, so they show the streaming rate)
+        for dt, R, D in ((torch.bfloat16, 65536, 1536), (torch.float32, 4096, 8192), (torch.float32, 8192, 4096)):
+            name = f"rmsnorm:{short[dt]}:{R}x{D}"
+            if want(name):
+                x, w = syn.rms_inputs(R, D, dt, 1001)
+                x, w = x.to(dev), w.to(dev)
+                out = torch.empty_like(x)
+                s = x.element_size()
+                entries.append(Entry(name, "rmsnorm", 2 * R * D * s + D * s, R, L.sra_rmsnorm,
+                                     (x.data_ptr(), w.data_ptr(), out.data_ptr(), R, D, D, D, syn.EPS, code[dt],
+                                      stream_handle), [x], [out], short[dt], keep=(x, w, out)))
     for T in Ts_add:
         name = f"add_rmsnorm:bf16:{T}x1536"
         if not want(name):
@@ -1030,6 +1037,14 @@ def run_sweep(args):
                 settings += [(v | (nv << 8) | (g << 16), f"{nm}/g{g}nv{nv}") for g in (2, 4, 8) for nv in (8, 16)]
             else:
                 settings.append((v, nm))
+        if op == "rmsnorm" and args.sweep_cps:
+            # the same register variants with at most c CTAs per SM (grid = c x SMs)
+            base = [(1, "cta_row", nv, 0) for nv in (2, 4, 8)] + [(7, "cta_lean", nv, 0) for nv in (4, 8)]
+            base += [(8, "warps_row", 16, 4), (8, "warps_row", 8, 8)]
+            for v, nm, nv, g in base:
+                for c in (1, 2, 3, 4, 6):
+                    settings.append((v | (nv << 8) | (g << 16) | (c << 24), f"{nm}/nv{nv}" + (f"g{g}" if g else "")
+                                     + f"/cps{c}"))
         for v, label in settings:
             sra.force_variant(op, v)
             try:

@@ -502,8 +502,9 @@ SRA_API int sra_set_pdl(int enable);
  * < sra_variant_count(op), optionally OR-ed with (nv << 8) to also force the
  * number of 16-byte accesses each thread holds in the register variants of
  * "rmsnorm" (nv in 1, 2, 3, 4, 6, 8; also 12 and 16 for the warp-per-row
- * variant; 8 or 16 for warps_row), and with (g << 16) to force the warps per row
- * of warps_row (g in 2, 4, 8). A forced setting that cannot serve a later
+ * variant; 8 or 16 for warps_row), with (g << 16) to force the warps per row
+ * of warps_row (g in 2, 4, 8), and with (c << 24) to launch at most c CTAs per
+ * SM (c in 1..15; "rmsnorm" only). A forced setting that cannot serve a later
  * call makes that call return SRA_ERR_VARIANT without enqueueing anything.
  * Returns SRA_OK, or SRA_ERR_ARG for an unknown op or out-of-range variant.
  */

@@ -369,6 +369,13 @@ int plan_norm(int64_t rows, int64_t D, int vec, bool add, int num_sms, const Sme
         const bool ok = plan_norm_variant(forced & 0xFF, rows, D, vec, add, num_sms, b, p);
         g_force_nv = 0;
         g_force_g = 0;
+        // bits 24..27: at most that many CTAs per SM (the grid shrinks; every kernel strides
+        // over its rows, so any grid is correct)
+        const int cps = (forced >> 24) & 0xF;
+        if (ok && cps) {
+            const bool pairs = p->variant == NORM_CTA_PAIR || p->variant == NORM_PAIR_SMEM;
+            p->grid = std::min<int64_t>(p->grid, static_cast<int64_t>(cps) * num_sms * (pairs ? 2 : 1));
+        }
         return ok ? SRA_OK : SRA_ERR_VARIANT;
     }
     const int64_t nacc = ceil_div(D, vec);
@@ -1126,7 +1133,7 @@ int sra_uclip(const void* x, const float* alpha, const float* gamma, void* out, 
 int sra_force_variant(const char* op, int variant) {
     std::atomic<int>* slot = force_slot(op);
     if (!slot) return SRA_ERR_ARG;
-    if (variant < -1 || (variant >= 0 && ((variant & 0xFF) >= variant_count(op) || (variant >> 24) != 0)))
+    if (variant < -1 || (variant >= 0 && ((variant & 0xFF) >= variant_count(op) || (variant >> 28) != 0)))
         return SRA_ERR_ARG;
     slot->store(variant, std::memory_order_relaxed);
     return SRA_OK;

@@ -331,7 +331,8 @@ def test_variant_control(L):
     assert sra.variant_name("rmsnorm", 9) is None
     assert L.sra_force_variant(b"rmsnorm", 9) == ARG
     assert L.sra_force_variant(b"rmsnorm", 8 | (16 << 8) | (4 << 16)) == OK   # warps_row, 16 accesses, 4 warps
-    assert L.sra_force_variant(b"rmsnorm", 1 << 24) == ARG
+    assert L.sra_force_variant(b"rmsnorm", 1 | (2 << 24)) == OK   # cta_row, at most 2 CTAs per SM
+    assert L.sra_force_variant(b"rmsnorm", 1 << 28) == ARG
     assert L.sra_force_variant(b"bogus", 0) == ARG
     assert L.sra_force_variant(b"rmsnorm", 2) == OK
     assert sra.pick_variant("rmsnorm", 512, 1536, num_sms=152) == 2
