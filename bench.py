@@ -1014,11 +1014,13 @@ def run_sweep(args):
     stream = torch.cuda.current_stream(dev)
     sh = int(stream.cuda_stream)
     sra.set_pdl(not args.no_pdl)
-    swept = ("rmsnorm", "add_rmsnorm", "swiglu", "reglu")
-    only = [o for o in args.only.split(",") if o] or list(swept)
+    swept = ("rmsnorm", "add_rmsnorm", "swiglu", "reglu", "linear")
+    only = [o for o in args.only.split(",") if o] or list(swept[:4])
     entries = [e for e in build_entries(dev, sh, only) if e.op in swept]
     if not args.only:
-        entries += [e for e in build_entries(dev, sh, companions=True) if e.op in swept]
+        entries += [e for e in build_entries(dev, sh, companions=True) if e.op in swept[:4]]
+    else:  # companion shapes named on the command line
+        entries += [e for e in build_entries(dev, sh, only, companions=True) if e.op in swept]
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device=dev)
     peak, _ = measured_peak()
     table = []
@@ -1026,13 +1028,15 @@ def run_sweep(args):
         row = {"name": e.name, "bytes": e.bytes, "auto": None, "variants": {}}
         n = int(min(64, max(1, -(-STREAM_BYTES // max(1, e.bytes)))))
         calls = e.replicas(n) if n > 1 else [e.launch]
-        op = "glu" if e.op in ("swiglu", "reglu") else "rmsnorm"
+        op = {"swiglu": "glu", "reglu": "glu", "linear": "linear"}.get(e.op, "rmsnorm")
         settings = [(-1, "auto")]
         for v in range(sra.variant_count(op)):
             nm = sra.variant_name(op, v)
             if nm in ("warp_rows", "cta_row", "cta_pair", "cta_lean"):
                 nvs = (1, 2, 3, 4, 6, 8, 12, 16) if nm == "warp_rows" else (1, 2, 3, 4, 6, 8)
                 settings += [(v | (nv << 8), f"{nm}/nv{nv}") for nv in nvs]
+            elif nm == "tcgen05":
+                settings += [(v, nm)] + [(v | (sk << 8), f"{nm}/splits{sk}") for sk in (2, 4, 6, 8, 12, 16)]
             elif nm == "warps_row":
                 settings += [(v | (nv << 8) | (g << 16), f"{nm}/g{g}nv{nv}") for g in (2, 4, 8) for nv in (8, 16)]
             else:

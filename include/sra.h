@@ -497,7 +497,10 @@ SRA_API int sra_set_pdl(int enable);
  * for an even n_head + 2 * n_kv_head), "glu" (0 = columns over threads and rows over
  * CTAs at 48 registers a thread, 1 = the same kernel with the registers the compiler
  * picks), "decode_attention" (0 = CUDA-core kernel,
- * 1 = mma.sync kernel for bf16 / fp16 with head_dim 64 or 128).
+ * 1 = mma.sync kernel for bf16 / fp16 with head_dim 64 or 128), "linear" (the
+ * projection of the _ws entry points once the prologue has run: 0 = mma.sync
+ * kernels, 1 = the tcgen05 kernel, for up to 64 rows and N a multiple of 128;
+ * OR-ed with (s << 8), s in 1..16, it also forces the tcgen05 kernel's K splits).
  * variant: -1 = automatic per-shape choice (the default); otherwise an index
  * < sra_variant_count(op), optionally OR-ed with (nv << 8) to also force the
  * number of 16-byte accesses each thread holds in the register variants of

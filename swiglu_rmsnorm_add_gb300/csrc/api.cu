@@ -18,7 +18,7 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_smem_optin[kMaxDevices];
-std::atomic<int> g_force_norm{-1}, g_force_rope{-1}, g_force_glu{-1}, g_force_attn{-1};
+std::atomic<int> g_force_norm{-1}, g_force_rope{-1}, g_force_glu{-1}, g_force_attn{-1}, g_force_lin{-1};
 thread_local bool g_pdl = false;  // programmatic dependent launch for this thread's calls
 thread_local int g_force_nv = 0;  // accesses per thread forced for A/B measurement (0 = planner's)
 thread_local int g_force_g = 0;   // warps per row forced for warps_row A/B measurement (0 = planner's)
@@ -545,6 +545,7 @@ std::atomic<int>* force_slot(const char* op) {
     if (std::strcmp(op, "rope_kv_store") == 0) return &g_force_rope;
     if (std::strcmp(op, "glu") == 0) return &g_force_glu;
     if (std::strcmp(op, "decode_attention") == 0) return &g_force_attn;
+    if (std::strcmp(op, "linear") == 0) return &g_force_lin;
     return nullptr;
 }
 
@@ -554,6 +555,7 @@ int variant_count(const char* op) {
     if (std::strcmp(op, "rope_kv_store") == 0) return ROPE_NUM_VARIANTS;
     if (std::strcmp(op, "glu") == 0) return GLU_NUM_VARIANTS;
     if (std::strcmp(op, "decode_attention") == 0) return 2;  // CUDA cores, mma.sync
+    if (std::strcmp(op, "linear") == 0) return 2;            // mma.sync, tcgen05 (projection over h)
     return SRA_ERR_ARG;
 }
 
@@ -980,11 +982,37 @@ static int linear_common(const void* x, const void* w_ln, const void* W, void* y
                         xs % 8 == 0 && (prologue != 0 || aligned16(w_ln));
     plan.narrow = false;
     plan.splits = 1;
+    plan.tcgen05 = false;
     // decode batches: 16-column CTAs over all of K, no cluster, when the B rows of h for all of
     // K fit in shared memory beside the W rings
     plan.narrow = plan.tensor_cores && B <= 16 &&
                   static_cast<int64_t>(linear16_smem(static_cast<int>(B), K)) <= std::min<int64_t>(limit, 200 * 1024);
-    if (plan.tensor_cores && !plan.narrow) {
+    // the projection of h (the workspace path) on tcgen05: up to 64 rows, 128-column slices.
+    // Chosen from K = 4096 up (measured on GB300 at batch 64: SwiGLU + down_proj [8960 -> 1536]
+    // 14.3 against 18.1 us with mma.sync; ln1 + qkv_proj [1536 -> 2048] 10.9 against 8.5 us,
+    // too few W tiles per CTA to amortise the tensor-memory set-up and the cluster epilogue);
+    // sra_force_variant("linear", 0 or 1) overrides it
+    const int lin_all = g_force_lin.load(std::memory_order_relaxed);
+    const int lin_forced = lin_all < 0 ? -1 : (lin_all & 0xFF);  // bits 8-15: K splits (A/B only)
+    const bool tc_wanted = lin_forced == 1 || (lin_forced < 0 && K >= 4096);
+    if (plan.tensor_cores && prologue == 3 && B <= 64 && N % 128 == 0 && tc_wanted &&
+        static_cast<int64_t>(linear_tc_smem()) <= limit) {
+        plan.tcgen05 = true;
+        // 128-column slices x K splits (a cluster of up to 16 CTAs, 8 where the device cannot
+        // place 16): two CTAs per SM (97 KB of shared memory each), at least two W tiles per CTA
+        const int64_t slices = N / 128, KT = K / 64;
+        while (plan.splits < 16 && slices * plan.splits * 2 <= 2 * static_cast<int64_t>(sms) &&
+               KT >= 4 * plan.splits)
+            plan.splits *= 2;
+        const int fs = (lin_all >> 8) & 0xFF;
+        if (fs) {
+            if (fs > 16 || fs > KT) return SRA_ERR_VARIANT;
+            plan.splits = fs;
+        }
+    } else if (lin_forced == 1 && prologue == 3) {
+        return SRA_ERR_VARIANT;
+    }
+    if (plan.tensor_cores && !plan.narrow && !plan.tcgen05) {
         // 64-column slices x row blocks x K splits (a cluster); two CTAs per SM fit (45 to 113 KB
         // each): aim for one wave of 1-2 CTAs per SM with at least four W tiles per CTA
         const int64_t slices = (N / 64) * ((B + plan.mt * 16 - 1) / (plan.mt * 16));
@@ -1054,6 +1082,8 @@ static int linear_ws(const void* x, const void* w_ln, const void* W, void* y, in
             (prologue == 0 && overlap(sy, span_of(w_ln, 1, 0, K, es))))
             return SRA_ERR_ALIAS;
     }
+    // a forced tcgen05 projection that cannot serve this call: nothing is enqueued
+    if (g_force_lin.load(std::memory_order_relaxed) == 1 && (B > 64 || N % 128 != 0)) return SRA_ERR_VARIANT;
     const int st = prologue == 0 ? sra_rmsnorm(x, w_ln, ws, B, K, xs, K, eps, dtype, stream)
                                  : sra_glu(x, ws, B, K, xs, K, prologue - 1, dtype, stream);
     if (st != SRA_OK) return st;
@@ -1147,11 +1177,13 @@ const char* sra_variant_name(const char* op, int variant) {
     static const char* const rope_names[] = {"token_cta", "token_cta2"};
     static const char* const glu_names[] = {"cols_rows", "cols_rows_regs"};
     static const char* const attn_names[] = {"cuda_cores", "mma_sync"};
+    static const char* const lin_names[] = {"mma_sync", "tcgen05"};
     const int n = variant_count(op);
     if (n < 0 || variant < 0 || variant >= n) return nullptr;
     if (std::strcmp(op, "rmsnorm") == 0) return norm_names[variant];
     if (std::strcmp(op, "rope_kv_store") == 0) return rope_names[variant];
     if (std::strcmp(op, "decode_attention") == 0) return attn_names[variant];
+    if (std::strcmp(op, "linear") == 0) return lin_names[variant];
     return glu_names[variant];
 }
 

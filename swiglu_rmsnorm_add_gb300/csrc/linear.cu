@@ -33,6 +33,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tcgen05.cuh"
 #include "tma.cuh"
 
 namespace cg = cooperative_groups;
@@ -544,6 +545,140 @@ __global__ void __launch_bounds__((warps_for(MT) + 1) * 32) linear_h_kernel(LinA
     cluster.sync();
 }
 
+// ---- the projection of rows that are already h on the fifth-generation tensor cores
+// (tcgen05), for up to 64 rows. The MMA's operands are swapped so that no accumulator lane is
+// padding: A is a 128-row tile of W (128 output columns of y), B the [64][64] tile of h (its
+// rows past B arrive as zeros from the tensor map's bounds), and D = W_tile . h_tile^T is
+// [128 output columns][64 rows], held in 64 columns of tensor memory with output column
+// n0 + i in lane i. One thread issues the TMA copies of stage t (W's [128][64] tile and h's
+// [64][64] tile, both with the 128-byte swizzle) into slot t % S; another waits for the
+// stage, issues its four MMAs (K = 16 each, operands read from shared memory through matrix
+// descriptors) and commits them to the slot's empty barrier, which the producer waits on
+// before it refills the slot. After the last stage the MMA thread commits to the accumulator
+// barrier; each warp then reads its quarter of the lanes (32 output columns x 64 rows) into a
+// partial tile in shared memory, and the cluster (K split over its CTAs) sums its ranks'
+// partial tiles as the other projection kernels do. No thread holds a fragment; the tensor
+// core reads the staged tiles itself.
+constexpr int kTcM = 128;    // output columns of y per CTA: the MMA's M
+constexpr int kTcN = 64;     // rows of h (at most): the MMA's N
+constexpr int kTcStages = 4;  // 97 KB of shared memory: two CTAs per SM
+__host__ __device__ constexpr size_t tc_wtile_bytes() { return static_cast<size_t>(kTcM) * kKT * 2; }
+__host__ __device__ constexpr size_t tc_htile_bytes() { return static_cast<size_t>(kTcN) * kKT * 2; }
+__host__ __device__ constexpr size_t tc_smem_bytes() {
+    return 1024 + (kTcStages * (tc_wtile_bytes() + tc_htile_bytes()) > static_cast<size_t>(kTcN) * kTcM * 4
+                       ? kTcStages * (tc_wtile_bytes() + tc_htile_bytes())
+                       : static_cast<size_t>(kTcN) * kTcM * 4);
+}
+
+template <typename T>
+__global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_constant__ CUtensorMap tmW,
+                                                        const __grid_constant__ CUtensorMap tmX) {
+    constexpr int S = kTcStages;
+    constexpr size_t SB = tc_wtile_bytes() + tc_htile_bytes();
+    constexpr uint32_t kCols = 64;  // tensor-memory columns: one fp32 accumulator column per row of h
+    constexpr uint32_t IDESC = tc::idesc_f16(std::is_same<T, __nv_bfloat16>::value, kTcM, kTcN);
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    __shared__ uint64_t full[S], empty[S], accb;
+    __shared__ uint32_t tmem_slot;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int SK = static_cast<int>(cluster.num_blocks());
+    const int rank = static_cast<int>(cluster.block_rank());
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int64_t n0 = (blockIdx.x / SK) * static_cast<int64_t>(kTcM);
+    const int rows = static_cast<int>(a.B < kTcN ? a.B : kTcN);
+    const int KT = static_cast<int>(a.K / kKT);
+    const int per = (KT + SK - 1) / SK;
+    const int kt0 = rank * per < KT ? rank * per : KT;
+    const int kt1 = kt0 + per < KT ? kt0 + per : KT;
+    const int ntiles = kt1 - kt0;
+    const int64_t kbase = static_cast<int64_t>(kt0) * kKT;
+    float* part = reinterpret_cast<float*>(smem);  // [kTcN rows][kTcM columns], after the ring drains
+    const T* W = static_cast<const T*>(a.W);
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < S; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init(&accb, 1);
+        mbar_init_fence();
+    }
+    if (warp == 0) {
+        tc::alloc(&tmem_slot, kCols);
+        tc::relinquish();
+    }
+    // (No L2 prefetch of the W slice before the dependency wait here: measured slower, the
+    // prefetch traffic of every CTA's whole slice competes with the tiles the pipeline needs.)
+    __syncthreads();  // barriers initialised, the tensor-memory address in shared memory
+    tc::fence_after();
+    const uint32_t tmem = tmem_slot;
+    pdl_enter();
+
+    // Lanes 1-31 of the producer and MMA warps wait at the warp barrier (not in a poll loop,
+    // which would take the warp's issue slots from lane 0) until lane 0 has left its loop.
+    if (warp == 1) {
+        if (lane == 0) {
+            for (int t = 0; t < ntiles; ++t) {
+                const int slot = t % S;
+                // the slot's previous stage (t - S) has been read by its MMAs
+                if (t >= S) mbar_wait(&empty[slot], static_cast<uint32_t>(((t / S) - 1) & 1));
+                unsigned char* st = smem + static_cast<size_t>(slot) * SB;
+                const int k0 = static_cast<int>(kbase) + t * kKT;
+                mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(SB));
+                tma_load_2d(st, &tmW, k0, static_cast<int>(n0), &full[slot]);
+                tma_load_2d(st + tc_wtile_bytes(), &tmX, k0, 0, &full[slot]);
+            }
+        }
+        __syncwarp();
+    } else if (warp == 0) {
+        if (lane == 0) {
+            for (int t = 0; t < ntiles; ++t) {
+                const int slot = t % S;
+                mbar_wait(&full[slot], static_cast<uint32_t>((t / S) & 1));
+                tc::fence_after();
+                const unsigned char* st = smem + static_cast<size_t>(slot) * SB;
+#pragma unroll
+                for (int k = 0; k < kKT / 16; ++k)
+                    tc::mma_f16(tmem, tc::sdesc_sw128(st, 32 * k), tc::sdesc_sw128(st + tc_wtile_bytes(), 32 * k),
+                                IDESC, (t | k) != 0 ? 1u : 0u);
+                tc::commit(&empty[slot]);  // the slot is free once these MMAs have read it
+            }
+            tc::commit(&accb);  // the accumulator is complete once every MMA above has
+        }
+        __syncwarp();
+    }
+    mbar_wait(&accb, 0);
+    __syncwarp();  // the warp-wide accumulator loads below need all 32 lanes together
+    tc::fence_after();
+
+    // ---- epilogue: warp w reads output columns n0 + 32 w + lane, one 16-column (row) group at a time
+#pragma unroll
+    for (int c0 = 0; c0 < kTcN; c0 += 16) {
+        uint32_t v[16];
+        tc::ld16(tmem + (static_cast<uint32_t>(32 * warp) << 16) + static_cast<uint32_t>(c0), v);
+        tc::wait_ld();
+#pragma unroll
+        for (int j = 0; j < 16; ++j) part[(c0 + j) * kTcM + 32 * warp + lane] = ntiles > 0 ? __uint_as_float(v[j]) : 0.0f;
+    }
+    tc::fence_before();
+    __syncthreads();  // every accumulator read is done: the tensor memory can go
+    if (warp == 0) tc::dealloc(tmem, kCols);
+    cluster.sync();
+    T* y = static_cast<T*>(a.y);
+    for (int idx = rank * 128 + threadIdx.x; idx < rows * kTcM; idx += SK * 128) {
+        const int r = idx / kTcM, c = idx - r * kTcM;
+        // every rank's value requested before the first add (the cluster holds at most 16 ranks)
+        float v[16];
+#pragma unroll
+        for (int q = 0; q < 16; ++q) v[q] = q < SK ? cluster.map_shared_rank(part, q)[r * kTcM + c] : 0.0f;
+        float sum = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 16; ++q) sum += v[q];
+        if (n0 + c < a.N) y[r * a.ys + n0 + c] = to_t<T>(sum);
+    }
+    cluster.sync();
+}
+
 // ---- decode batches: a CTA owns 16 columns of y over the whole of K; its eight warps
 // split K between them (each streaming its own W tiles through a private cp.async ring)
 // and meet only at the end, in shared memory: no cluster, no exchange. h for all of K
@@ -768,6 +903,45 @@ cudaError_t launch_h_mt(const LinArgs& a, const LinPlan& p, cudaStream_t s, cons
     return launch_kernel(kernel, grid, dim3((warps_for(MT) + 1) * 32), smem, s, p.pdl, p.splits, a, tmW, tmX);
 }
 
+template <typename T>
+cudaError_t launch_tc(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
+    // W [N][K] in [128][64] boxes and h [B][K] in [64][64] boxes, both with the 128-byte swizzle
+    const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
+    CUtensorMap tmW, tmX;
+    if (!encode_tmap_16(&tmW, a.W, 2, a.K, a.N, a.K * 2, kKT, kTcM, bf16, true) ||
+        !encode_tmap_16(&tmX, a.x, 2, a.K, a.B, a.xs * 2, kKT, kTcN, bf16, true))
+        return cudaErrorNotSupported;
+    auto kernel = linear_tc_kernel<T>;
+    const size_t smem = tc_smem_bytes();
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int splits = p.splits;
+    if (splits > 8) {
+        // a cluster of more than 8 CTAs is a non-portable size: use it only where the device can place one
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        int clusters = 0;
+        if (e == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = static_cast<unsigned>(splits);
+            attr.val.clusterDim.y = attr.val.clusterDim.z = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(splits));
+            cfg.blockDim = dim3(128);
+            cfg.dynamicSmemBytes = smem;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+        }
+        if (e != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            splits = 8;
+        }
+    }
+    const dim3 grid(static_cast<unsigned>((a.N + kTcM - 1) / kTcM * splits));
+    return launch_kernel(kernel, grid, dim3(128), smem, s, p.pdl, splits, a, tmW, tmX);
+}
+
 template <typename T, int PRO>
 cudaError_t launch_pro(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
     // tensor maps: W [N][K] and the input rows [B][K or 2K] in 64 x (64 or MT*16) boxes with the
@@ -798,6 +972,7 @@ cudaError_t launch_pro(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
 
 template <typename T>
 cudaError_t launch_typed(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
+    if (p.tcgen05) return p.prologue == 3 ? launch_tc<T>(a, p, s) : cudaErrorInvalidValue;
     if (p.narrow) {
         switch (p.prologue) {
             case 0: return launch16<T, 0>(a, p, s);
@@ -946,6 +1121,7 @@ size_t linear_smem(int mt, int prologue) {
     return prologue == 3 ? lin::smemh_bytes(mt) : lin::smem_bytes(mt, prologue);
 }
 size_t linear16_smem(int rows, int64_t K) { return lin::smem16_bytes(rows, K); }
+size_t linear_tc_smem() { return lin::tc_smem_bytes(); }
 
 cudaError_t launch_linear(const LinArgs& a, const LinPlan& p, int dtype, cudaStream_t s) {
     if (!p.tensor_cores) {

@@ -324,6 +324,11 @@ def test_variant_control(L):
     assert [sra.variant_name("glu", i) for i in range(2)] == ["cols_rows", "cols_rows_regs"]
     assert sra.variant_count("decode_attention") == 2
     assert [sra.variant_name("decode_attention", i) for i in range(2)] == ["cuda_cores", "mma_sync"]
+    assert sra.variant_count("linear") == 2
+    assert [sra.variant_name("linear", i) for i in range(2)] == ["mma_sync", "tcgen05"]
+    assert L.sra_force_variant(b"linear", 1 | (4 << 8)) == OK   # tcgen05 with 4 K splits
+    assert L.sra_force_variant(b"linear", 2) == ARG
+    assert L.sra_force_variant(b"linear", -1) == OK
     assert sra.variant_count("nope") == ARG
     assert [sra.variant_name("rmsnorm", i) for i in range(9)] == ["warp_rows", "cta_row", "cta_smem", "two_pass",
                                                                   "cta_pair", "warp_smem", "pair_smem", "cta_lean",

@@ -217,3 +217,87 @@ def test_norm_rows_beyond_the_fp32_sum_range(eps, dtype, B, K, N, ws):
     want = torch.empty(B, N, dtype=dtype)
     oracle.linear(h, W, want)
     assert_linear_close(got, want, h, W, f"norm range {dtype} B={B} K={K} eps={eps} ws={ws}")
+
+
+def _tc_case(prologue, dtype, B, K, N, seed):
+    """The workspace path with its projection forced onto the tcgen05 kernel."""
+    W = syn.linear_weight(N, K, dtype, seed)
+    wsp = sra.linear_workspace(B, K, dtype, DEV)
+    sra.force_variant("linear", 1)
+    try:
+        if prologue == "rmsnorm":
+            x = syn.normal((B, K), 0, 1, dtype, seed, 1)
+            w = syn.normal((K,), 1, 0.1, dtype, seed, 2)
+            got = sra.rmsnorm_linear(x.to(DEV), w.to(DEV), W.to(DEV), workspace=wsp).cpu()
+            h = torch.empty(B, K, dtype=dtype)
+            oracle.rmsnorm(x, w, h, 1e-6)
+        else:
+            gu = syn.normal((B, 2 * K), 0, 1, dtype, seed, 3)
+            got = sra.glu_linear(gu.to(DEV), W.to(DEV), act=prologue, workspace=wsp).cpu()
+            h = torch.empty(B, K, dtype=dtype)
+            oracle.glu(gu, h, prologue)
+    finally:
+        sra.force_variant("linear", -1)
+    want = torch.empty(B, N, dtype=dtype)
+    oracle.linear(h, W, want)
+    return got, want, h, W
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("prologue,B,K,N", [
+    ("rmsnorm", 32, 64, 128),       # one tile of K, one slice
+    ("rmsnorm", 33, 640, 256),      # ragged rows, K split
+    ("rmsnorm", 64, 1536, 2048),    # Qwen2.5-1.5B ln1 + qkv_proj, batch 64
+    ("silu", 64, 8960, 1536),       # Qwen2.5-1.5B SwiGLU + down_proj, batch 64
+    ("relu", 48, 1024, 384),
+    ("silu", 40, 4160, 640),        # K tiles not a multiple of the cluster's splits
+])
+def test_tcgen05_projection(dtype, prologue, B, K, N):
+    """The projection of h on the fifth-generation tensor cores (W tile as the MMA's A
+    operand, h as B, fp32 accumulator in tensor memory) against the oracle's rmsnorm /
+    glu then linear, at the fused projections' tolerance; no bounded wait runs out."""
+    before = sra.wait_timeouts()
+    got, want, h, W = _tc_case(prologue, dtype, B, K, N, 1050 + K + B)
+    torch.cuda.synchronize()
+    assert sra.wait_timeouts() == before
+    assert_linear_close(got, want, h, W, f"tcgen05 {prologue} {dtype} B={B} K={K} N={N}")
+
+
+def test_tcgen05_forced_where_it_cannot_serve():
+    """Forced onto the tcgen05 kernel, a call it cannot serve (more than 64 rows, or N not a
+    multiple of 128) fails before anything is enqueued; smaller batches, which take the fused
+    kernel without a workspace split, still run."""
+    W = syn.linear_weight(192, 256, torch.bfloat16, 1060).to(DEV)
+    x = syn.normal((80, 256), 0, 1, torch.bfloat16, 1060, 1).to(DEV)
+    w = syn.normal((256,), 1, 0.1, torch.bfloat16, 1060, 2).to(DEV)
+    sra.force_variant("linear", 1)
+    try:
+        with pytest.raises(sra.SRAError):
+            sra.rmsnorm_linear(x, w, W, workspace=sra.linear_workspace(80, 256, torch.bfloat16, DEV))
+        with pytest.raises(sra.SRAError):
+            sra.rmsnorm_linear(x[:40], w, W, workspace=sra.linear_workspace(40, 256, torch.bfloat16, DEV))
+        y = sra.rmsnorm_linear(x[:8], w, W, workspace=sra.linear_workspace(8, 256, torch.bfloat16, DEV))
+        torch.cuda.synchronize()
+        assert bool(torch.isfinite(y.float()).all())
+    finally:
+        sra.force_variant("linear", -1)
+
+
+@pytest.mark.parametrize("variant", [0, 1])
+def test_workspace_projection_both_kernels(variant):
+    """SwiGLU + down_proj at batch 64 over a workspace with the projection forced onto the
+    mma.sync kernel (0) and onto the tcgen05 kernel (1): both match the oracle."""
+    B, I, N = 64, 8960, 1536
+    gu = syn.normal((B, 2 * I), 0, 1, torch.bfloat16, 1061, 3)
+    W = syn.linear_weight(N, I, torch.bfloat16, 1061)
+    sra.force_variant("linear", variant)
+    try:
+        got = sra.glu_linear(gu.to(DEV), W.to(DEV), workspace=sra.linear_workspace(B, I, torch.bfloat16, DEV)).cpu()
+    finally:
+        sra.force_variant("linear", -1)
+    rows = torch.arange(0, B, 5)
+    h = torch.empty(len(rows), I, dtype=torch.bfloat16)
+    oracle.glu(gu[rows].contiguous(), h, "silu")
+    want = torch.empty(len(rows), N, dtype=torch.bfloat16)
+    oracle.linear(h, W, want)
+    assert_linear_close(got[rows], want, h, W, f"down_proj over a workspace, linear variant {variant}")
