@@ -73,6 +73,8 @@ def parse():
     p.add_argument("--no-pdl", action="store_true", help="launch without programmatic dependent launch")
     p.add_argument("--sweep-variants", action="store_true",
                    help="A/B: time every RMSNorm / GLU variant on every norm / GLU shape (prints its own JSON)")
+    p.add_argument("--force", default="",
+                   help="comma list op=variant applied with sra_force_variant before anything runs (profiling A/B)")
     p.add_argument("--sweep-cps", action="store_true",
                    help="with --sweep-variants: also cap the register RMSNorm variants at 1-6 CTAs per SM")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU-baseline duration")
@@ -659,6 +661,9 @@ def run_gpu(args):
     only = [o for o in args.only.split(",") if o]
     pdl = not args.no_pdl
     sra.set_pdl(pdl)
+    for f in (x for x in args.force.split(",") if x):
+        op, v = f.split("=")
+        sra.force_variant(op, int(v, 0))
 
     entries = build_entries(dev, sh, only)
     if only:  # a companion shape named on the command line is timed as a step entry of its own
@@ -743,10 +748,16 @@ def run_gpu(args):
     de = entries[dom]
     d_us = statistics.fmean(dom_ms) * 1e3
     achieved = de.bytes / (d_us * 1e-6) / 1e9
+    traffic = kernel_traffic(de.name)
     roofline = {"bound": "hbm", "kernel": de.name, "achieved": round(achieved, 1), "peak": peak,
                 "peak_source": peak_src, "unit": "GB/s", "frac": round(achieved / peak, 4),
-                "traffic": kernel_traffic(de.name), "algorithmic_bytes": de.bytes,
+                "traffic": traffic, "algorithmic_bytes": de.bytes,
                 "us_per_launch": round(d_us, 3), "timed": "CUDA events around its launch in every timed step"}
+    if traffic:
+        # the same launch on the DRAM bytes ncu counts for one launch: writes still dirty in L2 when
+        # the launch ends are written back later, so this is the rate the launch itself sustained
+        roofline["achieved_on_traffic"] = round(traffic / (d_us * 1e-6) / 1e9, 1)
+        roofline["frac_on_traffic"] = round(traffic / (d_us * 1e-6) / 1e9 / peak, 4)
 
     # per-kernel table: each launch timed alone (clean L2, event pair), after the step loop
     reps = max(10, min(50, args.steps))

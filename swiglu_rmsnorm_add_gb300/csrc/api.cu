@@ -1004,7 +1004,7 @@ static int linear_common(const void* x, const void* w_ln, const void* W, void* y
         while (plan.splits < 16 && slices * plan.splits * 2 <= 2 * static_cast<int64_t>(sms) &&
                KT >= 4 * plan.splits)
             plan.splits *= 2;
-        const int fs = (lin_all >> 8) & 0xFF;
+        const int fs = lin_all < 0 ? 0 : (lin_all >> 8) & 0xFF;
         if (fs) {
             if (fs > 16 || fs > KT) return SRA_ERR_VARIANT;
             plan.splits = fs;
