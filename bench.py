@@ -1015,7 +1015,8 @@ def run_gpu(args):
 
 def run_sweep(args):
     """Streaming time of every RMSNorm variant on every norm shape, and of every GLU
-    variant on the GLU shapes (dispatch evidence)."""
+    variant on the GLU shapes (dispatch evidence); projection and decode-attention
+    variants on the companion shapes named with --only."""
     import torch
 
     import swiglu_rmsnorm_add_gb300 as sra
@@ -1025,7 +1026,7 @@ def run_sweep(args):
     stream = torch.cuda.current_stream(dev)
     sh = int(stream.cuda_stream)
     sra.set_pdl(not args.no_pdl)
-    swept = ("rmsnorm", "add_rmsnorm", "swiglu", "reglu", "linear")
+    swept = ("rmsnorm", "add_rmsnorm", "swiglu", "reglu", "linear", "decode_attention")
     only = [o for o in args.only.split(",") if o] or list(swept[:4])
     entries = [e for e in build_entries(dev, sh, only) if e.op in swept]
     if not args.only:
@@ -1039,7 +1040,8 @@ def run_sweep(args):
         row = {"name": e.name, "bytes": e.bytes, "auto": None, "variants": {}}
         n = int(min(64, max(1, -(-STREAM_BYTES // max(1, e.bytes)))))
         calls = e.replicas(n) if n > 1 else [e.launch]
-        op = {"swiglu": "glu", "reglu": "glu", "linear": "linear"}.get(e.op, "rmsnorm")
+        op = {"swiglu": "glu", "reglu": "glu", "linear": "linear",
+              "decode_attention": "decode_attention"}.get(e.op, "rmsnorm")
         settings = [(-1, "auto")]
         for v in range(sra.variant_count(op)):
             nm = sra.variant_name(op, v)
@@ -1048,6 +1050,8 @@ def run_sweep(args):
                 settings += [(v | (nv << 8), f"{nm}/nv{nv}") for nv in nvs]
             elif nm == "tcgen05":
                 settings += [(v, nm)] + [(v | (sk << 8), f"{nm}/splits{sk}") for sk in (2, 4, 6, 8, 12, 16)]
+            elif op == "decode_attention" and nm != "cuda_cores":
+                settings += [(v, nm)] + [(v | (sk << 8), f"{nm}/splits{sk}") for sk in (1, 2, 4, 8, 16)]
             elif nm == "warps_row":
                 settings += [(v | (nv << 8) | (g << 16), f"{nm}/g{g}nv{nv}") for g in (2, 4, 8) for nv in (8, 16)]
             else:

@@ -497,7 +497,9 @@ SRA_API int sra_set_pdl(int enable);
  * for an even n_head + 2 * n_kv_head), "glu" (0 = columns over threads and rows over
  * CTAs at 48 registers a thread, 1 = the same kernel with the registers the compiler
  * picks), "decode_attention" (0 = CUDA-core kernel,
- * 1 = mma.sync kernel for bf16 / fp16 with head_dim 64 or 128), "linear" (the
+ * 1 = mma.sync kernel for bf16 / fp16 with head_dim 64 or 128, 2 = the same
+ * contraction with the K / V tiles moved by TMA; for 1 and 2, OR-ed with (s << 8),
+ * s in 1, 2, 4, 8, 16, it also forces the CTAs per (request, kv head)), "linear" (the
  * projection of the _ws entry points once the prologue has run: 0 = mma.sync
  * kernels, 1 = the tcgen05 kernel, for up to 64 rows and N a multiple of 128;
  * OR-ed with (s << 8), s in 1..16, it also forces the tcgen05 kernel's K splits).

@@ -554,7 +554,7 @@ int variant_count(const char* op) {
     if (std::strcmp(op, "rmsnorm") == 0) return NORM_NUM_VARIANTS;
     if (std::strcmp(op, "rope_kv_store") == 0) return ROPE_NUM_VARIANTS;
     if (std::strcmp(op, "glu") == 0) return GLU_NUM_VARIANTS;
-    if (std::strcmp(op, "decode_attention") == 0) return 2;  // CUDA cores, mma.sync
+    if (std::strcmp(op, "decode_attention") == 0) return 3;  // CUDA cores, mma.sync, mma.sync fed by TMA
     if (std::strcmp(op, "linear") == 0) return 2;            // mma.sync, tcgen05 (projection over h)
     return SRA_ERR_ARG;
 }
@@ -859,8 +859,12 @@ static int attention_impl(const void* q, const void* kv_cache, const int32_t* bl
                         static_cast<int64_t>(decode_attention_mma_smem(head_dim)) <= limit;
     const int forced_all = g_force_attn.load(std::memory_order_relaxed);
     const int forced = forced_all < 0 ? -1 : (forced_all & 0xFF);  // variant; bits 8-15: splits (A/B only)
-    if (forced == 1 && !plan.tensor_cores) return SRA_ERR_VARIANT;
+    if ((forced == 1 || forced == 2) && !plan.tensor_cores) return SRA_ERR_VARIANT;
     if (forced == 0) plan.tensor_cores = false;
+    // the TMA-fed kernel: a 4-D tensor map over the cache (16-byte strides hold for head_dim
+    // 64 and 128), its ring in one CTA's shared memory
+    plan.tma = forced == 2;
+    if (plan.tma && static_cast<int64_t>(decode_attention_tma_smem(head_dim)) > limit) return SRA_ERR_VARIANT;
     int splits = 1;
     if (plan.tensor_cores) {
         // one 8-warp CTA per SM at most (its K/V rings fill the SM's shared memory), and at
@@ -872,16 +876,17 @@ static int attention_impl(const void* q, const void* kv_cache, const int32_t* bl
         while (splits < 8 && groups * splits < 2 * static_cast<int64_t>(sms) && max_blocks_per_seq >= 4 * splits)
             splits *= 2;
     }
-    if (forced_all > 0 && (forced_all >> 8)) {
-        const int fs = forced_all >> 8;
+    if (forced_all > 0 && ((forced_all >> 8) & 0xFF)) {
+        const int fs = (forced_all >> 8) & 0xFF;
         if ((fs & (fs - 1)) || fs > (plan.tensor_cores ? 16 : 8)) return SRA_ERR_VARIANT;
         splits = fs;
     }
     plan.splits = splits;
     plan.stages = 4;
     if (static_cast<int64_t>(decode_attention_smem(group, head_dim, block_size, 4, es)) > limit) plan.stages = 2;
-    plan.smem = plan.tensor_cores ? decode_attention_mma_smem(head_dim)
-                                  : decode_attention_smem(group, head_dim, block_size, plan.stages, es);
+    plan.smem = plan.tma            ? decode_attention_tma_smem(head_dim)
+                : plan.tensor_cores ? decode_attention_mma_smem(head_dim)
+                                    : decode_attention_smem(group, head_dim, block_size, plan.stages, es);
     if (static_cast<int64_t>(plan.smem) > limit) return SRA_ERR_SHAPE;
     AttnArgs a;
     a.q = q;
@@ -1176,7 +1181,7 @@ const char* sra_variant_name(const char* op, int variant) {
                                              "warp_smem", "pair_smem", "cta_lean",  "warps_row"};
     static const char* const rope_names[] = {"token_cta", "token_cta2"};
     static const char* const glu_names[] = {"cols_rows", "cols_rows_regs"};
-    static const char* const attn_names[] = {"cuda_cores", "mma_sync"};
+    static const char* const attn_names[] = {"cuda_cores", "mma_sync", "mma_sync_tma"};
     static const char* const lin_names[] = {"mma_sync", "tcgen05"};
     const int n = variant_count(op);
     if (n < 0 || variant < 0 || variant >= n) return nullptr;

@@ -36,6 +36,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tma.cuh"
 
 namespace cg = cooperative_groups;
 
@@ -290,26 +291,30 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// mma.sync m16n8k16 with rows 8-15 of A zero (at most 8 query heads share a kv head): only
+// the C / D fragment registers of rows 0-7 (c0, c1) are kept.
 template <typename T>
 struct Mma;
 template <>
 struct Mma<__nv_bfloat16> {
-    __device__ __forceinline__ static void run(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    __device__ __forceinline__ static void run(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+        float z0, z1;  // rows 8-15 of A are zero: their results are dropped, not held
         asm volatile(
             "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-            "{%0,%1,%2,%3};"
-            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+            "{%0,%1,%10,%11};"
+            : "+f"(d[0]), "+f"(d[1]), "=f"(z0), "=f"(z1)
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.0f), "f"(0.0f));
     }
 };
 template <>
 struct Mma<__half> {
-    __device__ __forceinline__ static void run(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    __device__ __forceinline__ static void run(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+        float z0, z1;  // rows 8-15 of A are zero: their results are dropped, not held
         asm volatile(
             "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-            "{%0,%1,%2,%3};"
-            : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+            "{%0,%1,%10,%11};"
+            : "+f"(d[0]), "+f"(d[1]), "=f"(z0), "=f"(z1)
+            : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.0f), "f"(0.0f));
     }
 };
 
@@ -344,6 +349,84 @@ __device__ __forceinline__ float2 unpack2(uint32_t w) {
     return make_float2(f[0], f[1]);
 }
 
+// One 16-token tile of a warp: S = Q K^T (two 8-token halves), the online-softmax update of
+// (m, l) on the rows this lane holds, and O = O * corr + P V with P split into a T-rounded high
+// part and its residual. `addr(tok, chunk)` is the element offset of 16-byte chunk `chunk` of
+// token `tok`'s row in the K (and V) tile, whatever layout the tile was staged in; `valid` has
+// bit t set for the tile's tokens that count.
+template <typename T, int HD, typename Addr>
+__device__ __forceinline__ void tile_step(const T* Ks, const T* Vs, unsigned valid, const uint32_t (&qa)[HD / 16][2],
+                                          float (&o)[HD / 8][2], float& m, float& l, float scale_log2, int lane,
+                                          Addr addr) {
+    constexpr int KS = HD / 16;
+    constexpr int NB = HD / 8;
+    const unsigned FULL = 0xffffffffu;
+    const int ft = lane & 3;
+    // S = Q K^T: two 8-token blocks
+    float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    {
+        const int mi = lane >> 3, rr = lane & 7;
+        const int tok = 8 * (mi >> 1) + rr;
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+            uint32_t kb[4];
+            const int chunk = 2 * s + (mi & 1);
+            ldsm_x4(kb, Ks + addr(tok, chunk));
+            Mma<T>::run(sc[0], qa[s][0], qa[s][1], kb[0], kb[1]);
+            Mma<T>::run(sc[1], qa[s][0], qa[s][1], kb[2], kb[3]);
+        }
+    }
+    // online softmax on row fg (this thread's tokens: 8 nb + 2 ft + e)
+    float v[2][2];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            v[nb][e] = (valid >> (8 * nb + 2 * ft + e)) & 1u ? sc[nb][e] * scale_log2 : -INFINITY;
+            mx = fmaxf(mx, v[nb][e]);
+        }
+    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
+    const float m_new = fmaxf(m, mx);
+    const float corr = m_new == -INFINITY ? 1.0f : ex2(m - m_new);
+    float p[2][2];
+    float ps = 0.0f;
+#pragma unroll
+    for (int nb = 0; nb < 2; ++nb)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            p[nb][e] = v[nb][e] == -INFINITY ? 0.0f : ex2(v[nb][e] - m_new);
+            ps += p[nb][e];
+        }
+    l = l * corr + ps;
+    m = m_new;
+    // P as A fragments, high part and residual
+    uint32_t ph0 = pack2<T>(p[0][0], p[0][1]), ph1 = pack2<T>(p[1][0], p[1][1]);
+    const float2 h0 = unpack2<T>(ph0), h1 = unpack2<T>(ph1);
+    uint32_t pl0 = pack2<T>(p[0][0] - h0.x, p[0][1] - h0.y), pl1 = pack2<T>(p[1][0] - h1.x, p[1][1] - h1.y);
+    // O = O * corr + P V (the rescale only when some row's max moved)
+    if (__any_sync(FULL, corr != 1.0f)) {
+#pragma unroll
+        for (int d = 0; d < NB; ++d) o[d][0] *= corr, o[d][1] *= corr;
+    }
+    {
+        const int mi = lane >> 3, rr = lane & 7;
+        const int tok = 8 * (mi & 1) + rr;
+#pragma unroll
+        for (int d2 = 0; d2 < NB / 2; ++d2) {
+            uint32_t vb[4];
+            const int chunk = 2 * d2 + (mi >> 1);
+            ldsm_x4_trans(vb, Vs + addr(tok, chunk));
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                Mma<T>::run(o[2 * d2 + h], ph0, ph1, vb[2 * h], vb[2 * h + 1]);
+                Mma<T>::run(o[2 * d2 + h], pl0, pl1, vb[2 * h], vb[2 * h + 1]);
+            }
+        }
+    }
+}
+
 constexpr int kMmaWarps = 8;
 constexpr int kMmaTile = 16;    // tokens per warp tile
 constexpr int kMmaStages = 3;   // tiles per warp ring
@@ -357,268 +440,49 @@ __host__ __device__ inline size_t mma_smem(int HD) {
     return mma_ring_bytes(HD) + static_cast<size_t>(kMmaWarps) * kMmaStages * 4;  // + per-slot row masks
 }
 
-// GMERGE: the splits of a (request, kv head) are independent CTAs (a.gsplits of them, more
-// than a cluster holds): each writes its (max, sum, partial output) to the workspace, and the
-// CTA that finishes last (an atomic count per (request, kv head)) merges them and resets the
-// count to zero for the next call.
-template <typename T, int HD, bool GMERGE>
-__global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) {
-    constexpr int CPR = HD * 2 / 16;      // 16-byte chunks per row
-    constexpr int KS = HD / 16;           // k-steps of Q K^T
-    constexpr int NB = HD / 8;            // 8-dim blocks of O
-    constexpr int TE = kMmaTile * HD;     // elements of one K or V tile
-    extern __shared__ __align__(16) unsigned char smem[];
-    cg::cluster_group cluster = cg::this_cluster();
-    const int S = GMERGE ? a.gsplits : static_cast<int>(cluster.num_blocks());
-    const int rank = GMERGE ? static_cast<int>(blockIdx.x % a.gsplits) : static_cast<int>(cluster.block_rank());
-    const int64_t grp = blockIdx.x / S;
-    const int64_t b = grp / a.n_kv;
-    const int kvh = static_cast<int>(grp - b * a.n_kv);
-    const int G = a.group, BS = a.block_size;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int fg = lane >> 2, ft = lane & 3;  // fragment row group and thread-in-group
-    T* ring = reinterpret_cast<T*>(smem) + static_cast<size_t>(warp) * kMmaStages * 2 * TE;
-
-    {
-        // Before the dependency wait: warm what the first tiles need. First the loads that
-        // depend on nothing: this request's seq_len and this split's whole slice of the block
-        // table (so the later tiles' table reads hit the L2 and each tile costs one DRAM round
-        // trip, not two). Then the K and V rows of this warp's first two tiles: the split is a
-        // static slice of the table's capacity, so the tiles' tokens are known; their block ids
-        // are read relaxed (the previous kernel may still be writing them) and only steer
-        // prefetches. Everything used below is read again after the wait.
-        const int64_t cap0 = a.max_blocks * BS;
-        const int64_t per0 = ((cap0 + S - 1) / S + kMmaTile - 1) / kMmaTile * kMmaTile;
-        const int64_t s0 = rank * per0, s1 = cap0 < s0 + per0 ? cap0 : s0 + per0;
-        if (warp == 0 && lane == 0) prefetch_lines(a.seq_lens + b, 4, 0, 1);
-        if (warp == kMmaWarps - 1 && s0 < s1)
-            prefetch_lines(a.table + b * a.max_blocks + s0 / BS, ((s1 - 1) / BS - s0 / BS + 1) * 4, lane, 32);
-        int blk[2] = {-1, -1};
-        int64_t tok[2];
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            tok[j] = s0 + (warp + j * kMmaWarps) * kMmaTile + (lane & (kMmaTile - 1));
-            if (tok[j] < s1)
-                asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];"
-                             : "=r"(blk[j])
-                             : "l"(a.table + b * a.max_blocks + tok[j] / BS));
-        }
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            if (tok[j] < s1 && blk[j] >= 0 && blk[j] < a.num_blocks) {
-                const T* row = static_cast<const T*>(a.cache) +
-                               ((static_cast<int64_t>(blk[j]) * BS + tok[j] % BS) * a.n_kv + kvh) * HD +
-                               (lane >= kMmaTile ? a.num_blocks * BS * static_cast<int64_t>(a.n_kv) * HD : 0);
-                prefetch_lines(row, HD * 2, 0, 1);
-            }
-        }
-    }
-    pdl_enter();
-    int64_t len = a.seq_lens[b];
-    const int64_t cap = a.max_blocks * BS;
-    if ((len < 0 || len > cap) && kvh == 0 && rank == 0 && threadIdx.x == 0 && a.err) atomicAdd(a.err, 1);
-    len = len < 0 ? 0 : (len > cap ? cap : len);
-    // static split of the table's capacity (not of seq_len), so the block-table reads of the
-    // first tiles need not wait for seq_len; tokens at or past seq_len are masked
-    const int64_t per = ((cap + S - 1) / S + kMmaTile - 1) / kMmaTile * kMmaTile;
-    const int64_t t_begin = rank * per < cap ? rank * per : cap;
-    const int64_t t_lim = t_begin + per < cap ? t_begin + per : cap;
-    const int64_t t_end = len < t_begin ? t_begin : (len < t_lim ? len : t_lim);
-    const int32_t* table = a.table + b * a.max_blocks;
-    auto block_ok = [&](int32_t blk) { return blk >= 0 && blk < a.num_blocks; };
-    const int64_t tok_stride = static_cast<int64_t>(a.n_kv) * HD;
-    const int64_t v_plane = a.num_blocks * BS * tok_stride;
-    const T* cache = static_cast<const T*>(a.cache);
-    const int64_t n_tiles = (t_end - t_begin + kMmaTile - 1) / kMmaTile;
-    const int64_t n_static = (t_lim - t_begin + kMmaTile - 1) / kMmaTile;
-    const int bs_log2 = __ffs(BS) - 1;  // block_size is a power of two
-    unsigned* vmask = reinterpret_cast<unsigned*>(smem + mma_ring_bytes(HD)) + warp * kMmaStages;
+// The end of a (request, kv head, split) CTA of the tensor-core kernels: the warps' (m, l, O)
+// merged in shared memory (over the drained rings), then the splits merged through distributed
+// shared memory (a cluster) or, with GMERGE, through the workspace by the CTA that finishes
+// last. NW warps hold partials; warps past them (a copy-issuing warp) only join the barriers.
+template <typename T, int HD, bool GMERGE, int NW>
+__device__ __forceinline__ void finish_mma(const AttnArgs& a, unsigned char* smem, float m, float l,
+                                           float (&o)[HD / 8][2], int lane, int warp, int64_t grp, int64_t b,
+                                           int kvh, int S, int rank, int G, cg::cluster_group& cluster) {
+    constexpr int NB = HD / 8;
     const unsigned FULL = 0xffffffffu;
-    // This warp's tile u into ring slot (u / warps) % stages: lane r < 16 finds token r's row
-    // once; the 16-byte copies then go row by row, LPR lanes per row (contiguous), and each
-    // lane's destination offsets in a slot are fixed, computed once. Chunks are XOR-swizzled
-    // by row so the 8 rows one ldmatrix reads sit in 8 different bank groups. Rows past
-    // seq_len or in a bad block are zero-filled (no read) and masked.
-    constexpr int LPR = CPR < 32 ? CPR : 32;  // lanes per row
-    constexpr int RPI = 32 / LPR;              // rows per instruction
-    const int col = lane % LPR, rr0 = lane / LPR;
-    const int64_t kvh_off = static_cast<int64_t>(kvh) * HD;
-    int dst_off[kMmaTile / RPI][CPR / LPR];
-#pragma unroll
-    for (int i = 0; i < kMmaTile / RPI; ++i)
-#pragma unroll
-        for (int cc = 0; cc < CPR / LPR; ++cc) {
-            const int r = rr0 + RPI * i, ch = col + cc * LPR;
-            dst_off[i][cc] = r * HD + ((ch ^ (r & 7)) * 8);
-        }
-    // Block-table entry of token `lane` of tile u (lanes < 16; 0 past the static range). It is
-    // read one tile ahead of its use, so the copy issue never waits on the table's latency.
-    auto load_blk = [&](int64_t u) -> int32_t {
-        const int64_t tok = t_begin + u * kMmaTile + lane;
-        return lane < kMmaTile && tok < t_lim ? table[tok >> bs_log2] : 0;
-    };
-    auto issue = [&](int64_t u, int32_t blk) {
-        const int slot = static_cast<int>((u / kMmaWarps) % kMmaStages);
-        T* dst = ring + static_cast<size_t>(slot) * 2 * TE;
-        int64_t off = -1;  // element offset of token `lane`'s K row in the cache, -1: no row
-        if (lane < kMmaTile) {
-            const int64_t tok = t_begin + u * kMmaTile + lane;
-            if (tok < t_end) {
-                if (block_ok(blk)) {
-                    off = ((static_cast<int64_t>(blk) << bs_log2) + (tok & (BS - 1))) * tok_stride + kvh_off;
-                } else if (kvh == 0 && (tok & (BS - 1)) == 0 && a.err) {
-                    atomicAdd(a.err, 1);  // a bad block entry, counted once (kv head 0, its first token)
-                }
-            }
-        }
-        const unsigned valid = __ballot_sync(FULL, off >= 0) & 0xffffu;
-        if (lane == 0) vmask[slot] = valid;
-#pragma unroll
-        for (int i = 0; i < kMmaTile / RPI; ++i) {
-            const int64_t ro = __shfl_sync(FULL, off, rr0 + RPI * i);
-            const T* src = ro >= 0 ? cache + ro + col * 8 : cache;
-            const int n = ro >= 0 ? 16 : 0;
-#pragma unroll
-            for (int cc = 0; cc < CPR / LPR; ++cc) {
-                T* d = dst + dst_off[i][cc];
-                cp_async16_zfill(d, src + cc * LPR * 8, n);
-                cp_async16_zfill(d + TE, ro >= 0 ? src + cc * LPR * 8 + v_plane : cache, n);
-            }
-        }
-    };
-    {
-        int32_t blk0[kMmaStages - 1];
-#pragma unroll
-        for (int k = 0; k < kMmaStages - 1; ++k) blk0[k] = load_blk(warp + static_cast<int64_t>(k) * kMmaWarps);
-#pragma unroll
-        for (int k = 0; k < kMmaStages - 1; ++k) {
-            const int64_t u = warp + static_cast<int64_t>(k) * kMmaWarps;
-            if (u < n_static) issue(u, blk0[k]);
-            cp_async_commit();
-        }
-    }
-    int32_t blk_next = load_blk(warp + static_cast<int64_t>(kMmaStages - 1) * kMmaWarps);
-    // Q as A fragments (loaded while the first tiles are in flight): rows = query heads
-    // (zero past G), columns = dims of k-step s
-    uint32_t qa[KS][2];
-    {
-        const T* qrow = static_cast<const T*>(a.q) + b * a.qs + static_cast<int64_t>(kvh * G + fg) * HD;
-#pragma unroll
-        for (int s = 0; s < KS; ++s) {
-            qa[s][0] = fg < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * s + 2 * ft) : 0u;
-            qa[s][1] = fg < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * s + 8 + 2 * ft) : 0u;
-        }
-    }
-
-    float o[NB][4];  // C fragments of O; rows fg + 8 (c2, c3) stay zero
-#pragma unroll
-    for (int d = 0; d < NB; ++d) o[d][0] = o[d][1] = o[d][2] = o[d][3] = 0.0f;
-    float m = -INFINITY, l = 0.0f;
-    for (int64_t u = warp, k = 0; u < n_tiles; u += kMmaWarps, ++k) {
-        cp_async_wait<kMmaStages - 2>();
-        __syncwarp();
-        if (u + (kMmaStages - 1) * kMmaWarps < n_tiles) {
-            issue(u + (kMmaStages - 1) * kMmaWarps, blk_next);
-            blk_next = load_blk(u + kMmaStages * kMmaWarps);
-        }
-        cp_async_commit();
-        const T* Ks = ring + static_cast<size_t>(k % kMmaStages) * 2 * TE;
-        const T* Vs = Ks + TE;
-        const unsigned valid = vmask[k % kMmaStages];
-
-        // S = Q K^T: two 8-token blocks
-        float sc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-        {
-            const int mi = lane >> 3, rr = lane & 7;
-            const int tok = 8 * (mi >> 1) + rr;
-#pragma unroll
-            for (int s = 0; s < KS; ++s) {
-                uint32_t kb[4];
-                const int chunk = 2 * s + (mi & 1);
-                ldsm_x4(kb, Ks + tok * HD + ((chunk ^ (tok & 7)) * 8));
-                Mma<T>::run(sc[0], qa[s][0], qa[s][1], kb[0], kb[1]);
-                Mma<T>::run(sc[1], qa[s][0], qa[s][1], kb[2], kb[3]);
-            }
-        }
-        // online softmax on row fg (this thread's tokens: 8 nb + 2 ft + e)
-        float v[2][2];
-        float mx = -INFINITY;
-#pragma unroll
-        for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                v[nb][e] = (valid >> (8 * nb + 2 * ft + e)) & 1u ? sc[nb][e] * a.scale_log2 : -INFINITY;
-                mx = fmaxf(mx, v[nb][e]);
-            }
-        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(FULL, mx, 2));
-        const float m_new = fmaxf(m, mx);
-        const float corr = m_new == -INFINITY ? 1.0f : ex2(m - m_new);
-        float p[2][2];
-        float ps = 0.0f;
-#pragma unroll
-        for (int nb = 0; nb < 2; ++nb)
-#pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                p[nb][e] = v[nb][e] == -INFINITY ? 0.0f : ex2(v[nb][e] - m_new);
-                ps += p[nb][e];
-            }
-        l = l * corr + ps;
-        m = m_new;
-        // P as A fragments, high part and residual
-        uint32_t ph0 = pack2<T>(p[0][0], p[0][1]), ph1 = pack2<T>(p[1][0], p[1][1]);
-        const float2 h0 = unpack2<T>(ph0), h1 = unpack2<T>(ph1);
-        uint32_t pl0 = pack2<T>(p[0][0] - h0.x, p[0][1] - h0.y), pl1 = pack2<T>(p[1][0] - h1.x, p[1][1] - h1.y);
-        // O = O * corr + P V (the rescale only when some row's max moved)
-        if (__any_sync(FULL, corr != 1.0f)) {
-#pragma unroll
-            for (int d = 0; d < NB; ++d) o[d][0] *= corr, o[d][1] *= corr;
-        }
-        {
-            const int mi = lane >> 3, rr = lane & 7;
-            const int tok = 8 * (mi & 1) + rr;
-#pragma unroll
-            for (int d2 = 0; d2 < NB / 2; ++d2) {
-                uint32_t vb[4];
-                const int chunk = 2 * d2 + (mi >> 1);
-                ldsm_x4_trans(vb, Vs + tok * HD + ((chunk ^ (tok & 7)) * 8));
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    Mma<T>::run(o[2 * d2 + h], ph0, ph1, vb[2 * h], vb[2 * h + 1]);
-                    Mma<T>::run(o[2 * d2 + h], pl0, pl1, vb[2 * h], vb[2 * h + 1]);
-                }
-            }
-        }
-    }
-    cp_async_wait<0>();
+    const int fg = lane >> 2, ft = lane & 3;
     l += __shfl_xor_sync(FULL, l, 1);
     l += __shfl_xor_sync(FULL, l, 2);
 
     // warp partials into shared memory (over the rings, which are done)
     __syncthreads();
-    float* wm = reinterpret_cast<float*>(smem);          // [warps][8]
-    float* wl = wm + kMmaWarps * 8;                      // [warps][8]
-    float* wo = wl + kMmaWarps * 8;                      // [warps][8][HD]
-    float* pm = wo + kMmaWarps * 8 * HD;                 // [8]  CTA partials for the cluster merge
-    float* pl = pm + 8;                                  // [8]
-    float* pacc = pl + 8;                                // [8][HD]
-    if (ft == 0) {
-        wm[warp * 8 + fg] = m;
-        wl[warp * 8 + fg] = l;
-    }
+    float* wm = reinterpret_cast<float*>(smem);  // [warps][8]
+    float* wl = wm + NW * 8;                     // [warps][8]
+    float* wo = wl + NW * 8;                     // [warps][8][HD]
+    float* pm = wo + NW * 8 * HD;                // [8]  CTA partials for the cluster merge
+    float* pl = pm + 8;                          // [8]
+    float* pacc = pl + 8;                        // [8][HD]
+    if (warp < NW) {
+        if (ft == 0) {
+            wm[warp * 8 + fg] = m;
+            wl[warp * 8 + fg] = l;
+        }
 #pragma unroll
-    for (int d = 0; d < NB; ++d) {
-        wo[(warp * 8 + fg) * HD + 8 * d + 2 * ft] = o[d][0];
-        wo[(warp * 8 + fg) * HD + 8 * d + 2 * ft + 1] = o[d][1];
+        for (int d = 0; d < NB; ++d) {
+            wo[(warp * 8 + fg) * HD + 8 * d + 2 * ft] = o[d][0];
+            wo[(warp * 8 + fg) * HD + 8 * d + 2 * ft + 1] = o[d][1];
+        }
     }
     __syncthreads();
+    T* out = static_cast<T*>(a.out) + b * a.os + static_cast<int64_t>(kvh * G) * HD;
+    const bool alone = !GMERGE && S == 1;  // one CTA holds the whole (request, kv head)
     for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
         const int gg = idx / HD, d = idx - gg * HD;
         float M = -INFINITY;
-        for (int w = 0; w < kMmaWarps; ++w) M = fmaxf(M, wm[w * 8 + gg]);
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, wm[w * 8 + gg]);
         float num = 0.0f, den = 0.0f;
         if (M != -INFINITY) {
-            for (int w = 0; w < kMmaWarps; ++w) {
+            for (int w = 0; w < NW; ++w) {
                 const float mw = wm[w * 8 + gg];
                 if (mw == -INFINITY) continue;
                 const float sw = exp2f(mw - M);
@@ -626,10 +490,14 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
                 den = fmaf(sw, wl[w * 8 + gg], den);
             }
         }
-        pacc[idx] = num;
-        if (d == 0) pm[gg] = M, pl[gg] = den;
+        if (alone) {
+            out[idx] = from_f32<T>(den > 0.0f ? num / den : 0.0f);
+        } else {
+            pacc[idx] = num;
+            if (d == 0) pm[gg] = M, pl[gg] = den;
+        }
     }
-    T* out = static_cast<T*>(a.out) + b * a.os + static_cast<int64_t>(kvh * G) * HD;
+    if (alone) return;
     if constexpr (GMERGE) {
         // this split's partial into the workspace: [8 max][8 sum][8 x HD output]
         float* slot = a.ws_part + (static_cast<int64_t>(grp) * S + rank) * (16 + 8 * HD);
@@ -722,6 +590,181 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
     cluster.sync();
 }
 
+// GMERGE: the splits of a (request, kv head) are independent CTAs (a.gsplits of them, more
+// than a cluster holds): each writes its (max, sum, partial output) to the workspace, and the
+// CTA that finishes last (an atomic count per (request, kv head)) merges them and resets the
+// count to zero for the next call.
+template <typename T, int HD, bool GMERGE>
+__global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) {
+    constexpr int CPR = HD * 2 / 16;      // 16-byte chunks per row
+    constexpr int KS = HD / 16;           // k-steps of Q K^T
+    constexpr int NB = HD / 8;            // 8-dim blocks of O
+    constexpr int TE = kMmaTile * HD;     // elements of one K or V tile
+    extern __shared__ __align__(16) unsigned char smem[];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int S = GMERGE ? a.gsplits : static_cast<int>(cluster.num_blocks());
+    const int rank = GMERGE ? static_cast<int>(blockIdx.x % a.gsplits) : static_cast<int>(cluster.block_rank());
+    const int64_t grp = blockIdx.x / S;
+    const int64_t b = grp / a.n_kv;
+    const int kvh = static_cast<int>(grp - b * a.n_kv);
+    const int G = a.group, BS = a.block_size;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int fg = lane >> 2, ft = lane & 3;  // fragment row group and thread-in-group
+    T* ring = reinterpret_cast<T*>(smem) + static_cast<size_t>(warp) * kMmaStages * 2 * TE;
+
+    {
+        // Before the dependency wait: warm what the first tiles need. First the loads that
+        // depend on nothing: this request's seq_len and this split's whole slice of the block
+        // table (so the later tiles' table reads hit the L2 and each tile costs one DRAM round
+        // trip, not two). Then the K and V rows of this warp's first two tiles: the split is a
+        // static slice of the table's capacity, so the tiles' tokens are known; their block ids
+        // are read relaxed (the previous kernel may still be writing them) and only steer
+        // prefetches. Everything used below is read again after the wait.
+        const int64_t cap0 = a.max_blocks * BS;
+        const int64_t per0 = ((cap0 + S - 1) / S + kMmaTile - 1) / kMmaTile * kMmaTile;
+        const int64_t s0 = rank * per0, s1 = cap0 < s0 + per0 ? cap0 : s0 + per0;
+        if (warp == 0 && lane == 0) prefetch_lines(a.seq_lens + b, 4, 0, 1);
+        if (warp == kMmaWarps - 1 && s0 < s1)
+            prefetch_lines(a.table + b * a.max_blocks + s0 / BS, ((s1 - 1) / BS - s0 / BS + 1) * 4, lane, 32);
+        int blk[2] = {-1, -1};
+        int64_t tok[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            tok[j] = s0 + (warp + j * kMmaWarps) * kMmaTile + (lane & (kMmaTile - 1));
+            if (tok[j] < s1)
+                asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];"
+                             : "=r"(blk[j])
+                             : "l"(a.table + b * a.max_blocks + tok[j] / BS));
+        }
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            if (tok[j] < s1 && blk[j] >= 0 && blk[j] < a.num_blocks) {
+                const T* row = static_cast<const T*>(a.cache) +
+                               ((static_cast<int64_t>(blk[j]) * BS + tok[j] % BS) * a.n_kv + kvh) * HD +
+                               (lane >= kMmaTile ? a.num_blocks * BS * static_cast<int64_t>(a.n_kv) * HD : 0);
+                prefetch_lines(row, HD * 2, 0, 1);
+            }
+        }
+    }
+    pdl_enter();
+    const int64_t cap = a.max_blocks * BS;
+    // static split of the table's capacity (not of seq_len), so the block-table reads of the
+    // first tiles need not wait for seq_len; tokens at or past seq_len are masked
+    const int64_t per = ((cap + S - 1) / S + kMmaTile - 1) / kMmaTile * kMmaTile;
+    const int64_t t_begin = rank * per < cap ? rank * per : cap;
+    const int64_t t_lim = t_begin + per < cap ? t_begin + per : cap;
+    const int32_t* table = a.table + b * a.max_blocks;
+    const int bs_log2 = __ffs(BS) - 1;  // block_size is a power of two
+    // Block-table entry of token `lane` of tile u (lanes < 16; 0 past the static range). It is
+    // read one tile ahead of its use, so the copy issue never waits on the table's latency.
+    auto load_blk = [&](int64_t u) -> int32_t {
+        const int64_t tok = t_begin + u * kMmaTile + lane;
+        return lane < kMmaTile && tok < t_lim ? table[tok >> bs_log2] : 0;
+    };
+    // the first tiles' block ids and seq_len are requested together: one round trip, not two
+    int32_t blk0[kMmaStages];
+#pragma unroll
+    for (int k = 0; k < kMmaStages; ++k) blk0[k] = load_blk(warp + static_cast<int64_t>(k) * kMmaWarps);
+    int64_t len = a.seq_lens[b];
+    if ((len < 0 || len > cap) && kvh == 0 && rank == 0 && threadIdx.x == 0 && a.err) atomicAdd(a.err, 1);
+    len = len < 0 ? 0 : (len > cap ? cap : len);
+    const int64_t t_end = len < t_begin ? t_begin : (len < t_lim ? len : t_lim);
+    auto block_ok = [&](int32_t blk) { return blk >= 0 && blk < a.num_blocks; };
+    const int64_t tok_stride = static_cast<int64_t>(a.n_kv) * HD;
+    const int64_t v_plane = a.num_blocks * BS * tok_stride;
+    const T* cache = static_cast<const T*>(a.cache);
+    const int64_t n_tiles = (t_end - t_begin + kMmaTile - 1) / kMmaTile;
+    const int64_t n_static = (t_lim - t_begin + kMmaTile - 1) / kMmaTile;
+    unsigned* vmask = reinterpret_cast<unsigned*>(smem + mma_ring_bytes(HD)) + warp * kMmaStages;
+    const unsigned FULL = 0xffffffffu;
+    // This warp's tile u into ring slot (u / warps) % stages: lane r < 16 finds token r's row
+    // once; the 16-byte copies then go row by row, LPR lanes per row (contiguous), and each
+    // lane's destination offsets in a slot are fixed, computed once. Chunks are XOR-swizzled
+    // by row so the 8 rows one ldmatrix reads sit in 8 different bank groups. Rows past
+    // seq_len or in a bad block are zero-filled (no read) and masked.
+    constexpr int LPR = CPR < 32 ? CPR : 32;  // lanes per row
+    constexpr int RPI = 32 / LPR;              // rows per instruction
+    const int col = lane % LPR, rr0 = lane / LPR;
+    const int64_t kvh_off = static_cast<int64_t>(kvh) * HD;
+    int dst_off[kMmaTile / RPI][CPR / LPR];
+#pragma unroll
+    for (int i = 0; i < kMmaTile / RPI; ++i)
+#pragma unroll
+        for (int cc = 0; cc < CPR / LPR; ++cc) {
+            const int r = rr0 + RPI * i, ch = col + cc * LPR;
+            dst_off[i][cc] = r * HD + ((ch ^ (r & 7)) * 8);
+        }
+    auto issue = [&](int64_t u, int32_t blk) {
+        const int slot = static_cast<int>((u / kMmaWarps) % kMmaStages);
+        T* dst = ring + static_cast<size_t>(slot) * 2 * TE;
+        int64_t off = -1;  // element offset of token `lane`'s K row in the cache, -1: no row
+        if (lane < kMmaTile) {
+            const int64_t tok = t_begin + u * kMmaTile + lane;
+            if (tok < t_end) {
+                if (block_ok(blk)) {
+                    off = ((static_cast<int64_t>(blk) << bs_log2) + (tok & (BS - 1))) * tok_stride + kvh_off;
+                } else if (kvh == 0 && (tok & (BS - 1)) == 0 && a.err) {
+                    atomicAdd(a.err, 1);  // a bad block entry, counted once (kv head 0, its first token)
+                }
+            }
+        }
+        const unsigned valid = __ballot_sync(FULL, off >= 0) & 0xffffu;
+        if (lane == 0) vmask[slot] = valid;
+#pragma unroll
+        for (int i = 0; i < kMmaTile / RPI; ++i) {
+            const int64_t ro = __shfl_sync(FULL, off, rr0 + RPI * i);
+            const T* src = ro >= 0 ? cache + ro + col * 8 : cache;
+            const int n = ro >= 0 ? 16 : 0;
+#pragma unroll
+            for (int cc = 0; cc < CPR / LPR; ++cc) {
+                T* d = dst + dst_off[i][cc];
+                cp_async16_zfill(d, src + cc * LPR * 8, n);
+                cp_async16_zfill(d + TE, ro >= 0 ? src + cc * LPR * 8 + v_plane : cache, n);
+            }
+        }
+    };
+#pragma unroll
+    for (int k = 0; k < kMmaStages - 1; ++k) {
+        const int64_t u = warp + static_cast<int64_t>(k) * kMmaWarps;
+        if (u < n_static) issue(u, blk0[k]);
+        cp_async_commit();
+    }
+    int32_t blk_next = blk0[kMmaStages - 1];
+    // Q as A fragments (loaded while the first tiles are in flight): rows = query heads
+    // (zero past G), columns = dims of k-step s
+    uint32_t qa[KS][2];
+    {
+        const T* qrow = static_cast<const T*>(a.q) + b * a.qs + static_cast<int64_t>(kvh * G + fg) * HD;
+#pragma unroll
+        for (int s = 0; s < KS; ++s) {
+            qa[s][0] = fg < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * s + 2 * ft) : 0u;
+            qa[s][1] = fg < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * s + 8 + 2 * ft) : 0u;
+        }
+    }
+
+    float o[NB][2];  // C fragments of O (rows fg: c0, c1)
+#pragma unroll
+    for (int d = 0; d < NB; ++d) o[d][0] = o[d][1] = 0.0f;
+    float m = -INFINITY, l = 0.0f;
+    for (int64_t u = warp, k = 0; u < n_tiles; u += kMmaWarps, ++k) {
+        cp_async_wait<kMmaStages - 2>();
+        __syncwarp();
+        if (u + (kMmaStages - 1) * kMmaWarps < n_tiles) {
+            issue(u + (kMmaStages - 1) * kMmaWarps, blk_next);
+            blk_next = load_blk(u + kMmaStages * kMmaWarps);
+        }
+        cp_async_commit();
+        const T* Ks = ring + static_cast<size_t>(k % kMmaStages) * 2 * TE;
+        const T* Vs = Ks + TE;
+        const unsigned valid = vmask[k % kMmaStages];
+
+        tile_step<T, HD>(Ks, Vs, valid, qa, o, m, l, a.scale_log2, lane,
+                         [](int tok, int chunk) { return tok * HD + ((chunk ^ (tok & 7)) * 8); });
+    }
+    cp_async_wait<0>();
+    finish_mma<T, HD, GMERGE, kMmaWarps>(a, smem, m, l, o, lane, warp, grp, b, kvh, S, rank, G, cluster);
+}
+
 template <typename T, int HD>
 cudaError_t launch_mma(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
     const size_t smem = mma_smem(HD);
@@ -763,6 +806,243 @@ cudaError_t launch_mma(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
     return launch_kernel(kernel, grid, block, smem, s, p.pdl, splits, a);
 }
 
+
+// ------------------------------------------------------------------------------------------
+// Tensor-core path with the K / V tiles moved by TMA (bf16 / fp16, head_dim 64 or 128).
+//
+// The same work split, per-tile contraction and merge as decode_mma_kernel, with the data
+// movement taken off the compute warps: a ninth warp streams the tiles. It reads the
+// split's block-table entries 32 tiles at a time (one coalesced load, the entries passed by
+// shuffles) and for each 16-token tile issues the TMA box copies of its cache rows (a 4-D
+// tensor map over the cache: [HD][n_kv][num_blocks * block_size][K | V plane], boxes of 64
+// dims x 1 head x 16 rows (8 for blocks of 8 tokens), 128-byte swizzle) into ring slot
+// u % R, completing on the slot's full barrier, together with the tile's row mask. Compute
+// warp u % 8 waits for the slot, zeroes the V rows of tokens that do not count (past
+// seq_len, or in a bad block, whose rows are not copied), runs tile_step, and releases the
+// slot on its empty barrier. R = 96 KB of slots, so two CTAs share an SM.
+constexpr int kTmaWarps = 8;  // compute warps; warp 8 issues the copies
+constexpr int kTmaTile = 16;  // tokens per tile
+template <int HD>
+__host__ __device__ constexpr int tma_slots() { return HD == 128 ? 12 : 24; }
+template <int HD>
+__host__ __device__ constexpr size_t tma_slot_bytes() { return 2u * kTmaTile * HD * 2; }  // K and V tiles
+__host__ __device__ inline size_t tma_smem(int HD) {
+    const size_t ring = HD == 128 ? tma_slots<128>() * tma_slot_bytes<128>() : tma_slots<64>() * tma_slot_bytes<64>();
+    const size_t merge = (static_cast<size_t>(kTmaWarps) * 8 * (HD + 2) + 8 * (HD + 2)) * 4;
+    const size_t gmerge = static_cast<size_t>(kMaxGsplits) * 24 * 4 + 64 + 16 * 8 * static_cast<size_t>(HD) * 4;
+    size_t need = ring > merge ? ring : merge;
+    need = need > gmerge ? need : gmerge;
+    return 1024 + need;
+}
+
+template <typename T, int HD, bool GMERGE>
+__global__ void __maxnreg__(112) decode_tma_kernel(AttnArgs a,
+                                                                         const __grid_constant__ CUtensorMap tmC) {
+    constexpr int R = tma_slots<HD>();
+    constexpr int HALVES = HD / 64;
+    constexpr int KS = HD / 16, NB = HD / 8;
+    constexpr size_t SLOT = tma_slot_bytes<HD>();
+    constexpr size_t PLANE = SLOT / 2;          // bytes of the K (or V) tile
+    constexpr size_t HALF = kTmaTile * 128;     // bytes of one 64-dim half of a tile
+    extern __shared__ unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
+    __shared__ uint64_t full[R], empty[R];
+    __shared__ unsigned vmask[R];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int S = GMERGE ? a.gsplits : static_cast<int>(cluster.num_blocks());
+    const int rank = GMERGE ? static_cast<int>(blockIdx.x % a.gsplits) : static_cast<int>(cluster.block_rank());
+    const int64_t grp = blockIdx.x / S;
+    const int64_t b = grp / a.n_kv;
+    const int kvh = static_cast<int>(grp - b * a.n_kv);
+    const int G = a.group, BS = a.block_size;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int fg = lane >> 2, ft = lane & 3;
+    const unsigned FULL = 0xffffffffu;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < R; ++i) {
+            mbar_init(&full[i], 1);
+            mbar_init(&empty[i], 1);
+        }
+        mbar_init_fence();
+    }
+    {
+        // Before the dependency wait, hints only: this request's seq_len and this split's slice of
+        // the block table into L2 (the split is a static slice of the table's capacity).
+        const int64_t cap0 = a.max_blocks * BS;
+        const int64_t per0 = ((cap0 + S - 1) / S + kTmaTile - 1) / kTmaTile * kTmaTile;
+        const int64_t s0 = rank * per0, s1 = cap0 < s0 + per0 ? cap0 : s0 + per0;
+        if (warp == kTmaWarps && lane == 0) prefetch_lines(a.seq_lens + b, 4, 0, 1);
+        if (warp == kTmaWarps && s0 < s1)
+            prefetch_lines(a.table + b * a.max_blocks + s0 / BS, ((s1 - 1) / BS - s0 / BS + 1) * 4, lane, 32);
+    }
+    __syncthreads();  // the barriers are initialised
+    pdl_enter();
+    int64_t len = a.seq_lens[b];
+    const int64_t cap = a.max_blocks * BS;
+    if ((len < 0 || len > cap) && kvh == 0 && rank == 0 && threadIdx.x == 0 && a.err) atomicAdd(a.err, 1);
+    len = len < 0 ? 0 : (len > cap ? cap : len);
+    const int64_t per = ((cap + S - 1) / S + kTmaTile - 1) / kTmaTile * kTmaTile;
+    const int64_t t_begin = rank * per < cap ? rank * per : cap;
+    const int64_t t_lim = t_begin + per < cap ? t_begin + per : cap;
+    const int64_t t_end = len < t_begin ? t_begin : (len < t_lim ? len : t_lim);
+    const int64_t n_tiles = (t_end - t_begin + kTmaTile - 1) / kTmaTile;
+    const int bs_log2 = __ffs(BS) - 1;           // block_size is a power of two (8, 16 or 32)
+    const int RB = BS < kTmaTile ? BS : kTmaTile;  // cache rows per box
+    const int NBX = kTmaTile / RB;                // boxes (cache blocks) per tile: 1 or 2
+
+    float o[NB][2];
+#pragma unroll
+    for (int d = 0; d < NB; ++d) o[d][0] = o[d][1] = 0.0f;
+    float m = -INFINITY, l = 0.0f;
+    // A wait that gives up (counted in g_wait_timeouts) marks this thread: it waits no more, so a
+    // stalled copy costs one wait limit, not one per tile.
+    bool dead = false;
+    if (warp == kTmaWarps) {
+        const int32_t* table = a.table + b * a.max_blocks;
+        for (int64_t base = 0; base < n_tiles; base += 32) {
+            // lane i: the block ids of tile base + i (a second one for blocks of 8 tokens)
+            int32_t e0 = -1, e1 = -1;
+            if (base + lane < n_tiles) {
+                const int64_t t0 = t_begin + (base + lane) * kTmaTile;
+                e0 = table[t0 >> bs_log2];
+                if (NBX == 2 && t0 + RB < t_end) e1 = table[(t0 + RB) >> bs_log2];
+            }
+            const int cnt = n_tiles - base < 32 ? static_cast<int>(n_tiles - base) : 32;
+            for (int i = 0; i < cnt; ++i) {
+                const int32_t blk0 = __shfl_sync(FULL, e0, i), blk1 = __shfl_sync(FULL, e1, i);
+                if (lane == 0) {
+                    const int64_t u = base + i;
+                    const int slot = static_cast<int>(u % R);
+                    // the slot's previous tile (u - R) has been released by its warp
+                    if (u >= R && !dead) dead = !mbar_wait(&empty[slot], static_cast<uint32_t>(((u / R) - 1) & 1));
+                    const int64_t t0 = t_begin + u * kTmaTile;
+                    unsigned valid = 0;
+                    uint32_t bytes = 0;
+                    int32_t rows[2] = {-1, -1};
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        const int64_t tx = t0 + x * RB;  // first token of box x
+                        if (x >= NBX || tx >= t_end) break;
+                        const int32_t blk = x == 0 ? blk0 : blk1;
+                        if (blk < 0 || blk >= a.num_blocks) {
+                            // a bad block entry, counted once (kv head 0, the block's first token)
+                            if (kvh == 0 && (tx & (BS - 1)) == 0 && a.err) atomicAdd(a.err, 1);
+                            continue;
+                        }
+                        const int nv = t_end - tx < RB ? static_cast<int>(t_end - tx) : RB;
+                        valid |= ((1u << nv) - 1u) << (x * RB);
+                        bytes += static_cast<uint32_t>(2 * HALVES * RB * 128);
+                        rows[x] = static_cast<int32_t>((static_cast<int64_t>(blk) << bs_log2) + (tx & (BS - 1)));
+                    }
+                    vmask[slot] = valid;
+                    mbar_arrive_expect_tx(&full[slot], bytes);
+                    unsigned char* st = smem + static_cast<size_t>(slot) * SLOT;
+#pragma unroll
+                    for (int x = 0; x < 2; ++x) {
+                        if (rows[x] < 0) continue;
+#pragma unroll
+                        for (int plane = 0; plane < 2; ++plane)
+#pragma unroll
+                            for (int h = 0; h < HALVES; ++h)
+                                tma_load_4d(st + plane * PLANE + h * HALF + x * RB * 128, &tmC, h * 64, kvh, rows[x],
+                                            plane, &full[slot]);
+                    }
+                }
+                __syncwarp();
+            }
+        }
+    } else {
+        // Q as A fragments: rows = query heads (zero past G), columns = dims of k-step s
+        uint32_t qa[KS][2];
+        const T* qrow = static_cast<const T*>(a.q) + b * a.qs + static_cast<int64_t>(kvh * G + fg) * HD;
+#pragma unroll
+        for (int s2 = 0; s2 < KS; ++s2) {
+            qa[s2][0] = fg < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * s2 + 2 * ft) : 0u;
+            qa[s2][1] = fg < G ? *reinterpret_cast<const uint32_t*>(qrow + 16 * s2 + 8 + 2 * ft) : 0u;
+        }
+        // chunk c of token t's row: 64-dim half c / 8, its 16-byte chunk (c % 8) XOR t % 8 (the swizzle)
+        auto addr = [](int tok, int chunk) {
+            return (chunk >> 3) * (kTmaTile * 64) + tok * 64 + (((chunk & 7) ^ (tok & 7)) * 8);
+        };
+        for (int64_t u = warp; u < n_tiles; u += kTmaWarps) {
+            const int slot = static_cast<int>(u % R);
+            if (!dead) dead = !mbar_wait(&full[slot], static_cast<uint32_t>((u / R) & 1));
+            __syncwarp();
+            unsigned char* st = smem + static_cast<size_t>(slot) * SLOT;
+            const unsigned valid = vmask[slot];
+            if (valid != 0xffffu) {
+                // V rows of tokens that do not count hold stale bytes (never copied, or past the end
+                // of the request): zero them so that p = 0 meets 0, not whatever they hold
+                for (int c = lane; c < kTmaTile * HALVES * 8; c += 32) {
+                    const int r = c / (HALVES * 8), rest = c - r * (HALVES * 8);
+                    if (!((valid >> r) & 1u))
+                        *reinterpret_cast<uint4*>(st + PLANE + (rest >> 3) * HALF + r * 128 + (rest & 7) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async();  // before the copy engine refills the slot
+                __syncwarp();
+            }
+            tile_step<T, HD>(reinterpret_cast<const T*>(st), reinterpret_cast<const T*>(st + PLANE), valid, qa, o, m,
+                             l, a.scale_log2, lane, addr);
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[slot]);
+        }
+    }
+    finish_mma<T, HD, GMERGE, kTmaWarps>(a, smem, m, l, o, lane, warp, grp, b, kvh, S, rank, G, cluster);
+}
+
+template <typename T, int HD>
+cudaError_t launch_tma(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
+    // the cache as [HD][n_kv][num_blocks * block_size][2 planes], boxes of 64 dims x 1 head x up to 16 rows
+    const int BS = a.block_size;
+    const uint64_t dims[4] = {static_cast<uint64_t>(HD), static_cast<uint64_t>(a.n_kv),
+                              static_cast<uint64_t>(a.num_blocks) * BS, 2};
+    const uint64_t strides[3] = {static_cast<uint64_t>(HD) * 2, static_cast<uint64_t>(a.n_kv) * HD * 2,
+                                 static_cast<uint64_t>(a.num_blocks) * BS * a.n_kv * HD * 2};
+    const uint32_t box[4] = {64, 1, static_cast<uint32_t>(BS < kTmaTile ? BS : kTmaTile), 1};
+    CUtensorMap tm;
+    if (!encode_tmap_16_nd(&tm, a.cache, 4, dims, strides, box, std::is_same<T, __nv_bfloat16>::value, true))
+        return cudaErrorNotSupported;
+    const size_t smem = tma_smem(HD);
+    const dim3 block((kTmaWarps + 1) * 32);
+    if (a.gsplits > 0) {
+        auto kg = decode_tma_kernel<T, HD, true>;
+        const cudaError_t eg =
+            cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (eg != cudaSuccess) return eg;
+        return launch_kernel(kg, dim3(static_cast<unsigned>(a.B * a.n_kv * a.gsplits)), block, smem, s, p.pdl, 1, a,
+                             tm);
+    }
+    auto kernel = decode_tma_kernel<T, HD, false>;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int splits = p.splits;
+    if (splits > 8) {
+        // a 16-CTA cluster is a non-portable size: use it only where the device can place one
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+        int clusters = 0;
+        if (e == cudaSuccess) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = static_cast<unsigned>(splits);
+            attr.val.clusterDim.y = attr.val.clusterDim.z = 1;
+            cfg.gridDim = dim3(static_cast<unsigned>(splits));
+            cfg.blockDim = block;
+            cfg.dynamicSmemBytes = smem;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            e = cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg);
+        }
+        if (e != cudaSuccess || clusters < 1) {
+            cudaGetLastError();
+            splits = 8;
+        }
+    }
+    return launch_kernel(kernel, dim3(static_cast<unsigned>(a.B * a.n_kv * splits)), block, smem, s, p.pdl, splits,
+                         a, tm);
+}
+
 template <typename T, int HD, int STAGES>
 cudaError_t launch_hd(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
     auto kernel = decode_kernel<T, HD, STAGES>;
@@ -789,6 +1069,7 @@ cudaError_t launch_stages(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) 
 template <typename T>
 cudaError_t launch_typed(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
     if constexpr (sizeof(T) == 2) {
+        if (p.tma) return p.head_dim == 64 ? launch_tma<T, 64>(a, p, s) : launch_tma<T, 128>(a, p, s);
         if (p.tensor_cores) return p.head_dim == 64 ? launch_mma<T, 64>(a, p, s) : launch_mma<T, 128>(a, p, s);
     }
     return p.stages >= 4 ? launch_stages<T, 4>(a, p, s) : launch_stages<T, 2>(a, p, s);
@@ -797,6 +1078,7 @@ cudaError_t launch_typed(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
 }  // namespace attn
 
 size_t decode_attention_mma_smem(int head_dim) { return attn::mma_smem(head_dim); }
+size_t decode_attention_tma_smem(int head_dim) { return attn::tma_smem(head_dim); }
 
 size_t decode_attention_smem(int group, int head_dim, int block_size, int stages, int es) {
     return attn::layout(group, head_dim, block_size, stages, es).total;

@@ -1062,31 +1062,50 @@ cudaError_t launch_simple_typed(const LinArgs& a, const LinPlan& p, cudaStream_t
 
 }  // namespace lin
 
-bool encode_tmap_16(CUtensorMap* map, const void* base, int rank, uint64_t dim0, uint64_t dim1, uint64_t stride1,
-                    uint32_t box0, uint32_t box1, bool bf16, bool swizzle128) {
-    using Encode = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-    static const Encode encode = [] {
+namespace {
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeFn encoder() {
+    static const EncodeFn encode = [] {
         void* fn = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
                 cudaSuccess ||
             q != cudaDriverEntryPointSuccess) {
             cudaGetLastError();
-            return static_cast<Encode>(nullptr);
+            return static_cast<EncodeFn>(nullptr);
         }
-        return reinterpret_cast<Encode>(fn);
+        return reinterpret_cast<EncodeFn>(fn);
     }();
-    if (!encode || rank < 1 || rank > 2) return false;
-    const cuuint64_t dims[2] = {dim0, dim1};
-    const cuuint64_t strides[1] = {stride1};
-    const cuuint32_t box[2] = {box0, box1};
-    const cuuint32_t estr[2] = {1, 1};
+    return encode;
+}
+}  // namespace
+
+bool encode_tmap_16_nd(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                       const uint32_t* box, bool bf16, bool swizzle128) {
+    const EncodeFn encode = encoder();
+    if (!encode || rank < 1 || rank > 4) return false;
+    cuuint64_t d[4], st[3];
+    cuuint32_t bx[4], estr[4];
+    for (int i = 0; i < rank; ++i) {
+        d[i] = dims[i];
+        bx[i] = box[i];
+        estr[i] = 1;
+        if (i + 1 < rank) st[i] = strides[i];
+    }
     return encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
-                  static_cast<cuuint32_t>(rank), const_cast<void*>(base), dims, strides, box, estr,
+                  static_cast<cuuint32_t>(rank), const_cast<void*>(base), d, st, bx, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_tmap_16(CUtensorMap* map, const void* base, int rank, uint64_t dim0, uint64_t dim1, uint64_t stride1,
+                    uint32_t box0, uint32_t box1, bool bf16, bool swizzle128) {
+    if (rank < 1 || rank > 2) return false;
+    const uint64_t dims[2] = {dim0, dim1}, strides[1] = {stride1};
+    const uint32_t box[2] = {box0, box1};
+    return encode_tmap_16_nd(map, base, rank, dims, strides, box, bf16, swizzle128);
 }
 
 namespace lin {

@@ -85,6 +85,22 @@ __device__ __forceinline__ void tma_load_1d(void* dst, const CUtensorMap* map, i
         : "memory");
 }
 
+// Copy the box at element coordinates (c0, c1, c2, c3) of a 4-D tensor map into shared memory.
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, "
+        "%5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
+        : "memory");
+}
+
+// Host: encode a tensor map of 16-bit elements of rank 1-4: dims[i] elements along dimension i
+// (0 innermost), strides[i] bytes between consecutive indices of dimension i + 1, box[i] elements
+// per copy. 128-byte swizzle or none. Returns false when the driver rejects the description.
+bool encode_tmap_16_nd(CUtensorMap* map, const void* base, int rank, const uint64_t* dims, const uint64_t* strides,
+                       const uint32_t* box, bool bf16, bool swizzle128);
+
 // Host: encode a tensor map of 16-bit elements. rank 1: {dim0}, box {box0}; rank 2: {dim0, dim1}
 // with row stride `stride1` bytes, box {box0, box1}. Returns false (nothing encoded) when the
 // driver entry point is missing or the driver rejects the description.

@@ -322,8 +322,8 @@ def test_variant_control(L):
     assert sra.variant_count("rope_kv_store") == 2
     assert sra.variant_count("glu") == 2
     assert [sra.variant_name("glu", i) for i in range(2)] == ["cols_rows", "cols_rows_regs"]
-    assert sra.variant_count("decode_attention") == 2
-    assert [sra.variant_name("decode_attention", i) for i in range(2)] == ["cuda_cores", "mma_sync"]
+    assert sra.variant_count("decode_attention") == 3
+    assert [sra.variant_name("decode_attention", i) for i in range(3)] == ["cuda_cores", "mma_sync", "mma_sync_tma"]
     assert sra.variant_count("linear") == 2
     assert [sra.variant_name("linear", i) for i in range(2)] == ["mma_sync", "tcgen05"]
     assert L.sra_force_variant(b"linear", 1 | (4 << 8)) == OK   # tcgen05 with 4 K splits

@@ -89,10 +89,19 @@ def test_config_qwen25_long_context():
     assert_attention_close(got, want, cache, table, seq, "B=1 ctx=32768")
 
 
-@pytest.fixture(params=["auto", "cuda_cores"])
+VARIANT = {"auto": -1, "cuda_cores": 0, "mma_sync": 1, "mma_sync_tma": 2}
+
+
+def tensor_core_shape(dtype, hd):
+    """The shapes the two tensor-core kernels serve: 16-bit data, head_dim 64 or 128."""
+    return dtype != torch.float32 and hd in (64, 128)
+
+
+@pytest.fixture(params=["auto", "cuda_cores", "mma_sync_tma"])
 def attn_variant(request):
-    """Run under the automatic choice and with the CUDA-core kernel forced."""
-    sra.force_variant("decode_attention", -1 if request.param == "auto" else 0)
+    """Run under the automatic choice, with the CUDA-core kernel forced, and with the
+    TMA-fed tensor-core kernel forced."""
+    sra.force_variant("decode_attention", VARIANT[request.param])
     yield request.param
     sra.force_variant("decode_attention", -1)
 
@@ -102,6 +111,8 @@ def attn_variant(request):
 @pytest.mark.parametrize("n_head,n_kv", [(8, 8), (8, 4), (12, 2), (32, 4), (8, 1)])
 @pytest.mark.parametrize("bs", [8, 16, 32])
 def test_shapes_dtypes(dtype, hd, n_head, n_kv, bs, attn_variant):
+    if attn_variant == "mma_sync_tma" and not tensor_core_shape(dtype, hd):
+        pytest.skip("the TMA-fed kernel serves 16-bit data with head_dim 64 or 128")
     lens = [1, 5, bs, bs + 1, 3 * bs - 1, 200]
     q, cache, table, seq = syn.attention_inputs(6, lens, n_head, n_kv, hd, bs, 6 * (200 // bs + 2), dtype,
                                                 1015 + hd + bs)
@@ -121,12 +132,56 @@ def test_cuda_core_kernel_on_the_configs(B, ctx):
         sra.force_variant("decode_attention", -1)
 
 
-def test_forcing_the_mma_kernel_where_it_cannot_run():
+@pytest.mark.parametrize("variant", ["mma_sync", "mma_sync_tma"])
+@pytest.mark.parametrize("B,ctx,splits", [(1, 32768, 0), (32, 1024, 0), (3, 4097, 0), (64, 1024, 0), (2, 1000, 1),
+                                          (2, 1000, 2), (2, 1000, 4), (2, 1000, 8), (2, 1000, 16), (1, 300, 16)])
+def test_tensor_core_kernels_on_the_configs(variant, B, ctx, splits):
+    """Both tensor-core kernels, the planner's splits and every cluster size forced (splits
+    past the request's tiles hold no tokens and merge as empty partials)."""
+    sra.force_variant("decode_attention", VARIANT[variant] | (splits << 8))
+    try:
+        q, cache, table, seq = syn.attention_inputs(B, ctx, 12, 2, 128, 16, max(64, B * (ctx // 16 + 1)),
+                                                    torch.bfloat16, 1028)
+        before = sra.wait_timeouts()
+        got, want = run_both(q, cache, table, seq, expect_err=0)
+        assert sra.wait_timeouts() == before   # no copy wait gave up
+        assert_attention_close(got, want, cache, table, seq, f"{variant} B={B} ctx={ctx} splits={splits}")
+    finally:
+        sra.force_variant("decode_attention", -1)
+
+
+@pytest.mark.parametrize("variant", ["mma_sync", "mma_sync_tma"])
+@pytest.mark.parametrize("bs", [8, 16, 32])
+def test_tensor_core_kernels_mixed_lengths_and_bad_blocks(variant, bs):
+    """Batch 64 with lengths 1..1024 and a few bad table entries (a block of 8 tokens puts two
+    cache blocks in one 16-token tile; one of 32 spans two tiles)."""
+    lens = syn.rng(1029, bs).integers(1, 1025, size=64)
+    mb = 1024 // bs
+    q, cache, table, seq = syn.attention_inputs(64, lens, 12, 2, 128, bs, 64 * mb + 8, torch.bfloat16, 1029,
+                                                max_blocks=mb)
+    bad = 0
+    for b, j, v in ((0, 0, -1), (5, 1, 64 * mb + 8), (9, 3, 1 << 30), (63, 2, -7)):
+        if (j * bs) < int(seq[b]):
+            bad += 1
+        table[b, j] = v
+    sra.force_variant("decode_attention", VARIANT[variant])
+    try:
+        got, want = run_both(q, cache, table, seq, expect_err=bad)
+        assert_attention_close(got, want, cache, table, seq, f"{variant} mixed bs={bs}")
+    finally:
+        sra.force_variant("decode_attention", -1)
+
+
+@pytest.mark.parametrize("variant", ["mma_sync", "mma_sync_tma"])
+def test_forcing_a_tensor_core_kernel_where_it_cannot_run(variant):
     q, cache, table, seq = syn.attention_inputs(2, 40, 8, 2, 256, 16, 16, torch.bfloat16, 1021)
-    sra.force_variant("decode_attention", 1)
+    sra.force_variant("decode_attention", VARIANT[variant])
     try:
         with pytest.raises(sra.SRAError):
             sra.paged_decode_attention(q.to(DEV), cache.to(DEV), table.to(DEV), seq.to(DEV))
+        q32, c32, t32, s32 = syn.attention_inputs(2, 40, 8, 2, 128, 16, 16, torch.float32, 1021)
+        with pytest.raises(sra.SRAError):
+            sra.paged_decode_attention(q32.to(DEV), c32.to(DEV), t32.to(DEV), s32.to(DEV))
     finally:
         sra.force_variant("decode_attention", -1)
 
@@ -197,11 +252,20 @@ def test_reads_what_rope_kv_store_wrote():
 
 
 # ----------------------------------------------- global split through a workspace
+@pytest.mark.parametrize("variant", ["auto", "mma_sync_tma"])
 @pytest.mark.parametrize("B,ctx,n_head,n_kv,hd", [(1, 32768, 12, 2, 128), (2, 16384, 8, 1, 64), (1, 12000, 32, 4, 128),
                                                   (3, 9000, 12, 2, 128)])
-def test_workspace_split_matches_the_oracle_twice(B, ctx, n_head, n_kv, hd):
+def test_workspace_split_matches_the_oracle_twice(B, ctx, n_head, n_kv, hd, variant):
     """Long contexts over few (request, kv head) pairs take the workspace path; two calls in a
     row give the same bytes (the kernel leaves the workspace ready for the next call)."""
+    sra.force_variant("decode_attention", VARIANT[variant])
+    try:
+        _workspace_case(B, ctx, n_head, n_kv, hd)
+    finally:
+        sra.force_variant("decode_attention", -1)
+
+
+def _workspace_case(B, ctx, n_head, n_kv, hd):
     nb = B * ((ctx + 15) // 16) + 8
     q, cache, table, seq = syn.attention_inputs(B, ctx, n_head, n_kv, hd, 16, nb, torch.bfloat16, 1022 + B)
     seq[0] = ctx - 7 if B > 1 else seq[0]
