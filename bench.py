@@ -1049,7 +1049,8 @@ def run_sweep(args):
                 nvs = (1, 2, 3, 4, 6, 8, 12, 16) if nm == "warp_rows" else (1, 2, 3, 4, 6, 8)
                 settings += [(v | (nv << 8), f"{nm}/nv{nv}") for nv in nvs]
             elif nm == "tcgen05":
-                settings += [(v, nm)] + [(v | (sk << 8), f"{nm}/splits{sk}") for sk in (2, 4, 6, 8, 12, 16)]
+                settings += [(v, nm)] + [(v | (sk << 8) | (st << 16), f"{nm}/splits{sk}/stages{st}")
+                                         for st in (4, 8) for sk in (4, 6, 8, 10, 12, 16)]
             elif op == "decode_attention" and nm != "cuda_cores":
                 settings += [(v, nm)] + [(v | (sk << 8), f"{nm}/splits{sk}") for sk in (1, 2, 4, 8, 16)]
             elif nm == "warps_row":

@@ -502,7 +502,8 @@ SRA_API int sra_set_pdl(int enable);
  * s in 1, 2, 4, 8, 16, it also forces the CTAs per (request, kv head)), "linear" (the
  * projection of the _ws entry points once the prologue has run: 0 = mma.sync
  * kernels, 1 = the tcgen05 kernel, for up to 64 rows and N a multiple of 128;
- * OR-ed with (s << 8), s in 1..16, it also forces the tcgen05 kernel's K splits).
+ * OR-ed with (s << 8), s in 1..16, it also forces the tcgen05 kernel's K splits, and
+ * with (r << 16), r = 4 or 8, its ring depth in stages).
  * variant: -1 = automatic per-shape choice (the default); otherwise an index
  * < sra_variant_count(op), optionally OR-ed with (nv << 8) to also force the
  * number of 16-byte accesses each thread holds in the register variants of

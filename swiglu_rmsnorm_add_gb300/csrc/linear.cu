@@ -29,6 +29,8 @@
 // ldmatrix from swizzled shared memory).
 #include <cooperative_groups.h>
 
+#include <atomic>
+#include <mutex>
 #include <type_traits>
 
 #include "common.cuh"
@@ -561,19 +563,19 @@ __global__ void __launch_bounds__((warps_for(MT) + 1) * 32) linear_h_kernel(LinA
 // core reads the staged tiles itself.
 constexpr int kTcM = 128;    // output columns of y per CTA: the MMA's M
 constexpr int kTcN = 64;     // rows of h (at most): the MMA's N
-constexpr int kTcStages = 4;  // 97 KB of shared memory: two CTAs per SM
+// Ring depth: 4 stages (97 KB of shared memory, two CTAs per SM) or 8 (193 KB, one CTA per SM
+// with about twice the bytes in flight).
 __host__ __device__ constexpr size_t tc_wtile_bytes() { return static_cast<size_t>(kTcM) * kKT * 2; }
 __host__ __device__ constexpr size_t tc_htile_bytes() { return static_cast<size_t>(kTcN) * kKT * 2; }
-__host__ __device__ constexpr size_t tc_smem_bytes() {
-    return 1024 + (kTcStages * (tc_wtile_bytes() + tc_htile_bytes()) > static_cast<size_t>(kTcN) * kTcM * 4
-                       ? kTcStages * (tc_wtile_bytes() + tc_htile_bytes())
+__host__ __device__ constexpr size_t tc_smem_bytes(int stages) {
+    return 1024 + (stages * (tc_wtile_bytes() + tc_htile_bytes()) > static_cast<size_t>(kTcN) * kTcM * 4
+                       ? stages * (tc_wtile_bytes() + tc_htile_bytes())
                        : static_cast<size_t>(kTcN) * kTcM * 4);
 }
 
-template <typename T>
+template <typename T, int S>
 __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_constant__ CUtensorMap tmW,
                                                         const __grid_constant__ CUtensorMap tmX) {
-    constexpr int S = kTcStages;
     constexpr size_t SB = tc_wtile_bytes() + tc_htile_bytes();
     constexpr uint32_t kCols = 64;  // tensor-memory columns: one fp32 accumulator column per row of h
     constexpr uint32_t IDESC = tc::idesc_f16(std::is_same<T, __nv_bfloat16>::value, kTcM, kTcN);
@@ -903,7 +905,7 @@ cudaError_t launch_h_mt(const LinArgs& a, const LinPlan& p, cudaStream_t s, cons
     return launch_kernel(kernel, grid, dim3((warps_for(MT) + 1) * 32), smem, s, p.pdl, p.splits, a, tmW, tmX);
 }
 
-template <typename T>
+template <typename T, int STAGES>
 cudaError_t launch_tc(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
     // W [N][K] in [128][64] boxes and h [B][K] in [64][64] boxes, both with the 128-byte swizzle
     const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
@@ -911,8 +913,8 @@ cudaError_t launch_tc(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
     if (!encode_tmap_16(&tmW, a.W, 2, a.K, a.N, a.K * 2, kKT, kTcM, bf16, true) ||
         !encode_tmap_16(&tmX, a.x, 2, a.K, a.B, a.xs * 2, kKT, kTcN, bf16, true))
         return cudaErrorNotSupported;
-    auto kernel = linear_tc_kernel<T>;
-    const size_t smem = tc_smem_bytes();
+    auto kernel = linear_tc_kernel<T, STAGES>;
+    const size_t smem = tc_smem_bytes(STAGES);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int splits = p.splits;
@@ -972,7 +974,10 @@ cudaError_t launch_pro(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
 
 template <typename T>
 cudaError_t launch_typed(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
-    if (p.tcgen05) return p.prologue == 3 ? launch_tc<T>(a, p, s) : cudaErrorInvalidValue;
+    if (p.tcgen05) {
+        if (p.prologue != 3) return cudaErrorInvalidValue;
+        return p.tc_stages == 8 ? launch_tc<T, 8>(a, p, s) : launch_tc<T, 4>(a, p, s);
+    }
     if (p.narrow) {
         switch (p.prologue) {
             case 0: return launch16<T, 0>(a, p, s);
@@ -1140,7 +1145,56 @@ size_t linear_smem(int mt, int prologue) {
     return prologue == 3 ? lin::smemh_bytes(mt) : lin::smem_bytes(mt, prologue);
 }
 size_t linear16_smem(int rows, int64_t K) { return lin::smem16_bytes(rows, K); }
-size_t linear_tc_smem() { return lin::tc_smem_bytes(); }
+size_t linear_tc_smem(int stages) { return lin::tc_smem_bytes(stages); }
+
+// Clusters of `splits` CTAs of the tcgen05 projection (ring of `stages`) the device can hold at once.
+int linear_tc_max_clusters(int splits, int stages, bool bf16) {
+    // answers kept per (device, dtype, ring depth, cluster size): the query sets kernel attributes
+    static std::atomic<int> memo[16][2][2][17];
+    static std::once_flag once;
+    std::call_once(once, [] {
+        for (auto& a : memo)
+            for (auto& b : a)
+                for (auto& c : b)
+                    for (auto& d : c) d.store(-1);
+    });
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (splits < 1 || splits > 16) return 0;
+    std::atomic<int>* slot = dev >= 0 && dev < 16 ? &memo[dev][bf16 ? 1 : 0][stages == 8 ? 1 : 0][splits] : nullptr;
+    if (slot && slot->load() >= 0) return slot->load();
+    const size_t smem = lin::tc_smem_bytes(stages);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = static_cast<unsigned>(splits);
+    attr.val.clusterDim.y = attr.val.clusterDim.z = 1;
+    cfg.gridDim = dim3(static_cast<unsigned>(splits));
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = smem;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    auto query = [&](auto kernel) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+                cudaSuccess ||
+            (splits > 8 && cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                               cudaSuccess) ||
+            cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+    };
+    if (stages == 8)
+        bf16 ? query(lin::linear_tc_kernel<__nv_bfloat16, 8>) : query(lin::linear_tc_kernel<__half, 8>);
+    else
+        bf16 ? query(lin::linear_tc_kernel<__nv_bfloat16, 4>) : query(lin::linear_tc_kernel<__half, 4>);
+    if (slot) slot->store(n);
+    return n;
+}
 
 cudaError_t launch_linear(const LinArgs& a, const LinPlan& p, int dtype, cudaStream_t s) {
     if (!p.tensor_cores) {

@@ -219,11 +219,12 @@ def test_norm_rows_beyond_the_fp32_sum_range(eps, dtype, B, K, N, ws):
     assert_linear_close(got, want, h, W, f"norm range {dtype} B={B} K={K} eps={eps} ws={ws}")
 
 
-def _tc_case(prologue, dtype, B, K, N, seed):
-    """The workspace path with its projection forced onto the tcgen05 kernel."""
+def _tc_case(prologue, dtype, B, K, N, seed, force=1):
+    """The workspace path with its projection forced onto the tcgen05 kernel (`force`: the
+    variant word, K splits and ring depth included)."""
     W = syn.linear_weight(N, K, dtype, seed)
     wsp = sra.linear_workspace(B, K, dtype, DEV)
-    sra.force_variant("linear", 1)
+    sra.force_variant("linear", force)
     try:
         if prologue == "rmsnorm":
             x = syn.normal((B, K), 0, 1, dtype, seed, 1)
@@ -261,6 +262,25 @@ def test_tcgen05_projection(dtype, prologue, B, K, N):
     torch.cuda.synchronize()
     assert sra.wait_timeouts() == before
     assert_linear_close(got, want, h, W, f"tcgen05 {prologue} {dtype} B={B} K={K} N={N}")
+
+
+@pytest.mark.parametrize("stages", [4, 8])
+@pytest.mark.parametrize("splits", [1, 3, 5, 12, 16])
+@pytest.mark.parametrize("prologue,B,K,N", [("silu", 64, 8960, 1536), ("rmsnorm", 33, 1280, 256)])
+def test_tcgen05_ring_depth_and_splits(prologue, B, K, N, splits, stages):
+    """Both ring depths of the tcgen05 projection and K splits that are not powers of two
+    (clusters of 3, 5 and 12 CTAs; 16 is a non-portable size) against the oracle."""
+    before = sra.wait_timeouts()
+    try:
+        got, want, h, W = _tc_case(prologue, torch.bfloat16, B, K, N, 1062 + splits,
+                                   force=1 | (splits << 8) | (stages << 16))
+    except sra.SRAError:
+        if splits <= 8:
+            raise
+        pytest.skip(f"the device cannot place a {splits}-CTA cluster with a {stages}-stage ring")
+    torch.cuda.synchronize()
+    assert sra.wait_timeouts() == before
+    assert_linear_close(got, want, h, W, f"tcgen05 {prologue} splits={splits} stages={stages}")
 
 
 def test_tcgen05_forced_where_it_cannot_serve():
