@@ -1053,6 +1053,9 @@ def run_sweep(args):
                                          for st in (4, 8) for sk in (4, 6, 8, 10, 12, 16)]
             elif op == "decode_attention" and nm != "cuda_cores":
                 settings += [(v, nm)] + [(v | (sk << 8), f"{nm}/splits{sk}") for sk in (1, 2, 4, 8, 16)]
+                if nm == "mma_sync":   # 4-warp CTAs, two per SM
+                    settings += [(v | (4 << 16) | (sk << 8), f"{nm}/w4" + (f"/splits{sk}" if sk else ""))
+                                 for sk in (0, 1, 2, 4, 8, 16)]
             elif nm == "warps_row":
                 settings += [(v | (nv << 8) | (g << 16), f"{nm}/g{g}nv{nv}") for g in (2, 4, 8) for nv in (8, 16)]
             else:

@@ -499,7 +499,8 @@ SRA_API int sra_set_pdl(int enable);
  * picks), "decode_attention" (0 = CUDA-core kernel,
  * 1 = mma.sync kernel for bf16 / fp16 with head_dim 64 or 128, 2 = the same
  * contraction with the K / V tiles moved by TMA; for 1 and 2, OR-ed with (s << 8),
- * s in 1, 2, 4, 8, 16, it also forces the CTAs per (request, kv head)), "linear" (the
+ * s in 1, 2, 4, 8, 16, it also forces the CTAs per (request, kv head), and for 1,
+ * OR-ed with (4 << 16), it runs 4-warp CTAs, two per SM), "linear" (the
  * projection of the _ws entry points once the prologue has run: 0 = mma.sync
  * kernels, 1 = the tcgen05 kernel, for up to 64 rows and N a multiple of 128;
  * OR-ed with (s << 8), s in 1..16, it also forces the tcgen05 kernel's K splits, and

@@ -856,7 +856,7 @@ static int attention_impl(const void* q, const void* kv_cache, const int32_t* bl
     plan.tensor_cores = dtype != DT_F32 && (head_dim == 64 || head_dim == 128) &&
                         (reinterpret_cast<uintptr_t>(q) & 3u) == 0 && q_tok_stride % 2 == 0 &&
                         num_blocks * block_size < (int64_t(1) << 31) &&
-                        static_cast<int64_t>(decode_attention_mma_smem(head_dim)) <= limit;
+                        static_cast<int64_t>(decode_attention_mma_smem(head_dim, 8)) <= limit;
     const int forced_all = g_force_attn.load(std::memory_order_relaxed);
     const int forced = forced_all < 0 ? -1 : (forced_all & 0xFF);  // variant; bits 8-15: splits (A/B only)
     if ((forced == 1 || forced == 2) && !plan.tensor_cores) return SRA_ERR_VARIANT;
@@ -865,12 +865,20 @@ static int attention_impl(const void* q, const void* kv_cache, const int32_t* bl
     // 64 and 128), its ring in one CTA's shared memory
     plan.tma = forced == 2;
     if (plan.tma && static_cast<int64_t>(decode_attention_tma_smem(head_dim)) > limit) return SRA_ERR_VARIANT;
+    // mma.sync kernel: 8 warps per CTA (one CTA per SM) unless forced to 4 (two per SM)
+    const int forced_warps = forced_all < 0 ? 0 : (forced_all >> 16) & 0xFF;
+    if (forced_warps) {
+        if ((forced_warps != 4 && forced_warps != 8) || forced != 1) return SRA_ERR_VARIANT;
+        plan.mma_warps = forced_warps;
+    }
     int splits = 1;
     if (plan.tensor_cores) {
-        // one 8-warp CTA per SM at most (its K/V rings fill the SM's shared memory), and at
-        // least 256 tokens (two 16-token tiles per warp) per split
-        while (splits < 16 && groups * splits * 2 <= static_cast<int64_t>(sms) &&
-               max_blocks_per_seq * block_size >= 256 * static_cast<int64_t>(splits) * 2)
+        // as many CTAs as the SMs hold at once (the K/V rings fill an SM's shared memory with one
+        // 8-warp CTA or two 4-warp ones), and at least two 16-token tiles per warp per split
+        const int64_t per_sm = plan.mma_warps == 4 ? 2 : 1;
+        const int64_t min_tok = 32 * static_cast<int64_t>(plan.mma_warps);
+        while (splits < 16 && groups * splits * 2 <= per_sm * sms &&
+               max_blocks_per_seq * block_size >= min_tok * splits * 2)
             splits *= 2;
     } else {
         while (splits < 8 && groups * splits < 2 * static_cast<int64_t>(sms) && max_blocks_per_seq >= 4 * splits)
@@ -885,7 +893,7 @@ static int attention_impl(const void* q, const void* kv_cache, const int32_t* bl
     plan.stages = 4;
     if (static_cast<int64_t>(decode_attention_smem(group, head_dim, block_size, 4, es)) > limit) plan.stages = 2;
     plan.smem = plan.tma            ? decode_attention_tma_smem(head_dim)
-                : plan.tensor_cores ? decode_attention_mma_smem(head_dim)
+                : plan.tensor_cores ? decode_attention_mma_smem(head_dim, plan.mma_warps)
                                     : decode_attention_smem(group, head_dim, block_size, plan.stages, es);
     if (static_cast<int64_t>(plan.smem) > limit) return SRA_ERR_SHAPE;
     AttnArgs a;

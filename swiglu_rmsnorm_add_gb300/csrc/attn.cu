@@ -427,17 +427,20 @@ __device__ __forceinline__ void tile_step(const T* Ks, const T* Vs, unsigned val
     }
 }
 
-constexpr int kMmaWarps = 8;
 constexpr int kMmaTile = 16;    // tokens per warp tile
 constexpr int kMmaStages = 3;   // tiles per warp ring
 
-__host__ __device__ inline size_t mma_ring_bytes(int HD) {
-    const size_t ring = static_cast<size_t>(kMmaWarps) * kMmaStages * 2 * kMmaTile * HD * 2;
-    const size_t merge = (static_cast<size_t>(kMmaWarps) * 8 * (HD + 2) + 8 * (HD + 2)) * 4;
-    return ring > merge ? ring : merge;
+// Shared memory of an NW-warp CTA: the warps' rings, over which the merges later run (the
+// warps' partials; with a workspace split, the last CTA's merge buffers), then the row masks.
+__host__ __device__ inline size_t mma_ring_bytes(int HD, int NW) {
+    const size_t ring = static_cast<size_t>(NW) * kMmaStages * 2 * kMmaTile * HD * 2;
+    const size_t merge = (static_cast<size_t>(NW) * 8 * (HD + 2) + 8 * (HD + 2)) * 4;
+    const size_t gmerge = static_cast<size_t>(kMaxGsplits) * 24 * 4 + 64 + 16 * 8 * static_cast<size_t>(HD) * 4;
+    size_t need = ring > merge ? ring : merge;
+    return need > gmerge ? need : gmerge;
 }
-__host__ __device__ inline size_t mma_smem(int HD) {
-    return mma_ring_bytes(HD) + static_cast<size_t>(kMmaWarps) * kMmaStages * 4;  // + per-slot row masks
+__host__ __device__ inline size_t mma_smem(int HD, int NW) {
+    return mma_ring_bytes(HD, NW) + static_cast<size_t>(NW) * kMmaStages * 4;  // + per-slot row masks
 }
 
 // The end of a (request, kv head, split) CTA of the tensor-core kernels: the warps' (m, l, O)
@@ -523,9 +526,9 @@ __device__ __forceinline__ void finish_mma(const AttnArgs& a, unsigned char* sme
         for (int i = threadIdx.x; i < S * 4; i += blockDim.x)
             reinterpret_cast<float4*>(hm)[i] = __ldcg(reinterpret_cast<const float4*>(parts + (i >> 2) * PS) + (i & 3));
         __syncthreads();
-        // warp gg: M over the splits, the weights 2^(m_r - M) and the denominator
-        if (warp < G) {
-            const int gg = warp;
+        // warp w, query heads gg = w, w + warps, ...: M over the splits, the weights 2^(m_r - M)
+        // and the denominator
+        for (int gg = warp; gg < G; gg += static_cast<int>(blockDim.x >> 5)) {
             float M = -INFINITY;
             for (int r = lane; r < S; r += 32) M = fmaxf(M, hm[r * 16 + gg]);
             for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
@@ -594,8 +597,10 @@ __device__ __forceinline__ void finish_mma(const AttnArgs& a, unsigned char* sme
 // than a cluster holds): each writes its (max, sum, partial output) to the workspace, and the
 // CTA that finishes last (an atomic count per (request, kv head)) merges them and resets the
 // count to zero for the next call.
-template <typename T, int HD, bool GMERGE>
-__global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) {
+// NW warps per CTA: 8 (one CTA per SM) or 4 (two CTAs per SM, so a CTA of the next launch can
+// start beside one of this launch).
+template <typename T, int HD, bool GMERGE, int NW>
+__global__ void __launch_bounds__(NW * 32, NW == 4 ? 2 : 1) decode_mma_kernel(AttnArgs a) {
     constexpr int CPR = HD * 2 / 16;      // 16-byte chunks per row
     constexpr int KS = HD / 16;           // k-steps of Q K^T
     constexpr int NB = HD / 8;            // 8-dim blocks of O
@@ -624,13 +629,13 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
         const int64_t per0 = ((cap0 + S - 1) / S + kMmaTile - 1) / kMmaTile * kMmaTile;
         const int64_t s0 = rank * per0, s1 = cap0 < s0 + per0 ? cap0 : s0 + per0;
         if (warp == 0 && lane == 0) prefetch_lines(a.seq_lens + b, 4, 0, 1);
-        if (warp == kMmaWarps - 1 && s0 < s1)
+        if (warp == NW - 1 && s0 < s1)
             prefetch_lines(a.table + b * a.max_blocks + s0 / BS, ((s1 - 1) / BS - s0 / BS + 1) * 4, lane, 32);
         int blk[2] = {-1, -1};
         int64_t tok[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-            tok[j] = s0 + (warp + j * kMmaWarps) * kMmaTile + (lane & (kMmaTile - 1));
+            tok[j] = s0 + (warp + j * NW) * kMmaTile + (lane & (kMmaTile - 1));
             if (tok[j] < s1)
                 asm volatile("ld.relaxed.gpu.global.b32 %0, [%1];"
                              : "=r"(blk[j])
@@ -664,7 +669,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
     // the first tiles' block ids and seq_len are requested together: one round trip, not two
     int32_t blk0[kMmaStages];
 #pragma unroll
-    for (int k = 0; k < kMmaStages; ++k) blk0[k] = load_blk(warp + static_cast<int64_t>(k) * kMmaWarps);
+    for (int k = 0; k < kMmaStages; ++k) blk0[k] = load_blk(warp + static_cast<int64_t>(k) * NW);
     int64_t len = a.seq_lens[b];
     if ((len < 0 || len > cap) && kvh == 0 && rank == 0 && threadIdx.x == 0 && a.err) atomicAdd(a.err, 1);
     len = len < 0 ? 0 : (len > cap ? cap : len);
@@ -675,7 +680,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
     const T* cache = static_cast<const T*>(a.cache);
     const int64_t n_tiles = (t_end - t_begin + kMmaTile - 1) / kMmaTile;
     const int64_t n_static = (t_lim - t_begin + kMmaTile - 1) / kMmaTile;
-    unsigned* vmask = reinterpret_cast<unsigned*>(smem + mma_ring_bytes(HD)) + warp * kMmaStages;
+    unsigned* vmask = reinterpret_cast<unsigned*>(smem + mma_ring_bytes(HD, NW)) + warp * kMmaStages;
     const unsigned FULL = 0xffffffffu;
     // This warp's tile u into ring slot (u / warps) % stages: lane r < 16 finds token r's row
     // once; the 16-byte copies then go row by row, LPR lanes per row (contiguous), and each
@@ -695,7 +700,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
             dst_off[i][cc] = r * HD + ((ch ^ (r & 7)) * 8);
         }
     auto issue = [&](int64_t u, int32_t blk) {
-        const int slot = static_cast<int>((u / kMmaWarps) % kMmaStages);
+        const int slot = static_cast<int>((u / NW) % kMmaStages);
         T* dst = ring + static_cast<size_t>(slot) * 2 * TE;
         int64_t off = -1;  // element offset of token `lane`'s K row in the cache, -1: no row
         if (lane < kMmaTile) {
@@ -725,7 +730,7 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
     };
 #pragma unroll
     for (int k = 0; k < kMmaStages - 1; ++k) {
-        const int64_t u = warp + static_cast<int64_t>(k) * kMmaWarps;
+        const int64_t u = warp + static_cast<int64_t>(k) * NW;
         if (u < n_static) issue(u, blk0[k]);
         cp_async_commit();
     }
@@ -746,12 +751,12 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
 #pragma unroll
     for (int d = 0; d < NB; ++d) o[d][0] = o[d][1] = 0.0f;
     float m = -INFINITY, l = 0.0f;
-    for (int64_t u = warp, k = 0; u < n_tiles; u += kMmaWarps, ++k) {
+    for (int64_t u = warp, k = 0; u < n_tiles; u += NW, ++k) {
         cp_async_wait<kMmaStages - 2>();
         __syncwarp();
-        if (u + (kMmaStages - 1) * kMmaWarps < n_tiles) {
-            issue(u + (kMmaStages - 1) * kMmaWarps, blk_next);
-            blk_next = load_blk(u + kMmaStages * kMmaWarps);
+        if (u + (kMmaStages - 1) * NW < n_tiles) {
+            issue(u + (kMmaStages - 1) * NW, blk_next);
+            blk_next = load_blk(u + kMmaStages * NW);
         }
         cp_async_commit();
         const T* Ks = ring + static_cast<size_t>(k % kMmaStages) * 2 * TE;
@@ -762,21 +767,21 @@ __global__ void __launch_bounds__(kMmaWarps * 32) decode_mma_kernel(AttnArgs a) 
                          [](int tok, int chunk) { return tok * HD + ((chunk ^ (tok & 7)) * 8); });
     }
     cp_async_wait<0>();
-    finish_mma<T, HD, GMERGE, kMmaWarps>(a, smem, m, l, o, lane, warp, grp, b, kvh, S, rank, G, cluster);
+    finish_mma<T, HD, GMERGE, NW>(a, smem, m, l, o, lane, warp, grp, b, kvh, S, rank, G, cluster);
 }
 
-template <typename T, int HD>
+template <typename T, int HD, int NW>
 cudaError_t launch_mma(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
-    const size_t smem = mma_smem(HD);
+    const size_t smem = mma_smem(HD, NW);
     if (a.gsplits > 0) {
-        auto kg = decode_mma_kernel<T, HD, true>;
+        auto kg = decode_mma_kernel<T, HD, true, NW>;
         const cudaError_t eg =
             cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (eg != cudaSuccess) return eg;
-        const dim3 grid(static_cast<unsigned>(a.B * a.n_kv * a.gsplits)), block(kMmaWarps * 32);
+        const dim3 grid(static_cast<unsigned>(a.B * a.n_kv * a.gsplits)), block(NW * 32);
         return launch_kernel(kg, grid, block, smem, s, p.pdl, 1, a);
     }
-    auto kernel = decode_mma_kernel<T, HD, false>;
+    auto kernel = decode_mma_kernel<T, HD, false, NW>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int splits = p.splits;
@@ -791,7 +796,7 @@ cudaError_t launch_mma(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
             attr.val.clusterDim.x = static_cast<unsigned>(splits);
             attr.val.clusterDim.y = attr.val.clusterDim.z = 1;
             cfg.gridDim = dim3(static_cast<unsigned>(splits));
-            cfg.blockDim = dim3(kMmaWarps * 32);
+            cfg.blockDim = dim3(NW * 32);
             cfg.dynamicSmemBytes = smem;
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
@@ -802,7 +807,7 @@ cudaError_t launch_mma(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
             splits = 8;
         }
     }
-    const dim3 grid(static_cast<unsigned>(a.B * a.n_kv * splits)), block(kMmaWarps * 32);
+    const dim3 grid(static_cast<unsigned>(a.B * a.n_kv * splits)), block(NW * 32);
     return launch_kernel(kernel, grid, block, smem, s, p.pdl, splits, a);
 }
 
@@ -1070,14 +1075,17 @@ template <typename T>
 cudaError_t launch_typed(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
     if constexpr (sizeof(T) == 2) {
         if (p.tma) return p.head_dim == 64 ? launch_tma<T, 64>(a, p, s) : launch_tma<T, 128>(a, p, s);
-        if (p.tensor_cores) return p.head_dim == 64 ? launch_mma<T, 64>(a, p, s) : launch_mma<T, 128>(a, p, s);
+        if (p.tensor_cores) {
+            if (p.mma_warps == 4) return p.head_dim == 64 ? launch_mma<T, 64, 4>(a, p, s) : launch_mma<T, 128, 4>(a, p, s);
+            return p.head_dim == 64 ? launch_mma<T, 64, 8>(a, p, s) : launch_mma<T, 128, 8>(a, p, s);
+        }
     }
     return p.stages >= 4 ? launch_stages<T, 4>(a, p, s) : launch_stages<T, 2>(a, p, s);
 }
 
 }  // namespace attn
 
-size_t decode_attention_mma_smem(int head_dim) { return attn::mma_smem(head_dim); }
+size_t decode_attention_mma_smem(int head_dim, int warps) { return attn::mma_smem(head_dim, warps); }
 size_t decode_attention_tma_smem(int head_dim) { return attn::tma_smem(head_dim); }
 
 size_t decode_attention_smem(int group, int head_dim, int block_size, int stages, int es) {

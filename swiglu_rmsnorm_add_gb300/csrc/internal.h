@@ -158,6 +158,7 @@ struct AttnPlan {
     int stages;    // K/V tiles in flight per CTA (CUDA-core path)
     bool tensor_cores;  // bf16 / fp16, head_dim 64 or 128: the mma.sync path
     bool tma = false;   // ... with the K / V tiles moved by TMA (decode_tma_kernel)
+    int mma_warps = 8;  // warps per CTA of the mma.sync kernel: 8 (one CTA per SM) or 4 (two)
     size_t smem;
     bool pdl;
     int num_sms;
@@ -165,7 +166,7 @@ struct AttnPlan {
 
 cudaError_t launch_decode_attention(const AttnArgs& a, const AttnPlan& p, int dtype, cudaStream_t s);
 size_t decode_attention_smem(int group, int head_dim, int block_size, int stages, int es);
-size_t decode_attention_mma_smem(int head_dim);
+size_t decode_attention_mma_smem(int head_dim, int warps);
 size_t decode_attention_tma_smem(int head_dim);
 // Global-split plan of a decode-attention call: splits per (request, kv head) (0: none) and the
 // workspace bytes it needs.

@@ -89,7 +89,8 @@ def test_config_qwen25_long_context():
     assert_attention_close(got, want, cache, table, seq, "B=1 ctx=32768")
 
 
-VARIANT = {"auto": -1, "cuda_cores": 0, "mma_sync": 1, "mma_sync_tma": 2}
+VARIANT = {"auto": -1, "cuda_cores": 0, "mma_sync": 1, "mma_sync_tma": 2,
+           "mma_sync_w4": 1 | (4 << 16)}   # the mma.sync kernel with 4-warp CTAs (two per SM)
 
 
 def tensor_core_shape(dtype, hd):
@@ -97,10 +98,10 @@ def tensor_core_shape(dtype, hd):
     return dtype != torch.float32 and hd in (64, 128)
 
 
-@pytest.fixture(params=["auto", "cuda_cores", "mma_sync_tma"])
+@pytest.fixture(params=["auto", "cuda_cores", "mma_sync_tma", "mma_sync_w4"])
 def attn_variant(request):
-    """Run under the automatic choice, with the CUDA-core kernel forced, and with the
-    TMA-fed tensor-core kernel forced."""
+    """Run under the automatic choice, with the CUDA-core kernel forced, with the TMA-fed
+    tensor-core kernel forced, and with the mma.sync kernel in 4-warp CTAs forced."""
     sra.force_variant("decode_attention", VARIANT[request.param])
     yield request.param
     sra.force_variant("decode_attention", -1)
@@ -111,8 +112,8 @@ def attn_variant(request):
 @pytest.mark.parametrize("n_head,n_kv", [(8, 8), (8, 4), (12, 2), (32, 4), (8, 1)])
 @pytest.mark.parametrize("bs", [8, 16, 32])
 def test_shapes_dtypes(dtype, hd, n_head, n_kv, bs, attn_variant):
-    if attn_variant == "mma_sync_tma" and not tensor_core_shape(dtype, hd):
-        pytest.skip("the TMA-fed kernel serves 16-bit data with head_dim 64 or 128")
+    if attn_variant in ("mma_sync_tma", "mma_sync_w4") and not tensor_core_shape(dtype, hd):
+        pytest.skip("the tensor-core kernels serve 16-bit data with head_dim 64 or 128")
     lens = [1, 5, bs, bs + 1, 3 * bs - 1, 200]
     q, cache, table, seq = syn.attention_inputs(6, lens, n_head, n_kv, hd, bs, 6 * (200 // bs + 2), dtype,
                                                 1015 + hd + bs)
@@ -132,7 +133,7 @@ def test_cuda_core_kernel_on_the_configs(B, ctx):
         sra.force_variant("decode_attention", -1)
 
 
-@pytest.mark.parametrize("variant", ["mma_sync", "mma_sync_tma"])
+@pytest.mark.parametrize("variant", ["mma_sync", "mma_sync_tma", "mma_sync_w4"])
 @pytest.mark.parametrize("B,ctx,splits", [(1, 32768, 0), (32, 1024, 0), (3, 4097, 0), (64, 1024, 0), (2, 1000, 1),
                                           (2, 1000, 2), (2, 1000, 4), (2, 1000, 8), (2, 1000, 16), (1, 300, 16)])
 def test_tensor_core_kernels_on_the_configs(variant, B, ctx, splits):
@@ -150,7 +151,7 @@ def test_tensor_core_kernels_on_the_configs(variant, B, ctx, splits):
         sra.force_variant("decode_attention", -1)
 
 
-@pytest.mark.parametrize("variant", ["mma_sync", "mma_sync_tma"])
+@pytest.mark.parametrize("variant", ["mma_sync", "mma_sync_tma", "mma_sync_w4"])
 @pytest.mark.parametrize("bs", [8, 16, 32])
 def test_tensor_core_kernels_mixed_lengths_and_bad_blocks(variant, bs):
     """Batch 64 with lengths 1..1024 and a few bad table entries (a block of 8 tokens puts two
@@ -252,7 +253,7 @@ def test_reads_what_rope_kv_store_wrote():
 
 
 # ----------------------------------------------- global split through a workspace
-@pytest.mark.parametrize("variant", ["auto", "mma_sync_tma"])
+@pytest.mark.parametrize("variant", ["auto", "mma_sync_tma", "mma_sync_w4"])
 @pytest.mark.parametrize("B,ctx,n_head,n_kv,hd", [(1, 32768, 12, 2, 128), (2, 16384, 8, 1, 64), (1, 12000, 32, 4, 128),
                                                   (3, 9000, 12, 2, 128)])
 def test_workspace_split_matches_the_oracle_twice(B, ctx, n_head, n_kv, hd, variant):
