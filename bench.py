@@ -1076,6 +1076,8 @@ def run_sweep(args):
             except RuntimeError:
                 continue
             per = []
+            # an NVTX range per (shape, setting): an ncu launch list of this sweep can be split by it
+            torch.cuda.nvtx.range_push(f"sweep:{e.name}|{label}")
             for _ in range(3):
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 flush.fill_(1)
@@ -1087,6 +1089,7 @@ def run_sweep(args):
                 b.record(stream)
                 b.synchronize()
                 per.append(a.elapsed_time(b) * 1e3 / len(calls))
+            torch.cuda.nvtx.range_pop()
             us = statistics.median(per)
             rec = {"us": round(us, 3), "frac": round(e.bytes / (us * 1e-6) / 1e9 / peak, 4)}
             if v < 0:
