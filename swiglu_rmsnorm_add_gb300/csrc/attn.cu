@@ -298,22 +298,24 @@ struct Mma;
 template <>
 struct Mma<__nv_bfloat16> {
     __device__ __forceinline__ static void run(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-        float z0, z1;  // rows 8-15 of A are zero: their results are dropped, not held
+        // rows 8-15 of A are zero: their results go to registers local to the asm block
         asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-            "{%0,%1,%10,%11};"
-            : "+f"(d[0]), "+f"(d[1]), "=f"(z0), "=f"(z1)
+            "{\n\t.reg .f32 z0, z1;\n\t"
+            "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,z0,z1}, {%2,%3,%4,%5}, {%6,%7}, "
+            "{%0,%1,%8,%9};\n\t}"
+            : "+f"(d[0]), "+f"(d[1])
             : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.0f), "f"(0.0f));
     }
 };
 template <>
 struct Mma<__half> {
     __device__ __forceinline__ static void run(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-        float z0, z1;  // rows 8-15 of A are zero: their results are dropped, not held
+        // rows 8-15 of A are zero: their results go to registers local to the asm block
         asm volatile(
-            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
-            "{%0,%1,%10,%11};"
-            : "+f"(d[0]), "+f"(d[1]), "=f"(z0), "=f"(z1)
+            "{\n\t.reg .f32 z0, z1;\n\t"
+            "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,z0,z1}, {%2,%3,%4,%5}, {%6,%7}, "
+            "{%0,%1,%8,%9};\n\t}"
+            : "+f"(d[0]), "+f"(d[1])
             : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.0f), "f"(0.0f));
     }
 };
@@ -434,7 +436,7 @@ constexpr int kMmaStages = 3;   // tiles per warp ring
 // warps' partials; with a workspace split, the last CTA's merge buffers), then the row masks.
 __host__ __device__ inline size_t mma_ring_bytes(int HD, int NW) {
     const size_t ring = static_cast<size_t>(NW) * kMmaStages * 2 * kMmaTile * HD * 2;
-    const size_t merge = (static_cast<size_t>(NW) * 8 * (HD + 2) + 8 * (HD + 2)) * 4;
+    const size_t merge = (static_cast<size_t>(NW) * 8 * (HD + 11) + 8 * (HD + 2) + 17 * 8) * 4;
     const size_t gmerge = static_cast<size_t>(kMaxGsplits) * 24 * 4 + 64 + 16 * 8 * static_cast<size_t>(HD) * 4;
     size_t need = ring > merge ? ring : merge;
     return need > gmerge ? need : gmerge;
@@ -457,12 +459,16 @@ __device__ __forceinline__ void finish_mma(const AttnArgs& a, unsigned char* sme
     l += __shfl_xor_sync(FULL, l, 1);
     l += __shfl_xor_sync(FULL, l, 2);
 
-    // warp partials into shared memory (over the rings, which are done)
+    // warp partials into shared memory (over the rings, which are done). A row of O is HD + 8
+    // floats apart and each lane stores its pair as one 8-byte store, so the 16 lanes of a
+    // half-warp hit 16 different bank pairs (rows HD apart would put the 8 rows of a fragment
+    // in the same banks and serialise the stores 8-fold).
+    constexpr int WS = HD + 8;
     __syncthreads();
     float* wm = reinterpret_cast<float*>(smem);  // [warps][8]
     float* wl = wm + NW * 8;                     // [warps][8]
-    float* wo = wl + NW * 8;                     // [warps][8][HD]
-    float* pm = wo + NW * 8 * HD;                // [8]  CTA partials for the cluster merge
+    float* wo = wl + NW * 8;                     // [warps][8][WS]
+    float* pm = wo + NW * 8 * WS;                // [8]  CTA partials for the cluster merge
     float* pl = pm + 8;                          // [8]
     float* pacc = pl + 8;                        // [8][HD]
     if (warp < NW) {
@@ -471,33 +477,39 @@ __device__ __forceinline__ void finish_mma(const AttnArgs& a, unsigned char* sme
             wl[warp * 8 + fg] = l;
         }
 #pragma unroll
-        for (int d = 0; d < NB; ++d) {
-            wo[(warp * 8 + fg) * HD + 8 * d + 2 * ft] = o[d][0];
-            wo[(warp * 8 + fg) * HD + 8 * d + 2 * ft + 1] = o[d][1];
+        for (int d = 0; d < NB; ++d)
+            *reinterpret_cast<float2*>(wo + (warp * 8 + fg) * WS + 8 * d + 2 * ft) = make_float2(o[d][0], o[d][1]);
+    }
+    __syncthreads();
+    // the warps' merge weights 2^(m_w - M) and the denominator, once per query head (they do
+    // not depend on the output column); warps that saw no token weigh 0 and hold O = 0
+    float* sw = pacc + 8 * HD;  // [warps][8]
+    if (threadIdx.x < G) {
+        const int gg = threadIdx.x;
+        float M = -INFINITY;
+        for (int w = 0; w < NW; ++w) M = fmaxf(M, wm[w * 8 + gg]);
+        float den = 0.0f;
+        for (int w = 0; w < NW; ++w) {
+            const float mw = wm[w * 8 + gg];
+            const float e = (M == -INFINITY || mw == -INFINITY) ? 0.0f : exp2f(mw - M);
+            sw[w * 8 + gg] = e;
+            den = fmaf(e, wl[w * 8 + gg], den);
         }
+        pm[gg] = M;
+        pl[gg] = den;
     }
     __syncthreads();
     T* out = static_cast<T*>(a.out) + b * a.os + static_cast<int64_t>(kvh * G) * HD;
     const bool alone = !GMERGE && S == 1;  // one CTA holds the whole (request, kv head)
     for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
         const int gg = idx / HD, d = idx - gg * HD;
-        float M = -INFINITY;
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, wm[w * 8 + gg]);
-        float num = 0.0f, den = 0.0f;
-        if (M != -INFINITY) {
-            for (int w = 0; w < NW; ++w) {
-                const float mw = wm[w * 8 + gg];
-                if (mw == -INFINITY) continue;
-                const float sw = exp2f(mw - M);
-                num = fmaf(sw, wo[(w * 8 + gg) * HD + d], num);
-                den = fmaf(sw, wl[w * 8 + gg], den);
-            }
-        }
+        float num = 0.0f;
+        for (int w = 0; w < NW; ++w) num = fmaf(sw[w * 8 + gg], wo[(w * 8 + gg) * WS + d], num);
         if (alone) {
+            const float den = pl[gg];
             out[idx] = from_f32<T>(den > 0.0f ? num / den : 0.0f);
         } else {
             pacc[idx] = num;
-            if (d == 0) pm[gg] = M, pl[gg] = den;
         }
     }
     if (alone) return;
@@ -574,20 +586,34 @@ __device__ __forceinline__ void finish_mma(const AttnArgs& a, unsigned char* sme
         return;
     }
     cluster.sync();
-    for (int idx = rank * blockDim.x + threadIdx.x; idx < G * HD; idx += S * blockDim.x) {
-        const int gg = idx / HD;
+    // the splits' merge weights and the denominator, once per query head, then each output
+    // column's S partials requested together before the sums
+    float* cw = sw + NW * 8;    // [S][8]
+    float* cden = cw + 16 * 8;  // [8]
+    if (threadIdx.x < G) {
+        const int gg = threadIdx.x;
         float M = -INFINITY;
         for (int r = 0; r < S; ++r) M = fmaxf(M, cluster.map_shared_rank(pm, r)[gg]);
-        float num = 0.0f, den = 0.0f;
-        if (M != -INFINITY) {
-            for (int r = 0; r < S; ++r) {
-                const float mr = cluster.map_shared_rank(pm, r)[gg];
-                if (mr == -INFINITY) continue;
-                const float w = exp2f(mr - M);
-                num = fmaf(w, cluster.map_shared_rank(pacc, r)[idx], num);
-                den = fmaf(w, cluster.map_shared_rank(pl, r)[gg], den);
-            }
+        float den = 0.0f;
+        for (int r = 0; r < S; ++r) {
+            const float mr = cluster.map_shared_rank(pm, r)[gg];
+            const float e = (M == -INFINITY || mr == -INFINITY) ? 0.0f : exp2f(mr - M);
+            cw[r * 8 + gg] = e;
+            den = fmaf(e, cluster.map_shared_rank(pl, r)[gg], den);
         }
+        cden[gg] = den;
+    }
+    __syncthreads();
+    for (int idx = rank * blockDim.x + threadIdx.x; idx < G * HD; idx += S * blockDim.x) {
+        const int gg = idx / HD;
+        float v[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) v[r] = r < S ? cluster.map_shared_rank(pacc, r)[idx] : 0.0f;
+        float num = 0.0f;
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            if (r < S) num = fmaf(cw[r * 8 + gg], v[r], num);
+        const float den = cden[gg];
         out[idx] = from_f32<T>(den > 0.0f ? num / den : 0.0f);
     }
     cluster.sync();
@@ -833,7 +859,7 @@ template <int HD>
 __host__ __device__ constexpr size_t tma_slot_bytes() { return 2u * kTmaTile * HD * 2; }  // K and V tiles
 __host__ __device__ inline size_t tma_smem(int HD) {
     const size_t ring = HD == 128 ? tma_slots<128>() * tma_slot_bytes<128>() : tma_slots<64>() * tma_slot_bytes<64>();
-    const size_t merge = (static_cast<size_t>(kTmaWarps) * 8 * (HD + 2) + 8 * (HD + 2)) * 4;
+    const size_t merge = (static_cast<size_t>(kTmaWarps) * 8 * (HD + 11) + 8 * (HD + 2) + 17 * 8) * 4;
     const size_t gmerge = static_cast<size_t>(kMaxGsplits) * 24 * 4 + 64 + 16 * 8 * static_cast<size_t>(HD) * 4;
     size_t need = ring > merge ? ring : merge;
     need = need > gmerge ? need : gmerge;
