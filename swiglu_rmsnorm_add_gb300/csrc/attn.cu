@@ -432,6 +432,12 @@ __device__ __forceinline__ void tile_step(const T* Ks, const T* Vs, unsigned val
 constexpr int kMmaTile = 16;    // tokens per warp tile
 constexpr int kMmaStages = 3;   // tiles per warp ring
 
+// The cluster merge's inbox (outside the rings, so other CTAs of the cluster may write it while
+// this CTA still streams): every split's maxima and sums [16][8] each, then its partial output
+// columns for the slice of columns this CTA owns, [splits][slice] (slices of HD * 8 / splits
+// columns rounded up to 4: at most 8 * HD + 64 floats in all).
+__host__ __device__ constexpr size_t inbox_floats(int HD) { return 16 * 8 * 2 + 8 * static_cast<size_t>(HD) + 64; }
+
 // Shared memory of an NW-warp CTA: the warps' rings, over which the merges later run (the
 // warps' partials; with a workspace split, the last CTA's merge buffers), then the row masks.
 __host__ __device__ inline size_t mma_ring_bytes(int HD, int NW) {
@@ -441,16 +447,17 @@ __host__ __device__ inline size_t mma_ring_bytes(int HD, int NW) {
     size_t need = ring > merge ? ring : merge;
     return need > gmerge ? need : gmerge;
 }
-__host__ __device__ inline size_t mma_smem(int HD, int NW) {
-    return mma_ring_bytes(HD, NW) + static_cast<size_t>(NW) * kMmaStages * 4;  // + per-slot row masks
+__host__ __device__ inline size_t mma_inbox_offset(int HD, int NW) {  // after the per-slot row masks
+    return (mma_ring_bytes(HD, NW) + static_cast<size_t>(NW) * kMmaStages * 4 + 15) / 16 * 16;
 }
+__host__ __device__ inline size_t mma_smem(int HD, int NW) { return mma_inbox_offset(HD, NW) + inbox_floats(HD) * 4; }
 
 // The end of a (request, kv head, split) CTA of the tensor-core kernels: the warps' (m, l, O)
 // merged in shared memory (over the drained rings), then the splits merged through distributed
 // shared memory (a cluster) or, with GMERGE, through the workspace by the CTA that finishes
 // last. NW warps hold partials; warps past them (a copy-issuing warp) only join the barriers.
 template <typename T, int HD, bool GMERGE, int NW>
-__device__ __forceinline__ void finish_mma(const AttnArgs& a, unsigned char* smem, float m, float l,
+__device__ __forceinline__ void finish_mma(const AttnArgs& a, unsigned char* smem, float* inbox, float m, float l,
                                            float (&o)[HD / 8][2], int lane, int warp, int64_t grp, int64_t b,
                                            int kvh, int S, int rank, int G, cg::cluster_group& cluster) {
     constexpr int NB = HD / 8;
@@ -497,10 +504,21 @@ __device__ __forceinline__ void finish_mma(const AttnArgs& a, unsigned char* sme
         }
         pm[gg] = M;
         pl[gg] = den;
+        if (!GMERGE && S > 1) {
+            // this split's maxima and sums into every CTA's inbox
+            for (int q = 0; q < S; ++q) {
+                float* ib = cluster.map_shared_rank(inbox, q);
+                ib[rank * 8 + gg] = M;
+                ib[128 + rank * 8 + gg] = den;
+            }
+        }
     }
     __syncthreads();
     T* out = static_cast<T*>(a.out) + b * a.os + static_cast<int64_t>(kvh * G) * HD;
     const bool alone = !GMERGE && S == 1;  // one CTA holds the whole (request, kv head)
+    // cluster merge: CTA q owns output columns [q * C, (q + 1) * C) and receives every split's
+    // partials for them in its inbox (stores into other CTAs' shared memory, no round trip)
+    const int C = (G * HD + 4 * S - 1) / (4 * S) * 4;
     for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
         const int gg = idx / HD, d = idx - gg * HD;
         float num = 0.0f;
@@ -508,8 +526,11 @@ __device__ __forceinline__ void finish_mma(const AttnArgs& a, unsigned char* sme
         if (alone) {
             const float den = pl[gg];
             out[idx] = from_f32<T>(den > 0.0f ? num / den : 0.0f);
-        } else {
+        } else if (GMERGE) {
             pacc[idx] = num;
+        } else {
+            const int q = idx / C;
+            cluster.map_shared_rank(inbox, q)[256 + rank * C + (idx - q * C)] = num;
         }
     }
     if (alone) return;
@@ -585,38 +606,32 @@ __device__ __forceinline__ void finish_mma(const AttnArgs& a, unsigned char* sme
         if (threadIdx.x == 0) a.ws_count[grp] = 0;  // ready for the next call
         return;
     }
-    cluster.sync();
-    // the splits' merge weights and the denominator, once per query head, then each output
-    // column's S partials requested together before the sums
+    cluster.sync();  // every split's partials are in the owners' inboxes (release / acquire)
+    // the splits' merge weights and the denominator, once per query head, from the inbox
     float* cw = sw + NW * 8;    // [S][8]
     float* cden = cw + 16 * 8;  // [8]
     if (threadIdx.x < G) {
         const int gg = threadIdx.x;
         float M = -INFINITY;
-        for (int r = 0; r < S; ++r) M = fmaxf(M, cluster.map_shared_rank(pm, r)[gg]);
+        for (int r = 0; r < S; ++r) M = fmaxf(M, inbox[r * 8 + gg]);
         float den = 0.0f;
         for (int r = 0; r < S; ++r) {
-            const float mr = cluster.map_shared_rank(pm, r)[gg];
+            const float mr = inbox[r * 8 + gg];
             const float e = (M == -INFINITY || mr == -INFINITY) ? 0.0f : exp2f(mr - M);
             cw[r * 8 + gg] = e;
-            den = fmaf(e, cluster.map_shared_rank(pl, r)[gg], den);
+            den = fmaf(e, inbox[128 + r * 8 + gg], den);
         }
         cden[gg] = den;
     }
     __syncthreads();
-    for (int idx = rank * blockDim.x + threadIdx.x; idx < G * HD; idx += S * blockDim.x) {
+    const int c0 = rank * C, c1 = c0 + C < G * HD ? c0 + C : G * HD;
+    for (int idx = c0 + threadIdx.x; idx < c1; idx += blockDim.x) {
         const int gg = idx / HD;
-        float v[16];
-#pragma unroll
-        for (int r = 0; r < 16; ++r) v[r] = r < S ? cluster.map_shared_rank(pacc, r)[idx] : 0.0f;
         float num = 0.0f;
-#pragma unroll
-        for (int r = 0; r < 16; ++r)
-            if (r < S) num = fmaf(cw[r * 8 + gg], v[r], num);
+        for (int r = 0; r < S; ++r) num = fmaf(cw[r * 8 + gg], inbox[256 + r * C + (idx - c0)], num);
         const float den = cden[gg];
         out[idx] = from_f32<T>(den > 0.0f ? num / den : 0.0f);
     }
-    cluster.sync();
 }
 
 // GMERGE: the splits of a (request, kv head) are independent CTAs (a.gsplits of them, more
@@ -793,7 +808,8 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 2 : 1) decode_mma_kernel(At
                          [](int tok, int chunk) { return tok * HD + ((chunk ^ (tok & 7)) * 8); });
     }
     cp_async_wait<0>();
-    finish_mma<T, HD, GMERGE, NW>(a, smem, m, l, o, lane, warp, grp, b, kvh, S, rank, G, cluster);
+    finish_mma<T, HD, GMERGE, NW>(a, smem, reinterpret_cast<float*>(smem + mma_inbox_offset(HD, NW)), m, l, o, lane,
+                                  warp, grp, b, kvh, S, rank, G, cluster);
 }
 
 template <typename T, int HD, int NW>
@@ -863,7 +879,7 @@ __host__ __device__ inline size_t tma_smem(int HD) {
     const size_t gmerge = static_cast<size_t>(kMaxGsplits) * 24 * 4 + 64 + 16 * 8 * static_cast<size_t>(HD) * 4;
     size_t need = ring > merge ? ring : merge;
     need = need > gmerge ? need : gmerge;
-    return 1024 + need;
+    return 1024 + need + inbox_floats(HD) * 4;
 }
 
 template <typename T, int HD, bool GMERGE>
@@ -1019,7 +1035,8 @@ __global__ void __maxnreg__(112) decode_tma_kernel(AttnArgs a,
             if (lane == 0) mbar_arrive(&empty[slot]);
         }
     }
-    finish_mma<T, HD, GMERGE, kTmaWarps>(a, smem, m, l, o, lane, warp, grp, b, kvh, S, rank, G, cluster);
+    finish_mma<T, HD, GMERGE, kTmaWarps>(a, smem, reinterpret_cast<float*>(smem + tma_smem(HD) - 1024 - inbox_floats(HD) * 4),
+                                         m, l, o, lane, warp, grp, b, kvh, S, rank, G, cluster);
 }
 
 template <typename T, int HD>
