@@ -21,9 +21,10 @@
  *    load from and store to). The caller owns every buffer; the library never
  *    allocates, frees, zero-fills or keeps a pointer after the call returns.
  *    Two exceptions, both library-owned device arrays in the library's own
- *    module: the scratch array of sra_paged_decode_attention_noalloc (whose
- *    counters that call clears, and whose address it keeps per device), and the
- *    counter of bounded device waits that ran out (sra_wait_timeouts).
+ *    module: the scratch array of sra_paged_decode_attention_noalloc (which that
+ *    call writes its partial results into, and whose address it keeps per
+ *    device), and the counter of bounded device waits that ran out
+ *    (sra_wait_timeouts).
  *  - `stream` is a cudaStream_t passed as void* (NULL = the legacy default
  *    stream). Every call only enqueues work on that stream and returns at once;
  *    results are visible after the stream is synchronised. The kernel runs on
@@ -290,15 +291,16 @@ SRA_API int sra_paged_decode_attention(const void* q, const void* kv_cache, cons
  * 32 k cached tokens), the tensor-core kernel splits every pair over many
  * independent CTAs ([lsln] sec. 3: split the reduction, then merge the parts by
  * their max and sum of exponentials); each writes its partial result into the
- * workspace and the last to finish merges them. Otherwise the workspace is
- * unused and the call is sra_paged_decode_attention.
+ * workspace and a second kernel, launched right after them on the same stream,
+ * merges them. Otherwise the workspace is unused and the call is
+ * sra_paged_decode_attention.
  * workspace: device memory of at least
  *   sra_paged_decode_attention_workspace_size(B, n_head, n_kv_head, head_dim,
  *                                             max_blocks_per_seq, block_size, dtype)
- *   bytes, 16-byte aligned, zero-filled by the caller once before its first use;
- *   every call leaves it ready for the next (its counters back at zero). It must
- *   not overlap any other argument, and calls that share a workspace must not run
- *   concurrently (same stream, or ordered by events).
+ *   bytes, 16-byte aligned; its contents on entry do not matter (a leading area,
+ *   kept for the layout, is never written). It must not overlap any other
+ *   argument, and calls that share a workspace must not run concurrently (same
+ *   stream, or ordered by events).
  * Errors: those of sra_paged_decode_attention; workspace_bytes below the size the
  * shape needs, a negative size or a misaligned workspace -> SRA_ERR_ARG.
  */
@@ -333,7 +335,7 @@ SRA_API int64_t sra_paged_decode_attention_workspace_size(int64_t B, int n_head,
  * device (with it current); make that first call before any stream capture. The
  * address is kept per device and looked up again when the device's context has
  * changed (a call after cudaDeviceReset finds the array in the new context).
- * Every call clears the array's counters on `stream` before its kernel runs.
+ * Every call writes the partial results it then merges; nothing carries over.
  * Races: all calls on a device share the one array, so two calls that may run at
  * the same time on the GPU (different streams without an event between them, or
  * different host threads) corrupt each other's partial results; order them on one

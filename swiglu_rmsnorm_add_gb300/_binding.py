@@ -387,8 +387,8 @@ def dyht(x: torch.Tensor, alpha: torch.Tensor, gamma: torch.Tensor, out: torch.T
 
 def decode_attention_workspace(B: int, n_head: int, n_kv_head: int, head_dim: int, max_blocks: int,
                                block_size: int, dtype=torch.bfloat16, device="cuda") -> torch.Tensor | None:
-    """A zero-filled workspace for paged_decode_attention(..., workspace=...), or None when the
-    shape does not use one. Reuse it across calls (the kernel leaves it zeroed)."""
+    """A workspace for paged_decode_attention(..., workspace=...), or None when the shape does
+    not use one. Reuse it across calls (each call writes what it reads)."""
     n = lib().sra_paged_decode_attention_workspace_size(B, n_head, n_kv_head, head_dim, max_blocks, block_size,
                                                        DTYPE_CODE[dtype])
     if n < 0:

@@ -923,7 +923,6 @@ static int attention_impl(const void* q, const void* kv_cache, const int32_t* bl
                 overlap(sws, span_of(q, B, q_tok_stride, w, es)))
                 return SRA_ERR_ALIAS;
             a.gsplits = gs;
-            a.ws_count = static_cast<int32_t*>(workspace);
             a.ws_part = reinterpret_cast<float*>(static_cast<char*>(workspace) + ((B * n_kv_head * 4 + 255) / 256) * 256);
         }
     }

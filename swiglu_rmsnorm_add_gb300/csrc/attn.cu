@@ -535,75 +535,11 @@ __device__ __forceinline__ void finish_mma(const AttnArgs& a, unsigned char* sme
     }
     if (alone) return;
     if constexpr (GMERGE) {
-        // this split's partial into the workspace: [8 max][8 sum][8 x HD output]
+        // this split's partial into the workspace, [8 max][8 sum][8 x HD output]; the merge kernel
+        // that follows in the stream (decode_merge_kernel) combines the splits
         float* slot = a.ws_part + (static_cast<int64_t>(grp) * S + rank) * (16 + 8 * HD);
-        __syncthreads();
         for (int i = threadIdx.x; i < G * HD; i += blockDim.x) slot[16 + i] = pacc[i];
         if (threadIdx.x < G) slot[threadIdx.x] = pm[threadIdx.x], slot[8 + threadIdx.x] = pl[threadIdx.x];
-        __threadfence();
-        __syncthreads();
-        __shared__ int last;
-        if (threadIdx.x == 0) last = atomicAdd(a.ws_count + grp, 1) == S - 1;
-        __syncthreads();
-        if (!last) return;
-        __threadfence();  // the other splits' partials are visible past their counts
-        const float* parts = a.ws_part + static_cast<int64_t>(grp) * S * (16 + 8 * HD);
-        constexpr int PS = 16 + 8 * HD;  // floats per split's partial
-        constexpr int CH = 16;           // splits one thread sums with its loads all in flight
-        // the splits' maxima and sums into shared memory (over the drained rings), one
-        // 16-byte load per thread and quarter header, all independent
-        float* hm = reinterpret_cast<float*>(smem);        // [S][16]: 8 maxima, 8 sums
-        float* wr = hm + static_cast<size_t>(S) * 16;      // [S][8] merge weights
-        float* den = wr + static_cast<size_t>(S) * 8;      // [8]
-        float* part = den + 8;                             // [nq][G * HD] partial numerators
-        for (int i = threadIdx.x; i < S * 4; i += blockDim.x)
-            reinterpret_cast<float4*>(hm)[i] = __ldcg(reinterpret_cast<const float4*>(parts + (i >> 2) * PS) + (i & 3));
-        __syncthreads();
-        // warp w, query heads gg = w, w + warps, ...: M over the splits, the weights 2^(m_r - M)
-        // and the denominator
-        for (int gg = warp; gg < G; gg += static_cast<int>(blockDim.x >> 5)) {
-            float M = -INFINITY;
-            for (int r = lane; r < S; r += 32) M = fmaxf(M, hm[r * 16 + gg]);
-            for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
-            float d = 0.0f;
-            for (int r = lane; r < S; r += 32) {
-                const float mr = hm[r * 16 + gg];
-                const float w = (M == -INFINITY || mr == -INFINITY) ? 0.0f : exp2f(mr - M);
-                wr[r * 8 + gg] = w;
-                d = fmaf(w, hm[r * 16 + 8 + gg], d);
-            }
-            for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(FULL, d, o);
-            if (lane == 0) den[gg] = d;
-        }
-        __syncthreads();
-        // numerators: a task is 4 output columns over a chunk of CH splits, its CH loads
-        // issued together; the chunks' sums meet in shared memory
-        const int nslots = G * HD / 4, nq = (S + CH - 1) / CH;
-        for (int t = threadIdx.x; t < nslots * nq; t += blockDim.x) {
-            const int sl = t % nslots, q = t / nslots, gg = 4 * sl / HD;
-            float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-#pragma unroll
-            for (int j = 0; j < CH; ++j) {
-                const int r = q * CH + j;
-                if (r < S) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(parts + r * PS + 16) + sl);
-                    const float w = wr[r * 8 + gg];
-                    acc.x = fmaf(w, v.x, acc.x);
-                    acc.y = fmaf(w, v.y, acc.y);
-                    acc.z = fmaf(w, v.z, acc.z);
-                    acc.w = fmaf(w, v.w, acc.w);
-                }
-            }
-            reinterpret_cast<float4*>(part + static_cast<size_t>(q) * G * HD)[sl] = acc;
-        }
-        __syncthreads();
-        for (int idx = threadIdx.x; idx < G * HD; idx += blockDim.x) {
-            const int gg = idx / HD;
-            float num = 0.0f;
-            for (int q = 0; q < nq; ++q) num += part[q * G * HD + idx];
-            out[idx] = from_f32<T>(den[gg] > 0.0f ? num / den[gg] : 0.0f);
-        }
-        if (threadIdx.x == 0) a.ws_count[grp] = 0;  // ready for the next call
         return;
     }
     cluster.sync();  // every split's partials are in the owners' inboxes (release / acquire)
@@ -635,9 +571,8 @@ __device__ __forceinline__ void finish_mma(const AttnArgs& a, unsigned char* sme
 }
 
 // GMERGE: the splits of a (request, kv head) are independent CTAs (a.gsplits of them, more
-// than a cluster holds): each writes its (max, sum, partial output) to the workspace, and the
-// CTA that finishes last (an atomic count per (request, kv head)) merges them and resets the
-// count to zero for the next call.
+// than a cluster holds): each writes its (max, sum, partial output) to the workspace, and
+// decode_merge_kernel, launched after them, combines the records.
 // NW warps per CTA: 8 (one CTA per SM) or 4 (two CTAs per SM, so a CTA of the next launch can
 // start beside one of this launch).
 template <typename T, int HD, bool GMERGE, int NW>
@@ -812,6 +747,90 @@ __global__ void __launch_bounds__(NW * 32, NW == 4 ? 2 : 1) decode_mma_kernel(At
                                   warp, grp, b, kvh, S, rank, G, cluster);
 }
 
+// The merge of a workspace split: CTA (pair, chunk) combines the S splits' partials of 32
+// output columns (one query head: head_dim is a multiple of 32). Thread (p, j) reads column j of
+// splits p, p + 8, ... with all its loads issued together and before the weights are known; the
+// headers (each split's max and sum for the chunk's head) arrive in the same round trip. The
+// eight partial sums of a column meet in shared memory in split order, so the result does not
+// depend on timing. Launched right after the split kernel, with programmatic dependent launch:
+// its CTAs start early and wait for the splits' records.
+constexpr int kMergeCols = 32;
+template <typename T, int HD>
+__global__ void __launch_bounds__(256) decode_merge_kernel(AttnArgs a) {
+    constexpr int PS = 16 + 8 * HD;        // floats per split's record
+    constexpr int PER = kMaxGsplits / 8;  // splits one thread reads at most
+    __shared__ float wgt[kMaxGsplits];
+    __shared__ float red[8][kMergeCols];
+    __shared__ float wmax[8], wsum[8], stat[2];
+    const int S = a.gsplits, G = a.group;
+    const int64_t grp = blockIdx.x;
+    const int64_t b = grp / a.n_kv;
+    const int kvh = static_cast<int>(grp - b * a.n_kv);
+    const int c0 = blockIdx.y * kMergeCols, gg = c0 / HD;
+    const int j = threadIdx.x % kMergeCols, p = threadIdx.x / kMergeCols;
+    const unsigned FULL = 0xffffffffu;
+    pdl_enter();
+    const float* parts = a.ws_part + grp * S * PS;
+    float v[PER];
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int r = p + 8 * i;
+        v[i] = r < S ? __ldcg(parts + r * PS + 16 + c0 + j) : 0.0f;
+    }
+    float mr = -INFINITY, lr = 0.0f;
+    if (threadIdx.x < S) {
+        mr = __ldcg(parts + threadIdx.x * PS + gg);
+        lr = __ldcg(parts + threadIdx.x * PS + 8 + gg);
+    }
+    // M over the splits (threads of split r hold its max), then the weights and the denominator
+    float M = mr;
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(FULL, M, o));
+    if ((threadIdx.x & 31) == 0) wmax[threadIdx.x >> 5] = M;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        float mm = -INFINITY;
+        for (int w = 0; w < 8; ++w) mm = fmaxf(mm, wmax[w]);
+        stat[0] = mm;
+    }
+    __syncthreads();
+    M = stat[0];
+    const float e = (threadIdx.x < S && M != -INFINITY && mr != -INFINITY) ? exp2f(mr - M) : 0.0f;
+    if (threadIdx.x < S) wgt[threadIdx.x] = e;
+    // the denominator: the same fixed reduction tree every call (a warp's butterfly, then the
+    // warps' sums in order)
+    float d = e * lr;
+    for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(FULL, d, o);
+    if ((threadIdx.x & 31) == 0) wsum[threadIdx.x >> 5] = d;
+    __syncthreads();  // the weights and the warps' sums are in shared memory
+    if (threadIdx.x == 0) {
+        float t = 0.0f;
+        for (int w = 0; w < 8; ++w) t += wsum[w];
+        stat[1] = t;
+    }
+    float num = 0.0f;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+        const int r = p + 8 * i;
+        if (r < S) num = fmaf(wgt[r], v[i], num);
+    }
+    red[p][j] = num;
+    __syncthreads();
+    if (p == 0) {
+        float t = 0.0f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) t += red[q][j];
+        const float den = stat[1];
+        T* out = static_cast<T*>(a.out) + b * a.os + static_cast<int64_t>(kvh * G) * HD;
+        out[c0 + j] = from_f32<T>(den > 0.0f ? t / den : 0.0f);
+    }
+}
+
+template <typename T, int HD>
+cudaError_t launch_merge(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>(a.B * a.n_kv), static_cast<unsigned>(a.group * HD / kMergeCols));
+    return launch_kernel(decode_merge_kernel<T, HD>, grid, dim3(256), 0, s, p.pdl, 1, a);
+}
+
 template <typename T, int HD, int NW>
 cudaError_t launch_mma(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
     const size_t smem = mma_smem(HD, NW);
@@ -821,7 +840,8 @@ cudaError_t launch_mma(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
             cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (eg != cudaSuccess) return eg;
         const dim3 grid(static_cast<unsigned>(a.B * a.n_kv * a.gsplits)), block(NW * 32);
-        return launch_kernel(kg, grid, block, smem, s, p.pdl, 1, a);
+        const cudaError_t el = launch_kernel(kg, grid, block, smem, s, p.pdl, 1, a);
+        return el != cudaSuccess ? el : launch_merge<T, HD>(a, p, s);
     }
     auto kernel = decode_mma_kernel<T, HD, false, NW>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
@@ -1058,8 +1078,9 @@ cudaError_t launch_tma(const AttnArgs& a, const AttnPlan& p, cudaStream_t s) {
         const cudaError_t eg =
             cudaFuncSetAttribute(kg, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (eg != cudaSuccess) return eg;
-        return launch_kernel(kg, dim3(static_cast<unsigned>(a.B * a.n_kv * a.gsplits)), block, smem, s, p.pdl, 1, a,
-                             tm);
+        const cudaError_t el =
+            launch_kernel(kg, dim3(static_cast<unsigned>(a.B * a.n_kv * a.gsplits)), block, smem, s, p.pdl, 1, a, tm);
+        return el != cudaSuccess ? el : launch_merge<T, HD>(a, p, s);
     }
     auto kernel = decode_tma_kernel<T, HD, false>;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));

@@ -19,12 +19,12 @@
 #include "sra.h"
 
 // Room for the partials of every split this library plans on a GPU of up to 252 SMs
-// at head_dim 128 (the merge needs at most 256 bytes of counters plus one
-// (16 + 8 * head_dim) float record per CTA, and it plans at most one CTA per SM).
+// at head_dim 128 (a leading area of at most 256 bytes plus one (16 + 8 * head_dim)
+// float record per CTA, and it plans at most one CTA per SM).
 static constexpr int64_t kScratchBytes = SRA_NOALLOC_SCRATCH_BYTES;
 
 // Every GPU that loads this library holds this array until the process exits.
-// Zero at load; each call clears its counters before the kernel runs.
+// Each call writes the records it then reads; nothing carries over between calls.
 static __device__ __align__(256) unsigned char g_attn_scratch[kScratchBytes];
 
 namespace {
@@ -113,14 +113,6 @@ int sra_paged_decode_attention_noalloc(const void* q, const void* kv_cache, cons
     }
     void* scratch = scratch_on_current_device(dev);
     if (!scratch) return SRA_ERR_DEVICE;
-    // the per-(request, kv head) arrival counters lead the scratch; the kernel's last CTA
-    // leaves them at zero, but they are cleared here too, so a call never depends on how
-    // an earlier one ended
-    const size_t counters = static_cast<size_t>((B * n_kv_head * 4 + 255) / 256 * 256);
-    if (cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
-        cudaGetLastError();
-        return SRA_ERR_LAUNCH;
-    }
     return sra_paged_decode_attention_ws(q, kv_cache, block_table, seq_lens, out, B, n_head, n_kv_head, head_dim,
                                          q_tok_stride, out_tok_stride, num_blocks, block_size, max_blocks_per_seq,
                                          scale, scratch, kScratchBytes, err_count, dtype, stream);

@@ -144,11 +144,10 @@ struct AttnArgs {
     int64_t B, qs, os, num_blocks, max_blocks;
     int n_head, n_kv, group, block_size;
     float scale_log2;          // softmax scale * log2(e)
-    // global split (tensor-core kernel): gsplits > 0 CTAs per (request, kv head), merged
-    // through the workspace by the last one to finish
+    // global split (tensor-core kernel): gsplits > 0 CTAs per (request, kv head), their partials
+    // in the workspace, combined by the merge kernel launched after them
     int gsplits = 0;
-    float* ws_part = nullptr;     // [B * n_kv][gsplits][16 + 8 * head_dim]
-    int32_t* ws_count = nullptr;  // [B * n_kv], zero between calls
+    float* ws_part = nullptr;  // [B * n_kv][gsplits][16 + 8 * head_dim]
 };
 
 struct AttnPlan {

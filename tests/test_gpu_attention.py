@@ -279,7 +279,7 @@ def _workspace_case(B, ctx, n_head, n_kv, hd):
     torch.cuda.synchronize()
     assert int(err.item()) == 0
     assert torch.equal(a, b)
-    assert int(ws[:4 * B * n_kv].view(torch.int32).abs().sum()) == 0   # counters back at zero
+    assert int(ws[:4 * B * n_kv].view(torch.int32).abs().sum()) == 0   # the leading area is never written
     want = torch.empty_like(q)
     oracle.paged_decode_attention(q, cache, table, seq, want)
     assert_attention_close(a, want, cache, table, seq, f"workspace B={B} ctx={ctx}")
