@@ -43,7 +43,6 @@ namespace cg = cooperative_groups;
 namespace sra {
 namespace lin {
 
-constexpr int kWarps = 4;   // warps of a CTA for 16 rows; 32 or 64 rows take warps_for(MT)
 constexpr int kNT = 64;      // columns of y per CTA
 constexpr int kKT = 64;      // K per W tile
 
@@ -595,8 +594,7 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
     const int kt1 = kt0 + per < KT ? kt0 + per : KT;
     const int ntiles = kt1 - kt0;
     const int64_t kbase = static_cast<int64_t>(kt0) * kKT;
-    float* part = reinterpret_cast<float*>(smem);  // [kTcN rows][kTcM columns], after the ring drains
-    const T* W = static_cast<const T*>(a.W);
+    float* part = reinterpret_cast<float*>(smem);  // the K split's reduction, after the ring drains
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
@@ -666,17 +664,28 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
     __syncthreads();  // every accumulator read is done: the tensor memory can go
     if (warp == 0) tc::dealloc(tmem, kCols);
     cluster.sync();
+    // the K split's sum: each thread 4 adjacent columns of y at a time, every rank's 16-byte
+    // partial requested before the first add (the cluster holds at most 16 ranks)
     T* y = static_cast<T*>(a.y);
-    for (int idx = rank * 128 + threadIdx.x; idx < rows * kTcM; idx += SK * 128) {
-        const int r = idx / kTcM, c = idx - r * kTcM;
-        // every rank's value requested before the first add (the cluster holds at most 16 ranks)
-        float v[16];
+    for (int s4 = rank * 128 + threadIdx.x; s4 < rows * kTcM / 4; s4 += SK * 128) {
+        const int r = (4 * s4) / kTcM, c = 4 * s4 - r * kTcM;
+        float4 v[16];
 #pragma unroll
-        for (int q = 0; q < 16; ++q) v[q] = q < SK ? cluster.map_shared_rank(part, q)[r * kTcM + c] : 0.0f;
-        float sum = 0.0f;
+        for (int q = 0; q < 16; ++q)
+            v[q] = q < SK ? reinterpret_cast<const float4*>(cluster.map_shared_rank(part, q))[s4]
+                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
-        for (int q = 0; q < 16; ++q) sum += v[q];
-        if (n0 + c < a.N) y[r * a.ys + n0 + c] = to_t<T>(sum);
+        for (int q = 0; q < 16; ++q) {
+            sum.x += v[q].x;
+            sum.y += v[q].y;
+            sum.z += v[q].z;
+            sum.w += v[q].w;
+        }
+        const float f[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (n0 + c + e < a.N) y[r * a.ys + n0 + c + e] = to_t<T>(f[e]);
     }
     cluster.sync();
 }
