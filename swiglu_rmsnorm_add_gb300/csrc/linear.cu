@@ -612,6 +612,17 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
     __syncthreads();  // barriers initialised, the tensor-memory address in shared memory
     tc::fence_after();
     const uint32_t tmem = tmem_slot;
+    // The first stages' W tiles are requested before the dependency wait: this kernel runs only
+    // right after the prologue kernel of the same call, which writes h, not W, and which itself
+    // waited for everything before it in the stream before this kernel could start.
+    const int pre = ntiles < S ? ntiles : S;
+    if (warp == 1 && lane == 0) {
+        for (int t = 0; t < pre; ++t) {
+            mbar_arrive_expect_tx(&full[t], static_cast<uint32_t>(SB));
+            tma_load_2d(smem + static_cast<size_t>(t) * SB, &tmW, static_cast<int>(kbase) + t * kKT,
+                        static_cast<int>(n0), &full[t]);
+        }
+    }
     pdl_enter();
 
     // Lanes 1-31 of the producer and MMA warps wait at the warp barrier (not in a poll loop,
@@ -620,12 +631,14 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
         if (lane == 0) {
             for (int t = 0; t < ntiles; ++t) {
                 const int slot = t % S;
-                // the slot's previous stage (t - S) has been read by its MMAs
-                if (t >= S) mbar_wait(&empty[slot], static_cast<uint32_t>(((t / S) - 1) & 1));
                 unsigned char* st = smem + static_cast<size_t>(slot) * SB;
                 const int k0 = static_cast<int>(kbase) + t * kKT;
-                mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(SB));
-                tma_load_2d(st, &tmW, k0, static_cast<int>(n0), &full[slot]);
+                if (t >= pre) {
+                    // the slot's previous stage (t - S) has been read by its MMAs
+                    mbar_wait(&empty[slot], static_cast<uint32_t>(((t / S) - 1) & 1));
+                    mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(SB));
+                    tma_load_2d(st, &tmW, k0, static_cast<int>(n0), &full[slot]);
+                }
                 tma_load_2d(st + tc_wtile_bytes(), &tmX, k0, 0, &full[slot]);
             }
         }
