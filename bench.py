@@ -307,7 +307,7 @@ def build_entries(dev, stream_handle, only=(), companions=False):
                 gu = syn.normal((B, 2 * I), 0.0, 1.0, torch.bfloat16, 1031, 3).to(dev)
                 W = syn.linear_weight(N, I, torch.bfloat16, 1031).to(dev)
                 y = torch.empty(B, N, dtype=torch.bfloat16, device=dev)
-                ws = sra.linear_workspace(B, I, torch.bfloat16, dev)
+                ws = sra.linear_workspace(B, I, torch.bfloat16, dev, N)
                 nbytes = (N * I + B * 2 * I + B * N) * 2
                 entries.append(Entry(name, "linear", nbytes, B, L.sra_glu_linear_ws,
                                      (gu.data_ptr(), W.data_ptr(), y.data_ptr(), B, I, N, 2 * I, N, 0, ws.data_ptr(),

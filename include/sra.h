@@ -408,6 +408,10 @@ SRA_API int sra_glu_linear(const void* gate_up, const void* W, void* y, int64_t 
  * overlaps another argument -> SRA_ERR_ALIAS. Other arguments and errors as
  * sra_rmsnorm_linear / sra_glu_linear. The projection over h runs a warp-specialised
  * kernel: a producer warp streams W and h tiles by TMA, the other warps multiply.
+ * A workspace of sra_linear_workspace_size(B, K, N, dtype) bytes (more than B * K
+ * elements where the tcgen05 projection serves the call: up to 64 rows, N a multiple
+ * of 128) also holds that projection's K-split partials, which it then sums through
+ * L2 rather than through the cluster's shared memory; the result is the same.
  * Calls that share a workspace must not overlap on the GPU.
  */
 SRA_API int sra_rmsnorm_linear_ws(const void* x, const void* w_ln, const void* W, void* y, int64_t B, int64_t K,
@@ -416,6 +420,10 @@ SRA_API int sra_rmsnorm_linear_ws(const void* x, const void* w_ln, const void* W
 SRA_API int sra_glu_linear_ws(const void* gate_up, const void* W, void* y, int64_t B, int64_t I, int64_t N,
                               int64_t in_row_stride, int64_t y_row_stride, int act, void* workspace,
                               int64_t workspace_bytes, int dtype, void* stream);
+/* Bytes of the workspace the _ws projections use best for these sizes (K = I for the GLU
+ * one): B * K elements of `dtype` rounded up to 256 bytes, plus the tcgen05 projection's
+ * partials where it can serve the call. Negative sra_status for bad sizes or dtype. */
+SRA_API int64_t sra_linear_workspace_size(int64_t B, int64_t K, int64_t N, int dtype);
 
 /*
  * sra_uclip — [mer] sec. 0 (DyHT(x) = y * clamp(a x, -1, 1) in place of every

@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
             L.sra_paged_decode_attention_noalloc.argtypes = L.sra_paged_decode_attention.argtypes
             L.sra_paged_decode_attention_workspace_size.argtypes = [i64, i32, i32, i32, i64, i32, i32]
             L.sra_paged_decode_attention_workspace_size.restype = i64
+            L.sra_linear_workspace_size.argtypes = [i64, i64, i64, i32]
+            L.sra_linear_workspace_size.restype = i64
             L.sra_rmsnorm_linear.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, i32, vp]
             L.sra_glu_linear.argtypes = [vp, vp, vp, i64, i64, i64, i64, i64, i32, i32, vp]
             L.sra_rmsnorm_linear_ws.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, i64, f32, vp, i64, i32, vp]
@@ -477,9 +479,17 @@ def _linear_check(x, W, y, B, K, N):
         raise ValueError("x, W and y must share one dtype")
 
 
-def linear_workspace(B: int, K: int, dtype: torch.dtype, device) -> torch.Tensor:
-    """A workspace for rmsnorm_linear / glu_linear with B rows and K (or I) inputs: B * K elements."""
-    return torch.empty(max(1, B * K), dtype=dtype, device=device)
+def linear_workspace(B: int, K: int, dtype: torch.dtype, device, N: int | None = None) -> torch.Tensor:
+    """A workspace for rmsnorm_linear / glu_linear with B rows and K (or I) inputs: B * K elements,
+    or, given the output width N, the size the library uses best (room for the tcgen05
+    projection's partials where it serves the call)."""
+    if N is None:
+        return torch.empty(max(1, B * K), dtype=dtype, device=device)
+    n = lib().sra_linear_workspace_size(B, K, N, DTYPE_CODE[dtype])
+    if n < 0:
+        _check("sra_linear_workspace_size", int(n))
+    es = torch.empty(0, dtype=dtype).element_size()
+    return torch.empty(max(1, -(-int(n) // es)), dtype=dtype, device=device)
 
 
 def _ws_args(ws, x):

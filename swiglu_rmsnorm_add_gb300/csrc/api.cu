@@ -969,7 +969,8 @@ int sra_paged_decode_attention_ws(const void* q, const void* kv_cache, const int
 // ------------------------------------------------------------------- fused linear
 // prologue: 0 RMSNorm, 1 SwiGLU, 2 ReGLU, 3 none (x holds h; internal, from linear_ws)
 static int linear_common(const void* x, const void* w_ln, const void* W, void* y, int64_t B, int64_t K, int64_t N,
-                      int64_t xs, int64_t ys, float eps, int prologue, int dtype, void* stream) {
+                      int64_t xs, int64_t ys, float eps, int prologue, int dtype, void* stream,
+                      float* ws_part = nullptr) {
     if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
     if (B < 0 || K <= 0 || N <= 0) return SRA_ERR_SHAPE;
     const int64_t xw = prologue == 1 || prologue == 2 ? 2 * K : K;
@@ -1063,6 +1064,7 @@ static int linear_common(const void* x, const void* w_ln, const void* W, void* y
     a.xs = xs;
     a.ys = ys;
     a.eps = eps;
+    a.ws_part = plan.tcgen05 ? ws_part : nullptr;
     return status_from(launch_linear(a, plan, dtype, static_cast<cudaStream_t>(stream)));
 }
 
@@ -1097,7 +1099,11 @@ static int linear_ws(const void* x, const void* w_ln, const void* W, void* y, in
     if (!split)
         return linear_common(x, w_ln, W, y, B, K, N, xs, ys, eps, prologue, dtype, stream);
     if (ws_bytes < B * K * es) return SRA_ERR_ARG;
-    const Span sw = span_of(ws, 1, 0, B * K, es);
+    // a workspace with room past h for the tcgen05 projection's partials lets it sum its K split
+    // through L2 instead of the cluster's shared memory
+    const int64_t hb = linear_ws_h_bytes(B, K, es);
+    const bool part = B <= 64 && N % 128 == 0 && ws_bytes >= hb + linear_ws_part_bytes(N);
+    const Span sw = span_of(ws, 1, 0, part ? hb + linear_ws_part_bytes(N) : B * K * es, 1);
     if (overlap(sw, span_of(x, B, xs, xw, es)) || overlap(sw, span_of(W, 1, 0, N * K, es)) ||
         overlap(sw, span_of(y, B, ys, N, es)) || (prologue == 0 && overlap(sw, span_of(w_ln, 1, 0, K, es))))
         return SRA_ERR_ALIAS;
@@ -1113,7 +1119,16 @@ static int linear_ws(const void* x, const void* w_ln, const void* W, void* y, in
     const int st = prologue == 0 ? sra_rmsnorm(x, w_ln, ws, B, K, xs, K, eps, dtype, stream)
                                  : sra_glu(x, ws, B, K, xs, K, prologue - 1, dtype, stream);
     if (st != SRA_OK) return st;
-    return linear_common(ws, nullptr, W, y, B, K, N, K, ys, 0.0f, 3, dtype, stream);
+    return linear_common(ws, nullptr, W, y, B, K, N, K, ys, 0.0f, 3, dtype, stream,
+                         part ? reinterpret_cast<float*>(static_cast<char*>(ws) + hb) : nullptr);
+}
+
+int64_t sra_linear_workspace_size(int64_t B, int64_t K, int64_t N, int dtype) {
+    if (!valid_dtype(dtype)) return SRA_ERR_DTYPE;
+    if (B < 0 || K <= 0 || N <= 0) return SRA_ERR_SHAPE;
+    const int es = elem_bytes(dtype);
+    const int64_t h = linear_ws_h_bytes(B, K, es);
+    return B <= 64 && N % 128 == 0 && dtype != DT_F32 ? h + linear_ws_part_bytes(N) : h;
 }
 
 int sra_rmsnorm_linear_ws(const void* x, const void* w_ln, const void* W, void* y, int64_t B, int64_t K, int64_t N,

@@ -182,7 +182,14 @@ struct LinArgs {
     void* y;           // [B, N], row stride ys
     int64_t B, K, N, xs, ys;
     float eps;
+    // tcgen05 projection: where its K split's fp32 partials go through L2 ([N / 128][16][64][128]
+    // in the caller's workspace), or null to sum them through the cluster's shared memory
+    float* ws_part = nullptr;
 };
+// Workspace of the _ws projections: h [B, K] (rounded up to 256 bytes), then the tcgen05
+// projection's partials where it serves the call.
+inline int64_t linear_ws_h_bytes(int64_t B, int64_t K, int es) { return (B * K * es + 255) / 256 * 256; }
+inline int64_t linear_ws_part_bytes(int64_t N) { return N / 128 * 16 * 64 * 128 * 4; }
 
 struct LinPlan {
     int prologue;       // 0 RMSNorm, 1 SwiGLU, 2 ReGLU, 3 none (the input rows are h)

@@ -664,6 +664,51 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
     __syncwarp();  // the warp-wide accumulator loads below need all 32 lanes together
     tc::fence_after();
 
+    if (a.ws_part) {
+        // ---- epilogue through L2: this CTA's partial [64 rows][128 columns] goes straight from
+        // tensor memory to the workspace (lane = column: each row a coalesced 128-byte store per
+        // warp); after a cluster barrier (release / acquire: the cluster's global stores are
+        // visible to its CTAs) each CTA sums 4 adjacent columns at a time over the cluster's
+        // partials, every rank's 16-byte load issued before the first add
+        float* mine = a.ws_part + (static_cast<int64_t>(blockIdx.x / SK) * SK + rank) * (kTcN * kTcM);
+#pragma unroll
+        for (int c0 = 0; c0 < kTcN; c0 += 16) {
+            uint32_t v[16];
+            tc::ld16(tmem + (static_cast<uint32_t>(32 * warp) << 16) + static_cast<uint32_t>(c0), v);
+            tc::wait_ld();
+#pragma unroll
+            for (int j = 0; j < 16; ++j)
+                if (c0 + j < rows) mine[(c0 + j) * kTcM + 32 * warp + lane] = ntiles > 0 ? __uint_as_float(v[j]) : 0.0f;
+        }
+        tc::fence_before();
+        __syncthreads();
+        if (warp == 0) tc::dealloc(tmem, kCols);
+        cluster.sync();
+        const float* base = a.ws_part + static_cast<int64_t>(blockIdx.x / SK) * SK * (kTcN * kTcM);
+        T* y = static_cast<T*>(a.y);
+        for (int s4 = rank * 128 + threadIdx.x; s4 < rows * kTcM / 4; s4 += SK * 128) {
+            const int r = (4 * s4) / kTcM, c = 4 * s4 - r * kTcM;
+            float4 v[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                v[q] = q < SK ? __ldcg(reinterpret_cast<const float4*>(base + q * (kTcN * kTcM)) + s4)
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+            for (int q = 0; q < 16; ++q) {
+                sum.x += v[q].x;
+                sum.y += v[q].y;
+                sum.z += v[q].z;
+                sum.w += v[q].w;
+            }
+            const float f[4] = {sum.x, sum.y, sum.z, sum.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (n0 + c + e < a.N) y[r * a.ys + n0 + c + e] = to_t<T>(f[e]);
+        }
+        return;
+    }
+
     // ---- epilogue: warp w reads output columns n0 + 32 w + lane, one 16-column (row) group at a time
 #pragma unroll
     for (int c0 = 0; c0 < kTcN; c0 += 16) {

@@ -38,7 +38,8 @@ def test_header_declares_the_api():
     for n in ("sra_rmsnorm", "sra_add_rmsnorm", "sra_rope_kv_store", "sra_rope_kv_store_ex", "sra_glu",
               "sra_swiglu", "sra_uclip", "sra_paged_decode_attention", "sra_rope_kv_store_qk_uclip",
               "sra_rmsnorm_linear", "sra_glu_linear", "sra_paged_decode_attention_ws",
-              "sra_paged_decode_attention_workspace_size", "sra_paged_decode_attention_noalloc"):
+              "sra_paged_decode_attention_workspace_size", "sra_paged_decode_attention_noalloc",
+              "sra_linear_workspace_size"):
         assert n in names
 
 
@@ -238,6 +239,21 @@ def test_linear_workspace_validation(L):
     assert g(X, W, Y, 64, 64, 64, 128, 64, 0, WS, 64 * 64 * 2 - 2, BF16, None) == ARG
     assert g(X, W, Y, 64, 64, 64, 128, 64, 0, X + 128, 1 << 20, BF16, None) == ALIAS
     assert g(X, W, Y, 0, 64, 64, 128, 64, 1, WS, 0, BF16, None) == OK
+
+
+def test_linear_workspace_size(L):
+    f = L.sra_linear_workspace_size
+    f.argtypes = [ctypes.c_int64, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32]
+    f.restype = ctypes.c_int64
+    h = (64 * 8960 * 2 + 255) // 256 * 256
+    # up to 64 rows and N a multiple of 128 (the tcgen05 projection): h, then [N / 128][16][64][128] fp32
+    assert f(64, 8960, 1536, BF16) == h + 1536 // 128 * 16 * 64 * 128 * 4
+    assert f(65, 8960, 1536, BF16) == (65 * 8960 * 2 + 255) // 256 * 256
+    assert f(64, 8960, 1600, BF16) == h
+    assert f(64, 8960, 1536, 0) == (64 * 8960 * 4 + 255) // 256 * 256   # fp32 takes no tensor cores
+    assert f(0, 8960, 1536, BF16) == 1536 // 128 * 16 * 64 * 128 * 4
+    assert f(64, 8960, 1536, 9) == DTYPE
+    assert f(-1, 8960, 1536, BF16) == SHAPE
 
 
 def test_attention_workspace_validation(L):

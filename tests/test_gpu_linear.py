@@ -219,11 +219,12 @@ def test_norm_rows_beyond_the_fp32_sum_range(eps, dtype, B, K, N, ws):
     assert_linear_close(got, want, h, W, f"norm range {dtype} B={B} K={K} eps={eps} ws={ws}")
 
 
-def _tc_case(prologue, dtype, B, K, N, seed, force=1):
+def _tc_case(prologue, dtype, B, K, N, seed, force=1, l2=False):
     """The workspace path with its projection forced onto the tcgen05 kernel (`force`: the
-    variant word, K splits and ring depth included)."""
+    variant word, K splits and ring depth included); with `l2`, a workspace large enough for
+    the K split's partials, which are then summed through L2."""
     W = syn.linear_weight(N, K, dtype, seed)
-    wsp = sra.linear_workspace(B, K, dtype, DEV)
+    wsp = sra.linear_workspace(B, K, dtype, DEV, N if l2 else None)
     sra.force_variant("linear", force)
     try:
         if prologue == "rmsnorm":
@@ -264,6 +265,25 @@ def test_tcgen05_projection(dtype, prologue, B, K, N):
     assert_linear_close(got, want, h, W, f"tcgen05 {prologue} {dtype} B={B} K={K} N={N}")
 
 
+@pytest.mark.parametrize("l2", [False, True])
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("prologue,B,K,N", [
+    ("rmsnorm", 32, 64, 128),
+    ("rmsnorm", 33, 640, 256),
+    ("silu", 64, 8960, 1536),
+    ("relu", 48, 1024, 384),
+    ("silu", 40, 4160, 640),
+])
+def test_tcgen05_projection_partials_through_l2(dtype, prologue, B, K, N, l2):
+    """The K split summed through the cluster's shared memory (a workspace of B * K elements)
+    and through L2 (the size sra_linear_workspace_size gives): both against the oracle."""
+    before = sra.wait_timeouts()
+    got, want, h, W = _tc_case(prologue, dtype, B, K, N, 1070 + K + B, l2=l2)
+    torch.cuda.synchronize()
+    assert sra.wait_timeouts() == before
+    assert_linear_close(got, want, h, W, f"tcgen05 l2={l2} {prologue} {dtype} B={B} K={K} N={N}")
+
+
 @pytest.mark.parametrize("stages", [4, 8])
 @pytest.mark.parametrize("splits", [1, 3, 5, 12, 16])
 @pytest.mark.parametrize("prologue,B,K,N", [("silu", 64, 8960, 1536), ("rmsnorm", 33, 1280, 256)])
@@ -273,7 +293,7 @@ def test_tcgen05_ring_depth_and_splits(prologue, B, K, N, splits, stages):
     before = sra.wait_timeouts()
     try:
         got, want, h, W = _tc_case(prologue, torch.bfloat16, B, K, N, 1062 + splits,
-                                   force=1 | (splits << 8) | (stages << 16))
+                                   force=1 | (splits << 8) | (stages << 16), l2=splits % 2 == 1)
     except sra.SRAError:
         if splits <= 8:
             raise
