@@ -295,7 +295,7 @@ def build_entries(dev, stream_handle, only=(), companions=False):
                 w = syn.normal((K,), 1.0, 0.1, torch.bfloat16, 1030, 2).to(dev)
                 W = syn.linear_weight(N, K, torch.bfloat16, 1030).to(dev)
                 y = torch.empty(B, N, dtype=torch.bfloat16, device=dev)
-                ws = sra.linear_workspace(B, K, torch.bfloat16, dev)
+                ws = sra.linear_workspace(B, K, torch.bfloat16, dev, N)
                 nbytes = (N * K + B * K + K + B * N) * 2
                 entries.append(Entry(name, "linear", nbytes, B, L.sra_rmsnorm_linear_ws,
                                      (x.data_ptr(), w.data_ptr(), W.data_ptr(), y.data_ptr(), B, K, N, K, N, syn.EPS,

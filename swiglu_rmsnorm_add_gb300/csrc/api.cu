@@ -1007,7 +1007,9 @@ static int linear_common(const void* x, const void* w_ln, const void* W, void* y
     // sra_force_variant("linear", 0 or 1) overrides it
     const int lin_all = g_force_lin.load(std::memory_order_relaxed);
     const int lin_forced = lin_all < 0 ? -1 : (lin_all & 0xFF);  // bits 8-15: K splits (A/B only)
-    const bool tc_wanted = lin_forced == 1 || (lin_forced < 0 && K >= 4096);
+    // (measured at batch 64: from K = 4096 up always; from K = 1024 up when the partials go through
+    // L2, e.g. ln1 + qkv_proj [1536 -> 2048] 8.5 -> 7.6 us)
+    const bool tc_wanted = lin_forced == 1 || (lin_forced < 0 && (K >= 4096 || (ws_part && K >= 1024)));
     if (plan.tensor_cores && prologue == 3 && B <= 64 && N % 128 == 0 && tc_wanted &&
         static_cast<int64_t>(linear_tc_smem(4)) <= limit) {
         plan.tcgen05 = true;
