@@ -514,7 +514,9 @@ SRA_API int sra_set_pdl(int enable);
  * projection of the _ws entry points once the prologue has run: 0 = mma.sync
  * kernels, 1 = the tcgen05 kernel, for up to 64 rows and N a multiple of 128;
  * OR-ed with (s << 8), s in 1..16, it also forces the tcgen05 kernel's K splits, and
- * with (r << 16), r = 4 or 8, its ring depth in stages).
+ * with (r << 16), r = 4 or 8, its ring depth in stages), "linear_narrow" (the
+ * decode-batch projection kernel of the fused entry points, up to 16 rows: variant 0,
+ * OR-ed with (s << 8), s in 1..8, forces the CTAs of its cluster along K).
  * variant: -1 = automatic per-shape choice (the default); otherwise an index
  * < sra_variant_count(op), optionally OR-ed with (nv << 8) to also force the
  * number of 16-byte accesses each thread holds in the register variants of
@@ -535,7 +537,8 @@ SRA_API const char* sra_variant_name(const char* op, int variant);
  * (num_sms <= 0: query the current device). rmsnorm: a = rows, b = D;
  * rope_kv_store: a = T, b = n_head, c = n_kv_head, d = head_dim; glu: a = T, b = I,
  * c = act (0 = SiLU, 1 = ReLU);
- * decode_attention: a = B, b = n_head, c = n_kv_head, d = head_dim.
+ * decode_attention: a = B, b = n_head, c = n_kv_head, d = head_dim ("linear" and
+ * "linear_narrow" have no pick: SRA_ERR_ARG).
  * Negative sra_status on bad arguments. Enqueues nothing.
  */
 SRA_API int sra_pick_variant(const char* op, int64_t a, int64_t b, int64_t c, int64_t d, int dtype,

@@ -18,7 +18,8 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_smem_optin[kMaxDevices];
-std::atomic<int> g_force_norm{-1}, g_force_rope{-1}, g_force_glu{-1}, g_force_attn{-1}, g_force_lin{-1};
+std::atomic<int> g_force_norm{-1}, g_force_rope{-1}, g_force_glu{-1}, g_force_attn{-1}, g_force_lin{-1},
+    g_force_narrow{-1};
 thread_local bool g_pdl = false;  // programmatic dependent launch for this thread's calls
 thread_local int g_force_nv = 0;  // accesses per thread forced for A/B measurement (0 = planner's)
 thread_local int g_force_g = 0;   // warps per row forced for warps_row A/B measurement (0 = planner's)
@@ -546,6 +547,7 @@ std::atomic<int>* force_slot(const char* op) {
     if (std::strcmp(op, "glu") == 0) return &g_force_glu;
     if (std::strcmp(op, "decode_attention") == 0) return &g_force_attn;
     if (std::strcmp(op, "linear") == 0) return &g_force_lin;
+    if (std::strcmp(op, "linear_narrow") == 0) return &g_force_narrow;
     return nullptr;
 }
 
@@ -556,6 +558,7 @@ int variant_count(const char* op) {
     if (std::strcmp(op, "glu") == 0) return GLU_NUM_VARIANTS;
     if (std::strcmp(op, "decode_attention") == 0) return 3;  // CUDA cores, mma.sync, mma.sync fed by TMA
     if (std::strcmp(op, "linear") == 0) return 2;            // mma.sync, tcgen05 (projection over h)
+    if (std::strcmp(op, "linear_narrow") == 0) return 1;     // the decode-batch kernel (K split forced)
     return SRA_ERR_ARG;
 }
 
@@ -996,10 +999,23 @@ static int linear_common(const void* x, const void* w_ln, const void* W, void* y
     plan.narrow = false;
     plan.splits = 1;
     plan.tcgen05 = false;
-    // decode batches: 16-column CTAs over all of K, no cluster, when the B rows of h for all of
-    // K fit in shared memory beside the W rings
+    // decode batches: 16-column CTAs over all of K, when the B rows of h for all of K fit in
+    // shared memory beside the W rings. (The kernel can also split K over a cluster of up to 8
+    // CTAs, forced only: measured slower at every split count, e.g. SwiGLU + down_proj
+    // [8960 -> 1536] at batch 1 8.3 us unsplit against 9.5-16.2 us split 2-8 ways.)
     plan.narrow = plan.tensor_cores && B <= 16 &&
-                  static_cast<int64_t>(linear16_smem(static_cast<int>(B), K)) <= std::min<int64_t>(limit, 200 * 1024);
+                  static_cast<int64_t>(linear16_smem(static_cast<int>(B), K, 1)) <= std::min<int64_t>(limit, 200 * 1024);
+    if (plan.narrow) {
+        const int64_t KT = K / 64;
+        const int nf = g_force_narrow.load(std::memory_order_relaxed);
+        if (nf >= 0) {
+            const int fs = (nf >> 8) & 0xFF;  // variant 0; bits 8-15: the cluster's K split (1..8)
+            if (fs) {
+                if (fs > 8 || fs > KT) return SRA_ERR_VARIANT;
+                plan.splits = fs;
+            }
+        }
+    }
     // the projection of h (the workspace path) on tcgen05: up to 64 rows, 128-column slices.
     // Chosen from K = 4096 up (measured on GB300 at batch 64: SwiGLU + down_proj [8960 -> 1536]
     // 14.3 against 18.1 us with mma.sync; ln1 + qkv_proj [1536 -> 2048] 10.9 against 8.5 us,
@@ -1221,12 +1237,14 @@ const char* sra_variant_name(const char* op, int variant) {
     static const char* const glu_names[] = {"cols_rows", "cols_rows_regs"};
     static const char* const attn_names[] = {"cuda_cores", "mma_sync", "mma_sync_tma"};
     static const char* const lin_names[] = {"mma_sync", "tcgen05"};
+    static const char* const narrow_names[] = {"cluster_k_split"};
     const int n = variant_count(op);
     if (n < 0 || variant < 0 || variant >= n) return nullptr;
     if (std::strcmp(op, "rmsnorm") == 0) return norm_names[variant];
     if (std::strcmp(op, "rope_kv_store") == 0) return rope_names[variant];
     if (std::strcmp(op, "decode_attention") == 0) return attn_names[variant];
     if (std::strcmp(op, "linear") == 0) return lin_names[variant];
+    if (std::strcmp(op, "linear_narrow") == 0) return narrow_names[variant];
     return glu_names[variant];
 }
 
@@ -1259,6 +1277,7 @@ int sra_pick_variant(const char* op, int64_t a, int64_t b, int64_t c, int64_t d,
             return SRA_ERR_SHAPE;
         return dtype != DT_F32 && d <= 128 ? 1 : 0;
     }
+    if (std::strcmp(op, "glu") != 0) return SRA_ERR_ARG;  // the projections' plans depend on more than four sizes
     if (a < 0 || b <= 0) return SRA_ERR_SHAPE;
     GluPlan p;
     const int st = plan_glu(a, b, 16 / es, c == 1 ? 1 : 0, num_sms, &p);

@@ -208,7 +208,7 @@ size_t linear_tc_smem(int stages);
 int linear_tc_max_clusters(int splits, int stages, bool bf16);
 unsigned int linear_wait_timeouts();  // bounded waits of the fused-projection kernel that ran out
 cudaError_t launch_wait_selftest(int32_t* out, cudaStream_t s);  // a wait on a barrier nothing completes
-size_t linear16_smem(int rows, int64_t K);
+size_t linear16_smem(int rows, int64_t K, int splits);
 
 // ------------------------------------------------------------------- UClip
 struct UclipArgs {

@@ -748,12 +748,14 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
     cluster.sync();
 }
 
-// ---- decode batches: a CTA owns 16 columns of y over the whole of K; its eight warps
-// split K between them (each streaming its own W tiles through a private cp.async ring)
-// and meet only at the end, in shared memory: no cluster, no exchange. h for all of K
-// is built once, up front, while the first W tiles are in flight: the RMSNorm
-// normalises the full rows itself (B x K values), the GLU activates them. Only the B
-// real rows are stored; the A fragments of the padding rows read one zero row.
+// ---- decode batches: a cluster of SK CTAs owns 16 columns of y, each CTA a 1 / SK slice of
+// K (SK = 1: the whole of K, no cluster); a CTA's eight warps split its slice between them
+// (each streaming its own W tiles through a private cp.async ring) and meet at the end in
+// shared memory, and the cluster's CTAs then sum their slices' partials through distributed
+// shared memory. h for the CTA's slice of K is built once, up front, while the first W tiles
+// are in flight: the RMSNorm takes each row's norm over the full row itself (B x K values),
+// the GLU activates the slice. Only the B real rows are stored; the A fragments of the
+// padding rows read one zero row.
 constexpr int kNW16 = 8;       // warps
 constexpr int kStages16 = 6;   // W tiles in flight per warp
 constexpr int kTile16 = 16 * kKT;  // elements of a W tile (16 columns x 64 of K)
@@ -763,8 +765,10 @@ __host__ __device__ inline size_t ring16_bytes() {
     const size_t part = static_cast<size_t>(kNW16) * 16 * 16 * 4;
     return ring > part ? ring : part;
 }
-__host__ __device__ inline size_t smem16_bytes(int rows, int64_t K) {
-    return ring16_bytes() + static_cast<size_t>(rows + 1) * K * 2 + 2 * 64 * 4;
+// K elements of h one CTA of an SK-CTA cluster holds (its slice of K tiles, rounded up)
+__host__ __device__ inline int64_t kslice16(int64_t K, int SK) { return (K / kKT + SK - 1) / SK * kKT; }
+__host__ __device__ inline size_t smem16_bytes(int rows, int64_t K, int SK) {
+    return ring16_bytes() + static_cast<size_t>(rows + 1) * kslice16(K, SK) * 2 + 2 * 64 * 4;
 }
 
 template <typename T, int PRO>
@@ -772,15 +776,25 @@ __global__ void __launch_bounds__(kNW16 * 32) linear16_kernel(LinArgs a) {
     using V8 = Vec<T, 8>;
     using R8 = typename V8::Raw;
     extern __shared__ __align__(16) unsigned char smem[];
+    cg::cluster_group cluster = cg::this_cluster();
+    const int SK = static_cast<int>(cluster.num_blocks());
+    const int rank = static_cast<int>(cluster.block_rank());
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int64_t n0 = static_cast<int64_t>(blockIdx.x) * 16;
+    const int64_t n0 = static_cast<int64_t>(blockIdx.x / SK) * 16;
     const int rows = static_cast<int>(a.B < 16 ? a.B : 16);
-    const int KT = static_cast<int>(a.K / kKT);
+    // this CTA's slice of K: tiles [kt0, kt0 + KT), h columns [kb, kb + KL)
+    const int KTall = static_cast<int>(a.K / kKT);
+    const int per = (KTall + SK - 1) / SK;
+    const int kt0 = rank * per < KTall ? rank * per : KTall;
+    const int KT = (kt0 + per < KTall ? kt0 + per : KTall) - kt0;
+    const int64_t kb = static_cast<int64_t>(kt0) * kKT, KL = static_cast<int64_t>(KT) * kKT;
+    const int64_t HS = kslice16(a.K, SK);  // row stride of h in shared memory
     T* ring = reinterpret_cast<T*>(smem) + static_cast<size_t>(warp) * kStages16 * kTile16;
     float* part = reinterpret_cast<float*>(smem);  // [warps][16][16], after the rings drain
-    T* hsm = reinterpret_cast<T*>(smem + ring16_bytes());  // [rows][K], then one zero row
-    T* zrow = hsm + static_cast<int64_t>(rows) * a.K;
-    float* inv = reinterpret_cast<float*>(smem + ring16_bytes() + static_cast<size_t>(rows + 1) * a.K * 2);
+    float* csum = part + kNW16 * 256;              // [16][16] this CTA's sum, for the cluster
+    T* hsm = reinterpret_cast<T*>(smem + ring16_bytes());  // [rows][HS], then one zero row
+    T* zrow = hsm + static_cast<int64_t>(rows) * HS;
+    float* inv = reinterpret_cast<float*>(smem + ring16_bytes() + static_cast<size_t>(rows + 1) * HS * 2);
     float* pre = inv + 64;  // RMSNorm rows past fp32's sum range: a power-of-two pre-scale
     const T* W = static_cast<const T*>(a.W);
     const T* X = static_cast<const T*>(a.x);
@@ -789,26 +803,34 @@ __global__ void __launch_bounds__(kNW16 * 32) linear16_kernel(LinArgs a) {
     auto issue = [&](int j) {
         const int t = warp + j * kNW16;
         T* dst = ring + static_cast<size_t>(j % kStages16) * kTile16;
-        const T* src = W + n0 * a.K + static_cast<int64_t>(t) * kKT;
+        const T* src = W + n0 * a.K + kb + static_cast<int64_t>(t) * kKT;
 #pragma unroll
         for (int c = lane; c < 16 * 8; c += 32) {
             const int r = c >> 3, ch = c & 7;
             cp_async16(dst + r * kKT + swz(r, ch) * 8, src + static_cast<int64_t>(r) * a.K + ch * 8);
         }
     };
-    // Before the dependency wait: this CTA's 16 rows of W and the prologue's input rows
-    // into L2 (hints only; both are read again after the wait).
-    if (threadIdx.x < 16)
-        prefetch_l2(W + (n0 + threadIdx.x) * a.K, a.K * 2);
-    else if (threadIdx.x >= 32 && threadIdx.x - 32 < rows)
-        prefetch_l2(X + (threadIdx.x - 32) * a.xs, (PRO == 0 ? 1 : 2) * a.K * 2);
+    // Before the dependency wait: this CTA's slice of its 16 rows of W and the prologue's input
+    // (whole rows for the RMSNorm's norms, the slice of gate and up for the GLU) into L2 (hints
+    // only; both are read again after the wait).
+    if (threadIdx.x < 16) {
+        prefetch_l2(W + (n0 + threadIdx.x) * a.K + kb, KL * 2);
+    } else if (threadIdx.x >= 32 && threadIdx.x - 32 < rows) {
+        const T* xr = X + (threadIdx.x - 32) * a.xs;
+        if (PRO == 0) {
+            prefetch_l2(xr, a.K * 2);
+        } else {
+            prefetch_l2(xr + kb, KL * 2);
+            prefetch_l2(xr + a.K + kb, KL * 2);
+        }
+    }
     pdl_enter();
     for (int j = 0; j < kStages16 - 1; ++j) {
         if (j < mine) issue(j);
         cp_async_commit();
     }
 
-    const int cpr = static_cast<int>(a.K / 8);
+    const int cpr = static_cast<int>(KL / 8);  // 16-byte chunks of a row's slice
     for (int c = threadIdx.x; c < cpr; c += kNW16 * 32) reinterpret_cast<uint4*>(zrow)[c] = make_uint4(0, 0, 0, 0);
     if constexpr (PRO == 0) {
         // full-row sums of squares: a warp per row, four 16-byte loads per lane in flight
@@ -847,7 +869,7 @@ __global__ void __launch_bounds__(kNW16 * 32) linear16_kernel(LinArgs a) {
         }
         __syncthreads();
     }
-    // h for all of K: thread chunks c = tid + 256 u, the inputs of HB chunks loaded together
+    // h for the slice: thread chunks c = tid + 256 u, the inputs of HB chunks loaded together
     constexpr int HB = 8;
     const int total = rows * cpr;
     for (int c0 = threadIdx.x; c0 < total; c0 += HB * kNW16 * 32) {
@@ -857,9 +879,9 @@ __global__ void __launch_bounds__(kNW16 * 32) linear16_kernel(LinArgs a) {
             const int c = c0 + u * kNW16 * 32;
             if (c < total) {
                 const int r = c / cpr, ch = c - r * cpr;
-                const T* xr = X + r * a.xs + ch * 8;
+                const T* xr = X + r * a.xs + kb + ch * 8;
                 xv[u] = V8::load(xr);
-                gv[u] = PRO == 0 ? V8::load(static_cast<const T*>(a.w_ln) + ch * 8) : V8::load(xr + a.K);
+                gv[u] = PRO == 0 ? V8::load(static_cast<const T*>(a.w_ln) + kb + ch * 8) : V8::load(xr + a.K);
             }
         }
 #pragma unroll
@@ -871,8 +893,8 @@ __global__ void __launch_bounds__(kNW16 * 32) linear16_kernel(LinArgs a) {
                     // a chunk holding a gate below -64 (never on the configured inputs): each
                     // element through glu_mul, scalar, re-read from x
                     if (__builtin_expect(needs_careful<T, 8>(xv[u]), 0)) {
-                        const T* xr = X + r * a.xs + ch * 8;
-                        T* hp = hsm + static_cast<int64_t>(r) * a.K + swz(r, ch) * 8;
+                        const T* xr = X + r * a.xs + kb + ch * 8;
+                        T* hp = hsm + static_cast<int64_t>(r) * HS + swz(r, ch) * 8;
 #pragma unroll 1
                         for (int e = 0; e < 8; ++e) hp[e] = to_t<T>(glu_mul<0>(to_f32(xr[e]), to_f32(xr[e + a.K])));
                         continue;
@@ -889,7 +911,7 @@ __global__ void __launch_bounds__(kNW16 * 32) linear16_kernel(LinArgs a) {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) f[e] = glu_mul_fast<PRO - 1>(f[e], g[e]);
                 }
-                *reinterpret_cast<R8*>(hsm + static_cast<int64_t>(r) * a.K + swz(r, ch) * 8) = V8::pack(f);
+                *reinterpret_cast<R8*>(hsm + static_cast<int64_t>(r) * HS + swz(r, ch) * 8) = V8::pack(f);
             }
         }
     }
@@ -898,7 +920,7 @@ __global__ void __launch_bounds__(kNW16 * 32) linear16_kernel(LinArgs a) {
     float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     const int li = lane & 7, lm = lane >> 3;
     const int ar = (lm & 1) * 8 + li;  // this lane's A row in ldmatrix
-    const T* arow = ar < rows ? hsm + static_cast<int64_t>(ar) * a.K : zrow;
+    const T* arow = ar < rows ? hsm + static_cast<int64_t>(ar) * HS : zrow;
     for (int j = 0; j < mine; ++j) {
         const int t = warp + j * kNW16;
         cp_async_wait<kStages16 - 2>();
@@ -936,18 +958,32 @@ __global__ void __launch_bounds__(kNW16 * 32) linear16_kernel(LinArgs a) {
         float sum = 0.0f;
 #pragma unroll
         for (int w = 0; w < kNW16; ++w) sum += part[w * 256 + idx];
+        if (SK == 1)
+            y[(idx >> 4) * a.ys + n0 + (idx & 15)] = to_t<T>(sum);
+        else
+            csum[idx] = sum;
+    }
+    if (SK == 1) return;
+    // the cluster's slices of K: each CTA sums every SK-th output over the ranks, in rank order
+    cluster.sync();
+    for (int idx = rank + SK * static_cast<int>(threadIdx.x); idx < rows * 16; idx += SK * kNW16 * 32) {
+        float sum = 0.0f;
+        for (int q = 0; q < SK; ++q) sum += cluster.map_shared_rank(csum, q)[idx];
         y[(idx >> 4) * a.ys + n0 + (idx & 15)] = to_t<T>(sum);
     }
+    cluster.sync();  // every CTA's sums have been read
 }
 
 template <typename T, int PRO>
 cudaError_t launch16(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
     auto kernel = linear16_kernel<T, PRO>;
-    const size_t smem = smem16_bytes(static_cast<int>(a.B < 16 ? a.B : 16), a.K);
+    const int SK = p.splits;  // CTAs of a cluster along K
+    const size_t smem = smem16_bytes(static_cast<int>(a.B < 16 ? a.B : 16), a.K, SK);
     const cudaError_t e =
         cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    return launch_kernel(kernel, dim3(static_cast<unsigned>(a.N / 16)), dim3(kNW16 * 32), smem, s, p.pdl, 1, a);
+    return launch_kernel(kernel, dim3(static_cast<unsigned>(a.N / 16 * SK)), dim3(kNW16 * 32), smem, s, p.pdl, SK,
+                         a);
 }
 
 template <typename T, int MT, int PRO>
@@ -1211,7 +1247,7 @@ unsigned int linear_wait_timeouts() {
 size_t linear_smem(int mt, int prologue) {
     return prologue == 3 ? lin::smemh_bytes(mt) : lin::smem_bytes(mt, prologue);
 }
-size_t linear16_smem(int rows, int64_t K) { return lin::smem16_bytes(rows, K); }
+size_t linear16_smem(int rows, int64_t K, int splits) { return lin::smem16_bytes(rows, K, splits); }
 size_t linear_tc_smem(int stages) { return lin::tc_smem_bytes(stages); }
 
 // Clusters of `splits` CTAs of the tcgen05 projection (ring of `stages`) the device can hold at once.

@@ -338,6 +338,8 @@ def test_variant_control(L):
     assert sra.variant_count("rope_kv_store") == 2
     assert sra.variant_count("glu") == 2
     assert [sra.variant_name("glu", i) for i in range(2)] == ["cols_rows", "cols_rows_regs"]
+    assert sra.variant_count("linear_narrow") == 1
+    assert sra.variant_name("linear_narrow", 0) == "cluster_k_split"
     assert sra.variant_count("decode_attention") == 3
     assert [sra.variant_name("decode_attention", i) for i in range(3)] == ["cuda_cores", "mma_sync", "mma_sync_tma"]
     assert sra.variant_count("linear") == 2

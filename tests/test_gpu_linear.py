@@ -71,6 +71,25 @@ def glu_case(B, I, N, dtype, seed, act="silu", rows=None, ws=False):
     return got[sel], want, h, W
 
 
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 8])
+@pytest.mark.parametrize("case", ["norm", "silu", "relu"])
+@pytest.mark.parametrize("B", [1, 5, 16])
+def test_decode_batch_kernel_k_split(case, B, splits):
+    """The decode-batch projection kernel with its K split over clusters of 1-8 CTAs forced
+    (K = 1664: 26 tiles, so 3, 5 and 8 leave ragged slices; the RMSNorm rows still take their
+    norm over the whole row): against the oracle, and the same bytes for every split count up to
+    the fp32 sum's order."""
+    sra.force_variant("linear_narrow", splits << 8)
+    try:
+        if case == "norm":
+            got, want, h, W = norm_case(B, 1664, 384, torch.bfloat16, 1080 + B)
+        else:
+            got, want, h, W = glu_case(B, 1664, 384, torch.bfloat16, 1080 + B, act=case)
+    finally:
+        sra.force_variant("linear_narrow", -1)
+    assert_linear_close(got, want, h, W, f"narrow {case} B={B} splits={splits}")
+
+
 @pytest.mark.parametrize("B", syn.LINEAR_B)
 def test_config_qwen25_ln1_qkv(B):
     got, want, h, W = norm_case(B, syn.QWEN25_QKV["K"], syn.QWEN25_QKV["N"], torch.bfloat16, 1030)
