@@ -105,7 +105,6 @@ bool rows_overlap(const void* p1, int64_t rows1, int64_t s1, int64_t w1, const v
     return dm < W1 || dm + W2 > S;
 }
 
-int ceil_div_i(int64_t a, int64_t b) { return static_cast<int>((a + b - 1) / b); }
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int round_up32(int64_t v) { return static_cast<int>(((v + 31) / 32) * 32); }
 
@@ -1056,6 +1055,24 @@ static int linear_common(const void* x, const void* w_ln, const void* W, void* y
         }
     } else if (lin_forced == 1 && prologue == 3) {
         return SRA_ERR_VARIANT;
+    }
+    // the GLU fused into the tcgen05 projection (no workspace, one launch): from 17 to 64 rows
+    // (or forced onto it, from 1 row), N a multiple of 128; 3 stages of 32 KB, two CTAs per SM
+    if (plan.tensor_cores && (prologue == 1 || prologue == 2) && B <= 64 && N % 128 == 0 &&
+        (lin_forced == 1 || (lin_forced < 0 && B > 16)) && static_cast<int64_t>(linear_tc_smem(3, 1)) <= limit) {
+        plan.tcgen05 = true;
+        plan.narrow = false;
+        const int64_t slices = N / 128, KT = K / 64;
+        plan.splits = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>({16, 2 * sms / slices, KT / 4})));
+        const int fs = lin_all < 0 ? 0 : (lin_all >> 8) & 0xFF;
+        if (fs) {
+            if (fs > 16 || fs > KT) return SRA_ERR_VARIANT;
+            plan.splits = fs;
+        }
+        while (plan.splits > 1 && linear_tc_max_clusters(plan.splits, 3, dtype == DT_BF16, 1) < 1) {
+            if (fs) return SRA_ERR_VARIANT;
+            --plan.splits;
+        }
     }
     if (plan.tensor_cores && !plan.narrow && !plan.tcgen05) {
         // 64-column slices x row blocks x K splits (a cluster); two CTAs per SM fit (45 to 113 KB

@@ -566,21 +566,30 @@ constexpr int kTcN = 64;     // rows of h (at most): the MMA's N
 // with about twice the bytes in flight).
 __host__ __device__ constexpr size_t tc_wtile_bytes() { return static_cast<size_t>(kTcM) * kKT * 2; }
 __host__ __device__ constexpr size_t tc_htile_bytes() { return static_cast<size_t>(kTcN) * kKT * 2; }
-__host__ __device__ constexpr size_t tc_smem_bytes(int stages) {
-    return 1024 + (stages * (tc_wtile_bytes() + tc_htile_bytes()) > static_cast<size_t>(kTcN) * kTcM * 4
-                       ? stages * (tc_wtile_bytes() + tc_htile_bytes())
+// A stage: the W tile, then h's tile (prologue 3), or the gate and up tiles the activation warps
+// turn into h's tile in place (prologue 1 / 2: the GLU fused into the projection).
+__host__ __device__ constexpr size_t tc_stage_bytes(int pro) {
+    return tc_wtile_bytes() + (pro == 3 ? 1 : 2) * tc_htile_bytes();
+}
+__host__ __device__ constexpr size_t tc_smem_bytes(int stages, int pro = 3) {
+    return 1024 + (stages * tc_stage_bytes(pro) > static_cast<size_t>(kTcN) * kTcM * 4
+                       ? stages * tc_stage_bytes(pro)
                        : static_cast<size_t>(kTcN) * kTcM * 4);
 }
 
-template <typename T, int S>
+// PRO 3: h comes from the workspace (its own prologue kernel ran before). PRO 1 / 2: the GLU
+// (SwiGLU / ReGLU) is fused: each stage brings the gate and up tiles of this CTA's K range, warps
+// 2 and 3 turn them into h's tile in place (the same 128-byte swizzle, so the element-wise
+// product needs no index arithmetic) and release it to the MMA thread on a barrier of its own.
+template <typename T, int S, int PRO>
 __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_constant__ CUtensorMap tmW,
                                                         const __grid_constant__ CUtensorMap tmX) {
-    constexpr size_t SB = tc_wtile_bytes() + tc_htile_bytes();
+    constexpr size_t SB = tc_stage_bytes(PRO);
     constexpr uint32_t kCols = 64;  // tensor-memory columns: one fp32 accumulator column per row of h
     constexpr uint32_t IDESC = tc::idesc_f16(std::is_same<T, __nv_bfloat16>::value, kTcM, kTcN);
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    __shared__ uint64_t full[S], empty[S], accb;
+    __shared__ uint64_t full[S], empty[S], hready[S], accb;
     __shared__ uint32_t tmem_slot;
     cg::cluster_group cluster = cg::this_cluster();
     const int SK = static_cast<int>(cluster.num_blocks());
@@ -599,6 +608,7 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
+            mbar_init(&hready[i], 2);  // the two activation warps (prologue 1 / 2)
         }
         mbar_init(&accb, 1);
         mbar_init_fence();
@@ -612,10 +622,11 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
     __syncthreads();  // barriers initialised, the tensor-memory address in shared memory
     tc::fence_after();
     const uint32_t tmem = tmem_slot;
-    // The first stages' W tiles are requested before the dependency wait: this kernel runs only
-    // right after the prologue kernel of the same call, which writes h, not W, and which itself
-    // waited for everything before it in the stream before this kernel could start.
-    const int pre = ntiles < S ? ntiles : S;
+    // With h from the workspace, the first stages' W tiles are requested before the dependency
+    // wait: that kernel runs only right after the prologue kernel of the same call, which writes
+    // h, not W, and which itself waited for everything before it in the stream before this kernel
+    // could start. (The fused GLU follows whatever the caller ran before: nothing early.)
+    const int pre = PRO != 3 ? 0 : (ntiles < S ? ntiles : S);
     if (warp == 1 && lane == 0) {
         for (int t = 0; t < pre; ++t) {
             mbar_arrive_expect_tx(&full[t], static_cast<uint32_t>(SB));
@@ -635,11 +646,13 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
                 const int k0 = static_cast<int>(kbase) + t * kKT;
                 if (t >= pre) {
                     // the slot's previous stage (t - S) has been read by its MMAs
-                    mbar_wait(&empty[slot], static_cast<uint32_t>(((t / S) - 1) & 1));
+                    if (t >= S) mbar_wait(&empty[slot], static_cast<uint32_t>(((t / S) - 1) & 1));
                     mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(SB));
                     tma_load_2d(st, &tmW, k0, static_cast<int>(n0), &full[slot]);
                 }
                 tma_load_2d(st + tc_wtile_bytes(), &tmX, k0, 0, &full[slot]);
+                if (PRO != 3) tma_load_2d(st + tc_wtile_bytes() + tc_htile_bytes(), &tmX, static_cast<int>(a.K) + k0, 0,
+                                          &full[slot]);
             }
         }
         __syncwarp();
@@ -647,7 +660,7 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
         if (lane == 0) {
             for (int t = 0; t < ntiles; ++t) {
                 const int slot = t % S;
-                mbar_wait(&full[slot], static_cast<uint32_t>((t / S) & 1));
+                mbar_wait(PRO == 3 ? &full[slot] : &hready[slot], static_cast<uint32_t>((t / S) & 1));
                 tc::fence_after();
                 const unsigned char* st = smem + static_cast<size_t>(slot) * SB;
 #pragma unroll
@@ -659,6 +672,38 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
             tc::commit(&accb);  // the accumulator is complete once every MMA above has
         }
         __syncwarp();
+    } else if (PRO != 3) {
+        // activation warps 2 and 3: h = act(gate) * up over each stage's [64 rows][64] tiles, in
+        // place of the gate tile; a chunk holding a gate below -64 (never on the configured
+        // inputs) goes through glu_mul element by element
+        using V8 = Vec<T, 8>;
+        using R8 = typename V8::Raw;
+        const int at = threadIdx.x - 64;
+        for (int t = 0; t < ntiles; ++t) {
+            const int slot = t % S;
+            mbar_wait(&full[slot], static_cast<uint32_t>((t / S) & 1));
+            unsigned char* st = smem + static_cast<size_t>(slot) * SB + tc_wtile_bytes();
+            R8* gt = reinterpret_cast<R8*>(st);
+            const R8* ut = reinterpret_cast<const R8*>(st + tc_htile_bytes());
+#pragma unroll 4
+            for (int q = at; q < static_cast<int>(tc_htile_bytes() / 16); q += 64) {
+                const R8 gv = gt[q], uv = ut[q];
+                float g[8], u[8];
+                V8::unpack(gv, g);
+                V8::unpack(uv, u);
+                if (PRO == 1 && needs_careful<T, 8>(gv)) {
+#pragma unroll 1
+                    for (int e = 0; e < 8; ++e) g[e] = glu_mul<PRO - 1>(g[e], u[e]);
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) g[e] = glu_mul_fast<PRO - 1>(g[e], u[e]);
+                }
+                gt[q] = V8::pack(g);
+            }
+            fence_proxy_async();  // the tile is read by the tensor core (the async proxy)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&hready[slot]);
+        }
     }
     mbar_wait(&accb, 0);
     __syncwarp();  // the warp-wide accumulator loads below need all 32 lanes together
@@ -1008,16 +1053,17 @@ cudaError_t launch_h_mt(const LinArgs& a, const LinPlan& p, cudaStream_t s, cons
     return launch_kernel(kernel, grid, dim3((warps_for(MT) + 1) * 32), smem, s, p.pdl, p.splits, a, tmW, tmX);
 }
 
-template <typename T, int STAGES>
+template <typename T, int STAGES, int PRO>
 cudaError_t launch_tc(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
-    // W [N][K] in [128][64] boxes and h [B][K] in [64][64] boxes, both with the 128-byte swizzle
+    // W [N][K] in [128][64] boxes and h [B][K] (or gate_up [B][2K]) in [64][64] boxes, both with
+    // the 128-byte swizzle
     const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
     CUtensorMap tmW, tmX;
     if (!encode_tmap_16(&tmW, a.W, 2, a.K, a.N, a.K * 2, kKT, kTcM, bf16, true) ||
-        !encode_tmap_16(&tmX, a.x, 2, a.K, a.B, a.xs * 2, kKT, kTcN, bf16, true))
+        !encode_tmap_16(&tmX, a.x, 2, PRO == 3 ? a.K : 2 * a.K, a.B, a.xs * 2, kKT, kTcN, bf16, true))
         return cudaErrorNotSupported;
-    auto kernel = linear_tc_kernel<T, STAGES>;
-    const size_t smem = tc_smem_bytes(STAGES);
+    auto kernel = linear_tc_kernel<T, STAGES, PRO>;
+    const size_t smem = tc_smem_bytes(STAGES, PRO);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int splits = p.splits;
@@ -1078,8 +1124,12 @@ cudaError_t launch_pro(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
 template <typename T>
 cudaError_t launch_typed(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
     if (p.tcgen05) {
-        if (p.prologue != 3) return cudaErrorInvalidValue;
-        return p.tc_stages == 8 ? launch_tc<T, 8>(a, p, s) : launch_tc<T, 4>(a, p, s);
+        switch (p.prologue) {
+            case 1: return launch_tc<T, 3, 1>(a, p, s);  // the GLU fused: 3 stages of 32 KB, two CTAs per SM
+            case 2: return launch_tc<T, 3, 2>(a, p, s);
+            case 3: return p.tc_stages == 8 ? launch_tc<T, 8, 3>(a, p, s) : launch_tc<T, 4, 3>(a, p, s);
+            default: return cudaErrorInvalidValue;
+        }
     }
     if (p.narrow) {
         switch (p.prologue) {
@@ -1248,12 +1298,12 @@ size_t linear_smem(int mt, int prologue) {
     return prologue == 3 ? lin::smemh_bytes(mt) : lin::smem_bytes(mt, prologue);
 }
 size_t linear16_smem(int rows, int64_t K, int splits) { return lin::smem16_bytes(rows, K, splits); }
-size_t linear_tc_smem(int stages) { return lin::tc_smem_bytes(stages); }
+size_t linear_tc_smem(int stages, int prologue) { return lin::tc_smem_bytes(stages, prologue); }
 
 // Clusters of `splits` CTAs of the tcgen05 projection (ring of `stages`) the device can hold at once.
-int linear_tc_max_clusters(int splits, int stages, bool bf16) {
+int linear_tc_max_clusters(int splits, int stages, bool bf16, int prologue) {
     // answers kept per (device, dtype, ring depth, cluster size): the query sets kernel attributes
-    static std::atomic<int> memo[16][2][2][17];
+    static std::atomic<int> memo[16][2][3][17];
     static std::once_flag once;
     std::call_once(once, [] {
         for (auto& a : memo)
@@ -1267,9 +1317,10 @@ int linear_tc_max_clusters(int splits, int stages, bool bf16) {
         return 0;
     }
     if (splits < 1 || splits > 16) return 0;
-    std::atomic<int>* slot = dev >= 0 && dev < 16 ? &memo[dev][bf16 ? 1 : 0][stages == 8 ? 1 : 0][splits] : nullptr;
+    const int kind = prologue != 3 ? 2 : (stages == 8 ? 1 : 0);
+    std::atomic<int>* slot = dev >= 0 && dev < 16 ? &memo[dev][bf16 ? 1 : 0][kind][splits] : nullptr;
     if (slot && slot->load() >= 0) return slot->load();
-    const size_t smem = lin::tc_smem_bytes(stages);
+    const size_t smem = lin::tc_smem_bytes(kind == 2 ? 3 : stages, prologue != 3 ? 1 : 3);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
@@ -1291,10 +1342,12 @@ int linear_tc_max_clusters(int splits, int stages, bool bf16) {
             n = 0;
         }
     };
-    if (stages == 8)
-        bf16 ? query(lin::linear_tc_kernel<__nv_bfloat16, 8>) : query(lin::linear_tc_kernel<__half, 8>);
+    if (kind == 2)
+        bf16 ? query(lin::linear_tc_kernel<__nv_bfloat16, 3, 1>) : query(lin::linear_tc_kernel<__half, 3, 1>);
+    else if (kind == 1)
+        bf16 ? query(lin::linear_tc_kernel<__nv_bfloat16, 8, 3>) : query(lin::linear_tc_kernel<__half, 8, 3>);
     else
-        bf16 ? query(lin::linear_tc_kernel<__nv_bfloat16, 4>) : query(lin::linear_tc_kernel<__half, 4>);
+        bf16 ? query(lin::linear_tc_kernel<__nv_bfloat16, 4, 3>) : query(lin::linear_tc_kernel<__half, 4, 3>);
     if (slot) slot->store(n);
     return n;
 }

@@ -71,6 +71,39 @@ def glu_case(B, I, N, dtype, seed, act="silu", rows=None, ws=False):
     return got[sel], want, h, W
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("act", ["silu", "relu"])
+@pytest.mark.parametrize("B,I,N", [(1, 64, 128), (17, 640, 384), (40, 4160, 640), (64, 8960, 1536), (33, 1024, 256)])
+def test_glu_fused_into_the_tcgen05_projection(dtype, act, B, I, N):
+    """The GLU computed inside the tcgen05 projection (gate and up tiles by TMA, h's tile made in
+    place by two warps), forced from 1 row: against the oracle's glu then linear."""
+    sra.force_variant("linear", 1)
+    try:
+        before = sra.wait_timeouts()
+        got, want, h, W = glu_case(B, I, N, dtype, 1090 + B, act=act)
+        torch.cuda.synchronize()
+        assert sra.wait_timeouts() == before
+    finally:
+        sra.force_variant("linear", -1)
+    assert_linear_close(got, want, h, W, f"fused glu tcgen05 {act} {dtype} B={B} I={I} N={N}")
+
+
+def test_glu_fused_into_the_tcgen05_projection_far_negative_gates():
+    """Gates below -64 in some 8-element chunks take the careful SiLU inside the fused kernel."""
+    B, I, N = 24, 1024, 256
+    gu = syn.normal((B, 2 * I), 0, 1, torch.bfloat16, 1095, 3)
+    gu[:, 5] = -90.0
+    gu[3, 17:25] = -200.0
+    gu[7, 512] = -70.0
+    W = syn.linear_weight(N, I, torch.bfloat16, 1095)
+    got = sra.glu_linear(gu.to(DEV), W.to(DEV)).cpu()   # 24 rows: the fused tcgen05 kernel
+    h = torch.empty(B, I, dtype=torch.bfloat16)
+    oracle.glu(gu, h, "silu")
+    want = torch.empty(B, N, dtype=torch.bfloat16)
+    oracle.linear(h, W, want)
+    assert_linear_close(got, want, h, W, "fused glu far-negative gates")
+
+
 @pytest.mark.parametrize("splits", [1, 2, 3, 5, 8])
 @pytest.mark.parametrize("case", ["norm", "silu", "relu"])
 @pytest.mark.parametrize("B", [1, 5, 16])
