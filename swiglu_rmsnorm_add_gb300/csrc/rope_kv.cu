@@ -161,17 +161,17 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
         prefetch_l2(static_cast<const T*>(a.k) + t * a.ks, static_cast<int64_t>(a.n_kv) * a.head_dim * es);
         prefetch_l2(static_cast<const T*>(a.v) + t * a.vs, static_cast<int64_t>(a.n_kv) * a.head_dim * es);
     }
-    if (threadIdx.x == blockDim.x - 1 && blockIdx.x < a.T) {
-        // Warm the first token's cos / sin rows. The position is read before the dependency
-        // wait (a relaxed read: the previous kernel may still be writing it), so it only
-        // steers a prefetch; the position used below is read again after the wait.
-        int64_t p;
-        asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(p) : "l"(a.pos + blockIdx.x));
-        if (p >= 0 && p < a.max_pos) {
-            const int64_t half = a.head_dim >> 1;
-            prefetch_l2(a.cos + p * half, half * 4);
-            prefetch_l2(a.sin + p * half, half * 4);
-        }
+    // The CTA's first token's position, read before the dependency wait (relaxed: the previous
+    // kernel may still be writing it). It warms that token's cos / sin rows and, after the wait,
+    // says which rows to load together with the position's own read; the position read after
+    // the wait decides, and a different one (never, unless the previous kernel wrote it) loads
+    // its rows again.
+    int64_t p_pre = -1;
+    if (blockIdx.x < a.T) asm volatile("ld.relaxed.gpu.global.b64 %0, [%1];" : "=l"(p_pre) : "l"(a.pos + blockIdx.x));
+    if (threadIdx.x == blockDim.x - 1 && p_pre >= 0 && p_pre < a.max_pos) {
+        const int64_t half = a.head_dim >> 1;
+        prefetch_l2(a.cos + p_pre * half, half * 4);
+        prefetch_l2(a.sin + p_pre * half, half * 4);
     }
     pdl_enter();
 
@@ -190,11 +190,40 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
 
         for (int64_t t = blockIdx.x; t < a.T; t += gridDim.x) {
             const int64_t p = a.pos[t];
-            const bool pos_ok = p >= 0 && p < a.max_pos;
             int64_t slot = -1;
             if (kind != 0 || u == 0) slot = a.slot[t];
-            const bool slot_in_range = slot < capacity;
+            // element offsets of the task's two accesses
+            const int o0 = IL ? 2 * i0 : i0;
+            const int o1 = IL ? 2 * i0 + P : h + i0;
+            // the task's row and (from the early position) its cos / sin, requested with the
+            // position and the slot: none of these loads waits for them
+            const T* src = kind == 0   ? static_cast<const T*>(a.q) + t * a.qs + static_cast<int64_t>(head) * a.head_dim
+                           : kind == 1 ? static_cast<const T*>(a.k) + t * a.ks + static_cast<int64_t>(head) * a.head_dim
+                                       : static_cast<const T*>(a.v) + t * a.vs + static_cast<int64_t>(head) * a.head_dim;
+            const R r0 = V::load(src + o0);
+            const R r1 = V::load(src + o1);
+            // (not with the UClip parameters: their registers and these would not fit together)
+            const int64_t ps = !NORM && t == blockIdx.x && p_pre >= 0 && p_pre < a.max_pos ? p_pre : -1;
+            float c[P], s[P];
+            auto load_cs = [&](int64_t pp) {
+                const float* crow = a.cos + pp * h + i0;
+                const float* srow = a.sin + pp * h + i0;
+#pragma unroll
+                for (int j = 0; j < P; j += CW) {
+                    float cf[CW], sf[CW];
+                    C::unpack(C::load(crow + j), cf);
+                    C::unpack(C::load(srow + j), sf);
+#pragma unroll
+                    for (int q = 0; q < CW; ++q) {
+                        c[j + q] = cf[q];
+                        s[j + q] = sf[q];
+                    }
+                }
+            };
+            if (kind != 2 && ps >= 0) load_cs(ps);
 
+            const bool pos_ok = p >= 0 && p < a.max_pos;
+            const bool slot_in_range = slot < capacity;
             if (u == 0 && a.err != nullptr) {
                 const int bad = (pos_ok ? 0 : 1) + ((slot >= 0 && !slot_in_range) ? 1 : 0);
                 if (bad) atomicAdd(a.err, bad);
@@ -202,12 +231,9 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
             if (!pos_ok) continue;                       // q[t] unchanged, nothing cached
             if (kind != 0 && (slot < 0 || !slot_in_range)) continue;  // padding / bad slot
 
-            const T* src;
             T* dst;
             if (kind == 0) {
-                T* qh = static_cast<T*>(a.q) + t * a.qs + static_cast<int64_t>(head) * a.head_dim;
-                src = qh;
-                dst = qh;
+                dst = static_cast<T*>(a.q) + t * a.qs + static_cast<int64_t>(head) * a.head_dim;
             } else {
                 const int64_t blk = slot / a.block_size;
                 const int64_t off = slot - blk * a.block_size;
@@ -215,19 +241,13 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
                 dst = static_cast<T*>(a.cache) +
                       (((plane * a.num_blocks + blk) * a.block_size + off) * a.n_kv + head) *
                           static_cast<int64_t>(a.head_dim);
-                src = kind == 1 ? static_cast<const T*>(a.k) + t * a.ks + static_cast<int64_t>(head) * a.head_dim
-                                : static_cast<const T*>(a.v) + t * a.vs + static_cast<int64_t>(head) * a.head_dim;
             }
-            // element offsets of the task's two accesses
-            const int o0 = IL ? 2 * i0 : i0;
-            const int o1 = IL ? 2 * i0 + P : h + i0;
-            const R r0 = V::load(src + o0);
-            const R r1 = V::load(src + o1);
             if (kind == 2) {  // V: bit copy
                 V::store(dst + o0, r0);
                 V::store(dst + o1, r1);
                 continue;
             }
+            if (!NORM && p != ps) load_cs(p);
             float lo[P], hi[P];
             if constexpr (IL && P >= 2) {
                 float f0[P], f1[P];
@@ -252,20 +272,7 @@ __global__ void __launch_bounds__(1024) token_cta_kernel(RopeArgs a) {
                     lo[j] = round_trip<T>(uclip1(lo[j], alo[j], glo[j], a.clip_lo, a.clip_hi));
                     hi[j] = round_trip<T>(uclip1(hi[j], ahi[j], ghi[j], a.clip_lo, a.clip_hi));
                 }
-            }
-            float c[P], s[P];
-            const float* crow = a.cos + p * h + i0;
-            const float* srow = a.sin + p * h + i0;
-#pragma unroll
-            for (int j = 0; j < P; j += CW) {
-                float cf[CW], sf[CW];
-                C::unpack(C::load(crow + j), cf);
-                C::unpack(C::load(srow + j), sf);
-#pragma unroll
-                for (int q = 0; q < CW; ++q) {
-                    c[j + q] = cf[q];
-                    s[j + q] = sf[q];
-                }
+                load_cs(p);
             }
             float ylo[P], yhi[P];
 #pragma unroll
