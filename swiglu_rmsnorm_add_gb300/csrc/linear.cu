@@ -577,12 +577,18 @@ __host__ __device__ constexpr size_t tc_smem_bytes(int stages, int pro = 3) {
                        : static_cast<size_t>(kTcN) * kTcM * 4);
 }
 
+// Threads of the tcgen05 projection: warp 0 issues the MMAs, warp 1 the copies, warps 0-3 read
+// the accumulator back (a warp reaches only its quarter of the tensor-memory lanes); with the GLU
+// fused, warps 2-5 compute it (one warp on each of the SM's four schedulers).
+__host__ __device__ constexpr int tc_threads(int pro) { return pro == 3 ? 128 : 192; }
+constexpr int kTcActWarps = 4;
+
 // PRO 3: h comes from the workspace (its own prologue kernel ran before). PRO 1 / 2: the GLU
 // (SwiGLU / ReGLU) is fused: each stage brings the gate and up tiles of this CTA's K range, warps
-// 2 and 3 turn them into h's tile in place (the same 128-byte swizzle, so the element-wise
-// product needs no index arithmetic) and release it to the MMA thread on a barrier of its own.
+// 2-5 turn them into h's tile in place (the same 128-byte swizzle, so the element-wise product
+// needs no index arithmetic) and release it to the MMA thread on a barrier of its own.
 template <typename T, int S, int PRO>
-__global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_constant__ CUtensorMap tmW,
+__global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, const __grid_constant__ CUtensorMap tmW,
                                                         const __grid_constant__ CUtensorMap tmX) {
     constexpr size_t SB = tc_stage_bytes(PRO);
     constexpr uint32_t kCols = 64;  // tensor-memory columns: one fp32 accumulator column per row of h
@@ -608,7 +614,7 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
             mbar_init(&empty[i], 1);
-            mbar_init(&hready[i], 2);  // the two activation warps (prologue 1 / 2)
+            mbar_init(&hready[i], kTcActWarps);  // the activation warps (prologue 1 / 2)
         }
         mbar_init(&accb, 1);
         mbar_init_fence();
@@ -673,11 +679,16 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
         }
         __syncwarp();
     } else if (PRO != 3) {
-        // activation warps 2 and 3: h = act(gate) * up over each stage's [64 rows][64] tiles, in
+        // activation warps 2-5: h = act(gate) * up over each stage's [64 rows][64] tiles, in
         // place of the gate tile; a chunk holding a gate below -64 (never on the configured
         // inputs) goes through glu_mul element by element
+        // The thread's 8 gate vectors are read and checked first; unless a lane of the warp found
+        // a far-negative gate, the products run in one branch-free unrolled pass (8 independent
+        // vectors in flight), else vector by vector with the check.
         using V8 = Vec<T, 8>;
         using R8 = typename V8::Raw;
+        constexpr int NA = 32 * kTcActWarps;                                // activation threads
+        constexpr int NQ = static_cast<int>(tc_htile_bytes() / 16) / NA;  // vectors per thread
         const int at = threadIdx.x - 64;
         for (int t = 0; t < ntiles; ++t) {
             const int slot = t % S;
@@ -685,20 +696,38 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
             unsigned char* st = smem + static_cast<size_t>(slot) * SB + tc_wtile_bytes();
             R8* gt = reinterpret_cast<R8*>(st);
             const R8* ut = reinterpret_cast<const R8*>(st + tc_htile_bytes());
-#pragma unroll 4
-            for (int q = at; q < static_cast<int>(tc_htile_bytes() / 16); q += 64) {
-                const R8 gv = gt[q], uv = ut[q];
-                float g[8], u[8];
-                V8::unpack(gv, g);
-                V8::unpack(uv, u);
-                if (PRO == 1 && needs_careful<T, 8>(gv)) {
+            R8 gv[NQ];
+            bool careful = false;
+#pragma unroll
+            for (int i = 0; i < NQ; ++i) {
+                gv[i] = gt[at + NA * i];
+                if (PRO == 1) careful |= needs_careful<T, 8>(gv[i]);
+            }
+            if (PRO == 1 && __any_sync(0xffffffffu, careful)) {
 #pragma unroll 1
-                    for (int e = 0; e < 8; ++e) g[e] = glu_mul<PRO - 1>(g[e], u[e]);
-                } else {
+                for (int i = 0; i < NQ; ++i) {
+                    float g[8], u[8];
+                    V8::unpack(gv[i], g);
+                    V8::unpack(ut[at + NA * i], u);
+                    if (needs_careful<T, 8>(gv[i])) {
+#pragma unroll 1
+                        for (int e = 0; e < 8; ++e) g[e] = glu_mul<PRO - 1>(g[e], u[e]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) g[e] = glu_mul_fast<PRO - 1>(g[e], u[e]);
+                    }
+                    gt[at + NA * i] = V8::pack(g);
+                }
+            } else {
+#pragma unroll
+                for (int i = 0; i < NQ; ++i) {
+                    float g[8], u[8];
+                    V8::unpack(gv[i], g);
+                    V8::unpack(ut[at + NA * i], u);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) g[e] = glu_mul_fast<PRO - 1>(g[e], u[e]);
+                    gt[at + NA * i] = V8::pack(g);
                 }
-                gt[q] = V8::pack(g);
             }
             fence_proxy_async();  // the tile is read by the tensor core (the async proxy)
             __syncwarp();
@@ -717,7 +746,7 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
         // partials, every rank's 16-byte load issued before the first add
         float* mine = a.ws_part + (static_cast<int64_t>(blockIdx.x / SK) * SK + rank) * (kTcN * kTcM);
 #pragma unroll
-        for (int c0 = 0; c0 < kTcN; c0 += 16) {
+        for (int c0 = 0; c0 < kTcN && warp < 4; c0 += 16) {
             uint32_t v[16];
             tc::ld16(tmem + (static_cast<uint32_t>(32 * warp) << 16) + static_cast<uint32_t>(c0), v);
             tc::wait_ld();
@@ -731,7 +760,7 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
         cluster.sync();
         const float* base = a.ws_part + static_cast<int64_t>(blockIdx.x / SK) * SK * (kTcN * kTcM);
         T* y = static_cast<T*>(a.y);
-        for (int s4 = rank * 128 + threadIdx.x; s4 < rows * kTcM / 4; s4 += SK * 128) {
+        for (int s4 = rank * 128 + threadIdx.x; threadIdx.x < 128 && s4 < rows * kTcM / 4; s4 += SK * 128) {
             const int r = (4 * s4) / kTcM, c = 4 * s4 - r * kTcM;
             float4 v[16];
 #pragma unroll
@@ -754,9 +783,9 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
         return;
     }
 
-    // ---- epilogue: warp w reads output columns n0 + 32 w + lane, one 16-column (row) group at a time
+    // ---- epilogue: warp w (< 4) reads output columns n0 + 32 w + lane, one 16-column (row) group at a time
 #pragma unroll
-    for (int c0 = 0; c0 < kTcN; c0 += 16) {
+    for (int c0 = 0; c0 < kTcN && warp < 4; c0 += 16) {
         uint32_t v[16];
         tc::ld16(tmem + (static_cast<uint32_t>(32 * warp) << 16) + static_cast<uint32_t>(c0), v);
         tc::wait_ld();
@@ -770,7 +799,7 @@ __global__ void __launch_bounds__(128) linear_tc_kernel(LinArgs a, const __grid_
     // the K split's sum: each thread 4 adjacent columns of y at a time, every rank's 16-byte
     // partial requested before the first add (the cluster holds at most 16 ranks)
     T* y = static_cast<T*>(a.y);
-    for (int s4 = rank * 128 + threadIdx.x; s4 < rows * kTcM / 4; s4 += SK * 128) {
+    for (int s4 = rank * 128 + threadIdx.x; threadIdx.x < 128 && s4 < rows * kTcM / 4; s4 += SK * 128) {
         const int r = (4 * s4) / kTcM, c = 4 * s4 - r * kTcM;
         float4 v[16];
 #pragma unroll
@@ -1078,7 +1107,7 @@ cudaError_t launch_tc(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
             attr.val.clusterDim.x = static_cast<unsigned>(splits);
             attr.val.clusterDim.y = attr.val.clusterDim.z = 1;
             cfg.gridDim = dim3(static_cast<unsigned>(splits));
-            cfg.blockDim = dim3(128);
+            cfg.blockDim = dim3(tc_threads(PRO));
             cfg.dynamicSmemBytes = smem;
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
@@ -1090,7 +1119,7 @@ cudaError_t launch_tc(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
         }
     }
     const dim3 grid(static_cast<unsigned>((a.N + kTcM - 1) / kTcM * splits));
-    return launch_kernel(kernel, grid, dim3(128), smem, s, p.pdl, splits, a, tmW, tmX);
+    return launch_kernel(kernel, grid, dim3(tc_threads(PRO)), smem, s, p.pdl, splits, a, tmW, tmX);
 }
 
 template <typename T, int PRO>
@@ -1327,7 +1356,7 @@ int linear_tc_max_clusters(int splits, int stages, bool bf16, int prologue) {
     attr.val.clusterDim.x = static_cast<unsigned>(splits);
     attr.val.clusterDim.y = attr.val.clusterDim.z = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(splits));
-    cfg.blockDim = dim3(128);
+    cfg.blockDim = dim3(lin::tc_threads(prologue != 3 ? 1 : 3));
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
