@@ -579,13 +579,27 @@ __host__ __device__ constexpr size_t tc_smem_bytes(int stages, int pro = 3) {
 
 // Threads of the tcgen05 projection: warp 0 issues the MMAs, warp 1 the copies, warps 0-3 read
 // the accumulator back (a warp reaches only its quarter of the tensor-memory lanes); with the GLU
-// fused, warps 2-5 compute it (one warp on each of the SM's four schedulers).
-__host__ __device__ constexpr int tc_threads(int pro) { return pro == 3 ? 128 : 192; }
-constexpr int kTcActWarps = 4;
+// fused, warps 2-9 compute it (two warps on each of the SM's four schedulers: a tile's products
+// are short dependent chains, so the time per tile falls with the warps that share it).
+__host__ __device__ constexpr int tc_threads(int pro) { return pro == 3 ? 128 : 320; }
+constexpr int kTcActWarps = 8;
+
+// silu(g) * u on the fused projection's fast path (gates at or above kSiluFar; the rest take
+// glu_mul): sigma(g) = 1 / (1 + 2^(-g log2 e)) from two approximate instructions of the PTX ISA,
+// ex2.approx.ftz (relative error about 2^-22) and rcp.approx.ftz (about one ulp). Their operands
+// stay in range there: -g log2 e <= 92.4, so 1 + e^-g lies in [1, 2^93); an e^-g that flushes to
+// zero (g large) leaves 1, and a subnormal -g log2 e flushed to zero gives e^-g = 1, its value to
+// fp32's precision. The products g * sigma * u are ordinary (non-flushing) multiplies.
+__device__ __forceinline__ float silu_mul_mufu(float g, float u) {
+    float e, r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(e) : "f"(g * -1.4426950408889634f));
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+    return g * r * u;
+}
 
 // PRO 3: h comes from the workspace (its own prologue kernel ran before). PRO 1 / 2: the GLU
 // (SwiGLU / ReGLU) is fused: each stage brings the gate and up tiles of this CTA's K range, warps
-// 2-5 turn them into h's tile in place (the same 128-byte swizzle, so the element-wise product
+// 2-9 turn them into h's tile in place (the same 128-byte swizzle, so the element-wise product
 // needs no index arithmetic) and release it to the MMA thread on a barrier of its own.
 template <typename T, int S, int PRO>
 __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, const __grid_constant__ CUtensorMap tmW,
@@ -679,7 +693,7 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
         }
         __syncwarp();
     } else if (PRO != 3) {
-        // activation warps 2-5: h = act(gate) * up over each stage's [64 rows][64] tiles, in
+        // activation warps 2-9: h = act(gate) * up over each stage's [64 rows][64] tiles, in
         // place of the gate tile; a chunk holding a gate below -64 (never on the configured
         // inputs) goes through glu_mul element by element
         // The thread's 8 gate vectors are read and checked first; unless a lane of the warp found
@@ -725,7 +739,8 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
                     V8::unpack(gv[i], g);
                     V8::unpack(ut[at + NA * i], u);
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) g[e] = glu_mul_fast<PRO - 1>(g[e], u[e]);
+                    for (int e = 0; e < 8; ++e)
+                        g[e] = PRO == 1 ? silu_mul_mufu(g[e], u[e]) : glu_mul_fast<1>(g[e], u[e]);
                     gt[at + NA * i] = V8::pack(g);
                 }
             }
