@@ -645,13 +645,23 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
     // With h from the workspace, the first stages' W tiles are requested before the dependency
     // wait: that kernel runs only right after the prologue kernel of the same call, which writes
     // h, not W, and which itself waited for everything before it in the stream before this kernel
-    // could start. (The fused GLU follows whatever the caller ran before: nothing early.)
+    // could start. (The fused GLU follows whatever the caller ran before: no copies before the wait.)
     const int pre = PRO != 3 ? 0 : (ntiles < S ? ntiles : S);
     if (warp == 1 && lane == 0) {
         for (int t = 0; t < pre; ++t) {
             mbar_arrive_expect_tx(&full[t], static_cast<uint32_t>(SB));
             tma_load_2d(smem + static_cast<size_t>(t) * SB, &tmW, static_cast<int>(kbase) + t * kKT,
                         static_cast<int>(n0), &full[t]);
+        }
+        // With the GLU fused, the first stages' W, gate and up boxes are only prefetched into the
+        // L2 before the wait (hints, read again after it): their first copies then come from L2.
+        if (PRO != 3) {
+            for (int t = 0; t < S && t < ntiles; ++t) {
+                const int k0 = static_cast<int>(kbase) + t * kKT;
+                tma_prefetch_2d(&tmW, k0, static_cast<int>(n0));
+                tma_prefetch_2d(&tmX, k0, 0);
+                tma_prefetch_2d(&tmX, static_cast<int>(a.K) + k0, 0);
+            }
         }
     }
     pdl_enter();
