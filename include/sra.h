@@ -364,8 +364,10 @@ SRA_API int sra_paged_decode_attention_noalloc(const void* q, const void* kv_cac
  * W:    [N, K] of `dtype`, row-major (nn.Linear's [out, in] layout). Read only.
  * y:    [B, N] of `dtype`, row stride y_row_stride (>= N); must not overlap x, w_ln or W.
  * bf16 / fp16 with K and N multiples of 64 and 16-byte aligned x, w_ln, W (x_row_stride a
- * multiple of 8) run on the tensor cores (fp32 accumulation); other layouts and fp32 run
- * a CUDA-core kernel with the same result up to the order of the fp32 sums.
+ * multiple of 8) run on the tensor cores (fp32 accumulation; from 17 to 64 rows with N a
+ * multiple of 128 on the fifth-generation tensor cores, in one kernel that also takes the
+ * norm where its grid fits the GPU in one wave); other layouts and fp32 run a CUDA-core
+ * kernel with the same result up to the order of the fp32 sums.
  * Errors: unknown dtype -> SRA_ERR_DTYPE; B < 0, K <= 0 or N <= 0 (or K too long for
  * one CTA's shared memory on the CUDA-core path) -> SRA_ERR_SHAPE; short strides ->
  * SRA_ERR_STRIDE; eps negative or not finite -> SRA_ERR_ARG; NULL -> SRA_ERR_NULL;
@@ -511,10 +513,13 @@ SRA_API int sra_set_pdl(int enable);
  * contraction with the K / V tiles moved by TMA; for 1 and 2, OR-ed with (s << 8),
  * s in 1, 2, 4, 8, 16, it also forces the CTAs per (request, kv head), and for 1,
  * OR-ed with (4 << 16), it runs 4-warp CTAs, two per SM), "linear" (the
- * projection of the _ws entry points once the prologue has run: 0 = mma.sync
- * kernels, 1 = the tcgen05 kernel, for up to 64 rows and N a multiple of 128;
- * OR-ed with (s << 8), s in 1..16, it also forces the tcgen05 kernel's K splits, and
- * with (r << 16), r = 4 or 8, its ring depth in stages), "linear_narrow" (the
+ * projection kernels of the fused entry points and of the _ws entry points once
+ * their prologue has run: 0 = mma.sync kernels, 1 = the tcgen05 kernel, for up to
+ * 64 rows and N a multiple of 128, which for the fused entry points computes the
+ * RMSNorm or the GLU itself; OR-ed with (s << 8), s in 1..16, it also forces the
+ * tcgen05 kernel's K splits (with the RMSNorm fused, s >= K / 1024: a CTA holds at
+ * most 1024 columns of x), and with (r << 16), r = 4 or 8, the ring depth in stages
+ * of the projection over h), "linear_narrow" (the
  * decode-batch projection kernel of the fused entry points, up to 16 rows: variant 0,
  * OR-ed with (s << 8), s in 1..8, forces the CTAs of its cluster along K).
  * variant: -1 = automatic per-shape choice (the default); otherwise an index

@@ -198,14 +198,15 @@ struct LinPlan {
     int mt;             // 16-row m-tiles per CTA (1, 2 or 4)
     int splits;         // CTAs per cluster along K
     bool pdl;
-    bool tcgen05;       // <= 64 rows, N a multiple of 128: the tcgen05 kernel (prologue 3, or the GLU fused)
+    bool tcgen05;       // <= 64 rows, N a multiple of 128: the tcgen05 kernel (prologue 3, or the GLU or RMSNorm fused)
     int tc_stages = 4;  // its ring depth: 4 (two CTAs per SM) or 8 (one)
 };
 
 cudaError_t launch_linear(const LinArgs& a, const LinPlan& p, int dtype, cudaStream_t s);
 size_t linear_smem(int mt, int prologue);
-size_t linear_tc_smem(int stages, int prologue = 3);
-int linear_tc_max_clusters(int splits, int stages, bool bf16, int prologue = 3);
+size_t linear_tc_smem(int stages, int prologue = 3, int nx = 0);
+// nx: with the RMSNorm fused (prologue 0), the K tiles of x a CTA holds (at most 16)
+int linear_tc_max_clusters(int splits, int stages, bool bf16, int prologue = 3, int nx = 0);
 unsigned int linear_wait_timeouts();  // bounded waits of the fused-projection kernel that ran out
 cudaError_t launch_wait_selftest(int32_t* out, cudaStream_t s);  // a wait on a barrier nothing completes
 size_t linear16_smem(int rows, int64_t K, int splits);

@@ -567,21 +567,25 @@ constexpr int kTcN = 64;     // rows of h (at most): the MMA's N
 __host__ __device__ constexpr size_t tc_wtile_bytes() { return static_cast<size_t>(kTcM) * kKT * 2; }
 __host__ __device__ constexpr size_t tc_htile_bytes() { return static_cast<size_t>(kTcN) * kKT * 2; }
 // A stage: the W tile, then h's tile (prologue 3), or the gate and up tiles the activation warps
-// turn into h's tile in place (prologue 1 / 2: the GLU fused into the projection).
+// turn into h's tile in place (prologue 1 / 2: the GLU fused into the projection), or the W tile
+// alone (prologue 0: the RMSNorm fused, h's tiles held apart, `nx` of them, after the ring).
 __host__ __device__ constexpr size_t tc_stage_bytes(int pro) {
-    return tc_wtile_bytes() + (pro == 3 ? 1 : 2) * tc_htile_bytes();
+    return tc_wtile_bytes() + (pro == 0 ? 0 : (pro == 3 ? 1 : 2)) * tc_htile_bytes();
 }
-__host__ __device__ constexpr size_t tc_smem_bytes(int stages, int pro = 3) {
-    return 1024 + (stages * tc_stage_bytes(pro) > static_cast<size_t>(kTcN) * kTcM * 4
-                       ? stages * tc_stage_bytes(pro)
+__host__ __device__ constexpr size_t tc_smem_bytes(int stages, int pro = 3, int nx = 0) {
+    return 1024 + (stages * tc_stage_bytes(pro) + nx * tc_htile_bytes() > static_cast<size_t>(kTcN) * kTcM * 4
+                       ? stages * tc_stage_bytes(pro) + nx * tc_htile_bytes()
                        : static_cast<size_t>(kTcN) * kTcM * 4);
 }
+// Most K tiles a CTA of the fused RMSNorm holds (its whole K range stays in shared memory).
+constexpr int kTcNormMaxTiles = 16;
 
 // Threads of the tcgen05 projection: warp 0 issues the MMAs, warp 1 the copies, warps 0-3 read
 // the accumulator back (a warp reaches only its quarter of the tensor-memory lanes); with the GLU
 // fused, warps 2-9 compute it (two warps on each of the SM's four schedulers: a tile's products
-// are short dependent chains, so the time per tile falls with the warps that share it).
-__host__ __device__ constexpr int tc_threads(int pro) { return pro == 3 ? 128 : 320; }
+// are short dependent chains, so the time per tile falls with the warps that share it); with the
+// RMSNorm fused, all ten warps take the norm before the roles split.
+__host__ __device__ constexpr int tc_threads(int pro) { return pro == 3 ? 128 : 320; }  // 0: the norm's threads
 constexpr int kTcActWarps = 8;
 
 // silu(g) * u on the fused projection's fast path (gates at or above kSiluFar; the rest take
@@ -600,7 +604,11 @@ __device__ __forceinline__ float silu_mul_mufu(float g, float u) {
 // PRO 3: h comes from the workspace (its own prologue kernel ran before). PRO 1 / 2: the GLU
 // (SwiGLU / ReGLU) is fused: each stage brings the gate and up tiles of this CTA's K range, warps
 // 2-9 turn them into h's tile in place (the same 128-byte swizzle, so the element-wise product
-// needs no index arithmetic) and release it to the MMA thread on a barrier of its own.
+// needs no index arithmetic) and release it to the MMA thread on a barrier of its own. PRO 0:
+// the RMSNorm is fused: the CTA's x tiles (its whole K range) arrive in a region of their own,
+// every thread sums the squares of its share of a row, the cluster's ranks exchange their
+// partial sums, and each CTA normalises its tiles in place into h's tiles before the first MMA;
+// the ring then streams W alone.
 template <typename T, int S, int PRO>
 __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, const __grid_constant__ CUtensorMap tmW,
                                                         const __grid_constant__ CUtensorMap tmX) {
@@ -609,8 +617,14 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
     constexpr uint32_t IDESC = tc::idesc_f16(std::is_same<T, __nv_bfloat16>::value, kTcM, kTcN);
     extern __shared__ unsigned char smem_raw[];
     unsigned char* smem = smem_raw + ((1024 - (smem_u32(smem_raw) & 1023)) & 1023);
-    __shared__ uint64_t full[S], empty[S], hready[S], accb;
+    __shared__ uint64_t full[S], empty[S], hready[S], accb, xfull;
     __shared__ uint32_t tmem_slot;
+    // the fused RMSNorm's row statistics: every rank's partial sums, pushed here by the ranks
+    // (stat[q][r]: rank q's sum of row r), this rank's fp64 sums for rows past fp32's range, each
+    // row's 1 / rms and pre-scale
+    __shared__ float stat[PRO == 0 ? 16 : 1][PRO == 0 ? kTcN : 1], inv[PRO == 0 ? kTcN : 1], prev[PRO == 0 ? kTcN : 1];
+    __shared__ double dstat[PRO == 0 ? kTcN : 1];
+    __shared__ __align__(16) T wsl[PRO == 0 ? kTcNormMaxTiles * kKT : 8];  // the norm weight of the K range
     cg::cluster_group cluster = cg::this_cluster();
     const int SK = static_cast<int>(cluster.num_blocks());
     const int rank = static_cast<int>(cluster.block_rank());
@@ -624,6 +638,7 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
     const int ntiles = kt1 - kt0;
     const int64_t kbase = static_cast<int64_t>(kt0) * kKT;
     float* part = reinterpret_cast<float*>(smem);  // the K split's reduction, after the ring drains
+    unsigned char* xreg = smem + static_cast<size_t>(S) * SB;  // prologue 0: the CTA's x / h tiles
     if (threadIdx.x == 0) {
         for (int i = 0; i < S; ++i) {
             mbar_init(&full[i], 1);
@@ -631,6 +646,7 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
             mbar_init(&hready[i], kTcActWarps);  // the activation warps (prologue 1 / 2)
         }
         mbar_init(&accb, 1);
+        mbar_init(&xfull, 1);
         mbar_init_fence();
     }
     if (warp == 0) {
@@ -646,16 +662,17 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
     // wait: that kernel runs only right after the prologue kernel of the same call, which writes
     // h, not W, and which itself waited for everything before it in the stream before this kernel
     // could start. (The fused GLU follows whatever the caller ran before: no copies before the wait.)
-    const int pre = PRO != 3 ? 0 : (ntiles < S ? ntiles : S);
+    // (prologue 0: the first stages are requested right after the wait, with the x tiles)
+    const int pre = PRO == 1 || PRO == 2 ? 0 : (ntiles < S ? ntiles : S);
     if (warp == 1 && lane == 0) {
-        for (int t = 0; t < pre; ++t) {
+        for (int t = 0; PRO == 3 && t < pre; ++t) {
             mbar_arrive_expect_tx(&full[t], static_cast<uint32_t>(SB));
             tma_load_2d(smem + static_cast<size_t>(t) * SB, &tmW, static_cast<int>(kbase) + t * kKT,
                         static_cast<int>(n0), &full[t]);
         }
         // With the GLU fused, the first stages' W, gate and up boxes are only prefetched into the
         // L2 before the wait (hints, read again after it): their first copies then come from L2.
-        if (PRO != 3) {
+        if (PRO == 1 || PRO == 2) {
             for (int t = 0; t < S && t < ntiles; ++t) {
                 const int k0 = static_cast<int>(kbase) + t * kKT;
                 tma_prefetch_2d(&tmW, k0, static_cast<int>(n0));
@@ -663,8 +680,119 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
                 tma_prefetch_2d(&tmX, static_cast<int>(a.K) + k0, 0);
             }
         }
+        // With the RMSNorm fused: the first stages' W boxes and all of the CTA's x boxes.
+        if (PRO == 0) {
+            for (int t = 0; t < ntiles; ++t) {
+                const int k0 = static_cast<int>(kbase) + t * kKT;
+                if (t < S) tma_prefetch_2d(&tmW, k0, static_cast<int>(n0));
+                tma_prefetch_2d(&tmX, k0, 0);
+            }
+        }
     }
     pdl_enter();
+
+    if constexpr (PRO == 0) {
+        using V8 = Vec<T, 8>;
+        using R8 = typename V8::Raw;
+        if (warp == 1 && lane == 0) {
+            // the x tiles of the CTA's K range, then the first stages of W
+            mbar_arrive_expect_tx(&xfull, static_cast<uint32_t>(ntiles * tc_htile_bytes()));
+            for (int t = 0; t < ntiles; ++t)
+                tma_load_2d(xreg + static_cast<size_t>(t) * tc_htile_bytes(), &tmX, static_cast<int>(kbase) + t * kKT,
+                            0, &xfull);
+            for (int t = 0; t < ntiles && t < S; ++t) {
+                mbar_arrive_expect_tx(&full[t], static_cast<uint32_t>(SB));
+                tma_load_2d(smem + static_cast<size_t>(t) * SB, &tmW, static_cast<int>(kbase) + t * kKT,
+                            static_cast<int>(n0), &full[t]);
+            }
+        }
+        // the norm weight of the CTA's K range, staged while the x tiles arrive
+        for (int c = static_cast<int>(threadIdx.x); c < ntiles * (kKT / 8); c += tc_threads(0))
+            reinterpret_cast<R8*>(wsl)[c] = V8::load(static_cast<const T*>(a.w_ln) + kbase + c * 8);
+        mbar_wait(&xfull, 0);
+        // Partial sums of squares over the CTA's K range: thread i < 256 takes row i / 4 and its
+        // 16-byte chunks i % 4 and i % 4 + 4 of every tile (the 128-byte swizzle moves a row's
+        // chunks only within the row's 128 bytes), four lanes meeting by shuffles.
+        const int sr = static_cast<int>(threadIdx.x >> 2), sq = static_cast<int>(threadIdx.x & 3);
+        if (threadIdx.x < 4 * kTcN) {
+            float ss = 0.0f;
+            for (int t = 0; t < ntiles; ++t) {
+                const unsigned char* rp = xreg + static_cast<size_t>(t) * tc_htile_bytes() + sr * (kKT * 2);
+                float f[8], g[8];
+                V8::unpack(*reinterpret_cast<const R8*>(rp + sq * 16), f);
+                V8::unpack(*reinterpret_cast<const R8*>(rp + (sq + 4) * 16), g);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    ss = fmaf(f[e], f[e], ss);
+                    ss = fmaf(g[e], g[e], ss);
+                }
+            }
+            ss += __shfl_xor_sync(0xffffffffu, ss, 1);
+            ss += __shfl_xor_sync(0xffffffffu, ss, 2);
+            // into every rank's stat[rank][row] (remote stores: nothing waits for a round trip)
+            if (sq == 0)
+                for (int q = 0; q < SK; ++q) dsmem_st_f32(dsmem_addr(&stat[rank][sr], static_cast<uint32_t>(q)), ss);
+        }
+        cluster.sync();  // (release / acquire) every rank's partial sums are in this CTA's stat
+        int wide = 0;
+        if (threadIdx.x < kTcN) {
+            const int r = static_cast<int>(threadIdx.x);
+            float tot = 0.0f;
+            for (int q = 0; q < SK; ++q) tot += stat[q][r];
+            inv[r] = r < rows ? rsqrtf(tot / static_cast<float>(a.K) + a.eps) : 0.0f;
+            prev[r] = 1.0f;
+            wide = r < rows && !ss_in_range(tot, a.K, a.eps);
+        }
+        // Every rank adds the same partials in the same order, so `wide` is the same on all the
+        // cluster's ranks and the barrier below is reached by all of them or by none.
+        if (__syncthreads_or(wide)) {
+            // rows whose fp32 sum left fp32's range: the squares again in double, exchanged the same way
+            if (threadIdx.x < 4 * kTcN) {
+                double sd = 0.0;
+                for (int t = 0; t < ntiles; ++t) {
+                    const unsigned char* rp = xreg + static_cast<size_t>(t) * tc_htile_bytes() + sr * (kKT * 2);
+                    float f[8], g[8];
+                    V8::unpack(*reinterpret_cast<const R8*>(rp + sq * 16), f);
+                    V8::unpack(*reinterpret_cast<const R8*>(rp + (sq + 4) * 16), g);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        sd += static_cast<double>(f[e]) * f[e] + static_cast<double>(g[e]) * g[e];
+                }
+                sd += __shfl_xor_sync(0xffffffffu, sd, 1);
+                sd += __shfl_xor_sync(0xffffffffu, sd, 2);
+                if (sq == 0) dstat[sr] = sd;
+            }
+            cluster.sync();
+            if (threadIdx.x < rows) {
+                const int r = static_cast<int>(threadIdx.x);
+                float tot = 0.0f;
+                for (int q = 0; q < SK; ++q) tot += stat[q][r];
+                if (!ss_in_range(tot, a.K, a.eps)) {
+                    double sd = 0.0;
+                    for (int q = 0; q < SK; ++q) sd += cluster.map_shared_rank(dstat, q)[r];
+                    const WideScale sc = wide_scale(sd, a.K, a.eps);
+                    inv[r] = sc.rinv, prev[r] = sc.pre;
+                }
+            }
+            __syncthreads();
+        }
+        // h = x * pre * (1 / rms) * w, rounded to T, in place: chunk p of row r in a tile holds
+        // the row's columns 8 (p ^ (r % 8)) ... + 7 of the tile (the 128-byte swizzle). (The
+        // barriers above made the staged weight visible.)
+        for (int c = static_cast<int>(threadIdx.x); c < ntiles * kTcN * 8; c += tc_threads(0)) {
+            const int t = c / (kTcN * 8), rem = c - t * (kTcN * 8), r = rem >> 3, pch = rem & 7;
+            R8* hp = reinterpret_cast<R8*>(xreg + static_cast<size_t>(t) * tc_htile_bytes() + r * (kKT * 2) + pch * 16);
+            float f[8], g[8];
+            V8::unpack(*hp, f);
+            V8::unpack(reinterpret_cast<const R8*>(wsl)[t * (kKT / 8) + (pch ^ (r & 7))], g);
+            const float iv = inv[r], pv = prev[r];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = f[e] * pv * iv * g[e];
+            *hp = V8::pack(f);
+        }
+        fence_proxy_async();  // h's tiles are read by the tensor core (the async proxy)
+        __syncthreads();
+    }
 
     // Lanes 1-31 of the producer and MMA warps wait at the warp barrier (not in a poll loop,
     // which would take the warp's issue slots from lane 0) until lane 0 has left its loop.
@@ -680,9 +808,10 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
                     mbar_arrive_expect_tx(&full[slot], static_cast<uint32_t>(SB));
                     tma_load_2d(st, &tmW, k0, static_cast<int>(n0), &full[slot]);
                 }
-                tma_load_2d(st + tc_wtile_bytes(), &tmX, k0, 0, &full[slot]);
-                if (PRO != 3) tma_load_2d(st + tc_wtile_bytes() + tc_htile_bytes(), &tmX, static_cast<int>(a.K) + k0, 0,
-                                          &full[slot]);
+                if (PRO != 0) tma_load_2d(st + tc_wtile_bytes(), &tmX, k0, 0, &full[slot]);
+                if (PRO == 1 || PRO == 2)
+                    tma_load_2d(st + tc_wtile_bytes() + tc_htile_bytes(), &tmX, static_cast<int>(a.K) + k0, 0,
+                                &full[slot]);
             }
         }
         __syncwarp();
@@ -690,19 +819,20 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
         if (lane == 0) {
             for (int t = 0; t < ntiles; ++t) {
                 const int slot = t % S;
-                mbar_wait(PRO == 3 ? &full[slot] : &hready[slot], static_cast<uint32_t>((t / S) & 1));
+                mbar_wait(PRO == 1 || PRO == 2 ? &hready[slot] : &full[slot], static_cast<uint32_t>((t / S) & 1));
                 tc::fence_after();
                 const unsigned char* st = smem + static_cast<size_t>(slot) * SB;
+                const unsigned char* hb = PRO == 0 ? xreg + static_cast<size_t>(t) * tc_htile_bytes() : st + tc_wtile_bytes();
 #pragma unroll
                 for (int k = 0; k < kKT / 16; ++k)
-                    tc::mma_f16(tmem, tc::sdesc_sw128(st, 32 * k), tc::sdesc_sw128(st + tc_wtile_bytes(), 32 * k),
-                                IDESC, (t | k) != 0 ? 1u : 0u);
+                    tc::mma_f16(tmem, tc::sdesc_sw128(st, 32 * k), tc::sdesc_sw128(hb, 32 * k), IDESC,
+                                (t | k) != 0 ? 1u : 0u);
                 tc::commit(&empty[slot]);  // the slot is free once these MMAs have read it
             }
             tc::commit(&accb);  // the accumulator is complete once every MMA above has
         }
         __syncwarp();
-    } else if (PRO != 3) {
+    } else if (PRO == 1 || PRO == 2) {
         // activation warps 2-9: h = act(gate) * up over each stage's [64 rows][64] tiles, in
         // place of the gate tile; a chunk holding a gate below -64 (never on the configured
         // inputs) goes through glu_mul element by element
@@ -762,6 +892,9 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
     mbar_wait(&accb, 0);
     __syncwarp();  // the warp-wide accumulator loads below need all 32 lanes together
     tc::fence_after();
+    // the K split's sum: rank q sums float4s [q share4, (q + 1) share4) of the [rows][128] tile
+    const int tot4 = rows * kTcM / 4, share4 = (tot4 + SK - 1) / SK;
+    const int end4 = (rank + 1) * share4 < tot4 ? (rank + 1) * share4 : tot4;
 
     if (a.ws_part) {
         // ---- epilogue through L2: this CTA's partial [64 rows][128 columns] goes straight from
@@ -785,7 +918,7 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
         cluster.sync();
         const float* base = a.ws_part + static_cast<int64_t>(blockIdx.x / SK) * SK * (kTcN * kTcM);
         T* y = static_cast<T*>(a.y);
-        for (int s4 = rank * 128 + threadIdx.x; threadIdx.x < 128 && s4 < rows * kTcM / 4; s4 += SK * 128) {
+        for (int s4 = rank * share4 + threadIdx.x; s4 < end4; s4 += tc_threads(PRO)) {
             const int r = (4 * s4) / kTcM, c = 4 * s4 - r * kTcM;
             float4 v[16];
 #pragma unroll
@@ -824,13 +957,23 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
     // the K split's sum: each thread 4 adjacent columns of y at a time, every rank's 16-byte
     // partial requested before the first add (the cluster holds at most 16 ranks)
     T* y = static_cast<T*>(a.y);
-    for (int s4 = rank * 128 + threadIdx.x; threadIdx.x < 128 && s4 < rows * kTcM / 4; s4 += SK * 128) {
+    for (int s4 = rank * share4 + threadIdx.x; s4 < end4; s4 += tc_threads(PRO)) {
         const int r = (4 * s4) / kTcM, c = 4 * s4 - r * kTcM;
+        // (the fused prologues read the ranks' partials with explicit shared::cluster loads, which
+        // measured faster there; the projection of h keeps the generic ones, with which the
+        // compiler schedules its L2 path better: 8.2 against 7.7 us for ln1 + qkv_proj at batch 64)
         float4 v[16];
+        if constexpr (PRO == 3) {
 #pragma unroll
-        for (int q = 0; q < 16; ++q)
-            v[q] = q < SK ? reinterpret_cast<const float4*>(cluster.map_shared_rank(part, q))[s4]
-                          : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            for (int q = 0; q < 16; ++q)
+                v[q] = q < SK ? reinterpret_cast<const float4*>(cluster.map_shared_rank(part, q))[s4]
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        } else {
+            const uint32_t pa = smem_u32(reinterpret_cast<const float4*>(part) + s4);
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                v[q] = q < SK ? dsmem_ld_f4(dsmem_addr(pa, static_cast<uint32_t>(q))) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+        }
         float4 sum = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
 #pragma unroll
         for (int q = 0; q < 16; ++q) {
@@ -1114,10 +1257,16 @@ cudaError_t launch_tc(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
     const bool bf16 = std::is_same<T, __nv_bfloat16>::value;
     CUtensorMap tmW, tmX;
     if (!encode_tmap_16(&tmW, a.W, 2, a.K, a.N, a.K * 2, kKT, kTcM, bf16, true) ||
-        !encode_tmap_16(&tmX, a.x, 2, PRO == 3 ? a.K : 2 * a.K, a.B, a.xs * 2, kKT, kTcN, bf16, true))
+        !encode_tmap_16(&tmX, a.x, 2, PRO == 1 || PRO == 2 ? 2 * a.K : a.K, a.B, a.xs * 2, kKT, kTcN, bf16, true))
         return cudaErrorNotSupported;
     auto kernel = linear_tc_kernel<T, STAGES, PRO>;
-    const size_t smem = tc_smem_bytes(STAGES, PRO);
+    // prologue 0 holds the CTA's K range of x beside the ring: its size follows the split
+    const int64_t KT = a.K / kKT;
+    auto smem_for = [&](int sk) {
+        return tc_smem_bytes(STAGES, PRO, PRO == 0 ? static_cast<int>((KT + sk - 1) / sk) : 0);
+    };
+    if (PRO == 0 && (KT + p.splits - 1) / p.splits > kTcNormMaxTiles) return cudaErrorInvalidValue;
+    size_t smem = smem_for(p.splits);
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     int splits = p.splits;
@@ -1141,6 +1290,12 @@ cudaError_t launch_tc(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
         if (e != cudaSuccess || clusters < 1) {
             cudaGetLastError();
             splits = 8;
+            if (PRO == 0) {
+                if ((KT + splits - 1) / splits > kTcNormMaxTiles) return cudaErrorInvalidValue;
+                smem = smem_for(splits);
+                e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+                if (e != cudaSuccess) return e;
+            }
         }
     }
     const dim3 grid(static_cast<unsigned>((a.N + kTcM - 1) / kTcM * splits));
@@ -1179,6 +1334,7 @@ template <typename T>
 cudaError_t launch_typed(const LinArgs& a, const LinPlan& p, cudaStream_t s) {
     if (p.tcgen05) {
         switch (p.prologue) {
+            case 0: return launch_tc<T, 4, 0>(a, p, s);  // the RMSNorm fused: a 4-stage W ring
             case 1: return launch_tc<T, 3, 1>(a, p, s);  // the GLU fused: 3 stages of 32 KB, two CTAs per SM
             case 2: return launch_tc<T, 3, 2>(a, p, s);
             case 3: return p.tc_stages == 8 ? launch_tc<T, 8, 3>(a, p, s) : launch_tc<T, 4, 3>(a, p, s);
@@ -1352,18 +1508,21 @@ size_t linear_smem(int mt, int prologue) {
     return prologue == 3 ? lin::smemh_bytes(mt) : lin::smem_bytes(mt, prologue);
 }
 size_t linear16_smem(int rows, int64_t K, int splits) { return lin::smem16_bytes(rows, K, splits); }
-size_t linear_tc_smem(int stages, int prologue) { return lin::tc_smem_bytes(stages, prologue); }
+size_t linear_tc_smem(int stages, int prologue, int nx) { return lin::tc_smem_bytes(stages, prologue, nx); }
 
 // Clusters of `splits` CTAs of the tcgen05 projection (ring of `stages`) the device can hold at once.
-int linear_tc_max_clusters(int splits, int stages, bool bf16, int prologue) {
-    // answers kept per (device, dtype, ring depth, cluster size): the query sets kernel attributes
-    static std::atomic<int> memo[16][2][3][17];
+int linear_tc_max_clusters(int splits, int stages, bool bf16, int prologue, int nx) {
+    // answers kept per (device, dtype, kernel kind, x tiles held, cluster size): the query sets
+    // kernel attributes. Kinds: 0 / 1 the 4 / 8-stage projection of h, 2 the GLU fused, 3 the
+    // RMSNorm fused (with nx of its x tiles beside the ring)
+    static std::atomic<int> memo[16][2][4][lin::kTcNormMaxTiles + 1][17];
     static std::once_flag once;
     std::call_once(once, [] {
         for (auto& a : memo)
             for (auto& b : a)
                 for (auto& c : b)
-                    for (auto& d : c) d.store(-1);
+                    for (auto& d : c)
+                        for (auto& e : d) e.store(-1);
     });
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -1371,17 +1530,20 @@ int linear_tc_max_clusters(int splits, int stages, bool bf16, int prologue) {
         return 0;
     }
     if (splits < 1 || splits > 16) return 0;
-    const int kind = prologue != 3 ? 2 : (stages == 8 ? 1 : 0);
-    std::atomic<int>* slot = dev >= 0 && dev < 16 ? &memo[dev][bf16 ? 1 : 0][kind][splits] : nullptr;
+    if (prologue != 0) nx = 0;
+    if (nx < 0 || nx > lin::kTcNormMaxTiles) return 0;
+    const int kind = prologue == 0 ? 3 : (prologue != 3 ? 2 : (stages == 8 ? 1 : 0));
+    std::atomic<int>* slot = dev >= 0 && dev < 16 ? &memo[dev][bf16 ? 1 : 0][kind][nx][splits] : nullptr;
     if (slot && slot->load() >= 0) return slot->load();
-    const size_t smem = lin::tc_smem_bytes(kind == 2 ? 3 : stages, prologue != 3 ? 1 : 3);
+    const size_t smem = kind == 3 ? lin::tc_smem_bytes(4, 0, nx)
+                                  : lin::tc_smem_bytes(kind == 2 ? 3 : stages, prologue != 3 ? 1 : 3);
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr;
     attr.id = cudaLaunchAttributeClusterDimension;
     attr.val.clusterDim.x = static_cast<unsigned>(splits);
     attr.val.clusterDim.y = attr.val.clusterDim.z = 1;
     cfg.gridDim = dim3(static_cast<unsigned>(splits));
-    cfg.blockDim = dim3(lin::tc_threads(prologue != 3 ? 1 : 3));
+    cfg.blockDim = dim3(lin::tc_threads(prologue == 3 ? 3 : prologue));
     cfg.dynamicSmemBytes = smem;
     cfg.attrs = &attr;
     cfg.numAttrs = 1;
@@ -1396,7 +1558,9 @@ int linear_tc_max_clusters(int splits, int stages, bool bf16, int prologue) {
             n = 0;
         }
     };
-    if (kind == 2)
+    if (kind == 3)
+        bf16 ? query(lin::linear_tc_kernel<__nv_bfloat16, 4, 0>) : query(lin::linear_tc_kernel<__half, 4, 0>);
+    else if (kind == 2)
         bf16 ? query(lin::linear_tc_kernel<__nv_bfloat16, 3, 1>) : query(lin::linear_tc_kernel<__half, 3, 1>);
     else if (kind == 1)
         bf16 ? query(lin::linear_tc_kernel<__nv_bfloat16, 8, 3>) : query(lin::linear_tc_kernel<__half, 8, 3>);

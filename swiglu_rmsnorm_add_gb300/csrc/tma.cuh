@@ -77,6 +77,27 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, i
         "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_u32(bar))
         : "memory");
 }
+// Distributed shared memory: the shared::cluster address of `local` (a shared variable of this
+// CTA) in the CTA of the cluster with the given rank, and 4- / 16-byte accesses through it.
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t local_addr, uint32_t rank) {
+    uint32_t r;
+    asm("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local_addr), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ uint32_t dsmem_addr(const void* local, uint32_t rank) {
+    return dsmem_addr(smem_u32(local), rank);
+}
+__device__ __forceinline__ float4 dsmem_ld_f4(uint32_t addr) {
+    float4 v;
+    // (not volatile: the loads follow the barrier that made the data visible, and the
+    // compiler may then issue all of a thread's loads before their first use)
+    asm("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+__device__ __forceinline__ void dsmem_st_f32(uint32_t addr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+
 // Hint the L2 to fetch the box at (c0, c1) of a 2-D tensor map (no data moves to the SM, and no
 // barrier completes). A prefetch has no semantic effect, so it may run before a dependency wait on
 // data the previous kernel is still writing: the L2 is the point of coherence. c0 as for a load.

@@ -88,6 +88,41 @@ def test_glu_fused_into_the_tcgen05_projection(dtype, act, B, I, N):
     assert_linear_close(got, want, h, W, f"fused glu tcgen05 {act} {dtype} B={B} I={I} N={N}")
 
 
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16])
+@pytest.mark.parametrize("B,K,N", [(1, 64, 128), (17, 640, 384), (40, 4160, 640), (64, 1536, 2048), (33, 1024, 256),
+                                   (64, 8192, 256)])
+def test_rmsnorm_fused_into_the_tcgen05_projection(dtype, B, K, N):
+    """The RMSNorm computed inside the tcgen05 projection (the CTA's x tiles by TMA, the
+    cluster's partial sums of squares exchanged, h's tiles normed in place), forced from 1 row:
+    against the oracle's rmsnorm then linear; no bounded wait runs out."""
+    before = sra.wait_timeouts()
+    sra.force_variant("linear", 1)
+    try:
+        got, want, h, W = norm_case(B, K, N, dtype, 1090 + K + B)
+    finally:
+        sra.force_variant("linear", -1)
+    torch.cuda.synchronize()
+    assert sra.wait_timeouts() == before
+    assert_linear_close(got, want, h, W, f"fused rmsnorm tcgen05 {dtype} B={B} K={K} N={N}")
+
+
+@pytest.mark.parametrize("splits", [1, 3, 5, 12, 16])
+def test_rmsnorm_fused_tcgen05_splits(splits):
+    """The fused RMSNorm with its K split forced over clusters of 1-16 CTAs (16 tiles of K,
+    ragged ranges at 3, 5 and 12): against the oracle."""
+    try:
+        sra.force_variant("linear", 1 | (splits << 8))
+        try:
+            got, want, h, W = norm_case(33, 1024, 256, torch.bfloat16, 1095 + splits)
+        finally:
+            sra.force_variant("linear", -1)
+    except sra.SRAError:
+        if splits <= 8:
+            raise
+        pytest.skip(f"the device cannot place a {splits}-CTA cluster")
+    assert_linear_close(got, want, h, W, f"fused rmsnorm tcgen05 splits={splits}")
+
+
 def test_glu_fused_into_the_tcgen05_projection_far_negative_gates():
     """Gates below -64 in some 8-element chunks take the careful SiLU inside the fused kernel."""
     B, I, N = 24, 1024, 256
