@@ -38,8 +38,10 @@
  *    (cudaGetLastError after the launch). A zero-sized call (rows == 0 or
  *    T == 0) validates its arguments, enqueues nothing and returns SRA_OK.
  *  - No call waits for the device to finish, and no kernel traps or asserts. The
- *    only device-side waits are the fused projections' waits for their own tile
- *    copies; each is bounded and counted when it runs out (sra_wait_timeouts).
+ *    device-side waits are the fused projections' and the TMA-fed attention
+ *    variant's waits for their own tile copies, each bounded and counted when it
+ *    runs out (sra_wait_timeouts), and the cluster kernels' barriers among the
+ *    CTAs of one cluster, which the hardware schedules together.
  *  - Thread safety: calls may be made concurrently from several host threads.
  *    sra_force_variant changes process-wide state and is meant for A/B
  *    measurement only.
@@ -473,8 +475,8 @@ SRA_API int sra_last_cuda_error(void);
 /*
  * Bounded device waits that gave up, on the current device, since the library was
  * loaded. Kernels that stream tiles with tensor-memory-access copies
- * (sra_rmsnorm_linear, sra_glu_linear) wait on shared-memory barriers for those
- * copies; each wait is bounded (about a second), and a wait that runs out is
+ * (sra_rmsnorm_linear, sra_glu_linear and their _ws forms; decode attention's
+ * TMA-fed variant) wait on shared-memory barriers for those copies; each wait is bounded (about a second), and a wait that runs out is
  * counted here and the kernel goes on, so a copy that never completes cannot hang
  * the GPU (that call's output is then not valid). Reads the counter synchronously
  * (cudaMemcpyFromSymbol); 0 on a device that ran none of those kernels. No paper

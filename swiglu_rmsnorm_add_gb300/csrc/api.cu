@@ -710,7 +710,7 @@ int sra_version(void) { return SRA_VERSION; }
 
 int sra_last_cuda_error(void) { return g_last_cuda_error; }
 
-unsigned int sra_wait_timeouts(void) { return linear_wait_timeouts(); }
+unsigned int sra_wait_timeouts(void) { return linear_wait_timeouts() + attn_wait_timeouts(); }
 
 int sra_wait_selftest(int32_t* result, void* stream) {
     if (!result) return SRA_ERR_NULL;

@@ -1165,4 +1165,15 @@ cudaError_t launch_decode_attention(const AttnArgs& a, const AttnPlan& p, int dt
     }
 }
 
+// Bounded waits of this file's kernels (the TMA-fed attention variant) that ran out: the
+// counter in tma.cuh is per translation unit, so each file that waits reports its own copy.
+unsigned int attn_wait_timeouts() {
+    unsigned int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_wait_timeouts, sizeof(v)) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    return v;
+}
+
 }  // namespace sra

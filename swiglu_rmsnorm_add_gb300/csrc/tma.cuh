@@ -5,7 +5,7 @@
 // one thread with cp.async.bulk.tensor; the copy engine reports its bytes to an mbarrier,
 // which the consuming threads poll by phase parity. Every poll loop is bounded: after about
 // a second without completion the waiter counts a timeout in a device-wide counter
-// (sra_wait_timeouts() reads it) and goes on, so a copy that never lands cannot hang the GPU.
+// (sra_wait_timeouts() adds up those counters) and goes on, so a copy that never lands cannot hang the GPU.
 #pragma once
 
 #include <cuda.h>

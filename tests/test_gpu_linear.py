@@ -279,9 +279,10 @@ def test_bounded_wait_gives_up():
 @pytest.mark.parametrize("dtype,B,K,N,ws", [
     (torch.bfloat16, 1, 1536, 2048, False),     # decode-batch kernel
     (torch.bfloat16, 16, 1536, 2048, False),
-    (torch.bfloat16, 64, 1536, 2048, False),    # cluster kernel
+    (torch.bfloat16, 64, 1536, 2048, False),    # the RMSNorm fused into the tcgen05 projection
     (torch.bfloat16, 64, 1536, 2048, True),     # prologue kernel into a workspace
     (torch.float16, 33, 640, 192, False),
+    (torch.float16, 33, 640, 256, False),       # the RMSNorm fused into the tcgen05 projection
     (torch.float32, 5, 640, 192, False),        # CUDA-core kernel
     (torch.bfloat16, 3, 100, 40, False),
 ])
