@@ -653,8 +653,9 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
         tc::alloc(&tmem_slot, kCols);
         tc::relinquish();
     }
-    // (No L2 prefetch of the W slice before the dependency wait here: measured slower, the
-    // prefetch traffic of every CTA's whole slice competes with the tiles the pipeline needs.)
+    // (Before the dependency wait at most the first stages are prefetched into L2 below, never the
+    // CTA's whole W slice: that measured slower, its traffic competing with the tiles the pipeline
+    // needs.)
     __syncthreads();  // barriers initialised, the tensor-memory address in shared memory
     tc::fence_after();
     const uint32_t tmem = tmem_slot;

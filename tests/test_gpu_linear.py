@@ -76,7 +76,7 @@ def glu_case(B, I, N, dtype, seed, act="silu", rows=None, ws=False):
 @pytest.mark.parametrize("B,I,N", [(1, 64, 128), (17, 640, 384), (40, 4160, 640), (64, 8960, 1536), (33, 1024, 256)])
 def test_glu_fused_into_the_tcgen05_projection(dtype, act, B, I, N):
     """The GLU computed inside the tcgen05 projection (gate and up tiles by TMA, h's tile made in
-    place by two warps), forced from 1 row: against the oracle's glu then linear."""
+    place by eight warps), forced from 1 row: against the oracle's glu then linear."""
     sra.force_variant("linear", 1)
     try:
         before = sra.wait_timeouts()
