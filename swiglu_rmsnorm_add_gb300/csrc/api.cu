@@ -1079,7 +1079,8 @@ static int linear_common(const void* x, const void* w_ln, const void* W, void* y
     // K / (16 x 64). Chosen from 17 to 64 rows where the grid is one wave of two CTAs per SM
     // (at most 6 x tiles a CTA): measured on GB300 at batch 64, ln1 + qkv_proj [1536 -> 2048]
     // 8.7 against 9.9 us with mma.sync, but [4096 -> 4096] (8 x tiles, one CTA per SM, two
-    // waves) 34 against 26 us. Forced onto it, from 1 row and at any split that fits.
+    // waves) 34 against at most 26 us (back-to-back calls). Forced onto it, from 1 row and at any
+    // split that fits.
     if (plan.tensor_cores && prologue == 0 && B <= 64 && N % 128 == 0 &&
         (lin_forced == 1 || (lin_forced < 0 && B > 16))) {
         const int64_t slices = N / 128, KT = K / 64;
