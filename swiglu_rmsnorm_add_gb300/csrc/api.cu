@@ -1076,29 +1076,33 @@ static int linear_common(const void* x, const void* w_ln, const void* W, void* y
     }
     // the RMSNorm fused into the tcgen05 projection (one launch), N a multiple of 128: a CTA holds
     // its whole K range of x (at most 16 tiles) beside a 4-stage W ring, so the split is at least
-    // K / (16 x 64). Chosen from 17 to 64 rows where the grid is one wave of two CTAs per SM
-    // (at most 6 x tiles a CTA): measured on GB300 at batch 64, ln1 + qkv_proj [1536 -> 2048]
-    // 8.7 against 9.9 us with mma.sync, but [4096 -> 4096] (8 x tiles, one CTA per SM, two
-    // waves) 34 against at most 26 us (back-to-back calls). Forced onto it, from 1 row and at any
-    // split that fits.
+    // K / (16 x 64). Chosen from 33 rows, or from 17 with K >= 4096, at the largest split whose grid
+    // is one wave (two CTAs per SM up to 5 x tiles each, one beyond). Measured on GB300 (CUDA-graph
+    // replay, us per call, mma.sync against tcgen05): batch 64 [1536 -> 2048] 9.7 / 8.1, [4096 ->
+    // 4096] 26.4 / 17.4; batch 32 [4096 -> 4096] 19.5 / 16.9 but [1536 -> 2048] 7.5 / 8.4, batch 17
+    // 7.3 / 8.9. Forced onto it, from 1 row and at any split that fits.
     if (plan.tensor_cores && prologue == 0 && B <= 64 && N % 128 == 0 &&
-        (lin_forced == 1 || (lin_forced < 0 && B > 16))) {
+        (lin_forced == 1 || (lin_forced < 0 && (B > 32 || (B > 16 && K >= 4096))))) {
         const int64_t slices = N / 128, KT = K / 64;
         const int64_t min_split = (KT + 15) / 16;
+        const bool bf = dtype == DT_BF16;
         auto nx_of = [&](int k) { return static_cast<int>((KT + k - 1) / k); };
         auto fits = [&](int k) { return static_cast<int64_t>(linear_tc_smem(4, 0, nx_of(k))) <= limit; };
-        auto placed = [&](int k) { return linear_tc_max_clusters(k, 4, dtype == DT_BF16, 0, nx_of(k)) >= 1; };
+        auto placed = [&](int k) { return linear_tc_max_clusters(k, 4, bf, 0, nx_of(k)) >= 1; };
         const int fs = lin_all < 0 ? 0 : (lin_all >> 8) & 0xFF;
         int sk = 0;
         if (fs) {
             if (fs > 16 || fs > KT || fs < min_split || !fits(fs) || !placed(fs)) return SRA_ERR_VARIANT;
             sk = fs;
         } else {
-            // the largest split with at least 4 K tiles a CTA whose grid is one wave of two CTAs
-            // per SM; forced onto the kernel without one, the smallest split that fits
+            // the largest split with at least 4 K tiles a CTA whose grid is one wave; forced onto
+            // the kernel without one, the smallest split that fits
             for (int k = static_cast<int>(std::min<int64_t>(16, std::max<int64_t>(1, KT / 4))); k >= min_split && !sk;
-                 --k)
-                if (nx_of(k) <= 6 && slices * k <= 2 * static_cast<int64_t>(sms) && fits(k) && placed(k)) sk = k;
+                 --k) {
+                if (!fits(k)) continue;
+                const int per_sm = linear_tc_norm_ctas_per_sm(nx_of(k), bf);
+                if (per_sm >= 1 && slices * k <= static_cast<int64_t>(per_sm) * sms && placed(k)) sk = k;
+            }
             if (!sk && lin_forced == 1)
                 for (int k = static_cast<int>(std::max<int64_t>(1, min_split)); k <= 16 && k <= KT && !sk; ++k)
                     if (fits(k) && placed(k)) sk = k;

@@ -207,6 +207,7 @@ size_t linear_smem(int mt, int prologue);
 size_t linear_tc_smem(int stages, int prologue = 3, int nx = 0);
 // nx: with the RMSNorm fused (prologue 0), the K tiles of x a CTA holds (at most 16)
 int linear_tc_max_clusters(int splits, int stages, bool bf16, int prologue = 3, int nx = 0);
+int linear_tc_norm_ctas_per_sm(int nx, bool bf16);  // the fused-RMSNorm kernel's CTAs per SM
 unsigned int linear_wait_timeouts();  // bounded waits of the fused-projection kernels that ran out
 unsigned int attn_wait_timeouts();    // bounded waits of the TMA-fed attention kernel that ran out
 cudaError_t launch_wait_selftest(int32_t* out, cudaStream_t s);  // a wait on a barrier nothing completes

@@ -1511,6 +1511,39 @@ size_t linear_smem(int mt, int prologue) {
 size_t linear16_smem(int rows, int64_t K, int splits) { return lin::smem16_bytes(rows, K, splits); }
 size_t linear_tc_smem(int stages, int prologue, int nx) { return lin::tc_smem_bytes(stages, prologue, nx); }
 
+// CTAs of the tcgen05 projection with the RMSNorm fused (nx x tiles held) one SM holds at once
+// (its static shared memory included), kept per (device, dtype, nx).
+int linear_tc_norm_ctas_per_sm(int nx, bool bf16) {
+    static std::atomic<int> memo[16][2][lin::kTcNormMaxTiles + 1];
+    static std::once_flag once;
+    std::call_once(once, [] {
+        for (auto& a : memo)
+            for (auto& b : a)
+                for (auto& c : b) c.store(-1);
+    });
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    if (nx < 0 || nx > lin::kTcNormMaxTiles) return 0;
+    std::atomic<int>* slot = dev >= 0 && dev < 16 ? &memo[dev][bf16 ? 1 : 0][nx] : nullptr;
+    if (slot && slot->load() >= 0) return slot->load();
+    const size_t smem = lin::tc_smem_bytes(4, 0, nx);
+    int n = 0;
+    auto query = [&](auto kernel) {
+        if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+                cudaSuccess ||
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, lin::tc_threads(0), smem) != cudaSuccess) {
+            cudaGetLastError();
+            n = 0;
+        }
+    };
+    bf16 ? query(lin::linear_tc_kernel<__nv_bfloat16, 4, 0>) : query(lin::linear_tc_kernel<__half, 4, 0>);
+    if (slot) slot->store(n);
+    return n;
+}
+
 // Clusters of `splits` CTAs of the tcgen05 projection (ring of `stages`) the device can hold at once.
 int linear_tc_max_clusters(int splits, int stages, bool bf16, int prologue, int nx) {
     // answers kept per (device, dtype, kernel kind, x tiles held, cluster size): the query sets
