@@ -366,10 +366,10 @@ SRA_API int sra_paged_decode_attention_noalloc(const void* q, const void* kv_cac
  * W:    [N, K] of `dtype`, row-major (nn.Linear's [out, in] layout). Read only.
  * y:    [B, N] of `dtype`, row stride y_row_stride (>= N); must not overlap x, w_ln or W.
  * bf16 / fp16 with K and N multiples of 64 and 16-byte aligned x, w_ln, W (x_row_stride a
- * multiple of 8) run on the tensor cores (fp32 accumulation; from 17 to 64 rows with N a
- * multiple of 128 on the fifth-generation tensor cores, in one kernel that also takes the
- * norm where its grid fits the GPU in one wave); other layouts and fp32 run a CUDA-core
- * kernel with the same result up to the order of the fp32 sums.
+ * multiple of 8) run on the tensor cores (fp32 accumulation; with N a multiple of 128, from
+ * 33 to 64 rows, or from 17 with K >= 4096, on the fifth-generation tensor cores in one
+ * kernel that also takes the norm); other layouts and fp32 run a CUDA-core kernel with the
+ * same result up to the order of the fp32 sums.
  * Errors: unknown dtype -> SRA_ERR_DTYPE; B < 0, K <= 0 or N <= 0 (or K too long for
  * one CTA's shared memory on the CUDA-core path) -> SRA_ERR_SHAPE; short strides ->
  * SRA_ERR_STRIDE; eps negative or not finite -> SRA_ERR_ARG; NULL -> SRA_ERR_NULL;
@@ -389,7 +389,8 @@ SRA_API int sra_rmsnorm_linear(const void* x, const void* w_ln, const void* W, v
  *
  * gate_up: [B, 2I] of `dtype`, row stride in_row_stride (>= 2I). W: [N, I] row-major.
  * y: [B, N], row stride y_row_stride. act: sra_act_t. Layout rules, paths and errors
- * as sra_rmsnorm_linear (an unknown act -> SRA_ERR_ARG).
+ * as sra_rmsnorm_linear (an unknown act -> SRA_ERR_ARG), except that the one kernel on the
+ * fifth-generation tensor cores, computing the activation itself, serves from 4 rows.
  */
 SRA_API int sra_glu_linear(const void* gate_up, const void* W, void* y, int64_t B, int64_t I, int64_t N,
                            int64_t in_row_stride, int64_t y_row_stride, int act, int dtype, void* stream);

@@ -1056,10 +1056,16 @@ static int linear_common(const void* x, const void* w_ln, const void* W, void* y
     } else if (lin_forced == 1 && prologue == 3) {
         return SRA_ERR_VARIANT;
     }
-    // the GLU fused into the tcgen05 projection (no workspace, one launch): from 17 to 64 rows
-    // (or forced onto it, from 1 row), N a multiple of 128; 3 stages of 32 KB, two CTAs per SM
+    // the GLU fused into the tcgen05 projection (no workspace, one launch): from 4 to 64 rows (or
+    // forced onto it, from 1 row; not while the decode-batch kernel's split is forced), N a
+    // multiple of 128; 3 stages of 32 KB, two CTAs per SM. Measured on GB300 (CUDA-graph replay, us
+    // per call, decode-batch or mma.sync kernel against tcgen05): SwiGLU + down_proj [8960 -> 1536]
+    // batch 1 8.65 / 12.31, 3 11.88 / 12.42, 4 13.82 / 12.21, 16 17.17 / 12.42, 64 28.59 / 14.15;
+    // [14336 -> 4096] batch 2 35.97 / 45.18, 4 51.83 / 45.18, 64 88.18 / 48.26
+    const bool narrow_forced = g_force_narrow.load(std::memory_order_relaxed) >= 0;
     if (plan.tensor_cores && (prologue == 1 || prologue == 2) && B <= 64 && N % 128 == 0 &&
-        (lin_forced == 1 || (lin_forced < 0 && B > 16)) && static_cast<int64_t>(linear_tc_smem(3, 1)) <= limit) {
+        (lin_forced == 1 || (lin_forced < 0 && !narrow_forced && B >= 4)) &&
+        static_cast<int64_t>(linear_tc_smem(3, 1)) <= limit) {
         plan.tcgen05 = true;
         plan.narrow = false;
         const int64_t slices = N / 128, KT = K / 64;
