@@ -780,16 +780,26 @@ __global__ void __launch_bounds__(tc_threads(PRO)) linear_tc_kernel(LinArgs a, c
         // h = x * pre * (1 / rms) * w, rounded to T, in place: chunk p of row r in a tile holds
         // the row's columns 8 (p ^ (r % 8)) ... + 7 of the tile (the 128-byte swizzle). (The
         // barriers above made the staged weight visible.)
-        for (int c = static_cast<int>(threadIdx.x); c < ntiles * kTcN * 8; c += tc_threads(0)) {
-            const int t = c / (kTcN * 8), rem = c - t * (kTcN * 8), r = rem >> 3, pch = rem & 7;
-            R8* hp = reinterpret_cast<R8*>(xreg + static_cast<size_t>(t) * tc_htile_bytes() + r * (kKT * 2) + pch * 16);
-            float f[8], g[8];
-            V8::unpack(*hp, f);
-            V8::unpack(reinterpret_cast<const R8*>(wsl)[t * (kKT / 8) + (pch ^ (r & 7))], g);
-            const float iv = inv[r], pv = prev[r];
+        // Thread i < 256 owns the (row, chunk) positions i and i + 256 of every tile (consecutive
+        // threads: consecutive 16-byte chunks), so a position's row scale and weight column are
+        // found once and the tiles are an inner loop of plain address steps.
+        if (threadIdx.x < 4 * kTcN) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) f[e] = f[e] * pv * iv * g[e];
-            *hp = V8::pack(f);
+            for (int h2 = 0; h2 < 2; ++h2) {
+                const int q = static_cast<int>(threadIdx.x) + h2 * 4 * kTcN, r = q >> 3, pch = q & 7;
+                const float iv = inv[r], pv = prev[r];
+                unsigned char* hp0 = xreg + r * (kKT * 2) + pch * 16;
+                const R8* wp = reinterpret_cast<const R8*>(wsl) + (pch ^ (r & 7));
+                for (int t = 0; t < ntiles; ++t) {
+                    R8* hp = reinterpret_cast<R8*>(hp0 + static_cast<size_t>(t) * tc_htile_bytes());
+                    float f[8], g[8];
+                    V8::unpack(*hp, f);
+                    V8::unpack(wp[t * (kKT / 8)], g);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) f[e] = f[e] * pv * iv * g[e];
+                    *hp = V8::pack(f);
+                }
+            }
         }
         fence_proxy_async();  // h's tiles are read by the tensor core (the async proxy)
         __syncthreads();
