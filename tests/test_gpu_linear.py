@@ -204,6 +204,33 @@ def test_strided_rows_and_outputs():
     assert bool((ybuf[:, N:].cpu() == 3.0).all())
 
 
+@pytest.mark.parametrize("prologue", ["rmsnorm", "silu"])
+def test_strided_rows_and_outputs_fused_tcgen05(prologue):
+    """The one-launch tcgen05 kernels (forced) on padded input rows (row stride K + 64, or 2K + 64
+    for gate_up) writing into a wider y: matches the oracle, guard columns untouched."""
+    B, K, N = 20, 512, 256
+    W = syn.linear_weight(N, K, torch.bfloat16, 1097)
+    ybuf = torch.full((B, N + 8), 3.0, dtype=torch.bfloat16, device=DEV)
+    h = torch.empty(B, K, dtype=torch.bfloat16)
+    sra.force_variant("linear", 1)
+    try:
+        if prologue == "rmsnorm":
+            base = syn.normal((B, K + 64), 0, 1, torch.bfloat16, 1097, 1)
+            w = syn.normal((K,), 1, 0.1, torch.bfloat16, 1097, 2)
+            sra.rmsnorm_linear(base.to(DEV)[:, :K], w.to(DEV), W.to(DEV), ybuf[:, :N])
+            oracle.rmsnorm(base[:, :K].contiguous(), w, h, 1e-6)
+        else:
+            base = syn.normal((B, 2 * K + 64), 0, 1, torch.bfloat16, 1097, 3)
+            sra.glu_linear(base.to(DEV)[:, :2 * K], W.to(DEV), ybuf[:, :N])
+            oracle.glu(base[:, :2 * K].contiguous(), h, "silu")
+    finally:
+        sra.force_variant("linear", -1)
+    want = torch.empty(B, N, dtype=torch.bfloat16)
+    oracle.linear(h, W, want)
+    assert_linear_close(ybuf[:, :N], want, h, W, f"strided, fused tcgen05 {prologue}")
+    assert bool((ybuf[:, N:].cpu() == 3.0).all())
+
+
 def test_llama3_8b_down_sampled():
     """The Llama-3-8B down projection (I = 14336, N = 4096) at batch 64, sampled rows."""
     rows = torch.tensor([0, 13, 40, 63])
